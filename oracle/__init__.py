@@ -1,0 +1,196 @@
+"""FP64 attention oracle (test infrastructure only).
+
+Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU
+baseline leg may import this package. The CUDA library never calls it, and it
+shares no code with the CUDA library: the two meet only in the seeded input
+generator, which holds none of the method's arithmetic.
+
+The C source (``attn_oracle.c``) computes the plain definition: per query
+row, materialize the FP64 score row over the allowed keys, take its maximum,
+exponentiate, sum, divide ("Compare reasoning after your own attempt",
+"Reference tradeoffs to challenge": the FP64 materializing oracle). The
+summary merge follows the same page's A1 row and worked answer.
+
+Parity pins: every exported function is pinned in ``tests/test_oracle_pins.py``
+against worked answers from the pages, closed forms, invariants and an
+independent library formula; none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_LOCK = threading.Lock()
+_LIBS: dict = {}
+
+# -ffp-contract=off keeps the FP64 results identical on x86_64 and aarch64.
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off", "-fno-fast-math"]
+
+
+def lib_path(mutant: int = 0, out_dir: Optional[str] = None) -> str:
+    name = "liboracle.so" if mutant == 0 else f"liboracle_mutant{mutant}.so"
+    return os.path.join(out_dir or _HERE, name)
+
+
+def build(mutant: int = 0, out_dir: Optional[str] = None, force: bool = False) -> str:
+    """Compile the oracle with gcc; returns the shared-library path."""
+    path = lib_path(mutant, out_dir)
+    if not force and os.path.exists(path) and os.path.getmtime(path) >= os.path.getmtime(_SRC):
+        return path
+    tmp = path + f".tmp{os.getpid()}"
+    cmd = ["gcc", *CFLAGS, f"-DORACLE_MUTANT={mutant}", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, path)
+    return path
+
+
+def _load(mutant: int = 0, out_dir: Optional[str] = None) -> ctypes.CDLL:
+    key = (mutant, out_dir)
+    with _LOCK:
+        if key not in _LIBS:
+            lib = ctypes.CDLL(build(mutant, out_dir))
+            dp = ctypes.POINTER(ctypes.c_double)
+            i64p = ctypes.POINTER(ctypes.c_int64)
+            ci, cd = ctypes.c_int, ctypes.c_double
+            shape = [ci] * 6 + [ci, ci, cd]
+            lib.oracle_attn_f64.argtypes = [dp, dp, dp, dp, *shape, ci]
+            lib.oracle_attn_f64.restype = ci
+            lib.oracle_attn_rows_f64.argtypes = [dp, dp, dp, dp, *shape, i64p, ctypes.c_int64, ci]
+            lib.oracle_attn_rows_f64.restype = ci
+            lib.oracle_attn_weights_f64.argtypes = [dp, dp, *shape, ctypes.c_int64, dp]
+            lib.oracle_attn_weights_f64.restype = ci
+            lib.oracle_partial_f64.argtypes = [dp, dp, dp, *shape, ctypes.c_int64, ci, ci, dp, dp, dp]
+            lib.oracle_partial_f64.restype = ci
+            lib.oracle_merge_f64.argtypes = [ci, ci, dp, dp, dp, dp, dp, dp]
+            lib.oracle_merge_f64.restype = None
+            lib.oracle_mutant_id.restype = ci
+            _LIBS[key] = lib
+        return _LIBS[key]
+
+
+def _f64(a) -> np.ndarray:
+    """Exact widening to a contiguous float64 array (accepts numpy or torch CPU tensors)."""
+    if hasattr(a, "detach"):
+        a = a.detach().to("cpu")
+        import torch
+
+        a = a.to(torch.float64).numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+class Oracle:
+    """Handle on one build of the oracle (mutant 0 is the real one)."""
+
+    def __init__(self, mutant: int = 0, out_dir: Optional[str] = None):
+        self.lib = _load(mutant, out_dir)
+
+    @staticmethod
+    def _dims(q, k, v):
+        B, Hq, M, D = q.shape
+        Bk, Hkv, N, Dk = k.shape
+        if (Bk, Dk) != (B, D) or tuple(v.shape) != tuple(k.shape):
+            raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+        return B, Hq, Hkv, M, N, D
+
+    def attention(self, q, k, v, causal=False, window=0, scale=None, nthreads=0) -> np.ndarray:
+        """Full FP64 output [B, Hq, M, D]."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        B, Hq, Hkv, M, N, D = self._dims(q, k, v)
+        scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+        o = np.zeros((B, Hq, M, D), dtype=np.float64)
+        rc = self.lib.oracle_attn_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, Hq, Hkv, M, N, D,
+                                      int(causal), int(window), scale, int(nthreads))
+        if rc != 0:
+            raise ValueError(f"oracle_attn_f64 rejected the shape (rc={rc})")
+        return o
+
+    def attention_rows(self, q, k, v, rows: Sequence[int], causal=False, window=0, scale=None,
+                       nthreads=0) -> np.ndarray:
+        """FP64 output of selected rows only; rows index the flattened [B*Hq*M] row axis."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        B, Hq, Hkv, M, N, D = self._dims(q, k, v)
+        scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+        r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        o = np.zeros((len(r), D), dtype=np.float64)
+        rc = self.lib.oracle_attn_rows_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, Hq, Hkv, M, N, D,
+                                           int(causal), int(window), scale,
+                                           r.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                           len(r), int(nthreads))
+        if rc != 0:
+            raise ValueError(f"oracle_attn_rows_f64 rejected the call (rc={rc})")
+        return o
+
+    def weights(self, q, k, row: int, causal=False, window=0, scale=None) -> np.ndarray:
+        """Normalized attention weights of one row over the N keys."""
+        q, k = _f64(q), _f64(k)
+        B, Hq, Hkv, M, N, D = self._dims(q, k, k)
+        scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+        w = np.zeros(max(N, 1), dtype=np.float64)
+        rc = self.lib.oracle_attn_weights_f64(_ptr(q), _ptr(k), B, Hq, Hkv, M, N, D, int(causal),
+                                              int(window), scale, int(row), _ptr(w))
+        if rc != 0:
+            raise ValueError(f"oracle_attn_weights_f64 rejected the call (rc={rc})")
+        return w[:N]
+
+    def partial(self, q, k, v, row: int, j0: int, j1: int, causal=False, window=0, scale=None):
+        """Unnormalized summary (m, l, acc[D]) of one row over allowed keys in [j0, j1)."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        B, Hq, Hkv, M, N, D = self._dims(q, k, v)
+        scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+        m = np.zeros(1)
+        l = np.zeros(1)
+        acc = np.zeros(D)
+        rc = self.lib.oracle_partial_f64(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, M, N, D, int(causal),
+                                         int(window), scale, int(row), int(j0), int(j1), _ptr(m),
+                                         _ptr(l), _ptr(acc))
+        if rc != 0:
+            raise ValueError(f"oracle_partial_f64 rejected the call (rc={rc})")
+        return float(m[0]), float(l[0]), acc
+
+    def merge(self, m, l, acc):
+        """Merge S summaries: m[S], l[S], acc[S, D] -> (m, l, acc[D])."""
+        m = np.ascontiguousarray(np.asarray(m, dtype=np.float64).reshape(-1))
+        l = np.ascontiguousarray(np.asarray(l, dtype=np.float64).reshape(-1))
+        S = m.shape[0]
+        acc = np.ascontiguousarray(np.asarray(acc, dtype=np.float64).reshape(S, -1))
+        D = acc.shape[1]
+        mo, lo, ao = np.zeros(1), np.zeros(1), np.zeros(max(D, 1))
+        self.lib.oracle_merge_f64(S, D, _ptr(m), _ptr(l), _ptr(acc), _ptr(mo), _ptr(lo), _ptr(ao))
+        return float(mo[0]), float(lo[0]), ao[:D]
+
+
+_DEFAULT: Optional[Oracle] = None
+
+
+def default() -> Oracle:
+    global _DEFAULT
+    if _DEFAULT is None:
+        _DEFAULT = Oracle(0)
+    return _DEFAULT
+
+
+def attention(q, k, v, causal=False, window=0, scale=None, nthreads=0):
+    return default().attention(q, k, v, causal, window, scale, nthreads)
+
+
+def attention_rows(q, k, v, rows, causal=False, window=0, scale=None, nthreads=0):
+    return default().attention_rows(q, k, v, rows, causal, window, scale, nthreads)
+
+
+def merge(m, l, acc):
+    return default().merge(m, l, acc)
+
+
+def cpu_threads() -> int:
+    return os.cpu_count() or 1

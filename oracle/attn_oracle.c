@@ -1,0 +1,309 @@
+/*
+ * FP64 two-pass attention oracle.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path may include, link or
+ * call this file: only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg use it. It shares no source, header or table with the CUDA
+ * library.
+ *
+ * What it computes is the plain definition of scaled-dot-product attention
+ * that the streaming method reaches (up to rounding order):
+ *   "Intermediate and advanced kernel workshops", table "Scope and contracts"
+ *     (streaming_attention.attention row): softmax(scale * Q K^T) V with
+ *     scale = 1/sqrt(D) and the diagonal included when causal;
+ *   "Compare reasoning after your own attempt" (answer key), section
+ *     "Reference tradeoffs to challenge": the attention oracle materializes
+ *     FP64 scores, outside the timed call.
+ * For every query row it materializes the allowed score row in FP64, takes its
+ * maximum, exponentiates, sums and divides -- two passes over the row, no
+ * running state, no tiling.
+ *
+ * Readings where the pages are silent (each is also listed in the design
+ * notes of the repository):
+ *   - layout: Q,O are [B,Hq,M,D], K,V are [B,Hkv,N,D], row-major, D innermost;
+ *   - query row i sits at key position p_i = i + N - M (bottom-right causal
+ *     alignment; equals the pages' rule when M == N);
+ *   - window W > 0 keeps keys with p_i - W < j (W keys ending at p_i);
+ *   - GQA: query head h reads KV head h / (Hq / Hkv);
+ *   - a row with no allowed key outputs 0 (never NaN).
+ *
+ * The summary merge (oracle_merge_f64) follows the answer key's A1 row and
+ * its worked answer ("merging (2,2) and (4,1) yields (4,1+2*exp(-2))"): both
+ * summaries are re-expressed relative to the common maximum; (-inf, 0) is the
+ * empty summary and merging two empties must not form -inf - (-inf).
+ *
+ * ORACLE_MUTANT=<n> compiles a deliberately wrong variant; it exists only so
+ * that the pin tests can show that each planted mistake is caught.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL -1
+#define ORACLE_ENOMEM -2
+
+typedef struct {
+    int B, Hq, Hkv, M, N, D, causal, window;
+    double scale;
+} shape_t;
+
+static int check_shape(const shape_t* s) {
+    if (s->B < 0 || s->Hq < 0 || s->Hkv < 0 || s->M < 0 || s->N < 0 || s->D <= 0) return ORACLE_EINVAL;
+    if (s->Hq > 0 && (s->Hkv <= 0 || s->Hq % s->Hkv != 0)) return ORACLE_EINVAL;
+    return ORACLE_OK;
+}
+
+/* Position of query row i among the keys (bottom-right alignment). */
+static long query_position(const shape_t* s, long i) {
+#if ORACLE_MUTANT == 4
+    return i; /* planted: top-left alignment */
+#else
+    return i + (long)s->N - (long)s->M;
+#endif
+}
+
+/* Is key j visible to the query at position p? Causal keeps j <= p (diagonal
+ * included); a window W > 0 keeps the W keys ending at p. */
+static int key_allowed(const shape_t* s, long p, long j) {
+#if ORACLE_MUTANT == 1
+    if (s->causal && !(j < p)) return 0; /* planted: diagonal excluded */
+#else
+    if (s->causal && !(j <= p)) return 0;
+#endif
+#if ORACLE_MUTANT == 2
+    if (s->window > 0 && !(j >= p - s->window)) return 0; /* planted: W+1 keys */
+#else
+    if (s->window > 0 && !(j > p - s->window)) return 0;
+#endif
+    return 1;
+}
+
+static long kv_head(const shape_t* s, long h) {
+#if ORACLE_MUTANT == 3
+    return h % s->Hkv; /* planted: strided instead of contiguous groups */
+#else
+    return h / (s->Hq / s->Hkv);
+#endif
+}
+
+/* Pointers to the q row, and the K and V matrices [N, D] of the row's KV head. */
+static void row_operands(const shape_t* s, const double* q, const double* k, const double* v,
+                         long r, const double** qr, const double** kh, const double** vh, long* p) {
+    long bh = r / s->M, i = r % s->M;
+    long b = bh / s->Hq, h = bh % s->Hq;
+    long g = kv_head(s, h);
+    *qr = q + r * (long)s->D;
+    *kh = k + (b * s->Hkv + g) * (long)s->N * s->D;
+    *vh = v + (b * s->Hkv + g) * (long)s->N * s->D;
+    *p = query_position(s, i);
+}
+
+/* Score of key j: scale * <q_row, k_j>, summed in index order. */
+static double score(const shape_t* s, const double* qr, const double* kh, long j) {
+    double acc = 0.0;
+#if ORACLE_MUTANT == 8
+    for (long d = 0; d + 1 < s->D; ++d) acc += qr[d] * kh[j * s->D + d]; /* planted: last dim dropped */
+#elif ORACLE_MUTANT == 7
+    for (long d = 0; d < s->D; ++d) acc += qr[d] * kh[d * s->N + j]; /* planted: K read transposed */
+#else
+    for (long d = 0; d < s->D; ++d) acc += qr[d] * kh[j * s->D + d];
+#endif
+#if ORACLE_MUTANT == 6
+    return acc; /* planted: scale dropped */
+#else
+    return s->scale * acc;
+#endif
+}
+
+/* One output row, two passes over the materialized score row.
+ * srow: caller scratch of N doubles. Writes D values to out. */
+static void attend_row(const shape_t* s, const double* q, const double* k, const double* v,
+                       long r, double* srow, double* out) {
+    const double *qr, *kh, *vh;
+    long p;
+    row_operands(s, q, k, v, r, &qr, &kh, &vh, &p);
+    for (long d = 0; d < s->D; ++d) out[d] = 0.0;
+
+    /* pass 1: materialize the allowed scores and their maximum */
+    double mu = -INFINITY;
+    long count = 0;
+    for (long j = 0; j < s->N; ++j) {
+        if (!key_allowed(s, p, j)) { srow[j] = -INFINITY; continue; }
+        srow[j] = score(s, qr, kh, j);
+        if (srow[j] > mu) mu = srow[j];
+        ++count;
+    }
+    if (count == 0) return; /* empty allowed set: output 0 */
+
+    /* pass 2: weights exp(s - mu), their sum, and the weighted sum of V rows */
+    double z = 0.0;
+    for (long j = 0; j < s->N; ++j) {
+        if (srow[j] == -INFINITY) continue;
+        double w = exp(srow[j] - mu);
+        z += w;
+        for (long d = 0; d < s->D; ++d) out[d] += w * vh[j * s->D + d];
+    }
+#if ORACLE_MUTANT == 5
+    (void)z; /* planted: no normalization */
+#else
+    for (long d = 0; d < s->D; ++d) out[d] /= z;
+#endif
+}
+
+typedef struct {
+    const shape_t* s;
+    const double *q, *k, *v;
+    double* o;
+    const int64_t* rows; /* NULL: rows [lo, hi) of the full output */
+    int64_t lo, hi;
+    int status;
+} work_t;
+
+static void* worker(void* arg) {
+    work_t* w = (work_t*)arg;
+    double* srow = (double*)malloc(sizeof(double) * (size_t)(w->s->N > 0 ? w->s->N : 1));
+    if (!srow) { w->status = ORACLE_ENOMEM; return NULL; }
+    for (int64_t t = w->lo; t < w->hi; ++t) {
+        long r = w->rows ? (long)w->rows[t] : (long)t;
+        attend_row(w->s, w->q, w->k, w->v, r, srow, w->o + t * (int64_t)w->s->D);
+    }
+    free(srow);
+    w->status = ORACLE_OK;
+    return NULL;
+}
+
+static int run_rows(const shape_t* s, const double* q, const double* k, const double* v, double* o,
+                    const int64_t* rows, int64_t nrows, int nthreads) {
+    if (nrows <= 0) return ORACLE_OK;
+    if (nthreads <= 0) {
+        long c = sysconf(_SC_NPROCESSORS_ONLN);
+        nthreads = c > 0 ? (int)c : 1;
+    }
+    if (nthreads > nrows) nthreads = (int)nrows;
+    pthread_t* th = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+    work_t* ws = (work_t*)calloc((size_t)nthreads, sizeof(work_t));
+    if (!th || !ws) { free(th); free(ws); return ORACLE_ENOMEM; }
+    int status = ORACLE_OK;
+    for (int t = 0; t < nthreads; ++t) {
+        ws[t] = (work_t){s, q, k, v, o, rows, nrows * t / nthreads, nrows * (t + 1) / nthreads, ORACLE_OK};
+        if (pthread_create(&th[t], NULL, worker, &ws[t]) != 0) { worker(&ws[t]); th[t] = 0; }
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        if (th[t]) pthread_join(th[t], NULL);
+        if (ws[t].status != ORACLE_OK) status = ws[t].status;
+    }
+    free(th);
+    free(ws);
+    return status;
+}
+
+/* Full output o[B,Hq,M,D]. nthreads <= 0 uses every online core. */
+int oracle_attn_f64(const double* q, const double* k, const double* v, double* o,
+                    int B, int Hq, int Hkv, int M, int N, int D,
+                    int causal, int window, double scale, int nthreads) {
+    shape_t s = {B, Hq, Hkv, M, N, D, causal, window, scale};
+    if (check_shape(&s) != ORACLE_OK) return ORACLE_EINVAL;
+    return run_rows(&s, q, k, v, o, NULL, (int64_t)B * Hq * M, nthreads);
+}
+
+/* Selected rows only: rows[t] = (b*Hq + h)*M + i; o_rows is [nrows, D]. */
+int oracle_attn_rows_f64(const double* q, const double* k, const double* v, double* o_rows,
+                         int B, int Hq, int Hkv, int M, int N, int D,
+                         int causal, int window, double scale,
+                         const int64_t* rows, int64_t nrows, int nthreads) {
+    shape_t s = {B, Hq, Hkv, M, N, D, causal, window, scale};
+    if (check_shape(&s) != ORACLE_OK) return ORACLE_EINVAL;
+    int64_t total = (int64_t)B * Hq * M;
+    for (int64_t t = 0; t < nrows; ++t)
+        if (rows[t] < 0 || rows[t] >= total) return ORACLE_EINVAL;
+    return run_rows(&s, q, k, v, o_rows, rows, nrows, nthreads);
+}
+
+/* Normalized attention weights of one row over all N keys (0 where masked). */
+int oracle_attn_weights_f64(const double* q, const double* k,
+                            int B, int Hq, int Hkv, int M, int N, int D,
+                            int causal, int window, double scale, int64_t row, double* w) {
+    shape_t s = {B, Hq, Hkv, M, N, D, causal, window, scale};
+    if (check_shape(&s) != ORACLE_OK || row < 0 || row >= (int64_t)B * Hq * M) return ORACLE_EINVAL;
+    const double *qr, *kh, *vh;
+    long p;
+    row_operands(&s, q, k, k, (long)row, &qr, &kh, &vh, &p);
+    double mu = -INFINITY;
+    for (long j = 0; j < N; ++j) {
+        w[j] = key_allowed(&s, p, j) ? score(&s, qr, kh, j) : -INFINITY;
+        if (w[j] > mu) mu = w[j];
+    }
+    if (mu == -INFINITY) { for (long j = 0; j < N; ++j) w[j] = 0.0; return ORACLE_OK; }
+    double z = 0.0;
+    for (long j = 0; j < N; ++j) { w[j] = w[j] == -INFINITY ? 0.0 : exp(w[j] - mu); z += w[j]; }
+    for (long j = 0; j < N; ++j) w[j] /= z;
+    return ORACLE_OK;
+}
+
+/* Unnormalized summary (m, l, acc) of one row over the allowed keys in
+ * [j0, j1): m = max s_j, l = sum exp(s_j - m), acc = sum exp(s_j - m) v_j.
+ * An empty key set gives the empty summary (-inf, 0, 0). */
+int oracle_partial_f64(const double* q, const double* k, const double* v,
+                       int B, int Hq, int Hkv, int M, int N, int D,
+                       int causal, int window, double scale, int64_t row, int j0, int j1,
+                       double* m_out, double* l_out, double* acc_out) {
+    shape_t s = {B, Hq, Hkv, M, N, D, causal, window, scale};
+    if (check_shape(&s) != ORACLE_OK || row < 0 || row >= (int64_t)B * Hq * M) return ORACLE_EINVAL;
+    if (j0 < 0) j0 = 0;
+    if (j1 > N) j1 = N;
+    const double *qr, *kh, *vh;
+    long p;
+    row_operands(&s, q, k, v, (long)row, &qr, &kh, &vh, &p);
+    double mu = -INFINITY;
+    for (long j = j0; j < j1; ++j)
+        if (key_allowed(&s, p, j)) { double t = score(&s, qr, kh, j); if (t > mu) mu = t; }
+    *m_out = mu;
+    *l_out = 0.0;
+    for (long d = 0; d < D; ++d) acc_out[d] = 0.0;
+    if (mu == -INFINITY) return ORACLE_OK;
+    for (long j = j0; j < j1; ++j) {
+        if (!key_allowed(&s, p, j)) continue;
+        double w = exp(score(&s, qr, kh, j) - mu);
+        *l_out += w;
+        for (long d = 0; d < D; ++d) acc_out[d] += w * vh[j * D + d];
+    }
+    return ORACLE_OK;
+}
+
+/* Merge S summaries (m_s, l_s, acc_s[D]) into one, folding left to right:
+ * (m1,l1,a1) (+) (m2,l2,a2) = (m, l1 e^{m1-m} + l2 e^{m2-m}, a1 e^{m1-m} + a2 e^{m2-m}),
+ * m = max(m1, m2); a summary with m = -inf contributes weight 0. */
+void oracle_merge_f64(int S, int D, const double* m, const double* l, const double* acc,
+                      double* m_out, double* l_out, double* acc_out) {
+    double mc = -INFINITY, lc = 0.0;
+    for (int d = 0; d < D; ++d) acc_out[d] = 0.0;
+    for (int t = 0; t < S; ++t) {
+        double mn = m[t] > mc ? m[t] : mc;
+#if ORACLE_MUTANT == 10
+        double wc = exp(mc - mn), wt = exp(m[t] - mn); /* planted: no empty guard */
+#else
+        double wc = (mc == -INFINITY) ? 0.0 : exp(mc - mn);
+        double wt = (m[t] == -INFINITY) ? 0.0 : exp(m[t] - mn);
+#endif
+#if ORACLE_MUTANT == 9
+        lc = lc + l[t]; /* planted: raw denominator addition */
+        (void)wc;
+#else
+        lc = lc * wc + l[t] * wt;
+#endif
+        for (int d = 0; d < D; ++d) acc_out[d] = acc_out[d] * wc + acc[(int64_t)t * D + d] * wt;
+        mc = mn;
+    }
+    *m_out = mc;
+    *l_out = lc;
+}
+
+int oracle_mutant_id(void) { return ORACLE_MUTANT; }

@@ -1,0 +1,23 @@
+"""GB300-native streaming attention forward.
+
+The compute path is the C-ABI shared library built from ``csrc/``; the
+Python functions in ``binding`` only marshal arguments to it. Importing this
+package does not load the library: the first call does, and it raises if the
+library has not been built.
+"""
+from .binding import (  # noqa: F401
+    ATTN_BF16,
+    ATTN_FP16,
+    PATH_AUTO,
+    PATH_DECODE,
+    PATH_PREFILL,
+    PATH_SIMT,
+    AttnError,
+    attention,
+    attn_fwd,
+    attn_fwd_ex,
+    attn_fwd_host,
+    attn_workspace_bytes,
+    lib,
+    library_path,
+)

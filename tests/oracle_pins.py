@@ -1,0 +1,260 @@
+"""Pins for the FP64 oracle: checks against what the pages and mathematics fix.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises AssertionError when the
+oracle disagrees with an outside fact: a worked answer printed on the pages
+(fixtures under ``tests/golden/``), a closed form, an invariant, or an
+independent library formula on tiny inputs. ``test_oracle_pins.py`` runs them
+on the real oracle, and on deliberately broken builds to show that each
+planted mistake is caught by at least one pin.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _rand(shape, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(shape, generator=g, dtype=torch.float64).numpy()
+
+
+# --------------------------------------------------------------------------
+# Worked answers printed on the pages
+# --------------------------------------------------------------------------
+def a3_inputs():
+    """D=1 encoding of the A3 example: q = 1, k_j = logit_j, scale = 1."""
+    fx = _golden("a3_worked_example.json")
+    logits = [math.log(2.0) if x == "ln2" else float(x) for x in fx["logits"]]
+    q = np.ones((1, 1, 1, 1))
+    k = np.array(logits, dtype=np.float64).reshape(1, 1, 3, 1)
+    v = np.array(fx["values"], dtype=np.float64).reshape(1, 1, 3, 1)
+    return fx, q, k, v
+
+
+def pin_a3_worked_example(orc):
+    fx, q, k, v = a3_inputs()
+    for causal in (False, True):  # M=1 sits at position N-1, so causal sees every key
+        o = orc.attention(q, k, v, causal=causal, scale=1.0)[0, 0, 0, 0]
+        assert abs(o - fx["expected"]) <= fx["tol"], (causal, o)
+        assert abs(o - fx["missing_alpha_bug"]) > 0.5, o
+
+
+def pin_a1_merge_example(orc):
+    fx = _golden("a1_merge_example.json")
+    (m1, l1), (m2, l2) = fx["a"], fx["b"]
+    want_l = 1.0 + 2.0 * math.exp(-2.0)
+    for order in ((0, 1), (1, 0)):
+        ms = np.array([m1, m2])[list(order)]
+        ls = np.array([l1, l2])[list(order)]
+        acc = np.array([[3.0], [5.0]])[list(order)]
+        m, l, a = orc.merge(ms, ls, acc)
+        assert abs(m - fx["expected_m"]) <= fx["tol"], m
+        assert abs(l - want_l) <= fx["tol"], l
+        # the numerator follows the same weights: 3 e^{2-4} + 5 e^{4-4}
+        want_a = (3.0 * math.exp(-2.0) + 5.0) if order == (0, 1) else (5.0 + 3.0 * math.exp(-2.0))
+        assert abs(a[0] - want_a) <= 1e-12, a
+
+
+def pin_merge_empty(orc):
+    m, l, a = orc.merge([-np.inf, -np.inf], [0.0, 0.0], [[0.0, 0.0], [0.0, 0.0]])
+    assert m == -np.inf and l == 0.0 and np.all(a == 0.0), (m, l, a)
+    assert not np.isnan(l) and not np.any(np.isnan(a))
+    # the empty summary is an identity on either side
+    for order in ((0, 1), (1, 0)):
+        ms = np.array([-np.inf, 1.5])[list(order)]
+        ls = np.array([0.0, 2.5])[list(order)]
+        acc = np.array([[0.0, 0.0], [4.0, -1.0]])[list(order)]
+        m, l, a = orc.merge(ms, ls, acc)
+        assert m == 1.5 and abs(l - 2.5) < 1e-15 and np.allclose(a, [4.0, -1.0], atol=0, rtol=1e-15)
+
+
+def pin_merge_algebra(orc):
+    rng = np.random.default_rng(7)
+    for _ in range(20):
+        ms = rng.normal(0, 3, 3)
+        ls = rng.uniform(0.5, 4, 3)
+        acc = rng.normal(0, 1, (3, 4))
+        one = orc.merge(ms, ls, acc)
+        # left: ((a (+) b) (+) c) built explicitly
+        ab = orc.merge(ms[:2], ls[:2], acc[:2])
+        left = orc.merge([ab[0], ms[2]], [ab[1], ls[2]], np.stack([ab[2], acc[2]]))
+        bc = orc.merge(ms[1:], ls[1:], acc[1:])
+        right = orc.merge([ms[0], bc[0]], [ls[0], bc[1]], np.stack([acc[0], bc[2]]))
+        perm = [2, 0, 1]
+        swapped = orc.merge(ms[perm], ls[perm], acc[perm])
+        for other in (left, right, swapped):
+            assert abs(other[0] - one[0]) == 0.0
+            assert abs(other[1] - one[1]) <= 1e-12 * abs(one[1])
+            assert np.allclose(other[2], one[2], rtol=1e-12, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# Summaries: splitting the keys and merging equals the unsplit summary, and
+# the summary normalizes to the attention output
+# --------------------------------------------------------------------------
+def pin_split_merge(orc):
+    B, Hq, Hkv, M, N, D = 1, 2, 1, 5, 23, 6
+    q, k, v = _rand((B, Hq, M, D), 1), _rand((B, Hkv, N, D), 2), _rand((B, Hkv, N, D), 3)
+    for causal, window in ((False, 0), (True, 0), (True, 7)):
+        out = orc.attention(q, k, v, causal=causal, window=window)
+        for row in range(B * Hq * M):
+            m, l, a = orc.partial(q, k, v, row, 0, N, causal, window)
+            assert np.allclose(a / l, out.reshape(-1, D)[row], rtol=1e-12, atol=1e-13)
+            cuts = [0, 4, 5, 11, 17, 23]
+            parts = [orc.partial(q, k, v, row, c0, c1, causal, window) for c0, c1 in zip(cuts, cuts[1:])]
+            mm, ll, aa = orc.merge([p[0] for p in parts], [p[1] for p in parts], np.stack([p[2] for p in parts]))
+            assert mm == m and abs(ll - l) <= 1e-12 * l and np.allclose(aa, a, rtol=1e-12, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# Independent library formula on tiny inputs (all masks, GQA, ragged)
+# --------------------------------------------------------------------------
+def library_attention(q, k, v, causal, window, scale):
+    """softmax(scale Q K^T + mask) V with torch float64 routines; masks from
+    triangular library routines; rows with no allowed key give 0."""
+    q, k, v = (torch.from_numpy(np.asarray(x)) for x in (q, k, v))
+    B, Hq, M, D = q.shape
+    Hkv, N = k.shape[1], k.shape[2]
+    k = k.repeat_interleave(Hq // Hkv, dim=1)
+    v = v.repeat_interleave(Hq // Hkv, dim=1)
+    keep = torch.ones(M, N, dtype=torch.bool)
+    if causal:
+        keep &= torch.ones(M, N, dtype=torch.bool).tril(diagonal=N - M)
+    if window > 0:
+        keep &= torch.ones(M, N, dtype=torch.bool).triu(diagonal=N - M - window + 1)
+    s = torch.matmul(q, k.transpose(-1, -2)) * scale
+    s = s.masked_fill(~keep, float("-inf"))
+    w = torch.softmax(s, dim=-1)
+    w = torch.nan_to_num(w, nan=0.0)  # rows with every key masked
+    return torch.matmul(w, v).numpy()
+
+
+def pin_bruteforce(orc):
+    rng = np.random.default_rng(11)
+    for trial in range(40):
+        Hkv = int(rng.integers(1, 4))
+        Hq = Hkv * int(rng.integers(1, 4))
+        B, M, N = int(rng.integers(1, 3)), int(rng.integers(1, 9)), int(rng.integers(1, 9))
+        D = int(rng.choice([1, 3, 8, 16]))
+        causal = bool(rng.integers(0, 2))
+        window = int(rng.choice([0, 0, 1, 2, 5]))
+        q = _rand((B, Hq, M, D), 100 + trial)
+        k = _rand((B, Hkv, N, D), 200 + trial)
+        v = _rand((B, Hkv, N, D), 300 + trial)
+        scale = 1.0 / math.sqrt(D)
+        got = orc.attention(q, k, v, causal=causal, window=window)
+        want = library_attention(q, k, v, causal, window, scale)
+        assert np.allclose(got, want, rtol=1e-12, atol=1e-12), (B, Hq, Hkv, M, N, D, causal, window)
+
+
+# --------------------------------------------------------------------------
+# Invariants
+# --------------------------------------------------------------------------
+def pin_invariants(orc):
+    B, Hq, Hkv, M, N, D = 1, 2, 2, 9, 13, 5
+    q, k, v = _rand((B, Hq, M, D), 21), _rand((B, Hkv, N, D), 22), _rand((B, Hkv, N, D), 23)
+    for causal, window in ((False, 0), (True, 0), (True, 4), (False, 6)):
+        out = orc.attention(q, k, v, causal=causal, window=window).reshape(-1, D)
+        for row in range(B * Hq * M):
+            w = orc.weights(q, k, row, causal, window)
+            assert abs(w.sum() - 1.0) < 1e-13 and np.all(w >= 0)
+            bh, i = divmod(row, M)
+            vh = v[0, bh % Hq]
+            allowed = w > 0
+            lo, hi = vh[allowed].min(axis=0), vh[allowed].max(axis=0)
+            assert np.all(out[row] >= lo - 1e-12) and np.all(out[row] <= hi + 1e-12)
+        # adding a per-row constant to every logit changes nothing: one extra
+        # coordinate with q' = c_row / scale and k' = 1 adds c_row to the row
+        scale = 1.0 / math.sqrt(D)
+        c = np.arange(B * Hq * M, dtype=np.float64).reshape(B, Hq, M, 1) * 3.7 - 11.0
+        q2 = np.concatenate([q, c / scale], axis=-1)
+        k2 = np.concatenate([k, np.ones((B, Hkv, N, 1))], axis=-1)
+        v2 = np.concatenate([v, np.zeros((B, Hkv, N, 1))], axis=-1)
+        out2 = orc.attention(q2, k2, v2, causal=causal, window=window, scale=scale)[..., :D]
+        assert np.allclose(out2.reshape(-1, D), out, rtol=1e-10, atol=1e-11)
+    # noncausal output is equivariant to permuting keys and values together
+    perm = np.random.default_rng(3).permutation(N)
+    a = orc.attention(q, k, v)
+    b = orc.attention(q, k[:, :, perm], v[:, :, perm])
+    assert np.allclose(a, b, rtol=1e-12, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# Closed forms
+# --------------------------------------------------------------------------
+def pin_closed_forms(orc):
+    D = 4
+    q, k, v = _rand((1, 1, 6, D), 31), _rand((1, 1, 6, D), 32), _rand((1, 1, 6, D), 33)
+    # N = 1: every row returns v_0
+    o = orc.attention(q, k[:, :, :1], v[:, :, :1])
+    assert np.allclose(o, np.broadcast_to(v[:, :, :1], o.shape), rtol=0, atol=1e-15)
+    # q = 0: uniform weights over the allowed keys
+    o = orc.attention(np.zeros_like(q), k, v, causal=True)
+    for i in range(6):
+        assert np.allclose(o[0, 0, i], v[0, 0, : i + 1].mean(axis=0), rtol=1e-13, atol=1e-14)
+    # causal with M == N: row 0 sees only key 0
+    o = orc.attention(q, k, v, causal=True)
+    assert np.allclose(o[0, 0, 0], v[0, 0, 0], rtol=0, atol=1e-15)
+    # window = 1: each row sees only its own position
+    o = orc.attention(q, k, v, causal=True, window=1)
+    assert np.allclose(o[0, 0], v[0, 0], rtol=0, atol=1e-15)
+    # identical key rows: uniform weights
+    o = orc.attention(q, np.broadcast_to(k[:, :, :1], k.shape).copy(), v)
+    assert np.allclose(o[0, 0], np.broadcast_to(v[0, 0].mean(axis=0), (6, D)), rtol=1e-13, atol=1e-14)
+    # one query (decode) sits at position N-1: causal equals noncausal
+    a = orc.attention(q[:, :, :1], k, v, causal=True)
+    b = orc.attention(q[:, :, :1], k, v, causal=False)
+    assert np.allclose(a, b, rtol=0, atol=0)
+    # M > N causal: rows i < M-N have no allowed key and give 0
+    o = orc.attention(q, k[:, :, :2], v[:, :, :2], causal=True)
+    assert np.all(o[0, 0, :4] == 0.0) and np.allclose(o[0, 0, 4], v[0, 0, 0], atol=1e-15)
+    # N = 0 gives zeros, M = 0 gives an empty output
+    o = orc.attention(q, k[:, :, :0], v[:, :, :0])
+    assert o.shape == (1, 1, 6, D) and np.all(o == 0.0)
+    o = orc.attention(q[:, :, :0], k, v)
+    assert o.shape == (1, 1, 0, D)
+    # D = 1 with logits [0, ln 3] under scale 1: weights 1/4 and 3/4
+    o = orc.attention(np.ones((1, 1, 1, 1)), np.array([0.0, math.log(3.0)]).reshape(1, 1, 2, 1),
+                      np.array([8.0, 4.0]).reshape(1, 1, 2, 1), scale=1.0)
+    assert abs(o[0, 0, 0, 0] - 5.0) < 1e-14
+    # the default scale is 1/sqrt(D): scaling q by 2 and passing scale/2 is the same
+    a = orc.attention(q, k, v)
+    b = orc.attention(2.0 * q, k, v, scale=0.5 / math.sqrt(D))
+    assert np.allclose(a, b, rtol=1e-13, atol=1e-14)
+
+
+def pin_gqa_map(orc):
+    """Hq=4 over Hkv=2: heads 0,1 read KV head 0 and heads 2,3 read KV head 1."""
+    D, N = 3, 5
+    q = _rand((1, 4, 2, D), 41)
+    k = np.broadcast_to(_rand((1, 2, 1, D), 42), (1, 2, N, D)).copy()  # uniform weights within a head
+    v = np.zeros((1, 2, N, D))
+    v[0, 0] = 1.0
+    v[0, 1] = 2.0
+    o = orc.attention(q, k, v)
+    assert np.allclose(o[0, 0], 1.0) and np.allclose(o[0, 1], 1.0)
+    assert np.allclose(o[0, 2], 2.0) and np.allclose(o[0, 3], 2.0)
+
+
+ALL_PINS = [
+    pin_a3_worked_example,
+    pin_a1_merge_example,
+    pin_merge_empty,
+    pin_merge_algebra,
+    pin_split_merge,
+    pin_bruteforce,
+    pin_invariants,
+    pin_closed_forms,
+    pin_gqa_map,
+]

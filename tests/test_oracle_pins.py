@@ -1,0 +1,73 @@
+"""The oracle against its pins (CPU only), and planted mistakes against the pins."""
+import math
+import os
+import tempfile
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle_pins as P
+
+
+@pytest.mark.parametrize("pin", P.ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(pin, oracle_lib):
+    pin(oracle_lib)
+
+
+def _stream(logits, values, tile, rescale_numerator=True):
+    """Running (m, l, a) over key tiles, as the A3 row of the answer key
+    describes; with rescale_numerator=False it reproduces the missing-alpha bug."""
+    m, l, a = -math.inf, 0.0, 0.0
+    for t0 in range(0, len(logits), tile):
+        s = logits[t0:t0 + tile]
+        m_new = max(m, max(s))
+        alpha = 0.0 if m == -math.inf else math.exp(m - m_new)
+        p = [math.exp(x - m_new) for x in s]
+        l = l * alpha + sum(p)
+        a = (a * alpha if rescale_numerator else a) + sum(pi * vi for pi, vi in zip(p, values[t0:t0 + tile]))
+        m = m_new
+    return a / l
+
+
+def test_a3_fixture_discriminates_missing_alpha():
+    fx, q, k, v = P.a3_inputs()
+    logits = list(k.reshape(-1))
+    values = list(v.reshape(-1))
+    assert abs(_stream(logits, values, tile=2) - fx["expected"]) < 1e-12
+    assert abs(_stream(logits, values, tile=2, rescale_numerator=False) - fx["missing_alpha_bug"]) < 1e-12
+
+
+# Each planted mistake (compiled with ORACLE_MUTANT=n) must fail at least one pin.
+MUTANTS = {
+    1: "causal mask drops the diagonal",
+    2: "window keeps W+1 keys",
+    3: "GQA strided head map",
+    4: "top-left causal alignment",
+    5: "output not normalized",
+    6: "scale dropped",
+    7: "K read transposed",
+    8: "last head dimension dropped",
+    9: "merge adds raw denominators",
+    10: "merge without the empty guard",
+}
+
+
+@pytest.fixture(scope="module")
+def mutant_dir():
+    with tempfile.TemporaryDirectory() as d:
+        yield d
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS), ids=lambda n: f"m{n}")
+def test_planted_mistake_is_caught(mutant, mutant_dir):
+    orc = oracle.Oracle(mutant, out_dir=mutant_dir)
+    assert orc.lib.oracle_mutant_id() == mutant
+    failed = []
+    for pin in P.ALL_PINS:
+        try:
+            with np.errstate(all="ignore"):
+                pin(orc)
+        except (AssertionError, ValueError, IndexError):
+            failed.append(pin.__name__)
+    assert failed, f"mutant {mutant} ({MUTANTS[mutant]}) passed every pin"
