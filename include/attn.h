@@ -1,0 +1,161 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) streaming attention forward library.
+ *
+ * The operation (every entry point below computes it or one of its parts):
+ *   O[b,h,i,:] = sum_j softmax_j(scale * <Q[b,h,i,:], K[b,g,j,:]>) V[b,g,j,:]
+ * over the keys j that row i may see, computed as a stream over key tiles that
+ * carries a running (m, l, acc) state per row and never forms the full score
+ * matrix ("Intermediate and advanced kernel workshops", table "Scope and
+ * contracts", streaming_attention.attention row; answer key, central-idea
+ * table, A3 row: carry (m, l, a) while multiplying one score tile at a time).
+ *
+ * Conventions shared by every entry point:
+ *   Layout      Q and O are [B, Hq, M, D]; K and V are [B, Hkv, N, D]; all
+ *               row-major and contiguous, D innermost. The pages define one
+ *               head [N, D] contiguous; batching and heads are this library's
+ *               extension.
+ *   GQA         query head h reads KV head g = h / (Hq / Hkv); Hq % Hkv == 0.
+ *   Positions   query row i sits at key position p_i = i + N - M
+ *               (bottom-right alignment; with M == N it is the pages' rule).
+ *   causal      != 0 keeps keys j <= p_i (diagonal included, as on the pages).
+ *   window      W > 0 keeps keys j > p_i - W (the W keys ending at p_i);
+ *               W <= 0 disables it.
+ *   scale       multiplies the logits; 0.0f selects the pages' 1/sqrt(D).
+ *   Masked keys score -inf ("Kernel Notes & Checklist", gotchas ledger:
+ *               masked and padded columns must be -inf, never 0). A row with
+ *               no visible key (N == 0, or causal with p_i < 0) outputs 0,
+ *               never NaN (same ledger, ghost rows).
+ *   Precision   FP16 or BF16 in and out, FP32 accumulation, one cast at the
+ *               end (scope table: FP32 epilogue, then one output cast). P is
+ *               rounded to the input type before the P.V product (contract
+ *               notes under the scope table).
+ *   Pointers    q, k, v, o are DEVICE pointers owned by the caller, 16-byte
+ *               aligned; o must not overlap q, k or v. They may be NULL only
+ *               when the tensor has zero elements.
+ *   Streams     `stream` is a cudaStream_t (NULL = legacy default stream).
+ *               Every call is asynchronous on it and never synchronizes,
+ *               except attn_fwd_host and attn_last_device_status.
+ *   Values      only metadata is validated, never values (scope notes: wrappers
+ *               validate metadata but do not scan values); inputs must be
+ *               finite. Every tensor's element count must fit a signed 32-bit
+ *               index (same notes).
+ *   Errors      a negative attn_status_t; nothing is thrown across the ABI.
+ *               On a validation error no kernel has been launched.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+/* Exported symbols stay visible when the library is built with hidden default visibility. */
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { ATTN_BF16 = 0, ATTN_FP16 = 1, ATTN_FP32 = 2 } attn_dtype_t;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_NULL = -1,      /* a required pointer is NULL */
+    ATTN_ERR_SHAPE = -2,     /* a negative size, or Hkv == 0 with Hq > 0 */
+    ATTN_ERR_DTYPE = -3,     /* dtype is not ATTN_BF16 / ATTN_FP16 */
+    ATTN_ERR_HEADDIM = -4,   /* D is not supported by the requested path */
+    ATTN_ERR_GQA = -5,       /* Hq is not a multiple of Hkv */
+    ATTN_ERR_OVERFLOW = -6,  /* an element count does not fit a signed 32-bit index */
+    ATTN_ERR_ALIGN = -7,     /* a pointer is not 16-byte aligned */
+    ATTN_ERR_WORKSPACE = -8, /* workspace NULL or smaller than attn_workspace_bytes() */
+    ATTN_ERR_CUDA = -9,      /* a CUDA runtime/driver call failed (launch, copy, ...) */
+    ATTN_ERR_TIMEOUT = -10,  /* a kernel gave up on a bounded wait (see attn_last_device_status) */
+    ATTN_ERR_PATH = -11      /* the requested path cannot run this problem */
+} attn_status_t;
+
+/* Kernel paths. AUTO picks: split-KV decode when (Hq/Hkv)*M <= 16 and the
+ * visible key range is long; the tcgen05 prefill kernel for D in {64, 128};
+ * the SIMT kernel otherwise (D in {16, 32, 64, 128}). */
+typedef enum {
+    ATTN_PATH_AUTO = 0,
+    ATTN_PATH_SIMT = 1,    /* CUDA-core streaming kernel, any supported D */
+    ATTN_PATH_PREFILL = 2, /* warp-specialized TMA + tcgen05 + TMEM kernel, D in {64,128} */
+    ATTN_PATH_DECODE = 3   /* split-KV over grouped query heads, then the merge kernel */
+} attn_path_t;
+
+/* Forward attention, the spec entry point.
+ *   q [B,Hq,M,D], k/v [B,Hkv,N,D], o [B,Hq,M,D]: device pointers (see above).
+ *   dtype: ATTN_BF16 or ATTN_FP16 for all four tensors.
+ * Picks the path as ATTN_PATH_AUTO does. When that path needs workspace
+ * (split-KV decode) it is allocated stream-ordered on `stream` with
+ * cudaMallocAsync and released with cudaFreeAsync after the launches.
+ * Empty problems: B*Hq == 0 or M == 0 launches nothing; N == 0 zero-fills o.
+ * Returns ATTN_OK or a negative status. */
+ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o,
+                      int B, int Hq, int Hkv, int M, int N, int D,
+                      int causal, int window, float scale, int dtype, void* stream);
+
+/* Bytes of caller workspace that attn_fwd_ex needs for this problem on this
+ * path (0 when the path needs none). Returns 0 for invalid shapes too. */
+ATTN_API size_t attn_workspace_bytes(int B, int Hq, int Hkv, int M, int N, int D,
+                                     int causal, int window, int path);
+
+/* attn_fwd with an explicit path and caller-owned device workspace.
+ *   path: an attn_path_t; a forced path that cannot run the problem returns
+ *         ATTN_ERR_PATH (or ATTN_ERR_HEADDIM for an unsupported D).
+ *   workspace: device memory of at least attn_workspace_bytes(...) bytes,
+ *         16-byte aligned, or NULL when that is 0. It must stay untouched
+ *         until the work queued on `stream` has finished. */
+ATTN_API int attn_fwd_ex(const void* q, const void* k, const void* v, void* o,
+                         int B, int Hq, int Hkv, int M, int N, int D,
+                         int causal, int window, float scale, int dtype, int path,
+                         void* workspace, size_t ws_bytes, void* stream);
+
+/* Merge of split summaries, the pages' common-maximum rule (answer key,
+ * central-idea table, A1 row, and its worked answer: (2,2) and (4,1) merge
+ * to (4, 1+2e^-2)).
+ *   m, l: device float [rows][S]; acc: device float [rows][S][D]. Summary s of
+ *   a row is (m_s, l_s, acc_s) with l_s = sum exp(x - m_s) and acc_s the
+ *   matching unnormalized sum of value rows; (-inf, 0, 0) is the empty one.
+ *   o: device [rows][D] in out_dtype (ATTN_BF16, ATTN_FP16 or ATTN_FP32),
+ *   receives sum_s w_s acc_s / sum_s w_s l_s with w_s = exp(m_s - max m), or
+ *   0 when every summary is empty.
+ *   m_out, l_out: optional device float [rows] (NULL to skip) receiving the
+ *   merged summary.
+ * rows >= 0, 1 <= S <= 4096, 1 <= D <= 256. */
+ATTN_API int attn_merge(const float* m, const float* l, const float* acc, void* o,
+                        float* m_out, float* l_out, int rows, int S, int D, int out_dtype,
+                        void* stream);
+
+/* End-to-end call on HOST buffers: copies q, k, v from host memory into the
+ * caller's device buffers, runs attn_fwd_ex with ATTN_PATH_AUTO, copies o back
+ * to host memory, and synchronizes `stream` before returning.
+ *   *_h: host pointers (pinned memory gives asynchronous copies);
+ *   *_d: device buffers of the same sizes, owned by the caller;
+ *   workspace/ws_bytes: as attn_fwd_ex (may be NULL/0 when none is needed).
+ * Returns ATTN_OK, a validation status, or ATTN_ERR_CUDA. */
+ATTN_API int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h,
+                           void* q_d, void* k_d, void* v_d, void* o_d,
+                           int B, int Hq, int Hkv, int M, int N, int D,
+                           int causal, int window, float scale, int dtype,
+                           void* workspace, size_t ws_bytes, void* stream);
+
+/* Human-readable text for a status code (static storage). */
+ATTN_API const char* attn_strerror(int status);
+
+/* Synchronizes `stream`, then returns and clears the device status word that
+ * kernels set when a bounded wait gives up: ATTN_OK when none did, else
+ * ATTN_ERR_TIMEOUT. ATTN_ERR_CUDA if the synchronization itself failed. */
+ATTN_API int attn_last_device_status(void* stream);
+
+/* Library ABI version (major*100 + minor). */
+ATTN_API int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

@@ -8,6 +8,7 @@ library has not been built.
 from .binding import (  # noqa: F401
     ATTN_BF16,
     ATTN_FP16,
+    ATTN_FP32,
     PATH_AUTO,
     PATH_DECODE,
     PATH_PREFILL,
@@ -17,7 +18,10 @@ from .binding import (  # noqa: F401
     attn_fwd,
     attn_fwd_ex,
     attn_fwd_host,
+    attn_merge,
     attn_workspace_bytes,
+    last_device_status,
     lib,
     library_path,
+    strerror,
 )

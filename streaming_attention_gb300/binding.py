@@ -1,0 +1,173 @@
+"""ctypes binding of the C ABI declared in ``include/attn.h``.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libattn_gb300.so``. The library is loaded on first use; if it is
+missing, the call raises -- there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_FILE = os.path.join(_HERE, "libattn_gb300.so")
+
+ATTN_BF16, ATTN_FP16, ATTN_FP32 = 0, 1, 2
+PATH_AUTO, PATH_SIMT, PATH_PREFILL, PATH_DECODE = 0, 1, 2, 3
+ATTN_OK = 0
+
+_DTYPES = {torch.bfloat16: ATTN_BF16, torch.float16: ATTN_FP16, torch.float32: ATTN_FP32}
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({strerror(status)})")
+
+
+def library_path() -> str:
+    return _LIB_FILE
+
+
+def lib() -> ctypes.CDLL:
+    """Load the shared library (raises FileNotFoundError if it was not built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_FILE):
+                raise FileNotFoundError(
+                    f"{_LIB_FILE} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+            L = ctypes.CDLL(_LIB_FILE)
+            vp, ci, cf, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+            L.attn_fwd.argtypes = [vp, vp, vp, vp] + [ci] * 8 + [cf, ci, vp]
+            L.attn_fwd.restype = ci
+            L.attn_fwd_ex.argtypes = [vp, vp, vp, vp] + [ci] * 8 + [cf, ci, ci, vp, sz, vp]
+            L.attn_fwd_ex.restype = ci
+            L.attn_workspace_bytes.argtypes = [ci] * 9
+            L.attn_workspace_bytes.restype = sz
+            L.attn_merge.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, vp]
+            L.attn_merge.restype = ci
+            L.attn_fwd_host.argtypes = [vp] * 8 + [ci] * 8 + [cf, ci, vp, sz, vp]
+            L.attn_fwd_host.restype = ci
+            L.attn_strerror.argtypes = [ci]
+            L.attn_strerror.restype = ctypes.c_char_p
+            L.attn_last_device_status.argtypes = [vp]
+            L.attn_last_device_status.restype = ci
+            L.attn_version.argtypes = []
+            L.attn_version.restype = ci
+            _lib = L
+        return _lib
+
+
+def strerror(status: int) -> str:
+    try:
+        return lib().attn_strerror(int(status)).decode()
+    except FileNotFoundError:
+        return "library not loaded"
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None or t.numel() == 0 else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(status: int, where: str) -> None:
+    if status != ATTN_OK:
+        raise AttnError(status, where)
+
+
+def _dims(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: Optional[torch.Tensor]):
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D: [B, Hq, M, D] and [B, Hkv, N, D]")
+    B, Hq, M, D = q.shape
+    Bk, Hkv, N, Dk = k.shape
+    if (Bk, Dk) != (B, D) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    if o is not None and tuple(o.shape) != tuple(q.shape):
+        raise ValueError("o must have the shape of q")
+    for t in (q, k, v) + ((o,) if o is not None else ()):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+        if t.dtype != q.dtype:
+            raise ValueError("q, k, v, o must share one dtype")
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("dtype must be bfloat16 or float16")
+    return B, Hq, Hkv, M, N, D
+
+
+def attn_workspace_bytes(B, Hq, Hkv, M, N, D, causal=False, window=0, path=PATH_AUTO) -> int:
+    return int(lib().attn_workspace_bytes(B, Hq, Hkv, M, N, D, int(bool(causal)), int(window), int(path)))
+
+
+def attn_fwd(q, k, v, o, causal=False, window=0, scale=0.0, stream=None) -> None:
+    """C-ABI ``attn_fwd`` on device tensors; writes ``o`` in place."""
+    B, Hq, Hkv, M, N, D = _dims(q, k, v, o)
+    st = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, Hq, Hkv, M, N, D, int(bool(causal)), int(window),
+                        float(scale or 0.0), _DTYPES[q.dtype], _stream(stream))
+    _check(st, "attn_fwd")
+
+
+def attn_fwd_ex(q, k, v, o, causal=False, window=0, scale=0.0, path=PATH_AUTO, workspace=None,
+                stream=None) -> None:
+    """C-ABI ``attn_fwd_ex``: explicit path, caller workspace (a uint8 device tensor)."""
+    B, Hq, Hkv, M, N, D = _dims(q, k, v, o)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, Hq, Hkv, M, N, D, int(bool(causal)),
+                           int(window), float(scale or 0.0), _DTYPES[q.dtype], int(path), _ptr(workspace),
+                           ws_bytes, _stream(stream))
+    _check(st, "attn_fwd_ex")
+
+
+def attention(q, k, v, causal=False, window=0, scale=0.0, path=PATH_AUTO, stream=None) -> torch.Tensor:
+    """Allocates a fresh contiguous output on q's device and runs the forward."""
+    o = torch.empty_like(q)
+    if path == PATH_AUTO:
+        attn_fwd(q, k, v, o, causal, window, scale, stream)
+    else:
+        B, Hq, Hkv, M, N, D = _dims(q, k, v, o)
+        nbytes = attn_workspace_bytes(B, Hq, Hkv, M, N, D, causal, window, path)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device) if nbytes else None
+        attn_fwd_ex(q, k, v, o, causal, window, scale, path, ws, stream)
+    return o
+
+
+def attn_merge(m, l, acc, out_dtype=torch.float32, with_stats=False, stream=None):
+    """C-ABI ``attn_merge``: m, l [rows, S] and acc [rows, S, D] float32 device tensors."""
+    rows, S = m.shape
+    D = acc.shape[-1]
+    o = torch.empty((rows, D), dtype=out_dtype, device=m.device)
+    mo = torch.empty(rows, dtype=torch.float32, device=m.device) if with_stats else None
+    lo = torch.empty(rows, dtype=torch.float32, device=m.device) if with_stats else None
+    st = lib().attn_merge(_ptr(m), _ptr(l), _ptr(acc), _ptr(o), _ptr(mo), _ptr(lo), rows, S, D,
+                          _DTYPES[out_dtype], _stream(stream))
+    _check(st, "attn_merge")
+    return (o, mo, lo) if with_stats else o
+
+
+def attn_fwd_host(q_h, k_h, v_h, o_h, q_d, k_d, v_d, o_d, causal=False, window=0, scale=0.0, workspace=None,
+                  stream=None) -> None:
+    """C-ABI ``attn_fwd_host``: host (pinned) tensors in and out, device staging buffers."""
+    B, Hq, Hkv, M, N, D = _dims(q_d, k_d, v_d, o_d)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().attn_fwd_host(_ptr(q_h), _ptr(k_h), _ptr(v_h), _ptr(o_h), _ptr(q_d), _ptr(k_d), _ptr(v_d),
+                             _ptr(o_d), B, Hq, Hkv, M, N, D, int(bool(causal)), int(window), float(scale or 0.0),
+                             _DTYPES[q_d.dtype], _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "attn_fwd_host")
+
+
+def last_device_status(stream=None) -> int:
+    return int(lib().attn_last_device_status(_stream(stream)))

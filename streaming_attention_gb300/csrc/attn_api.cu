@@ -1,0 +1,244 @@
+// C ABI entry points: metadata validation, path choice, workspace handling.
+// Every step of the computation runs in the kernels of this library.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "attn.h"
+#include "attn_internal.h"
+
+namespace attn {
+namespace {
+
+// Device status word: kernels set it when a bounded wait gives up.
+__device__ int g_status_word;
+
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices] = {};
+
+int* status_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int*>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+constexpr int64_t kI32Max = 2147483647LL;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool simt_head_dim(int D) { return D == 16 || D == 32 || D == 64 || D == 128; }
+
+// Validates metadata only (never values) and fills the problem description.
+int validate(const void* q, const void* k, const void* v, const void* o, int B, int Hq, int Hkv, int M, int N,
+             int D, int causal, int window, float scale, int dtype, Problem* p) {
+    if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_DTYPE;
+    if (B < 0 || Hq < 0 || Hkv < 0 || M < 0 || N < 0 || D <= 0) return ATTN_ERR_SHAPE;
+    if (Hq > 0 && Hkv == 0) return ATTN_ERR_SHAPE;
+    if (Hq > 0 && Hq % Hkv != 0) return ATTN_ERR_GQA;
+    if (!simt_head_dim(D)) return ATTN_ERR_HEADDIM;
+    const int64_t nq = (int64_t)B * Hq * M * D;
+    const int64_t nk = (int64_t)B * Hkv * N * D;
+    if (nq > kI32Max || nk > kI32Max) return ATTN_ERR_OVERFLOW;
+    if ((nq > 0 && (!q || !o)) || (nk > 0 && (!k || !v))) return ATTN_ERR_NULL;
+    if ((q && !aligned16(q)) || (k && !aligned16(k)) || (v && !aligned16(v)) || (o && !aligned16(o)))
+        return ATTN_ERR_ALIGN;
+    p->B = B;
+    p->Hq = Hq;
+    p->Hkv = Hkv;
+    p->M = M;
+    p->N = N;
+    p->D = D;
+    p->causal = causal ? 1 : 0;
+    p->window = window > 0 ? window : 0;
+    p->scale = (scale == 0.0f) ? (float)(1.0 / sqrt((double)D)) : scale;
+    p->scale_log2 = p->scale * kLog2e;
+    p->dtype = dtype;
+    p->G = Hkv > 0 ? Hq / Hkv : 1;
+    // union of the visible key ranges: row 0 gives the lowest start, row M-1
+    // the highest end (both bounds grow with the position)
+    int lo0 = 0, hi0 = 0, lo1 = 0, hi1 = 0;
+    key_range(0 + N - M, N, p->causal, p->window, &lo0, &hi0);
+    key_range(M - 1 + N - M, N, p->causal, p->window, &lo1, &hi1);
+    p->klo = lo0;
+    p->khi = hi1 > lo0 ? hi1 : lo0;
+    return ATTN_OK;
+}
+
+bool empty_output(const Problem& p) { return (int64_t)p.B * p.Hq * p.M == 0; }
+
+int choose_path(const Problem& p, int path) {
+    if (path != ATTN_PATH_AUTO) return path;
+    if (decode_supported(p) && (int64_t)p.G * p.M <= 16 && (p.khi - p.klo) >= 512) return ATTN_PATH_DECODE;
+    if (prefill_supported(p)) return ATTN_PATH_PREFILL;
+    return ATTN_PATH_SIMT;
+}
+
+size_t workspace_for(const Problem& p, int path) {
+    if (path != ATTN_PATH_DECODE || !decode_supported(p)) return 0;
+    int chunk = 0, S = 0;
+    if (decode_plan(p, &chunk, &S) != ATTN_OK) return 0;
+    return split_workspace_bytes(p.B * p.Hq * p.M, S, p.D);
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+int run(const Problem& p, const void* q, const void* k, const void* v, void* o, int path, void* ws,
+        size_t ws_bytes, cudaStream_t stream) {
+    if (path == ATTN_PATH_PREFILL && p.D != 64 && p.D != 128) return ATTN_ERR_HEADDIM;
+    if (path == ATTN_PATH_DECODE && !decode_supported(p)) return ATTN_ERR_HEADDIM;
+    if (empty_output(p)) return ATTN_OK;
+    if (p.N == 0) {  // every row sees no key: output 0
+        const size_t bytes = (size_t)p.B * p.Hq * p.M * p.D * 2;
+        return cuda_status(cudaMemsetAsync(o, 0, bytes, stream));
+    }
+    int* status = status_ptr();
+    if (!status) return ATTN_ERR_CUDA;
+    switch (path) {
+        case ATTN_PATH_SIMT:
+            return cuda_status(launch_simt(p, q, k, v, o, 0, 1, nullptr, stream));
+        case ATTN_PATH_PREFILL:
+            if (!prefill_supported(p)) return ATTN_ERR_PATH;
+            return launch_prefill(p, q, k, v, o, status, stream);
+        case ATTN_PATH_DECODE: {
+            int chunk = 0, S = 0;
+            int rc = decode_plan(p, &chunk, &S);
+            if (rc != ATTN_OK) return rc;
+            const int rows = p.B * p.Hq * p.M;
+            if (!ws || ws_bytes < split_workspace_bytes(rows, S, p.D)) return ATTN_ERR_WORKSPACE;
+            if (!aligned16(ws)) return ATTN_ERR_ALIGN;
+            SplitWorkspace w = split_workspace(ws, rows, S, p.D);
+            cudaError_t e = launch_decode(p, q, k, v, chunk, S, w, status, stream);
+            if (e != cudaSuccess) return ATTN_ERR_CUDA;
+            return cuda_status(launch_merge(w.m, w.l, w.acc, o, nullptr, nullptr, rows, S, p.D, p.dtype, 1.0f,
+                                            true, stream));
+        }
+        default:
+            return ATTN_ERR_PATH;
+    }
+}
+
+}  // namespace
+
+size_t split_workspace_bytes(int rows, int S, int D) {
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    const size_t ml = up((size_t)rows * S * sizeof(float));
+    return 2 * ml + up((size_t)rows * S * D * sizeof(float));
+}
+
+SplitWorkspace split_workspace(void* base, int rows, int S, int D) {
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    const size_t ml = up((size_t)rows * S * sizeof(float));
+    (void)D;
+    char* c = static_cast<char*>(base);
+    return SplitWorkspace{reinterpret_cast<float*>(c), reinterpret_cast<float*>(c + ml),
+                          reinterpret_cast<float*>(c + 2 * ml)};
+}
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int M, int N, int D,
+                int causal, int window, float scale, int dtype, int path, void* workspace, size_t ws_bytes,
+                void* stream) {
+    if (path < ATTN_PATH_AUTO || path > ATTN_PATH_DECODE) return ATTN_ERR_PATH;
+    Problem p;
+    int rc = validate(q, k, v, o, B, Hq, Hkv, M, N, D, causal, window, scale, dtype, &p);
+    if (rc != ATTN_OK) return rc;
+    return run(p, q, k, v, o, choose_path(p, path), workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int M, int N, int D,
+             int causal, int window, float scale, int dtype, void* stream) {
+    Problem p;
+    int rc = validate(q, k, v, o, B, Hq, Hkv, M, N, D, causal, window, scale, dtype, &p);
+    if (rc != ATTN_OK) return rc;
+    const int path = choose_path(p, ATTN_PATH_AUTO);
+    const size_t bytes = empty_output(p) || p.N == 0 ? 0 : workspace_for(p, path);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (bytes == 0) return run(p, q, k, v, o, path, nullptr, 0, s);
+    void* ws = nullptr;
+    if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    rc = run(p, q, k, v, o, path, ws, bytes, s);
+    if (cudaFreeAsync(ws, s) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
+    return rc;
+}
+
+size_t attn_workspace_bytes(int B, int Hq, int Hkv, int M, int N, int D, int causal, int window, int path) {
+    Problem p;
+    // placeholder non-null pointers: only the shape is checked here
+    static const int16_t dummy[8] __attribute__((aligned(16))) = {};
+    if (validate(dummy, dummy, dummy, dummy, B, Hq, Hkv, M, N, D, causal, window, 0.f, ATTN_BF16, &p) != ATTN_OK)
+        return 0;
+    if (path < ATTN_PATH_AUTO || path > ATTN_PATH_DECODE) return 0;
+    if (empty_output(p) || p.N == 0) return 0;
+    return workspace_for(p, choose_path(p, path));
+}
+
+int attn_merge(const float* m, const float* l, const float* acc, void* o, float* m_out, float* l_out, int rows,
+               int S, int D, int out_dtype, void* stream) {
+    if (rows < 0 || S < 1 || S > 4096 || D < 1 || D > 256) return ATTN_ERR_SHAPE;
+    if (out_dtype != ATTN_BF16 && out_dtype != ATTN_FP16 && out_dtype != ATTN_FP32) return ATTN_ERR_DTYPE;
+    if ((int64_t)rows * S * D > kI32Max) return ATTN_ERR_OVERFLOW;
+    if (rows == 0) return ATTN_OK;
+    if (!m || !l || !acc || !o) return ATTN_ERR_NULL;
+    return cuda_status(launch_merge(m, l, acc, o, m_out, l_out, rows, S, D, out_dtype, kLog2e, false,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, void* q_d, void* k_d, void* v_d,
+                  void* o_d, int B, int Hq, int Hkv, int M, int N, int D, int causal, int window, float scale,
+                  int dtype, void* workspace, size_t ws_bytes, void* stream) {
+    Problem p;
+    int rc = validate(q_d, k_d, v_d, o_d, B, Hq, Hkv, M, N, D, causal, window, scale, dtype, &p);
+    if (rc != ATTN_OK) return rc;
+    const size_t qb = (size_t)B * Hq * M * D * 2, kb = (size_t)B * Hkv * N * D * 2;
+    if ((qb && (!q_h || !o_h)) || (kb && (!k_h || !v_h))) return ATTN_ERR_NULL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (qb && cudaMemcpyAsync(q_d, q_h, qb, cudaMemcpyHostToDevice, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (kb && cudaMemcpyAsync(k_d, k_h, kb, cudaMemcpyHostToDevice, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (kb && cudaMemcpyAsync(v_d, v_h, kb, cudaMemcpyHostToDevice, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    const int path = choose_path(p, ATTN_PATH_AUTO);
+    rc = run(p, q_d, k_d, v_d, o_d, path, workspace, ws_bytes, s);
+    if (rc != ATTN_OK) return rc;
+    if (qb && cudaMemcpyAsync(o_h, o_d, qb, cudaMemcpyDeviceToHost, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    return cuda_status(cudaStreamSynchronize(s));
+}
+
+const char* attn_strerror(int status) {
+    switch (status) {
+        case ATTN_OK: return "ok";
+        case ATTN_ERR_NULL: return "a required pointer is NULL";
+        case ATTN_ERR_SHAPE: return "invalid shape (negative size, or Hkv == 0 with Hq > 0)";
+        case ATTN_ERR_DTYPE: return "unsupported dtype";
+        case ATTN_ERR_HEADDIM: return "unsupported head dimension for this path";
+        case ATTN_ERR_GQA: return "Hq is not a multiple of Hkv";
+        case ATTN_ERR_OVERFLOW: return "element count exceeds signed 32-bit indexing";
+        case ATTN_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+        case ATTN_ERR_CUDA: return "CUDA call failed";
+        case ATTN_ERR_TIMEOUT: return "a kernel gave up on a bounded wait";
+        case ATTN_ERR_PATH: return "the requested path cannot run this problem";
+        default: return "unknown status";
+    }
+}
+
+int attn_last_device_status(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_status_word, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+    return word ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+int attn_version(void) { return 100; }
+
+}  // extern "C"

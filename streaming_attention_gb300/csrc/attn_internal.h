@@ -1,0 +1,63 @@
+// Internal declarations shared by the CUDA sources of the library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "attn.h"
+
+namespace attn {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// One forward problem, validated. Positions follow the bottom-right rule
+// p_i = i + N - M; klo/khi bound the keys that any row of the problem may see.
+struct Problem {
+    int B, Hq, Hkv, M, N, D;
+    int causal, window;
+    float scale;       // logit scale (resolved: never 0)
+    float scale_log2;  // scale * log2(e): logits are handled in base 2
+    int dtype;         // ATTN_BF16 / ATTN_FP16
+    int G;             // Hq / Hkv
+    int klo, khi;      // union of the visible key ranges over all rows
+};
+
+// Keys [lo, hi) visible to the query at position p (hi <= lo: none).
+__host__ __device__ inline void key_range(int p, int N, int causal, int window, int* lo, int* hi) {
+    int h = causal ? (p + 1 < N ? p + 1 : N) : N;
+    int l = (window > 0) ? (p - window + 1 > 0 ? p - window + 1 : 0) : 0;
+    if (h < 0) h = 0;
+    *lo = l;
+    *hi = h;
+}
+
+// Split-KV workspace: the union key range [klo, khi) is cut into S chunks of
+// `chunk` keys; partial summaries are [rows][S] floats m and l (m in base-2
+// logit units) and [rows][S][D] floats acc. Each part is 256-byte aligned.
+struct SplitWorkspace {
+    float* m;
+    float* l;
+    float* acc;
+};
+size_t split_workspace_bytes(int rows, int S, int D);
+SplitWorkspace split_workspace(void* base, int rows, int S, int D);
+
+// Launchers (all asynchronous on `stream`; return a CUDA error).
+cudaError_t launch_simt(const Problem& p, const void* q, const void* k, const void* v, void* o,
+                        int chunk, int S, const SplitWorkspace* ws, cudaStream_t stream);
+cudaError_t launch_merge(const float* m, const float* l, const float* acc, void* o, float* m_out,
+                         float* l_out, int rows, int S, int D, int out_dtype, float unit,
+                         bool programmatic, cudaStream_t stream);
+cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const void* v,
+                          int chunk, int S, const SplitWorkspace& ws, int* status,
+                          cudaStream_t stream);
+bool decode_supported(const Problem& p);
+int decode_plan(const Problem& p, int* chunk, int* S);
+
+// tcgen05 prefill: returns ATTN_OK, ATTN_ERR_PATH (cannot run this problem)
+// or ATTN_ERR_CUDA.
+int launch_prefill(const Problem& p, const void* q, const void* k, const void* v, void* o,
+                   int* status, cudaStream_t stream);
+bool prefill_supported(const Problem& p);
+
+}  // namespace attn

@@ -1,0 +1,107 @@
+"""The C-ABI library loads and exports every symbol declared in include/attn.h,
+and metadata validation answers with status codes. No compute call is made:
+everything here runs without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import streaming_attention_gb300 as sa
+from streaming_attention_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    B.build()
+    return sa.lib()
+
+
+def declared_symbols():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            names += re.findall(r"ATTN_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", text)
+    return names
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_symbols()
+    assert "attn_fwd" in names and len(names) >= 8, names
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in include/ but not exported"
+
+
+def test_version_and_strerror(L):
+    assert L.attn_version() >= 100
+    for st in range(0, -12, -1):
+        assert sa.strerror(st) and sa.strerror(st) != "unknown status", st
+    assert sa.strerror(-99) == "unknown status"
+
+
+A16 = ctypes.c_void_p(0x10000)   # 16-byte aligned placeholder (never dereferenced)
+A8 = ctypes.c_void_p(0x10008)
+
+
+def fwd(L, q=A16, k=A16, v=A16, o=A16, B_=1, Hq=2, Hkv=2, M=8, N=8, D=64, causal=0, window=0, dtype=0):
+    return L.attn_fwd(q, k, v, o, B_, Hq, Hkv, M, N, D, causal, window, 0.0, dtype, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dtype=7), -3),
+    (dict(B_=-1), -2),
+    (dict(M=-1), -2),
+    (dict(N=-5), -2),
+    (dict(D=0), -2),
+    (dict(Hkv=0), -2),
+    (dict(Hq=6, Hkv=4), -5),
+    (dict(D=48), -4),
+    (dict(D=256), -4),
+    (dict(B_=64, Hq=64, M=4096, D=128), -6),
+    (dict(q=None), -1),
+    (dict(o=None), -1),
+    (dict(k=None), -1),
+    (dict(q=A8), -7),
+    (dict(v=A8), -7),
+])
+def test_validation_status(L, kw, status):
+    assert fwd(L, **kw) == status
+
+
+def test_forced_path_checks(L):
+    # an out-of-range path value is rejected before any launch
+    st = L.attn_fwd_ex(A16, A16, A16, A16, 1, 2, 2, 8, 8, 64, 0, 0, 0.0, 0, 9, None, 0, None)
+    assert st == -11
+    # decode and prefill need D in {64, 128}
+    for path in (sa.PATH_DECODE, sa.PATH_PREFILL):
+        st = L.attn_fwd_ex(A16, A16, A16, A16, 1, 2, 2, 8, 8, 32, 0, 0, 0.0, 0, path, None, 0, None)
+        assert st == -4, path
+
+
+def test_workspace_bytes(L):
+    # prefill and SIMT need none; decode needs room for its split summaries
+    assert sa.attn_workspace_bytes(2, 32, 32, 4096, 4096, 128, True, 0, sa.PATH_SIMT) == 0
+    n = sa.attn_workspace_bytes(8, 32, 8, 1, 8192, 128, True, 4096, sa.PATH_DECODE)
+    rows = 8 * 32
+    assert n >= rows * 4 * (128 + 2)
+    assert sa.attn_workspace_bytes(8, 32, 8, 1, 8192, 128, True, 4096, sa.PATH_AUTO) == n
+    assert sa.attn_workspace_bytes(-1, 32, 8, 1, 8192, 128, True, 4096, 0) == 0
+
+
+def test_merge_validation(L):
+    assert L.attn_merge(A16, A16, A16, A16, None, None, 4, 0, 64, 2, None) == -2
+    assert L.attn_merge(A16, A16, A16, A16, None, None, 4, 2, 64, 5, None) == -3
+    assert L.attn_merge(None, A16, A16, A16, None, None, 4, 2, 64, 2, None) == -1
+    assert L.attn_merge(A16, A16, A16, A16, None, None, 0, 2, 64, 2, None) == 0
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    from streaming_attention_gb300 import binding
+
+    monkeypatch.setattr(binding, "_LIB_FILE", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(binding, "_lib", None)
+    with pytest.raises(FileNotFoundError):
+        binding.lib()

@@ -1,0 +1,194 @@
+"""CUDA path against the FP64 oracle, element by element on the same seeded inputs."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import streaming_attention_gb300 as sa
+from parity import check
+from streaming_attention_gb300.inputs import (DECODE_GQA, LONG_CAUSAL, PREFILL_D64, PREFILL_D128, TINY,
+                                              TINY_RAGGED, make_qkv, sample_rows, workload_inputs)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+ALL_PATHS = [sa.PATH_AUTO, sa.PATH_SIMT, sa.PATH_PREFILL, sa.PATH_DECODE]
+PATH_NAMES = {0: "auto", 1: "simt", 2: "prefill", 3: "decode"}
+
+
+def run(q, k, v, causal, window=0, path=sa.PATH_AUTO, scale=0.0):
+    o = sa.attention(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, window=window, path=path, scale=scale)
+    torch.cuda.synchronize()
+    return o
+
+
+@pytest.fixture(autouse=True)
+def no_device_timeouts():
+    yield
+    assert sa.last_device_status() == 0, "a kernel gave up on a bounded wait"
+
+
+@pytest.mark.parametrize("path", ALL_PATHS, ids=PATH_NAMES.get)
+@pytest.mark.parametrize("w", [TINY, TINY_RAGGED], ids=lambda w: w.name)
+@pytest.mark.parametrize("causal", [False, True])
+def test_tiny(w, causal, path):
+    q, k, v = workload_inputs(w)
+    want = oracle.attention(q, k, v, causal=causal)
+    check(run(q, k, v, causal, path=path), want, w.dtype, f"{w.name} causal={causal} path={path}")
+
+
+@pytest.mark.parametrize("path", ALL_PATHS, ids=PATH_NAMES.get)
+def test_empty_dims(path):
+    q, k, v = make_qkv(1, 2, 2, 0, 16, 64, torch.bfloat16, 0)
+    o = run(q, k, v, True, path=path)
+    assert o.shape == (1, 2, 0, 64)
+    q, k, v = make_qkv(1, 2, 2, 16, 0, 64, torch.bfloat16, 0)
+    o = run(q, k, v, False, path=path)
+    assert o.shape == (1, 2, 16, 64) and torch.all(o == 0)
+    q, k, v = make_qkv(0, 2, 2, 16, 16, 64, torch.bfloat16, 0)
+    assert run(q, k, v, False, path=path).shape == (0, 2, 16, 64)
+
+
+@pytest.mark.parametrize("path", [sa.PATH_SIMT, sa.PATH_PREFILL, sa.PATH_DECODE], ids=PATH_NAMES.get)
+def test_a3_worked_example_across_tiles(path):
+    """The answer key's A3 example (logits 0, 0, ln 2 over values 1, 3, 10 give
+    6; the missing-alpha bug gives 7) at D=64, with the ln 2 key in the second
+    128-key tile so that the running maximum rises in a later tile. Filler keys
+    score -80 and carry value 0."""
+    D, N = 64, 129
+    q = torch.zeros(1, 1, 1, D)
+    q[..., 0] = 1.0
+    k = torch.zeros(1, 1, N, D)
+    k[0, 0, :, 0] = -80.0
+    k[0, 0, 0, 0] = 0.0
+    k[0, 0, 1, 0] = 0.0
+    k[0, 0, 128, 0] = math.log(2.0)
+    v = torch.zeros(1, 1, N, D)
+    v[0, 0, 0, 0], v[0, 0, 1, 0], v[0, 0, 128, 0] = 1.0, 3.0, 10.0
+    q, k, v = (t.to(torch.bfloat16) for t in (q, k, v))
+    for causal in (False, True):
+        o = run(q, k, v, causal, path=path, scale=1.0)
+        x = float(o[0, 0, 0, 0])
+        assert abs(x - 6.0) <= 2e-2 and abs(x - 7.0) > 0.5, x
+        check(o, oracle.attention(q, k, v, causal=causal, scale=1.0), torch.bfloat16, "a3")
+
+
+@pytest.mark.parametrize("path", [sa.PATH_SIMT, sa.PATH_PREFILL], ids=PATH_NAMES.get)
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "fp16"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("shape", [(1, 2, 2, 300, 300), (2, 4, 2, 129, 385), (1, 2, 1, 385, 129),
+                                   (1, 1, 1, 1, 257), (1, 3, 3, 256, 256)], ids=str)
+@pytest.mark.parametrize("mask", [(False, 0), (True, 0), (True, 100), (False, 70)], ids=str)
+def test_mid_sizes_full_compare(shape, mask, D, dtype, path):
+    """Several tiles with ragged tails, M != N (both ways), GQA, all masks."""
+    B, Hq, Hkv, M, N = shape
+    causal, window = mask
+    q, k, v = make_qkv(B, Hq, Hkv, M, N, D, dtype, seed=M * 7 + N)
+    want = oracle.attention(q, k, v, causal=causal, window=window)
+    check(run(q, k, v, causal, window, path), want, dtype, f"{shape} {mask} D={D} path={path}")
+
+
+@pytest.mark.parametrize("D", [16, 32])
+@pytest.mark.parametrize("mask", [(False, 0), (True, 0), (True, 9)], ids=str)
+def test_small_head_dims_simt(D, mask):
+    q, k, v = make_qkv(2, 4, 2, 77, 45, D, torch.float16, seed=D)
+    want = oracle.attention(q, k, v, causal=mask[0], window=mask[1])
+    check(run(q, k, v, mask[0], mask[1], sa.PATH_AUTO), want, torch.float16, f"D={D}")
+
+
+@pytest.mark.parametrize("path", [sa.PATH_SIMT, sa.PATH_PREFILL], ids=PATH_NAMES.get)
+def test_fully_masked_rows_are_zero(path):
+    """Causal with M > N: the first M-N rows see no key and must be 0, not NaN."""
+    q, k, v = make_qkv(1, 2, 2, 200, 50, 64, torch.bfloat16, seed=5)
+    o = run(q, k, v, True, path=path)
+    assert torch.isfinite(o).all() and torch.all(o[:, :, :150] == 0)
+    check(o, oracle.attention(q, k, v, causal=True), torch.bfloat16, "M>N causal")
+
+
+@pytest.mark.parametrize("shape", [(2, 8, 2, 1, 1000), (1, 16, 4, 3, 2500), (3, 4, 4, 2, 700), (1, 32, 2, 1, 600)],
+                         ids=str)
+@pytest.mark.parametrize("mask", [(True, 0), (True, 333), (False, 0)], ids=str)
+def test_decode_split_paths(shape, mask):
+    B, Hq, Hkv, M, N = shape
+    q, k, v = make_qkv(B, Hq, Hkv, M, N, 128, torch.bfloat16, seed=N)
+    want = oracle.attention(q, k, v, causal=mask[0], window=mask[1])
+    for path in (sa.PATH_DECODE, sa.PATH_AUTO, sa.PATH_SIMT):
+        check(run(q, k, v, mask[0], mask[1], path), want, torch.bfloat16, f"{shape} {mask} path={path}")
+
+
+def sampled(w, causal, window, path, dtype=None, count=192):
+    dtype = dtype or w.dtype
+    q, k, v = workload_inputs(w, dtype)
+    o = run(q, k, v, causal, window, path)
+    rows = sample_rows(w.B, w.Hq, w.M, count, seed=w.seed)
+    want = oracle.attention_rows(q, k, v, rows, causal=causal, window=window)
+    got = o.reshape(-1, w.D)[torch.tensor(rows, device=o.device)]
+    assert torch.isfinite(o).all()
+    return check(got, want, dtype, f"{w.name} causal={causal} path={path}")
+
+
+@pytest.mark.parametrize("path", [sa.PATH_AUTO, sa.PATH_SIMT], ids=PATH_NAMES.get)
+@pytest.mark.parametrize("causal", [False, True])
+def test_prefill_d64_full_size(causal, path):
+    sampled(PREFILL_D64, causal, 0, path)
+
+
+@pytest.mark.parametrize("variant", ["bf16_causal", "bf16_noncausal", "fp16_causal"])
+def test_prefill_d128_full_size(variant):
+    dtype = torch.float16 if variant.startswith("fp16") else torch.bfloat16
+    sampled(PREFILL_D128, "noncausal" not in variant, 0, sa.PATH_AUTO, dtype)
+
+
+@pytest.mark.parametrize("path", [sa.PATH_AUTO, sa.PATH_DECODE, sa.PATH_SIMT], ids=PATH_NAMES.get)
+def test_decode_gqa_full_size(path):
+    w = DECODE_GQA
+    q, k, v = workload_inputs(w)
+    o = run(q, k, v, True, w.window, path)
+    want = oracle.attention(q, k, v, causal=True, window=w.window)  # 256 rows: the full output
+    check(o, want, w.dtype, f"decode path={path}")
+
+
+def test_long_causal_stress_full_size():
+    sampled(LONG_CAUSAL, True, 0, sa.PATH_AUTO, count=160)
+
+
+def test_merge_kernel_worked_example():
+    """The answer key's A1 worked answer through the GPU merge kernel."""
+    m = torch.tensor([[2.0, 4.0], [-math.inf, -math.inf], [-math.inf, 1.5]], device=DEV)
+    l = torch.tensor([[2.0, 1.0], [0.0, 0.0], [0.0, 2.5]], device=DEV)
+    acc = torch.tensor([[[3.0], [5.0]], [[0.0], [0.0]], [[0.0], [4.0]]], device=DEV)
+    o, mo, lo = sa.attn_merge(m, l, acc, torch.float32, with_stats=True)
+    torch.cuda.synchronize()
+    assert float(mo[0]) == 4.0 and abs(float(lo[0]) - (1 + 2 * math.exp(-2))) < 1e-6
+    assert abs(float(o[0, 0]) - (5 + 3 * math.exp(-2)) / (1 + 2 * math.exp(-2))) < 1e-6
+    assert float(mo[1]) == -math.inf and float(lo[1]) == 0.0 and float(o[1, 0]) == 0.0
+    assert float(mo[2]) == 1.5 and abs(float(lo[2]) - 2.5) < 1e-6 and abs(float(o[2, 0]) - 1.6) < 1e-6
+
+
+def test_merge_kernel_random_against_oracle():
+    g = torch.Generator().manual_seed(3)
+    rows, S, D = 37, 19, 128
+    m = torch.randn(rows, S, generator=g) * 4
+    m[::5, ::3] = -math.inf
+    l = torch.rand(rows, S, generator=g) * 3
+    l[m == -math.inf] = 0
+    acc = torch.randn(rows, S, D, generator=g)
+    acc[m == -math.inf] = 0
+    o = sa.attn_merge(m.to(DEV), l.to(DEV), acc.to(DEV), torch.float32).cpu().double().numpy()
+    for r in range(rows):
+        mm, ll, aa = oracle.merge(m[r].double().numpy(), l[r].double().numpy(), acc[r].double().numpy())
+        want = aa / ll if ll > 0 else np.zeros(D)
+        assert np.allclose(o[r], want, rtol=1e-5, atol=1e-5)
+
+
+def test_host_end_to_end_matches_device_call():
+    w = TINY_RAGGED
+    q, k, v = workload_inputs(w)
+    qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+    oh = torch.empty_like(qh).pin_memory()
+    qd, kd, vd = (t.to(DEV) for t in (q, k, v))
+    od = torch.empty_like(qd)
+    sa.attn_fwd_host(qh, kh, vh, oh, qd, kd, vd, od, causal=True)
+    ref = run(q, k, v, True)
+    assert torch.equal(oh, ref.cpu())
