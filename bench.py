@@ -1,0 +1,444 @@
+"""Benchmark of the streaming attention forward on one node.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+A step is one attention forward over the workload (one call of the library's
+C ABI; inputs resident in HBM). Device time comes from CUDA events on the
+launching stream around each step, with an L2 flush (a buffer twice the L2
+size is overwritten) between steps, outside the timed events. Under torchrun
+each rank runs the same per-rank workload (weak scaling, no collective on the
+data path); the step time is the maximum over ranks.
+
+``--impl reference`` times the FP64 CPU oracle (the only reference this
+project has) on a bounded sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from streaming_attention_gb300.inputs import DECODE_GQA, PREFILL_D128, WORKLOADS, workload_inputs  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s (decode: GB/s) and % of GB300 roofline, 1 GPU"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DEFAULT_WORKLOAD = PREFILL_D128.name
+
+
+# ----------------------------------------------------------------------------
+# Work accounting (algorithmic, allowed pairs only)
+# ----------------------------------------------------------------------------
+def visible_keys(i, M, N, causal, window):
+    p = i + N - M
+    hi = min(N, p + 1) if causal else N
+    lo = max(0, p - window + 1) if window > 0 else 0
+    return max(0, hi - lo)
+
+
+def allowed_pairs(M, N, causal, window):
+    if not causal and window <= 0:
+        return M * N
+    return sum(visible_keys(i, M, N, causal, window) for i in range(M))
+
+
+def flops(w, causal=None, window=None):
+    causal = w.causal if causal is None else causal
+    window = w.window if window is None else window
+    return 4.0 * w.D * w.B * w.Hq * allowed_pairs(w.M, w.N, causal, window)
+
+
+def decode_bytes(w):
+    """Q + O + the K and V rows that any query row may see, each read once."""
+    esz = 2
+    lo = max(0, (w.N - w.M) - w.window + 1) if w.window > 0 else 0
+    hi = w.N  # the last row sits at position N-1
+    kv = 2 * w.B * w.Hkv * (hi - lo) * w.D * esz
+    qo = 2 * w.B * w.Hq * w.M * w.D * esz
+    return float(kv + qo)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------
+# Distributed helpers (torchrun: one process per GPU)
+# ----------------------------------------------------------------------------
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def dist_init(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# Our arm
+# ----------------------------------------------------------------------------
+def time_calls(fn, steps, warmup, stream, flush):
+    """Per-step device time (ms) of fn() with an L2 flush between steps."""
+    for _ in range(warmup):
+        fn()
+        flush()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn()
+        e.record(stream)
+        flush()
+        times.append((s, e))
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in times]
+
+
+def path_launches(path_name):
+    return {"decode": 2}.get(path_name, 1)
+
+
+def chosen_path(w):
+    import streaming_attention_gb300 as sa
+
+    G = w.Hq // w.Hkv
+    lo = max(0, (w.N - w.M) - w.window + 1) if w.window > 0 else 0
+    if w.D in (64, 128) and G * w.M <= 16 and (w.N - lo) >= 512:
+        return sa.PATH_DECODE, "decode"
+    return sa.PATH_AUTO, "prefill_or_simt"
+
+
+def run_ours(args):
+    import streaming_attention_gb300 as sa
+    from streaming_attention_gb300 import build as sab
+
+    rank, local, world = dist_env()
+    torch.cuda.set_device(local)
+    dist_init(world, "nccl")
+    dev = torch.device("cuda", local)
+    sab.build()
+    w = WORKLOADS[args.workload]
+    stream = torch.cuda.current_stream(dev)
+
+    q, k, v = workload_inputs(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    od = torch.empty_like(qd)
+    path, path_name = chosen_path(w)
+    nbytes = sa.attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.M, w.N, w.D, w.causal, w.window, path)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    def step():
+        sa.attn_fwd_ex(qd, kd, vd, od, w.causal, w.window, 0.0, path, ws if nbytes else None, stream)
+
+    decode = path_name == "decode"
+    work = decode_bytes(w) if decode else flops(w)
+    unit = "GB/s" if decode else "TFLOP/s"
+    scale = 1e9 if decode else 1e12
+
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        times = time_calls(step, args.steps, args.warmup, stream, flush)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = clk.summary()
+    ms = statistics.mean(times)
+    ms_max = max_over_ranks(ms, world, dev)
+    value = world * work / (ms_max * 1e-3) / scale
+    status = sa.last_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+
+    # end to end: host (pinned) buffers through the C ABI, copies inside the timed region
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    oh = torch.empty_like(qh).pin_memory()
+    e2e_times = []
+    for i in range(args.warmup + args.steps):
+        flush()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        sa.attn_fwd_host(qh, kh, vh, oh, qd, kd, vd, od, w.causal, w.window, 0.0, ws if nbytes else None, stream)
+        t1 = time.perf_counter()
+        if i >= args.warmup:
+            e2e_times.append(t1 - t0)
+    e2e_s = max_over_ranks(statistics.mean(e2e_times), world, dev)
+    h2d = (q.numel() + k.numel() + v.numel()) * q.element_size()
+    d2h = od.numel() * od.element_size()
+
+    pk, pk_src = peaks()
+    if decode:
+        peak, bound, r_unit = pk["hbm_gbs"], "hbm", "GB/s"
+    else:
+        peak, bound, r_unit = pk["bf16_tflops"], "tensor", "TFLOP/s"
+        if w.dtype == torch.float16:
+            peak = pk["bf16_tflops"]  # fp16 and bf16 share the dense tensor rate
+    achieved = work / (ms * 1e-3) / scale
+    traffic = stored_traffic(w.name)
+
+    also = {}
+    if not args.no_extra and world == 1:
+        also = extra_measurements(args, dev, stream, flush)
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": unit,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == torch.bfloat16 else "fp16",
+        "data": "synthetic (seeded N(0,1), rounded to the input dtype)",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "M": w.M, "N": w.N, "D": w.D,
+                   "causal": w.causal, "window": w.window, "path": path_name,
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "flushed between steps (2x L2 buffer overwritten)",
+                   "timing": "CUDA events per step on the launching stream"},
+        "e2e": {"value": round(world * work / e2e_s / scale, 3), "unit": unit, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": path_launches(path_name) * args.steps,
+        "roofline": {"bound": bound, "achieved": round(achieved, 3), "peak": peak, "unit": r_unit,
+                     "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": pk_src},
+        "clocks": clocks,
+    }
+    if also:
+        line["also"] = also
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def stored_traffic(workload_name):
+    """DRAM bytes per launch from a committed ncu capture, if it matches the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    ent = d.get(workload_name)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, ent["source"])
+    import hashlib
+
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != ent["source_sha"]:
+        return None
+    return ent["bytes_per_launch"]
+
+
+def extra_measurements(args, dev, stream, flush):
+    """Secondary figures on the same box: noncausal D=128 prefill and GQA decode."""
+    import streaming_attention_gb300 as sa
+
+    out = {}
+    steps = max(3, min(args.steps, 10))
+    for name, w, causal in (("prefill_d128_bf16_noncausal", PREFILL_D128, False),
+                            ("decode_gqa", DECODE_GQA, DECODE_GQA.causal)):
+        if name.startswith("prefill") and args.workload != PREFILL_D128.name:
+            continue
+        q, k, v = workload_inputs(w)
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+        od = torch.empty_like(qd)
+        path, pname = chosen_path(w)
+        nb = sa.attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.M, w.N, w.D, causal, w.window, path)
+        ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
+        fn = lambda: sa.attn_fwd_ex(qd, kd, vd, od, causal, w.window, 0.0, path, ws if nb else None, stream)  # noqa
+        ms = statistics.median(time_calls(fn, steps, 3, stream, flush))
+        if pname == "decode":
+            out[name] = {"GB/s": round(decode_bytes(w) / (ms * 1e-3) / 1e9, 1), "us": round(ms * 1e3, 2),
+                         "path": pname}
+        else:
+            out[name] = {"TFLOP/s": round(flops(w, causal) / (ms * 1e-3) / 1e12, 2), "us": round(ms * 1e3, 1),
+                         "path": pname}
+        del qd, kd, vd, od, ws
+    return out
+
+
+# ----------------------------------------------------------------------------
+# CPU baseline / reference arm: the FP64 oracle on a bounded sample
+# ----------------------------------------------------------------------------
+def oracle_sample(w, seconds, seed=0):
+    """Times the oracle on random rows of the workload until about `seconds`
+    of CPU work; returns (flops done, wall seconds, rows, threads)."""
+    import numpy as np
+
+    import oracle
+
+    q, k, v = workload_inputs(w)
+    q64, k64, v64 = (t.to(torch.float64).numpy() for t in (q, k, v))
+    rng = np.random.default_rng(seed)
+    total_rows = w.B * w.Hq * w.M
+    threads = oracle.cpu_threads()
+    done_flops, wall, nrows = 0.0, 0.0, 0
+    batch = max(threads * 4, 64)
+    while wall < seconds:
+        rows = rng.integers(0, total_rows, batch)
+        t0 = time.perf_counter()
+        oracle.attention_rows(q64, k64, v64, rows, causal=w.causal, window=w.window, nthreads=threads)
+        dt = time.perf_counter() - t0
+        wall += dt
+        nrows += len(rows)
+        done_flops += sum(4.0 * w.D * visible_keys(int(r) % w.M, w.M, w.N, w.causal, w.window) for r in rows)
+        if dt < seconds / 8:
+            batch *= 2
+    return done_flops, wall, nrows, threads
+
+
+def cpu_baseline(w, seconds):
+    fl, wall, nrows, threads = oracle_sample(w, seconds)
+    return {"value": round(fl / wall / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{nrows} random query rows of {w.name} ({fl / 1e9:.1f} GFLOP FP64, {wall:.1f} s)"}
+
+
+def run_reference(args):
+    rank, local, world = dist_env()
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
+    for _ in range(args.warmup):
+        oracle_sample(w, min(1.0, per_step), seed=1)
+    fl_tot, wall_tot, rows_tot, threads = 0.0, 0.0, 0, 1
+    for s in range(args.steps):
+        fl, wall, nrows, threads = oracle_sample(w, per_step, seed=100 + s)
+        fl_tot += fl
+        wall_tot += wall
+        rows_tot += nrows
+    value = fl_tot / wall_tot / 1e12
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(wall_tot / args.steps * 1e3, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1), rounded to the input dtype, widened to FP64)",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "M": w.M, "N": w.N, "D": w.D,
+                   "causal": w.causal, "window": w.window},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows_tot} random query rows over {args.steps} steps"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
