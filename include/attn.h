@@ -143,6 +143,32 @@ ATTN_API int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, vo
                            int causal, int window, float scale, int dtype,
                            void* workspace, size_t ws_bytes, void* stream);
 
+/* Split-KV decode forward that allocates no memory.
+ * The source pages have no counterpart to this entry point: it exists for
+ * callers that cannot allocate device memory when they run the forward --
+ * for example code inside an allocator hook or custom memory pool (which must
+ * not re-enter cudaMalloc), or a latency-critical loop whose rules forbid
+ * allocation. attn_fwd would allocate the split workspace with
+ * cudaMallocAsync, and attn_fwd_ex needs the caller to provide it.
+ * Instead, this call keeps the split summaries in one fixed device array of
+ * ATTN_NOALLOC_SCRATCH_BYTES bytes that the library holds on every GPU that
+ * loads it, until the process exits. It calls no cudaMalloc, cudaFree or
+ * other allocating routine.
+ *   Arguments, layout and errors are those of attn_fwd; the caller still
+ *   provides q, k, v and o. D must be 64 or 128.
+ *   Returns ATTN_ERR_WORKSPACE when the problem's split summaries
+ *   (attn_workspace_bytes(..., ATTN_PATH_DECODE)) exceed the array.
+ *   The first call on a device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   Every call, on any stream, shares the one array and leaves its contents
+ *   behind: calls whose work may overlap on the GPU race and must be
+ *   serialized by the caller (one stream, or events). Nothing in the array
+ *   needs clearing: each call writes every summary it reads. */
+#define ATTN_NOALLOC_SCRATCH_BYTES (8u << 20)
+ATTN_API int attn_fwd_decode_noalloc(const void* q, const void* k, const void* v, void* o,
+                                     int B, int Hq, int Hkv, int M, int N, int D,
+                                     int causal, int window, float scale, int dtype, void* stream);
+
 /* Human-readable text for a status code (static storage). */
 ATTN_API const char* attn_strerror(int status);
 

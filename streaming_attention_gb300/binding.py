@@ -60,6 +60,8 @@ def lib() -> ctypes.CDLL:
             L.attn_strerror.restype = ctypes.c_char_p
             L.attn_last_device_status.argtypes = [vp]
             L.attn_last_device_status.restype = ci
+            L.attn_fwd_decode_noalloc.argtypes = [vp, vp, vp, vp] + [ci] * 8 + [cf, ci, vp]
+            L.attn_fwd_decode_noalloc.restype = ci
             L.attn_version.argtypes = []
             L.attn_version.restype = ci
             _lib = L
@@ -167,6 +169,15 @@ def attn_fwd_host(q_h, k_h, v_h, o_h, q_d, k_d, v_d, o_d, causal=False, window=0
                              _ptr(o_d), B, Hq, Hkv, M, N, D, int(bool(causal)), int(window), float(scale or 0.0),
                              _DTYPES[q_d.dtype], _ptr(workspace), ws_bytes, _stream(stream))
     _check(st, "attn_fwd_host")
+
+
+def attn_fwd_decode_noalloc(q, k, v, o, causal=False, window=0, scale=0.0, stream=None) -> None:
+    """C-ABI ``attn_fwd_decode_noalloc``: the split-KV decode path using the
+    library's fixed scratch array, for callers that cannot allocate."""
+    B, Hq, Hkv, M, N, D = _dims(q, k, v, o)
+    st = lib().attn_fwd_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, Hq, Hkv, M, N, D, int(bool(causal)),
+                                       int(window), float(scale or 0.0), _DTYPES[q.dtype], _stream(stream))
+    _check(st, "attn_fwd_decode_noalloc")
 
 
 def last_device_status(stream=None) -> int:

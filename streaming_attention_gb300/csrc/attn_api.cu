@@ -124,6 +124,13 @@ int run(const Problem& p, const void* q, const void* k, const void* v, void* o, 
 
 }  // namespace
 
+int validate_problem(const void* q, const void* k, const void* v, const void* o, int B, int Hq, int Hkv, int M,
+                     int N, int D, int causal, int window, float scale, int dtype, Problem* p) {
+    return validate(q, k, v, o, B, Hq, Hkv, M, N, D, causal, window, scale, dtype, p);
+}
+
+int* device_status_ptr() { return status_ptr(); }
+
 size_t split_workspace_bytes(int rows, int S, int D) {
     auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
     const size_t ml = up((size_t)rows * S * sizeof(float));

@@ -54,6 +54,11 @@ cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const 
 bool decode_supported(const Problem& p);
 int decode_plan(const Problem& p, int* chunk, int* S);
 
+// Metadata validation and the device status word, shared by every entry point.
+int validate_problem(const void* q, const void* k, const void* v, const void* o, int B, int Hq, int Hkv, int M,
+                     int N, int D, int causal, int window, float scale, int dtype, Problem* p);
+int* device_status_ptr();
+
 // tcgen05 prefill: returns ATTN_OK, ATTN_ERR_PATH (cannot run this problem)
 // or ATTN_ERR_CUDA.
 int launch_prefill(const Problem& p, const void* q, const void* k, const void* v, void* o,
