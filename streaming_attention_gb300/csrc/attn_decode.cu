@@ -1,7 +1,11 @@
-// Split-KV decode: the union key range is cut into S chunks; each chunk's
-// partial (m, l, acc) summaries go to the workspace, and the merge kernel
-// combines them on the same stream (answer key, central-idea table, A2 row:
+// Split-KV decode dispatch: the union key range [klo, khi) is cut into S
+// chunks of whole 128-key tiles; each chunk's partial (m, l, acc) summaries
+// go to the workspace, and the merge kernel combines them on the same stream
+// ("Compare reasoning after your own attempt", central-idea table, A2 row:
 // partial stats, rescaled merge, same-stream order).
+//
+// D = 128 with at most 16 grouped query rows per KV head runs the tcgen05
+// split kernel; other shapes run the SIMT kernel in split mode.
 #include "attn_internal.h"
 
 namespace attn {
@@ -9,12 +13,14 @@ namespace attn {
 bool decode_supported(const Problem& p) { return p.D == 64 || p.D == 128; }
 
 int decode_plan(const Problem& p, int* chunk, int* S) {
-    const int range = p.khi - p.klo;
+    if (decode_tc_supported(p)) return decode_plan_tc(p, chunk, S);
+    const int kbase = split_base(p);
+    const int range = p.khi > kbase ? p.khi - kbase : 1;
     int c = 256;
-    int s = range > 0 ? (range + c - 1) / c : 1;
+    int s = (range + c - 1) / c;
     if (s > 4096) {
-        s = 4096;
-        c = (range + s - 1) / s;
+        c = ((range + 4095) / 4096 + 127) / 128 * 128;
+        s = (range + c - 1) / c;
     }
     *chunk = c;
     *S = s;
@@ -23,7 +29,7 @@ int decode_plan(const Problem& p, int* chunk, int* S) {
 
 cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const void* v, int chunk, int S,
                           const SplitWorkspace& ws, int* status, cudaStream_t stream) {
-    (void)status;
+    if (decode_tc_supported(p)) return launch_decode_tc(p, q, k, v, chunk, S, ws, status, stream);
     return launch_simt(p, q, k, v, nullptr, chunk, S, &ws, stream);
 }
 

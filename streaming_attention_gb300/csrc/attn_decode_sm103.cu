@@ -1,0 +1,492 @@
+// Split-KV decode on the tcgen05 tensor cores (sm_103a), D = 128.
+//
+// Decode has few query rows per KV head: the R = (Hq/Hkv) * M rows that share
+// one KV head (GQA grouping) are processed together, padded to 16. The score
+// tile is computed transposed, S^T[128 keys x 16 rows] = K_tile Q^T, so the
+// 128 keys fill the MMA's M dimension instead of 112 padded query rows; then
+// O^T[128 dims x 16 rows] += V_tile^T P^T. One thread owns one key for the
+// softmax (TMEM lane = key) and one head dimension for the accumulator (TMEM
+// lane = d). The row maximum of a tile is reduced across the 128 threads with
+// warp shuffles and a shared-memory exchange; row sums stay per-thread until
+// the end.
+//
+// Each CTA streams one split (a run of 128-key tiles) of one KV head through a
+// 3-slot TMA ring, K and V tiles in the order the MMAs consume them, and
+// writes the split's unnormalized summary (m, l, acc) for its rows; the merge
+// kernel combines splits with the common-maximum rule ("Compare reasoning
+// after your own attempt", central-idea table, A1 and A2 rows). Masks, ghost
+// rows, lazy rescale and bounded waits follow the prefill kernel.
+#include <mutex>
+
+#include "attn_internal.h"
+#include "sm100_ptx.cuh"
+#include "tma_map.h"
+
+namespace attn {
+namespace {
+
+using namespace ptx;
+
+constexpr int DBN = 128;  // keys per tile (MMA M of the score product)
+constexpr int DNR = 16;   // grouped rows, padded (MMA N)
+constexpr int DD = 128;   // head dimension (MMA M of the value product)
+constexpr int kSlots = 3;
+constexpr int kDecThreads = 192;  // warps 0-3 softmax, 4 TMA, 5 MMA
+constexpr int kDecLoadWarp = 4, kDecMmaWarp = 5;
+constexpr uint64_t kDecTimeoutNs = 1000000000ull;
+constexpr float kDecRescale = 8.0f;
+
+constexpr int kTileBytes = DBN * DD * 2;    // 32 KB (K or V tile)
+constexpr int kChunkBytes = DBN * 128;      // 64 columns of a 128-row tile
+constexpr int kQBytes = DNR * DD * 2;       // 4 KB
+constexpr int kQChunk = DNR * 128;          // 2 KB
+constexpr int kOffQ = 0;
+constexpr int kOffP = kOffQ + kQBytes;            // two P^T buffers, 4 KB each
+constexpr int kOffRing = 12288;                   // 1024-aligned
+constexpr int kOffBar = kOffRing + kSlots * kTileBytes;
+constexpr int kNumBars = 1 + 2 * kSlots + 2 + 2 + 2 + 1 + 2 + 1;
+constexpr int kOffRed = kOffBar + 8 * kNumBars;   // float [2][4][16] tile maxima
+constexpr int kOffLRed = kOffRed + 2 * 4 * DNR * 4;  // float [4][16] row sums
+constexpr int kOffMisc = kOffLRed + 4 * DNR * 4;
+constexpr int kDecSmem = kOffMisc + 16 + 1024;
+
+// TMEM columns: S^T buffers at 0 and 16, O^T at 32
+constexpr uint32_t kTmemCols = 64;
+__host__ __device__ constexpr uint32_t dcol_s(int b) { return b ? 16u : 0u; }
+constexpr uint32_t kColOT = 32;
+
+struct DecodeParams {
+    float* ws_m;
+    float* ws_l;
+    float* ws_acc;
+    int* status;
+    int Hq, Hkv, M, N, G, R;
+    int causal, window;
+    float scale_log2;
+    int klo, khi, kbase, chunk, S;
+};
+
+__device__ bool dwait_one(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag, int* status,
+                          bool abortable = true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (abortable && *abort_flag) return false;
+        if (globaltimer_ns() - t0 > kDecTimeoutNs) {
+            *abort_flag = 1u;
+            atomicExch(status, 1);
+            return false;
+        }
+    }
+}
+
+__device__ bool dwait_warp(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag, int* status) {
+    const int lane = threadIdx.x & 31;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        const bool done = mbar_try_wait(bar, parity);
+        if (__all_sync(0xffffffffu, done)) return true;
+        int stop = 0;
+        if (lane == 0) {
+            if (*abort_flag) {
+                stop = 1;
+            } else if (globaltimer_ns() - t0 > kDecTimeoutNs) {
+                *abort_flag = 1u;
+                atomicExch(status, 1);
+                stop = 1;
+            }
+        }
+        if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+    }
+}
+
+// Sequence position u of the ring -> (is V, tile index): K_0, K_1, V_0, K_2, V_1, ..., K_{T-1}, V_{T-2}, V_{T-1}
+__device__ __forceinline__ void ring_item(int u, int T, bool* is_v, int* tile) {
+    if (u == 2 * T - 1) {
+        *is_v = true;
+        *tile = T - 1;
+    } else if (u == 0) {
+        *is_v = false;
+        *tile = 0;
+    } else if (u & 1) {
+        *is_v = false;
+        *tile = (u + 1) / 2;
+    } else {
+        *is_v = true;
+        *tile = (u - 2) / 2;
+    }
+}
+__device__ __forceinline__ int ring_pos_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
+__device__ __forceinline__ int ring_pos_v(int j, int T) { return j == T - 1 ? 2 * T - 1 : 2 * j + 2; }
+
+template <bool kBF16>
+__global__ void __launch_bounds__(kDecThreads)
+    attn_decode_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sQ = sbase + kOffQ, sP = sbase + kOffP, sRing = sbase + kOffRing;
+    const uint32_t bar_q = sbase + kOffBar;
+    const uint32_t bar_full0 = bar_q + 8, bar_empty0 = bar_full0 + 8 * kSlots;
+    // one P-ready barrier per P^T buffer: the MMA issues S_{j+1} before PV_j, so the
+    // softmax may finish tile j+1 before the MMA observes tile j; per-buffer phases
+    // cannot run two ahead (S_{j+2} is issued only after PV_j)
+    const uint32_t bar_s0 = bar_empty0 + 8 * kSlots, bar_p0 = bar_s0 + 16, bar_free0 = bar_p0 + 16;
+    const uint32_t bar_o = bar_free0 + 16;
+    const uint32_t bar_red0 = bar_o + 8, bar_lred = bar_red0 + 16;  // shared-memory exchanges of the softmax
+    float* red = reinterpret_cast<float*>(smem + kOffRed);
+    float* lred = reinterpret_cast<float*>(smem + kOffLRed);
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int split = blockIdx.x;
+    const int grp = blockIdx.y;  // b * Hkv + g
+    const int b = grp / p.Hkv, g = grp % p.Hkv;
+    const int row_base = (b * p.Hq + g * p.G) * p.M;  // first global row of the group
+    const int k0 = p.kbase + split * p.chunk;         // tile-aligned start of this split
+    const int kend = min(k0 + p.chunk, p.khi);
+    const int T = kend > max(k0, p.klo) ? (kend - k0 + DBN - 1) / DBN : 0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar_q, 1);
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(bar_full0 + 8 * s, 1);
+            mbar_init(bar_empty0 + 8 * s, 1);
+        }
+        mbar_init(bar_s0, 1);
+        mbar_init(bar_s0 + 8, 1);
+        mbar_init(bar_p0, 128);
+        mbar_init(bar_p0 + 8, 128);
+        mbar_init(bar_free0, 1);
+        mbar_init(bar_free0 + 8, 1);
+        mbar_init(bar_o, 1);
+        mbar_init(bar_red0, 128);
+        mbar_init(bar_red0 + 8, 128);
+        mbar_init(bar_lred, 128);
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    // P^T buffers start at zero (rows >= R are never written afterwards)
+    for (int x = threadIdx.x; x < 2 * kQBytes / 16; x += blockDim.x)
+        reinterpret_cast<uint4*>(smem + kOffP)[x] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    if (warp == kDecMmaWarp) {
+        tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kDecLoadWarp) {
+        if (lane == 0 && T > 0) {
+            prefetch_tmap(&tmQ);
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+            mbar_arrive_expect_tx(bar_q, kQBytes);
+            for (int c = 0; c < 2; ++c) tma_load_3d(sQ + c * kQChunk, &tmQ, c * 64, row_base, 0, bar_q);
+            int issued = 0;
+            for (int u = 0; u < 2 * T; ++u) {
+                const int s = u % kSlots;
+                if (u >= kSlots && !dwait_one(bar_empty0 + 8 * s, ((u / kSlots) - 1) & 1, abort_flag, p.status))
+                    break;
+                bool is_v;
+                int tile;
+                ring_item(u, T, &is_v, &tile);
+                mbar_arrive_expect_tx(bar_full0 + 8 * s, kTileBytes);
+                const CUtensorMap* tm = is_v ? &tmV : &tmK;
+                for (int c = 0; c < 2; ++c)
+                    tma_load_3d(sRing + s * kTileBytes + c * kChunkBytes, tm, c * 64, k0 + tile * DBN, grp,
+                                bar_full0 + 8 * s);
+                issued = u + 1;
+            }
+            dwait_one(bar_q, 0, abort_flag, p.status, false);
+            for (int u = max(0, issued - kSlots); u < issued; ++u)
+                dwait_one(bar_full0 + 8 * (u % kSlots), (u / kSlots) & 1, abort_flag, p.status, false);
+        }
+    } else if (warp == kDecMmaWarp) {
+        if (lane == 0 && T > 0) {
+            constexpr uint32_t idS = idesc_f16(kBF16, DBN, DNR, false, false);
+            constexpr uint32_t idPV = idesc_f16(kBF16, DD, DNR, false, true);
+            auto issue_s = [&](int j) {
+                const int u = ring_pos_k(j), s = u % kSlots;
+                if (!dwait_one(bar_full0 + 8 * s, (u / kSlots) & 1, abort_flag, p.status)) return false;
+                tc_fence_after();
+                for (int kk = 0; kk < DD / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                    const uint64_t a = sw128_desc(sRing + s * kTileBytes + off, 16, 1024);
+                    const uint64_t bq = sw128_desc(sQ + (kk >> 2) * kQChunk + (kk & 3) * 32, 16, 1024);
+                    mma_ss(tmem + dcol_s(j & 1), a, bq, idS, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(bar_s0 + 8 * (j & 1));
+                mma_commit(bar_empty0 + 8 * s);
+                return true;
+            };
+            auto issue_pv = [&](int j) {
+                const int u = ring_pos_v(j, T), s = u % kSlots;
+                if (!dwait_one(bar_full0 + 8 * s, (u / kSlots) & 1, abort_flag, p.status)) return false;
+                if (!dwait_one(bar_p0 + 8 * (j & 1), (j >> 1) & 1, abort_flag, p.status)) return false;
+                tc_fence_after();
+                for (int kk = 0; kk < DBN / 16; ++kk) {
+                    const uint64_t a = sw128_desc(sRing + s * kTileBytes + kk * 16 * 128, kChunkBytes, 1024);
+                    const uint64_t bp = sw128_desc(sP + (j & 1) * kQBytes + (kk >> 2) * kQChunk + (kk & 3) * 32, 16,
+                                                   1024);
+                    mma_ss(tmem + kColOT, a, bp, idPV, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(bar_free0 + 8 * (j & 1));
+                mma_commit(bar_empty0 + 8 * s);
+                return true;
+            };
+            bool ok = dwait_one(bar_q, 0, abort_flag, p.status);
+            for (int j = 0; ok && j < T; ++j) {
+                ok = issue_s(j);
+                if (ok && j > 0) ok = issue_pv(j - 1);
+            }
+            if (ok) issue_pv(T - 1);
+            mma_commit(bar_o);
+            dwait_one(bar_o, 0, abort_flag, p.status, false);
+        }
+        __syncwarp();
+    } else {
+        // softmax: thread = key within the tile (and = head dimension for O^T)
+        const int kl = threadIdx.x;  // 0..127
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const float c = p.scale_log2;
+        int lo[DNR], hi[DNR];
+#pragma unroll
+        for (int r = 0; r < DNR; ++r) {
+            const int i = r % p.M;
+            key_range(i + p.N - p.M, p.N, p.causal, p.window, &lo[r], &hi[r]);
+            if (r >= p.R) hi[r] = lo[r];  // padding rows see nothing
+        }
+        float m_ref[DNR], l_part[DNR];
+#pragma unroll
+        for (int r = 0; r < DNR; ++r) {
+            m_ref[r] = -INFINITY;
+            l_part[r] = 0.f;
+        }
+        bool ok = true;
+        for (int j = 0; j < T; ++j) {
+            const int key = k0 + j * DBN + kl;
+            if (!(ok = dwait_warp(bar_s0 + 8 * (j & 1), (j >> 1) & 1, abort_flag, p.status))) break;
+            tc_fence_after();
+            uint32_t sr[16];
+            tmem_ld_x16(tmem + lane_base + dcol_s(j & 1), sr);
+            asm volatile("tcgen05.wait::ld.sync.aligned;"
+                         : "+r"(sr[0]), "+r"(sr[1]), "+r"(sr[2]), "+r"(sr[3]), "+r"(sr[4]), "+r"(sr[5]), "+r"(sr[6]),
+                           "+r"(sr[7]), "+r"(sr[8]), "+r"(sr[9]), "+r"(sr[10]), "+r"(sr[11]), "+r"(sr[12]),
+                           "+r"(sr[13]), "+r"(sr[14]), "+r"(sr[15])::"memory");
+            float t[DNR];
+#pragma unroll
+            for (int r = 0; r < DNR; ++r)
+                t[r] = (key >= lo[r] && key < hi[r]) ? __uint_as_float(sr[r]) * c : -INFINITY;
+            // tile row maxima across the 128 keys
+            float* redj = red + (j & 1) * 4 * DNR;
+#pragma unroll
+            for (int r = 0; r < DNR; ++r) {
+                if (r < p.R) {
+                    float x = t[r];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+                    if (lane == 0) redj[warp * DNR + r] = x;
+                }
+            }
+            mbar_arrive(bar_red0 + 8 * (j & 1));
+            if (!(ok = dwait_warp(bar_red0 + 8 * (j & 1), (j >> 1) & 1, abort_flag, p.status))) break;
+            bool need_any = false;
+            float alpha[DNR];
+#pragma unroll
+            for (int r = 0; r < DNR; ++r) {
+                alpha[r] = 1.f;
+                if (r < p.R) {
+                    const float mt = fmaxf(fmaxf(redj[r], redj[DNR + r]), fmaxf(redj[2 * DNR + r], redj[3 * DNR + r]));
+                    const float m_new = fmaxf(m_ref[r], mt);
+                    if (m_new > m_ref[r] + kDecRescale) {
+                        alpha[r] = ex2(m_ref[r] - m_new);
+                        l_part[r] *= alpha[r];
+                        m_ref[r] = m_new;
+                        need_any = true;
+                    }
+                }
+            }
+            // P^T buffer j&1 was last read by the value product of tile j-2
+            if (j >= 2 && !(ok = dwait_warp(bar_free0 + 8 * (j & 1), ((j - 2) >> 1) & 1, abort_flag, p.status)))
+                break;
+            uint8_t* pbuf = smem + kOffP + (j & 1) * kQBytes;
+            const int kc = kl >> 6, k64 = kl & 63;
+#pragma unroll
+            for (int r = 0; r < DNR; ++r) {
+                if (r < p.R) {
+                    const float m_use = (m_ref[r] == -INFINITY) ? 0.f : m_ref[r];
+                    const float pr = ex2(t[r] - m_use);
+                    l_part[r] += pr;
+                    const uint32_t pk = kBF16 ? pack_bf16(pr, 0.f) : pack_f16(pr, 0.f);
+                    const int off = kc * kQChunk + r * 128 + ((((k64 >> 3) ^ (r & 7))) << 4) + (k64 & 7) * 2;
+                    *reinterpret_cast<uint16_t*>(pbuf + off) = (uint16_t)(pk & 0xFFFFu);
+                }
+            }
+            // lazy rescale of O^T (needs the value product of tile j-1 complete)
+            if (need_any && j > 0) {
+                if (!(ok = dwait_warp(bar_free0 + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag, p.status)))
+                    break;
+                tc_fence_after();
+                uint32_t o[16];
+                tmem_ld_x16(tmem + lane_base + kColOT, o);
+                asm volatile("tcgen05.wait::ld.sync.aligned;"
+                             : "+r"(o[0]), "+r"(o[1]), "+r"(o[2]), "+r"(o[3]), "+r"(o[4]), "+r"(o[5]), "+r"(o[6]),
+                               "+r"(o[7]), "+r"(o[8]), "+r"(o[9]), "+r"(o[10]), "+r"(o[11]), "+r"(o[12]),
+                               "+r"(o[13]), "+r"(o[14]), "+r"(o[15])::"memory");
+#pragma unroll
+                for (int r = 0; r < DNR; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[r]);
+                tmem_st_x16(tmem + lane_base + kColOT, o);
+                tmem_wait_st();
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar_p0 + 8 * (j & 1));
+        }
+
+        // summary of this split: m (base 2), l, acc for the group's rows
+        int stop = 0;
+        if (lane == 0) stop = *abort_flag ? 1 : 0;
+        stop = __shfl_sync(0xffffffffu, stop, 0);
+        bool have = ok && !stop && T > 0 && dwait_warp(bar_o, 0, abort_flag, p.status);
+        if (have) {
+            tc_fence_after();
+#pragma unroll
+            for (int r = 0; r < DNR; ++r) {
+                if (r < p.R) {
+                    float x = l_part[r];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+                    if (lane == 0) lred[warp * DNR + r] = x;
+                }
+            }
+            mbar_arrive(bar_lred);
+            have = dwait_warp(bar_lred, 0, abort_flag, p.status);
+        }
+        if (have) {
+            uint32_t o[16];
+            tmem_ld_x16(tmem + lane_base + kColOT, o);
+            asm volatile("tcgen05.wait::ld.sync.aligned;"
+                         : "+r"(o[0]), "+r"(o[1]), "+r"(o[2]), "+r"(o[3]), "+r"(o[4]), "+r"(o[5]), "+r"(o[6]),
+                           "+r"(o[7]), "+r"(o[8]), "+r"(o[9]), "+r"(o[10]), "+r"(o[11]), "+r"(o[12]), "+r"(o[13]),
+                           "+r"(o[14]), "+r"(o[15])::"memory");
+#pragma unroll
+            for (int r = 0; r < DNR; ++r) {
+                if (r < p.R) {
+                    const size_t slot = (size_t)(row_base + r) * p.S + split;
+                    p.ws_acc[slot * DD + kl] = __uint_as_float(o[r]);
+                    if (kl == 0) {
+                        p.ws_m[slot] = m_ref[r];
+                        p.ws_l[slot] = lred[r] + lred[DNR + r] + lred[2 * DNR + r] + lred[3 * DNR + r];
+                    }
+                }
+            }
+        } else if (T == 0) {
+            // no key of this split: the empty summary
+            for (int r = 0; r < p.R; ++r) {
+                const size_t slot = (size_t)(row_base + r) * p.S + split;
+                p.ws_acc[slot * DD + kl] = 0.f;
+                if (kl == 0) {
+                    p.ws_m[slot] = -INFINITY;
+                    p.ws_l[slot] = 0.f;
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kDecMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+    // the merge kernel may start its prologue
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+int sm_count() {
+    static int n = 0;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+                                                      cudaSuccess)
+            n = 148;
+    });
+    return n;
+}
+
+template <bool kBF16>
+cudaError_t launch_decode_t(const Problem& pr, const void* q, const void* k, const void* v, int chunk, int S,
+                            const SplitWorkspace& ws, int* status, cudaStream_t stream) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(attn_decode_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        kDecSmem);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    CUtensorMap tq, tk, tv;
+    if (!make_tensor_map(&tq, q, DD, pr.B * pr.Hq * pr.M, 1, DNR, kBF16) ||
+        !make_tensor_map(&tk, k, DD, pr.N, pr.B * pr.Hkv, DBN, kBF16) ||
+        !make_tensor_map(&tv, v, DD, pr.N, pr.B * pr.Hkv, DBN, kBF16))
+        return cudaErrorInvalidValue;
+    DecodeParams dp;
+    dp.ws_m = ws.m;
+    dp.ws_l = ws.l;
+    dp.ws_acc = ws.acc;
+    dp.status = status;
+    dp.Hq = pr.Hq;
+    dp.Hkv = pr.Hkv;
+    dp.M = pr.M;
+    dp.N = pr.N;
+    dp.G = pr.G;
+    dp.R = pr.G * pr.M;
+    dp.causal = pr.causal;
+    dp.window = pr.window;
+    dp.scale_log2 = pr.scale_log2;
+    dp.klo = pr.klo;
+    dp.khi = pr.khi;
+    dp.kbase = split_base(pr);
+    dp.chunk = chunk;
+    dp.S = S;
+    dim3 grid(S, pr.B * pr.Hkv);
+    attn_decode_kernel<kBF16><<<grid, kDecThreads, kDecSmem, stream>>>(tq, tk, tv, dp);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool decode_tc_supported(const Problem& p) { return p.D == DD && p.G * p.M <= DNR && p.B * p.Hkv <= 65535; }
+
+// Splits: every CTA resident at once when possible (two per SM), each
+// streaming an equal run of 128-key tiles; more splits only while the grid
+// still fits in one wave.
+int decode_plan_tc(const Problem& p, int* chunk, int* S) {
+    const int kbase = split_base(p);
+    const int tiles = p.khi > kbase ? (p.khi - kbase + DBN - 1) / DBN : 1;
+    const int groups = p.B * p.Hkv;
+    const int slots = 2 * sm_count();
+    int s = groups > 0 ? slots / groups : 1;
+    if (s < 1) s = 1;
+    if (s > tiles) s = tiles;
+    if (s > 4096) s = 4096;
+    const int per = (tiles + s - 1) / s;
+    *chunk = per * DBN;
+    *S = (tiles + per - 1) / per;
+    return ATTN_OK;
+}
+
+cudaError_t launch_decode_tc(const Problem& p, const void* q, const void* k, const void* v, int chunk, int S,
+                             const SplitWorkspace& ws, int* status, cudaStream_t stream) {
+    return p.dtype == ATTN_BF16 ? launch_decode_t<true>(p, q, k, v, chunk, S, ws, status, stream)
+                                : launch_decode_t<false>(p, q, k, v, chunk, S, ws, status, stream);
+}
+
+}  // namespace attn

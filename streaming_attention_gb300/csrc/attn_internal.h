@@ -32,8 +32,11 @@ __host__ __device__ inline void key_range(int p, int N, int causal, int window, 
 }
 
 // Split-KV workspace: the union key range [klo, khi) is cut into S chunks of
-// `chunk` keys; partial summaries are [rows][S] floats m and l (m in base-2
+// `chunk` keys (a multiple of 128) starting at split_base(p); partial summaries are [rows][S] floats m and l (m in base-2
 // logit units) and [rows][S][D] floats acc. Each part is 256-byte aligned.
+// Splits start at the visible range's start rounded down to a 128-key tile.
+inline int split_base(const Problem& p) { return (p.klo / 128) * 128; }
+
 struct SplitWorkspace {
     float* m;
     float* l;
@@ -53,6 +56,11 @@ cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const 
                           cudaStream_t stream);
 bool decode_supported(const Problem& p);
 int decode_plan(const Problem& p, int* chunk, int* S);
+// tcgen05 split kernel (D = 128, at most 16 grouped rows per KV head)
+bool decode_tc_supported(const Problem& p);
+int decode_plan_tc(const Problem& p, int* chunk, int* S);
+cudaError_t launch_decode_tc(const Problem& p, const void* q, const void* k, const void* v, int chunk, int S,
+                             const SplitWorkspace& ws, int* status, cudaStream_t stream);
 
 // Metadata validation and the device status word, shared by every entry point.
 int validate_problem(const void* q, const void* k, const void* v, const void* o, int B, int Hq, int Hkv, int M,

@@ -29,14 +29,11 @@
 // Every wait is bounded (1 s); on expiry the CTA raises an abort flag, sets
 // the device status word, drains its in-flight copies and MMAs, frees TMEM
 // and exits.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-#include <cuda_runtime.h>
-
 #include <mutex>
 
 #include "attn_internal.h"
 #include "sm100_ptx.cuh"
+#include "tma_map.h"
 
 namespace attn {
 namespace {
@@ -418,35 +415,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    });
-    return fn;
-}
-
-// [heads][rows][D] 16-bit tensor, boxes of 64 x 128 x 1 with 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, int D, int rows, int heads, bool bf16) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)heads};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)rows * D * 2};
-    cuuint32_t box[3] = {64, 128, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 template <int D, bool kBF16>
 int launch_t(const Problem& pr, const void* q, const void* k, const void* v, void* o, int* status,
              cudaStream_t stream) {
@@ -459,8 +427,9 @@ int launch_t(const Problem& pr, const void* q, const void* k, const void* v, voi
     });
     if (attr_err != cudaSuccess) return ATTN_ERR_CUDA;
     CUtensorMap tq, tk, tv;
-    if (!make_map(&tq, q, D, pr.M, pr.B * pr.Hq, kBF16) || !make_map(&tk, k, D, pr.N, pr.B * pr.Hkv, kBF16) ||
-        !make_map(&tv, v, D, pr.N, pr.B * pr.Hkv, kBF16))
+    if (!make_tensor_map(&tq, q, D, pr.M, pr.B * pr.Hq, BM, kBF16) ||
+        !make_tensor_map(&tk, k, D, pr.N, pr.B * pr.Hkv, BN, kBF16) ||
+        !make_tensor_map(&tv, v, D, pr.N, pr.B * pr.Hkv, BN, kBF16))
         return ATTN_ERR_CUDA;
     PrefillParams pp;
     pp.o = o;

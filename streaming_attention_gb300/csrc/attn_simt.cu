@@ -55,7 +55,7 @@ struct SimtArgs {
     int B, Hq, Hkv, M, N, G;
     int causal, window;
     float scale_log2;
-    int klo, khi, chunk, S;
+    int klo, khi, kbase, chunk, S;  // splits: [kbase + z*chunk, +chunk) within [klo, khi)
     int partial;  // 1: write (m, l, acc) summaries; 0: write normalized o
 };
 
@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) attn_simt_kernel(SimtArgs 
     int lo_first, hi_first, lo_last, hi_last;
     key_range(i0 + off, a.N, a.causal, a.window, &lo_first, &hi_first);
     key_range(i_last + off, a.N, a.causal, a.window, &lo_last, &hi_last);
-    const int s_lo = a.klo + blockIdx.z * a.chunk;
+    const int s_lo = a.kbase + blockIdx.z * a.chunk;
     const int s_hi = min(s_lo + a.chunk, a.khi);
     const int lo = max(lo_first, s_lo);
     const int hi = min(hi_last, s_hi);
@@ -273,6 +273,7 @@ cudaError_t launch_simt(const Problem& p, const void* q, const void* k, const vo
     a.scale_log2 = p.scale_log2;
     a.klo = ws ? p.klo : 0;
     a.khi = ws ? p.khi : p.N;
+    a.kbase = ws ? split_base(p) : 0;
     a.chunk = ws ? chunk : (p.N > 0 ? p.N : 1);
     a.S = ws ? S : 1;
     a.partial = ws ? 1 : 0;

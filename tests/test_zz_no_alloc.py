@@ -56,8 +56,18 @@ def test_noalloc_matches_attn_fwd_on_two_calls_in_a_row():
 
 
 def test_noalloc_rejects_problems_beyond_its_array():
-    # 4096 query rows x 32 splits of (D+2) floats is far above the fixed array;
-    # the call returns ATTN_ERR_WORKSPACE before touching any memory.
-    p = ctypes.c_void_p(0x10000)
-    st = sa.lib().attn_fwd_decode_noalloc(p, p, p, p, 16, 128, 16, 2, 8192, 128, 1, 0, 0.0, sa.ATTN_BF16, None)
+    """A decode whose split summaries exceed the fixed array is refused with
+    ATTN_ERR_WORKSPACE. The tensors are real device buffers of the full shape,
+    so nothing could touch invalid memory even if the call were accepted."""
+    B, Hq, Hkv, M, N, D = 8, 32, 8, 4, 8192, 64
+    need = sa.attn_workspace_bytes(B, Hq, Hkv, M, N, D, True, 0, sa.PATH_DECODE)
+    assert need > 8 << 20, need  # precondition: the problem does not fit the array
+    q, k, v = make_qkv(B, Hq, Hkv, M, N, D, torch.bfloat16, seed=5)
+    q, k, v = q.to(DEV), k.to(DEV), v.to(DEV)
+    o = torch.empty_like(q)
+    st = sa.lib().attn_fwd_decode_noalloc(
+        ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
+        ctypes.c_void_p(o.data_ptr()), B, Hq, Hkv, M, N, D, 1, 0, 0.0, sa.ATTN_BF16,
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
     assert st == -8, sa.strerror(st)
