@@ -4,8 +4,8 @@
 
 A step is one attention forward over the workload (one call of the library's
 C ABI; inputs resident in HBM). Device time comes from CUDA events on the
-launching stream around each step, with an L2 flush (a buffer twice the L2
-size is overwritten) between steps, outside the timed events. Under torchrun
+launching stream around a CUDA-graph replay of each step, with an L2 flush
+(a read of a buffer twice the L2 size) between steps, outside the timed events. Under torchrun
 each rank runs the same per-rank workload (weak scaling, no collective on the
 data path); the step time is the maximum over ranks.
 
@@ -158,9 +158,10 @@ class ClockSampler:
 # Our arm
 # ----------------------------------------------------------------------------
 def time_calls(fn, steps, warmup, stream, flush):
-    """Per-step device time (ms) of fn() with an L2 flush between steps."""
+    """Per-step device time (ms) of fn(stream) with an L2 flush between steps,
+    timed with CUDA events on the launching stream."""
     for _ in range(warmup):
-        fn()
+        fn(stream)
         flush()
     torch.cuda.synchronize()
     times = []
@@ -168,12 +169,46 @@ def time_calls(fn, steps, warmup, stream, flush):
         s = torch.cuda.Event(enable_timing=True)
         e = torch.cuda.Event(enable_timing=True)
         s.record(stream)
-        fn()
+        fn(stream)
         e.record(stream)
         flush()
         times.append((s, e))
     torch.cuda.synchronize()
     return [s.elapsed_time(e) for s, e in times]
+
+
+def capture(fn, warmup):
+    """One call of fn captured in a CUDA graph (after warm-up on a side stream)."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(warmup):
+            fn(side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(fn, steps, warmup, flush):
+    """Per-step device time (ms) of the captured call replayed, L2 flushed between replays."""
+    g = capture(fn, warmup)
+    return time_calls(lambda st: g.replay(), steps, warmup, torch.cuda.current_stream(), flush)
+
+
+def l2_flusher(dev):
+    """Evicts L2 by reading a buffer twice the L2 size. Reading leaves clean
+    lines, so the next step pays no write-back of the flush's own data."""
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    buf = torch.ones(2 * max(l2, 64 << 20) // 8, dtype=torch.int64, device=dev)
+
+    def flush():
+        buf.sum()
+
+    return flush
 
 
 def path_launches(path_name):
@@ -208,14 +243,10 @@ def run_ours(args):
     path, path_name = chosen_path(w)
     nbytes = sa.attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.M, w.N, w.D, w.causal, w.window, path)
     ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush_buf = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=dev)
+    flush = l2_flusher(dev)
 
-    def flush():
-        flush_buf.fill_(1)
-
-    def step():
-        sa.attn_fwd_ex(qd, kd, vd, od, w.causal, w.window, 0.0, path, ws if nbytes else None, stream)
+    def step(st):
+        sa.attn_fwd_ex(qd, kd, vd, od, w.causal, w.window, 0.0, path, ws if nbytes else None, st)
 
     decode = path_name == "decode"
     work = decode_bytes(w) if decode else flops(w)
@@ -225,7 +256,8 @@ def run_ours(args):
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        times = time_calls(step, args.steps, args.warmup, stream, flush)
+        times = time_graph(step, args.steps, args.warmup, flush)
+        eager = time_calls(step, args.steps, args.warmup, stream, flush)
     torch.cuda.synchronize()
     barrier(world)
     clocks = clk.summary()
@@ -282,8 +314,9 @@ def run_ours(args):
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "M": w.M, "N": w.N, "D": w.D,
                    "causal": w.causal, "window": w.window, "path": path_name,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "l2": "flushed between steps (2x L2 buffer overwritten)",
-                   "timing": "CUDA events per step on the launching stream"},
+                   "l2": "flushed between steps (a 2x-L2 buffer read; clean lines, no write-back)",
+                   "timing": "CUDA events around a CUDA-graph replay of one C-ABI call, per step",
+                   "eager_ms_per_step": round(statistics.mean(eager), 4)},
         "e2e": {"value": round(world * work / e2e_s / scale, 3), "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": path_launches(path_name) * args.steps,
@@ -335,8 +368,8 @@ def extra_measurements(args, dev, stream, flush):
         path, pname = chosen_path(w)
         nb = sa.attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.M, w.N, w.D, causal, w.window, path)
         ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
-        fn = lambda: sa.attn_fwd_ex(qd, kd, vd, od, causal, w.window, 0.0, path, ws if nb else None, stream)  # noqa
-        ms = statistics.median(time_calls(fn, steps, 3, stream, flush))
+        fn = lambda st: sa.attn_fwd_ex(qd, kd, vd, od, causal, w.window, 0.0, path, ws if nb else None, st)  # noqa
+        ms = statistics.median(time_graph(fn, steps, 3, flush))
         if pname == "decode":
             out[name] = {"GB/s": round(decode_bytes(w) / (ms * 1e-3) / 1e9, 1), "us": round(ms * 1e3, 2),
                          "path": pname}

@@ -120,7 +120,8 @@ __device__ __forceinline__ void ring_item(int u, int T, bool* is_v, int* tile) {
 __device__ __forceinline__ int ring_pos_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
 __device__ __forceinline__ int ring_pos_v(int j, int T) { return j == T - 1 ? 2 * T - 1 : 2 * j + 2; }
 
-template <bool kBF16>
+// RP: grouped rows handled by the softmax (R <= RP <= 16); the MMA always uses N = 16.
+template <bool kBF16, int RP>
 __global__ void __launch_bounds__(kDecThreads)
     attn_decode_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
@@ -181,6 +182,9 @@ __global__ void __launch_bounds__(kDecThreads)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Let the merge grid launch now: its CTAs wait in griddepcontrol.wait, which
+    // returns only after this whole grid has finished and its writes are visible.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == kDecLoadWarp) {
         if (lane == 0 && T > 0) {
@@ -256,16 +260,16 @@ __global__ void __launch_bounds__(kDecThreads)
         const int kl = threadIdx.x;  // 0..127
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         const float c = p.scale_log2;
-        int lo[DNR], hi[DNR];
+        int lo[RP], hi[RP];
 #pragma unroll
-        for (int r = 0; r < DNR; ++r) {
+        for (int r = 0; r < RP; ++r) {
             const int i = r % p.M;
             key_range(i + p.N - p.M, p.N, p.causal, p.window, &lo[r], &hi[r]);
-            if (r >= p.R) hi[r] = lo[r];  // padding rows see nothing
+            if (r >= p.R) hi[r] = lo[r];  // padding rows see nothing: their scores are -inf, p = 0
         }
-        float m_ref[DNR], l_part[DNR];
+        float m_ref[RP], l_part[RP];
 #pragma unroll
-        for (int r = 0; r < DNR; ++r) {
+        for (int r = 0; r < RP; ++r) {
             m_ref[r] = -INFINITY;
             l_part[r] = 0.f;
         }
@@ -280,37 +284,33 @@ __global__ void __launch_bounds__(kDecThreads)
                          : "+r"(sr[0]), "+r"(sr[1]), "+r"(sr[2]), "+r"(sr[3]), "+r"(sr[4]), "+r"(sr[5]), "+r"(sr[6]),
                            "+r"(sr[7]), "+r"(sr[8]), "+r"(sr[9]), "+r"(sr[10]), "+r"(sr[11]), "+r"(sr[12]),
                            "+r"(sr[13]), "+r"(sr[14]), "+r"(sr[15])::"memory");
-            float t[DNR];
+            float t[RP];
 #pragma unroll
-            for (int r = 0; r < DNR; ++r)
+            for (int r = 0; r < RP; ++r)
                 t[r] = (key >= lo[r] && key < hi[r]) ? __uint_as_float(sr[r]) * c : -INFINITY;
             // tile row maxima across the 128 keys
             float* redj = red + (j & 1) * 4 * DNR;
 #pragma unroll
-            for (int r = 0; r < DNR; ++r) {
-                if (r < p.R) {
-                    float x = t[r];
+            for (int r = 0; r < RP; ++r) {
+                float x = t[r];
 #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-                    if (lane == 0) redj[warp * DNR + r] = x;
-                }
+                for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+                if (lane == 0) redj[warp * DNR + r] = x;
             }
             mbar_arrive(bar_red0 + 8 * (j & 1));
             if (!(ok = dwait_warp(bar_red0 + 8 * (j & 1), (j >> 1) & 1, abort_flag, p.status))) break;
             bool need_any = false;
-            float alpha[DNR];
+            float alpha[RP];
 #pragma unroll
-            for (int r = 0; r < DNR; ++r) {
+            for (int r = 0; r < RP; ++r) {
                 alpha[r] = 1.f;
-                if (r < p.R) {
-                    const float mt = fmaxf(fmaxf(redj[r], redj[DNR + r]), fmaxf(redj[2 * DNR + r], redj[3 * DNR + r]));
-                    const float m_new = fmaxf(m_ref[r], mt);
-                    if (m_new > m_ref[r] + kDecRescale) {
-                        alpha[r] = ex2(m_ref[r] - m_new);
-                        l_part[r] *= alpha[r];
-                        m_ref[r] = m_new;
-                        need_any = true;
-                    }
+                const float mt = fmaxf(fmaxf(redj[r], redj[DNR + r]), fmaxf(redj[2 * DNR + r], redj[3 * DNR + r]));
+                const float m_new = fmaxf(m_ref[r], mt);
+                if (m_new > m_ref[r] + kDecRescale) {
+                    alpha[r] = ex2(m_ref[r] - m_new);
+                    l_part[r] *= alpha[r];
+                    m_ref[r] = m_new;
+                    need_any = true;
                 }
             }
             // P^T buffer j&1 was last read by the value product of tile j-2
@@ -319,15 +319,13 @@ __global__ void __launch_bounds__(kDecThreads)
             uint8_t* pbuf = smem + kOffP + (j & 1) * kQBytes;
             const int kc = kl >> 6, k64 = kl & 63;
 #pragma unroll
-            for (int r = 0; r < DNR; ++r) {
-                if (r < p.R) {
-                    const float m_use = (m_ref[r] == -INFINITY) ? 0.f : m_ref[r];
-                    const float pr = ex2(t[r] - m_use);
-                    l_part[r] += pr;
-                    const uint32_t pk = kBF16 ? pack_bf16(pr, 0.f) : pack_f16(pr, 0.f);
-                    const int off = kc * kQChunk + r * 128 + ((((k64 >> 3) ^ (r & 7))) << 4) + (k64 & 7) * 2;
-                    *reinterpret_cast<uint16_t*>(pbuf + off) = (uint16_t)(pk & 0xFFFFu);
-                }
+            for (int r = 0; r < RP; ++r) {
+                const float m_use = (m_ref[r] == -INFINITY) ? 0.f : m_ref[r];
+                const float pr = ex2(t[r] - m_use);
+                l_part[r] += pr;
+                const uint32_t pk = kBF16 ? pack_bf16(pr, 0.f) : pack_f16(pr, 0.f);
+                const int off = kc * kQChunk + r * 128 + ((((k64 >> 3) ^ (r & 7))) << 4) + (k64 & 7) * 2;
+                *reinterpret_cast<uint16_t*>(pbuf + off) = (uint16_t)(pk & 0xFFFFu);
             }
             // lazy rescale of O^T (needs the value product of tile j-1 complete)
             if (need_any && j > 0) {
@@ -341,7 +339,7 @@ __global__ void __launch_bounds__(kDecThreads)
                                "+r"(o[7]), "+r"(o[8]), "+r"(o[9]), "+r"(o[10]), "+r"(o[11]), "+r"(o[12]),
                                "+r"(o[13]), "+r"(o[14]), "+r"(o[15])::"memory");
 #pragma unroll
-                for (int r = 0; r < DNR; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[r]);
+                for (int r = 0; r < RP; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[r]);
                 tmem_st_x16(tmem + lane_base + kColOT, o);
                 tmem_wait_st();
             }
@@ -358,7 +356,7 @@ __global__ void __launch_bounds__(kDecThreads)
         if (have) {
             tc_fence_after();
 #pragma unroll
-            for (int r = 0; r < DNR; ++r) {
+            for (int r = 0; r < RP; ++r) {
                 if (r < p.R) {
                     float x = l_part[r];
 #pragma unroll
@@ -377,7 +375,7 @@ __global__ void __launch_bounds__(kDecThreads)
                            "+r"(o[7]), "+r"(o[8]), "+r"(o[9]), "+r"(o[10]), "+r"(o[11]), "+r"(o[12]), "+r"(o[13]),
                            "+r"(o[14]), "+r"(o[15])::"memory");
 #pragma unroll
-            for (int r = 0; r < DNR; ++r) {
+            for (int r = 0; r < RP; ++r) {
                 if (r < p.R) {
                     const size_t slot = (size_t)(row_base + r) * p.S + split;
                     p.ws_acc[slot * DD + kl] = __uint_as_float(o[r]);
@@ -406,8 +404,6 @@ __global__ void __launch_bounds__(kDecThreads)
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
-    // the merge kernel may start its prologue
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 int sm_count() {
@@ -422,13 +418,13 @@ int sm_count() {
     return n;
 }
 
-template <bool kBF16>
+template <bool kBF16, int RP>
 cudaError_t launch_decode_t(const Problem& pr, const void* q, const void* k, const void* v, int chunk, int S,
                             const SplitWorkspace& ws, int* status, cudaStream_t stream) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(attn_decode_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(attn_decode_kernel<kBF16, RP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         kDecSmem);
     });
     if (attr_err != cudaSuccess) return attr_err;
@@ -457,7 +453,7 @@ cudaError_t launch_decode_t(const Problem& pr, const void* q, const void* k, con
     dp.chunk = chunk;
     dp.S = S;
     dim3 grid(S, pr.B * pr.Hkv);
-    attn_decode_kernel<kBF16><<<grid, kDecThreads, kDecSmem, stream>>>(tq, tk, tv, dp);
+    attn_decode_kernel<kBF16, RP><<<grid, kDecThreads, kDecSmem, stream>>>(tq, tk, tv, dp);
     return cudaGetLastError();
 }
 
@@ -485,8 +481,14 @@ int decode_plan_tc(const Problem& p, int* chunk, int* S) {
 
 cudaError_t launch_decode_tc(const Problem& p, const void* q, const void* k, const void* v, int chunk, int S,
                              const SplitWorkspace& ws, int* status, cudaStream_t stream) {
-    return p.dtype == ATTN_BF16 ? launch_decode_t<true>(p, q, k, v, chunk, S, ws, status, stream)
-                                : launch_decode_t<false>(p, q, k, v, chunk, S, ws, status, stream);
+    const int R = p.G * p.M;
+    const bool bf = p.dtype == ATTN_BF16;
+    if (R <= 4) return bf ? launch_decode_t<true, 4>(p, q, k, v, chunk, S, ws, status, stream)
+                          : launch_decode_t<false, 4>(p, q, k, v, chunk, S, ws, status, stream);
+    if (R <= 8) return bf ? launch_decode_t<true, 8>(p, q, k, v, chunk, S, ws, status, stream)
+                          : launch_decode_t<false, 8>(p, q, k, v, chunk, S, ws, status, stream);
+    return bf ? launch_decode_t<true, 16>(p, q, k, v, chunk, S, ws, status, stream)
+              : launch_decode_t<false, 16>(p, q, k, v, chunk, S, ws, status, stream);
 }
 
 }  // namespace attn

@@ -165,68 +165,46 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) attn_simt_kernel(SimtArgs 
     }
 }
 
-// Merge of S summaries per row. unit converts the stored maxima to base 2
-// (1 for base-2 maxima, log2(e) for natural-log maxima).
-__global__ void __launch_bounds__(128) attn_merge_kernel(const float* __restrict__ m, const float* __restrict__ l,
-                                                         const float* __restrict__ acc, void* o, float* m_out,
-                                                         float* l_out, int S, int D, int out_dtype, float unit,
-                                                         int programmatic) {
-    extern __shared__ float w[];  // [S] weights
-    __shared__ float red[32];
-    __shared__ float bc;
+// Merge of S summaries, one thread per output element (row, d): every load is
+// independent of the arithmetic, so the whole merge is one memory round trip.
+// unit converts the stored maxima to base 2 (1 for base-2 maxima, log2(e) for
+// natural-log maxima).
+constexpr int kMergeThreads = 256;
+
+__global__ void __launch_bounds__(kMergeThreads)
+    attn_merge_kernel(const float* __restrict__ m, const float* __restrict__ l, const float* __restrict__ acc,
+                      void* o, float* m_out, float* l_out, int rows, int S, int D, int out_dtype, float unit,
+                      int programmatic) {
     if (programmatic) asm volatile("griddepcontrol.wait;" ::: "memory");
-    const size_t row = blockIdx.x;
+    const size_t idx = (size_t)blockIdx.x * kMergeThreads + threadIdx.x;
+    const size_t row = idx / D;
+    const int d = (int)(idx % D);
+    if (row >= (size_t)rows) return;
     const float* mr = m + row * S;
     const float* lr = l + row * S;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    const float* ar = acc + row * S * D + d;
 
     float mx = -INFINITY;
-    for (int s = tid; s < S; s += blockDim.x) mx = fmaxf(mx, mr[s]);
-    mx = warp_max(mx);
-    if (lane == 0) red[warp] = mx;
-    __syncthreads();
-    if (tid == 0) {
-        float x = red[0];
-        for (int t = 1; t < nw; ++t) x = fmaxf(x, red[t]);
-        bc = x;
-    }
-    __syncthreads();
-    mx = bc;
-
-    float lsum = 0.f;
-    for (int s = tid; s < S; s += blockDim.x) {
+#pragma unroll 8
+    for (int s = 0; s < S; ++s) mx = fmaxf(mx, mr[s]);
+    float L = 0.f, x = 0.f;
+#pragma unroll 8
+    for (int s = 0; s < S; ++s) {
         const float ms = mr[s];
         // an empty summary (m = -inf) weighs 0; never forms -inf - (-inf)
         const float ws = (ms == -INFINITY) ? 0.f : exp2f((ms - mx) * unit);
-        w[s] = ws;
-        lsum += ws * lr[s];
+        L = fmaf(ws, lr[s], L);
+        x = fmaf(ws, ar[(size_t)s * D], x);
     }
-    lsum = warp_sum(lsum);
-    __syncthreads();
-    if (lane == 0) red[warp] = lsum;
-    __syncthreads();
-    if (tid == 0) {
-        float x = 0.f;
-        for (int t = 0; t < nw; ++t) x += red[t];
-        bc = x;
-    }
-    __syncthreads();
-    const float L = bc;
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-
-    const float* ar = acc + row * (size_t)S * D;
-    for (int d = tid; d < D; d += blockDim.x) {
-        float x = 0.f;
-        for (int s = 0; s < S; ++s) x = fmaf(w[s], ar[(size_t)s * D + d], x);
-        x *= inv;
-        if (out_dtype == ATTN_BF16)
-            reinterpret_cast<__nv_bfloat16*>(o)[row * D + d] = __float2bfloat16_rn(x);
-        else if (out_dtype == ATTN_FP16)
-            reinterpret_cast<__half*>(o)[row * D + d] = __float2half_rn(x);
-        else
-            reinterpret_cast<float*>(o)[row * D + d] = x;
-    }
-    if (tid == 0) {
+    x *= L > 0.f ? 1.f / L : 0.f;
+    const size_t out = row * D + d;
+    if (out_dtype == ATTN_BF16)
+        reinterpret_cast<__nv_bfloat16*>(o)[out] = __float2bfloat16_rn(x);
+    else if (out_dtype == ATTN_FP16)
+        reinterpret_cast<__half*>(o)[out] = __float2half_rn(x);
+    else
+        reinterpret_cast<float*>(o)[out] = x;
+    if (d == 0) {
         if (m_out) m_out[row] = mx;
         if (l_out) l_out[row] = L;
     }
@@ -286,16 +264,16 @@ cudaError_t launch_merge(const float* m, const float* l, const float* acc, void*
                          cudaStream_t stream) {
     if (rows == 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(rows);
-    cfg.blockDim = dim3(128);
-    cfg.dynamicSmemBytes = sizeof(float) * (size_t)S;
+    cfg.gridDim = dim3((unsigned)(((size_t)rows * D + kMergeThreads - 1) / kMergeThreads));
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = programmatic ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, attn_merge_kernel, m, l, acc, o, m_out, l_out, S, D, out_dtype, unit,
+    return cudaLaunchKernelEx(&cfg, attn_merge_kernel, m, l, acc, o, m_out, l_out, rows, S, D, out_dtype, unit,
                               programmatic ? 1 : 0);
 }
 
