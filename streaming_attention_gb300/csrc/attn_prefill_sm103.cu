@@ -1,10 +1,11 @@
 // Prefill forward on the 5th-generation tensor cores (tcgen05 + TMEM), sm_103a.
 //
-// One CTA owns two 128-row query tiles of one (batch, head) and streams the
+// Persistent kernel: one CTA per SM walks a list of work tiles, each two
+// 128-row query tiles (256 rows) of one (batch, head), and streams the
 // key/value tiles they may see. Warp roles:
-//   warps 0-3  softmax for query tile 0 (one TMEM lane = one row = one thread)
-//   warps 4-7  softmax for query tile 1
-//   warp 8     TMA producer: Q once, then K_j, V_j through a shared-memory ring
+//   warps 0-3  softmax + epilogue for query tile 0 (one TMEM lane = one row = one thread)
+//   warps 4-7  softmax + epilogue for query tile 1
+//   warp 8     TMA producer: Q of each work tile, then K_j, V_j through a shared-memory ring
 //   warp 9     MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 [384,384+D).
 // P_t (16-bit, two per column) overwrites the first 64 columns of S_t.
@@ -18,8 +19,15 @@
 // Notes & Checklist", gotchas ledger), a row whose keys are all masked so far
 // uses 0 as its maximum so it never forms -inf - (-inf) (same ledger, ghost
 // rows), and only tiles that cross a mask edge pay for masking (same ledger,
-// boundary checks are not free). Key tiles that no row of the CTA may see are
-// never loaded (causal and window tile skipping).
+// boundary checks are not free). Key tiles that no row of a work tile may see
+// are never loaded (causal and window tile skipping).
+//
+// Work tiles are ordered longest first (causal) and dealt to the CTAs in a
+// serpentine order, which balances causal work to about 1 %. Across work
+// tiles the K/V ring and every barrier phase carry on: Q of the next tile is
+// loaded as soon as the last score product of the current one has read Q, and
+// the next tile's first value product into O_t waits only until the epilogue
+// of the current tile has pulled O_t out of TMEM, so epilogues overlap MMAs.
 //
 // Rescaling is lazy: a row's reference maximum moves only when the new
 // maximum exceeds it by more than 8 (base-2 units), so p = 2^(t - m_ref) <= 256
@@ -42,7 +50,7 @@ using namespace ptx;
 
 constexpr int BM = 128;  // rows per query tile
 constexpr int BN = 128;  // keys per key/value tile
-constexpr int NQ = 2;    // query tiles per CTA
+constexpr int NQ = 2;    // query tiles per work tile
 constexpr int kThreads = 320;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -58,7 +66,8 @@ struct Cfg {
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = NQ * kTileBytes;
     static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
-    static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 1;
+    // q_full, q_free, full[S], empty[S], s_full[2], p_full[2], o_final, o_free[2], drain
+    static constexpr int kNumBars = 2 + 2 * kStages + 2 + 2 + 1 + 2 + 1;
     static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
 };
@@ -73,15 +82,44 @@ struct PrefillParams {
     int M, N, Hq, Hkv, G;
     int causal, window;
     float scale_log2;
+    int BH;     // B * Hq
+    int nqb;    // work tiles per head (ceil(M / 256))
+    int tiles;  // BH * nqb
 };
 
-struct Shared {
-    uint32_t bar_q, bar_full0, bar_empty0, bar_s0, bar_p0, bar_o;
-    __device__ uint32_t full(int s) const { return bar_full0 + 8u * s; }
-    __device__ uint32_t empty(int s) const { return bar_empty0 + 8u * s; }
-    __device__ uint32_t s_full(int t) const { return bar_s0 + 8u * t; }
-    __device__ uint32_t p_full(int t) const { return bar_p0 + 8u * t; }
+struct Bars {
+    uint32_t q_full, q_free, full0, empty0, s0, p0, o_final, o_free0, drain;
+    __device__ uint32_t full(int s) const { return full0 + 8u * s; }
+    __device__ uint32_t empty(int s) const { return empty0 + 8u * s; }
+    __device__ uint32_t s_full(int t) const { return s0 + 8u * t; }
+    __device__ uint32_t p_full(int t) const { return p0 + 8u * t; }
+    __device__ uint32_t o_free(int t) const { return o_free0 + 8u * t; }
 };
+
+// Geometry of one work tile: its head, first row and the key tiles it visits.
+struct Work {
+    int bh, kvh, row0, jt0, n;
+};
+
+// w-th work tile of this CTA (serpentine over a longest-first order); false when done.
+__device__ __forceinline__ bool work_tile(const PrefillParams& p, int w, Work* t) {
+    const int grid = gridDim.x, c = blockIdx.x;
+    const int idx = w * grid + ((w & 1) ? grid - 1 - c : c);
+    if (idx >= p.tiles) return false;
+    const int qb = p.nqb - 1 - idx / p.BH;
+    t->bh = idx % p.BH;
+    const int b = t->bh / p.Hq, h = t->bh % p.Hq;
+    t->kvh = b * p.Hkv + h / p.G;
+    t->row0 = qb * (NQ * BM);
+    const int off = p.N - p.M;  // row i sits at key position i + off
+    const int last_row = min(t->row0 + NQ * BM - 1, p.M - 1);
+    int klo = 0, khi = p.N, unused = 0;
+    key_range(t->row0 + off, p.N, p.causal, p.window, &klo, &unused);
+    key_range(last_row + off, p.N, p.causal, p.window, &unused, &khi);
+    t->jt0 = klo / BN;
+    t->n = (khi > klo) ? (khi + BN - 1) / BN - t->jt0 : 0;
+    return true;
+}
 
 // Single-thread bounded wait. abortable: give up as soon as another thread raised the abort flag.
 __device__ bool wait_one(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag, int* status,
@@ -136,43 +174,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sQ = sbase + C::kQOff;
     const uint32_t sKV = sbase + C::kKVOff;
-    Shared sh;
-    sh.bar_q = sbase + C::kBarOff;
-    sh.bar_full0 = sh.bar_q + 8;
-    sh.bar_empty0 = sh.bar_full0 + 8 * C::kStages;
-    sh.bar_s0 = sh.bar_empty0 + 8 * C::kStages;
-    sh.bar_p0 = sh.bar_s0 + 16;
-    sh.bar_o = sh.bar_p0 + 16;
+    Bars bar;
+    bar.q_full = sbase + C::kBarOff;
+    bar.q_free = bar.q_full + 8;
+    bar.full0 = bar.q_free + 8;
+    bar.empty0 = bar.full0 + 8 * C::kStages;
+    bar.s0 = bar.empty0 + 8 * C::kStages;
+    bar.p0 = bar.s0 + 16;
+    bar.o_final = bar.p0 + 16;
+    bar.o_free0 = bar.o_final + 8;
+    bar.drain = bar.o_free0 + 16;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff);
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // ---- which rows and keys this CTA owns --------------------------------
-    const int bh = blockIdx.x;
-    const int qb = gridDim.y - 1 - blockIdx.y;  // longest (causal) blocks first
-    const int b = bh / p.Hq, h = bh % p.Hq;
-    const int kvh = b * p.Hkv + h / p.G;
-    const int row0 = qb * (NQ * BM);
-    const int off = p.N - p.M;  // row i sits at key position i + off
-    const int last_row = min(row0 + NQ * BM - 1, p.M - 1);
-    int klo = 0, khi = p.N, lo_unused = 0, hi_unused = 0;
-    key_range(row0 + off, p.N, p.causal, p.window, &klo, &hi_unused);
-    key_range(last_row + off, p.N, p.causal, p.window, &lo_unused, &khi);
-    const int jt0 = klo / BN;
-    const int n = (khi > klo) ? (khi + BN - 1) / BN - jt0 : 0;  // key tiles to visit
-
     if (threadIdx.x == 0) {
-        mbar_init(sh.bar_q, 1);
+        mbar_init(bar.q_full, 1);
+        mbar_init(bar.q_free, 1);
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(sh.full(s), 1);
-            mbar_init(sh.empty(s), 1);
+            mbar_init(bar.full(s), 1);
+            mbar_init(bar.empty(s), 1);
         }
         for (int t = 0; t < NQ; ++t) {
-            mbar_init(sh.s_full(t), 1);
-            mbar_init(sh.p_full(t), 4 * 32);
+            mbar_init(bar.s_full(t), 1);
+            mbar_init(bar.p_full(t), 4 * 32);
+            mbar_init(bar.o_free(t), 4 * 32);
         }
-        mbar_init(sh.bar_o, 1);
+        mbar_init(bar.o_final, 1);
+        mbar_init(bar.drain, 1);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -187,39 +217,52 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kLoadWarp) {
         // ---------------- TMA producer ----------------
-        if (lane == 0 && n > 0) {
+        if (lane == 0) {
             prefetch_tmap(&tmQ);
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
-            mbar_arrive_expect_tx(sh.bar_q, NQ * C::kTileBytes);
-            for (int t = 0; t < NQ; ++t)
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(sQ + t * C::kTileBytes + c * C::kChunkBytes, &tmQ, c * 64, row0 + t * BM, bh,
-                                sh.bar_q);
-            int issued = 0;
-            // K_j and V_j alternate through the ring in the order the MMA uses them
-            for (int u = 0; u < 2 * n; ++u) {
-                const int s = u % C::kStages;
-                if (u >= C::kStages &&
-                    !wait_one(sh.empty(s), ((u / C::kStages) - 1) & 1, abort_flag, p.status))
-                    break;
-                mbar_arrive_expect_tx(sh.full(s), C::kTileBytes);
-                const CUtensorMap* tm = (u & 1) ? &tmV : &tmK;
-                const int key0 = (jt0 + u / 2) * BN;
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(sKV + s * C::kTileBytes + c * C::kChunkBytes, tm, c * 64, key0, kvh, sh.full(s));
-                issued = u + 1;
+            int u = 0, tc = 0;  // ring position and work tiles with keys, across the whole walk
+            int q_issued = 0;   // Q loads issued
+            bool ok = true;
+            Work wk;
+            for (int w = 0; ok && work_tile(p, w, &wk); ++w) {
+                if (wk.n == 0) continue;
+                // Q of this tile may overwrite Q of the previous one once its last score product read it
+                if (tc > 0 && !(ok = wait_one(bar.q_free, (tc - 1) & 1, abort_flag, p.status))) break;
+                mbar_arrive_expect_tx(bar.q_full, NQ * C::kTileBytes);
+                for (int t = 0; t < NQ; ++t)
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d(sQ + t * C::kTileBytes + c * C::kChunkBytes, &tmQ, c * 64, wk.row0 + t * BM,
+                                    wk.bh, bar.q_full);
+                ++q_issued;
+                // K_j and V_j alternate through the ring in the order the MMA uses them
+                for (int x = 0; x < 2 * wk.n; ++x, ++u) {
+                    const int s = u % C::kStages;
+                    if (u >= C::kStages &&
+                        !(ok = wait_one(bar.empty(s), ((u / C::kStages) - 1) & 1, abort_flag, p.status)))
+                        break;
+                    mbar_arrive_expect_tx(bar.full(s), C::kTileBytes);
+                    const CUtensorMap* tm = (x & 1) ? &tmV : &tmK;
+                    const int key0 = (wk.jt0 + x / 2) * BN;
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d(sKV + s * C::kTileBytes + c * C::kChunkBytes, tm, c * 64, key0, wk.kvh,
+                                    bar.full(s));
+                }
+                ++tc;
             }
             // every issued copy must land before the CTA may exit
-            wait_one(sh.bar_q, 0, abort_flag, p.status, false);
-            for (int u = max(0, issued - C::kStages); u < issued; ++u)
-                wait_one(sh.full(u % C::kStages), (u / C::kStages) & 1, abort_flag, p.status, false);
+            if (q_issued > 0) wait_one(bar.q_full, (q_issued - 1) & 1, abort_flag, p.status, false);
+            for (int x = max(0, u - C::kStages); x < u; ++x)
+                wait_one(bar.full(x % C::kStages), (x / C::kStages) & 1, abort_flag, p.status, false);
         }
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issuer ----------------
-        if (lane == 0 && n > 0) {
+        if (lane == 0) {
             constexpr uint32_t idS = idesc_f16(kBF16, BM, BN, false);
             constexpr uint32_t idPV = idesc_f16(kBF16, BM, D, true);
+            int u = 0, tc = 0;
+            int ps[NQ] = {0, 0};  // P tiles consumed per query tile, across the walk
+            bool ok = true;
             auto issue_s = [&](int t, int slot) {
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off_k = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
@@ -228,178 +271,192 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_ss(tmem + col_s(t), a, bd, idS, kk > 0 ? 1u : 0u);
                 }
             };
+            // O_t += P_t V; the first product of a tile overwrites O_t, after the
+            // previous tile's epilogue has read it out
             auto issue_pv = [&](int t, int slot, bool first) {
+                if (!wait_one(bar.p_full(t), ps[t] & 1, abort_flag, p.status)) return false;
+                ++ps[t];
+                if (first && tc > 0 && !wait_one(bar.o_free(t), (tc - 1) & 1, abort_flag, p.status)) return false;
+                tc_fence_after();
                 for (int kk = 0; kk < BN / 16; ++kk) {
                     const uint64_t bd = sw128_desc(sKV + slot * C::kTileBytes + kk * 16 * 128, C::kChunkBytes, 1024);
                     mma_ts(tmem + col_o(t), tmem + col_s(t) + kk * 8, bd, idPV, (first && kk == 0) ? 0u : 1u);
                 }
+                return true;
             };
-            bool ok = wait_one(sh.bar_q, 0, abort_flag, p.status);
-            tc_fence_after();
-            int slot_v_prev = 0;
-            for (int jj = 0; ok && jj < n; ++jj) {
-                const int uk = 2 * jj, sk = uk % C::kStages;
-                if (!(ok = wait_one(sh.full(sk), (uk / C::kStages) & 1, abort_flag, p.status))) break;
+            Work wk;
+            for (int w = 0; ok && work_tile(p, w, &wk); ++w) {
+                const int n = wk.n;
+                if (n == 0) continue;
+                if (!(ok = wait_one(bar.q_full, tc & 1, abort_flag, p.status))) break;
                 tc_fence_after();
-                issue_s(0, sk);
-                mma_commit(sh.s_full(0));
-                if (jj > 0) {
-                    if (!(ok = wait_one(sh.p_full(1), (jj - 1) & 1, abort_flag, p.status))) break;
+                int slot_v_prev = 0;
+                for (int jj = 0; jj < n; ++jj) {
+                    const int uk = u++, sk = uk % C::kStages;
+                    const int uv = u++, sv = uv % C::kStages;
+                    if (!(ok = wait_one(bar.full(sk), (uk / C::kStages) & 1, abort_flag, p.status))) break;
                     tc_fence_after();
-                    issue_pv(1, slot_v_prev, jj - 1 == 0);
-                    mma_commit(sh.empty(slot_v_prev));
+                    issue_s(0, sk);
+                    mma_commit(bar.s_full(0));
+                    if (jj > 0) {
+                        if (!(ok = issue_pv(1, slot_v_prev, jj - 1 == 0))) break;
+                        mma_commit(bar.empty(slot_v_prev));
+                    }
+                    issue_s(1, sk);
+                    mma_commit(bar.s_full(1));
+                    if (jj == n - 1) mma_commit(bar.q_free);  // Q is read for the last time
+                    mma_commit(bar.empty(sk));
+                    if (!(ok = wait_one(bar.full(sv), (uv / C::kStages) & 1, abort_flag, p.status))) break;
+                    if (!(ok = issue_pv(0, sv, jj == 0))) break;
+                    slot_v_prev = sv;
                 }
-                issue_s(1, sk);
-                mma_commit(sh.s_full(1));
-                mma_commit(sh.empty(sk));
-                const int uv = 2 * jj + 1, sv = uv % C::kStages;
-                if (!(ok = wait_one(sh.full(sv), (uv / C::kStages) & 1, abort_flag, p.status))) break;
-                if (!(ok = wait_one(sh.p_full(0), jj & 1, abort_flag, p.status))) break;
-                tc_fence_after();
-                issue_pv(0, sv, jj == 0);
-                slot_v_prev = sv;
+                if (!ok) break;
+                if (!(ok = issue_pv(1, slot_v_prev, n - 1 == 0))) break;
+                mma_commit(bar.empty(slot_v_prev));
+                mma_commit(bar.o_final);  // this tile's O_0 and O_1 are final
+                ++tc;
             }
-            if (ok && wait_one(sh.p_full(1), (n - 1) & 1, abort_flag, p.status)) {
-                tc_fence_after();
-                issue_pv(1, slot_v_prev, n - 1 == 0);
-                mma_commit(sh.empty(slot_v_prev));
-            }
-            // all MMAs done -> O final (and TMEM/smem safe to release)
-            mma_commit(sh.bar_o);
-            wait_one(sh.bar_o, 0, abort_flag, p.status, false);
+            // all MMAs done before TMEM and shared memory are released
+            mma_commit(bar.drain);
+            wait_one(bar.drain, 0, abort_flag, p.status, false);
         }
         __syncwarp();
     } else {
         // ---------------- softmax warps ----------------
-        const int t = warp >> 2;            // query tile
-        const int wq = warp & 3;            // TMEM lane quarter
+        const int t = warp >> 2;  // query tile
+        const int wq = warp & 3;  // TMEM lane quarter
         const int r_in_tile = wq * 32 + lane;
-        const int row = row0 + t * BM + r_in_tile;
-        const int pos = row + off;
-        const int tile_first_pos = row0 + t * BM + off;
-        const int tile_last_pos = tile_first_pos + BM - 1;
         const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
         const uint32_t tS = tmem + lane_base + col_s(t);
         const uint32_t tO = tmem + lane_base + col_o(t);
         const float c = p.scale_log2;
         const float masked_s = c >= 0.f ? -INFINITY : INFINITY;  // scores that give t = -inf
-
-        float m_ref = -INFINITY;  // reference maximum (base-2 scaled units)
-        float l = 0.f;
+        const int off = p.N - p.M;
+        int g = 0, tc = 0;  // score tiles and work tiles with keys, across the walk
         bool ok = true;
-        for (int jj = 0; jj < n; ++jj) {
-            const int key0 = (jt0 + jj) * BN;
-            if (!(ok = wait_warp(sh.s_full(t), jj & 1, abort_flag, p.status))) break;
-            tc_fence_after();
-            uint32_t s[4][32];
+        Work wk;
+        for (int w = 0; ok && work_tile(p, w, &wk); ++w) {
+            const int row = wk.row0 + t * BM + r_in_tile;
+            uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + ((size_t)wk.bh * p.M + row) * D;
+            if (wk.n == 0) {  // no row of this tile sees any key: output 0
+                if (row < p.M) {
+                    uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) tmem_ld_x32(tS + q4 * 32, s[q4]);
-            tmem_wait_ld_x32(s[0]);
-            reg_after_x32(s[1]);
-            reg_after_x32(s[2]);
-            reg_after_x32(s[3]);
-
-            // mask only tiles that cross an edge (ragged N, causal diagonal, window start)
-            const bool need_mask = (key0 + BN > p.N) || (p.causal && key0 + BN - 1 > tile_first_pos) ||
-                                   (p.window > 0 && key0 <= tile_last_pos - p.window);
-            if (need_mask) {
-                int lo = 0, hi = 0;
-                key_range(pos, p.N, p.causal, p.window, &lo, &hi);
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int key = key0 + q4 * 32 + e;
-                        if (key < lo || key >= hi) s[q4][e] = __float_as_uint(masked_s);
-                    }
-            }
-            float mx;
-            if (c >= 0.f) {
-                mx = -INFINITY;
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(s[q4][e]));
-            } else {
-                mx = INFINITY;
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) mx = fminf(mx, __uint_as_float(s[q4][e]));
-            }
-            const float m_tile = mx * c;  // -inf when the whole tile is masked for this row
-            const float m_new = fmaxf(m_ref, m_tile);
-            const bool need = m_new > m_ref + kRescaleThreshold;
-            float alpha = 1.f;
-            if (need) {
-                alpha = ex2(m_ref - m_new);  // m_ref = -inf -> 0
-                l *= alpha;
-                m_ref = m_new;
-            }
-            // ghost-row pin: while every key so far is masked, exponentiate against 0
-            const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-            const float neg_m = -m_use;
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t packed[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float p0 = ex2(fmaf(__uint_as_float(s[q4][2 * e]), c, neg_m));
-                    const float p1 = ex2(fmaf(__uint_as_float(s[q4][2 * e + 1]), c, neg_m));
-                    l += p0 + p1;
-                    packed[e] = pack2<kBF16>(p0, p1);
+                    for (int v4 = 0; v4 < D / 8; ++v4) dst[v4] = make_uint4(0, 0, 0, 0);
                 }
-                tmem_st_x16(tS + q4 * 16, packed);  // P overwrites the first 64 columns of S
+                continue;
             }
-            // rescale the accumulator (the PV of the previous tile has completed:
-            // its commit preceded this tile's score commit)
-            if (__any_sync(0xffffffffu, need) && jj > 0) {
-#pragma unroll
-                for (int ch = 0; ch < D / 32; ++ch) {
-                    uint32_t o[32];
-                    tmem_ld_x32(tO + ch * 32, o);
-                    tmem_wait_ld_x32(o);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tmem_st_x32(tO + ch * 32, o);
-                }
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(sh.p_full(t));
-        }
-
-        // ---------------- epilogue: O / l, one cast, store rows < M ----------------
-        int stop = 0;
-        if (lane == 0) stop = *abort_flag ? 1 : 0;
-        stop = __shfl_sync(0xffffffffu, stop, 0);
-        if (ok && !stop) {
-            const bool have = n > 0 && wait_warp(sh.bar_o, 0, abort_flag, p.status);
-            if (n == 0 || have) {
+            const int pos = row + off;
+            const int tile_first_pos = wk.row0 + t * BM + off;
+            const int tile_last_pos = tile_first_pos + BM - 1;
+            float m_ref = -INFINITY;  // reference maximum (base-2 scaled units)
+            float l = 0.f;
+            for (int jj = 0; jj < wk.n; ++jj, ++g) {
+                const int key0 = (wk.jt0 + jj) * BN;
+                if (!(ok = wait_warp(bar.s_full(t), g & 1, abort_flag, p.status))) break;
                 tc_fence_after();
-                const float inv = l > 0.f ? 1.f / l : 0.f;  // no visible key: output 0
-                uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + ((size_t)bh * p.M + row) * D;
+                uint32_t s[4][32];
 #pragma unroll
-                for (int ch = 0; ch < D / 32; ++ch) {
-                    uint32_t o[32];
-                    if (n > 0) {
+                for (int q4 = 0; q4 < 4; ++q4) tmem_ld_x32(tS + q4 * 32, s[q4]);
+                tmem_wait_ld_x32(s[0]);
+                reg_after_x32(s[1]);
+                reg_after_x32(s[2]);
+                reg_after_x32(s[3]);
+
+                // mask only tiles that cross an edge (ragged N, causal diagonal, window start)
+                const bool need_mask = (key0 + BN > p.N) || (p.causal && key0 + BN - 1 > tile_first_pos) ||
+                                       (p.window > 0 && key0 <= tile_last_pos - p.window);
+                if (need_mask) {
+                    int lo = 0, hi = 0;
+                    key_range(pos, p.N, p.causal, p.window, &lo, &hi);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const int key = key0 + q4 * 32 + e;
+                            if (key < lo || key >= hi) s[q4][e] = __float_as_uint(masked_s);
+                        }
+                }
+                float mx;
+                if (c >= 0.f) {
+                    mx = -INFINITY;
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(s[q4][e]));
+                } else {
+                    mx = INFINITY;
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) mx = fminf(mx, __uint_as_float(s[q4][e]));
+                }
+                const float m_tile = mx * c;  // -inf when the whole tile is masked for this row
+                const float m_new = fmaxf(m_ref, m_tile);
+                const bool need = m_new > m_ref + kRescaleThreshold;
+                float alpha = 1.f;
+                if (need) {
+                    alpha = ex2(m_ref - m_new);  // m_ref = -inf -> 0
+                    l *= alpha;
+                    m_ref = m_new;
+                }
+                // ghost-row pin: while every key so far is masked, exponentiate against 0
+                const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+                const float neg_m = -m_use;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float p0 = ex2(fmaf(__uint_as_float(s[q4][2 * e]), c, neg_m));
+                        const float p1 = ex2(fmaf(__uint_as_float(s[q4][2 * e + 1]), c, neg_m));
+                        l += p0 + p1;
+                        packed[e] = pack2<kBF16>(p0, p1);
+                    }
+                    tmem_st_x16(tS + q4 * 16, packed);  // P overwrites the first 64 columns of S
+                }
+                // rescale the accumulator (the value product of the previous key tile
+                // has completed: its commit preceded this tile's score commit)
+                if (__any_sync(0xffffffffu, need) && jj > 0) {
+#pragma unroll
+                    for (int ch = 0; ch < D / 32; ++ch) {
+                        uint32_t o[32];
                         tmem_ld_x32(tO + ch * 32, o);
                         tmem_wait_ld_x32(o);
-                    } else {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = 0u;
-                    }
-                    uint32_t w[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        w[e] = pack2<kBF16>(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
-                    if (row < p.M) {
-                        uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
-#pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4)
-                            dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st_x32(tO + ch * 32, o);
                     }
                 }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar.p_full(t));
+            }
+            if (!ok) break;
+
+            // ---------------- epilogue: O / l, one cast, store rows < M ----------------
+            if (!(ok = wait_warp(bar.o_final, tc & 1, abort_flag, p.status))) break;
+            ++tc;
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;  // no visible key: output 0
+            uint32_t w16[D / 2];  // the row as packed 16-bit pairs
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) {
+                uint32_t o[32];
+                tmem_ld_x32(tO + ch * 32, o);
+                tmem_wait_ld_x32(o);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    w16[ch * 16 + e] = pack2<kBF16>(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+            }
+            // O_t may now take the next tile's first value product
+            tc_fence_before();
+            mbar_arrive(bar.o_free(t));
+            if (row < p.M) {
+                uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+                for (int v4 = 0; v4 < D / 8; ++v4)
+                    dst[v4] = make_uint4(w16[4 * v4], w16[4 * v4 + 1], w16[4 * v4 + 2], w16[4 * v4 + 3]);
             }
         }
     }
@@ -412,9 +469,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// ---------------------------------------------------------------------------
-// host side
-// ---------------------------------------------------------------------------
+int sm_count_prefill() {
+    static int n = 0;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+                                                      cudaSuccess)
+            n = 148;
+    });
+    return n;
+}
+
 template <int D, bool kBF16>
 int launch_t(const Problem& pr, const void* q, const void* k, const void* v, void* o, int* status,
              cudaStream_t stream) {
@@ -442,7 +508,10 @@ int launch_t(const Problem& pr, const void* q, const void* k, const void* v, voi
     pp.causal = pr.causal;
     pp.window = pr.window;
     pp.scale_log2 = pr.scale_log2;
-    dim3 grid(pr.B * pr.Hq, (pr.M + NQ * BM - 1) / (NQ * BM));
+    pp.BH = pr.B * pr.Hq;
+    pp.nqb = (pr.M + NQ * BM - 1) / (NQ * BM);
+    pp.tiles = pp.BH * pp.nqb;
+    const int grid = pp.tiles < sm_count_prefill() ? pp.tiles : sm_count_prefill();
     attn_prefill_kernel<D, kBF16><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, pp);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -450,7 +519,7 @@ int launch_t(const Problem& pr, const void* q, const void* k, const void* v, voi
 }  // namespace
 
 bool prefill_supported(const Problem& p) {
-    return (p.D == 64 || p.D == 128) && (p.M + NQ * BM - 1) / (NQ * BM) <= 65535;
+    return (p.D == 64 || p.D == 128) && (int64_t)p.B * p.Hq * ((p.M + NQ * BM - 1) / (NQ * BM)) < (1LL << 31);
 }
 
 int launch_prefill(const Problem& p, const void* q, const void* k, const void* v, void* o, int* status,

@@ -89,6 +89,22 @@ def test_mid_sizes_full_compare(shape, mask, D, dtype, path):
     check(run(q, k, v, causal, window, path), want, dtype, f"{shape} {mask} D={D} path={path}")
 
 
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("case", [(40, 8, 4, 600, 200, True, 0), (24, 16, 16, 384, 384, True, 0),
+                                  (20, 12, 3, 512, 700, False, 0), (30, 8, 8, 300, 900, True, 257)], ids=str)
+def test_prefill_many_work_tiles(case, D):
+    """More work tiles than SMs, so each persistent CTA walks several of them:
+    the K/V ring and barrier phases carry across tiles, and (first case) some
+    work tiles see no key at all (M > N causal) and are written as zeros."""
+    B, Hq, Hkv, M, N, causal, window = case
+    q, k, v = make_qkv(B, Hq, Hkv, M, N, D, torch.bfloat16, seed=B + M + N)
+    o = run(q, k, v, causal, window, sa.PATH_PREFILL)
+    rows = sample_rows(B, Hq, M, 400, seed=M)
+    want = oracle.attention_rows(q, k, v, rows, causal=causal, window=window)
+    assert torch.isfinite(o).all()
+    check(o.reshape(-1, D)[torch.tensor(rows, device=o.device)], want, torch.bfloat16, f"{case} D={D}")
+
+
 @pytest.mark.parametrize("D", [16, 32])
 @pytest.mark.parametrize("mask", [(False, 0), (True, 0), (True, 9)], ids=str)
 def test_small_head_dims_simt(D, mask):
