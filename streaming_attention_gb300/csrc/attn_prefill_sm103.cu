@@ -164,6 +164,24 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     return kBF16 ? pack_bf16(lo, hi) : pack_f16(lo, hi);
 }
 
+// MMA groups issued from precomputed descriptors: the issuing thread must
+// keep up with the tensor core (a 128x128x16 MMA retires in 64 cycles), so
+// each K step only adds a compile-time offset to a 64-bit descriptor.
+template <int D>
+__device__ __forceinline__ void mma_group_s(uint32_t d_tmem, uint64_t a0, uint64_t b0, uint32_t idesc) {
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off = (uint64_t)((((kk >> 2) * Cfg<D>::kChunkBytes) + (kk & 3) * 32) >> 4);
+        mma_ss(d_tmem, a0 + off, b0 + off, idesc, kk > 0 ? 1u : 0u);
+    }
+}
+__device__ __forceinline__ void mma_group_pv(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0, uint32_t idesc,
+                                             bool first) {
+#pragma unroll
+    for (int kk = 0; kk < BN / 16; ++kk)
+        mma_ts(d_tmem, a_tmem + kk * 8, b0 + (uint64_t)((kk * 16 * 128) >> 4), idesc, (first && kk == 0) ? 0u : 1u);
+}
+
 template <int D, bool kBF16>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -263,13 +281,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             int u = 0, tc = 0;
             int ps[NQ] = {0, 0};  // P tiles consumed per query tile, across the walk
             bool ok = true;
+            // descriptors: Q_0, Q_1, and ring slot 0 (K-major for K, MN-major for V);
+            // slot s adds s * kTileBytes to the 14-bit address field
+            const uint64_t dq0 = sw128_desc(sQ, 16, 1024);
+            const uint64_t dq1 = sw128_desc(sQ + C::kTileBytes, 16, 1024);
+            const uint64_t dk = sw128_desc(sKV, 16, 1024);
+            const uint64_t dv = sw128_desc(sKV, C::kChunkBytes, 1024);
+            constexpr uint64_t kSlotStep = (uint64_t)(C::kTileBytes >> 4);
             auto issue_s = [&](int t, int slot) {
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off_k = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-                    const uint64_t a = sw128_desc(sQ + t * C::kTileBytes + off_k, 16, 1024);
-                    const uint64_t bd = sw128_desc(sKV + slot * C::kTileBytes + off_k, 16, 1024);
-                    mma_ss(tmem + col_s(t), a, bd, idS, kk > 0 ? 1u : 0u);
-                }
+                mma_group_s<D>(tmem + col_s(t), t ? dq1 : dq0, dk + (uint64_t)slot * kSlotStep, idS);
             };
             // O_t += P_t V; the first product of a tile overwrites O_t, after the
             // previous tile's epilogue has read it out
@@ -278,10 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++ps[t];
                 if (first && tc > 0 && !wait_one(bar.o_free(t), (tc - 1) & 1, abort_flag, p.status)) return false;
                 tc_fence_after();
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t bd = sw128_desc(sKV + slot * C::kTileBytes + kk * 16 * 128, C::kChunkBytes, 1024);
-                    mma_ts(tmem + col_o(t), tmem + col_s(t) + kk * 8, bd, idPV, (first && kk == 0) ? 0u : 1u);
-                }
+                mma_group_pv(tmem + col_o(t), tmem + col_s(t), dv + (uint64_t)slot * kSlotStep, idPV, first);
                 return true;
             };
             Work wk;
