@@ -185,6 +185,10 @@ __global__ void __launch_bounds__(kDecThreads)
     // Let the merge grid launch now: its CTAs wait in griddepcontrol.wait, which
     // returns only after this whole grid has finished and its writes are visible.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // This grid is itself launched programmatically, so the kernel before it in
+    // the stream (which may have written Q, K or V, or still read the workspace)
+    // can still be running: the setup above touched no global memory; wait here.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp == kDecLoadWarp) {
         if (lane == 0 && T > 0) {
@@ -452,9 +456,19 @@ cudaError_t launch_decode_t(const Problem& pr, const void* q, const void* k, con
     dp.kbase = split_base(pr);
     dp.chunk = chunk;
     dp.S = S;
-    dim3 grid(S, pr.B * pr.Hkv);
-    attn_decode_kernel<kBF16, RP><<<grid, kDecThreads, kDecSmem, stream>>>(tq, tk, tv, dp);
-    return cudaGetLastError();
+    // Programmatic launch: CTAs may start their setup (barriers, TMEM) while the
+    // previous kernel in the stream drains; griddepcontrol.wait orders the rest.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(S, pr.B * pr.Hkv);
+    cfg.blockDim = dim3(kDecThreads);
+    cfg.dynamicSmemBytes = kDecSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_decode_kernel<kBF16, RP>, tq, tk, tv, dp);
 }
 
 }  // namespace

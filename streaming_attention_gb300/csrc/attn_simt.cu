@@ -175,6 +175,9 @@ __global__ void __launch_bounds__(kMergeThreads)
     attn_merge_kernel(const float* __restrict__ m, const float* __restrict__ l, const float* __restrict__ acc,
                       void* o, float* m_out, float* l_out, int rows, int S, int D, int out_dtype, float unit,
                       int programmatic) {
+    // A programmatically launched successor (the next decode split grid) may start
+    // its setup now; it waits for this grid's completion before touching memory.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (programmatic) asm volatile("griddepcontrol.wait;" ::: "memory");
     const size_t idx = (size_t)blockIdx.x * kMergeThreads + threadIdx.x;
     const size_t row = idx / D;
