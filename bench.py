@@ -33,7 +33,11 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-from streaming_attention_gb300.inputs import DECODE_GQA, PREFILL_D128, WORKLOADS, workload_inputs  # noqa: E402
+from streaming_attention_gb300.inputs import (  # noqa: E402
+    DECODE_GQA, LONG_CAUSAL, PREFILL_D64, PREFILL_D128, WORKLOADS, workload_inputs)
+
+# the D=128 prefill shape in FP16 (same seed and sizes)
+FP16_D128 = PREFILL_D128.with_(dtype=torch.float16, name="prefill_b2_h32_4096x4096_d128_fp16_causal")
 
 METRIC = "attention fwd TFLOP/s (decode: GB/s) and % of GB300 roofline, 1 GPU"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -104,6 +108,13 @@ def max_over_ranks(x: float, world: int, device) -> float:
     t = torch.tensor([x], dtype=torch.float64, device=device)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job(work_per_rank, ms_per_step, world, device, scale):
+    """(slowest rank's ms per step, whole-job throughput): every rank does the
+    same work per step, so the job's rate is world x work over the slowest rank."""
+    ms_max = max_over_ranks(ms_per_step, world, device)
+    return ms_max, world * work_per_rank / (ms_max * 1e-3) / scale
 
 
 # ----------------------------------------------------------------------------
@@ -329,8 +340,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier(world)
     clocks = clk.summary()
-    ms_max = max_over_ranks(ms, world, dev)
-    value = world * work / (ms_max * 1e-3) / scale
+    ms_max, value = whole_job(work, ms, world, dev, scale)
     status = sa.last_device_status()
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
@@ -430,8 +440,12 @@ def extra_measurements(args, dev, stream, flush):
     out = {}
     steps = max(3, min(args.steps, 10))
     for name, w, causal in (("prefill_d128_bf16_noncausal", PREFILL_D128, False),
+                            ("prefill_d128_fp16_causal", FP16_D128, True),
+                            ("prefill_d64_bf16_noncausal", PREFILL_D64, False),
+                            ("prefill_d64_bf16_causal", PREFILL_D64, True),
+                            ("long_causal_16k_fp16", LONG_CAUSAL, True),
                             ("decode_gqa", DECODE_GQA, DECODE_GQA.causal)):
-        if name.startswith("prefill") and args.workload != PREFILL_D128.name:
+        if name.startswith(("prefill", "long")) and args.workload != PREFILL_D128.name:
             continue
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size
         _, sets, _ = rotation(w, dev, l2)

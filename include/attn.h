@@ -7,7 +7,8 @@
  * carries a running (m, l, acc) state per row and never forms the full score
  * matrix ("Intermediate and advanced kernel workshops", table "Scope and
  * contracts", streaming_attention.attention row; answer key, central-idea
- * table, A3 row: carry (m, l, a) while multiplying one score tile at a time).
+ * table, A3 row: each row keeps a running (m, l, a), and only one tile of scores
+ * exists at any time).
  *
  * Conventions shared by every entry point:
  *   Layout      Q and O are [B, Hq, M, D]; K and V are [B, Hkv, N, D]; all
@@ -17,7 +18,7 @@
  *   GQA         query head h reads KV head g = h / (Hq / Hkv); Hq % Hkv == 0.
  *   Positions   query row i sits at key position p_i = i + N - M
  *               (bottom-right alignment; with M == N it is the pages' rule).
- *   causal      != 0 keeps keys j <= p_i (diagonal included, as on the pages).
+ *   causal      != 0 keeps keys j <= p_i (a row sees its own position).
  *   window      W > 0 keeps keys j > p_i - W (the W keys ending at p_i);
  *               W <= 0 disables it.
  *   scale       multiplies the logits; 0.0f selects the pages' 1/sqrt(D).

@@ -10,7 +10,7 @@
  * that the streaming method reaches (up to rounding order):
  *   "Intermediate and advanced kernel workshops", table "Scope and contracts"
  *     (streaming_attention.attention row): softmax(scale * Q K^T) V with
- *     scale = 1/sqrt(D) and the diagonal included when causal;
+ *     scale = 1/sqrt(D), and a causal row also sees the key at its own position;
  *   "Compare reasoning after your own attempt" (answer key), section
  *     "Reference tradeoffs to challenge": the attention oracle materializes
  *     FP64 scores, outside the timed call.
@@ -28,9 +28,10 @@
  *   - a row with no allowed key outputs 0 (never NaN).
  *
  * The summary merge (oracle_merge_f64) follows the answer key's A1 row and
- * its worked answer ("merging (2,2) and (4,1) yields (4,1+2*exp(-2))"): both
- * summaries are re-expressed relative to the common maximum; (-inf, 0) is the
- * empty summary and merging two empties must not form -inf - (-inf).
+ * its A1 worked answer (the summaries (2,2) and (4,1) combine to
+ * (4, 1 + 2 e^-2)): both summaries are rescaled to the larger of the two
+ * maxima before they are added; (-inf, 0) is the empty summary, and merging
+ * two empties must not form -inf - (-inf).
  *
  * ORACLE_MUTANT=<n> compiles a deliberately wrong variant; it exists only so
  * that the pin tests can show that each planted mistake is caught.
@@ -294,7 +295,7 @@ void oracle_merge_f64(int S, int D, const double* m, const double* l, const doub
         double wt = (m[t] == -INFINITY) ? 0.0 : exp(m[t] - mn);
 #endif
 #if ORACLE_MUTANT == 9
-        lc = lc + l[t]; /* planted: raw denominator addition */
+        lc = lc + l[t]; /* planted: sums the denominators without rescaling */
         (void)wc;
 #else
         lc = lc * wc + l[t] * wt;

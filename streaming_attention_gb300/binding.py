@@ -135,7 +135,7 @@ def attn_fwd_ex(q, k, v, o, causal=False, window=0, scale=0.0, path=PATH_AUTO, w
 
 
 def attention(q, k, v, causal=False, window=0, scale=0.0, path=PATH_AUTO, stream=None) -> torch.Tensor:
-    """Allocates a fresh contiguous output on q's device and runs the forward."""
+    """Makes a new contiguous output tensor on q's device, then runs the forward into it."""
     o = torch.empty_like(q)
     if path == PATH_AUTO:
         attn_fwd(q, k, v, o, causal, window, scale, stream)

@@ -2,7 +2,7 @@
 // chunks of whole 128-key tiles; each chunk's partial (m, l, acc) summaries
 // go to the workspace, and the merge kernel combines them on the same stream
 // ("Compare reasoning after your own attempt", central-idea table, A2 row:
-// partial stats, rescaled merge, same-stream order).
+// each split's statistics are combined after rescaling; the stream orders the kernels).
 //
 // D = 128 with at most 16 grouped query rows per KV head runs the tcgen05
 // split kernel; other shapes run the SIMT kernel in split mode.

@@ -247,6 +247,42 @@ def pin_gqa_map(orc):
     assert np.allclose(o[0, 2], 2.0) and np.allclose(o[0, 3], 2.0)
 
 
+# --------------------------------------------------------------------------
+# Row sampling and the weight vector against the same torch float64 formula
+# --------------------------------------------------------------------------
+def library_weights(q, k, causal, window, scale):
+    """softmax(scale Q K^T + mask) with torch float64 routines, [B, Hq, M, N]."""
+    q, k = (torch.from_numpy(np.asarray(x)) for x in (q, k))
+    B, Hq, M, D = q.shape
+    Hkv, N = k.shape[1], k.shape[2]
+    k = k.repeat_interleave(Hq // Hkv, dim=1)
+    keep = torch.ones(M, N, dtype=torch.bool)
+    if causal:
+        keep &= torch.ones(M, N, dtype=torch.bool).tril(diagonal=N - M)
+    if window > 0:
+        keep &= torch.ones(M, N, dtype=torch.bool).triu(diagonal=N - M - window + 1)
+    s = (torch.matmul(q, k.transpose(-1, -2)) * scale).masked_fill(~keep, float("-inf"))
+    return torch.nan_to_num(torch.softmax(s, dim=-1), nan=0.0).numpy()
+
+
+def pin_rows_and_weights(orc):
+    rng = np.random.default_rng(17)
+    for trial in range(12):
+        Hkv = int(rng.integers(1, 3))
+        Hq = Hkv * int(rng.integers(1, 4))
+        B, M, N, D = int(rng.integers(1, 3)), int(rng.integers(1, 7)), int(rng.integers(1, 9)), 4
+        causal, window = bool(rng.integers(0, 2)), int(rng.choice([0, 2, 3]))
+        q, k, v = _rand((B, Hq, M, D), 400 + trial), _rand((B, Hkv, N, D), 500 + trial), _rand((B, Hkv, N, D), 600 + trial)
+        scale = 1.0 / math.sqrt(D)
+        want_o = library_attention(q, k, v, causal, window, scale).reshape(-1, D)
+        want_w = library_weights(q, k, causal, window, scale).reshape(-1, N)
+        rows = rng.integers(0, B * Hq * M, 7)
+        got = orc.attention_rows(q, k, v, rows, causal=causal, window=window)
+        assert np.allclose(got, want_o[rows], rtol=1e-12, atol=1e-12)
+        for r in rows:
+            assert np.allclose(orc.weights(q, k, int(r), causal, window), want_w[r], rtol=1e-12, atol=1e-14)
+
+
 ALL_PINS = [
     pin_a3_worked_example,
     pin_a1_merge_example,
@@ -257,4 +293,5 @@ ALL_PINS = [
     pin_invariants,
     pin_closed_forms,
     pin_gqa_map,
+    pin_rows_and_weights,
 ]

@@ -1,0 +1,62 @@
+"""The multi-rank side of bench.py on CPU: two gloo ranks (no GPU), checking
+the barrier, the max over ranks of the step time and the whole-job value."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    import bench
+
+    r, local, w = bench.dist_env()
+    assert (r, local, w) == (rank, rank, world)
+    bench.dist_init(w, "gloo")
+    bench.barrier(w)
+    ms = 2.0 + rank  # rank 1 is the slower one
+    ms_max, value = bench.whole_job(1e9, ms, w, torch.device("cpu"), 1e9)
+    out[rank] = (ms_max, value)
+    bench.barrier(w)
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_the_slowest_step():
+    world = 2
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as mgr:
+        out = mgr.dict()
+        procs = [ctx.Process(target=_rank_main, args=(r, world, port, out)) for r in range(world)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(120)
+        for p in procs:
+            if p.is_alive():
+                p.kill()
+                pytest.fail("a rank did not finish")
+            assert p.exitcode == 0
+        res = dict(out)
+    # both ranks see the slower rank's 3 ms; 2 ranks x 1 GB each per 3 ms = 666.7 GB/s
+    for r in range(world):
+        ms_max, value = res[r]
+        assert ms_max == pytest.approx(3.0)
+        assert value == pytest.approx(2 * 1e9 / 3e-3 / 1e9)
+
+
+def test_single_rank_needs_no_process_group():
+    import bench
+
+    ms_max, value = bench.whole_job(5e12, 10.0, 1, torch.device("cpu"), 1e12)
+    assert ms_max == 10.0 and value == pytest.approx(500.0)

@@ -17,7 +17,7 @@ def test_pin(pin, oracle_lib):
 
 def _stream(logits, values, tile, rescale_numerator=True):
     """Running (m, l, a) over key tiles, as the A3 row of the answer key
-    describes; with rescale_numerator=False it reproduces the missing-alpha bug."""
+    describes; with rescale_numerator=False it reproduces the unrescaled-accumulator mistake."""
     m, l, a = -math.inf, 0.0, 0.0
     for t0 in range(0, len(logits), tile):
         s = logits[t0:t0 + tile]
@@ -48,7 +48,7 @@ MUTANTS = {
     6: "scale dropped",
     7: "K read transposed",
     8: "last head dimension dropped",
-    9: "merge adds raw denominators",
+    9: "merge sums denominators without rescaling",
     10: "merge without the empty guard",
 }
 

@@ -53,7 +53,7 @@ def test_empty_dims(path):
 @pytest.mark.parametrize("path", [sa.PATH_SIMT, sa.PATH_PREFILL, sa.PATH_DECODE], ids=PATH_NAMES.get)
 def test_a3_worked_example_across_tiles(path):
     """The answer key's A3 example (logits 0, 0, ln 2 over values 1, 3, 10 give
-    6; the missing-alpha bug gives 7) at D=64, with the ln 2 key in the second
+    6; leaving the accumulator unrescaled gives 7) at D=64, with the ln 2 key in the second
     128-key tile so that the running maximum rises in a later tile. Filler keys
     score -80 and carry value 0."""
     D, N = 64, 129
