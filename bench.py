@@ -465,7 +465,48 @@ def extra_measurements(args, dev, stream, flush):
             out[name] = {"TFLOP/s": round(flops(w, causal) / (ms * 1e-3) / 1e12, 2), "us": round(ms * 1e3, 1),
                          "cold_call_us": round(cold * 1e3, 1), "path": pname}
         del sets, ws
+    if args.workload in (PREFILL_D128.name, DECODE_GQA.name):
+        for ps in (16, 128):
+            out[f"decode_gqa_paged{ps}"] = paged_decode_measure(DECODE_GQA, ps, steps, dev, stream, flush)
     return out
+
+
+def paged_decode_measure(w, page_size, steps, dev, stream, flush):
+    """The decode workload with its cache cut into pages of `page_size` keys,
+    stored in a shuffled order in the pool (attn_decode_paged)."""
+    import numpy as np
+
+    import streaming_attention_gb300 as sa
+
+    q, k, v = workload_inputs(w)
+    npg = w.N // page_size
+    perm = torch.from_numpy(np.random.default_rng(w.seed).permutation(w.B * npg))
+
+    def pool(x):  # [B, Hkv, N, D] -> [B * npg, Hkv, page_size, D], page i stored at slot perm[i]
+        pg = x.reshape(w.B, w.Hkv, npg, page_size, w.D).permute(0, 2, 1, 3, 4).reshape(w.B * npg, w.Hkv,
+                                                                                   page_size, w.D)
+        out = torch.empty_like(pg)
+        out[perm] = pg
+        return out
+
+    table = perm.reshape(w.B, npg).to(torch.int32)
+    per_set = 2 * q.numel() * 2 + 2 * k.numel() * 2
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    r = max(2, min(8, math.ceil(3 * l2 / per_set) + 1))
+    kp, vp = pool(k), pool(v)
+    sets = [(q.to(dev), kp.to(dev), vp.to(dev), torch.empty_like(q, device=dev)) for _ in range(r)]
+    td = table.to(dev)
+    lens = torch.full((w.B,), w.N, dtype=torch.int32, device=dev)
+    nb = sa.attn_decode_paged_workspace_bytes(w.B, w.Hq, w.Hkv, w.M, w.D, page_size, npg, w.N, w.causal, w.window)
+    ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
+
+    def fn_on(t, st):
+        sa.attn_decode_paged(t[0], t[1], t[2], td, lens, t[3], w.N, w.causal, w.window, 0.0, ws, st)
+
+    ms = time_steady(fn_on, sets, steps, 3, stream)
+    cold = statistics.median(time_graph(lambda st: fn_on(sets[0], st), steps, 3, flush))
+    return {"GB/s": round(decode_bytes(w) / (ms * 1e-3) / 1e9, 1), "us": round(ms * 1e3, 2),
+            "cold_call_us": round(cold * 1e3, 2), "path": f"paged decode, {page_size}-key pages, shuffled pool"}
 
 
 # ----------------------------------------------------------------------------

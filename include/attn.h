@@ -170,6 +170,51 @@ ATTN_API int attn_fwd_decode_noalloc(const void* q, const void* k, const void* v
                                      int B, int Hq, int Hkv, int M, int N, int D,
                                      int causal, int window, float scale, int dtype, void* stream);
 
+/* Split-KV decode over a PAGED KV cache: the KV-cache slice of the course's
+ * plan ("Kernel Notes & Checklist", section 3, the plan, week +3: sliding
+ * window + GQA + KV-cache slice). Each sequence b attends over its own first
+ * L_b = min(seq_lens[b], max_pages * page_size, max_seq_len) keys, with the
+ * conventions above (positions p_i = i + L_b - M, causal, window, GQA), so
+ * the result equals attn_fwd on sequence b's keys gathered into a contiguous
+ * [1, Hkv, L_b, D] cache.
+ *   q, o        device [B, Hq, M, D], dtype, 16-byte aligned; M query rows per
+ *               sequence (1 for decode, more for speculative decode).
+ *   k_pages,    device pools [num_pages, Hkv, page_size, D], dtype, 16-byte
+ *   v_pages     aligned: page n holds page_size consecutive keys of every KV
+ *               head, each head's rows contiguous (the same head-major layout
+ *               as k and v of attn_fwd). A contiguous [B, Hkv, Nmax, D] cache
+ *               is the special case page_size = Nmax, max_pages = 1,
+ *               block_table[b] = b.
+ *   block_table device int32 [B, max_pages], 4-byte aligned: key j of
+ *               sequence b is row j % page_size of page
+ *               block_table[b * max_pages + j / page_size]. Only the entries
+ *               of pages holding the first L_b keys are read; they must lie in
+ *               [0, num_pages) (an entry outside reads a page of zeros: no
+ *               fault, but a wrong result).
+ *   seq_lens    device int32 [B], 4-byte aligned (negative counts as 0).
+ *   page_size   16, 32, 64 or a multiple of 128.
+ *   max_seq_len a host-side bound of the seq_lens values: it sizes the split
+ *               plan; keys past it are ignored.
+ *   D must be 128 (ATTN_ERR_HEADDIM) and (Hq/Hkv) * M at most 16
+ *   (ATTN_ERR_PATH); B * Hkv <= 65535.
+ *   Every element of a page that a sequence uses must be finite, also in the
+ *   rows of its last page past L_b: masked keys get probability 0, and their
+ *   value rows are still multiplied by it.
+ *   workspace: device memory of attn_decode_paged_workspace_bytes(...) bytes,
+ *   16-byte aligned; NULL makes the call allocate it stream-ordered
+ *   (cudaMallocAsync / cudaFreeAsync on `stream`), as attn_fwd does.
+ *   When num_pages == 0 or min(max_seq_len, max_pages * page_size) == 0, o is
+ *   zero-filled. */
+ATTN_API size_t attn_decode_paged_workspace_bytes(int B, int Hq, int Hkv, int M, int D,
+                                                  int page_size, int max_pages, int max_seq_len,
+                                                  int causal, int window);
+ATTN_API int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                               const int* block_table, const int* seq_lens, void* o,
+                               int B, int Hq, int Hkv, int M, int D,
+                               int num_pages, int page_size, int max_pages, int max_seq_len,
+                               int causal, int window, float scale, int dtype,
+                               void* workspace, size_t ws_bytes, void* stream);
+
 /* Human-readable text for a status code (static storage). */
 ATTN_API const char* attn_strerror(int status);
 

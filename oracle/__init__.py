@@ -158,6 +158,30 @@ class Oracle:
             raise ValueError(f"oracle_partial_f64 rejected the call (rc={rc})")
         return float(m[0]), float(l[0]), acc
 
+    def attention_paged(self, q, k_pages, v_pages, block_table, seq_lens, max_seq_len, causal=True, window=0,
+                        scale=None, nthreads=0) -> np.ndarray:
+        """Decode over a paged KV cache, by its definition: gather each
+        sequence's first L_b keys out of the pages into a contiguous cache,
+        then take the plain attention of that sequence's rows over them.
+        q [B, Hq, M, D]; pools [num_pages, Hkv, page_size, D]; block_table
+        [B, max_pages]; L_b = clamp(seq_lens[b], 0, min(max_seq_len,
+        max_pages * page_size)). Returns [B, Hq, M, D] in FP64."""
+        q, kp, vp = _f64(q), _f64(k_pages), _f64(v_pages)
+        table = np.asarray(block_table, dtype=np.int64)
+        lens = np.asarray(seq_lens, dtype=np.int64).reshape(-1)
+        B, Hq, M, D = q.shape
+        num_pages, Hkv, page_size, _ = kp.shape
+        cap = min(int(max_seq_len), table.shape[1] * page_size)
+        o = np.zeros((B, Hq, M, D), dtype=np.float64)
+        for b in range(B):
+            L = int(min(max(lens[b], 0), cap))
+            j = np.arange(L)
+            pages, rows = table[b, j // page_size], j % page_size
+            kb = np.ascontiguousarray(kp[pages, :, rows, :].transpose(1, 0, 2))[None]  # [1, Hkv, L, D]
+            vb = np.ascontiguousarray(vp[pages, :, rows, :].transpose(1, 0, 2))[None]
+            o[b] = self.attention(q[b:b + 1], kb, vb, causal, window, scale, nthreads)[0]
+        return o
+
     def merge(self, m, l, acc):
         """Merge S summaries: m[S], l[S], acc[S, D] -> (m, l, acc[D])."""
         m = np.ascontiguousarray(np.asarray(m, dtype=np.float64).reshape(-1))
@@ -190,6 +214,12 @@ def attention_rows(q, k, v, rows, causal=False, window=0, scale=None, nthreads=0
 
 def merge(m, l, acc):
     return default().merge(m, l, acc)
+
+
+def attention_paged(q, k_pages, v_pages, block_table, seq_lens, max_seq_len, causal=True, window=0, scale=None,
+                    nthreads=0):
+    return default().attention_paged(q, k_pages, v_pages, block_table, seq_lens, max_seq_len, causal, window,
+                                     scale, nthreads)
 
 
 def cpu_threads() -> int:

@@ -15,7 +15,10 @@ from .binding import (  # noqa: F401
     PATH_SIMT,
     AttnError,
     attention,
+    attn_decode_paged,
+    attn_decode_paged_workspace_bytes,
     attn_fwd,
+    attn_fwd_decode_noalloc,
     attn_fwd_ex,
     attn_fwd_host,
     attn_merge,

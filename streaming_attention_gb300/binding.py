@@ -62,6 +62,10 @@ def lib() -> ctypes.CDLL:
             L.attn_last_device_status.restype = ci
             L.attn_fwd_decode_noalloc.argtypes = [vp, vp, vp, vp] + [ci] * 8 + [cf, ci, vp]
             L.attn_fwd_decode_noalloc.restype = ci
+            L.attn_decode_paged_workspace_bytes.argtypes = [ci] * 10
+            L.attn_decode_paged_workspace_bytes.restype = sz
+            L.attn_decode_paged.argtypes = [vp] * 6 + [ci] * 11 + [cf, ci, vp, sz, vp]
+            L.attn_decode_paged.restype = ci
             L.attn_version.argtypes = []
             L.attn_version.restype = ci
             _lib = L
@@ -178,6 +182,46 @@ def attn_fwd_decode_noalloc(q, k, v, o, causal=False, window=0, scale=0.0, strea
     st = lib().attn_fwd_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, Hq, Hkv, M, N, D, int(bool(causal)),
                                        int(window), float(scale or 0.0), _DTYPES[q.dtype], _stream(stream))
     _check(st, "attn_fwd_decode_noalloc")
+
+
+def _paged_dims(q, k_pages, v_pages, block_table, seq_lens, o):
+    if q.dim() != 4 or k_pages.dim() != 4 or tuple(v_pages.shape) != tuple(k_pages.shape):
+        raise ValueError("q is [B, Hq, M, D]; k_pages and v_pages are [num_pages, Hkv, page_size, D]")
+    B, Hq, M, D = q.shape
+    num_pages, Hkv, page_size, Dk = k_pages.shape
+    if Dk != D or (o is not None and tuple(o.shape) != tuple(q.shape)):
+        raise ValueError("head dimensions or output shape do not match")
+    if block_table.dim() != 2 or block_table.shape[0] != B or block_table.dtype != torch.int32:
+        raise ValueError("block_table must be int32 [B, max_pages]")
+    if seq_lens.shape != (B,) or seq_lens.dtype != torch.int32:
+        raise ValueError("seq_lens must be int32 [B]")
+    for t in (q, k_pages, v_pages, block_table, seq_lens) + ((o,) if o is not None else ()):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    if k_pages.dtype != q.dtype or v_pages.dtype != q.dtype or (o is not None and o.dtype != q.dtype):
+        raise ValueError("q, k_pages, v_pages, o must share one dtype")
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("dtype must be bfloat16 or float16")
+    return B, Hq, Hkv, M, D, num_pages, page_size, block_table.shape[1]
+
+
+def attn_decode_paged_workspace_bytes(B, Hq, Hkv, M, D, page_size, max_pages, max_seq_len, causal=True,
+                                      window=0) -> int:
+    return int(lib().attn_decode_paged_workspace_bytes(B, Hq, Hkv, M, D, page_size, max_pages, max_seq_len,
+                                                       int(bool(causal)), int(window)))
+
+
+def attn_decode_paged(q, k_pages, v_pages, block_table, seq_lens, o, max_seq_len, causal=True, window=0,
+                      scale=0.0, workspace=None, stream=None) -> None:
+    """C-ABI ``attn_decode_paged``: decode over a paged KV cache; writes ``o`` in place.
+    ``workspace`` None lets the library allocate it stream-ordered."""
+    B, Hq, Hkv, M, D, num_pages, page_size, max_pages = _paged_dims(q, k_pages, v_pages, block_table, seq_lens, o)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().attn_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seq_lens),
+                                 _ptr(o), B, Hq, Hkv, M, D, num_pages, page_size, max_pages, int(max_seq_len),
+                                 int(bool(causal)), int(window), float(scale or 0.0), _DTYPES[q.dtype],
+                                 _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "attn_decode_paged")
 
 
 def last_device_status(stream=None) -> int:

@@ -64,6 +64,18 @@ struct DecodeParams {
     int causal, window;
     float scale_log2;
     int klo, khi, kbase, chunk, S;
+    // paged KV cache: K/V pools [pages][Hkv][page_size][D]; sequence b's key j is
+    // row j % page_size of page block_table[b][j / page_size]; b holds seq_lens[b] keys
+    const int* block_table;
+    const int* seq_lens;
+    int page_size, max_pages, max_len;
+    int oob_z;  // a pool coordinate past its last (page, head): TMA reads zeros there
+};
+
+// Keys of one CTA's sequence: its length and the union [klo, khi) of the
+// ranges its M query rows may see; splits start at kbase (a tile boundary).
+struct SeqRange {
+    int N, klo, khi, kbase;
 };
 
 __device__ bool dwait_one(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag, int* status,
@@ -121,7 +133,8 @@ __device__ __forceinline__ int ring_pos_k(int j) { return j == 0 ? 0 : 2 * j - 1
 __device__ __forceinline__ int ring_pos_v(int j, int T) { return j == T - 1 ? 2 * T - 1 : 2 * j + 2; }
 
 // RP: grouped rows handled by the softmax (R <= RP <= 16); the MMA always uses N = 16.
-template <bool kBF16, int RP>
+// kPaged: K/V come from a paged pool through a block table, with a length per sequence.
+template <bool kBF16, int RP, bool kPaged>
 __global__ void __launch_bounds__(kDecThreads)
     attn_decode_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
@@ -147,9 +160,6 @@ __global__ void __launch_bounds__(kDecThreads)
     const int grp = blockIdx.y;  // b * Hkv + g
     const int b = grp / p.Hkv, g = grp % p.Hkv;
     const int row_base = (b * p.Hq + g * p.G) * p.M;  // first global row of the group
-    const int k0 = p.kbase + split * p.chunk;         // tile-aligned start of this split
-    const int kend = min(k0 + p.chunk, p.khi);
-    const int T = kend > max(k0, p.klo) ? (kend - k0 + DBN - 1) / DBN : 0;
 
     if (threadIdx.x == 0) {
         mbar_init(bar_q, 1);
@@ -190,8 +200,23 @@ __global__ void __launch_bounds__(kDecThreads)
     // can still be running: the setup above touched no global memory; wait here.
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
+    SeqRange sq{p.N, p.klo, p.khi, p.kbase};
+    if constexpr (kPaged) {
+        // lengths are clamped to what the block table and the split plan cover
+        sq.N = min(max(__ldg(p.seq_lens + b), 0), p.max_len);
+        int lo0, hi0, lo1, hi1;
+        key_range(sq.N - p.M, sq.N, p.causal, p.window, &lo0, &hi0);
+        key_range(sq.N - 1, sq.N, p.causal, p.window, &lo1, &hi1);
+        sq.klo = lo0;
+        sq.khi = max(hi1, lo0);
+        sq.kbase = (lo0 / DBN) * DBN;
+    }
+    const int k0 = sq.kbase + split * p.chunk;  // tile-aligned start of this split
+    const int kend = min(k0 + p.chunk, sq.khi);
+    const int T = kend > max(k0, sq.klo) ? (kend - k0 + DBN - 1) / DBN : 0;
+
     if (warp == kDecLoadWarp) {
-        if (lane == 0 && T > 0) {
+        if (!kPaged && lane == 0 && T > 0) {
             prefetch_tmap(&tmQ);
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
@@ -215,6 +240,66 @@ __global__ void __launch_bounds__(kDecThreads)
             dwait_one(bar_q, 0, abort_flag, p.status, false);
             for (int u = max(0, issued - kSlots); u < issued; ++u)
                 dwait_one(bar_full0 + 8 * (u % kSlots), (u / kSlots) & 1, abort_flag, p.status, false);
+        } else if (kPaged && T > 0) {
+            // The whole warp: lane i < nsub copies the i-th page-sized piece of
+            // each tile (one box per page, or per 128 rows of a larger page), so
+            // the small boxes of small pages are issued in parallel. A lane
+            // loads its page number one K tile ahead and keeps it for the V
+            // tile (3 ring positions later). Keys past the sequence and bad
+            // page numbers read a coordinate outside the pool: TMA fills zeros.
+            if (lane == 0) {
+                prefetch_tmap(&tmQ);
+                prefetch_tmap(&tmK);
+                prefetch_tmap(&tmV);
+                mbar_arrive_expect_tx(bar_q, kQBytes);
+                for (int c = 0; c < 2; ++c) tma_load_3d(sQ + c * kQChunk, &tmQ, c * 64, row_base, 0, bar_q);
+            }
+            const int sub = min(p.page_size, DBN), nsub = DBN / sub;
+            const int npages = p.oob_z / p.Hkv;
+            auto page_of = [&](int tile) {
+                const int key = k0 + tile * DBN + lane * sub;
+                return (lane < nsub && key < sq.N)
+                           ? __ldg(p.block_table + (size_t)b * p.max_pages + key / p.page_size)
+                           : -1;
+            };
+            int pf = page_of(0), e0 = -1, e1 = -1;
+            int issued = 0;
+            for (int u = 0; u < 2 * T; ++u) {
+                const int s = u % kSlots;
+                int ok = 1;
+                if (u >= kSlots && lane == 0)
+                    ok = dwait_one(bar_empty0 + 8 * s, ((u / kSlots) - 1) & 1, abort_flag, p.status) ? 1 : 0;
+                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+                bool is_v;
+                int tile;
+                ring_item(u, T, &is_v, &tile);
+                if (!is_v) {
+                    if (tile & 1)
+                        e1 = pf;
+                    else
+                        e0 = pf;
+                    if (tile + 1 < T) pf = page_of(tile + 1);
+                }
+                const int page = (tile & 1) ? e1 : e0;
+                if (lane == 0) mbar_arrive_expect_tx(bar_full0 + 8 * s, kTileBytes);
+                __syncwarp();
+                if (lane < nsub) {
+                    const CUtensorMap* tm = is_v ? &tmV : &tmK;
+                    const int key = k0 + tile * DBN + lane * sub;
+                    const bool in = key < sq.N && page >= 0 && page < npages;
+                    const int y = in ? key % p.page_size : 0;
+                    const int z = in ? page * p.Hkv + g : p.oob_z;
+                    const uint32_t dst = sRing + s * kTileBytes + lane * sub * 128;
+                    for (int c = 0; c < 2; ++c)
+                        tma_load_3d(dst + c * kChunkBytes, tm, c * 64, y, z, bar_full0 + 8 * s);
+                }
+                issued = u + 1;
+            }
+            if (lane == 0) {
+                dwait_one(bar_q, 0, abort_flag, p.status, false);
+                for (int u = max(0, issued - kSlots); u < issued; ++u)
+                    dwait_one(bar_full0 + 8 * (u % kSlots), (u / kSlots) & 1, abort_flag, p.status, false);
+            }
         }
     } else if (warp == kDecMmaWarp) {
         if (lane == 0 && T > 0) {
@@ -268,7 +353,7 @@ __global__ void __launch_bounds__(kDecThreads)
 #pragma unroll
         for (int r = 0; r < RP; ++r) {
             const int i = r % p.M;
-            key_range(i + p.N - p.M, p.N, p.causal, p.window, &lo[r], &hi[r]);
+            key_range(i + sq.N - p.M, sq.N, p.causal, p.window, &lo[r], &hi[r]);
             if (r >= p.R) hi[r] = lo[r];  // padding rows see nothing: their scores are -inf, p = 0
         }
         float m_ref[RP], l_part[RP];
@@ -422,22 +507,28 @@ int sm_count() {
     return n;
 }
 
-template <bool kBF16, int RP>
-cudaError_t launch_decode_t(const Problem& pr, const void* q, const void* k, const void* v, int chunk, int S,
-                            const SplitWorkspace& ws, int* status, cudaStream_t stream) {
+template <bool kBF16, int RP, bool kPaged>
+cudaError_t launch_decode_t(const Problem& pr, const void* q, const void* k, const void* v, const PagedKV* kv,
+                            int chunk, int S, const SplitWorkspace& ws, int* status, cudaStream_t stream) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(attn_decode_kernel<kBF16, RP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        kDecSmem);
+        attr_err = cudaFuncSetAttribute(attn_decode_kernel<kBF16, RP, kPaged>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
     });
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap tq, tk, tv;
-    if (!make_tensor_map(&tq, q, DD, pr.B * pr.Hq * pr.M, 1, DNR, kBF16) ||
-        !make_tensor_map(&tk, k, DD, pr.N, pr.B * pr.Hkv, DBN, kBF16) ||
-        !make_tensor_map(&tv, v, DD, pr.N, pr.B * pr.Hkv, DBN, kBF16))
+    if (!make_tensor_map(&tq, q, DD, pr.B * pr.Hq * pr.M, 1, DNR, kBF16)) return cudaErrorInvalidValue;
+    if (kPaged) {
+        const int box = kv->page_size < DBN ? kv->page_size : DBN;
+        if (!make_tensor_map(&tk, kv->k_pages, DD, kv->page_size, kv->num_pages * pr.Hkv, box, kBF16) ||
+            !make_tensor_map(&tv, kv->v_pages, DD, kv->page_size, kv->num_pages * pr.Hkv, box, kBF16))
+            return cudaErrorInvalidValue;
+    } else if (!make_tensor_map(&tk, k, DD, pr.N, pr.B * pr.Hkv, DBN, kBF16) ||
+               !make_tensor_map(&tv, v, DD, pr.N, pr.B * pr.Hkv, DBN, kBF16)) {
         return cudaErrorInvalidValue;
-    DecodeParams dp;
+    }
+    DecodeParams dp = {};
     dp.ws_m = ws.m;
     dp.ws_l = ws.l;
     dp.ws_acc = ws.acc;
@@ -456,6 +547,14 @@ cudaError_t launch_decode_t(const Problem& pr, const void* q, const void* k, con
     dp.kbase = split_base(pr);
     dp.chunk = chunk;
     dp.S = S;
+    if (kPaged) {
+        dp.block_table = kv->block_table;
+        dp.seq_lens = kv->seq_lens;
+        dp.page_size = kv->page_size;
+        dp.max_pages = kv->max_pages;
+        dp.max_len = kv->max_len;
+        dp.oob_z = kv->num_pages * pr.Hkv;
+    }
     // Programmatic launch: CTAs may start their setup (barriers, TMEM) while the
     // previous kernel in the stream drains; griddepcontrol.wait orders the rest.
     cudaLaunchConfig_t cfg = {};
@@ -468,20 +567,25 @@ cudaError_t launch_decode_t(const Problem& pr, const void* q, const void* k, con
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_decode_kernel<kBF16, RP>, tq, tk, tv, dp);
+    return cudaLaunchKernelEx(&cfg, attn_decode_kernel<kBF16, RP, kPaged>, tq, tk, tv, dp);
 }
 
-}  // namespace
+template <bool kPaged>
+cudaError_t launch_decode_any(const Problem& p, const void* q, const void* k, const void* v, const PagedKV* kv,
+                              int chunk, int S, const SplitWorkspace& ws, int* status, cudaStream_t stream) {
+    const int R = p.G * p.M;
+    const bool bf = p.dtype == ATTN_BF16;
+    if (R <= 4) return bf ? launch_decode_t<true, 4, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream)
+                          : launch_decode_t<false, 4, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream);
+    if (R <= 8) return bf ? launch_decode_t<true, 8, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream)
+                          : launch_decode_t<false, 8, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream);
+    return bf ? launch_decode_t<true, 16, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream)
+              : launch_decode_t<false, 16, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream);
+}
 
-bool decode_tc_supported(const Problem& p) { return p.D == DD && p.G * p.M <= DNR && p.B * p.Hkv <= 65535; }
-
-// Splits: every CTA resident at once when possible (two per SM), each
-// streaming an equal run of 128-key tiles; more splits only while the grid
-// still fits in one wave.
-int decode_plan_tc(const Problem& p, int* chunk, int* S) {
-    const int kbase = split_base(p);
-    const int tiles = p.khi > kbase ? (p.khi - kbase + DBN - 1) / DBN : 1;
-    const int groups = p.B * p.Hkv;
+// Splits of `tiles` key tiles over `groups` KV groups: every CTA resident at
+// once when possible (two per SM), each streaming an equal run of tiles.
+void plan_splits(int tiles, int groups, int* chunk, int* S) {
     const int slots = 2 * sm_count();
     int s = groups > 0 ? slots / groups : 1;
     if (s < 1) s = 1;
@@ -490,19 +594,43 @@ int decode_plan_tc(const Problem& p, int* chunk, int* S) {
     const int per = (tiles + s - 1) / s;
     *chunk = per * DBN;
     *S = (tiles + per - 1) / per;
+}
+
+}  // namespace
+
+bool decode_tc_supported(const Problem& p) { return p.D == DD && p.G * p.M <= DNR && p.B * p.Hkv <= 65535; }
+
+int decode_plan_tc(const Problem& p, int* chunk, int* S) {
+    const int kbase = split_base(p);
+    const int tiles = p.khi > kbase ? (p.khi - kbase + DBN - 1) / DBN : 1;
+    plan_splits(tiles, p.B * p.Hkv, chunk, S);
     return ATTN_OK;
 }
 
 cudaError_t launch_decode_tc(const Problem& p, const void* q, const void* k, const void* v, int chunk, int S,
                              const SplitWorkspace& ws, int* status, cudaStream_t stream) {
-    const int R = p.G * p.M;
-    const bool bf = p.dtype == ATTN_BF16;
-    if (R <= 4) return bf ? launch_decode_t<true, 4>(p, q, k, v, chunk, S, ws, status, stream)
-                          : launch_decode_t<false, 4>(p, q, k, v, chunk, S, ws, status, stream);
-    if (R <= 8) return bf ? launch_decode_t<true, 8>(p, q, k, v, chunk, S, ws, status, stream)
-                          : launch_decode_t<false, 8>(p, q, k, v, chunk, S, ws, status, stream);
-    return bf ? launch_decode_t<true, 16>(p, q, k, v, chunk, S, ws, status, stream)
-              : launch_decode_t<false, 16>(p, q, k, v, chunk, S, ws, status, stream);
+    return launch_decode_any<false>(p, q, k, v, nullptr, chunk, S, ws, status, stream);
+}
+
+// Paged: the plan must cover any sequence up to kv.max_len keys. Without a
+// window a sequence's range starts at key 0; with one it spans at most
+// window + M - 1 keys from an unaligned start.
+int decode_plan_paged(const Problem& p, const PagedKV& kv, int* chunk, int* S) {
+    const int len_tiles = (kv.max_len + DBN - 1) / DBN;
+    int tiles = len_tiles;
+    if (p.window > 0) {
+        const long long span = (long long)p.window + p.M - 1 + (DBN - 1);
+        const long long wt = (span + DBN - 1) / DBN;
+        if (wt < tiles) tiles = (int)wt;
+    }
+    if (tiles < 1) tiles = 1;
+    plan_splits(tiles, p.B * p.Hkv, chunk, S);
+    return ATTN_OK;
+}
+
+cudaError_t launch_decode_paged(const Problem& p, const void* q, const PagedKV& kv, int chunk, int S,
+                                const SplitWorkspace& ws, int* status, cudaStream_t stream) {
+    return launch_decode_any<true>(p, q, nullptr, nullptr, &kv, chunk, S, ws, status, stream);
 }
 
 }  // namespace attn

@@ -62,6 +62,20 @@ int decode_plan_tc(const Problem& p, int* chunk, int* S);
 cudaError_t launch_decode_tc(const Problem& p, const void* q, const void* k, const void* v, int chunk, int S,
                              const SplitWorkspace& ws, int* status, cudaStream_t stream);
 
+// Paged KV cache (decode): pools [num_pages][Hkv][page_size][D]; sequence b's
+// key j lives in row j % page_size of page block_table[b * max_pages + j / page_size];
+// sequence b holds min(seq_lens[b], max_len) keys.
+struct PagedKV {
+    const void* k_pages;
+    const void* v_pages;
+    const int* block_table;
+    const int* seq_lens;
+    int num_pages, page_size, max_pages, max_len;
+};
+int decode_plan_paged(const Problem& p, const PagedKV& kv, int* chunk, int* S);
+cudaError_t launch_decode_paged(const Problem& p, const void* q, const PagedKV& kv, int chunk, int S,
+                                const SplitWorkspace& ws, int* status, cudaStream_t stream);
+
 // Metadata validation and the device status word, shared by every entry point.
 int validate_problem(const void* q, const void* k, const void* v, const void* o, int B, int Hq, int Hkv, int M,
                      int N, int D, int causal, int window, float scale, int dtype, Problem* p);

@@ -1,0 +1,137 @@
+// C ABI of split-KV decode over a paged KV cache: metadata validation, the
+// split plan, the tcgen05 split kernel in paged mode and the merge kernel.
+// Attention over a KV-cache slice is the decode step the course's plan names
+// next ("Kernel Notes & Checklist", section 3, the plan, week +3: sliding
+// window + GQA + KV-cache slice); pages of the cache are gathered by the TMA
+// producer through the block table, so no copy of the cache is ever made.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "attn.h"
+#include "attn_internal.h"
+
+namespace attn {
+namespace {
+
+constexpr int64_t kI32Max = 2147483647LL;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool page_size_ok(int ps) { return ps == 16 || ps == 32 || ps == 64 || (ps > 0 && ps % 128 == 0); }
+
+struct PagedCall {
+    Problem p;
+    PagedKV kv;
+};
+
+// Metadata only (never values): shapes, head dimension, group size, 32-bit
+// element counts, null pointers of non-empty tensors, alignment.
+int validate_paged(const void* q, const void* kp, const void* vp, const int* table, const int* lens, const void* o,
+                   int B, int Hq, int Hkv, int M, int D, int num_pages, int page_size, int max_pages,
+                   int max_seq_len, int causal, int window, float scale, int dtype, PagedCall* c) {
+    if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_DTYPE;
+    if (B < 0 || Hq < 0 || Hkv < 0 || M < 0 || D <= 0 || num_pages < 0 || max_pages < 0 || max_seq_len < 0)
+        return ATTN_ERR_SHAPE;
+    if (Hq > 0 && Hkv == 0) return ATTN_ERR_SHAPE;
+    if (!page_size_ok(page_size)) return ATTN_ERR_SHAPE;
+    if (Hq > 0 && Hq % Hkv != 0) return ATTN_ERR_GQA;
+    if (D != 128) return ATTN_ERR_HEADDIM;
+    const int G = Hkv > 0 ? Hq / Hkv : 1;
+    if ((int64_t)G * M > 16) return ATTN_ERR_PATH;
+    const int64_t nq = (int64_t)B * Hq * M * D;
+    const int64_t npool = (int64_t)num_pages * Hkv * page_size * D;
+    const int64_t ntab = (int64_t)B * max_pages;
+    if (nq > kI32Max || npool > kI32Max || ntab > kI32Max || (int64_t)B * Hkv > 65535) return ATTN_ERR_OVERFLOW;
+    if ((nq > 0 && (!q || !o)) || (npool > 0 && (!kp || !vp)) || (ntab > 0 && !table) || (B > 0 && !lens))
+        return ATTN_ERR_NULL;
+    if ((q && !aligned(q, 16)) || (o && !aligned(o, 16)) || (kp && !aligned(kp, 16)) || (vp && !aligned(vp, 16)) ||
+        (table && !aligned(table, 4)) || (lens && !aligned(lens, 4)))
+        return ATTN_ERR_ALIGN;
+    const int64_t cover = (int64_t)max_pages * page_size;
+    const int max_len = (int)(cover < max_seq_len ? cover : max_seq_len);
+    Problem& p = c->p;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.M = M;
+    p.N = max_len;
+    p.D = D;
+    p.causal = causal ? 1 : 0;
+    p.window = window > 0 ? window : 0;
+    p.scale = (scale == 0.0f) ? (float)(1.0 / sqrt((double)D)) : scale;
+    p.scale_log2 = p.scale * kLog2e;
+    p.dtype = dtype;
+    p.G = G;
+    p.klo = 0;  // per sequence, in the kernel
+    p.khi = max_len;
+    c->kv = PagedKV{kp, vp, table, lens, num_pages, page_size, max_pages, max_len};
+    return ATTN_OK;
+}
+
+bool nothing_to_attend(const PagedCall& c) { return c.kv.max_len == 0 || c.kv.num_pages == 0 || c.p.Hkv == 0; }
+
+size_t paged_workspace(const PagedCall& c) {
+    int chunk = 0, S = 0;
+    decode_plan_paged(c.p, c.kv, &chunk, &S);
+    return split_workspace_bytes(c.p.B * c.p.Hq * c.p.M, S, c.p.D);
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+int run_paged(const PagedCall& c, const void* q, void* o, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    const Problem& p = c.p;
+    int chunk = 0, S = 0;
+    decode_plan_paged(p, c.kv, &chunk, &S);
+    const int rows = p.B * p.Hq * p.M;
+    if (!ws || ws_bytes < split_workspace_bytes(rows, S, p.D)) return ATTN_ERR_WORKSPACE;
+    if (!aligned(ws, 16)) return ATTN_ERR_ALIGN;
+    int* status = device_status_ptr();
+    if (!status) return ATTN_ERR_CUDA;
+    SplitWorkspace w = split_workspace(ws, rows, S, p.D);
+    if (launch_decode_paged(p, q, c.kv, chunk, S, w, status, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    return cuda_status(launch_merge(w.m, w.l, w.acc, o, nullptr, nullptr, rows, S, p.D, p.dtype, 1.0f, true,
+                                    stream));
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+size_t attn_decode_paged_workspace_bytes(int B, int Hq, int Hkv, int M, int D, int page_size, int max_pages,
+                                         int max_seq_len, int causal, int window) {
+    static const int16_t dummy[8] __attribute__((aligned(16))) = {};
+    const int* idummy = reinterpret_cast<const int*>(dummy);
+    PagedCall c;
+    if (validate_paged(dummy, dummy, dummy, idummy, idummy, dummy, B, Hq, Hkv, M, D, 1, page_size, max_pages,
+                       max_seq_len, causal, window, 0.f, ATTN_BF16, &c) != ATTN_OK)
+        return 0;
+    if ((int64_t)B * Hq * M == 0 || nothing_to_attend(c)) return 0;
+    return paged_workspace(c);
+}
+
+int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
+                      const int* seq_lens, void* o, int B, int Hq, int Hkv, int M, int D, int num_pages,
+                      int page_size, int max_pages, int max_seq_len, int causal, int window, float scale, int dtype,
+                      void* workspace, size_t ws_bytes, void* stream) {
+    PagedCall c;
+    int rc = validate_paged(q, k_pages, v_pages, block_table, seq_lens, o, B, Hq, Hkv, M, D, num_pages, page_size,
+                            max_pages, max_seq_len, causal, window, scale, dtype, &c);
+    if (rc != ATTN_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((int64_t)B * Hq * M == 0) return ATTN_OK;
+    if (nothing_to_attend(c))  // no sequence can hold a key: every row outputs 0
+        return cuda_status(cudaMemsetAsync(o, 0, (size_t)B * Hq * M * D * 2, s));
+    if (workspace) return run_paged(c, q, o, workspace, ws_bytes, s);
+    const size_t bytes = paged_workspace(c);
+    void* ws = nullptr;
+    if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    rc = run_paged(c, q, o, ws, bytes, s);
+    if (cudaFreeAsync(ws, s) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
+    return rc;
+}
+
+}  // extern "C"

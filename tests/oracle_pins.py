@@ -283,6 +283,55 @@ def pin_rows_and_weights(orc):
             assert np.allclose(orc.weights(q, k, int(r), causal, window), want_w[r], rtol=1e-12, atol=1e-14)
 
 
+# --------------------------------------------------------------------------
+# Paged KV cache: pages cut from a contiguous cache, in any order, with a
+# length per sequence, against the torch float64 formula on the truncated
+# contiguous cache
+# --------------------------------------------------------------------------
+def to_pages(k, page_size, rng=None):
+    """[B, Hkv, N, D] -> pool [B * N / page_size, Hkv, page_size, D] and block
+    table [B, N / page_size]; with rng the pool's pages are shuffled."""
+    B, Hkv, N, D = k.shape
+    npg = N // page_size
+    pool = k.reshape(B, Hkv, npg, page_size, D).transpose(0, 2, 1, 3, 4).reshape(B * npg, Hkv, page_size, D)
+    table = np.arange(B * npg, dtype=np.int64).reshape(B, npg)
+    if rng is not None:
+        perm = rng.permutation(B * npg)  # page i moves to slot perm[i]
+        moved = np.empty_like(pool)
+        moved[perm] = pool
+        pool, table = moved, perm[table]
+    return np.ascontiguousarray(pool), table
+
+
+def pin_paged(orc):
+    rng = np.random.default_rng(29)
+    B, Hq, Hkv, M, D, ps, npg = 3, 4, 2, 2, 5, 4, 6
+    N = ps * npg
+    q, k, v = _rand((B, Hq, M, D), 41), _rand((B, Hkv, N, D), 42), _rand((B, Hkv, N, D), 43)
+    scale = 1.0 / math.sqrt(D)
+    for shuffle in (False, True):
+        r = np.random.default_rng(5) if shuffle else None
+        kp, table = to_pages(k, ps, r)
+        r = np.random.default_rng(5) if shuffle else None
+        vp, table_v = to_pages(v, ps, r)
+        assert np.array_equal(table, table_v)
+        for causal, window in ((True, 0), (False, 0), (True, 7), (False, 5)):
+            # every sequence full: the contiguous attention
+            full = orc.attention_paged(q, kp, vp, table, [N] * B, N, causal, window)
+            assert np.allclose(full, library_attention(q, k, v, causal, window, scale), rtol=1e-12, atol=1e-12)
+            # ragged lengths, one empty sequence, one past the table (clamped)
+            lens = [0, 13, N + 9]
+            got = orc.attention_paged(q, kp, vp, table, lens, N + 9, causal, window)
+            for b, L in enumerate(lens):
+                L = min(L, N)
+                want = library_attention(q[b:b + 1], k[b:b + 1, :, :L], v[b:b + 1, :, :L], causal, window, scale)
+                assert np.allclose(got[b:b + 1], want, rtol=1e-12, atol=1e-12), (shuffle, causal, window, b)
+            # max_seq_len below the lengths cuts every sequence there
+            cut = orc.attention_paged(q, kp, vp, table, [N] * B, 9, causal, window)
+            want = library_attention(q, k[:, :, :9], v[:, :, :9], causal, window, scale)
+            assert np.allclose(cut, want, rtol=1e-12, atol=1e-12)
+
+
 ALL_PINS = [
     pin_a3_worked_example,
     pin_a1_merge_example,
@@ -294,4 +343,5 @@ ALL_PINS = [
     pin_closed_forms,
     pin_gqa_map,
     pin_rows_and_weights,
+    pin_paged,
 ]

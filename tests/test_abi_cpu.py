@@ -105,3 +105,53 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "_lib", None)
     with pytest.raises(FileNotFoundError):
         binding.lib()
+
+
+A4 = ctypes.c_void_p(0x10004)
+
+
+def paged(L, q=A16, kp=A16, vp=A16, table=A16, lens=A16, o=A16, B_=2, Hq=8, Hkv=2, M=1, D=128, num_pages=4,
+          page_size=16, max_pages=2, max_seq_len=32, dtype=0):
+    return L.attn_decode_paged(q, kp, vp, table, lens, o, B_, Hq, Hkv, M, D, num_pages, page_size, max_pages,
+                               max_seq_len, 1, 0, 0.0, dtype, None, 0, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dtype=5), -3),
+    (dict(B_=-1), -2),
+    (dict(num_pages=-1), -2),
+    (dict(max_pages=-3), -2),
+    (dict(max_seq_len=-1), -2),
+    (dict(page_size=48), -2),
+    (dict(page_size=8), -2),
+    (dict(page_size=0), -2),
+    (dict(Hkv=0), -2),
+    (dict(Hq=6, Hkv=4), -5),
+    (dict(D=64), -4),
+    (dict(Hq=16, Hkv=2, M=3), -11),   # 8 grouped heads x 3 rows > 16
+    (dict(num_pages=1 << 20, page_size=128), -6),
+    (dict(B_=70000, Hkv=1, Hq=1), -6),
+    (dict(q=None), -1),
+    (dict(kp=None), -1),
+    (dict(table=None), -1),
+    (dict(lens=None), -1),
+    (dict(o=A8), -7),
+    (dict(vp=A8), -7),
+    (dict(table=ctypes.c_void_p(0x10002)), -7),
+])
+def test_paged_validation_status(L, kw, status):
+    assert paged(L, **kw) == status
+
+
+def test_paged_workspace_bytes(L):
+    # the decode workload as pages of 16 keys: rows x splits x (2 + D) floats, 256-byte aligned parts
+    nb = sa.attn_decode_paged_workspace_bytes(8, 32, 8, 1, 128, 16, 512, 8192, True, 4096)
+    rows = 8 * 32
+    assert nb > 0 and nb % 256 == 0
+    S = nb // (rows * 4 * 130)
+    assert 1 <= S <= 64
+    assert sa.attn_decode_paged_workspace_bytes(8, 32, 8, 1, 64, 16, 512, 8192, True, 0) == 0   # D = 64
+    assert sa.attn_decode_paged_workspace_bytes(8, 32, 8, 1, 128, 16, 512, 0, True, 0) == 0     # no keys
+    assert sa.attn_decode_paged_workspace_bytes(0, 32, 8, 1, 128, 16, 512, 8192, True, 0) == 0  # no rows
+    # a 4-byte aligned table and length array are accepted (validation passes, nothing launched: B = 0)
+    assert paged(L, table=A4, lens=A4, B_=0) == 0

@@ -1,0 +1,123 @@
+"""Decode over a paged KV cache (attn_decode_paged) against the FP64 oracle's
+paged definition, on the same seeded inputs, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import streaming_attention_gb300 as sa
+from oracle_pins import to_pages
+from parity import check
+from streaming_attention_gb300.inputs import DECODE_GQA, make_qkv, workload_inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(autouse=True)
+def no_device_timeouts():
+    yield
+    assert sa.last_device_status() == 0, "a kernel gave up on a bounded wait"
+
+
+def paged_case(B, Hq, Hkv, M, Ncap, page_size, dtype, seed, shuffle=True):
+    """Seeded q and a contiguous cache cut into pages (shuffled in the pool)."""
+    q, k, v = make_qkv(B, Hq, Hkv, M, Ncap, 128, dtype, seed)
+    r = np.random.default_rng(seed) if shuffle else None
+    kp, table = to_pages(k.float().numpy(), page_size, r)
+    r = np.random.default_rng(seed) if shuffle else None
+    vp, _ = to_pages(v.float().numpy(), page_size, r)
+    kp, vp = torch.from_numpy(kp).to(dtype), torch.from_numpy(vp).to(dtype)
+    return q, kp, vp, torch.from_numpy(table.astype(np.int32))
+
+
+def run_paged(q, kp, vp, table, lens, max_seq_len, causal, window, workspace=True):
+    qd, kd, vd = q.to(DEV), kp.to(DEV), vp.to(DEV)
+    td, ld = table.to(DEV), torch.tensor(lens, dtype=torch.int32, device=DEV)
+    o = torch.full_like(qd, float("nan"))
+    ws = None
+    if workspace:
+        B, Hq, M, D = q.shape
+        nb = sa.attn_decode_paged_workspace_bytes(B, Hq, kp.shape[1], M, D, kp.shape[2], table.shape[1],
+                                                  max_seq_len, causal, window)
+        ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=DEV)
+    sa.attn_decode_paged(qd, kd, vd, td, ld, o, max_seq_len, causal, window, workspace=ws)
+    torch.cuda.synchronize()
+    return o
+
+
+@pytest.mark.parametrize("page_size", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("causal,window", [(True, 0), (True, 300), (False, 0), (False, 200)])
+def test_paged_ragged_lengths(page_size, causal, window):
+    B, Hq, Hkv, M, Ncap = 5, 8, 2, 1, 1024
+    q, kp, vp, table = paged_case(B, Hq, Hkv, M, Ncap, page_size, torch.bfloat16, 7)
+    lens = [1000, 1, 0, 1024, 517]
+    o = run_paged(q, kp, vp, table, lens, Ncap, causal, window)
+    want = oracle.attention_paged(q, kp, vp, table, lens, Ncap, causal, window)
+    check(o, want, torch.bfloat16, f"page {page_size} causal={causal} window={window}")
+    assert torch.all(o[2] == 0)  # the empty sequence
+
+
+@pytest.mark.parametrize("G,M", [(4, 4), (2, 8), (16, 1), (1, 3)])
+def test_paged_grouped_and_speculative_rows(G, M):
+    """Speculative decode: M > 1 query rows per sequence, G * M <= 16 grouped rows."""
+    B, Hkv, Ncap, ps = 3, 2, 768, 64
+    q, kp, vp, table = paged_case(B, G * Hkv, Hkv, M, Ncap, ps, torch.float16, 11)
+    lens = [768, 301, 2]
+    for causal, window in ((True, 0), (True, 129)):
+        o = run_paged(q, kp, vp, table, lens, Ncap, causal, window)
+        want = oracle.attention_paged(q, kp, vp, table, lens, Ncap, causal, window)
+        check(o, want, torch.float16, f"G={G} M={M} causal={causal} window={window}")
+
+
+def test_paged_contiguous_cache_is_one_page_per_sequence():
+    """A contiguous [B, Hkv, N, D] cache is the pool with page_size N and the
+    block table [[0], [1], ...]: equal to attn_fwd's decode on the same cache."""
+    B, Hq, Hkv, M, N = 4, 16, 4, 1, 1280
+    q, k, v = make_qkv(B, Hq, Hkv, M, N, 128, torch.bfloat16, 13)
+    table = torch.arange(B, dtype=torch.int32).reshape(B, 1)
+    o = run_paged(q, k, v, table, [N] * B, N, True, 1000)
+    ref = sa.attention(q.to(DEV), k.to(DEV), v.to(DEV), causal=True, window=1000, path=sa.PATH_DECODE)
+    torch.cuda.synchronize()
+    assert torch.allclose(o.float(), ref.float(), atol=2e-2, rtol=0)
+    check(o, oracle.attention(q, k, v, causal=True, window=1000), torch.bfloat16, "contiguous as one page")
+
+
+def test_paged_max_seq_len_cuts_lengths_and_library_workspace():
+    B, Hq, Hkv, M, Ncap, ps = 2, 4, 1, 2, 640, 32
+    q, kp, vp, table = paged_case(B, Hq, Hkv, M, Ncap, ps, torch.bfloat16, 17)
+    lens = [640, 640]
+    o = run_paged(q, kp, vp, table, lens, 333, True, 0, workspace=False)
+    want = oracle.attention_paged(q, kp, vp, table, lens, 333, True, 0)
+    check(o, want, torch.bfloat16, "max_seq_len 333, library-allocated workspace")
+
+
+def test_paged_empty_problems():
+    q, kp, vp, table = paged_case(2, 4, 2, 1, 256, 16, torch.bfloat16, 19)
+    o = run_paged(q, kp, vp, table, [0, 0], 256, True, 0)
+    assert torch.all(o == 0)
+    o = run_paged(q, kp, vp, table, [256, 100], 0, True, 0)  # max_seq_len 0
+    assert torch.all(o == 0)
+    q0 = q[:0].contiguous()
+    o = run_paged(q0, kp, vp, table[:0].contiguous(), [], 256, True, 0)
+    assert o.shape == (0, 4, 1, 128)
+
+
+def test_paged_decode_workload_full_size():
+    """The GQA decode workload (B=8, Hq=32, Hkv=8, N=8192, window 4096) with its
+    cache cut into 16-key pages in shuffled order, against the oracle on every
+    row and against the contiguous decode path."""
+    w = DECODE_GQA
+    q, k, v = workload_inputs(w)
+    r = np.random.default_rng(3)
+    kp, table = to_pages(k.float().numpy(), 16, r)
+    r = np.random.default_rng(3)
+    vp, _ = to_pages(v.float().numpy(), 16, r)
+    kp, vp = torch.from_numpy(kp).to(w.dtype), torch.from_numpy(vp).to(w.dtype)
+    table = torch.from_numpy(table.astype(np.int32))
+    o = run_paged(q, kp, vp, table, [w.N] * w.B, w.N, w.causal, w.window)
+    want = oracle.attention_paged(q, kp, vp, table, [w.N] * w.B, w.N, w.causal, w.window)
+    check(o, want, w.dtype, "paged decode workload")
+    ref = sa.attention(q.to(DEV), k.to(DEV), v.to(DEV), causal=w.causal, window=w.window, path=sa.PATH_DECODE)
+    torch.cuda.synchronize()
+    assert torch.allclose(o.float(), ref.float(), atol=2e-2, rtol=0)
