@@ -465,10 +465,41 @@ def extra_measurements(args, dev, stream, flush):
             out[name] = {"TFLOP/s": round(flops(w, causal) / (ms * 1e-3) / 1e12, 2), "us": round(ms * 1e3, 1),
                          "cold_call_us": round(cold * 1e3, 1), "path": pname}
         del sets, ws
+    if args.workload == PREFILL_D128.name:
+        out["prefill_d128_bf16_causal_backward"] = backward_measure(PREFILL_D128, True, steps, dev, stream)
+        out["prefill_d128_bf16_noncausal_backward"] = backward_measure(PREFILL_D128, False, steps, dev, stream)
     if args.workload in (PREFILL_D128.name, DECODE_GQA.name):
         for ps in (16, 128):
             out[f"decode_gqa_paged{ps}"] = paged_decode_measure(DECODE_GQA, ps, steps, dev, stream, flush)
     return out
+
+
+def backward_measure(w, causal, steps, dev, stream):
+    """attn_bwd on the workload (forward output and log-sum-exp from attn_fwd_lse,
+    a seeded N(0,1) dO); algorithmic FLOPs 2.5x the forward's (five products of
+    the forward's size over the allowed pairs: dV, dP, dS*K, dS^T*Q and the
+    recomputed S)."""
+    import streaming_attention_gb300 as sa
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    _, sets, _ = rotation(w, dev, l2)
+    bsets = []
+    for qd, kd, vd, od in sets:
+        lse = torch.empty(qd.shape[:3], dtype=torch.float32, device=dev)
+        sa.attn_fwd_lse(qd, kd, vd, od, lse, causal, w.window)
+        d_o = torch.randn(qd.shape, generator=torch.Generator().manual_seed(12)).to(w.dtype).to(dev)
+        bsets.append((qd, kd, vd, od, d_o, lse, torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)))
+    del sets
+    ws = torch.empty(max(sa.attn_bwd_workspace_bytes(w.B, w.Hq, w.M), 1), dtype=torch.uint8, device=dev)
+
+    def fn_on(t, st):
+        sa.attn_bwd(*t, causal=causal, window=w.window, workspace=ws, stream=st)
+
+    ms = time_steady(fn_on, bsets, steps, 3, stream)
+    work = 2.5 * flops(w, causal)
+    del bsets
+    return {"TFLOP/s": round(work / (ms * 1e-3) / 1e12, 2), "us": round(ms * 1e3, 1),
+            "flops": "2.5x forward (five products over allowed pairs)", "path": "backward (dK/dV kernel + dQ kernel)"}
 
 
 def paged_decode_measure(w, page_size, steps, dev, stream, flush):

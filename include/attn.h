@@ -115,6 +115,44 @@ ATTN_API int attn_fwd_ex(const void* q, const void* k, const void* v, void* o,
                          int causal, int window, float scale, int dtype, int path,
                          void* workspace, size_t ws_bytes, void* stream);
 
+/* attn_fwd_ex that also writes each row's log-sum-exp of its logits,
+ *   lse[b,h,i] = ln sum_{j visible} exp(scale * <Q[b,h,i,:], K[b,g,j,:]>),
+ * natural log, -inf for a row with no visible key: the summary (m, l) of the
+ * answer key's A1 row folded into one number (m + ln l), which the backward
+ * pass needs and with which the outputs of calls over disjoint key ranges merge
+ * (attn_merge with m = lse, l = 1, acc = o).
+ *   lse: device float [B, Hq, M], 4-byte aligned, owned by the caller; NULL only
+ *        when the output is empty.
+ *   workspace: as attn_fwd_ex, or NULL to have it allocated stream-ordered
+ *        (cudaMallocAsync / cudaFreeAsync) as attn_fwd does. */
+ATTN_API int attn_fwd_lse(const void* q, const void* k, const void* v, void* o, float* lse,
+                          int B, int Hq, int Hkv, int M, int N, int D,
+                          int causal, int window, float scale, int dtype, int path,
+                          void* workspace, size_t ws_bytes, void* stream);
+
+/* Backward pass: gradients of L = sum(dO * O) for O = attention(Q, K, V).
+ * Each row of the weight gradient is the softmax vector-Jacobian product of
+ * that row ("Intermediate and advanced kernel workshops", workshop I2, softmax
+ * backward; answer key, I2 row and worked answer), with P recomputed from the
+ * forward's log-sum-exp (attn_fwd_lse) instead of being stored:
+ *   P = exp(scale Q K^T - lse) over the visible keys, dV = P^T dO,
+ *   dP = dO V^T, dS = P * (dP - rowsum(dO * O)), dQ = scale dS K,
+ *   dK = scale dS^T Q; with GQA, dK and dV of a KV head sum over its query heads.
+ *   q, o, d_o, dq: device [B, Hq, M, D]; k, v, dk, dv: device [B, Hkv, N, D];
+ *   all of dtype, 16-byte aligned; lse: device float [B, Hq, M] from the forward
+ *   of the same q, k, v, causal, window and scale. dq, dk, dv are written (not
+ *   accumulated) and must not overlap the inputs.
+ *   D must be 64 or 128 (ATTN_ERR_HEADDIM). M == 0 or N == 0: the gradients
+ *   that exist are zero-filled.
+ *   workspace: device memory of attn_bwd_workspace_bytes(B, Hq, M) bytes,
+ *   16-byte aligned, or NULL to have it allocated stream-ordered. */
+ATTN_API size_t attn_bwd_workspace_bytes(int B, int Hq, int M);
+ATTN_API int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* d_o,
+                      const float* lse, void* dq, void* dk, void* dv,
+                      int B, int Hq, int Hkv, int M, int N, int D,
+                      int causal, int window, float scale, int dtype,
+                      void* workspace, size_t ws_bytes, void* stream);
+
 /* Merge of split summaries, the pages' common-maximum rule (answer key,
  * central-idea table, A1 row, and its worked answer: (2,2) and (4,1) merge
  * to (4, 1+2e^-2)).

@@ -62,6 +62,8 @@ def _load(mutant: int = 0, out_dir: Optional[str] = None) -> ctypes.CDLL:
             shape = [ci] * 6 + [ci, ci, cd]
             lib.oracle_attn_f64.argtypes = [dp, dp, dp, dp, *shape, ci]
             lib.oracle_attn_f64.restype = ci
+            lib.oracle_attn_lse_f64.argtypes = [dp, dp, dp, dp, dp, *shape, ci]
+            lib.oracle_attn_lse_f64.restype = ci
             lib.oracle_attn_rows_f64.argtypes = [dp, dp, dp, dp, *shape, i64p, ctypes.c_int64, ci]
             lib.oracle_attn_rows_f64.restype = ci
             lib.oracle_attn_weights_f64.argtypes = [dp, dp, *shape, ctypes.c_int64, dp]
@@ -114,6 +116,20 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"oracle_attn_f64 rejected the shape (rc={rc})")
         return o
+
+    def attention_lse(self, q, k, v, causal=False, window=0, scale=None, nthreads=0):
+        """Full FP64 output [B, Hq, M, D] and each row's log-sum-exp [B, Hq, M]
+        (natural log of the sum of exp of its allowed logits; -inf when none)."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        B, Hq, Hkv, M, N, D = self._dims(q, k, v)
+        scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+        o = np.zeros((B, Hq, M, D), dtype=np.float64)
+        lse = np.full((B, Hq, M), -np.inf, dtype=np.float64)
+        rc = self.lib.oracle_attn_lse_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, M, N, D,
+                                          int(causal), int(window), scale, int(nthreads))
+        if rc != 0:
+            raise ValueError(f"oracle_attn_lse_f64 rejected the shape (rc={rc})")
+        return o, lse
 
     def attention_rows(self, q, k, v, rows: Sequence[int], causal=False, window=0, scale=None,
                        nthreads=0) -> np.ndarray:
@@ -208,6 +224,10 @@ def attention(q, k, v, causal=False, window=0, scale=None, nthreads=0):
     return default().attention(q, k, v, causal, window, scale, nthreads)
 
 
+def attention_lse(q, k, v, causal=False, window=0, scale=None, nthreads=0):
+    return default().attention_lse(q, k, v, causal, window, scale, nthreads)
+
+
 def attention_rows(q, k, v, rows, causal=False, window=0, scale=None, nthreads=0):
     return default().attention_rows(q, k, v, rows, causal, window, scale, nthreads)
 
@@ -224,3 +244,55 @@ def attention_paged(q, k_pages, v_pages, block_table, seq_lens, max_seq_len, cau
 
 def cpu_threads() -> int:
     return os.cpu_count() or 1
+
+
+# --------------------------------------------------------------------------
+# Backward pass, FP64, by its definition
+# --------------------------------------------------------------------------
+def visible_mask(M, N, causal, window):
+    """[M, N] boolean: key j visible to query row i (position i + N - M)."""
+    pos = np.arange(M)[:, None] + (N - M)
+    j = np.arange(N)[None, :]
+    keep = np.ones((M, N), dtype=bool)
+    if causal:
+        keep &= j <= pos
+    if window > 0:
+        keep &= j > pos - window
+    return keep
+
+
+def attention_backward(q, k, v, do, causal=False, window=0, scale=None, heads=None):
+    """Gradients (dq, dk, dv) of L = sum(do * o) for o = attention(q, k, v), in FP64.
+
+    For each (b, h): the weights P = softmax(scale * q k^T over the visible
+    keys) are materialized; dv = P^T do; dP = do v^T; each row of dS is the
+    softmax vector-Jacobian product of that row, dS = P * (dP - sum_j P dP)
+    ("Intermediate and advanced kernel workshops", workshop I2, softmax
+    backward: one reduction of y*g, then y * (g - that sum)); dq = scale dS k;
+    dk = scale dS^T q. With GQA, dk and dv of a KV head sum over its query
+    heads. Rows with no visible key contribute nothing. `heads`, if given, is a
+    list of (b, h) pairs to evaluate (dk, dv then hold only their share)."""
+    q, k, v, do = (_f64(x) for x in (q, k, v, do))
+    B, Hq, M, D = q.shape
+    Hkv, N = k.shape[1], k.shape[2]
+    G = Hq // Hkv if Hkv else 1
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    keep = visible_mask(M, N, causal, window)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    pairs = heads if heads is not None else [(b, h) for b in range(B) for h in range(Hq)]
+    for b, h in pairs:
+        g = h // G
+        s = np.where(keep, scale * (q[b, h] @ k[b, g].T), -np.inf)
+        mu = s.max(axis=1, keepdims=True)
+        any_key = np.isfinite(mu)
+        e = np.where(keep, np.exp(s - np.where(any_key, mu, 0.0)), 0.0)
+        z = e.sum(axis=1, keepdims=True)
+        p = np.divide(e, z, out=np.zeros_like(e), where=z > 0)
+        dv[b, g] += p.T @ do[b, h]
+        dp = do[b, h] @ v[b, g].T
+        ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+        dq[b, h] = scale * (ds @ k[b, g])
+        dk[b, g] += scale * (ds.T @ q[b, h])
+    return dq, dk, dv

@@ -125,9 +125,10 @@ static double score(const shape_t* s, const double* qr, const double* kh, long j
 }
 
 /* One output row, two passes over the materialized score row.
- * srow: caller scratch of N doubles. Writes D values to out. */
+ * srow: caller scratch of N doubles. Writes D values to out, and when lse is
+ * not NULL the row's log-sum-exp ln sum_j exp(s_j) (-inf for no allowed key). */
 static void attend_row(const shape_t* s, const double* q, const double* k, const double* v,
-                       long r, double* srow, double* out) {
+                       long r, double* srow, double* out, double* lse) {
     const double *qr, *kh, *vh;
     long p;
     row_operands(s, q, k, v, r, &qr, &kh, &vh, &p);
@@ -142,6 +143,7 @@ static void attend_row(const shape_t* s, const double* q, const double* k, const
         if (srow[j] > mu) mu = srow[j];
         ++count;
     }
+    if (lse) *lse = -INFINITY;
     if (count == 0) return; /* empty allowed set: output 0 */
 
     /* pass 2: weights exp(s - mu), their sum, and the weighted sum of V rows */
@@ -152,6 +154,7 @@ static void attend_row(const shape_t* s, const double* q, const double* k, const
         z += w;
         for (long d = 0; d < s->D; ++d) out[d] += w * vh[j * s->D + d];
     }
+    if (lse) *lse = mu + log(z);
 #if ORACLE_MUTANT == 5
     (void)z; /* planted: no normalization */
 #else
@@ -163,6 +166,7 @@ typedef struct {
     const shape_t* s;
     const double *q, *k, *v;
     double* o;
+    double* lse;         /* NULL: no log-sum-exp output */
     const int64_t* rows; /* NULL: rows [lo, hi) of the full output */
     int64_t lo, hi;
     int status;
@@ -174,7 +178,7 @@ static void* worker(void* arg) {
     if (!srow) { w->status = ORACLE_ENOMEM; return NULL; }
     for (int64_t t = w->lo; t < w->hi; ++t) {
         long r = w->rows ? (long)w->rows[t] : (long)t;
-        attend_row(w->s, w->q, w->k, w->v, r, srow, w->o + t * (int64_t)w->s->D);
+        attend_row(w->s, w->q, w->k, w->v, r, srow, w->o + t * (int64_t)w->s->D, w->lse ? w->lse + t : NULL);
     }
     free(srow);
     w->status = ORACLE_OK;
@@ -182,7 +186,7 @@ static void* worker(void* arg) {
 }
 
 static int run_rows(const shape_t* s, const double* q, const double* k, const double* v, double* o,
-                    const int64_t* rows, int64_t nrows, int nthreads) {
+                    double* lse, const int64_t* rows, int64_t nrows, int nthreads) {
     if (nrows <= 0) return ORACLE_OK;
     if (nthreads <= 0) {
         long c = sysconf(_SC_NPROCESSORS_ONLN);
@@ -194,7 +198,7 @@ static int run_rows(const shape_t* s, const double* q, const double* k, const do
     if (!th || !ws) { free(th); free(ws); return ORACLE_ENOMEM; }
     int status = ORACLE_OK;
     for (int t = 0; t < nthreads; ++t) {
-        ws[t] = (work_t){s, q, k, v, o, rows, nrows * t / nthreads, nrows * (t + 1) / nthreads, ORACLE_OK};
+        ws[t] = (work_t){s, q, k, v, o, lse, rows, nrows * t / nthreads, nrows * (t + 1) / nthreads, ORACLE_OK};
         if (pthread_create(&th[t], NULL, worker, &ws[t]) != 0) { worker(&ws[t]); th[t] = 0; }
     }
     for (int t = 0; t < nthreads; ++t) {
@@ -212,7 +216,16 @@ int oracle_attn_f64(const double* q, const double* k, const double* v, double* o
                     int causal, int window, double scale, int nthreads) {
     shape_t s = {B, Hq, Hkv, M, N, D, causal, window, scale};
     if (check_shape(&s) != ORACLE_OK) return ORACLE_EINVAL;
-    return run_rows(&s, q, k, v, o, NULL, (int64_t)B * Hq * M, nthreads);
+    return run_rows(&s, q, k, v, o, NULL, NULL, (int64_t)B * Hq * M, nthreads);
+}
+
+/* Full output and each row's log-sum-exp lse[B,Hq,M] = ln sum_{j allowed} exp(s_j). */
+int oracle_attn_lse_f64(const double* q, const double* k, const double* v, double* o, double* lse,
+                        int B, int Hq, int Hkv, int M, int N, int D,
+                        int causal, int window, double scale, int nthreads) {
+    shape_t s = {B, Hq, Hkv, M, N, D, causal, window, scale};
+    if (check_shape(&s) != ORACLE_OK) return ORACLE_EINVAL;
+    return run_rows(&s, q, k, v, o, lse, NULL, (int64_t)B * Hq * M, nthreads);
 }
 
 /* Selected rows only: rows[t] = (b*Hq + h)*M + i; o_rows is [nrows, D]. */
@@ -225,7 +238,7 @@ int oracle_attn_rows_f64(const double* q, const double* k, const double* v, doub
     int64_t total = (int64_t)B * Hq * M;
     for (int64_t t = 0; t < nrows; ++t)
         if (rows[t] < 0 || rows[t] >= total) return ORACLE_EINVAL;
-    return run_rows(&s, q, k, v, o_rows, rows, nrows, nthreads);
+    return run_rows(&s, q, k, v, o_rows, NULL, rows, nrows, nthreads);
 }
 
 /* Normalized attention weights of one row over all N keys (0 where masked). */

@@ -15,12 +15,16 @@ from .binding import (  # noqa: F401
     PATH_SIMT,
     AttnError,
     attention,
+    attention_lse,
+    attn_bwd,
+    attn_bwd_workspace_bytes,
     attn_decode_paged,
     attn_decode_paged_workspace_bytes,
     attn_fwd,
     attn_fwd_decode_noalloc,
     attn_fwd_ex,
     attn_fwd_host,
+    attn_fwd_lse,
     attn_merge,
     attn_workspace_bytes,
     last_device_status,

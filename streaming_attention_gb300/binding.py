@@ -66,6 +66,12 @@ def lib() -> ctypes.CDLL:
             L.attn_decode_paged_workspace_bytes.restype = sz
             L.attn_decode_paged.argtypes = [vp] * 6 + [ci] * 11 + [cf, ci, vp, sz, vp]
             L.attn_decode_paged.restype = ci
+            L.attn_fwd_lse.argtypes = [vp] * 5 + [ci] * 8 + [cf, ci, ci, vp, sz, vp]
+            L.attn_fwd_lse.restype = ci
+            L.attn_bwd_workspace_bytes.argtypes = [ci, ci, ci]
+            L.attn_bwd_workspace_bytes.restype = sz
+            L.attn_bwd.argtypes = [vp] * 9 + [ci] * 8 + [cf, ci, vp, sz, vp]
+            L.attn_bwd.restype = ci
             L.attn_version.argtypes = []
             L.attn_version.restype = ci
             _lib = L
@@ -136,6 +142,48 @@ def attn_fwd_ex(q, k, v, o, causal=False, window=0, scale=0.0, path=PATH_AUTO, w
                            int(window), float(scale or 0.0), _DTYPES[q.dtype], int(path), _ptr(workspace),
                            ws_bytes, _stream(stream))
     _check(st, "attn_fwd_ex")
+
+
+def attn_fwd_lse(q, k, v, o, lse, causal=False, window=0, scale=0.0, path=PATH_AUTO, workspace=None,
+                 stream=None) -> None:
+    """C-ABI ``attn_fwd_lse``: writes ``o`` and the per-row log-sum-exp ``lse``
+    (float32 [B, Hq, M]); ``workspace`` None lets the library allocate it."""
+    B, Hq, Hkv, M, N, D = _dims(q, k, v, o)
+    if lse.shape != (B, Hq, M) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, Hq, M] tensor")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().attn_fwd_lse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, M, N, D,
+                            int(bool(causal)), int(window), float(scale or 0.0), _DTYPES[q.dtype], int(path),
+                            _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "attn_fwd_lse")
+
+
+def attention_lse(q, k, v, causal=False, window=0, scale=0.0, path=PATH_AUTO, stream=None):
+    """New output and log-sum-exp tensors, then the forward into them: (o, lse)."""
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    attn_fwd_lse(q, k, v, o, lse, causal, window, scale, path, None, stream)
+    return o, lse
+
+
+def attn_bwd_workspace_bytes(B, Hq, M) -> int:
+    return int(lib().attn_bwd_workspace_bytes(B, Hq, M))
+
+
+def attn_bwd(q, k, v, o, d_o, lse, dq, dk, dv, causal=False, window=0, scale=0.0, workspace=None,
+             stream=None) -> None:
+    """C-ABI ``attn_bwd``: writes dq, dk, dv (shapes and dtype of q, k, v)."""
+    B, Hq, Hkv, M, N, D = _dims(q, k, v, o)
+    for t, ref in ((d_o, q), (dq, q), (dk, k), (dv, k)):
+        if tuple(t.shape) != tuple(ref.shape) or t.dtype != q.dtype or not t.is_contiguous():
+            raise ValueError("d_o/dq must match q and dk/dv must match k (shape, dtype, contiguous)")
+    if lse.shape != (B, Hq, M) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, Hq, M] tensor")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(d_o), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                        B, Hq, Hkv, M, N, D, int(bool(causal)), int(window), float(scale or 0.0), _DTYPES[q.dtype],
+                        _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "attn_bwd")
 
 
 def attention(q, k, v, causal=False, window=0, scale=0.0, path=PATH_AUTO, stream=None) -> torch.Tensor:

@@ -66,6 +66,7 @@ int validate(const void* q, const void* k, const void* v, const void* o, int B, 
     key_range(M - 1 + N - M, N, p->causal, p->window, &lo1, &hi1);
     p->klo = lo0;
     p->khi = hi1 > lo0 ? hi1 : lo0;
+    p->lse = nullptr;
     return ATTN_OK;
 }
 
@@ -92,7 +93,8 @@ int run(const Problem& p, const void* q, const void* k, const void* v, void* o, 
     if (path == ATTN_PATH_PREFILL && p.D != 64 && p.D != 128) return ATTN_ERR_HEADDIM;
     if (path == ATTN_PATH_DECODE && !decode_supported(p)) return ATTN_ERR_HEADDIM;
     if (empty_output(p)) return ATTN_OK;
-    if (p.N == 0) {  // every row sees no key: output 0
+    if (p.N == 0) {  // every row sees no key: output 0 (and a log-sum-exp of -inf)
+        if (p.lse) return cuda_status(launch_simt(p, q, k, v, o, 0, 1, nullptr, stream));
         const size_t bytes = (size_t)p.B * p.Hq * p.M * p.D * 2;
         return cuda_status(cudaMemsetAsync(o, 0, bytes, stream));
     }
@@ -114,8 +116,8 @@ int run(const Problem& p, const void* q, const void* k, const void* v, void* o, 
             SplitWorkspace w = split_workspace(ws, rows, S, p.D);
             cudaError_t e = launch_decode(p, q, k, v, chunk, S, w, status, stream);
             if (e != cudaSuccess) return ATTN_ERR_CUDA;
-            return cuda_status(launch_merge(w.m, w.l, w.acc, o, nullptr, nullptr, rows, S, p.D, p.dtype, 1.0f,
-                                            true, stream));
+            return cuda_status(launch_merge(w.m, w.l, w.acc, o, nullptr, nullptr, p.lse, rows, S, p.D, p.dtype,
+                                            1.0f, true, stream));
         }
         default:
             return ATTN_ERR_PATH;
@@ -178,6 +180,27 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq
     return rc;
 }
 
+int attn_fwd_lse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int M,
+                 int N, int D, int causal, int window, float scale, int dtype, int path, void* workspace,
+                 size_t ws_bytes, void* stream) {
+    if (path < ATTN_PATH_AUTO || path > ATTN_PATH_DECODE) return ATTN_ERR_PATH;
+    Problem p;
+    int rc = validate(q, k, v, o, B, Hq, Hkv, M, N, D, causal, window, scale, dtype, &p);
+    if (rc != ATTN_OK) return rc;
+    if (!empty_output(p) && !lse) return ATTN_ERR_NULL;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_ALIGN;
+    p.lse = lse;
+    path = choose_path(p, path);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t bytes = empty_output(p) || p.N == 0 ? 0 : workspace_for(p, path);
+    if (workspace || bytes == 0) return run(p, q, k, v, o, path, workspace, ws_bytes, s);
+    void* ws = nullptr;
+    if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    rc = run(p, q, k, v, o, path, ws, bytes, s);
+    if (cudaFreeAsync(ws, s) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
+    return rc;
+}
+
 size_t attn_workspace_bytes(int B, int Hq, int Hkv, int M, int N, int D, int causal, int window, int path) {
     Problem p;
     // placeholder non-null pointers: only the shape is checked here
@@ -196,7 +219,7 @@ int attn_merge(const float* m, const float* l, const float* acc, void* o, float*
     if ((int64_t)rows * S * D > kI32Max) return ATTN_ERR_OVERFLOW;
     if (rows == 0) return ATTN_OK;
     if (!m || !l || !acc || !o) return ATTN_ERR_NULL;
-    return cuda_status(launch_merge(m, l, acc, o, m_out, l_out, rows, S, D, out_dtype, kLog2e, false,
+    return cuda_status(launch_merge(m, l, acc, o, m_out, l_out, nullptr, rows, S, D, out_dtype, kLog2e, false,
                                     static_cast<cudaStream_t>(stream)));
 }
 
@@ -247,5 +270,52 @@ int attn_last_device_status(void* stream) {
 }
 
 int attn_version(void) { return 100; }
+
+}  // extern "C"
+
+extern "C" {
+
+size_t attn_bwd_workspace_bytes(int B, int Hq, int M) {
+    if (B < 0 || Hq < 0 || M < 0) return 0;
+    if ((int64_t)B * Hq * M == 0) return 0;
+    return bwd_workspace_bytes(B, Hq, M);
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* d_o, const float* lse, void* dq,
+             void* dk, void* dv, int B, int Hq, int Hkv, int M, int N, int D, int causal, int window, float scale,
+             int dtype, void* workspace, size_t ws_bytes, void* stream) {
+    Problem p;
+    int rc = validate(q, k, v, o, B, Hq, Hkv, M, N, D, causal, window, scale, dtype, &p);
+    if (rc != ATTN_OK) return rc;
+    if (D != 64 && D != 128) return ATTN_ERR_HEADDIM;
+    const int64_t nq = (int64_t)B * Hq * M * D, nk = (int64_t)B * Hkv * N * D;
+    if ((nq > 0 && (!d_o || !lse || !dq)) || (nk > 0 && (!dk || !dv))) return ATTN_ERR_NULL;
+    if ((d_o && !aligned16(d_o)) || (dq && !aligned16(dq)) || (dk && !aligned16(dk)) || (dv && !aligned16(dv)) ||
+        (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+        return ATTN_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // no query row, or no key: the gradients that exist are zero
+    if (nq == 0 || nk == 0) {
+        if (nq > 0 && cudaMemsetAsync(dq, 0, (size_t)nq * 2, s) != cudaSuccess) return ATTN_ERR_CUDA;
+        if (nk > 0 && (cudaMemsetAsync(dk, 0, (size_t)nk * 2, s) != cudaSuccess ||
+                       cudaMemsetAsync(dv, 0, (size_t)nk * 2, s) != cudaSuccess))
+            return ATTN_ERR_CUDA;
+        return ATTN_OK;
+    }
+    int* status = status_ptr();
+    if (!status) return ATTN_ERR_CUDA;
+    BwdArgs a{q, k, v, o, d_o, lse, dq, dk, dv};
+    const size_t need = bwd_workspace_bytes(B, Hq, M);
+    if (workspace) {
+        if (ws_bytes < need) return ATTN_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
+        return cuda_status(launch_bwd(p, a, workspace, status, s));
+    }
+    void* ws = nullptr;
+    if (cudaMallocAsync(&ws, need, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    rc = cuda_status(launch_bwd(p, a, ws, status, s));
+    if (cudaFreeAsync(ws, s) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
+    return rc;
+}
 
 }  // extern "C"

@@ -1,0 +1,638 @@
+// Backward pass of the streaming attention forward on the tcgen05 tensor
+// cores (sm_103a), D in {64, 128}.
+//
+// With the forward's per-row log-sum-exp (lse) the weights of any (row, key)
+// pair are recomputed exactly, P = exp(scale s - lse), so the backward needs
+// no running state. Each row of dS is the softmax vector-Jacobian product of
+// that row, dS = P * (dP - delta) with dP = dO V^T and delta = sum_j P dP =
+// rowsum(dO * O) ("Intermediate and advanced kernel workshops", workshop I2,
+// softmax backward; the answer key's I2 row: one FP32 reduction, then the
+// probability-weighted difference). Then dV = P^T dO, dK = scale dS^T Q and
+// dQ = scale dS K.
+//
+// Two kernels, each owning its outputs, so no output is ever accumulated
+// across CTAs:
+//   dK/dV kernel: one CTA per (128-key tile, KV head); K and V stay in shared
+//     memory while the query tiles of all G query heads of the group stream
+//     through a 2-stage TMA ring (Q, dO, and their rows' lse and delta).
+//     S^T = K Q^T and dP^T = V dO^T land in TMEM (TMEM lane = key); the four
+//     elementwise warps turn them into P^T and dS^T (16-bit, written over the
+//     first half of each), and the MMA warp accumulates dV += P^T dO and
+//     dK += dS^T Q in TMEM.
+//   dQ kernel: one CTA per (128-row query tile, query head); Q and dO stay,
+//     K and V tiles stream; S = Q K^T and dP = dO V^T in TMEM (lane = row),
+//     dS over dP, dQ += dS K.
+// S and dP are thus computed twice (7 products instead of 5); in exchange
+// neither kernel needs atomics or a transpose through shared memory.
+// Tiles outside the causal / window range are skipped; only edge tiles mask.
+// Every wait is bounded (1 s); on expiry a CTA sets the device status word,
+// drains its copies and MMAs, frees TMEM and exits.
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "attn_internal.h"
+#include "sm100_ptx.cuh"
+#include "tma_map.h"
+
+namespace attn {
+namespace {
+
+using namespace ptx;
+
+constexpr int BT = 128;           // query rows per query tile and keys per key tile
+constexpr int kBwdThreads = 192;  // warps 0-3 elementwise, 4 TMA, 5 MMA
+constexpr int kBLoadWarp = 4, kBMmaWarp = 5;
+constexpr uint64_t kBwdTimeoutNs = 1000000000ull;
+
+// Shared memory: two stationary tiles, a 2-stage ring of tile pairs, the
+// per-row vectors of each stage (dK/dV kernel), barriers.
+template <int D>
+struct BCfg {
+    static constexpr int kTile = BT * D * 2;  // one [128][D] 16-bit tile
+    static constexpr int kChunk = BT * 128;   // one 64-column (128-byte) chunk of a tile
+    static constexpr int kChunks = D / 64;
+    static constexpr int kStages = 2;
+    static constexpr int kOffStat = 0;                                  // 2 stationary tiles
+    static constexpr int kOffStage = 2 * kTile;                         // stage s: 2 tiles at + s * 2 * kTile
+    static constexpr int kOffVec = kOffStage + kStages * 2 * kTile;     // stage s: lse2[128], delta[128]
+    static constexpr int kOffBar = kOffVec + kStages * 2 * BT * 4;
+    // stat_full, full[2], empty[2], st_full, p_full, done, drain
+    static constexpr int kNumBars = 1 + 2 * kStages + 4;
+    static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+    static constexpr int kSmem = kOffMisc + 16 + 1024;
+    // TMEM columns
+    static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + D;
+};
+
+struct BwdParams {
+    void* out0;          // dK (dK/dV kernel) or dQ (dQ kernel)
+    void* out1;          // dV (dK/dV kernel)
+    const float* lse2;   // [B*Hq][Mpad]: lse * log2(e); -inf past M
+    const float* delta;  // [B*Hq][Mpad]: rowsum(dO * O); 0 past M
+    int* status;
+    int Hq, Hkv, M, N, G, Mpad;
+    int causal, window;
+    float scale, scale_log2;
+    int groups;  // B * Hkv (dK/dV) or B * Hq (dQ)
+    int ntile;   // key tiles (dK/dV) or query tiles (dQ)
+};
+
+__device__ bool bwait_one(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag, int* status,
+                          bool abortable = true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (abortable && *abort_flag) return false;
+        if (globaltimer_ns() - t0 > kBwdTimeoutNs) {
+            *abort_flag = 1u;
+            atomicExch(status, 1);
+            return false;
+        }
+    }
+}
+
+__device__ bool bwait_warp(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag, int* status) {
+    const int lane = threadIdx.x & 31;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        const bool done = mbar_try_wait(bar, parity);
+        if (__all_sync(0xffffffffu, done)) return true;
+        int stop = 0;
+        if (lane == 0) {
+            if (*abort_flag) {
+                stop = 1;
+            } else if (globaltimer_ns() - t0 > kBwdTimeoutNs) {
+                *abort_flag = 1u;
+                atomicExch(status, 1);
+                stop = 1;
+            }
+        }
+        if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+    }
+}
+
+// C = A B^T over D (both operands K-major [128][D] tiles, 128 x 128 result)
+template <int D>
+__device__ __forceinline__ void mma_rows_by_rows(uint32_t d_tmem, uint64_t a0, uint64_t b0, uint32_t idesc) {
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off = (uint64_t)((((kk >> 2) * BCfg<D>::kChunk) + (kk & 3) * 32) >> 4);
+        mma_ss(d_tmem, a0 + off, b0 + off, idesc, kk > 0 ? 1u : 0u);
+    }
+}
+// C (+)= A B over 128: A 16-bit in TMEM (128 lanes x 128 along K), B a [128][D]
+// tile read MN-major (N = D)
+__device__ __forceinline__ void mma_tmem_by_tile(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0, uint32_t idesc,
+                                                 bool first) {
+#pragma unroll
+    for (int kk = 0; kk < BT / 16; ++kk)
+        mma_ts(d_tmem, a_tmem + kk * 8, b0 + (uint64_t)((kk * 16 * 128) >> 4), idesc, (first && kk == 0) ? 0u : 1u);
+}
+
+template <bool kBF16>
+__device__ __forceinline__ uint32_t bpack2(float lo, float hi) {
+    return kBF16 ? pack_bf16(lo, hi) : pack_f16(lo, hi);
+}
+
+// Writes one [D] row of FP32 TMEM columns (this thread's lane) as 16-bit values.
+template <int D, bool kBF16>
+__device__ __forceinline__ void store_row(uint32_t taddr, float mul, uint16_t* dst, bool write) {
+#pragma unroll
+    for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld_x32(taddr + ch * 32, v);
+        tmem_wait_ld_x32(v);
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+            w[e] = bpack2<kBF16>(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+        if (write) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 32);
+#pragma unroll
+            for (int x = 0; x < 4; ++x) d4[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+        }
+    }
+}
+
+// Shared setup of both kernels: barriers, TMEM (512 columns), abort flag.
+struct BSetup {
+    uint32_t sbase, bar_stat, bar_full0, bar_empty0, bar_st, bar_p, bar_done, bar_drain, tmem;
+    volatile uint32_t* abort_flag;
+    __device__ uint32_t full(int s) const { return bar_full0 + 8u * s; }
+    __device__ uint32_t empty(int s) const { return bar_empty0 + 8u * s; }
+};
+
+template <int D>
+__device__ __forceinline__ BSetup bwd_setup(uint8_t* smem) {
+    using C = BCfg<D>;
+    BSetup b;
+    b.sbase = smem_u32(smem);
+    b.bar_stat = b.sbase + C::kOffBar;
+    b.bar_full0 = b.bar_stat + 8;
+    b.bar_empty0 = b.bar_full0 + 8 * C::kStages;
+    b.bar_st = b.bar_empty0 + 8 * C::kStages;
+    b.bar_p = b.bar_st + 8;
+    b.bar_done = b.bar_p + 8;
+    b.bar_drain = b.bar_done + 8;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc);
+    b.abort_flag = tmem_slot + 1;
+    if (threadIdx.x == 0) {
+        mbar_init(b.bar_stat, 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(b.full(s), 1);
+            mbar_init(b.empty(s), 1);
+        }
+        mbar_init(b.bar_st, 1);
+        mbar_init(b.bar_p, 4 * 32);
+        mbar_init(b.bar_done, 1);
+        mbar_init(b.bar_drain, 1);
+        *b.abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if ((threadIdx.x >> 5) == kBMmaWarp) {
+        tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    b.tmem = *tmem_slot;
+    return b;
+}
+
+__device__ __forceinline__ void bwd_teardown(const BSetup& b) {
+    tc_fence_before();
+    __syncthreads();
+    if ((threadIdx.x >> 5) == kBMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(b.tmem, 512);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// dK / dV: one CTA per (128-key tile, KV head)
+// ---------------------------------------------------------------------------
+template <int D, bool kBF16>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                         const BwdParams p) {
+    using C = BCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const BSetup bs = bwd_setup<D>(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // tile 0 of every group first: under a causal mask it sees the most query rows
+    const int jt = blockIdx.x / p.groups, grp = blockIdx.x % p.groups;
+    const int b = grp / p.Hkv, g = grp % p.Hkv;
+    const int k0 = jt * BT, k1 = min(k0 + BT, p.N);
+    const int off = p.N - p.M;  // query row i sits at key position i + off
+    // query rows that see a key of [k0, k1): causal needs i + off >= k0, a window
+    // needs i + off < (k1 - 1) + window
+    int i_lo = 0, i_hi = p.M;
+    if (p.causal) i_lo = max(0, k0 - off);
+    if (p.window > 0) i_hi = min(p.M, k1 - 1 + p.window - off);
+    const int qt0 = i_lo / BT;
+    const int nq = i_hi > i_lo ? (i_hi + BT - 1) / BT - qt0 : 0;
+    const int T = p.G * nq;  // (query head of the group, query tile) pairs
+
+    if (warp == kBLoadWarp) {
+        if (lane == 0 && T > 0) {
+            prefetch_tmap(&tmQ);
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+            prefetch_tmap(&tmdO);
+            mbar_arrive_expect_tx(bs.bar_stat, 2 * C::kTile);
+            for (int c = 0; c < C::kChunks; ++c) {
+                tma_load_3d(bs.sbase + C::kOffStat + c * C::kChunk, &tmK, c * 64, k0, grp, bs.bar_stat);
+                tma_load_3d(bs.sbase + C::kOffStat + C::kTile + c * C::kChunk, &tmV, c * 64, k0, grp, bs.bar_stat);
+            }
+            int issued = 0;
+            for (int it = 0; it < T; ++it) {
+                const int s = it & 1;
+                if (it >= 2 && !bwait_one(bs.empty(s), ((it >> 1) - 1) & 1, bs.abort_flag, p.status)) break;
+                const int h = g * p.G + it / nq, i0 = (qt0 + it % nq) * BT;
+                const int bh = b * p.Hq + h;
+                mbar_arrive_expect_tx(bs.full(s), 2 * C::kTile + 2 * BT * 4);
+                const uint32_t dq = bs.sbase + C::kOffStage + s * 2 * C::kTile;
+                for (int c = 0; c < C::kChunks; ++c) {
+                    tma_load_3d(dq + c * C::kChunk, &tmQ, c * 64, i0, bh, bs.full(s));
+                    tma_load_3d(dq + C::kTile + c * C::kChunk, &tmdO, c * 64, i0, bh, bs.full(s));
+                }
+                const uint32_t vec = bs.sbase + C::kOffVec + s * 2 * BT * 4;
+                bulk_g2s(vec, p.lse2 + (size_t)bh * p.Mpad + i0, BT * 4, bs.full(s));
+                bulk_g2s(vec + BT * 4, p.delta + (size_t)bh * p.Mpad + i0, BT * 4, bs.full(s));
+                issued = it + 1;
+            }
+            // every issued copy lands before the CTA may exit
+            bwait_one(bs.bar_stat, 0, bs.abort_flag, p.status, false);
+            for (int x = max(0, issued - 2); x < issued; ++x)
+                bwait_one(bs.full(x & 1), (x >> 1) & 1, bs.abort_flag, p.status, false);
+        }
+    } else if (warp == kBMmaWarp) {
+        if (lane == 0 && T > 0) {
+            constexpr uint32_t idS = idesc_f16(kBF16, BT, BT, false);
+            constexpr uint32_t idAcc = idesc_f16(kBF16, BT, D, true);
+            const uint64_t dK = sw128_desc(bs.sbase + C::kOffStat, 16, 1024);
+            const uint64_t dV = sw128_desc(bs.sbase + C::kOffStat + C::kTile, 16, 1024);
+            bool ok = bwait_one(bs.bar_stat, 0, bs.abort_flag, p.status);
+            for (int it = 0; ok && it < T; ++it) {
+                const int s = it & 1;
+                if (!(ok = bwait_one(bs.full(s), (it >> 1) & 1, bs.abort_flag, p.status))) break;
+                tc_fence_after();
+                const uint32_t sq = bs.sbase + C::kOffStage + s * 2 * C::kTile, sdo = sq + C::kTile;
+                mma_rows_by_rows<D>(bs.tmem + C::kColS, dK, sw128_desc(sq, 16, 1024), idS);    // S^T = K Q^T
+                mma_rows_by_rows<D>(bs.tmem + C::kColDP, dV, sw128_desc(sdo, 16, 1024), idS);  // dP^T = V dO^T
+                mma_commit(bs.bar_st);
+                if (!(ok = bwait_one(bs.bar_p, it & 1, bs.abort_flag, p.status))) break;
+                tc_fence_after();
+                // dV += P^T dO and dK += dS^T Q (P^T, dS^T over the first 64 columns of S^T, dP^T)
+                mma_tmem_by_tile(bs.tmem + C::kColAcc1, bs.tmem + C::kColS, sw128_desc(sdo, C::kChunk, 1024), idAcc,
+                                 it == 0);
+                mma_tmem_by_tile(bs.tmem + C::kColAcc0, bs.tmem + C::kColDP, sw128_desc(sq, C::kChunk, 1024), idAcc,
+                                 it == 0);
+                mma_commit(bs.empty(s));
+            }
+            if (ok) mma_commit(bs.bar_done);
+            mma_commit(bs.bar_drain);
+            bwait_one(bs.bar_drain, 0, bs.abort_flag, p.status, false);
+        }
+        __syncwarp();
+    } else {
+        // elementwise: thread = key of the tile (TMEM lane); columns = query rows
+        const int kl = threadIdx.x;
+        const int key = k0 + kl;
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const float c = p.scale_log2;
+        bool ok = true;
+        for (int it = 0; it < T; ++it) {
+            const int s = it & 1;
+            const int i0 = (qt0 + it % nq) * BT;
+            if (!(ok = bwait_warp(bs.bar_st, it & 1, bs.abort_flag, p.status))) break;
+            // the stage's row vectors came by bulk copy: observe their barrier too (its
+            // phase cannot move on before this tile's products, which need p_full)
+            if (!(ok = bwait_warp(bs.full(s), (it >> 1) & 1, bs.abort_flag, p.status))) break;
+            tc_fence_after();
+            const float* lse2 = reinterpret_cast<const float*>(smem + C::kOffVec + s * 2 * BT * 4);
+            const float* del = lse2 + BT;
+            const bool need_mask = (i0 + BT > p.M) || (k0 + BT > p.N) ||
+                                   (p.causal && k0 + BT - 1 > i0 + off) ||
+                                   (p.window > 0 && k0 <= i0 + BT - 1 + off - p.window);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t sv[32], dpv[32];
+                tmem_ld_x32(bs.tmem + lane_base + C::kColS + q4 * 32, sv);
+                tmem_ld_x32(bs.tmem + lane_base + C::kColDP + q4 * 32, dpv);
+                tmem_wait_ld_x32(sv);
+                reg_after_x32(dpv);
+                uint32_t pk[16], dk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    float pr[2], ds[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int r = q4 * 32 + 2 * e + u;
+                        float pv = ex2(fmaf(__uint_as_float(sv[2 * e + u]), c, -lse2[r]));
+                        if (need_mask) {
+                            const int pos = i0 + r + off;
+                            const bool vis = key < p.N && i0 + r < p.M && (!p.causal || key <= pos) &&
+                                             (p.window <= 0 || key > pos - p.window);
+                            pv = vis ? pv : 0.f;
+                        }
+                        pr[u] = pv;
+                        ds[u] = pv * (__uint_as_float(dpv[2 * e + u]) - del[r]);
+                    }
+                    pk[e] = bpack2<kBF16>(pr[0], pr[1]);
+                    dk[e] = bpack2<kBF16>(ds[0], ds[1]);
+                }
+                tmem_st_x16(bs.tmem + lane_base + C::kColS + q4 * 16, pk);
+                tmem_st_x16(bs.tmem + lane_base + C::kColDP + q4 * 16, dk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bs.bar_p);
+        }
+        uint16_t* dk_row = reinterpret_cast<uint16_t*>(p.out0) + ((size_t)grp * p.N + key) * D;
+        uint16_t* dv_row = reinterpret_cast<uint16_t*>(p.out1) + ((size_t)grp * p.N + key) * D;
+        const bool write = key < p.N;
+        if (T == 0) {  // no query row sees these keys: zero gradients
+            if (write) {
+#pragma unroll
+                for (int x = 0; x < D / 8; ++x) {
+                    reinterpret_cast<uint4*>(dk_row)[x] = make_uint4(0, 0, 0, 0);
+                    reinterpret_cast<uint4*>(dv_row)[x] = make_uint4(0, 0, 0, 0);
+                }
+            }
+        } else if (ok && bwait_warp(bs.bar_done, 0, bs.abort_flag, p.status)) {
+            tc_fence_after();
+            store_row<D, kBF16>(bs.tmem + lane_base + C::kColAcc0, p.scale, dk_row, write);
+            store_row<D, kBF16>(bs.tmem + lane_base + C::kColAcc1, 1.f, dv_row, write);
+        }
+    }
+    bwd_teardown(bs);
+}
+
+// ---------------------------------------------------------------------------
+// dQ: one CTA per (128-row query tile, query head)
+// ---------------------------------------------------------------------------
+template <int D, bool kBF16>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                       const BwdParams p) {
+    using C = BCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const BSetup bs = bwd_setup<D>(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // the last query tile of every head first: under a causal mask it sees the most keys
+    const int qt = p.ntile - 1 - (int)(blockIdx.x / p.groups), bh = blockIdx.x % p.groups;
+    const int b = bh / p.Hq, h = bh % p.Hq;
+    const int grp = b * p.Hkv + h / p.G;
+    const int i0 = qt * BT, i_last = min(i0 + BT, p.M) - 1;
+    const int off = p.N - p.M;
+    int lo = 0, hi = 0, unused = 0;
+    key_range(i0 + off, p.N, p.causal, p.window, &lo, &unused);
+    key_range(i_last + off, p.N, p.causal, p.window, &unused, &hi);
+    const int kt0 = lo / BT;
+    const int T = hi > lo ? (hi + BT - 1) / BT - kt0 : 0;  // key tiles
+
+    if (warp == kBLoadWarp) {
+        if (lane == 0 && T > 0) {
+            prefetch_tmap(&tmQ);
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+            prefetch_tmap(&tmdO);
+            mbar_arrive_expect_tx(bs.bar_stat, 2 * C::kTile);
+            for (int c = 0; c < C::kChunks; ++c) {
+                tma_load_3d(bs.sbase + C::kOffStat + c * C::kChunk, &tmQ, c * 64, i0, bh, bs.bar_stat);
+                tma_load_3d(bs.sbase + C::kOffStat + C::kTile + c * C::kChunk, &tmdO, c * 64, i0, bh, bs.bar_stat);
+            }
+            int issued = 0;
+            for (int it = 0; it < T; ++it) {
+                const int s = it & 1;
+                if (it >= 2 && !bwait_one(bs.empty(s), ((it >> 1) - 1) & 1, bs.abort_flag, p.status)) break;
+                const int k0 = (kt0 + it) * BT;
+                mbar_arrive_expect_tx(bs.full(s), 2 * C::kTile);
+                const uint32_t dk = bs.sbase + C::kOffStage + s * 2 * C::kTile;
+                for (int c = 0; c < C::kChunks; ++c) {
+                    tma_load_3d(dk + c * C::kChunk, &tmK, c * 64, k0, grp, bs.full(s));
+                    tma_load_3d(dk + C::kTile + c * C::kChunk, &tmV, c * 64, k0, grp, bs.full(s));
+                }
+                issued = it + 1;
+            }
+            bwait_one(bs.bar_stat, 0, bs.abort_flag, p.status, false);
+            for (int x = max(0, issued - 2); x < issued; ++x)
+                bwait_one(bs.full(x & 1), (x >> 1) & 1, bs.abort_flag, p.status, false);
+        }
+    } else if (warp == kBMmaWarp) {
+        if (lane == 0 && T > 0) {
+            constexpr uint32_t idS = idesc_f16(kBF16, BT, BT, false);
+            constexpr uint32_t idAcc = idesc_f16(kBF16, BT, D, true);
+            const uint64_t dQ = sw128_desc(bs.sbase + C::kOffStat, 16, 1024);
+            const uint64_t ddO = sw128_desc(bs.sbase + C::kOffStat + C::kTile, 16, 1024);
+            bool ok = bwait_one(bs.bar_stat, 0, bs.abort_flag, p.status);
+            for (int it = 0; ok && it < T; ++it) {
+                const int s = it & 1;
+                if (!(ok = bwait_one(bs.full(s), (it >> 1) & 1, bs.abort_flag, p.status))) break;
+                tc_fence_after();
+                const uint32_t sk = bs.sbase + C::kOffStage + s * 2 * C::kTile, sv = sk + C::kTile;
+                mma_rows_by_rows<D>(bs.tmem + C::kColS, dQ, sw128_desc(sk, 16, 1024), idS);    // S = Q K^T
+                mma_rows_by_rows<D>(bs.tmem + C::kColDP, ddO, sw128_desc(sv, 16, 1024), idS);  // dP = dO V^T
+                mma_commit(bs.bar_st);
+                if (!(ok = bwait_one(bs.bar_p, it & 1, bs.abort_flag, p.status))) break;
+                tc_fence_after();
+                // dQ += dS K (dS over the first 64 columns of dP)
+                mma_tmem_by_tile(bs.tmem + C::kColAcc0, bs.tmem + C::kColDP, sw128_desc(sk, C::kChunk, 1024), idAcc,
+                                 it == 0);
+                mma_commit(bs.empty(s));
+            }
+            if (ok) mma_commit(bs.bar_done);
+            mma_commit(bs.bar_drain);
+            bwait_one(bs.bar_drain, 0, bs.abort_flag, p.status, false);
+        }
+        __syncwarp();
+    } else {
+        // elementwise: thread = query row of the tile (TMEM lane); columns = keys
+        const int r = threadIdx.x;
+        const int row = i0 + r;
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const float c = p.scale_log2;
+        const float lse2 = p.lse2[(size_t)bh * p.Mpad + row];  // -inf past M
+        const float del = p.delta[(size_t)bh * p.Mpad + row];
+        const int pos = row + off;
+        bool ok = true;
+        for (int it = 0; it < T; ++it) {
+            const int k0 = (kt0 + it) * BT;
+            if (!(ok = bwait_warp(bs.bar_st, it & 1, bs.abort_flag, p.status))) break;
+            tc_fence_after();
+            const bool need_mask = (i0 + BT > p.M) || (k0 + BT > p.N) ||
+                                   (p.causal && k0 + BT - 1 > i0 + off) ||
+                                   (p.window > 0 && k0 <= i0 + BT - 1 + off - p.window);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t sv[32], dpv[32];
+                tmem_ld_x32(bs.tmem + lane_base + C::kColS + q4 * 32, sv);
+                tmem_ld_x32(bs.tmem + lane_base + C::kColDP + q4 * 32, dpv);
+                tmem_wait_ld_x32(sv);
+                reg_after_x32(dpv);
+                uint32_t dk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    float ds[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        float pv = ex2(fmaf(__uint_as_float(sv[2 * e + u]), c, -lse2));
+                        if (need_mask) {
+                            const int key = k0 + q4 * 32 + 2 * e + u;
+                            const bool vis = key < p.N && row < p.M && (!p.causal || key <= pos) &&
+                                             (p.window <= 0 || key > pos - p.window);
+                            pv = vis ? pv : 0.f;
+                        }
+                        ds[u] = pv * (__uint_as_float(dpv[2 * e + u]) - del);
+                    }
+                    dk[e] = bpack2<kBF16>(ds[0], ds[1]);
+                }
+                tmem_st_x16(bs.tmem + lane_base + C::kColDP + q4 * 16, dk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bs.bar_p);
+        }
+        uint16_t* dq_row = reinterpret_cast<uint16_t*>(p.out0) + ((size_t)bh * p.M + row) * D;
+        const bool write = row < p.M;
+        if (T == 0) {  // no key visible to any row of the tile: zero gradient
+            if (write)
+#pragma unroll
+                for (int x = 0; x < D / 8; ++x) reinterpret_cast<uint4*>(dq_row)[x] = make_uint4(0, 0, 0, 0);
+        } else if (ok && bwait_warp(bs.bar_done, 0, bs.abort_flag, p.status)) {
+            tc_fence_after();
+            store_row<D, kBF16>(bs.tmem + lane_base + C::kColAcc0, p.scale, dq_row, write);
+        }
+    }
+    bwd_teardown(bs);
+}
+
+// delta = rowsum(dO * O) and lse2 = lse * log2(e) per row, padded to Mpad rows
+// per head (-inf and 0 past M), one warp per row.
+template <bool kBF16>
+__global__ void __launch_bounds__(256)
+    attn_bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ d_o, const float* __restrict__ lse,
+                        float* lse2, float* delta, int M, int Mpad, int D, int rows_pad) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gr = blockIdx.x * 8 + warp;
+    if (gr >= rows_pad) return;
+    const int bh = gr / Mpad, i = gr % Mpad;
+    if (i >= M) {
+        if (lane == 0) {
+            lse2[gr] = -INFINITY;
+            delta[gr] = 0.f;
+        }
+        return;
+    }
+    const size_t row = (size_t)bh * M + i;
+    float acc = 0.f;
+    for (int d = lane; d < D; d += 32) {
+        const uint16_t a = o[row * D + d], bb = d_o[row * D + d];
+        float fa, fb;
+        if (kBF16) {
+            fa = __uint_as_float((uint32_t)a << 16);
+            fb = __uint_as_float((uint32_t)bb << 16);
+        } else {
+            fa = __half2float(__ushort_as_half(a));
+            fb = __half2float(__ushort_as_half(bb));
+        }
+        acc = fmaf(fa, fb, acc);
+    }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (lane == 0) {
+        delta[gr] = acc;
+        lse2[gr] = lse[row] * kLog2e;
+    }
+}
+
+template <int D, bool kBF16>
+cudaError_t launch_bwd_t(const Problem& pr, const BwdArgs& a, const float* lse2, const float* delta, int Mpad,
+                         int* status, cudaStream_t stream) {
+    using C = BCfg<D>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        C::kSmem);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(attn_bwd_dq_kernel<D, kBF16>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    const int rows_pad = pr.B * pr.Hq * Mpad;
+    attn_bwd_pre_kernel<kBF16><<<(rows_pad + 7) / 8, 256, 0, stream>>>(
+        static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.d_o), a.lse, const_cast<float*>(lse2),
+        const_cast<float*>(delta), pr.M, Mpad, D, rows_pad);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    CUtensorMap tq, tk, tv, tdo;
+    if (!make_tensor_map(&tq, a.q, D, pr.M, pr.B * pr.Hq, BT, kBF16) ||
+        !make_tensor_map(&tdo, a.d_o, D, pr.M, pr.B * pr.Hq, BT, kBF16) ||
+        !make_tensor_map(&tk, a.k, D, pr.N, pr.B * pr.Hkv, BT, kBF16) ||
+        !make_tensor_map(&tv, a.v, D, pr.N, pr.B * pr.Hkv, BT, kBF16))
+        return cudaErrorInvalidValue;
+    BwdParams bp = {};
+    bp.lse2 = lse2;
+    bp.delta = delta;
+    bp.status = status;
+    bp.Hq = pr.Hq;
+    bp.Hkv = pr.Hkv;
+    bp.M = pr.M;
+    bp.N = pr.N;
+    bp.G = pr.G;
+    bp.Mpad = Mpad;
+    bp.causal = pr.causal;
+    bp.window = pr.window;
+    bp.scale = pr.scale;
+    bp.scale_log2 = pr.scale_log2;
+    // dK, dV
+    bp.out0 = a.dk;
+    bp.out1 = a.dv;
+    bp.groups = pr.B * pr.Hkv;
+    bp.ntile = (pr.N + BT - 1) / BT;
+    attn_bwd_dkdv_kernel<D, kBF16><<<bp.groups * bp.ntile, kBwdThreads, C::kSmem, stream>>>(tq, tk, tv, tdo, bp);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // dQ
+    bp.out0 = a.dq;
+    bp.out1 = nullptr;
+    bp.groups = pr.B * pr.Hq;
+    bp.ntile = (pr.M + BT - 1) / BT;
+    attn_bwd_dq_kernel<D, kBF16><<<bp.groups * bp.ntile, kBwdThreads, C::kSmem, stream>>>(tq, tk, tv, tdo, bp);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t bwd_workspace_bytes(int B, int Hq, int M) {
+    const size_t Mpad = ((size_t)M + BT - 1) / BT * BT;
+    const size_t part = ((size_t)B * Hq * Mpad * sizeof(float) + 255) & ~(size_t)255;
+    return 2 * part;
+}
+
+cudaError_t launch_bwd(const Problem& p, const BwdArgs& a, void* ws, int* status, cudaStream_t stream) {
+    const int Mpad = (p.M + BT - 1) / BT * BT;
+    const size_t part = ((size_t)p.B * p.Hq * Mpad * sizeof(float) + 255) & ~(size_t)255;
+    const float* lse2 = static_cast<const float*>(ws);
+    const float* delta = reinterpret_cast<const float*>(static_cast<const char*>(ws) + part);
+    const bool bf = p.dtype == ATTN_BF16;
+    if (p.D == 128)
+        return bf ? launch_bwd_t<128, true>(p, a, lse2, delta, Mpad, status, stream)
+                  : launch_bwd_t<128, false>(p, a, lse2, delta, Mpad, status, stream);
+    if (p.D == 64)
+        return bf ? launch_bwd_t<64, true>(p, a, lse2, delta, Mpad, status, stream)
+                  : launch_bwd_t<64, false>(p, a, lse2, delta, Mpad, status, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace attn

@@ -9,6 +9,7 @@
 namespace attn {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 
 // One forward problem, validated. Positions follow the bottom-right rule
 // p_i = i + N - M; klo/khi bound the keys that any row of the problem may see.
@@ -20,6 +21,7 @@ struct Problem {
     int dtype;         // ATTN_BF16 / ATTN_FP16
     int G;             // Hq / Hkv
     int klo, khi;      // union of the visible key ranges over all rows
+    float* lse;        // optional [B*Hq*M] natural-log sum of exp of the logits (nullptr: not written)
 };
 
 // Keys [lo, hi) visible to the query at position p (hi <= lo: none).
@@ -49,7 +51,7 @@ SplitWorkspace split_workspace(void* base, int rows, int S, int D);
 cudaError_t launch_simt(const Problem& p, const void* q, const void* k, const void* v, void* o,
                         int chunk, int S, const SplitWorkspace* ws, cudaStream_t stream);
 cudaError_t launch_merge(const float* m, const float* l, const float* acc, void* o, float* m_out,
-                         float* l_out, int rows, int S, int D, int out_dtype, float unit,
+                         float* l_out, float* lse_out, int rows, int S, int D, int out_dtype, float unit,
                          bool programmatic, cudaStream_t stream);
 cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const void* v,
                           int chunk, int S, const SplitWorkspace& ws, int* status,
@@ -75,6 +77,15 @@ struct PagedKV {
 int decode_plan_paged(const Problem& p, const PagedKV& kv, int* chunk, int* S);
 cudaError_t launch_decode_paged(const Problem& p, const void* q, const PagedKV& kv, int chunk, int S,
                                 const SplitWorkspace& ws, int* status, cudaStream_t stream);
+
+// Backward pass (tcgen05, D in {64, 128}): the caller's tensors, device pointers.
+struct BwdArgs {
+    const void *q, *k, *v, *o, *d_o;
+    const float* lse;  // [B*Hq*M], natural log, from the forward
+    void *dq, *dk, *dv;
+};
+size_t bwd_workspace_bytes(int B, int Hq, int M);
+cudaError_t launch_bwd(const Problem& p, const BwdArgs& a, void* ws, int* status, cudaStream_t stream);
 
 // Metadata validation and the device status word, shared by every entry point.
 int validate_problem(const void* q, const void* k, const void* v, const void* o, int B, int Hq, int Hkv, int M,

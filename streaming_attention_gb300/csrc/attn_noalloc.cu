@@ -72,7 +72,8 @@ extern "C" int attn_fwd_decode_noalloc(const void* q, const void* k, const void*
     // kernel of this same call, so nothing has to be cleared first.
     SplitWorkspace w = split_workspace(base, rows, S, p.D);
     if (launch_decode(p, q, k, v, chunk, S, w, status, s) != cudaSuccess) return ATTN_ERR_CUDA;
-    if (launch_merge(w.m, w.l, w.acc, o, nullptr, nullptr, rows, S, p.D, p.dtype, 1.0f, true, s) != cudaSuccess)
+    if (launch_merge(w.m, w.l, w.acc, o, nullptr, nullptr, nullptr, rows, S, p.D, p.dtype, 1.0f, true, s) !=
+        cudaSuccess)
         return ATTN_ERR_CUDA;
     return ATTN_OK;
 }

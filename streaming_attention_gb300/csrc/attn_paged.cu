@@ -65,6 +65,7 @@ int validate_paged(const void* q, const void* kp, const void* vp, const int* tab
     p.G = G;
     p.klo = 0;  // per sequence, in the kernel
     p.khi = max_len;
+    p.lse = nullptr;
     c->kv = PagedKV{kp, vp, table, lens, num_pages, page_size, max_pages, max_len};
     return ATTN_OK;
 }
@@ -90,8 +91,8 @@ int run_paged(const PagedCall& c, const void* q, void* o, void* ws, size_t ws_by
     if (!status) return ATTN_ERR_CUDA;
     SplitWorkspace w = split_workspace(ws, rows, S, p.D);
     if (launch_decode_paged(p, q, c.kv, chunk, S, w, status, stream) != cudaSuccess) return ATTN_ERR_CUDA;
-    return cuda_status(launch_merge(w.m, w.l, w.acc, o, nullptr, nullptr, rows, S, p.D, p.dtype, 1.0f, true,
-                                    stream));
+    return cuda_status(
+        launch_merge(w.m, w.l, w.acc, o, nullptr, nullptr, nullptr, rows, S, p.D, p.dtype, 1.0f, true, stream));
 }
 
 }  // namespace

@@ -78,6 +78,7 @@ __host__ __device__ constexpr uint32_t col_o(int t) { return t ? 384u : 256u; }
 
 struct PrefillParams {
     void* o;
+    float* lse;  // optional per-row log-sum-exp (natural log)
     int* status;
     int M, N, Hq, Hkv, G;
     int causal, window;
@@ -357,6 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + ((size_t)wk.bh * p.M + row) * D;
             if (wk.n == 0) {  // no row of this tile sees any key: output 0
                 if (row < p.M) {
+                    if (p.lse) p.lse[(size_t)wk.bh * p.M + row] = -INFINITY;
                     uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
                     for (int v4 = 0; v4 < D / 8; ++v4) dst[v4] = make_uint4(0, 0, 0, 0);
@@ -456,6 +458,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++tc;
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;  // no visible key: output 0
+            // log sum_j e^(scale s_j) = ln 2 * (m_ref + log2 l) (p was taken against m_ref)
+            if (p.lse && row < p.M)
+                p.lse[(size_t)wk.bh * p.M + row] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
             uint32_t w16[D / 2];  // the row as packed 16-bit pairs
 #pragma unroll
             for (int ch = 0; ch < D / 32; ++ch) {
@@ -516,6 +521,7 @@ int launch_t(const Problem& pr, const void* q, const void* k, const void* v, voi
         return ATTN_ERR_CUDA;
     PrefillParams pp;
     pp.o = o;
+    pp.lse = pr.lse;
     pp.status = status;
     pp.M = pr.M;
     pp.N = pr.N;

@@ -57,6 +57,7 @@ struct SimtArgs {
     float scale_log2;
     int klo, khi, kbase, chunk, S;  // splits: [kbase + z*chunk, +chunk) within [klo, khi)
     int partial;  // 1: write (m, l, acc) summaries; 0: write normalized o
+    float* lse;   // optional per-row log-sum-exp (natural log) when writing o
 };
 
 template <typename T, int D>
@@ -156,6 +157,8 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) attn_simt_kernel(SimtArgs 
         }
     } else {
         const float inv = l > 0.f ? 1.f / l : 0.f;  // no visible key: output 0
+        // log sum_j e^(scale s_j) = ln 2 * (m + log2 l); -inf for a row with no key
+        if (a.lse && lane == 0) a.lse[row] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
         T* O = reinterpret_cast<T*>(a.o) + row * D;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) {
@@ -173,8 +176,8 @@ constexpr int kMergeThreads = 256;
 
 __global__ void __launch_bounds__(kMergeThreads)
     attn_merge_kernel(const float* __restrict__ m, const float* __restrict__ l, const float* __restrict__ acc,
-                      void* o, float* m_out, float* l_out, int rows, int S, int D, int out_dtype, float unit,
-                      int programmatic) {
+                      void* o, float* m_out, float* l_out, float* lse_out, int rows, int S, int D, int out_dtype,
+                      float unit, int programmatic) {
     // A programmatically launched successor (the next decode split grid) may start
     // its setup now; it waits for this grid's completion before touching memory.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -210,6 +213,8 @@ __global__ void __launch_bounds__(kMergeThreads)
     if (d == 0) {
         if (m_out) m_out[row] = mx;
         if (l_out) l_out[row] = L;
+        // the merged log-sum-exp in natural log: mx * unit is the base-2 maximum
+        if (lse_out) lse_out[row] = L > 0.f ? (mx * unit + log2f(L)) * kLn2 : -INFINITY;
     }
 }
 
@@ -258,12 +263,13 @@ cudaError_t launch_simt(const Problem& p, const void* q, const void* k, const vo
     a.chunk = ws ? chunk : (p.N > 0 ? p.N : 1);
     a.S = ws ? S : 1;
     a.partial = ws ? 1 : 0;
+    a.lse = ws ? nullptr : p.lse;
     if (p.dtype == ATTN_BF16) return launch_simt_d<__nv_bfloat16>(a, p.D, stream);
     return launch_simt_d<__half>(a, p.D, stream);
 }
 
 cudaError_t launch_merge(const float* m, const float* l, const float* acc, void* o, float* m_out, float* l_out,
-                         int rows, int S, int D, int out_dtype, float unit, bool programmatic,
+                         float* lse_out, int rows, int S, int D, int out_dtype, float unit, bool programmatic,
                          cudaStream_t stream) {
     if (rows == 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
@@ -276,8 +282,8 @@ cudaError_t launch_merge(const float* m, const float* l, const float* acc, void*
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = programmatic ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, attn_merge_kernel, m, l, acc, o, m_out, l_out, rows, S, D, out_dtype, unit,
-                              programmatic ? 1 : 0);
+    return cudaLaunchKernelEx(&cfg, attn_merge_kernel, m, l, acc, o, m_out, l_out, lse_out, rows, S, D, out_dtype,
+                              unit, programmatic ? 1 : 0);
 }
 
 }  // namespace attn

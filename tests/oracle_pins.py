@@ -332,6 +332,125 @@ def pin_paged(orc):
             assert np.allclose(cut, want, rtol=1e-12, atol=1e-12)
 
 
+# --------------------------------------------------------------------------
+# Log-sum-exp of each row
+# --------------------------------------------------------------------------
+def pin_lse(orc):
+    # A3 worked example: logits 0, 0, ln 2 -> ln(1 + 1 + 2) = ln 4
+    fx, q, k, v = a3_inputs()
+    _, lse = orc.attention_lse(q, k, v, scale=1.0)
+    assert abs(lse[0, 0, 0] - math.log(4.0)) < 1e-12
+    # library formula (torch.logsumexp over masked float64 logits), all masks, GQA
+    rng = np.random.default_rng(23)
+    for trial in range(20):
+        Hkv = int(rng.integers(1, 3))
+        Hq = Hkv * int(rng.integers(1, 3))
+        B, M, N, D = 1, int(rng.integers(1, 7)), int(rng.integers(1, 9)), 3
+        causal, window = bool(rng.integers(0, 2)), int(rng.choice([0, 1, 3]))
+        q, k, v = _rand((B, Hq, M, D), 700 + trial), _rand((B, Hkv, N, D), 800 + trial), _rand((B, Hkv, N, D), 900 + trial)
+        scale = 1.0 / math.sqrt(D)
+        o, lse = orc.attention_lse(q, k, v, causal=causal, window=window)
+        qt, kt = torch.from_numpy(q), torch.from_numpy(k).repeat_interleave(Hq // Hkv, dim=1)
+        keep = torch.ones(M, N, dtype=torch.bool)
+        if causal:
+            keep &= torch.ones(M, N, dtype=torch.bool).tril(diagonal=N - M)
+        if window > 0:
+            keep &= torch.ones(M, N, dtype=torch.bool).triu(diagonal=N - M - window + 1)
+        s = (torch.matmul(qt, kt.transpose(-1, -2)) * scale).masked_fill(~keep, float("-inf"))
+        want = torch.logsumexp(s, dim=-1).numpy()
+        assert np.array_equal(np.isinf(lse), np.isinf(want))
+        fin = np.isfinite(want)
+        assert np.allclose(lse[fin], want[fin], rtol=1e-12, atol=1e-12)
+        assert np.allclose(o, library_attention(q, k, v, causal, window, scale), rtol=1e-12, atol=1e-12)
+    # q = 0: every visible logit is 0, so lse = ln(number of visible keys)
+    q0 = np.zeros((1, 1, 6, 2))
+    k0, v0 = _rand((1, 1, 6, 2), 1), _rand((1, 1, 6, 2), 2)
+    _, lse = orc.attention_lse(q0, k0, v0, causal=True, window=4)
+    assert np.allclose(lse[0, 0], np.log([1, 2, 3, 4, 4, 4]), rtol=0, atol=1e-14)
+    # a row with no visible key: -inf
+    _, lse = orc.attention_lse(_rand((1, 1, 3, 2), 3), _rand((1, 1, 1, 2), 4), _rand((1, 1, 1, 2), 5), causal=True)
+    assert lse[0, 0, 0] == -np.inf and lse[0, 0, 1] == -np.inf and np.isfinite(lse[0, 0, 2])
+
+
+# --------------------------------------------------------------------------
+# Backward pass
+# --------------------------------------------------------------------------
+def pin_backward_i2_example(orc):
+    """The answer key's I2 worked answer inside attention: one query row (q = 1,
+    D = 1, scale 1) over two keys with logits ln 0.25 and ln 0.75 has weights
+    y = (0.25, 0.75); values (2, -1) and do = 1 make dP = g = (2, -1), so the
+    logit gradient is the softmax input gradient, and dK = dS * q = dx."""
+    fx = _golden("i2_softmax_vjp_example.json")
+    y, g = np.array(fx["y"]), np.array(fx["g"])
+    q = np.ones((1, 1, 1, 1))
+    k = np.log(y).reshape(1, 1, 2, 1)
+    v = g.reshape(1, 1, 2, 1)
+    do = np.ones((1, 1, 1, 1))
+    dq, dk, dv = orc_backward(q, k, v, do, False, 0, 1.0)
+    assert np.allclose(dk.reshape(-1), fx["dx"], rtol=0, atol=fx["tol"])
+    assert np.allclose(dv.reshape(-1), y, rtol=0, atol=1e-15)            # dv = P^T do
+    assert abs(dq.reshape(-1)[0] - float(np.dot(fx["dx"], np.log(y)))) < 1e-12  # dq = dS k
+
+
+def orc_backward(q, k, v, do, causal, window, scale):
+    import oracle
+    return oracle.attention_backward(q, k, v, do, causal=causal, window=window, scale=scale)
+
+
+def pin_backward_finite_differences(orc):
+    """Central differences of the forward oracle (L = sum do * o) against the
+    backward oracle, for every input element of small cases with every mask."""
+    rng = np.random.default_rng(31)
+    h = 1e-6
+    for causal, window, Hq, Hkv in ((False, 0, 2, 1), (True, 0, 2, 2), (True, 3, 4, 2), (False, 2, 1, 1)):
+        B, M, N, D = 1, 4, 5, 3
+        q, k, v = _rand((B, Hq, M, D), 51), _rand((B, Hkv, N, D), 52), _rand((B, Hkv, N, D), 53)
+        do = rng.standard_normal((B, Hq, M, D))
+        scale = 1.0 / math.sqrt(D)
+        dq, dk, dv = orc_backward(q, k, v, do, causal, window, scale)
+
+        def loss(q_, k_, v_):
+            return float((orc.attention(q_, k_, v_, causal=causal, window=window) * do).sum())
+
+        for x, grad, which in ((q, dq, 0), (k, dk, 1), (v, dv, 2)):
+            for idx in np.ndindex(x.shape):
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += h
+                xm[idx] -= h
+                args_p = [q, k, v]
+                args_m = [q, k, v]
+                args_p[which], args_m[which] = xp, xm
+                fd = (loss(*args_p) - loss(*args_m)) / (2 * h)
+                assert abs(fd - grad[idx]) < 1e-6, (causal, window, which, idx, fd, grad[idx])
+
+
+def pin_backward_autograd(orc):
+    """torch.autograd in float64 (masked softmax built from library routines)."""
+    rng = np.random.default_rng(37)
+    for trial in range(10):
+        Hkv = int(rng.integers(1, 3))
+        Hq = Hkv * int(rng.integers(1, 3))
+        B, M, N, D = int(rng.integers(1, 3)), int(rng.integers(1, 7)), int(rng.integers(1, 8)), 4
+        causal, window = bool(rng.integers(0, 2)), int(rng.choice([0, 2, 3]))
+        q, k, v = _rand((B, Hq, M, D), 60 + trial), _rand((B, Hkv, N, D), 70 + trial), _rand((B, Hkv, N, D), 80 + trial)
+        do = rng.standard_normal((B, Hq, M, D))
+        scale = 1.0 / math.sqrt(D)
+        qt, kt, vt = (torch.from_numpy(x).requires_grad_(True) for x in (q, k, v))
+        kk, vv = kt.repeat_interleave(Hq // Hkv, dim=1), vt.repeat_interleave(Hq // Hkv, dim=1)
+        keep = torch.ones(M, N, dtype=torch.bool)
+        if causal:
+            keep &= torch.ones(M, N, dtype=torch.bool).tril(diagonal=N - M)
+        if window > 0:
+            keep &= torch.ones(M, N, dtype=torch.bool).triu(diagonal=N - M - window + 1)
+        s = (torch.matmul(qt, kk.transpose(-1, -2)) * scale).masked_fill(~keep, float("-inf"))
+        w = torch.nan_to_num(torch.softmax(s, dim=-1), nan=0.0)
+        o = torch.matmul(w, vv)
+        (o * torch.from_numpy(do)).sum().backward()
+        dq, dk, dv = orc_backward(q, k, v, do, causal, window, scale)
+        for got, want in ((dq, qt.grad), (dk, kt.grad), (dv, vt.grad)):
+            assert np.allclose(got, want.numpy(), rtol=1e-11, atol=1e-12), (trial, causal, window)
+
+
 ALL_PINS = [
     pin_a3_worked_example,
     pin_a1_merge_example,
@@ -344,4 +463,8 @@ ALL_PINS = [
     pin_gqa_map,
     pin_rows_and_weights,
     pin_paged,
+    pin_lse,
+    pin_backward_i2_example,
+    pin_backward_finite_differences,
+    pin_backward_autograd,
 ]
