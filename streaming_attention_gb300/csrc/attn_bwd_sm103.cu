@@ -57,8 +57,8 @@ struct BCfg {
     static constexpr int kOffStage = 2 * kTile;                         // stage s: 2 tiles at + s * 2 * kTile
     static constexpr int kOffVec = kOffStage + kStages * 2 * kTile;     // stage s: lse2[128], delta[128]
     static constexpr int kOffBar = kOffVec + kStages * 2 * BT * 4;
-    // stat_full, full[2], empty[2], st_full, p_full, done, drain
-    static constexpr int kNumBars = 1 + 2 * kStages + 4;
+    // stat_full, full[2], empty[2], st_full[2], p_full[2], done, drain
+    static constexpr int kNumBars = 1 + 2 * kStages + 6;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
     static constexpr int kSmem = kOffMisc + 16 + 1024;
     // TMEM columns
@@ -122,14 +122,16 @@ __device__ __forceinline__ void mma_rows_by_rows(uint32_t d_tmem, uint64_t a0, u
         mma_ss(d_tmem, a0 + off, b0 + off, idesc, kk > 0 ? 1u : 0u);
     }
 }
-// C (+)= A B over 128: A 16-bit in TMEM (128 lanes x 128 along K), B a [128][D]
-// tile read MN-major (N = D)
-__device__ __forceinline__ void mma_tmem_by_tile(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0, uint32_t idesc,
+// C (+)= A B over 64: A 16-bit in TMEM (128 lanes x 64 along K), B 64 rows of a
+// [128][D] tile read MN-major (N = D), starting at b0
+__device__ __forceinline__ void mma_tmem_by_half(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0, uint32_t idesc,
                                                  bool first) {
 #pragma unroll
-    for (int kk = 0; kk < BT / 16; ++kk)
+    for (int kk = 0; kk < BT / 32; ++kk)
         mma_ts(d_tmem, a_tmem + kk * 8, b0 + (uint64_t)((kk * 16 * 128) >> 4), idesc, (first && kk == 0) ? 0u : 1u);
 }
+// 64 rows of a swizzled [128][D] tile start 64 * 128 bytes into each 64-column chunk
+constexpr uint32_t kHalfRows = 64 * 128;
 
 template <bool kBF16>
 __device__ __forceinline__ uint32_t bpack2(float lo, float hi) {
@@ -158,10 +160,12 @@ __device__ __forceinline__ void store_row(uint32_t taddr, float mul, uint16_t* d
 
 // Shared setup of both kernels: barriers, TMEM (512 columns), abort flag.
 struct BSetup {
-    uint32_t sbase, bar_stat, bar_full0, bar_empty0, bar_st, bar_p, bar_done, bar_drain, tmem;
+    uint32_t sbase, bar_stat, bar_full0, bar_empty0, bar_st0, bar_p0, bar_done, bar_drain, tmem;
     volatile uint32_t* abort_flag;
     __device__ uint32_t full(int s) const { return bar_full0 + 8u * s; }
     __device__ uint32_t empty(int s) const { return bar_empty0 + 8u * s; }
+    __device__ uint32_t st(int h) const { return bar_st0 + 8u * h; }  // half h of S, dP computed
+    __device__ uint32_t pp(int h) const { return bar_p0 + 8u * h; }   // half h of P / dS written
 };
 
 template <int D>
@@ -172,9 +176,9 @@ __device__ __forceinline__ BSetup bwd_setup(uint8_t* smem) {
     b.bar_stat = b.sbase + C::kOffBar;
     b.bar_full0 = b.bar_stat + 8;
     b.bar_empty0 = b.bar_full0 + 8 * C::kStages;
-    b.bar_st = b.bar_empty0 + 8 * C::kStages;
-    b.bar_p = b.bar_st + 8;
-    b.bar_done = b.bar_p + 8;
+    b.bar_st0 = b.bar_empty0 + 8 * C::kStages;
+    b.bar_p0 = b.bar_st0 + 16;
+    b.bar_done = b.bar_p0 + 16;
     b.bar_drain = b.bar_done + 8;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc);
     b.abort_flag = tmem_slot + 1;
@@ -184,8 +188,10 @@ __device__ __forceinline__ BSetup bwd_setup(uint8_t* smem) {
             mbar_init(b.full(s), 1);
             mbar_init(b.empty(s), 1);
         }
-        mbar_init(b.bar_st, 1);
-        mbar_init(b.bar_p, 4 * 32);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(b.st(h), 1);
+            mbar_init(b.pp(h), 4 * 32);
+        }
         mbar_init(b.bar_done, 1);
         mbar_init(b.bar_drain, 1);
         *b.abort_flag = 0u;
@@ -278,23 +284,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             constexpr uint32_t idAcc = idesc_f16(kBF16, BT, D, true);
             const uint64_t dK = sw128_desc(bs.sbase + C::kOffStat, 16, 1024);
             const uint64_t dV = sw128_desc(bs.sbase + C::kOffStat + C::kTile, 16, 1024);
-            bool ok = bwait_one(bs.bar_stat, 0, bs.abort_flag, p.status);
+            // Half-tile software pipeline: while the elementwise warps work on one
+            // half (64 query rows) of a tile, the tensor core computes the other half's
+            // S^T, dP^T or the previous half's dV, dK products.
+            constexpr uint32_t idH = idesc_f16(kBF16, BT, BT / 2, false);
+            auto stage_q = [&](int it) { return bs.sbase + C::kOffStage + (it & 1) * 2 * C::kTile; };
+            auto issue_sdp = [&](int it, int h) {  // S^T, dP^T of half h of query tile it
+                const uint32_t sq = stage_q(it) + h * kHalfRows;
+                mma_rows_by_rows<D>(bs.tmem + C::kColS + h * 64, dK, sw128_desc(sq, 16, 1024), idH);
+                mma_rows_by_rows<D>(bs.tmem + C::kColDP + h * 64, dV, sw128_desc(sq + C::kTile, 16, 1024), idH);
+                mma_commit(bs.st(h));
+            };
+            bool ok = bwait_one(bs.bar_stat, 0, bs.abort_flag, p.status) &&
+                      bwait_one(bs.full(0), 0, bs.abort_flag, p.status);
+            if (ok) {
+                tc_fence_after();
+                issue_sdp(0, 0);
+                issue_sdp(0, 1);
+            }
             for (int it = 0; ok && it < T; ++it) {
-                const int s = it & 1;
-                if (!(ok = bwait_one(bs.full(s), (it >> 1) & 1, bs.abort_flag, p.status))) break;
-                tc_fence_after();
-                const uint32_t sq = bs.sbase + C::kOffStage + s * 2 * C::kTile, sdo = sq + C::kTile;
-                mma_rows_by_rows<D>(bs.tmem + C::kColS, dK, sw128_desc(sq, 16, 1024), idS);    // S^T = K Q^T
-                mma_rows_by_rows<D>(bs.tmem + C::kColDP, dV, sw128_desc(sdo, 16, 1024), idS);  // dP^T = V dO^T
-                mma_commit(bs.bar_st);
-                if (!(ok = bwait_one(bs.bar_p, it & 1, bs.abort_flag, p.status))) break;
-                tc_fence_after();
-                // dV += P^T dO and dK += dS^T Q (P^T, dS^T over the first 64 columns of S^T, dP^T)
-                mma_tmem_by_tile(bs.tmem + C::kColAcc1, bs.tmem + C::kColS, sw128_desc(sdo, C::kChunk, 1024), idAcc,
-                                 it == 0);
-                mma_tmem_by_tile(bs.tmem + C::kColAcc0, bs.tmem + C::kColDP, sw128_desc(sq, C::kChunk, 1024), idAcc,
-                                 it == 0);
-                mma_commit(bs.empty(s));
+                const uint32_t sq = stage_q(it);
+                for (int h = 0; h < 2; ++h) {
+                    if (!(ok = bwait_one(bs.pp(h), it & 1, bs.abort_flag, p.status))) break;
+                    tc_fence_after();
+                    // dV += P^T dO and dK += dS^T Q over this half's 64 rows
+                    const uint32_t rows = sq + h * kHalfRows;
+                    mma_tmem_by_half(bs.tmem + C::kColAcc1, bs.tmem + C::kColS + h * 64,
+                                     sw128_desc(rows + C::kTile, C::kChunk, 1024), idAcc, it == 0 && h == 0);
+                    mma_tmem_by_half(bs.tmem + C::kColAcc0, bs.tmem + C::kColDP + h * 64,
+                                     sw128_desc(rows, C::kChunk, 1024), idAcc, it == 0 && h == 0);
+                    if (h == 1) mma_commit(bs.empty(it & 1));  // Q, dO of this tile fully read
+                    if (it + 1 < T) {
+                        if (h == 0 && !(ok = bwait_one(bs.full((it + 1) & 1), ((it + 1) >> 1) & 1, bs.abort_flag,
+                                                       p.status)))
+                            break;
+                        tc_fence_after();
+                        issue_sdp(it + 1, h);
+                    }
+                }
             }
             if (ok) mma_commit(bs.bar_done);
             mma_commit(bs.bar_drain);
@@ -308,52 +335,61 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         const float c = p.scale_log2;
         bool ok = true;
-        for (int it = 0; it < T; ++it) {
+        for (int it = 0; ok && it < T; ++it) {
             const int s = it & 1;
             const int i0 = (qt0 + it % nq) * BT;
-            if (!(ok = bwait_warp(bs.bar_st, it & 1, bs.abort_flag, p.status))) break;
-            // the stage's row vectors came by bulk copy: observe their barrier too (its
-            // phase cannot move on before this tile's products, which need p_full)
-            if (!(ok = bwait_warp(bs.full(s), (it >> 1) & 1, bs.abort_flag, p.status))) break;
-            tc_fence_after();
-            const float* lse2 = reinterpret_cast<const float*>(smem + C::kOffVec + s * 2 * BT * 4);
-            const float* del = lse2 + BT;
             const bool need_mask = (i0 + BT > p.M) || (k0 + BT > p.N) ||
                                    (p.causal && k0 + BT - 1 > i0 + off) ||
                                    (p.window > 0 && k0 <= i0 + BT - 1 + off - p.window);
+            const float* lse2 = reinterpret_cast<const float*>(smem + C::kOffVec + s * 2 * BT * 4);
+            const float* del = lse2 + BT;
+            for (int h = 0; h < 2; ++h) {
+                if (!(ok = bwait_warp(bs.st(h), it & 1, bs.abort_flag, p.status))) break;
+                // the stage's row vectors came by bulk copy: observe their barrier too (its
+                // phase cannot move on before this tile's products, which need p_full)
+                if (h == 0 && !(ok = bwait_warp(bs.full(s), (it >> 1) & 1, bs.abort_flag, p.status))) break;
+                tc_fence_after();
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t sv[32], dpv[32];
-                tmem_ld_x32(bs.tmem + lane_base + C::kColS + q4 * 32, sv);
-                tmem_ld_x32(bs.tmem + lane_base + C::kColDP + q4 * 32, dpv);
-                tmem_wait_ld_x32(sv);
-                reg_after_x32(dpv);
-                uint32_t pk[16], dk[16];
+                for (int j = 0; j < 2; ++j) {
+                    const int c0 = h * 64 + j * 32;  // TMEM column = query row of the tile
+                    uint32_t sv[32], dpv[32];
+                    tmem_ld_x32(bs.tmem + lane_base + C::kColS + c0, sv);
+                    tmem_ld_x32(bs.tmem + lane_base + C::kColDP + c0, dpv);
+                    tmem_wait_ld_x32(sv);
+                    reg_after_x32(dpv);
+                    uint32_t pk[16], dk[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float pr[2], ds[2];
+                    for (int g4 = 0; g4 < 8; ++g4) {
+                        const float4 l4 = reinterpret_cast<const float4*>(lse2 + c0)[g4];
+                        const float4 d4 = reinterpret_cast<const float4*>(del + c0)[g4];
+                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+                        float pr[4], ds[4];
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int r = q4 * 32 + 2 * e + u;
-                        float pv = ex2(fmaf(__uint_as_float(sv[2 * e + u]), c, -lse2[r]));
-                        if (need_mask) {
-                            const int pos = i0 + r + off;
-                            const bool vis = key < p.N && i0 + r < p.M && (!p.causal || key <= pos) &&
-                                             (p.window <= 0 || key > pos - p.window);
-                            pv = vis ? pv : 0.f;
+                        for (int u = 0; u < 4; ++u) {
+                            const int e = g4 * 4 + u;
+                            float pv = ex2(fmaf(__uint_as_float(sv[e]), c, -lv[u]));
+                            if (need_mask) {
+                                const int pos = i0 + c0 + e + off;
+                                const bool vis = key < p.N && i0 + c0 + e < p.M && (!p.causal || key <= pos) &&
+                                                 (p.window <= 0 || key > pos - p.window);
+                                pv = vis ? pv : 0.f;
+                            }
+                            pr[u] = pv;
+                            ds[u] = pv * (__uint_as_float(dpv[e]) - dv4[u]);
                         }
-                        pr[u] = pv;
-                        ds[u] = pv * (__uint_as_float(dpv[2 * e + u]) - del[r]);
+                        pk[2 * g4] = bpack2<kBF16>(pr[0], pr[1]);
+                        pk[2 * g4 + 1] = bpack2<kBF16>(pr[2], pr[3]);
+                        dk[2 * g4] = bpack2<kBF16>(ds[0], ds[1]);
+                        dk[2 * g4 + 1] = bpack2<kBF16>(ds[2], ds[3]);
                     }
-                    pk[e] = bpack2<kBF16>(pr[0], pr[1]);
-                    dk[e] = bpack2<kBF16>(ds[0], ds[1]);
+                    // P^T, dS^T over the first 32 columns of this half
+                    tmem_st_x16(bs.tmem + lane_base + C::kColS + h * 64 + j * 16, pk);
+                    tmem_st_x16(bs.tmem + lane_base + C::kColDP + h * 64 + j * 16, dk);
                 }
-                tmem_st_x16(bs.tmem + lane_base + C::kColS + q4 * 16, pk);
-                tmem_st_x16(bs.tmem + lane_base + C::kColDP + q4 * 16, dk);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bs.pp(h));
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bs.bar_p);
         }
         uint16_t* dk_row = reinterpret_cast<uint16_t*>(p.out0) + ((size_t)grp * p.N + key) * D;
         uint16_t* dv_row = reinterpret_cast<uint16_t*>(p.out1) + ((size_t)grp * p.N + key) * D;
@@ -435,21 +471,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             constexpr uint32_t idAcc = idesc_f16(kBF16, BT, D, true);
             const uint64_t dQ = sw128_desc(bs.sbase + C::kOffStat, 16, 1024);
             const uint64_t ddO = sw128_desc(bs.sbase + C::kOffStat + C::kTile, 16, 1024);
-            bool ok = bwait_one(bs.bar_stat, 0, bs.abort_flag, p.status);
+            // half-tile software pipeline over the 64-key halves of each key tile
+            constexpr uint32_t idH = idesc_f16(kBF16, BT, BT / 2, false);
+            auto stage_k = [&](int it) { return bs.sbase + C::kOffStage + (it & 1) * 2 * C::kTile; };
+            auto issue_sdp = [&](int it, int h) {  // S, dP over half h of key tile it
+                const uint32_t sk = stage_k(it) + h * kHalfRows;
+                mma_rows_by_rows<D>(bs.tmem + C::kColS + h * 64, dQ, sw128_desc(sk, 16, 1024), idH);
+                mma_rows_by_rows<D>(bs.tmem + C::kColDP + h * 64, ddO, sw128_desc(sk + C::kTile, 16, 1024), idH);
+                mma_commit(bs.st(h));
+            };
+            bool ok = bwait_one(bs.bar_stat, 0, bs.abort_flag, p.status) &&
+                      bwait_one(bs.full(0), 0, bs.abort_flag, p.status);
+            if (ok) {
+                tc_fence_after();
+                issue_sdp(0, 0);
+                issue_sdp(0, 1);
+            }
             for (int it = 0; ok && it < T; ++it) {
-                const int s = it & 1;
-                if (!(ok = bwait_one(bs.full(s), (it >> 1) & 1, bs.abort_flag, p.status))) break;
-                tc_fence_after();
-                const uint32_t sk = bs.sbase + C::kOffStage + s * 2 * C::kTile, sv = sk + C::kTile;
-                mma_rows_by_rows<D>(bs.tmem + C::kColS, dQ, sw128_desc(sk, 16, 1024), idS);    // S = Q K^T
-                mma_rows_by_rows<D>(bs.tmem + C::kColDP, ddO, sw128_desc(sv, 16, 1024), idS);  // dP = dO V^T
-                mma_commit(bs.bar_st);
-                if (!(ok = bwait_one(bs.bar_p, it & 1, bs.abort_flag, p.status))) break;
-                tc_fence_after();
-                // dQ += dS K (dS over the first 64 columns of dP)
-                mma_tmem_by_tile(bs.tmem + C::kColAcc0, bs.tmem + C::kColDP, sw128_desc(sk, C::kChunk, 1024), idAcc,
-                                 it == 0);
-                mma_commit(bs.empty(s));
+                const uint32_t sk = stage_k(it);
+                for (int h = 0; h < 2; ++h) {
+                    if (!(ok = bwait_one(bs.pp(h), it & 1, bs.abort_flag, p.status))) break;
+                    tc_fence_after();
+                    // dQ += dS K over this half's 64 keys
+                    mma_tmem_by_half(bs.tmem + C::kColAcc0, bs.tmem + C::kColDP + h * 64,
+                                     sw128_desc(sk + h * kHalfRows, C::kChunk, 1024), idAcc, it == 0 && h == 0);
+                    if (h == 1) mma_commit(bs.empty(it & 1));  // K, V of this tile fully read
+                    if (it + 1 < T) {
+                        if (h == 0 && !(ok = bwait_one(bs.full((it + 1) & 1), ((it + 1) >> 1) & 1, bs.abort_flag,
+                                                       p.status)))
+                            break;
+                        tc_fence_after();
+                        issue_sdp(it + 1, h);
+                    }
+                }
             }
             if (ok) mma_commit(bs.bar_done);
             mma_commit(bs.bar_drain);
@@ -466,42 +520,46 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const float del = p.delta[(size_t)bh * p.Mpad + row];
         const int pos = row + off;
         bool ok = true;
-        for (int it = 0; it < T; ++it) {
+        for (int it = 0; ok && it < T; ++it) {
             const int k0 = (kt0 + it) * BT;
-            if (!(ok = bwait_warp(bs.bar_st, it & 1, bs.abort_flag, p.status))) break;
-            tc_fence_after();
             const bool need_mask = (i0 + BT > p.M) || (k0 + BT > p.N) ||
                                    (p.causal && k0 + BT - 1 > i0 + off) ||
                                    (p.window > 0 && k0 <= i0 + BT - 1 + off - p.window);
+            for (int h = 0; h < 2; ++h) {
+                if (!(ok = bwait_warp(bs.st(h), it & 1, bs.abort_flag, p.status))) break;
+                tc_fence_after();
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t sv[32], dpv[32];
-                tmem_ld_x32(bs.tmem + lane_base + C::kColS + q4 * 32, sv);
-                tmem_ld_x32(bs.tmem + lane_base + C::kColDP + q4 * 32, dpv);
-                tmem_wait_ld_x32(sv);
-                reg_after_x32(dpv);
-                uint32_t dk[16];
+                for (int j = 0; j < 2; ++j) {
+                    const int c0 = h * 64 + j * 32;  // TMEM column = key of the tile
+                    uint32_t sv[32], dpv[32];
+                    tmem_ld_x32(bs.tmem + lane_base + C::kColS + c0, sv);
+                    tmem_ld_x32(bs.tmem + lane_base + C::kColDP + c0, dpv);
+                    tmem_wait_ld_x32(sv);
+                    reg_after_x32(dpv);
+                    uint32_t dk[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float ds[2];
+                    for (int e2 = 0; e2 < 16; ++e2) {
+                        float ds[2];
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        float pv = ex2(fmaf(__uint_as_float(sv[2 * e + u]), c, -lse2));
-                        if (need_mask) {
-                            const int key = k0 + q4 * 32 + 2 * e + u;
-                            const bool vis = key < p.N && row < p.M && (!p.causal || key <= pos) &&
-                                             (p.window <= 0 || key > pos - p.window);
-                            pv = vis ? pv : 0.f;
+                        for (int u = 0; u < 2; ++u) {
+                            const int e = 2 * e2 + u;
+                            float pv = ex2(fmaf(__uint_as_float(sv[e]), c, -lse2));
+                            if (need_mask) {
+                                const int key = k0 + c0 + e;
+                                const bool vis = key < p.N && row < p.M && (!p.causal || key <= pos) &&
+                                                 (p.window <= 0 || key > pos - p.window);
+                                pv = vis ? pv : 0.f;
+                            }
+                            ds[u] = pv * (__uint_as_float(dpv[e]) - del);
                         }
-                        ds[u] = pv * (__uint_as_float(dpv[2 * e + u]) - del);
+                        dk[e2] = bpack2<kBF16>(ds[0], ds[1]);
                     }
-                    dk[e] = bpack2<kBF16>(ds[0], ds[1]);
+                    tmem_st_x16(bs.tmem + lane_base + C::kColDP + h * 64 + j * 16, dk);  // dS over dP
                 }
-                tmem_st_x16(bs.tmem + lane_base + C::kColDP + q4 * 16, dk);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bs.pp(h));
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bs.bar_p);
         }
         uint16_t* dq_row = reinterpret_cast<uint16_t*>(p.out0) + ((size_t)bh * p.M + row) * D;
         const bool write = row < p.M;
