@@ -30,6 +30,7 @@
 #include <cuda_fp16.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "attn_internal.h"
 #include "sm100_ptx.cuh"
@@ -231,8 +232,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const BSetup bs = bwd_setup<D>(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // tile 0 of every group first: under a causal mask it sees the most query rows
-    const int jt = blockIdx.x / p.groups, grp = blockIdx.x % p.groups;
+    // The key tiles of one group are consecutive CTAs, so the CTAs running at once
+    // share a few groups' Q and dO in L2; each starts its walk over the query
+    // tiles at a different tile, so at any moment they fetch different tiles (one
+    // DRAM read each, then L2 hits) instead of all missing on the same one.
+    const int jt = blockIdx.x % p.ntile, grp = blockIdx.x / p.ntile;
     const int b = grp / p.Hkv, g = grp % p.Hkv;
     const int k0 = jt * BT, k1 = min(k0 + BT, p.N);
     const int off = p.N - p.M;  // query row i sits at key position i + off
@@ -244,6 +248,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int qt0 = i_lo / BT;
     const int nq = i_hi > i_lo ? (i_hi + BT - 1) / BT - qt0 : 0;
     const int T = p.G * nq;  // (query head of the group, query tile) pairs
+    const int rot = T > 0 ? (int)(((long long)jt * 7) % T) : 0;
 
     if (warp == kBLoadWarp) {
         if (lane == 0 && T > 0) {
@@ -260,7 +265,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int it = 0; it < T; ++it) {
                 const int s = it & 1;
                 if (it >= 2 && !bwait_one(bs.empty(s), ((it >> 1) - 1) & 1, bs.abort_flag, p.status)) break;
-                const int h = g * p.G + it / nq, i0 = (qt0 + it % nq) * BT;
+                const int x = (it + rot) % T;
+                const int h = g * p.G + x / nq, i0 = (qt0 + x % nq) * BT;
                 const int bh = b * p.Hq + h;
                 mbar_arrive_expect_tx(bs.full(s), 2 * C::kTile + 2 * BT * 4);
                 const uint32_t dq = bs.sbase + C::kOffStage + s * 2 * C::kTile;
@@ -337,7 +343,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bool ok = true;
         for (int it = 0; ok && it < T; ++it) {
             const int s = it & 1;
-            const int i0 = (qt0 + it % nq) * BT;
+            const int i0 = (qt0 + (it + rot) % T % nq) * BT;
             const bool need_mask = (i0 + BT > p.M) || (k0 + BT > p.N) ||
                                    (p.causal && k0 + BT - 1 > i0 + off) ||
                                    (p.window > 0 && k0 <= i0 + BT - 1 + off - p.window);
@@ -358,30 +364,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     tmem_wait_ld_x32(sv);
                     reg_after_x32(dpv);
                     uint32_t pk[16], dk[16];
-#pragma unroll
-                    for (int g4 = 0; g4 < 8; ++g4) {
-                        const float4 l4 = reinterpret_cast<const float4*>(lse2 + c0)[g4];
-                        const float4 d4 = reinterpret_cast<const float4*>(del + c0)[g4];
-                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-                        float pr[4], ds[4];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int e = g4 * 4 + u;
-                            float pv = ex2(fmaf(__uint_as_float(sv[e]), c, -lv[u]));
-                            if (need_mask) {
-                                const int pos = i0 + c0 + e + off;
-                                const bool vis = key < p.N && i0 + c0 + e < p.M && (!p.causal || key <= pos) &&
-                                                 (p.window <= 0 || key > pos - p.window);
-                                pv = vis ? pv : 0.f;
-                            }
-                            pr[u] = pv;
-                            ds[u] = pv * (__uint_as_float(dpv[e]) - dv4[u]);
-                        }
-                        pk[2 * g4] = bpack2<kBF16>(pr[0], pr[1]);
-                        pk[2 * g4 + 1] = bpack2<kBF16>(pr[2], pr[3]);
-                        dk[2 * g4] = bpack2<kBF16>(ds[0], ds[1]);
-                        dk[2 * g4 + 1] = bpack2<kBF16>(ds[2], ds[3]);
+                    // visible query rows of this chunk for this thread's key: e in [elo, ehi)
+                    int elo = 0, ehi = 32;
+                    if (need_mask) {
+                        const int r0 = i0 + c0;  // row of e = 0, at position r0 + off
+                        if (key >= p.N) ehi = 0;
+                        ehi = min(ehi, p.M - r0);
+                        if (p.causal) elo = max(elo, key - r0 - off);
+                        if (p.window > 0) ehi = min(ehi, key + p.window - r0 - off);
                     }
+                    auto chunk = [&](auto masked) {
+#pragma unroll
+                        for (int g4 = 0; g4 < 8; ++g4) {
+                            const float4 l4 = reinterpret_cast<const float4*>(lse2 + c0)[g4];
+                            const float4 d4 = reinterpret_cast<const float4*>(del + c0)[g4];
+                            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+                            float pr[4], ds[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int e = g4 * 4 + u;
+                                float pv = ex2(fmaf(__uint_as_float(sv[e]), c, -lv[u]));
+                                if (decltype(masked)::value) pv = (e >= elo && e < ehi) ? pv : 0.f;
+                                pr[u] = pv;
+                                ds[u] = pv * (__uint_as_float(dpv[e]) - dv4[u]);
+                            }
+                            pk[2 * g4] = bpack2<kBF16>(pr[0], pr[1]);
+                            pk[2 * g4 + 1] = bpack2<kBF16>(pr[2], pr[3]);
+                            dk[2 * g4] = bpack2<kBF16>(ds[0], ds[1]);
+                            dk[2 * g4 + 1] = bpack2<kBF16>(ds[2], ds[3]);
+                        }
+                    };
+                    if (need_mask)
+                        chunk(std::true_type{});
+                    else
+                        chunk(std::false_type{});
                     // P^T, dS^T over the first 32 columns of this half
                     tmem_st_x16(bs.tmem + lane_base + C::kColS + h * 64 + j * 16, pk);
                     tmem_st_x16(bs.tmem + lane_base + C::kColDP + h * 64 + j * 16, dk);
@@ -425,8 +441,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const BSetup bs = bwd_setup<D>(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // the last query tile of every head first: under a causal mask it sees the most keys
-    const int qt = p.ntile - 1 - (int)(blockIdx.x / p.groups), bh = blockIdx.x % p.groups;
+    // The query tiles of one head are consecutive CTAs (the last, under a causal
+    // mask the longest, first) so the CTAs running at once share its K and V in
+    // L2; each starts its walk over the key tiles at a different tile.
+    const int qt = p.ntile - 1 - (int)(blockIdx.x % p.ntile), bh = blockIdx.x / p.ntile;
     const int b = bh / p.Hq, h = bh % p.Hq;
     const int grp = b * p.Hkv + h / p.G;
     const int i0 = qt * BT, i_last = min(i0 + BT, p.M) - 1;
@@ -436,6 +454,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     key_range(i_last + off, p.N, p.causal, p.window, &unused, &hi);
     const int kt0 = lo / BT;
     const int T = hi > lo ? (hi + BT - 1) / BT - kt0 : 0;  // key tiles
+    const int rot = T > 0 ? (int)(((long long)qt * 7) % T) : 0;
 
     if (warp == kBLoadWarp) {
         if (lane == 0 && T > 0) {
@@ -452,7 +471,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int it = 0; it < T; ++it) {
                 const int s = it & 1;
                 if (it >= 2 && !bwait_one(bs.empty(s), ((it >> 1) - 1) & 1, bs.abort_flag, p.status)) break;
-                const int k0 = (kt0 + it) * BT;
+                const int k0 = (kt0 + (it + rot) % T) * BT;
                 mbar_arrive_expect_tx(bs.full(s), 2 * C::kTile);
                 const uint32_t dk = bs.sbase + C::kOffStage + s * 2 * C::kTile;
                 for (int c = 0; c < C::kChunks; ++c) {
@@ -521,7 +540,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int pos = row + off;
         bool ok = true;
         for (int it = 0; ok && it < T; ++it) {
-            const int k0 = (kt0 + it) * BT;
+            const int k0 = (kt0 + (it + rot) % T) * BT;
             const bool need_mask = (i0 + BT > p.M) || (k0 + BT > p.N) ||
                                    (p.causal && k0 + BT - 1 > i0 + off) ||
                                    (p.window > 0 && k0 <= i0 + BT - 1 + off - p.window);
@@ -537,23 +556,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     tmem_wait_ld_x32(sv);
                     reg_after_x32(dpv);
                     uint32_t dk[16];
-#pragma unroll
-                    for (int e2 = 0; e2 < 16; ++e2) {
-                        float ds[2];
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const int e = 2 * e2 + u;
-                            float pv = ex2(fmaf(__uint_as_float(sv[e]), c, -lse2));
-                            if (need_mask) {
-                                const int key = k0 + c0 + e;
-                                const bool vis = key < p.N && row < p.M && (!p.causal || key <= pos) &&
-                                                 (p.window <= 0 || key > pos - p.window);
-                                pv = vis ? pv : 0.f;
-                            }
-                            ds[u] = pv * (__uint_as_float(dpv[e]) - del);
-                        }
-                        dk[e2] = bpack2<kBF16>(ds[0], ds[1]);
+                    // visible keys of this chunk for this thread's row: e in [elo, ehi)
+                    int elo = 0, ehi = 32;
+                    if (need_mask) {
+                        const int kc = k0 + c0;  // key of e = 0
+                        if (row >= p.M) ehi = 0;
+                        ehi = min(ehi, p.N - kc);
+                        if (p.causal) ehi = min(ehi, pos + 1 - kc);
+                        if (p.window > 0) elo = max(elo, pos - p.window + 1 - kc);
                     }
+                    auto chunk = [&](auto masked) {
+#pragma unroll
+                        for (int e2 = 0; e2 < 16; ++e2) {
+                            float ds[2];
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const int e = 2 * e2 + u;
+                                float pv = ex2(fmaf(__uint_as_float(sv[e]), c, -lse2));
+                                if (decltype(masked)::value) pv = (e >= elo && e < ehi) ? pv : 0.f;
+                                ds[u] = pv * (__uint_as_float(dpv[e]) - del);
+                            }
+                            dk[e2] = bpack2<kBF16>(ds[0], ds[1]);
+                        }
+                    };
+                    if (need_mask)
+                        chunk(std::true_type{});
+                    else
+                        chunk(std::false_type{});
                     tmem_st_x16(bs.tmem + lane_base + C::kColDP + h * 64 + j * 16, dk);  // dS over dP
                 }
                 tmem_wait_st();
