@@ -64,6 +64,7 @@ struct BCfg {
     static constexpr int kSmem = kOffMisc + 16 + 1024;
     // TMEM columns
     static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + D;
+    static constexpr uint32_t kColP = 384;  // dQ kernel: P (16-bit pairs), moved out of S
 };
 
 struct BwdParams {
@@ -123,16 +124,35 @@ __device__ __forceinline__ void mma_rows_by_rows(uint32_t d_tmem, uint64_t a0, u
         mma_ss(d_tmem, a0 + off, b0 + off, idesc, kk > 0 ? 1u : 0u);
     }
 }
-// C (+)= A B over 64: A 16-bit in TMEM (128 lanes x 64 along K), B 64 rows of a
-// [128][D] tile read MN-major (N = D), starting at b0
-__device__ __forceinline__ void mma_tmem_by_half(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0, uint32_t idesc,
+// C (+)= A B over 128: A 16-bit in TMEM (128 lanes x 128 along K), B a [128][D]
+// tile read MN-major (N = D)
+__device__ __forceinline__ void mma_tmem_by_tile(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0, uint32_t idesc,
                                                  bool first) {
 #pragma unroll
-    for (int kk = 0; kk < BT / 32; ++kk)
+    for (int kk = 0; kk < BT / 16; ++kk)
         mma_ts(d_tmem, a_tmem + kk * 8, b0 + (uint64_t)((kk * 16 * 128) >> 4), idesc, (first && kk == 0) ? 0u : 1u);
 }
-// 64 rows of a swizzled [128][D] tile start 64 * 128 bytes into each 64-column chunk
-constexpr uint32_t kHalfRows = 64 * 128;
+
+// Orders later uses of r after the preceding asm statements (no instruction).
+__device__ __forceinline__ void reg_after_x16(uint32_t (&r)[16]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15])::"memory");
+}
+
+// 16-bit pair (low half first) -> two floats
+template <bool kBF16>
+__device__ __forceinline__ void unpack2(uint32_t w, float& lo, float& hi) {
+    if (kBF16) {
+        lo = __uint_as_float(w << 16);
+        hi = __uint_as_float(w & 0xFFFF0000u);
+    } else {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
+        lo = f.x;
+        hi = f.y;
+    }
+}
 
 template <bool kBF16>
 __device__ __forceinline__ uint32_t bpack2(float lo, float hi) {
@@ -165,8 +185,8 @@ struct BSetup {
     volatile uint32_t* abort_flag;
     __device__ uint32_t full(int s) const { return bar_full0 + 8u * s; }
     __device__ uint32_t empty(int s) const { return bar_empty0 + 8u * s; }
-    __device__ uint32_t st(int h) const { return bar_st0 + 8u * h; }  // half h of S, dP computed
-    __device__ uint32_t pp(int h) const { return bar_p0 + 8u * h; }   // half h of P / dS written
+    __device__ uint32_t st(int x) const { return bar_st0 + 8u * x; }  // x = 0: S computed; 1: dP computed
+    __device__ uint32_t pp(int x) const { return bar_p0 + 8u * x; }   // x = 0: P written; 1: dS written
 };
 
 template <int D>
@@ -290,44 +310,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             constexpr uint32_t idAcc = idesc_f16(kBF16, BT, D, true);
             const uint64_t dK = sw128_desc(bs.sbase + C::kOffStat, 16, 1024);
             const uint64_t dV = sw128_desc(bs.sbase + C::kOffStat + C::kTile, 16, 1024);
-            // Half-tile software pipeline: while the elementwise warps work on one
-            // half (64 query rows) of a tile, the tensor core computes the other half's
-            // S^T, dP^T or the previous half's dV, dK products.
-            constexpr uint32_t idH = idesc_f16(kBF16, BT, BT / 2, false);
+            // Two-phase pipeline: S^T and dP^T of a tile are full 128-wide products; the
+            // elementwise warps write P^T over S^T (phase A) while dP^T is computed, then
+            // dS^T over dP^T (phase B). dV needs only phase A; the next tile's S^T goes in
+            // as soon as phase B has read P^T, ahead of this tile's dK product.
             auto stage_q = [&](int it) { return bs.sbase + C::kOffStage + (it & 1) * 2 * C::kTile; };
-            auto issue_sdp = [&](int it, int h) {  // S^T, dP^T of half h of query tile it
-                const uint32_t sq = stage_q(it) + h * kHalfRows;
-                mma_rows_by_rows<D>(bs.tmem + C::kColS + h * 64, dK, sw128_desc(sq, 16, 1024), idH);
-                mma_rows_by_rows<D>(bs.tmem + C::kColDP + h * 64, dV, sw128_desc(sq + C::kTile, 16, 1024), idH);
-                mma_commit(bs.st(h));
+            auto issue_s = [&](int it) {  // S^T = K Q^T
+                mma_rows_by_rows<D>(bs.tmem + C::kColS, dK, sw128_desc(stage_q(it), 16, 1024), idS);
+                mma_commit(bs.st(0));
+            };
+            auto issue_dp = [&](int it) {  // dP^T = V dO^T
+                mma_rows_by_rows<D>(bs.tmem + C::kColDP, dV, sw128_desc(stage_q(it) + C::kTile, 16, 1024), idS);
+                mma_commit(bs.st(1));
             };
             bool ok = bwait_one(bs.bar_stat, 0, bs.abort_flag, p.status) &&
                       bwait_one(bs.full(0), 0, bs.abort_flag, p.status);
             if (ok) {
                 tc_fence_after();
-                issue_sdp(0, 0);
-                issue_sdp(0, 1);
+                issue_s(0);
+                issue_dp(0);
             }
             for (int it = 0; ok && it < T; ++it) {
                 const uint32_t sq = stage_q(it);
-                for (int h = 0; h < 2; ++h) {
-                    if (!(ok = bwait_one(bs.pp(h), it & 1, bs.abort_flag, p.status))) break;
+                if (!(ok = bwait_one(bs.pp(0), it & 1, bs.abort_flag, p.status))) break;
+                tc_fence_after();
+                mma_tmem_by_tile(bs.tmem + C::kColAcc1, bs.tmem + C::kColS, sw128_desc(sq + C::kTile, C::kChunk, 1024),
+                                 idAcc, it == 0);  // dV += P^T dO
+                if (!(ok = bwait_one(bs.pp(1), it & 1, bs.abort_flag, p.status))) break;
+                tc_fence_after();
+                const bool more = it + 1 < T;
+                if (more) {
+                    if (!(ok = bwait_one(bs.full((it + 1) & 1), ((it + 1) >> 1) & 1, bs.abort_flag, p.status))) break;
                     tc_fence_after();
-                    // dV += P^T dO and dK += dS^T Q over this half's 64 rows
-                    const uint32_t rows = sq + h * kHalfRows;
-                    mma_tmem_by_half(bs.tmem + C::kColAcc1, bs.tmem + C::kColS + h * 64,
-                                     sw128_desc(rows + C::kTile, C::kChunk, 1024), idAcc, it == 0 && h == 0);
-                    mma_tmem_by_half(bs.tmem + C::kColAcc0, bs.tmem + C::kColDP + h * 64,
-                                     sw128_desc(rows, C::kChunk, 1024), idAcc, it == 0 && h == 0);
-                    if (h == 1) mma_commit(bs.empty(it & 1));  // Q, dO of this tile fully read
-                    if (it + 1 < T) {
-                        if (h == 0 && !(ok = bwait_one(bs.full((it + 1) & 1), ((it + 1) >> 1) & 1, bs.abort_flag,
-                                                       p.status)))
-                            break;
-                        tc_fence_after();
-                        issue_sdp(it + 1, h);
-                    }
+                    issue_s(it + 1);
                 }
+                mma_tmem_by_tile(bs.tmem + C::kColAcc0, bs.tmem + C::kColDP, sw128_desc(sq, C::kChunk, 1024), idAcc,
+                                 it == 0);  // dK += dS^T Q
+                mma_commit(bs.empty(it & 1));  // Q, dO of this tile fully read
+                if (more) issue_dp(it + 1);
             }
             if (ok) mma_commit(bs.bar_done);
             mma_commit(bs.bar_drain);
@@ -349,63 +369,84 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                    (p.window > 0 && k0 <= i0 + BT - 1 + off - p.window);
             const float* lse2 = reinterpret_cast<const float*>(smem + C::kOffVec + s * 2 * BT * 4);
             const float* del = lse2 + BT;
-            for (int h = 0; h < 2; ++h) {
-                if (!(ok = bwait_warp(bs.st(h), it & 1, bs.abort_flag, p.status))) break;
-                // the stage's row vectors came by bulk copy: observe their barrier too (its
-                // phase cannot move on before this tile's products, which need p_full)
-                if (h == 0 && !(ok = bwait_warp(bs.full(s), (it >> 1) & 1, bs.abort_flag, p.status))) break;
-                tc_fence_after();
+            // ---- phase A: P^T = exp2(S^T c - lse2) over the first 64 columns of S^T ----
+            if (!(ok = bwait_warp(bs.st(0), it & 1, bs.abort_flag, p.status))) break;
+            // the stage's row vectors came by bulk copy: observe their barrier too (its
+            // phase cannot move on before this tile's products, which need this thread)
+            if (!(ok = bwait_warp(bs.full(s), (it >> 1) & 1, bs.abort_flag, p.status))) break;
+            tc_fence_after();
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int c0 = h * 64 + j * 32;  // TMEM column = query row of the tile
-                    uint32_t sv[32], dpv[32];
-                    tmem_ld_x32(bs.tmem + lane_base + C::kColS + c0, sv);
-                    tmem_ld_x32(bs.tmem + lane_base + C::kColDP + c0, dpv);
-                    tmem_wait_ld_x32(sv);
-                    reg_after_x32(dpv);
-                    uint32_t pk[16], dk[16];
-                    // visible query rows of this chunk for this thread's key: e in [elo, ehi)
-                    int elo = 0, ehi = 32;
-                    if (need_mask) {
-                        const int r0 = i0 + c0;  // row of e = 0, at position r0 + off
-                        if (key >= p.N) ehi = 0;
-                        ehi = min(ehi, p.M - r0);
-                        if (p.causal) elo = max(elo, key - r0 - off);
-                        if (p.window > 0) ehi = min(ehi, key + p.window - r0 - off);
-                    }
-                    auto chunk = [&](auto masked) {
-#pragma unroll
-                        for (int g4 = 0; g4 < 8; ++g4) {
-                            const float4 l4 = reinterpret_cast<const float4*>(lse2 + c0)[g4];
-                            const float4 d4 = reinterpret_cast<const float4*>(del + c0)[g4];
-                            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-                            float pr[4], ds[4];
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const int e = g4 * 4 + u;
-                                float pv = ex2(fmaf(__uint_as_float(sv[e]), c, -lv[u]));
-                                if (decltype(masked)::value) pv = (e >= elo && e < ehi) ? pv : 0.f;
-                                pr[u] = pv;
-                                ds[u] = pv * (__uint_as_float(dpv[e]) - dv4[u]);
-                            }
-                            pk[2 * g4] = bpack2<kBF16>(pr[0], pr[1]);
-                            pk[2 * g4 + 1] = bpack2<kBF16>(pr[2], pr[3]);
-                            dk[2 * g4] = bpack2<kBF16>(ds[0], ds[1]);
-                            dk[2 * g4 + 1] = bpack2<kBF16>(ds[2], ds[3]);
-                        }
-                    };
-                    if (need_mask)
-                        chunk(std::true_type{});
-                    else
-                        chunk(std::false_type{});
-                    // P^T, dS^T over the first 32 columns of this half
-                    tmem_st_x16(bs.tmem + lane_base + C::kColS + h * 64 + j * 16, pk);
-                    tmem_st_x16(bs.tmem + lane_base + C::kColDP + h * 64 + j * 16, dk);
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const int c0 = q4 * 32;  // TMEM column = query row of the tile
+                uint32_t sv[32];
+                tmem_ld_x32(bs.tmem + lane_base + C::kColS + c0, sv);
+                tmem_wait_ld_x32(sv);
+                // visible query rows of this chunk for this thread's key: e in [elo, ehi)
+                int elo = 0, ehi = 32;
+                if (need_mask) {
+                    const int r0 = i0 + c0;  // row of e = 0, at position r0 + off
+                    if (key >= p.N) ehi = 0;
+                    ehi = min(ehi, p.M - r0);
+                    if (p.causal) elo = max(elo, key - r0 - off);
+                    if (p.window > 0) ehi = min(ehi, key + p.window - r0 - off);
                 }
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(bs.pp(h));
+                uint32_t pk[16];
+                auto chunk = [&](auto masked) {
+#pragma unroll
+                    for (int g4 = 0; g4 < 8; ++g4) {
+                        const float4 l4 = reinterpret_cast<const float4*>(lse2 + c0)[g4];
+                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                        float pr[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int e = g4 * 4 + u;
+                            float pv = ex2(fmaf(__uint_as_float(sv[e]), c, -lv[u]));
+                            if (decltype(masked)::value) pv = (e >= elo && e < ehi) ? pv : 0.f;
+                            pr[u] = pv;
+                        }
+                        pk[2 * g4] = bpack2<kBF16>(pr[0], pr[1]);
+                        pk[2 * g4 + 1] = bpack2<kBF16>(pr[2], pr[3]);
+                    }
+                };
+                if (need_mask)
+                    chunk(std::true_type{});
+                else
+                    chunk(std::false_type{});
+                tmem_st_x16(bs.tmem + lane_base + C::kColS + q4 * 16, pk);
             }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bs.pp(0));
+            // ---- phase B: dS^T = P^T (dP^T - delta) over the first 64 columns of dP^T ----
+            // (masked entries have P = 0 already)
+            if (!(ok = bwait_warp(bs.st(1), it & 1, bs.abort_flag, p.status))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const int c0 = q4 * 32;
+                uint32_t dpv[32], pv16[16];
+                tmem_ld_x32(bs.tmem + lane_base + C::kColDP + c0, dpv);
+                tmem_ld_x16(bs.tmem + lane_base + C::kColS + q4 * 16, pv16);
+                tmem_wait_ld_x32(dpv);
+                reg_after_x16(pv16);
+                uint32_t dk[16];
+#pragma unroll
+                for (int g4 = 0; g4 < 8; ++g4) {
+                    const float4 d4 = reinterpret_cast<const float4*>(del + c0)[g4];
+                    float p0, p1, p2, p3;
+                    unpack2<kBF16>(pv16[2 * g4], p0, p1);
+                    unpack2<kBF16>(pv16[2 * g4 + 1], p2, p3);
+                    const int e = g4 * 4;
+                    dk[2 * g4] = bpack2<kBF16>(p0 * (__uint_as_float(dpv[e]) - d4.x),
+                                               p1 * (__uint_as_float(dpv[e + 1]) - d4.y));
+                    dk[2 * g4 + 1] = bpack2<kBF16>(p2 * (__uint_as_float(dpv[e + 2]) - d4.z),
+                                                   p3 * (__uint_as_float(dpv[e + 3]) - d4.w));
+                }
+                tmem_st_x16(bs.tmem + lane_base + C::kColDP + q4 * 16, dk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bs.pp(1));
         }
         uint16_t* dk_row = reinterpret_cast<uint16_t*>(p.out0) + ((size_t)grp * p.N + key) * D;
         uint16_t* dv_row = reinterpret_cast<uint16_t*>(p.out1) + ((size_t)grp * p.N + key) * D;
@@ -490,39 +531,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             constexpr uint32_t idAcc = idesc_f16(kBF16, BT, D, true);
             const uint64_t dQ = sw128_desc(bs.sbase + C::kOffStat, 16, 1024);
             const uint64_t ddO = sw128_desc(bs.sbase + C::kOffStat + C::kTile, 16, 1024);
-            // half-tile software pipeline over the 64-key halves of each key tile
-            constexpr uint32_t idH = idesc_f16(kBF16, BT, BT / 2, false);
+            // Two-phase pipeline: full 128-wide S and dP; phase A moves P (16-bit) out of S,
+            // which frees S for the next tile's product at once; phase B writes dS over dP.
             auto stage_k = [&](int it) { return bs.sbase + C::kOffStage + (it & 1) * 2 * C::kTile; };
-            auto issue_sdp = [&](int it, int h) {  // S, dP over half h of key tile it
-                const uint32_t sk = stage_k(it) + h * kHalfRows;
-                mma_rows_by_rows<D>(bs.tmem + C::kColS + h * 64, dQ, sw128_desc(sk, 16, 1024), idH);
-                mma_rows_by_rows<D>(bs.tmem + C::kColDP + h * 64, ddO, sw128_desc(sk + C::kTile, 16, 1024), idH);
-                mma_commit(bs.st(h));
+            auto issue_s = [&](int it) {  // S = Q K^T
+                mma_rows_by_rows<D>(bs.tmem + C::kColS, dQ, sw128_desc(stage_k(it), 16, 1024), idS);
+                mma_commit(bs.st(0));
+            };
+            auto issue_dp = [&](int it) {  // dP = dO V^T
+                mma_rows_by_rows<D>(bs.tmem + C::kColDP, ddO, sw128_desc(stage_k(it) + C::kTile, 16, 1024), idS);
+                mma_commit(bs.st(1));
             };
             bool ok = bwait_one(bs.bar_stat, 0, bs.abort_flag, p.status) &&
                       bwait_one(bs.full(0), 0, bs.abort_flag, p.status);
             if (ok) {
                 tc_fence_after();
-                issue_sdp(0, 0);
-                issue_sdp(0, 1);
+                issue_s(0);
+                issue_dp(0);
             }
             for (int it = 0; ok && it < T; ++it) {
                 const uint32_t sk = stage_k(it);
-                for (int h = 0; h < 2; ++h) {
-                    if (!(ok = bwait_one(bs.pp(h), it & 1, bs.abort_flag, p.status))) break;
+                const bool more = it + 1 < T;
+                if (!(ok = bwait_one(bs.pp(0), it & 1, bs.abort_flag, p.status))) break;
+                if (more) {
+                    if (!(ok = bwait_one(bs.full((it + 1) & 1), ((it + 1) >> 1) & 1, bs.abort_flag, p.status))) break;
                     tc_fence_after();
-                    // dQ += dS K over this half's 64 keys
-                    mma_tmem_by_half(bs.tmem + C::kColAcc0, bs.tmem + C::kColDP + h * 64,
-                                     sw128_desc(sk + h * kHalfRows, C::kChunk, 1024), idAcc, it == 0 && h == 0);
-                    if (h == 1) mma_commit(bs.empty(it & 1));  // K, V of this tile fully read
-                    if (it + 1 < T) {
-                        if (h == 0 && !(ok = bwait_one(bs.full((it + 1) & 1), ((it + 1) >> 1) & 1, bs.abort_flag,
-                                                       p.status)))
-                            break;
-                        tc_fence_after();
-                        issue_sdp(it + 1, h);
-                    }
+                    issue_s(it + 1);
                 }
+                if (!(ok = bwait_one(bs.pp(1), it & 1, bs.abort_flag, p.status))) break;
+                tc_fence_after();
+                mma_tmem_by_tile(bs.tmem + C::kColAcc0, bs.tmem + C::kColDP, sw128_desc(sk, C::kChunk, 1024), idAcc,
+                                 it == 0);  // dQ += dS K
+                mma_commit(bs.empty(it & 1));  // K, V of this tile fully read
+                if (more) issue_dp(it + 1);
             }
             if (ok) mma_commit(bs.bar_done);
             mma_commit(bs.bar_drain);
@@ -544,51 +585,72 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const bool need_mask = (i0 + BT > p.M) || (k0 + BT > p.N) ||
                                    (p.causal && k0 + BT - 1 > i0 + off) ||
                                    (p.window > 0 && k0 <= i0 + BT - 1 + off - p.window);
-            for (int h = 0; h < 2; ++h) {
-                if (!(ok = bwait_warp(bs.st(h), it & 1, bs.abort_flag, p.status))) break;
-                tc_fence_after();
+            // ---- phase A: P = exp2(S c - lse2), moved to its own columns ----
+            if (!(ok = bwait_warp(bs.st(0), it & 1, bs.abort_flag, p.status))) break;
+            tc_fence_after();
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int c0 = h * 64 + j * 32;  // TMEM column = key of the tile
-                    uint32_t sv[32], dpv[32];
-                    tmem_ld_x32(bs.tmem + lane_base + C::kColS + c0, sv);
-                    tmem_ld_x32(bs.tmem + lane_base + C::kColDP + c0, dpv);
-                    tmem_wait_ld_x32(sv);
-                    reg_after_x32(dpv);
-                    uint32_t dk[16];
-                    // visible keys of this chunk for this thread's row: e in [elo, ehi)
-                    int elo = 0, ehi = 32;
-                    if (need_mask) {
-                        const int kc = k0 + c0;  // key of e = 0
-                        if (row >= p.M) ehi = 0;
-                        ehi = min(ehi, p.N - kc);
-                        if (p.causal) ehi = min(ehi, pos + 1 - kc);
-                        if (p.window > 0) elo = max(elo, pos - p.window + 1 - kc);
-                    }
-                    auto chunk = [&](auto masked) {
-#pragma unroll
-                        for (int e2 = 0; e2 < 16; ++e2) {
-                            float ds[2];
-#pragma unroll
-                            for (int u = 0; u < 2; ++u) {
-                                const int e = 2 * e2 + u;
-                                float pv = ex2(fmaf(__uint_as_float(sv[e]), c, -lse2));
-                                if (decltype(masked)::value) pv = (e >= elo && e < ehi) ? pv : 0.f;
-                                ds[u] = pv * (__uint_as_float(dpv[e]) - del);
-                            }
-                            dk[e2] = bpack2<kBF16>(ds[0], ds[1]);
-                        }
-                    };
-                    if (need_mask)
-                        chunk(std::true_type{});
-                    else
-                        chunk(std::false_type{});
-                    tmem_st_x16(bs.tmem + lane_base + C::kColDP + h * 64 + j * 16, dk);  // dS over dP
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const int c0 = q4 * 32;  // TMEM column = key of the tile
+                uint32_t sv[32];
+                tmem_ld_x32(bs.tmem + lane_base + C::kColS + c0, sv);
+                tmem_wait_ld_x32(sv);
+                // visible keys of this chunk for this thread's row: e in [elo, ehi)
+                int elo = 0, ehi = 32;
+                if (need_mask) {
+                    const int kc = k0 + c0;  // key of e = 0
+                    if (row >= p.M) ehi = 0;
+                    ehi = min(ehi, p.N - kc);
+                    if (p.causal) ehi = min(ehi, pos + 1 - kc);
+                    if (p.window > 0) elo = max(elo, pos - p.window + 1 - kc);
                 }
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(bs.pp(h));
+                uint32_t pk[16];
+                auto chunk = [&](auto masked) {
+#pragma unroll
+                    for (int e2 = 0; e2 < 16; ++e2) {
+                        float pr[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int e = 2 * e2 + u;
+                            float pv = ex2(fmaf(__uint_as_float(sv[e]), c, -lse2));
+                            if (decltype(masked)::value) pv = (e >= elo && e < ehi) ? pv : 0.f;
+                            pr[u] = pv;
+                        }
+                        pk[e2] = bpack2<kBF16>(pr[0], pr[1]);
+                    }
+                };
+                if (need_mask)
+                    chunk(std::true_type{});
+                else
+                    chunk(std::false_type{});
+                tmem_st_x16(bs.tmem + lane_base + C::kColP + q4 * 16, pk);
             }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bs.pp(0));
+            // ---- phase B: dS = P (dP - delta) over the first 64 columns of dP ----
+            if (!(ok = bwait_warp(bs.st(1), it & 1, bs.abort_flag, p.status))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const int c0 = q4 * 32;
+                uint32_t dpv[32], pv16[16];
+                tmem_ld_x32(bs.tmem + lane_base + C::kColDP + c0, dpv);
+                tmem_ld_x16(bs.tmem + lane_base + C::kColP + q4 * 16, pv16);
+                tmem_wait_ld_x32(dpv);
+                reg_after_x16(pv16);
+                uint32_t dk[16];
+#pragma unroll
+                for (int e2 = 0; e2 < 16; ++e2) {
+                    float p0, p1;
+                    unpack2<kBF16>(pv16[e2], p0, p1);
+                    dk[e2] = bpack2<kBF16>(p0 * (__uint_as_float(dpv[2 * e2]) - del),
+                                           p1 * (__uint_as_float(dpv[2 * e2 + 1]) - del));
+                }
+                tmem_st_x16(bs.tmem + lane_base + C::kColDP + q4 * 16, dk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bs.pp(1));
         }
         uint16_t* dq_row = reinterpret_cast<uint16_t*>(p.out0) + ((size_t)bh * p.M + row) * D;
         const bool write = row < p.M;
