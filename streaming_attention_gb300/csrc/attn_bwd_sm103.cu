@@ -42,8 +42,9 @@ namespace {
 using namespace ptx;
 
 constexpr int BT = 128;           // query rows per query tile and keys per key tile
-constexpr int kBwdThreads = 192;  // warps 0-3 elementwise, 4 TMA, 5 MMA
-constexpr int kBLoadWarp = 4, kBMmaWarp = 5;
+// warps 0-7 elementwise (warp w: TMEM lanes 32*(w%4).., column half w/4), 8 TMA, 9 MMA
+constexpr int kBwdThreads = 320;
+constexpr int kBLoadWarp = 8, kBMmaWarp = 9;
 constexpr uint64_t kBwdTimeoutNs = 1000000000ull;
 
 // Shared memory: two stationary tiles, a 2-stage ring of tile pairs, the
@@ -124,13 +125,20 @@ __device__ __forceinline__ void mma_rows_by_rows(uint32_t d_tmem, uint64_t a0, u
         mma_ss(d_tmem, a0 + off, b0 + off, idesc, kk > 0 ? 1u : 0u);
     }
 }
-// C (+)= A B over 128: A 16-bit in TMEM (128 lanes x 128 along K), B a [128][D]
-// tile read MN-major (N = D)
+// A 16-bit operand of 128 along K lives in TMEM as two packed blocks: K 0..63 in
+// columns [0, 32) and K 64..127 in columns [64, 96) of its region, each written
+// in place over the 32-bit values of its own 64 columns by one elementwise
+// warpgroup (so the two warpgroups never touch each other's columns).
+__device__ __forceinline__ constexpr uint32_t packed_col(int q4) { return (q4 >> 1) * 64 + (q4 & 1) * 16; }
+
+// C (+)= A B over 128: A 16-bit in TMEM (packed as above), B a [128][D] tile read
+// MN-major (N = D)
 __device__ __forceinline__ void mma_tmem_by_tile(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0, uint32_t idesc,
                                                  bool first) {
 #pragma unroll
     for (int kk = 0; kk < BT / 16; ++kk)
-        mma_ts(d_tmem, a_tmem + kk * 8, b0 + (uint64_t)((kk * 16 * 128) >> 4), idesc, (first && kk == 0) ? 0u : 1u);
+        mma_ts(d_tmem, a_tmem + (kk >> 2) * 64 + (kk & 3) * 8, b0 + (uint64_t)((kk * 16 * 128) >> 4), idesc,
+               (first && kk == 0) ? 0u : 1u);
 }
 
 // Orders later uses of r after the preceding asm statements (no instruction).
@@ -159,11 +167,13 @@ __device__ __forceinline__ uint32_t bpack2(float lo, float hi) {
     return kBF16 ? pack_bf16(lo, hi) : pack_f16(lo, hi);
 }
 
-// Writes one [D] row of FP32 TMEM columns (this thread's lane) as 16-bit values.
+// Writes half `half` of one [D] row of FP32 TMEM columns (this thread's lane) as
+// 16-bit values.
 template <int D, bool kBF16>
-__device__ __forceinline__ void store_row(uint32_t taddr, float mul, uint16_t* dst, bool write) {
+__device__ __forceinline__ void store_row(uint32_t taddr, float mul, uint16_t* dst, bool write, int half) {
 #pragma unroll
-    for (int ch = 0; ch < D / 32; ++ch) {
+    for (int c = 0; c < D / 64; ++c) {
+        const int ch = half * (D / 64) + c;
         uint32_t v[32];
         tmem_ld_x32(taddr + ch * 32, v);
         tmem_wait_ld_x32(v);
@@ -211,7 +221,7 @@ __device__ __forceinline__ BSetup bwd_setup(uint8_t* smem) {
         }
         for (int h = 0; h < 2; ++h) {
             mbar_init(b.st(h), 1);
-            mbar_init(b.pp(h), 4 * 32);
+            mbar_init(b.pp(h), 8 * 32);
         }
         mbar_init(b.bar_done, 1);
         mbar_init(b.bar_drain, 1);
@@ -356,9 +366,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         __syncwarp();
     } else {
         // elementwise: thread = key of the tile (TMEM lane); columns = query rows
-        const int kl = threadIdx.x;
+        const int kl = (warp & 3) * 32 + lane, half = warp >> 2;  // key; column half of the tile
         const int key = k0 + kl;
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const float c = p.scale_log2;
         bool ok = true;
         for (int it = 0; ok && it < T; ++it) {
@@ -369,15 +379,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                    (p.window > 0 && k0 <= i0 + BT - 1 + off - p.window);
             const float* lse2 = reinterpret_cast<const float*>(smem + C::kOffVec + s * 2 * BT * 4);
             const float* del = lse2 + BT;
-            // ---- phase A: P^T = exp2(S^T c - lse2) over the first 64 columns of S^T ----
+            // ---- phase A: P^T = exp2(S^T c - lse2), packed over S^T ----
             if (!(ok = bwait_warp(bs.st(0), it & 1, bs.abort_flag, p.status))) break;
             // the stage's row vectors came by bulk copy: observe their barrier too (its
             // phase cannot move on before this tile's products, which need this thread)
             if (!(ok = bwait_warp(bs.full(s), (it >> 1) & 1, bs.abort_flag, p.status))) break;
             tc_fence_after();
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                const int c0 = q4 * 32;  // TMEM column = query row of the tile
+            for (int qq = 0; qq < 2; ++qq) {
+                const int q4 = 2 * half + qq, c0 = q4 * 32;  // TMEM column = query row of the tile
                 uint32_t sv[32];
                 tmem_ld_x32(bs.tmem + lane_base + C::kColS + c0, sv);
                 tmem_wait_ld_x32(sv);
@@ -412,21 +422,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     chunk(std::true_type{});
                 else
                     chunk(std::false_type{});
-                tmem_st_x16(bs.tmem + lane_base + C::kColS + q4 * 16, pk);
+                tmem_st_x16(bs.tmem + lane_base + C::kColS + packed_col(q4), pk);
             }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bs.pp(0));
-            // ---- phase B: dS^T = P^T (dP^T - delta) over the first 64 columns of dP^T ----
+            // ---- phase B: dS^T = P^T (dP^T - delta), packed over dP^T ----
             // (masked entries have P = 0 already)
             if (!(ok = bwait_warp(bs.st(1), it & 1, bs.abort_flag, p.status))) break;
             tc_fence_after();
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                const int c0 = q4 * 32;
+            for (int qq = 0; qq < 2; ++qq) {
+                const int q4 = 2 * half + qq, c0 = q4 * 32;
                 uint32_t dpv[32], pv16[16];
                 tmem_ld_x32(bs.tmem + lane_base + C::kColDP + c0, dpv);
-                tmem_ld_x16(bs.tmem + lane_base + C::kColS + q4 * 16, pv16);
+                tmem_ld_x16(bs.tmem + lane_base + C::kColS + packed_col(q4), pv16);
                 tmem_wait_ld_x32(dpv);
                 reg_after_x16(pv16);
                 uint32_t dk[16];
@@ -442,7 +452,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     dk[2 * g4 + 1] = bpack2<kBF16>(p2 * (__uint_as_float(dpv[e + 2]) - d4.z),
                                                    p3 * (__uint_as_float(dpv[e + 3]) - d4.w));
                 }
-                tmem_st_x16(bs.tmem + lane_base + C::kColDP + q4 * 16, dk);
+                tmem_st_x16(bs.tmem + lane_base + C::kColDP + packed_col(q4), dk);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -454,15 +464,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (T == 0) {  // no query row sees these keys: zero gradients
             if (write) {
 #pragma unroll
-                for (int x = 0; x < D / 8; ++x) {
+                for (int x = half * (D / 16); x < (half + 1) * (D / 16); ++x) {
                     reinterpret_cast<uint4*>(dk_row)[x] = make_uint4(0, 0, 0, 0);
                     reinterpret_cast<uint4*>(dv_row)[x] = make_uint4(0, 0, 0, 0);
                 }
             }
         } else if (ok && bwait_warp(bs.bar_done, 0, bs.abort_flag, p.status)) {
             tc_fence_after();
-            store_row<D, kBF16>(bs.tmem + lane_base + C::kColAcc0, p.scale, dk_row, write);
-            store_row<D, kBF16>(bs.tmem + lane_base + C::kColAcc1, 1.f, dv_row, write);
+            store_row<D, kBF16>(bs.tmem + lane_base + C::kColAcc0, p.scale, dk_row, write, half);
+            store_row<D, kBF16>(bs.tmem + lane_base + C::kColAcc1, 1.f, dv_row, write, half);
         }
     }
     bwd_teardown(bs);
@@ -572,9 +582,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         __syncwarp();
     } else {
         // elementwise: thread = query row of the tile (TMEM lane); columns = keys
-        const int r = threadIdx.x;
+        const int r = (warp & 3) * 32 + lane, half = warp >> 2;  // row; column half of the tile
         const int row = i0 + r;
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const float c = p.scale_log2;
         const float lse2 = p.lse2[(size_t)bh * p.Mpad + row];  // -inf past M
         const float del = p.delta[(size_t)bh * p.Mpad + row];
@@ -589,8 +599,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (!(ok = bwait_warp(bs.st(0), it & 1, bs.abort_flag, p.status))) break;
             tc_fence_after();
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                const int c0 = q4 * 32;  // TMEM column = key of the tile
+            for (int qq = 0; qq < 2; ++qq) {
+                const int q4 = 2 * half + qq, c0 = q4 * 32;  // TMEM column = key of the tile
                 uint32_t sv[32];
                 tmem_ld_x32(bs.tmem + lane_base + C::kColS + c0, sv);
                 tmem_wait_ld_x32(sv);
@@ -627,12 +637,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bs.pp(0));
-            // ---- phase B: dS = P (dP - delta) over the first 64 columns of dP ----
+            // ---- phase B: dS = P (dP - delta), packed over dP ----
             if (!(ok = bwait_warp(bs.st(1), it & 1, bs.abort_flag, p.status))) break;
             tc_fence_after();
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                const int c0 = q4 * 32;
+            for (int qq = 0; qq < 2; ++qq) {
+                const int q4 = 2 * half + qq, c0 = q4 * 32;
                 uint32_t dpv[32], pv16[16];
                 tmem_ld_x32(bs.tmem + lane_base + C::kColDP + c0, dpv);
                 tmem_ld_x16(bs.tmem + lane_base + C::kColP + q4 * 16, pv16);
@@ -646,7 +656,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     dk[e2] = bpack2<kBF16>(p0 * (__uint_as_float(dpv[2 * e2]) - del),
                                            p1 * (__uint_as_float(dpv[2 * e2 + 1]) - del));
                 }
-                tmem_st_x16(bs.tmem + lane_base + C::kColDP + q4 * 16, dk);
+                tmem_st_x16(bs.tmem + lane_base + C::kColDP + packed_col(q4), dk);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -657,10 +667,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (T == 0) {  // no key visible to any row of the tile: zero gradient
             if (write)
 #pragma unroll
-                for (int x = 0; x < D / 8; ++x) reinterpret_cast<uint4*>(dq_row)[x] = make_uint4(0, 0, 0, 0);
+                for (int x = half * (D / 16); x < (half + 1) * (D / 16); ++x)
+                    reinterpret_cast<uint4*>(dq_row)[x] = make_uint4(0, 0, 0, 0);
         } else if (ok && bwait_warp(bs.bar_done, 0, bs.abort_flag, p.status)) {
             tc_fence_after();
-            store_row<D, kBF16>(bs.tmem + lane_base + C::kColAcc0, p.scale, dq_row, write);
+            store_row<D, kBF16>(bs.tmem + lane_base + C::kColAcc0, p.scale, dq_row, write, half);
         }
     }
     bwd_teardown(bs);
