@@ -468,6 +468,8 @@ def extra_measurements(args, dev, stream, flush):
     if args.workload == PREFILL_D128.name:
         out["prefill_d128_bf16_causal_backward"] = backward_measure(PREFILL_D128, True, steps, dev, stream)
         out["prefill_d128_bf16_noncausal_backward"] = backward_measure(PREFILL_D128, False, steps, dev, stream)
+    if args.workload == PREFILL_D128.name:
+        out["split_softmax_bf16_m1024_n131072"] = split_softmax_measure(1024, 131072, 4096, steps, dev, stream)
     if args.workload in (PREFILL_D128.name, DECODE_GQA.name):
         for ps in (16, 128):
             out[f"decode_gqa_paged{ps}"] = paged_decode_measure(DECODE_GQA, ps, steps, dev, stream, flush)
@@ -500,6 +502,26 @@ def backward_measure(w, causal, steps, dev, stream):
     del bsets
     return {"TFLOP/s": round(work / (ms * 1e-3) / 1e12, 2), "us": round(ms * 1e3, 1),
             "flops": "2.5x forward (five products over allowed pairs)", "path": "backward (dK/dV kernel + dQ kernel)"}
+
+
+def split_softmax_measure(M, N, chunk, steps, dev, stream):
+    """Wide-row split softmax of a seeded N(0,1) [M, N] BF16 matrix; bytes are the
+    method's own traffic: x read twice (statistics, then normalization), y
+    written once."""
+    import streaming_attention_gb300 as sa
+
+    x = (torch.randn(M, N, generator=torch.Generator().manual_seed(7)) * 4).to(torch.bfloat16)
+    sets = [(x.to(dev), torch.empty(M, N, dtype=torch.bfloat16, device=dev)) for _ in range(3)]
+    ws = torch.empty(sa.attn_split_softmax_workspace_bytes(M, N, chunk), dtype=torch.uint8, device=dev)
+
+    def fn_on(t, st):
+        sa.split_softmax(t[0], chunk, y=t[1], workspace=ws, stream=st)
+
+    ms = time_steady(fn_on, sets, steps, 3, stream)
+    nbytes = 3.0 * M * N * 2
+    del sets
+    return {"GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1), "us": round(ms * 1e3, 1),
+            "bytes": "x read twice + y written once", "path": f"split softmax, chunk {chunk}"}
 
 
 def paged_decode_measure(w, page_size, steps, dev, stream, flush):

@@ -253,6 +253,22 @@ ATTN_API int attn_decode_paged(const void* q, const void* k_pages, const void* v
                                int causal, int window, float scale, int dtype,
                                void* workspace, size_t ws_bytes, void* stream);
 
+/* Wide-row split softmax, the course's workshop A2 ("Intermediate and advanced
+ * kernel workshops": three ordered kernels with per-call scratch; answer key,
+ * A2 row and worked answer): y[i,:] = softmax(x[i,:]) for each row of a
+ * contiguous [M, N] matrix, computed as partial statistics per chunk of
+ * `chunk` columns, their merge relative to the common maximum, then a reread
+ * that normalizes, all on `stream`.
+ *   x, y: device [M, N], dtype ATTN_FP32, ATTN_FP16 or ATTN_BF16 (both), 16-byte
+ *         aligned; FP32 arithmetic, one cast of y. 1 <= N <= 131072; M >= 0
+ *         (M == 0 launches nothing). chunk: 256, 1024 or 4096.
+ *   workspace: 8 * M * (ceil(N / chunk) + 1) bytes (a float pair per chunk and
+ *         one merged pair per row), 8-byte aligned, or NULL to have it
+ *         allocated stream-ordered. Values are not validated; x must be finite. */
+ATTN_API size_t attn_split_softmax_workspace_bytes(int M, int N, int chunk);
+ATTN_API int attn_split_softmax(const void* x, void* y, int M, int N, int chunk, int dtype,
+                                void* workspace, size_t ws_bytes, void* stream);
+
 /* Human-readable text for a status code (static storage). */
 ATTN_API const char* attn_strerror(int status);
 

@@ -296,3 +296,17 @@ def attention_backward(q, k, v, do, causal=False, window=0, scale=None, heads=No
         dq[b, h] = scale * (ds @ k[b, g])
         dk[b, g] += scale * (ds.T @ q[b, h])
     return dq, dk, dv
+
+
+# --------------------------------------------------------------------------
+# Row softmax, FP64, by its definition
+# --------------------------------------------------------------------------
+def softmax_rows(x):
+    """softmax of each row of a 2-D array in FP64: exp(x - max) / sum. The
+    wide-row split method ("Intermediate and advanced kernel workshops", A2)
+    reaches this exactly up to rounding; the oracle is the definition."""
+    x = _f64(x)
+    if x.shape[0] == 0:
+        return x.copy()
+    e = np.exp(x - x.max(axis=1, keepdims=True))
+    return e / e.sum(axis=1, keepdims=True)

@@ -26,9 +26,11 @@ from .binding import (  # noqa: F401
     attn_fwd_host,
     attn_fwd_lse,
     attn_merge,
+    attn_split_softmax_workspace_bytes,
     attn_workspace_bytes,
     last_device_status,
     lib,
+    split_softmax,
     library_path,
     strerror,
 )

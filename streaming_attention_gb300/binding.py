@@ -72,6 +72,10 @@ def lib() -> ctypes.CDLL:
             L.attn_bwd_workspace_bytes.restype = sz
             L.attn_bwd.argtypes = [vp] * 9 + [ci] * 8 + [cf, ci, vp, sz, vp]
             L.attn_bwd.restype = ci
+            L.attn_split_softmax_workspace_bytes.argtypes = [ci, ci, ci]
+            L.attn_split_softmax_workspace_bytes.restype = sz
+            L.attn_split_softmax.argtypes = [vp, vp, ci, ci, ci, ci, vp, sz, vp]
+            L.attn_split_softmax.restype = ci
             L.attn_version.argtypes = []
             L.attn_version.restype = ci
             _lib = L
@@ -270,6 +274,24 @@ def attn_decode_paged(q, k_pages, v_pages, block_table, seq_lens, o, max_seq_len
                                  int(bool(causal)), int(window), float(scale or 0.0), _DTYPES[q.dtype],
                                  _ptr(workspace), ws_bytes, _stream(stream))
     _check(st, "attn_decode_paged")
+
+
+def attn_split_softmax_workspace_bytes(M, N, chunk=1024) -> int:
+    return int(lib().attn_split_softmax_workspace_bytes(M, N, chunk))
+
+
+def split_softmax(x, chunk=1024, y=None, workspace=None, stream=None) -> torch.Tensor:
+    """C-ABI ``attn_split_softmax``: row softmax of a contiguous 2-D tensor; returns y."""
+    if x.dim() != 2 or not x.is_contiguous() or x.dtype not in _DTYPES:
+        raise ValueError("x must be a contiguous 2-D float32/float16/bfloat16 tensor")
+    M, N = x.shape
+    if y is None:
+        y = torch.empty_like(x)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().attn_split_softmax(_ptr(x), _ptr(y), M, N, int(chunk), _DTYPES[x.dtype], _ptr(workspace), ws_bytes,
+                                  _stream(stream))
+    _check(st, "attn_split_softmax")
+    return y
 
 
 def last_device_status(stream=None) -> int:

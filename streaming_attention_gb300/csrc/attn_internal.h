@@ -87,6 +87,12 @@ struct BwdArgs {
 size_t bwd_workspace_bytes(int B, int Hq, int M);
 cudaError_t launch_bwd(const Problem& p, const BwdArgs& a, void* ws, int* status, cudaStream_t stream);
 
+// Wide-row split softmax (three kernels, scratch [M][T + 1] float2)
+bool split_softmax_chunk_ok(int chunk);
+size_t split_softmax_ws_bytes(int M, int N, int chunk);
+cudaError_t launch_split_softmax(const void* x, void* y, int M, int N, int chunk, int dtype, void* ws,
+                                 cudaStream_t stream);
+
 // Metadata validation and the device status word, shared by every entry point.
 int validate_problem(const void* q, const void* k, const void* v, const void* o, int B, int Hq, int Hkv, int M,
                      int N, int D, int causal, int window, float scale, int dtype, Problem* p);

@@ -451,6 +451,24 @@ def pin_backward_autograd(orc):
             assert np.allclose(got, want.numpy(), rtol=1e-11, atol=1e-12), (trial, causal, window)
 
 
+# --------------------------------------------------------------------------
+# Row softmax (wide-row split softmax oracle)
+# --------------------------------------------------------------------------
+def pin_softmax_rows(orc):
+    import oracle
+    rng = np.random.default_rng(41)
+    x = rng.standard_normal((6, 37)) * 5
+    got = oracle.softmax_rows(x)
+    want = torch.softmax(torch.from_numpy(x), dim=-1).numpy()  # library routine, float64
+    assert np.allclose(got, want, rtol=1e-13, atol=1e-15)
+    assert np.allclose(got.sum(axis=1), 1.0, rtol=0, atol=1e-14)
+    assert np.allclose(oracle.softmax_rows(x + rng.standard_normal((6, 1)) * 100), got, rtol=1e-12, atol=1e-15)
+    assert np.allclose(oracle.softmax_rows(np.full((2, 8), 3.5)), 1.0 / 8, rtol=0, atol=1e-16)  # constant row
+    one = np.zeros((1, 5)); one[0, 2] = 1000.0
+    assert np.allclose(oracle.softmax_rows(one), [[0, 0, 1, 0, 0]], rtol=0, atol=1e-300)
+    assert oracle.softmax_rows(np.zeros((0, 4))).shape == (0, 4)
+
+
 ALL_PINS = [
     pin_a3_worked_example,
     pin_a1_merge_example,
@@ -467,4 +485,5 @@ ALL_PINS = [
     pin_backward_i2_example,
     pin_backward_finite_differences,
     pin_backward_autograd,
+    pin_softmax_rows,
 ]

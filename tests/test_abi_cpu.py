@@ -155,3 +155,26 @@ def test_paged_workspace_bytes(L):
     assert sa.attn_decode_paged_workspace_bytes(0, 32, 8, 1, 128, 16, 512, 8192, True, 0) == 0  # no rows
     # a 4-byte aligned table and length array are accepted (validation passes, nothing launched: B = 0)
     assert paged(L, table=A4, lens=A4, B_=0) == 0
+
+
+def test_split_softmax_scratch_matches_the_a2_worked_answer(L):
+    import json
+    fx = json.load(open(os.path.join(ROOT, "tests", "golden", "a2_split_softmax_example.json")))
+    assert -(-fx["N"] // fx["chunk"]) == fx["chunks"]
+    assert sa.attn_split_softmax_workspace_bytes(fx["M"], fx["N"], fx["chunk"]) == fx["scratch_bytes"]
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dtype=9), -3),
+    (dict(M=-1), -2),
+    (dict(N=0), -2),
+    (dict(N=131073), -2),
+    (dict(chunk=512), -2),
+    (dict(M=20000, N=131072), -6),
+    (dict(x=None), -1),
+    (dict(y=A8), -7),
+])
+def test_split_softmax_validation(L, kw, status):
+    a = dict(x=A16, y=A16, M=4, N=100, chunk=1024, dtype=0)
+    a.update(kw)
+    assert L.attn_split_softmax(a["x"], a["y"], a["M"], a["N"], a["chunk"], a["dtype"], None, 0, None) == status
