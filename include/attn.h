@@ -277,6 +277,13 @@ ATTN_API const char* attn_strerror(int status);
  * ATTN_ERR_TIMEOUT. ATTN_ERR_CUDA if the synchronization itself failed. */
 ATTN_API int attn_last_device_status(void* stream);
 
+/* Self-test of failure reporting: launches one CTA that waits on an mbarrier
+ * phase nothing completes, gives up after timeout_us microseconds (1 ..
+ * 2,000,000) exactly as the kernels' bounded waits do, and sets the device
+ * status word; attn_last_device_status then returns ATTN_ERR_TIMEOUT. No fault,
+ * trap or hang: the context stays usable. The pages have no counterpart. */
+ATTN_API int attn_selftest_bounded_wait(unsigned timeout_us, void* stream);
+
 /* Library ABI version (major*100 + minor). */
 ATTN_API int attn_version(void);
 

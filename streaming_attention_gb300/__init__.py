@@ -30,6 +30,7 @@ from .binding import (  # noqa: F401
     attn_workspace_bytes,
     last_device_status,
     lib,
+    selftest_bounded_wait,
     split_softmax,
     library_path,
     strerror,

@@ -76,6 +76,8 @@ def lib() -> ctypes.CDLL:
             L.attn_split_softmax_workspace_bytes.restype = sz
             L.attn_split_softmax.argtypes = [vp, vp, ci, ci, ci, ci, vp, sz, vp]
             L.attn_split_softmax.restype = ci
+            L.attn_selftest_bounded_wait.argtypes = [ctypes.c_uint, vp]
+            L.attn_selftest_bounded_wait.restype = ci
             L.attn_version.argtypes = []
             L.attn_version.restype = ci
             _lib = L
@@ -292,6 +294,11 @@ def split_softmax(x, chunk=1024, y=None, workspace=None, stream=None) -> torch.T
                                   _stream(stream))
     _check(st, "attn_split_softmax")
     return y
+
+
+def selftest_bounded_wait(timeout_us=20000, stream=None) -> None:
+    """C-ABI ``attn_selftest_bounded_wait``: a wait that runs out on purpose (no fault)."""
+    _check(lib().attn_selftest_bounded_wait(int(timeout_us), _stream(stream)), "attn_selftest_bounded_wait")
 
 
 def last_device_status(stream=None) -> int:

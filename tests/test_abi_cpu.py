@@ -178,3 +178,8 @@ def test_split_softmax_validation(L, kw, status):
     a = dict(x=A16, y=A16, M=4, N=100, chunk=1024, dtype=0)
     a.update(kw)
     assert L.attn_split_softmax(a["x"], a["y"], a["M"], a["N"], a["chunk"], a["dtype"], None, 0, None) == status
+
+
+def test_selftest_rejects_bad_limits(L):
+    assert L.attn_selftest_bounded_wait(0, None) == -2
+    assert L.attn_selftest_bounded_wait(3000000, None) == -2
