@@ -466,6 +466,10 @@ def extra_measurements(args, dev, stream, flush):
                          "cold_call_us": round(cold * 1e3, 1), "path": pname}
         del sets, ws
     if args.workload == PREFILL_D128.name:
+        for causal in (True, False):
+            name = "prefill_d128_e4m3_" + ("causal" if causal else "noncausal")
+            out[name] = fp8_measure(PREFILL_D128, causal, steps, dev, stream, flush)
+    if args.workload == PREFILL_D128.name:
         out["prefill_d128_bf16_causal_backward"] = backward_measure(PREFILL_D128, True, steps, dev, stream)
         out["prefill_d128_bf16_noncausal_backward"] = backward_measure(PREFILL_D128, False, steps, dev, stream)
     if args.workload == PREFILL_D128.name:
@@ -474,6 +478,37 @@ def extra_measurements(args, dev, stream, flush):
         for ps in (16, 128):
             out[f"decode_gqa_paged{ps}"] = paged_decode_measure(DECODE_GQA, ps, steps, dev, stream, flush)
     return out
+
+
+def fp8_measure(w, causal, steps, dev, stream, flush):
+    """attn_fwd_fp8 on the workload's shape with seeded E4M3 inputs (descale 1)
+    and a BF16 output; the same algorithmic FLOPs as the 16-bit forward, and the
+    roofline peak is the 8-bit dense rate: the measured BF16 peak times the
+    nominal 8-bit / 16-bit ratio of 2."""
+    import streaming_attention_gb300 as sa
+    from streaming_attention_gb300.inputs import make_qkv_fp8
+
+    q, k, v = make_qkv_fp8(w.B, w.Hq, w.Hkv, w.M, w.N, w.D, w.seed)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    per_set = q.numel() * 3 + k.numel() * 2
+    r = max(2, min(8, math.ceil(3 * l2 / per_set) + 1))
+    sets = [(q.to(dev), k.to(dev), v.to(dev), torch.empty(q.shape, dtype=torch.bfloat16, device=dev))
+            for _ in range(r)]
+
+    def fn_on(t, st):
+        sa.attn_fwd_fp8(t[0], t[1], t[2], t[3], None, causal, w.window, 0.0, 1.0, 1.0, 1.0, st)
+
+    ms = time_steady(fn_on, sets, steps, 3, stream)
+    cold = statistics.median(time_graph(lambda st: fn_on(sets[0], st), steps, 3, flush))
+    tf = flops(w, causal) / (ms * 1e-3) / 1e12
+    pk, pk_src = peaks()
+    fp8_peak = 2.0 * pk["bf16_tflops"] if pk.get("bf16_tflops") else None
+    del sets
+    return {"TFLOP/s": round(tf, 2), "us": round(ms * 1e3, 1), "cold_call_us": round(cold * 1e3, 1),
+            "frac_of_fp8_peak": round(tf / fp8_peak, 4) if fp8_peak else None,
+            "fp8_peak_tflops": round(fp8_peak, 1) if fp8_peak else None, "peak_source": pk_src,
+            "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4) if pk.get("bf16_tflops") else None,
+            "path": "prefill tcgen05 kind::f8f6f4 (E4M3 Q, K, V and P)"}
 
 
 def backward_measure(w, causal, steps, dev, stream):

@@ -130,6 +130,33 @@ ATTN_API int attn_fwd_lse(const void* q, const void* k, const void* v, void* o, 
                           int causal, int window, float scale, int dtype, int path,
                           void* workspace, size_t ws_bytes, void* stream);
 
+/* Forward pass on 8-bit E4M3 inputs (the OCP 8-bit floating-point E4M3
+ * encoding: 1 sign, 4 exponent bits with bias 7, 3 mantissa bits, subnormals,
+ * no infinities, S.1111.111 is NaN) with per-tensor dequantization factors:
+ * the operation is the forward pass of attn_fwd on the dequantized tensors
+ *   Q = q_descale * q, K = k_descale * k, V = v_descale * v,
+ *   O = softmax(scale * Q K^T over the visible keys) V,
+ * written as BF16 or FP16 (out_dtype). Both products run on the tensor cores
+ * with 8-bit operands: the probabilities P (relative to each row's running
+ * reference maximum, at most 2^8) are rounded to E4M3 before the value
+ * product, while the row sum l adds the unrounded FP32 values. The rounding
+ * of P is the one approximation beyond FP32 accumulation: each output
+ * element's error is at most 2^-4 times the weighted mean of |V| over its row
+ * (plus 2^-10 / l per key for probabilities below E4M3's normal range).
+ * An FP8 extension of the tcgen05 prefill kernel: the pages use 16-bit inputs
+ * only.
+ *   q: device bytes [B, Hq, M, D]; k, v: device bytes [B, Hkv, N, D]; o: device
+ *   [B, Hq, M, D] of out_dtype (ATTN_BF16 / ATTN_FP16, else ATTN_ERR_DTYPE); all
+ *   16-byte aligned. lse: as attn_fwd_lse (of the dequantized logits), or NULL.
+ *   D must be 128 (ATTN_ERR_HEADDIM). Descale factors must be finite (not
+ *   checked). M == 0: nothing is written; N == 0: o is zero-filled (and lse
+ *   set to -inf). Needs no workspace. */
+ATTN_API int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
+                          int B, int Hq, int Hkv, int M, int N, int D,
+                          int causal, int window, float scale,
+                          float q_descale, float k_descale, float v_descale,
+                          int out_dtype, void* stream);
+
 /* Backward pass: gradients of L = sum(dO * O) for O = attention(Q, K, V).
  * Each row of the weight gradient is the softmax vector-Jacobian product of
  * that row ("Intermediate and advanced kernel workshops", workshop I2, softmax

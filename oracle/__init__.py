@@ -10,6 +10,9 @@ row, materialize the FP64 score row over the allowed keys, take its maximum,
 exponentiate, sum, divide ("Compare reasoning after your own attempt",
 "Reference tradeoffs to challenge": the FP64 materializing oracle). The
 summary merge follows the same page's A1 row and worked answer.
+``decode_e4m3`` writes out the E4M3 code table of the OCP 8-bit
+floating-point format, and ``attention_fp8`` is the plain attention of the
+decoded tensors times their dequantization factors.
 
 Parity pins: every exported function is pinned in ``tests/test_oracle_pins.py``
 against worked answers from the pages, closed forms, invariants and an
@@ -310,3 +313,42 @@ def softmax_rows(x):
         return x.copy()
     e = np.exp(x - x.max(axis=1, keepdims=True))
     return e / e.sum(axis=1, keepdims=True)
+
+
+# --------------------------------------------------------------------------
+# 8-bit E4M3 inputs, by definition
+
+
+def decode_e4m3(codes) -> np.ndarray:
+    """Exact FP64 values of E4M3 codes (the OCP 8-bit floating-point format's
+    E4M3 encoding): bit 7 sign, bits 6-3 exponent field e (bias 7), bits 2-0
+    mantissa m; e = 0 is subnormal, m/8 * 2^-6; otherwise (1 + m/8) * 2^(e-7);
+    e = 15 with m = 7 is NaN (no infinities). Accepts a uint8 array or an
+    E4M3 / uint8 torch tensor."""
+    if hasattr(codes, "detach"):
+        import torch
+
+        t = codes.detach().to("cpu")
+        if t.dtype != torch.uint8:
+            t = t.view(torch.uint8)
+        codes = t.numpy()
+    b = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = (b & 0x7).astype(np.float64)
+    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2((e - 7).astype(np.float64)))
+    mag = np.where((e == 15) & (b & 0x7 == 7), np.nan, mag)
+    return sign * mag
+
+
+def attention_fp8(q, k, v, q_descale=1.0, k_descale=1.0, v_descale=1.0, causal=False, window=0, scale=None,
+                  nthreads=0, with_lse=False):
+    """Attention of dequantized E4M3 inputs: Q = q_descale * q, K = k_descale * k,
+    V = v_descale * v (each product exact in FP64), then the plain FP64
+    attention (and log-sum-exp) of those tensors."""
+    qd = float(q_descale) * decode_e4m3(q)
+    kd = float(k_descale) * decode_e4m3(k)
+    vd = float(v_descale) * decode_e4m3(v)
+    if with_lse:
+        return attention_lse(qd, kd, vd, causal, window, scale, nthreads)
+    return attention(qd, kd, vd, causal, window, scale, nthreads)

@@ -15,6 +15,7 @@ from .binding import (  # noqa: F401
     PATH_SIMT,
     AttnError,
     attention,
+    attention_fp8,
     attention_lse,
     attn_bwd,
     attn_bwd_workspace_bytes,
@@ -23,6 +24,7 @@ from .binding import (  # noqa: F401
     attn_fwd,
     attn_fwd_decode_noalloc,
     attn_fwd_ex,
+    attn_fwd_fp8,
     attn_fwd_host,
     attn_fwd_lse,
     attn_merge,

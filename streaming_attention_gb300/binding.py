@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
             L.attn_decode_paged.restype = ci
             L.attn_fwd_lse.argtypes = [vp] * 5 + [ci] * 8 + [cf, ci, ci, vp, sz, vp]
             L.attn_fwd_lse.restype = ci
+            L.attn_fwd_fp8.argtypes = [vp] * 5 + [ci] * 8 + [cf, cf, cf, cf, ci, vp]
+            L.attn_fwd_fp8.restype = ci
             L.attn_bwd_workspace_bytes.argtypes = [ci, ci, ci]
             L.attn_bwd_workspace_bytes.restype = sz
             L.attn_bwd.argtypes = [vp] * 9 + [ci] * 8 + [cf, ci, vp, sz, vp]
@@ -170,6 +172,39 @@ def attention_lse(q, k, v, causal=False, window=0, scale=0.0, path=PATH_AUTO, st
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
     attn_fwd_lse(q, k, v, o, lse, causal, window, scale, path, None, stream)
     return o, lse
+
+
+def attn_fwd_fp8(q, k, v, o, lse=None, causal=False, window=0, scale=0.0, q_descale=1.0, k_descale=1.0,
+                 v_descale=1.0, stream=None) -> None:
+    """C-ABI ``attn_fwd_fp8``: q, k, v are E4M3 (``torch.float8_e4m3fn``) device
+    tensors, ``o`` BF16 or FP16 of q's shape, ``lse`` an optional float32
+    [B, Hq, M] tensor."""
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D: [B, Hq, M, D] and [B, Hkv, N, D]")
+    B, Hq, M, D = q.shape
+    Bk, Hkv, N, Dk = k.shape
+    if (Bk, Dk) != (B, D) or tuple(v.shape) != tuple(k.shape) or tuple(o.shape) != tuple(q.shape):
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)} o{tuple(o.shape)}")
+    for t in (q, k, v):
+        if t.dtype != torch.float8_e4m3fn or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous float8_e4m3fn tensors")
+    if o.dtype not in (torch.bfloat16, torch.float16) or not o.is_contiguous():
+        raise ValueError("o must be a contiguous bfloat16 or float16 tensor")
+    if lse is not None and (lse.shape != (B, Hq, M) or lse.dtype != torch.float32 or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous float32 [B, Hq, M] tensor")
+    st = lib().attn_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, M, N, D,
+                            int(bool(causal)), int(window), float(scale or 0.0), float(q_descale),
+                            float(k_descale), float(v_descale), _DTYPES[o.dtype], _stream(stream))
+    _check(st, "attn_fwd_fp8")
+
+
+def attention_fp8(q, k, v, causal=False, window=0, scale=0.0, q_descale=1.0, k_descale=1.0, v_descale=1.0,
+                  out_dtype=torch.bfloat16, with_lse=False, stream=None):
+    """New output tensor (and log-sum-exp when ``with_lse``), then ``attn_fwd_fp8`` into it."""
+    o = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device) if with_lse else None
+    attn_fwd_fp8(q, k, v, o, lse, causal, window, scale, q_descale, k_descale, v_descale, stream)
+    return (o, lse) if with_lse else o
 
 
 def attn_bwd_workspace_bytes(B, Hq, M) -> int:

@@ -103,5 +103,9 @@ int* device_status_ptr();
 int launch_prefill(const Problem& p, const void* q, const void* k, const void* v, void* o,
                    int* status, cudaStream_t stream);
 bool prefill_supported(const Problem& p);
+// The same kernel on E4M3 inputs (D = 128); p.dtype is the output type and
+// p.scale_log2 already includes the Q and K dequantization factors.
+int launch_prefill_e4m3(const Problem& p, const void* q, const void* k, const void* v, void* o, int* status,
+                        float v_scale, cudaStream_t stream);
 
 }  // namespace attn

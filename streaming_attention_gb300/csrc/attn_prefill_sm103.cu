@@ -57,12 +57,17 @@ constexpr int kMmaWarp = 9;
 constexpr uint64_t kTimeoutNs = 1000000000ull;
 constexpr float kRescaleThreshold = 8.0f;
 
-template <int D>
+// Input element kinds: 16-bit (output of the same type) or 8-bit E4M3 (output BF16 or FP16).
+constexpr int kInF16 = 0, kInBF16 = 1, kInE4M3 = 2;
+
+template <int D, int EB>  // EB: bytes per input element
 struct Cfg {
-    static constexpr int kChunks = D / 64;            // 128-byte swizzle chunks along D
+    static constexpr int kRowBytes = D * EB;
+    static constexpr int kChunks = kRowBytes / 128;   // 128-byte swizzle chunks along D
+    static constexpr int kChunkElems = 128 / EB;      // elements of D per chunk
     static constexpr int kChunkBytes = BM * 128;      // one chunk of a 128-row tile
-    static constexpr int kTileBytes = BM * D * 2;     // one Q, K or V tile
-    static constexpr int kStages = (D == 128) ? 4 : 8;
+    static constexpr int kTileBytes = BM * kRowBytes; // one Q, K or V tile
+    static constexpr int kStages = (kRowBytes == 256) ? 4 : 8;
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = NQ * kTileBytes;
     static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
@@ -82,7 +87,8 @@ struct PrefillParams {
     int* status;
     int M, N, Hq, Hkv, G;
     int causal, window;
-    float scale_log2;
+    float scale_log2;  // for 8-bit inputs this includes the Q and K dequantization factors
+    float v_scale;     // V dequantization factor (1 for 16-bit inputs), applied with 1 / l
     int BH;     // B * Hq
     int nqb;    // work tiles per head (ceil(M / 256))
     int tiles;  // BH * nqb
@@ -166,28 +172,43 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 }
 
 // MMA groups issued from precomputed descriptors: the issuing thread must
-// keep up with the tensor core (a 128x128x16 MMA retires in 64 cycles), so
-// each K step only adds a compile-time offset to a 64-bit descriptor.
-template <int D>
+// keep up with the tensor core (a 128x128 MMA step retires in 64 cycles for
+// 16-bit inputs, 32 for 8-bit), so each K step only adds a compile-time offset
+// to a 64-bit descriptor. Every K step covers 32 bytes of a row: 16 elements
+// of 16 bits or 32 of 8 bits.
+template <int D, int EB>
 __device__ __forceinline__ void mma_group_s(uint32_t d_tmem, uint64_t a0, uint64_t b0, uint32_t idesc) {
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t off = (uint64_t)((((kk >> 2) * Cfg<D>::kChunkBytes) + (kk & 3) * 32) >> 4);
-        mma_ss(d_tmem, a0 + off, b0 + off, idesc, kk > 0 ? 1u : 0u);
+    for (int kk = 0; kk < D * EB / 32; ++kk) {
+        const uint64_t off = (uint64_t)((((kk >> 2) * Cfg<D, EB>::kChunkBytes) + (kk & 3) * 32) >> 4);
+        if constexpr (EB == 1)
+            mma_ss_f8(d_tmem, a0 + off, b0 + off, idesc, kk > 0 ? 1u : 0u);
+        else
+            mma_ss(d_tmem, a0 + off, b0 + off, idesc, kk > 0 ? 1u : 0u);
     }
 }
+// P from TMEM (8 columns per K step: two 16-bit or four 8-bit values per
+// column), V from a shared-memory slot (MN-major: one K step is kKStep key rows)
+template <int EB>
 __device__ __forceinline__ void mma_group_pv(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0, uint32_t idesc,
                                              bool first) {
+    constexpr int kStep = 32 / EB;
 #pragma unroll
-    for (int kk = 0; kk < BN / 16; ++kk)
-        mma_ts(d_tmem, a_tmem + kk * 8, b0 + (uint64_t)((kk * 16 * 128) >> 4), idesc, (first && kk == 0) ? 0u : 1u);
+    for (int kk = 0; kk < BN / kStep; ++kk) {
+        const uint64_t b = b0 + (uint64_t)((kk * kStep * 128) >> 4);
+        if constexpr (EB == 1)
+            mma_ts_f8(d_tmem, a_tmem + kk * 8, b, idesc, (first && kk == 0) ? 0u : 1u);
+        else
+            mma_ts(d_tmem, a_tmem + kk * 8, b, idesc, (first && kk == 0) ? 0u : 1u);
+    }
 }
 
-template <int D, bool kBF16>
+template <int D, int kIn, bool kBF16>  // kBF16: output type (and input type for 16-bit inputs)
 __global__ void __launch_bounds__(kThreads, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
-    using C = Cfg<D>;
+    constexpr int EB = kIn == kInE4M3 ? 1 : 2;
+    using C = Cfg<D, EB>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -251,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(bar.q_full, NQ * C::kTileBytes);
                 for (int t = 0; t < NQ; ++t)
                     for (int c = 0; c < C::kChunks; ++c)
-                        tma_load_3d(sQ + t * C::kTileBytes + c * C::kChunkBytes, &tmQ, c * 64, wk.row0 + t * BM,
+                        tma_load_3d(sQ + t * C::kTileBytes + c * C::kChunkBytes, &tmQ, c * C::kChunkElems, wk.row0 + t * BM,
                                     wk.bh, bar.q_full);
                 ++q_issued;
                 // K_j and V_j alternate through the ring in the order the MMA uses them
@@ -264,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const CUtensorMap* tm = (x & 1) ? &tmV : &tmK;
                     const int key0 = (wk.jt0 + x / 2) * BN;
                     for (int c = 0; c < C::kChunks; ++c)
-                        tma_load_3d(sKV + s * C::kTileBytes + c * C::kChunkBytes, tm, c * 64, key0, wk.kvh,
+                        tma_load_3d(sKV + s * C::kTileBytes + c * C::kChunkBytes, tm, c * C::kChunkElems, key0, wk.kvh,
                                     bar.full(s));
                 }
                 ++tc;
@@ -277,8 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
-            constexpr uint32_t idS = idesc_f16(kBF16, BM, BN, false);
-            constexpr uint32_t idPV = idesc_f16(kBF16, BM, D, true);
+            constexpr uint32_t idS = EB == 1 ? idesc_e4m3(BM, BN, false) : idesc_f16(kBF16, BM, BN, false);
+            constexpr uint32_t idPV = EB == 1 ? idesc_e4m3(BM, D, true) : idesc_f16(kBF16, BM, D, true);
             int u = 0, tc = 0;
             int ps[NQ] = {0, 0};  // P tiles consumed per query tile, across the walk
             bool ok = true;
@@ -290,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dv = sw128_desc(sKV, C::kChunkBytes, 1024);
             constexpr uint64_t kSlotStep = (uint64_t)(C::kTileBytes >> 4);
             auto issue_s = [&](int t, int slot) {
-                mma_group_s<D>(tmem + col_s(t), t ? dq1 : dq0, dk + (uint64_t)slot * kSlotStep, idS);
+                mma_group_s<D, EB>(tmem + col_s(t), t ? dq1 : dq0, dk + (uint64_t)slot * kSlotStep, idS);
             };
             // O_t += P_t V; the first product of a tile overwrites O_t, after the
             // previous tile's epilogue has read it out
@@ -299,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++ps[t];
                 if (first && tc > 0 && !wait_one(bar.o_free(t), (tc - 1) & 1, abort_flag, p.status)) return false;
                 tc_fence_after();
-                mma_group_pv(tmem + col_o(t), tmem + col_s(t), dv + (uint64_t)slot * kSlotStep, idPV, first);
+                mma_group_pv<EB>(tmem + col_o(t), tmem + col_s(t), dv + (uint64_t)slot * kSlotStep, idPV, first);
                 return true;
             };
             Work wk;
@@ -424,15 +445,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float neg_m = -m_use;
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
-                    uint32_t packed[16];
+                    if constexpr (EB == 2) {
+                        uint32_t packed[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float p0 = ex2(fmaf(__uint_as_float(s[q4][2 * e]), c, neg_m));
-                        const float p1 = ex2(fmaf(__uint_as_float(s[q4][2 * e + 1]), c, neg_m));
-                        l += p0 + p1;
-                        packed[e] = pack2<kBF16>(p0, p1);
+                        for (int e = 0; e < 16; ++e) {
+                            const float p0 = ex2(fmaf(__uint_as_float(s[q4][2 * e]), c, neg_m));
+                            const float p1 = ex2(fmaf(__uint_as_float(s[q4][2 * e + 1]), c, neg_m));
+                            l += p0 + p1;
+                            packed[e] = pack2<kBF16>(p0, p1);
+                        }
+                        tmem_st_x16(tS + q4 * 16, packed);  // P overwrites the first 64 columns of S
+                    } else {
+                        // P rounded to E4M3 for the value product (p <= 256 < 448); l
+                        // sums the unrounded FP32 values
+                        uint32_t packed[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            float pv[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) pv[i] = ex2(fmaf(__uint_as_float(s[q4][4 * e + i]), c, neg_m));
+                            l += (pv[0] + pv[1]) + (pv[2] + pv[3]);
+                            packed[e] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
+                        }
+                        tmem_st_x8(tS + q4 * 8, packed);  // P overwrites the first 32 columns of S
                     }
-                    tmem_st_x16(tS + q4 * 16, packed);  // P overwrites the first 64 columns of S
                 }
                 // rescale the accumulator (the value product of the previous key tile
                 // has completed: its commit preceded this tile's score commit)
@@ -457,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = wait_warp(bar.o_final, tc & 1, abort_flag, p.status))) break;
             ++tc;
             tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;  // no visible key: output 0
+            const float inv = l > 0.f ? p.v_scale / l : 0.f;  // no visible key: output 0
             // log sum_j e^(scale s_j) = ln 2 * (m_ref + log2 l) (p was taken against m_ref)
             if (p.lse && row < p.M)
                 p.lse[(size_t)wk.bh * p.M + row] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
@@ -503,21 +539,22 @@ int sm_count_prefill() {
     return n;
 }
 
-template <int D, bool kBF16>
-int launch_t(const Problem& pr, const void* q, const void* k, const void* v, void* o, int* status,
+template <int D, int kIn, bool kBF16>
+int launch_t(const Problem& pr, const void* q, const void* k, const void* v, void* o, int* status, float v_scale,
              cudaStream_t stream) {
-    using C = Cfg<D>;
+    constexpr int EB = kIn == kInE4M3 ? 1 : 2;
+    using C = Cfg<D, EB>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(attn_prefill_kernel<D, kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(attn_prefill_kernel<D, kIn, kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         C::kSmemBytes);
     });
     if (attr_err != cudaSuccess) return ATTN_ERR_CUDA;
     CUtensorMap tq, tk, tv;
-    if (!make_tensor_map(&tq, q, D, pr.M, pr.B * pr.Hq, BM, kBF16) ||
-        !make_tensor_map(&tk, k, D, pr.N, pr.B * pr.Hkv, BN, kBF16) ||
-        !make_tensor_map(&tv, v, D, pr.N, pr.B * pr.Hkv, BN, kBF16))
+    if (!make_tensor_map(&tq, q, D, pr.M, pr.B * pr.Hq, BM, kBF16, EB) ||
+        !make_tensor_map(&tk, k, D, pr.N, pr.B * pr.Hkv, BN, kBF16, EB) ||
+        !make_tensor_map(&tv, v, D, pr.N, pr.B * pr.Hkv, BN, kBF16, EB))
         return ATTN_ERR_CUDA;
     PrefillParams pp;
     pp.o = o;
@@ -531,11 +568,12 @@ int launch_t(const Problem& pr, const void* q, const void* k, const void* v, voi
     pp.causal = pr.causal;
     pp.window = pr.window;
     pp.scale_log2 = pr.scale_log2;
+    pp.v_scale = v_scale;
     pp.BH = pr.B * pr.Hq;
     pp.nqb = (pr.M + NQ * BM - 1) / (NQ * BM);
     pp.tiles = pp.BH * pp.nqb;
     const int grid = pp.tiles < sm_count_prefill() ? pp.tiles : sm_count_prefill();
-    attn_prefill_kernel<D, kBF16><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, pp);
+    attn_prefill_kernel<D, kIn, kBF16><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, pp);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -548,11 +586,18 @@ bool prefill_supported(const Problem& p) {
 int launch_prefill(const Problem& p, const void* q, const void* k, const void* v, void* o, int* status,
                    cudaStream_t stream) {
     const bool bf16 = p.dtype == ATTN_BF16;
-    if (p.D == 128) return bf16 ? launch_t<128, true>(p, q, k, v, o, status, stream)
-                                : launch_t<128, false>(p, q, k, v, o, status, stream);
-    if (p.D == 64) return bf16 ? launch_t<64, true>(p, q, k, v, o, status, stream)
-                               : launch_t<64, false>(p, q, k, v, o, status, stream);
+    if (p.D == 128) return bf16 ? launch_t<128, kInBF16, true>(p, q, k, v, o, status, 1.f, stream)
+                                : launch_t<128, kInF16, false>(p, q, k, v, o, status, 1.f, stream);
+    if (p.D == 64) return bf16 ? launch_t<64, kInBF16, true>(p, q, k, v, o, status, 1.f, stream)
+                               : launch_t<64, kInF16, false>(p, q, k, v, o, status, 1.f, stream);
     return ATTN_ERR_HEADDIM;
+}
+
+int launch_prefill_e4m3(const Problem& p, const void* q, const void* k, const void* v, void* o, int* status,
+                        float v_scale, cudaStream_t stream) {
+    if (p.D != 128) return ATTN_ERR_HEADDIM;
+    return p.dtype == ATTN_BF16 ? launch_t<128, kInE4M3, true>(p, q, k, v, o, status, v_scale, stream)
+                                : launch_t<128, kInE4M3, false>(p, q, k, v, o, status, v_scale, stream);
 }
 
 }  // namespace attn

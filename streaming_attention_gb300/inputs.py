@@ -86,6 +86,21 @@ def make_qkv(B: int, Hq: int, Hkv: int, M: int, N: int, D: int, dtype: torch.dty
     return q.to(dtype), k.to(dtype), v.to(dtype)
 
 
+def make_qkv_fp8(B: int, Hq: int, Hkv: int, M: int, N: int, D: int, seed: int, q_descale: float = 1.0,
+                 k_descale: float = 1.0, v_descale: float = 1.0):
+    """Seeded E4M3 inputs (``torch.float8_e4m3fn``, on the CPU): the FP32 normal
+    draws of ``make_qkv`` divided by each tensor's dequantization factor, then
+    rounded to E4M3 (round to nearest even), so that descale * stored value is
+    about N(0, 1)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    q = torch.randn((B, Hq, M, D), generator=g, dtype=torch.float32) / q_descale
+    k = torch.randn((B, Hkv, N, D), generator=g, dtype=torch.float32) / k_descale
+    v = torch.randn((B, Hkv, N, D), generator=g, dtype=torch.float32) / v_descale
+    f8 = torch.float8_e4m3fn
+    return q.to(f8), k.to(f8), v.to(f8)
+
+
 def workload_inputs(w: Workload, dtype: Optional[torch.dtype] = None):
     return make_qkv(w.B, w.Hq, w.Hkv, w.M, w.N, w.D, dtype or w.dtype, w.seed, w.ramp_bias)
 

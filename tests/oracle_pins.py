@@ -469,6 +469,59 @@ def pin_softmax_rows(orc):
     assert oracle.softmax_rows(np.zeros((0, 4))).shape == (0, 4)
 
 
+# --------------------------------------------------------------------------
+# E4M3 inputs: the code table and the dequantized attention
+# --------------------------------------------------------------------------
+def pin_e4m3_decode(orc):
+    import oracle
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.decode_e4m3(codes)
+    # closed forms of the encoding (bias 7, 3 mantissa bits, subnormals below 2^-6)
+    want = {0x00: 0.0, 0x38: 1.0, 0xB8: -1.0, 0x7E: 448.0, 0xFE: -448.0, 0x01: 2.0 ** -9,
+            0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x3F: 1.875, 0x40: 2.0, 0x30: 0.5, 0x3C: 1.5, 0x77: 240.0}
+    for c, val in want.items():
+        assert got[c] == val, (hex(c), got[c], val)
+    assert np.signbit(got[0x80]) and got[0x80] == 0.0
+    assert np.isnan(got[0x7F]) and np.isnan(got[0xFF]) and np.isnan(got).sum() == 2
+    # magnitudes strictly increase with the code; the sign bit mirrors them
+    assert np.all(np.diff(got[:0x7F]) > 0)
+    assert np.array_equal(got[0x80:0xFF], -got[:0x7F])
+    # the library's own E4M3 conversion agrees on every code
+    lib = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(lib), np.isnan(got))
+    assert np.array_equal(lib[~np.isnan(lib)], got[~np.isnan(got)])
+    # and rounding each finite value back to E4M3 returns its code
+    fin = ~np.isnan(got)
+    back = torch.from_numpy(got[fin]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(back, codes[fin])
+
+
+def pin_attention_fp8(orc):
+    import oracle
+    g = torch.Generator().manual_seed(44)
+    f8 = torch.float8_e4m3fn
+    B, Hq, Hkv, M, N, D = 1, 4, 2, 9, 13, 16
+    q = (torch.randn(B, Hq, M, D, generator=g) * 2).to(f8)
+    k = (torch.randn(B, Hkv, N, D, generator=g) * 3).to(f8)
+    v = (torch.randn(B, Hkv, N, D, generator=g) * 4).to(f8)
+    qd, kd, vd, scale = 0.5, 0.125, 0.25, 0.3
+    for causal, window in ((False, 0), (True, 0), (True, 5)):
+        got = oracle.attention_fp8(q, k, v, qd, kd, vd, causal=causal, window=window, scale=scale)
+        # a library formula on the library's own FP8 -> FP64 conversion
+        want = library_attention(q.to(torch.float64).numpy() * qd, k.to(torch.float64).numpy() * kd,
+                                 v.to(torch.float64).numpy() * vd, causal, window, scale)
+        assert np.allclose(got, want, rtol=1e-12, atol=1e-13), (causal, window)
+        # homogeneity: the Q and K factors only rescale the logits, the V factor the output
+        plain = oracle.attention_fp8(q, k, v, 1.0, 1.0, 1.0, causal=causal, window=window, scale=scale * qd * kd)
+        assert np.allclose(got, vd * plain, rtol=1e-12, atol=1e-14)
+    # all-zero queries weight every visible key equally: the mean of V's rows
+    z = torch.zeros(B, Hq, M, D).to(f8)
+    got = oracle.attention_fp8(z, k, v, 1.0, 1.0, vd, causal=False)
+    vv = vd * v.to(torch.float64).numpy()
+    want = np.repeat(vv.mean(axis=2, keepdims=True), Hq // Hkv, axis=1).repeat(M, axis=2)
+    assert np.allclose(got, want, rtol=1e-13, atol=1e-14)
+
+
 ALL_PINS = [
     pin_a3_worked_example,
     pin_a1_merge_example,
@@ -486,4 +539,6 @@ ALL_PINS = [
     pin_backward_finite_differences,
     pin_backward_autograd,
     pin_softmax_rows,
+    pin_e4m3_decode,
+    pin_attention_fp8,
 ]

@@ -183,3 +183,22 @@ def test_split_softmax_validation(L, kw, status):
 def test_selftest_rejects_bad_limits(L):
     assert L.attn_selftest_bounded_wait(0, None) == -2
     assert L.attn_selftest_bounded_wait(3000000, None) == -2
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dtype=7), -3),
+    (dict(dtype=2), -3),                 # FP32 output is not offered
+    (dict(D=64), -4),
+    (dict(D=48), -4),
+    (dict(Hq=6, Hkv=4), -5),
+    (dict(k=None), -1),
+    (dict(q=A8), -7),
+    (dict(lse=ctypes.c_void_p(0x10002)), -7),
+    (dict(M=0), 0),                      # empty output: nothing to do, no launch
+])
+def test_fp8_validation_status(L, kw, status):
+    a = dict(q=A16, k=A16, v=A16, o=A16, lse=None, B_=1, Hq=2, Hkv=2, M=8, N=8, D=128, dtype=0)
+    a.update(kw)
+    st = L.attn_fwd_fp8(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B_"], a["Hq"], a["Hkv"], a["M"], a["N"],
+                        a["D"], 1, 0, 0.0, 1.0, 1.0, 1.0, a["dtype"], None)
+    assert st == status

@@ -1,0 +1,92 @@
+"""Forward pass on E4M3 inputs (attn_fwd_fp8) against the FP64 oracle of the
+dequantized tensors, through the C ABI. Tolerances: the rounding model of the
+probabilities in ``fp8_tolerance``; exact-mean cases (all-zero queries, where
+every probability is exactly 1) at the output cast's precision."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import streaming_attention_gb300 as sa
+from fp8_tolerance import CAST, bounds, check_fp8, row_bounds
+from streaming_attention_gb300.inputs import PREFILL_D128, make_qkv_fp8, sample_rows
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(autouse=True)
+def no_device_timeouts():
+    yield
+    assert sa.last_device_status() == 0, "a kernel gave up on a bounded wait"
+
+
+def deq(t, d):
+    return float(d) * oracle.decode_e4m3(t)
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float16], ids=["bf16", "fp16"])
+@pytest.mark.parametrize("shape,causal,window,descale", [
+    ((1, 2, 2, 256, 256, 128), False, 0, (1.0, 1.0, 1.0)),
+    ((1, 2, 2, 256, 256, 128), True, 0, (1.0, 1.0, 1.0)),
+    ((2, 4, 2, 200, 333, 128), True, 0, (0.5, 0.25, 2.0)),     # GQA, ragged, M < N, descales
+    ((1, 4, 1, 384, 384, 128), True, 150, (1.0, 1.0, 1.0)),    # window, four heads share one KV head
+    ((1, 2, 2, 333, 200, 128), False, 0, (0.125, 1.0, 0.5)),   # M > N
+    ((1, 2, 2, 300, 100, 128), True, 0, (1.0, 1.0, 1.0)),      # rows with no visible key
+    ((1, 3, 1, 1, 777, 128), True, 64, (1.0, 1.0, 1.0)),       # one query row
+])
+def test_fp8_forward_against_oracle(out_dtype, shape, causal, window, descale):
+    B, Hq, Hkv, M, N, D = shape
+    qd, kd, vd = descale
+    q, k, v = make_qkv_fp8(B, Hq, Hkv, M, N, D, 21, qd, kd, vd)
+    scale = 1.0 / np.sqrt(D)
+    o, lse = sa.attention_fp8(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, window=window, q_descale=qd,
+                              k_descale=kd, v_descale=vd, out_dtype=out_dtype, with_lse=True)
+    torch.cuda.synchronize()
+    want, want_lse = oracle.attention_fp8(q, k, v, qd, kd, vd, causal=causal, window=window, with_lse=True)
+    H, sigma, wabs = bounds(deq(q, qd), deq(k, kd), deq(v, vd), causal, window, scale)
+    check_fp8(o, want, H, sigma, wabs, out_dtype, f"{shape} causal={causal} window={window}")
+    g = lse.cpu().double().numpy()
+    assert np.array_equal(np.isneginf(g), np.isneginf(want_lse))
+    fin = np.isfinite(want_lse)
+    if fin.any():
+        assert np.abs(g[fin] - want_lse[fin]).max() <= 2e-3
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_zero_queries_give_exact_means(causal):
+    """All-zero queries: every visible key scores 0, every probability is exactly
+    1 in E4M3, and each output row is the mean of its visible V rows."""
+    B, Hq, Hkv, M, N, D = 1, 2, 1, 256, 300, 128
+    _, k, v = make_qkv_fp8(B, Hq, Hkv, M, N, D, 22, 1.0, 1.0, 0.5)
+    q = torch.zeros(B, Hq, M, D).to(torch.float8_e4m3fn)
+    o = sa.attention_fp8(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, v_descale=0.5)
+    torch.cuda.synchronize()
+    want = oracle.attention_fp8(q, k, v, 1.0, 1.0, 0.5, causal=causal)
+    err = np.abs(o.cpu().double().numpy() - want)
+    assert (err <= CAST[torch.bfloat16] * np.abs(want) + 1e-5).all(), err.max()
+
+
+def test_fp8_empty_dims():
+    q, k, v = make_qkv_fp8(1, 2, 2, 0, 64, 128, 0)
+    o = sa.attention_fp8(q.to(DEV), k.to(DEV), v.to(DEV), causal=True)
+    assert o.shape == (1, 2, 0, 128)
+    q, k, v = make_qkv_fp8(1, 2, 2, 64, 0, 128, 0)
+    o, lse = sa.attention_fp8(q.to(DEV), k.to(DEV), v.to(DEV), with_lse=True)
+    torch.cuda.synchronize()
+    assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+
+
+def test_fp8_full_size_sampled_rows():
+    """The causal prefill shape (B=2, H=32, M=N=4096, D=128) in E4M3, checked on
+    sampled rows: first and last rows of query tiles, the tail, random rows."""
+    w = PREFILL_D128
+    q, k, v = make_qkv_fp8(w.B, w.Hq, w.Hkv, w.M, w.N, w.D, 23)
+    o = sa.attention_fp8(q.to(DEV), k.to(DEV), v.to(DEV), causal=True)
+    torch.cuda.synchronize()
+    rows = sample_rows(w.B, w.Hq, w.M, 96)
+    qf, kf, vf = deq(q, 1.0), deq(k, 1.0), deq(v, 1.0)
+    want = oracle.attention_rows(qf, kf, vf, rows, causal=True)
+    got = o.reshape(-1, w.D)[torch.tensor(rows)].cpu()
+    H, sigma, wabs = row_bounds(qf, kf, vf, rows, True, 0, 1.0 / np.sqrt(w.D))
+    check_fp8(got, want, H, sigma, wabs, torch.bfloat16, "full size")
