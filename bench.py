@@ -66,13 +66,13 @@ def flops(w, causal=None, window=None):
     return 4.0 * w.D * w.B * w.Hq * allowed_pairs(w.M, w.N, causal, window)
 
 
-def decode_bytes(w):
-    """Q + O + the K and V rows that any query row may see, each read once."""
-    esz = 2
+def decode_bytes(w, in_bytes=2):
+    """Q + O + the K and V rows that any query row may see, each read once
+    (Q, K, V of in_bytes per element; O always 16-bit)."""
     lo = max(0, (w.N - w.M) - w.window + 1) if w.window > 0 else 0
     hi = w.N  # the last row sits at position N-1
-    kv = 2 * w.B * w.Hkv * (hi - lo) * w.D * esz
-    qo = 2 * w.B * w.Hq * w.M * w.D * esz
+    kv = 2 * w.B * w.Hkv * (hi - lo) * w.D * in_bytes
+    qo = w.B * w.Hq * w.M * w.D * (in_bytes + 2)
     return float(kv + qo)
 
 
@@ -475,6 +475,9 @@ def extra_measurements(args, dev, stream, flush):
     if args.workload == PREFILL_D128.name:
         out["split_softmax_bf16_m1024_n131072"] = split_softmax_measure(1024, 131072, 4096, steps, dev, stream)
     if args.workload in (PREFILL_D128.name, DECODE_GQA.name):
+        out["decode_gqa_e4m3"] = fp8_decode_measure(DECODE_GQA, None, steps, dev, stream, flush)
+        out["decode_gqa_e4m3_paged128"] = fp8_decode_measure(DECODE_GQA, 128, steps, dev, stream, flush)
+    if args.workload in (PREFILL_D128.name, DECODE_GQA.name):
         for ps in (16, 128):
             out[f"decode_gqa_paged{ps}"] = paged_decode_measure(DECODE_GQA, ps, steps, dev, stream, flush)
     return out
@@ -496,7 +499,8 @@ def fp8_measure(w, causal, steps, dev, stream, flush):
             for _ in range(r)]
 
     def fn_on(t, st):
-        sa.attn_fwd_fp8(t[0], t[1], t[2], t[3], None, causal, w.window, 0.0, 1.0, 1.0, 1.0, st)
+        sa.attn_fwd_fp8(t[0], t[1], t[2], t[3], None, causal, w.window, 0.0, 1.0, 1.0, 1.0, path=sa.PATH_PREFILL,
+                        stream=st)
 
     ms = time_steady(fn_on, sets, steps, 3, stream)
     cold = statistics.median(time_graph(lambda st: fn_on(sets[0], st), steps, 3, flush))
@@ -509,6 +513,61 @@ def fp8_measure(w, causal, steps, dev, stream, flush):
             "fp8_peak_tflops": round(fp8_peak, 1) if fp8_peak else None, "peak_source": pk_src,
             "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4) if pk.get("bf16_tflops") else None,
             "path": "prefill tcgen05 kind::f8f6f4 (E4M3 Q, K, V and P)"}
+
+
+def fp8_decode_measure(w, page_size, steps, dev, stream, flush):
+    """The decode workload on E4M3 inputs (descale 1, BF16 output): contiguous
+    (attn_fwd_fp8, decode path) or a paged cache of `page_size`-key pages in a
+    shuffled pool (attn_decode_paged_fp8). Bytes count 1 per Q/K/V element."""
+    import numpy as np
+
+    import streaming_attention_gb300 as sa
+    from streaming_attention_gb300.inputs import make_qkv_fp8
+
+    q, k, v = make_qkv_fp8(w.B, w.Hq, w.Hkv, w.M, w.N, w.D, w.seed)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    per_set = 2 * k.numel() + 3 * q.numel()
+    r = max(2, min(8, math.ceil(3 * l2 / per_set) + 1))
+    if page_size:
+        npg = w.N // page_size
+        perm = torch.from_numpy(np.random.default_rng(w.seed).permutation(w.B * npg))
+
+        def pool(x):  # page i of the cache stored at pool slot perm[i] (rearranged as raw bytes)
+            x = x.view(torch.uint8)
+            pg = x.reshape(w.B, w.Hkv, npg, page_size, w.D).permute(0, 2, 1, 3, 4).reshape(
+                w.B * npg, w.Hkv, page_size, w.D)
+            out = torch.empty_like(pg)
+            out[perm] = pg
+            return out.view(torch.float8_e4m3fn)
+
+        k, v = pool(k), pool(v)
+        td = perm.reshape(w.B, npg).to(torch.int32).to(dev)
+        lens = torch.full((w.B,), w.N, dtype=torch.int32, device=dev)
+        nb = sa.attn_decode_paged_workspace_bytes(w.B, w.Hq, w.Hkv, w.M, w.D, page_size, npg, w.N, w.causal,
+                                                  w.window)
+    else:
+        nb = sa.attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.M, w.N, w.D, w.causal, w.window, sa.PATH_DECODE)
+    ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
+    sets = [(q.to(dev), k.to(dev), v.to(dev), torch.empty(q.shape, dtype=torch.bfloat16, device=dev))
+            for _ in range(r)]
+
+    def fn_on(t, st):
+        if page_size:
+            sa.attn_decode_paged_fp8(t[0], t[1], t[2], td, lens, t[3], w.N, w.causal, w.window, 0.0, 1.0, 1.0,
+                                     1.0, ws, st)
+        else:
+            sa.attn_fwd_fp8(t[0], t[1], t[2], t[3], None, w.causal, w.window, 0.0, 1.0, 1.0, 1.0, sa.PATH_DECODE,
+                            ws, st)
+
+    ms = time_steady(fn_on, sets, steps, 3, stream)
+    cold = statistics.median(time_graph(lambda st: fn_on(sets[0], st), steps, 3, flush))
+    del sets
+    pk, pk_src = peaks()
+    gbs = decode_bytes(w, 1) / (ms * 1e-3) / 1e9
+    return {"GB/s": round(gbs, 1), "us": round(ms * 1e3, 2), "cold_call_us": round(cold * 1e3, 2),
+            "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4), "peak_source": pk_src,
+            "bytes": "E4M3 Q, K, V (1 byte each) + BF16 O",
+            "path": (f"paged decode, {page_size}-key pages, shuffled pool" if page_size else "decode") + ", E4M3"}
 
 
 def backward_measure(w, causal, steps, dev, stream):

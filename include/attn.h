@@ -143,19 +143,25 @@ ATTN_API int attn_fwd_lse(const void* q, const void* k, const void* v, void* o, 
  * of P is the one approximation beyond FP32 accumulation: each output
  * element's error is at most 2^-4 times the weighted mean of |V| over its row
  * (plus 2^-10 / l per key for probabilities below E4M3's normal range).
- * An FP8 extension of the tcgen05 prefill kernel: the pages use 16-bit inputs
- * only.
+ * An FP8 extension of the tcgen05 kernels: the pages use 16-bit inputs only.
  *   q: device bytes [B, Hq, M, D]; k, v: device bytes [B, Hkv, N, D]; o: device
  *   [B, Hq, M, D] of out_dtype (ATTN_BF16 / ATTN_FP16, else ATTN_ERR_DTYPE); all
  *   16-byte aligned. lse: as attn_fwd_lse (of the dequantized logits), or NULL.
  *   D must be 128 (ATTN_ERR_HEADDIM). Descale factors must be finite (not
- *   checked). M == 0: nothing is written; N == 0: o is zero-filled (and lse
- *   set to -inf). Needs no workspace. */
+ *   checked).
+ *   path: ATTN_PATH_AUTO (split-KV decode when (Hq/Hkv) * M <= 16 and the
+ *   visible key range spans at least 512 keys, else prefill), ATTN_PATH_PREFILL,
+ *   or ATTN_PATH_DECODE ((Hq/Hkv) * M <= 16, else ATTN_ERR_PATH); ATTN_PATH_SIMT
+ *   is not offered (ATTN_ERR_PATH).
+ *   workspace: for the decode path, attn_workspace_bytes(...) bytes of the same
+ *   problem and path (the split plan is the 16-bit one), 16-byte aligned, or
+ *   NULL to have it allocated stream-ordered; the prefill path needs none.
+ *   M == 0: nothing is written; N == 0: o is zero-filled (and lse set to -inf). */
 ATTN_API int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
                           int B, int Hq, int Hkv, int M, int N, int D,
                           int causal, int window, float scale,
                           float q_descale, float k_descale, float v_descale,
-                          int out_dtype, void* stream);
+                          int out_dtype, int path, void* workspace, size_t ws_bytes, void* stream);
 
 /* Backward pass: gradients of L = sum(dO * O) for O = attention(Q, K, V).
  * Each row of the weight gradient is the softmax vector-Jacobian product of
@@ -279,6 +285,20 @@ ATTN_API int attn_decode_paged(const void* q, const void* k_pages, const void* v
                                int num_pages, int page_size, int max_pages, int max_seq_len,
                                int causal, int window, float scale, int dtype,
                                void* workspace, size_t ws_bytes, void* stream);
+
+/* attn_decode_paged on an E4M3 cache: q and both pools hold E4M3 bytes (the
+ * encoding of attn_fwd_fp8) with per-tensor dequantization factors, and the
+ * operation is attn_decode_paged of the dequantized tensors, written as
+ * out_dtype (ATTN_BF16 / ATTN_FP16). The probabilities are rounded to E4M3
+ * for the value product as in attn_fwd_fp8. Arguments, limits and workspace
+ * (attn_decode_paged_workspace_bytes) as attn_decode_paged. */
+ATTN_API int attn_decode_paged_fp8(const void* q, const void* k_pages, const void* v_pages,
+                                   const int* block_table, const int* seq_lens, void* o,
+                                   int B, int Hq, int Hkv, int M, int D, int num_pages,
+                                   int page_size, int max_pages, int max_seq_len,
+                                   int causal, int window, float scale,
+                                   float q_descale, float k_descale, float v_descale, int out_dtype,
+                                   void* workspace, size_t ws_bytes, void* stream);
 
 /* Wide-row split softmax, the course's workshop A2 ("Intermediate and advanced
  * kernel workshops": three ordered kernels with per-call scratch; answer key,

@@ -20,6 +20,7 @@ from .binding import (  # noqa: F401
     attn_bwd,
     attn_bwd_workspace_bytes,
     attn_decode_paged,
+    attn_decode_paged_fp8,
     attn_decode_paged_workspace_bytes,
     attn_fwd,
     attn_fwd_decode_noalloc,

@@ -66,9 +66,11 @@ def lib() -> ctypes.CDLL:
             L.attn_decode_paged_workspace_bytes.restype = sz
             L.attn_decode_paged.argtypes = [vp] * 6 + [ci] * 11 + [cf, ci, vp, sz, vp]
             L.attn_decode_paged.restype = ci
+            L.attn_decode_paged_fp8.argtypes = [vp] * 6 + [ci] * 11 + [cf] * 4 + [ci, vp, sz, vp]
+            L.attn_decode_paged_fp8.restype = ci
             L.attn_fwd_lse.argtypes = [vp] * 5 + [ci] * 8 + [cf, ci, ci, vp, sz, vp]
             L.attn_fwd_lse.restype = ci
-            L.attn_fwd_fp8.argtypes = [vp] * 5 + [ci] * 8 + [cf, cf, cf, cf, ci, vp]
+            L.attn_fwd_fp8.argtypes = [vp] * 5 + [ci] * 8 + [cf, cf, cf, cf, ci, ci, vp, sz, vp]
             L.attn_fwd_fp8.restype = ci
             L.attn_bwd_workspace_bytes.argtypes = [ci, ci, ci]
             L.attn_bwd_workspace_bytes.restype = sz
@@ -175,10 +177,11 @@ def attention_lse(q, k, v, causal=False, window=0, scale=0.0, path=PATH_AUTO, st
 
 
 def attn_fwd_fp8(q, k, v, o, lse=None, causal=False, window=0, scale=0.0, q_descale=1.0, k_descale=1.0,
-                 v_descale=1.0, stream=None) -> None:
+                 v_descale=1.0, path=PATH_AUTO, workspace=None, stream=None) -> None:
     """C-ABI ``attn_fwd_fp8``: q, k, v are E4M3 (``torch.float8_e4m3fn``) device
     tensors, ``o`` BF16 or FP16 of q's shape, ``lse`` an optional float32
-    [B, Hq, M] tensor."""
+    [B, Hq, M] tensor; ``workspace`` None lets the library allocate the decode
+    path's workspace."""
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("q, k, v must be 4-D: [B, Hq, M, D] and [B, Hkv, N, D]")
     B, Hq, M, D = q.shape
@@ -192,18 +195,20 @@ def attn_fwd_fp8(q, k, v, o, lse=None, causal=False, window=0, scale=0.0, q_desc
         raise ValueError("o must be a contiguous bfloat16 or float16 tensor")
     if lse is not None and (lse.shape != (B, Hq, M) or lse.dtype != torch.float32 or not lse.is_contiguous()):
         raise ValueError("lse must be a contiguous float32 [B, Hq, M] tensor")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = lib().attn_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, M, N, D,
                             int(bool(causal)), int(window), float(scale or 0.0), float(q_descale),
-                            float(k_descale), float(v_descale), _DTYPES[o.dtype], _stream(stream))
+                            float(k_descale), float(v_descale), _DTYPES[o.dtype], int(path), _ptr(workspace),
+                            ws_bytes, _stream(stream))
     _check(st, "attn_fwd_fp8")
 
 
 def attention_fp8(q, k, v, causal=False, window=0, scale=0.0, q_descale=1.0, k_descale=1.0, v_descale=1.0,
-                  out_dtype=torch.bfloat16, with_lse=False, stream=None):
+                  out_dtype=torch.bfloat16, with_lse=False, path=PATH_AUTO, stream=None):
     """New output tensor (and log-sum-exp when ``with_lse``), then ``attn_fwd_fp8`` into it."""
     o = torch.empty(q.shape, dtype=out_dtype, device=q.device)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device) if with_lse else None
-    attn_fwd_fp8(q, k, v, o, lse, causal, window, scale, q_descale, k_descale, v_descale, stream)
+    attn_fwd_fp8(q, k, v, o, lse, causal, window, scale, q_descale, k_descale, v_descale, path, None, stream)
     return (o, lse) if with_lse else o
 
 
@@ -273,7 +278,7 @@ def attn_fwd_decode_noalloc(q, k, v, o, causal=False, window=0, scale=0.0, strea
     _check(st, "attn_fwd_decode_noalloc")
 
 
-def _paged_dims(q, k_pages, v_pages, block_table, seq_lens, o):
+def _paged_dims(q, k_pages, v_pages, block_table, seq_lens, o, e4m3=False):
     if q.dim() != 4 or k_pages.dim() != 4 or tuple(v_pages.shape) != tuple(k_pages.shape):
         raise ValueError("q is [B, Hq, M, D]; k_pages and v_pages are [num_pages, Hkv, page_size, D]")
     B, Hq, M, D = q.shape
@@ -287,10 +292,16 @@ def _paged_dims(q, k_pages, v_pages, block_table, seq_lens, o):
     for t in (q, k_pages, v_pages, block_table, seq_lens) + ((o,) if o is not None else ()):
         if not t.is_contiguous():
             raise ValueError("tensors must be contiguous")
-    if k_pages.dtype != q.dtype or v_pages.dtype != q.dtype or (o is not None and o.dtype != q.dtype):
-        raise ValueError("q, k_pages, v_pages, o must share one dtype")
-    if q.dtype not in (torch.bfloat16, torch.float16):
-        raise ValueError("dtype must be bfloat16 or float16")
+    if e4m3:
+        if any(t.dtype != torch.float8_e4m3fn for t in (q, k_pages, v_pages)):
+            raise ValueError("q, k_pages, v_pages must be float8_e4m3fn")
+        if o.dtype not in (torch.bfloat16, torch.float16):
+            raise ValueError("o must be bfloat16 or float16")
+    else:
+        if k_pages.dtype != q.dtype or v_pages.dtype != q.dtype or (o is not None and o.dtype != q.dtype):
+            raise ValueError("q, k_pages, v_pages, o must share one dtype")
+        if q.dtype not in (torch.bfloat16, torch.float16):
+            raise ValueError("dtype must be bfloat16 or float16")
     return B, Hq, Hkv, M, D, num_pages, page_size, block_table.shape[1]
 
 
@@ -311,6 +322,22 @@ def attn_decode_paged(q, k_pages, v_pages, block_table, seq_lens, o, max_seq_len
                                  int(bool(causal)), int(window), float(scale or 0.0), _DTYPES[q.dtype],
                                  _ptr(workspace), ws_bytes, _stream(stream))
     _check(st, "attn_decode_paged")
+
+
+def attn_decode_paged_fp8(q, k_pages, v_pages, block_table, seq_lens, o, max_seq_len, causal=True, window=0,
+                          scale=0.0, q_descale=1.0, k_descale=1.0, v_descale=1.0, workspace=None,
+                          stream=None) -> None:
+    """C-ABI ``attn_decode_paged_fp8``: q and the pools are float8_e4m3fn, ``o``
+    BF16 or FP16; writes ``o`` in place."""
+    B, Hq, Hkv, M, D, num_pages, page_size, max_pages = _paged_dims(q, k_pages, v_pages, block_table, seq_lens, o,
+                                                                     e4m3=True)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().attn_decode_paged_fp8(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table), _ptr(seq_lens),
+                                     _ptr(o), B, Hq, Hkv, M, D, num_pages, page_size, max_pages, int(max_seq_len),
+                                     int(bool(causal)), int(window), float(scale or 0.0), float(q_descale),
+                                     float(k_descale), float(v_descale), _DTYPES[o.dtype], _ptr(workspace),
+                                     ws_bytes, _stream(stream))
+    _check(st, "attn_decode_paged_fp8")
 
 
 def attn_split_softmax_workspace_bytes(M, N, chunk=1024) -> int:

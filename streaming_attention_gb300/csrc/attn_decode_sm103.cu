@@ -30,25 +30,34 @@ using namespace ptx;
 constexpr int DBN = 128;  // keys per tile (MMA M of the score product)
 constexpr int DNR = 16;   // grouped rows, padded (MMA N)
 constexpr int DD = 128;   // head dimension (MMA M of the value product)
-constexpr int kSlots = 3;
 constexpr int kDecThreads = 192;  // warps 0-3 softmax, 4 TMA, 5 MMA
 constexpr int kDecLoadWarp = 4, kDecMmaWarp = 5;
 constexpr uint64_t kDecTimeoutNs = 1000000000ull;
 constexpr float kDecRescale = 8.0f;
 
-constexpr int kTileBytes = DBN * DD * 2;    // 32 KB (K or V tile)
-constexpr int kChunkBytes = DBN * 128;      // 64 columns of a 128-row tile
-constexpr int kQBytes = DNR * DD * 2;       // 4 KB
-constexpr int kQChunk = DNR * 128;          // 2 KB
-constexpr int kOffQ = 0;
-constexpr int kOffP = kOffQ + kQBytes;            // two P^T buffers, 4 KB each
-constexpr int kOffRing = 12288;                   // 1024-aligned
-constexpr int kOffBar = kOffRing + kSlots * kTileBytes;
-constexpr int kNumBars = 1 + 2 * kSlots + 2 + 2 + 2 + 1 + 2 + 1;
-constexpr int kOffRed = kOffBar + 8 * kNumBars;   // float [2][4][16] tile maxima
-constexpr int kOffLRed = kOffRed + 2 * 4 * DNR * 4;  // float [4][16] row sums
-constexpr int kOffMisc = kOffLRed + 4 * DNR * 4;
-constexpr int kDecSmem = kOffMisc + 16 + 1024;
+constexpr int kChunkBytes = DBN * 128;  // one 128-byte column chunk of a 128-row tile
+constexpr int kQChunk = DNR * 128;      // one 128-byte column chunk of the 16-row Q or P^T tile
+
+// Shared-memory plan for EB-byte inputs (2: BF16/FP16, 1: E4M3). The ring keeps
+// about 96 KB of K/V in flight per CTA either way (3 slots of 32 KB, 6 of 16 KB).
+template <int EB>
+struct DCfg {
+    static constexpr int kSlots = EB == 1 ? 6 : 3;
+    static constexpr int kTileBytes = DBN * DD * EB;  // K or V tile
+    static constexpr int kChunks = DD * EB / 128;     // column chunks of a row
+    static constexpr int kChunkElems = 128 / EB;      // elements of D per chunk
+    static constexpr int kQBytes = DNR * DD * EB;
+    static constexpr int kPBytes = DNR * DBN * EB;    // one P^T buffer
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffP = kOffQ + kQBytes;     // two P^T buffers
+    static constexpr int kOffRing = 12288;            // 1024-aligned
+    static constexpr int kOffBar = kOffRing + kSlots * kTileBytes;
+    static constexpr int kNumBars = 1 + 2 * kSlots + 2 + 2 + 2 + 1 + 2 + 1;
+    static constexpr int kOffRed = kOffBar + 8 * kNumBars;  // float [2][4][16] tile maxima
+    static constexpr int kOffLRed = kOffRed + 2 * 4 * DNR * 4;  // float [4][16] row sums
+    static constexpr int kOffMisc = kOffLRed + 4 * DNR * 4;
+    static constexpr int kSmem = kOffMisc + 16 + 1024;
+};
 
 // TMEM columns: S^T buffers at 0 and 16, O^T at 32
 constexpr uint32_t kTmemCols = 64;
@@ -132,17 +141,22 @@ __device__ __forceinline__ void ring_item(int u, int T, bool* is_v, int* tile) {
 __device__ __forceinline__ int ring_pos_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
 __device__ __forceinline__ int ring_pos_v(int j, int T) { return j == T - 1 ? 2 * T - 1 : 2 * j + 2; }
 
+// EB: bytes per input element (2: BF16 or FP16 by kBF16; 1: E4M3, both products
+// kind::f8f6f4 and P^T rounded to E4M3).
 // RP: grouped rows handled by the softmax (R <= RP <= 16); the MMA always uses N = 16.
 // kPaged: K/V come from a paged pool through a block table, with a length per sequence.
-template <bool kBF16, int RP, bool kPaged>
+template <int EB, bool kBF16, int RP, bool kPaged>
 __global__ void __launch_bounds__(kDecThreads)
     attn_decode_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
+    using C = DCfg<EB>;
+    constexpr int kSlots = C::kSlots;
+    constexpr int kTileBytes = C::kTileBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t sQ = sbase + kOffQ, sP = sbase + kOffP, sRing = sbase + kOffRing;
-    const uint32_t bar_q = sbase + kOffBar;
+    const uint32_t sQ = sbase + C::kOffQ, sP = sbase + C::kOffP, sRing = sbase + C::kOffRing;
+    const uint32_t bar_q = sbase + C::kOffBar;
     const uint32_t bar_full0 = bar_q + 8, bar_empty0 = bar_full0 + 8 * kSlots;
     // one P-ready barrier per P^T buffer: the MMA issues S_{j+1} before PV_j, so the
     // softmax may finish tile j+1 before the MMA observes tile j; per-buffer phases
@@ -150,9 +164,9 @@ __global__ void __launch_bounds__(kDecThreads)
     const uint32_t bar_s0 = bar_empty0 + 8 * kSlots, bar_p0 = bar_s0 + 16, bar_free0 = bar_p0 + 16;
     const uint32_t bar_o = bar_free0 + 16;
     const uint32_t bar_red0 = bar_o + 8, bar_lred = bar_red0 + 16;  // shared-memory exchanges of the softmax
-    float* red = reinterpret_cast<float*>(smem + kOffRed);
-    float* lred = reinterpret_cast<float*>(smem + kOffLRed);
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc);
+    float* red = reinterpret_cast<float*>(smem + C::kOffRed);
+    float* lred = reinterpret_cast<float*>(smem + C::kOffLRed);
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc);
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -181,8 +195,8 @@ __global__ void __launch_bounds__(kDecThreads)
         fence_mbar_init();
     }
     // P^T buffers start at zero (rows >= R are never written afterwards)
-    for (int x = threadIdx.x; x < 2 * kQBytes / 16; x += blockDim.x)
-        reinterpret_cast<uint4*>(smem + kOffP)[x] = make_uint4(0, 0, 0, 0);
+    for (int x = threadIdx.x; x < 2 * C::kPBytes / 16; x += blockDim.x)
+        reinterpret_cast<uint4*>(smem + C::kOffP)[x] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (warp == kDecMmaWarp) {
         tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
@@ -220,8 +234,9 @@ __global__ void __launch_bounds__(kDecThreads)
             prefetch_tmap(&tmQ);
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
-            mbar_arrive_expect_tx(bar_q, kQBytes);
-            for (int c = 0; c < 2; ++c) tma_load_3d(sQ + c * kQChunk, &tmQ, c * 64, row_base, 0, bar_q);
+            mbar_arrive_expect_tx(bar_q, C::kQBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_load_3d(sQ + c * kQChunk, &tmQ, c * C::kChunkElems, row_base, 0, bar_q);
             int issued = 0;
             for (int u = 0; u < 2 * T; ++u) {
                 const int s = u % kSlots;
@@ -232,9 +247,9 @@ __global__ void __launch_bounds__(kDecThreads)
                 ring_item(u, T, &is_v, &tile);
                 mbar_arrive_expect_tx(bar_full0 + 8 * s, kTileBytes);
                 const CUtensorMap* tm = is_v ? &tmV : &tmK;
-                for (int c = 0; c < 2; ++c)
-                    tma_load_3d(sRing + s * kTileBytes + c * kChunkBytes, tm, c * 64, k0 + tile * DBN, grp,
-                                bar_full0 + 8 * s);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d(sRing + s * kTileBytes + c * kChunkBytes, tm, c * C::kChunkElems, k0 + tile * DBN,
+                                grp, bar_full0 + 8 * s);
                 issued = u + 1;
             }
             dwait_one(bar_q, 0, abort_flag, p.status, false);
@@ -251,8 +266,9 @@ __global__ void __launch_bounds__(kDecThreads)
                 prefetch_tmap(&tmQ);
                 prefetch_tmap(&tmK);
                 prefetch_tmap(&tmV);
-                mbar_arrive_expect_tx(bar_q, kQBytes);
-                for (int c = 0; c < 2; ++c) tma_load_3d(sQ + c * kQChunk, &tmQ, c * 64, row_base, 0, bar_q);
+                mbar_arrive_expect_tx(bar_q, C::kQBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d(sQ + c * kQChunk, &tmQ, c * C::kChunkElems, row_base, 0, bar_q);
             }
             const int sub = min(p.page_size, DBN), nsub = DBN / sub;
             const int npages = p.oob_z / p.Hkv;
@@ -290,8 +306,8 @@ __global__ void __launch_bounds__(kDecThreads)
                     const int y = in ? key % p.page_size : 0;
                     const int z = in ? page * p.Hkv + g : p.oob_z;
                     const uint32_t dst = sRing + s * kTileBytes + lane * sub * 128;
-                    for (int c = 0; c < 2; ++c)
-                        tma_load_3d(dst + c * kChunkBytes, tm, c * 64, y, z, bar_full0 + 8 * s);
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d(dst + c * kChunkBytes, tm, c * C::kChunkElems, y, z, bar_full0 + 8 * s);
                 }
                 issued = u + 1;
             }
@@ -303,17 +319,23 @@ __global__ void __launch_bounds__(kDecThreads)
         }
     } else if (warp == kDecMmaWarp) {
         if (lane == 0 && T > 0) {
-            constexpr uint32_t idS = idesc_f16(kBF16, DBN, DNR, false, false);
-            constexpr uint32_t idPV = idesc_f16(kBF16, DD, DNR, false, true);
+            constexpr uint32_t idS =
+                EB == 1 ? idesc_e4m3(DBN, DNR, false, false) : idesc_f16(kBF16, DBN, DNR, false, false);
+            constexpr uint32_t idPV =
+                EB == 1 ? idesc_e4m3(DD, DNR, false, true) : idesc_f16(kBF16, DD, DNR, false, true);
             auto issue_s = [&](int j) {
                 const int u = ring_pos_k(j), s = u % kSlots;
                 if (!dwait_one(bar_full0 + 8 * s, (u / kSlots) & 1, abort_flag, p.status)) return false;
                 tc_fence_after();
-                for (int kk = 0; kk < DD / 16; ++kk) {
+                // one K step covers 32 bytes of D: 16 elements of 16 bits, 32 of 8
+                for (int kk = 0; kk < DD * EB / 32; ++kk) {
                     const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
                     const uint64_t a = sw128_desc(sRing + s * kTileBytes + off, 16, 1024);
                     const uint64_t bq = sw128_desc(sQ + (kk >> 2) * kQChunk + (kk & 3) * 32, 16, 1024);
-                    mma_ss(tmem + dcol_s(j & 1), a, bq, idS, kk > 0 ? 1u : 0u);
+                    if constexpr (EB == 1)
+                        mma_ss_f8(tmem + dcol_s(j & 1), a, bq, idS, kk > 0 ? 1u : 0u);
+                    else
+                        mma_ss(tmem + dcol_s(j & 1), a, bq, idS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(bar_s0 + 8 * (j & 1));
                 mma_commit(bar_empty0 + 8 * s);
@@ -324,11 +346,16 @@ __global__ void __launch_bounds__(kDecThreads)
                 if (!dwait_one(bar_full0 + 8 * s, (u / kSlots) & 1, abort_flag, p.status)) return false;
                 if (!dwait_one(bar_p0 + 8 * (j & 1), (j >> 1) & 1, abort_flag, p.status)) return false;
                 tc_fence_after();
-                for (int kk = 0; kk < DBN / 16; ++kk) {
-                    const uint64_t a = sw128_desc(sRing + s * kTileBytes + kk * 16 * 128, kChunkBytes, 1024);
-                    const uint64_t bp = sw128_desc(sP + (j & 1) * kQBytes + (kk >> 2) * kQChunk + (kk & 3) * 32, 16,
-                                                   1024);
-                    mma_ss(tmem + kColOT, a, bp, idPV, (j > 0 || kk > 0) ? 1u : 0u);
+                // one K step covers 32 / EB keys: that many 128-byte rows of V
+                for (int kk = 0; kk < DBN * EB / 32; ++kk) {
+                    const uint64_t a =
+                        sw128_desc(sRing + s * kTileBytes + kk * (32 / EB) * 128, kChunkBytes, 1024);
+                    const uint64_t bp = sw128_desc(sP + (j & 1) * C::kPBytes + (kk >> 2) * kQChunk + (kk & 3) * 32,
+                                                   16, 1024);
+                    if constexpr (EB == 1)
+                        mma_ss_f8(tmem + kColOT, a, bp, idPV, (j > 0 || kk > 0) ? 1u : 0u);
+                    else
+                        mma_ss(tmem + kColOT, a, bp, idPV, (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(bar_free0 + 8 * (j & 1));
                 mma_commit(bar_empty0 + 8 * s);
@@ -405,16 +432,22 @@ __global__ void __launch_bounds__(kDecThreads)
             // P^T buffer j&1 was last read by the value product of tile j-2
             if (j >= 2 && !(ok = dwait_warp(bar_free0 + 8 * (j & 1), ((j - 2) >> 1) & 1, abort_flag, p.status)))
                 break;
-            uint8_t* pbuf = smem + kOffP + (j & 1) * kQBytes;
-            const int kc = kl >> 6, k64 = kl & 63;
+            uint8_t* pbuf = smem + C::kOffP + (j & 1) * C::kPBytes;
 #pragma unroll
             for (int r = 0; r < RP; ++r) {
                 const float m_use = (m_ref[r] == -INFINITY) ? 0.f : m_ref[r];
                 const float pr = ex2(t[r] - m_use);
                 l_part[r] += pr;
-                const uint32_t pk = kBF16 ? pack_bf16(pr, 0.f) : pack_f16(pr, 0.f);
-                const int off = kc * kQChunk + r * 128 + ((((k64 >> 3) ^ (r & 7))) << 4) + (k64 & 7) * 2;
-                *reinterpret_cast<uint16_t*>(pbuf + off) = (uint16_t)(pk & 0xFFFFu);
+                // P^T row r, key kl, in the 128-byte swizzle: 16-byte granule g of row r sits at g ^ (r & 7)
+                if constexpr (EB == 1) {
+                    const int off = r * 128 + ((((kl >> 4) ^ (r & 7))) << 4) + (kl & 15);
+                    pbuf[off] = (uint8_t)(pack_e4m3x4(pr, 0.f, 0.f, 0.f) & 0xFFu);
+                } else {
+                    const int kc = kl >> 6, k64 = kl & 63;
+                    const uint32_t pk = kBF16 ? pack_bf16(pr, 0.f) : pack_f16(pr, 0.f);
+                    const int off = kc * kQChunk + r * 128 + ((((k64 >> 3) ^ (r & 7))) << 4) + (k64 & 7) * 2;
+                    *reinterpret_cast<uint16_t*>(pbuf + off) = (uint16_t)(pk & 0xFFFFu);
+                }
             }
             // lazy rescale of O^T (needs the value product of tile j-1 complete)
             if (need_any && j > 0) {
@@ -507,25 +540,25 @@ int sm_count() {
     return n;
 }
 
-template <bool kBF16, int RP, bool kPaged>
+template <int EB, bool kBF16, int RP, bool kPaged>
 cudaError_t launch_decode_t(const Problem& pr, const void* q, const void* k, const void* v, const PagedKV* kv,
                             int chunk, int S, const SplitWorkspace& ws, int* status, cudaStream_t stream) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(attn_decode_kernel<kBF16, RP, kPaged>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
+        attr_err = cudaFuncSetAttribute(attn_decode_kernel<EB, kBF16, RP, kPaged>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, DCfg<EB>::kSmem);
     });
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap tq, tk, tv;
-    if (!make_tensor_map(&tq, q, DD, pr.B * pr.Hq * pr.M, 1, DNR, kBF16)) return cudaErrorInvalidValue;
+    if (!make_tensor_map(&tq, q, DD, pr.B * pr.Hq * pr.M, 1, DNR, kBF16, EB)) return cudaErrorInvalidValue;
     if (kPaged) {
         const int box = kv->page_size < DBN ? kv->page_size : DBN;
-        if (!make_tensor_map(&tk, kv->k_pages, DD, kv->page_size, kv->num_pages * pr.Hkv, box, kBF16) ||
-            !make_tensor_map(&tv, kv->v_pages, DD, kv->page_size, kv->num_pages * pr.Hkv, box, kBF16))
+        if (!make_tensor_map(&tk, kv->k_pages, DD, kv->page_size, kv->num_pages * pr.Hkv, box, kBF16, EB) ||
+            !make_tensor_map(&tv, kv->v_pages, DD, kv->page_size, kv->num_pages * pr.Hkv, box, kBF16, EB))
             return cudaErrorInvalidValue;
-    } else if (!make_tensor_map(&tk, k, DD, pr.N, pr.B * pr.Hkv, DBN, kBF16) ||
-               !make_tensor_map(&tv, v, DD, pr.N, pr.B * pr.Hkv, DBN, kBF16)) {
+    } else if (!make_tensor_map(&tk, k, DD, pr.N, pr.B * pr.Hkv, DBN, kBF16, EB) ||
+               !make_tensor_map(&tv, v, DD, pr.N, pr.B * pr.Hkv, DBN, kBF16, EB)) {
         return cudaErrorInvalidValue;
     }
     DecodeParams dp = {};
@@ -560,27 +593,35 @@ cudaError_t launch_decode_t(const Problem& pr, const void* q, const void* k, con
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(S, pr.B * pr.Hkv);
     cfg.blockDim = dim3(kDecThreads);
-    cfg.dynamicSmemBytes = kDecSmem;
+    cfg.dynamicSmemBytes = DCfg<EB>::kSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_decode_kernel<kBF16, RP, kPaged>, tq, tk, tv, dp);
+    return cudaLaunchKernelEx(&cfg, attn_decode_kernel<EB, kBF16, RP, kPaged>, tq, tk, tv, dp);
 }
 
+// e4m3: 8-bit inputs (the problem's dtype is then the output type, which the
+// split kernel never writes)
 template <bool kPaged>
 cudaError_t launch_decode_any(const Problem& p, const void* q, const void* k, const void* v, const PagedKV* kv,
-                              int chunk, int S, const SplitWorkspace& ws, int* status, cudaStream_t stream) {
+                              int chunk, int S, const SplitWorkspace& ws, int* status, cudaStream_t stream,
+                              bool e4m3 = false) {
     const int R = p.G * p.M;
+    if (e4m3) {
+        if (R <= 4) return launch_decode_t<1, true, 4, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream);
+        if (R <= 8) return launch_decode_t<1, true, 8, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream);
+        return launch_decode_t<1, true, 16, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream);
+    }
     const bool bf = p.dtype == ATTN_BF16;
-    if (R <= 4) return bf ? launch_decode_t<true, 4, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream)
-                          : launch_decode_t<false, 4, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream);
-    if (R <= 8) return bf ? launch_decode_t<true, 8, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream)
-                          : launch_decode_t<false, 8, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream);
-    return bf ? launch_decode_t<true, 16, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream)
-              : launch_decode_t<false, 16, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream);
+    if (R <= 4) return bf ? launch_decode_t<2, true, 4, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream)
+                          : launch_decode_t<2, false, 4, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream);
+    if (R <= 8) return bf ? launch_decode_t<2, true, 8, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream)
+                          : launch_decode_t<2, false, 8, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream);
+    return bf ? launch_decode_t<2, true, 16, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream)
+              : launch_decode_t<2, false, 16, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream);
 }
 
 // Splits of `tiles` key tiles over `groups` KV groups: every CTA resident at
@@ -629,8 +670,13 @@ int decode_plan_paged(const Problem& p, const PagedKV& kv, int* chunk, int* S) {
 }
 
 cudaError_t launch_decode_paged(const Problem& p, const void* q, const PagedKV& kv, int chunk, int S,
-                                const SplitWorkspace& ws, int* status, cudaStream_t stream) {
-    return launch_decode_any<true>(p, q, nullptr, nullptr, &kv, chunk, S, ws, status, stream);
+                                const SplitWorkspace& ws, int* status, cudaStream_t stream, bool e4m3) {
+    return launch_decode_any<true>(p, q, nullptr, nullptr, &kv, chunk, S, ws, status, stream, e4m3);
+}
+
+cudaError_t launch_decode_e4m3(const Problem& p, const void* q, const void* k, const void* v, int chunk, int S,
+                               const SplitWorkspace& ws, int* status, cudaStream_t stream) {
+    return launch_decode_any<false>(p, q, k, v, nullptr, chunk, S, ws, status, stream, true);
 }
 
 }  // namespace attn

@@ -1,5 +1,8 @@
-// C ABI of the forward pass on E4M3 inputs: metadata validation, the empty
-// and key-less cases, and the tcgen05 prefill kernel in its 8-bit form.
+// C ABI of attention on E4M3 inputs: metadata validation, the empty and
+// key-less cases, the path choice, and the tcgen05 prefill and split-KV decode
+// kernels in their 8-bit forms (the decode's summaries merge with the V
+// dequantization factor applied). Paged decode on an E4M3 cache is in
+// attn_paged.cu.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -17,6 +20,29 @@ __global__ void fill_f32_kernel(float* x, int64_t n, float value) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// AUTO: the split-KV decode for few grouped rows over a long key range (the
+// rule of the 16-bit forward), else the prefill kernel
+int choose_fp8_path(const Problem& p, int path) {
+    if (path != ATTN_PATH_AUTO) return path;
+    if (decode_tc_supported(p) && (p.khi - p.klo) >= 512) return ATTN_PATH_DECODE;
+    return ATTN_PATH_PREFILL;
+}
+
+int run_decode(const Problem& p, const void* q, const void* k, const void* v, void* o, float v_descale, void* ws,
+               size_t ws_bytes, int* status, cudaStream_t s) {
+    int chunk = 0, S = 0;
+    decode_plan_tc(p, &chunk, &S);
+    const int rows = p.B * p.Hq * p.M;
+    if (!ws || ws_bytes < split_workspace_bytes(rows, S, p.D)) return ATTN_ERR_WORKSPACE;
+    if (!aligned16(ws)) return ATTN_ERR_ALIGN;
+    SplitWorkspace w = split_workspace(ws, rows, S, p.D);
+    if (launch_decode_e4m3(p, q, k, v, chunk, S, w, status, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    return cuda_status(
+        launch_merge(w.m, w.l, w.acc, o, nullptr, nullptr, p.lse, rows, S, p.D, p.dtype, 1.0f, true, s, v_descale));
+}
+
 }  // namespace
 }  // namespace attn
 
@@ -24,7 +50,9 @@ using namespace attn;
 
 extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                             int Hkv, int M, int N, int D, int causal, int window, float scale, float q_descale,
-                            float k_descale, float v_descale, int out_dtype, void* stream) {
+                            float k_descale, float v_descale, int out_dtype, int path, void* workspace,
+                            size_t ws_bytes, void* stream) {
+    if (path < ATTN_PATH_AUTO || path > ATTN_PATH_DECODE || path == ATTN_PATH_SIMT) return ATTN_ERR_PATH;
     Problem p;
     // the 16-bit validation covers sizes, GQA, element counts, pointers and
     // alignment; the element count of an 8-bit tensor is the same bound
@@ -33,6 +61,9 @@ extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o
     if (D != 128) return ATTN_ERR_HEADDIM;
     const int64_t rows = (int64_t)B * Hq * M;
     if (rows > 0 && lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_ALIGN;
+    path = choose_fp8_path(p, path);
+    if (path == ATTN_PATH_DECODE && !decode_tc_supported(p)) return ATTN_ERR_PATH;
+    if (path == ATTN_PATH_PREFILL && !prefill_supported(p)) return ATTN_ERR_PATH;
     if (rows == 0) return ATTN_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (N == 0) {  // no keys: output 0, log-sum-exp -inf
@@ -49,6 +80,14 @@ extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o
     p.lse = lse;
     // logits of the dequantized tensors: scale * q_descale * k_descale * <q, k>
     p.scale_log2 = (float)((double)p.scale * (double)q_descale * (double)k_descale * (double)kLog2e);
-    if (!prefill_supported(p)) return ATTN_ERR_PATH;
-    return launch_prefill_e4m3(p, q, k, v, o, status, v_descale, s);
+    if (path == ATTN_PATH_PREFILL) return launch_prefill_e4m3(p, q, k, v, o, status, v_descale, s);
+    if (workspace) return run_decode(p, q, k, v, o, v_descale, workspace, ws_bytes, status, s);
+    int chunk = 0, S = 0;
+    decode_plan_tc(p, &chunk, &S);
+    const size_t bytes = split_workspace_bytes(p.B * p.Hq * p.M, S, p.D);
+    void* ws = nullptr;
+    if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    rc = run_decode(p, q, k, v, o, v_descale, ws, bytes, status, s);
+    if (cudaFreeAsync(ws, s) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
+    return rc;
 }

@@ -52,7 +52,7 @@ cudaError_t launch_simt(const Problem& p, const void* q, const void* k, const vo
                         int chunk, int S, const SplitWorkspace* ws, cudaStream_t stream);
 cudaError_t launch_merge(const float* m, const float* l, const float* acc, void* o, float* m_out,
                          float* l_out, float* lse_out, int rows, int S, int D, int out_dtype, float unit,
-                         bool programmatic, cudaStream_t stream);
+                         bool programmatic, cudaStream_t stream, float out_scale = 1.0f);
 cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const void* v,
                           int chunk, int S, const SplitWorkspace& ws, int* status,
                           cudaStream_t stream);
@@ -75,8 +75,13 @@ struct PagedKV {
     int num_pages, page_size, max_pages, max_len;
 };
 int decode_plan_paged(const Problem& p, const PagedKV& kv, int* chunk, int* S);
+// e4m3: Q and the pools hold E4M3 bytes (p.scale_log2 then includes the Q and K
+// dequantization factors; the merge applies V's)
 cudaError_t launch_decode_paged(const Problem& p, const void* q, const PagedKV& kv, int chunk, int S,
-                                const SplitWorkspace& ws, int* status, cudaStream_t stream);
+                                const SplitWorkspace& ws, int* status, cudaStream_t stream, bool e4m3 = false);
+// The tcgen05 split kernel on contiguous E4M3 inputs (same plan as launch_decode_tc)
+cudaError_t launch_decode_e4m3(const Problem& p, const void* q, const void* k, const void* v, int chunk, int S,
+                               const SplitWorkspace& ws, int* status, cudaStream_t stream);
 
 // Backward pass (tcgen05, D in {64, 128}): the caller's tensors, device pointers.
 struct BwdArgs {

@@ -1,5 +1,6 @@
-// C ABI of split-KV decode over a paged KV cache: metadata validation, the
-// split plan, the tcgen05 split kernel in paged mode and the merge kernel.
+// C ABI of split-KV decode over a paged KV cache (16-bit or E4M3): metadata
+// validation, the split plan, the tcgen05 split kernel in paged mode and the
+// merge kernel.
 // Attention over a KV-cache slice is the decode step the course's plan names
 // next ("Kernel Notes & Checklist", section 3, the plan, week +3: sliding
 // window + GQA + KV-cache slice); pages of the cache are gathered by the TMA
@@ -80,7 +81,8 @@ size_t paged_workspace(const PagedCall& c) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
-int run_paged(const PagedCall& c, const void* q, void* o, void* ws, size_t ws_bytes, cudaStream_t stream) {
+int run_paged(const PagedCall& c, const void* q, void* o, void* ws, size_t ws_bytes, cudaStream_t stream,
+              bool e4m3 = false, float v_descale = 1.0f) {
     const Problem& p = c.p;
     int chunk = 0, S = 0;
     decode_plan_paged(p, c.kv, &chunk, &S);
@@ -90,9 +92,9 @@ int run_paged(const PagedCall& c, const void* q, void* o, void* ws, size_t ws_by
     int* status = device_status_ptr();
     if (!status) return ATTN_ERR_CUDA;
     SplitWorkspace w = split_workspace(ws, rows, S, p.D);
-    if (launch_decode_paged(p, q, c.kv, chunk, S, w, status, stream) != cudaSuccess) return ATTN_ERR_CUDA;
-    return cuda_status(
-        launch_merge(w.m, w.l, w.acc, o, nullptr, nullptr, nullptr, rows, S, p.D, p.dtype, 1.0f, true, stream));
+    if (launch_decode_paged(p, q, c.kv, chunk, S, w, status, stream, e4m3) != cudaSuccess) return ATTN_ERR_CUDA;
+    return cuda_status(launch_merge(w.m, w.l, w.acc, o, nullptr, nullptr, nullptr, rows, S, p.D, p.dtype, 1.0f, true,
+                                    stream, v_descale));
 }
 
 }  // namespace
@@ -131,6 +133,29 @@ int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages, c
     void* ws = nullptr;
     if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) return ATTN_ERR_CUDA;
     rc = run_paged(c, q, o, ws, bytes, s);
+    if (cudaFreeAsync(ws, s) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
+    return rc;
+}
+
+int attn_decode_paged_fp8(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
+                          const int* seq_lens, void* o, int B, int Hq, int Hkv, int M, int D, int num_pages,
+                          int page_size, int max_pages, int max_seq_len, int causal, int window, float scale,
+                          float q_descale, float k_descale, float v_descale, int out_dtype, void* workspace,
+                          size_t ws_bytes, void* stream) {
+    PagedCall c;
+    int rc = validate_paged(q, k_pages, v_pages, block_table, seq_lens, o, B, Hq, Hkv, M, D, num_pages, page_size,
+                            max_pages, max_seq_len, causal, window, scale, out_dtype, &c);
+    if (rc != ATTN_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((int64_t)B * Hq * M == 0) return ATTN_OK;
+    if (nothing_to_attend(c)) return cuda_status(cudaMemsetAsync(o, 0, (size_t)B * Hq * M * D * 2, s));
+    // logits of the dequantized tensors: scale * q_descale * k_descale * <q, k>
+    c.p.scale_log2 = (float)((double)c.p.scale * (double)q_descale * (double)k_descale * (double)kLog2e);
+    if (workspace) return run_paged(c, q, o, workspace, ws_bytes, s, true, v_descale);
+    const size_t bytes = paged_workspace(c);
+    void* ws = nullptr;
+    if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    rc = run_paged(c, q, o, ws, bytes, s, true, v_descale);
     if (cudaFreeAsync(ws, s) != cudaSuccess && rc == ATTN_OK) rc = ATTN_ERR_CUDA;
     return rc;
 }

@@ -171,13 +171,14 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) attn_simt_kernel(SimtArgs 
 // Merge of S summaries, one thread per output element (row, d): every load is
 // independent of the arithmetic, so the whole merge is one memory round trip.
 // unit converts the stored maxima to base 2 (1 for base-2 maxima, log2(e) for
-// natural-log maxima).
+// natural-log maxima); out_scale multiplies the merged output (a V
+// dequantization factor; 1 otherwise).
 constexpr int kMergeThreads = 256;
 
 __global__ void __launch_bounds__(kMergeThreads)
     attn_merge_kernel(const float* __restrict__ m, const float* __restrict__ l, const float* __restrict__ acc,
                       void* o, float* m_out, float* l_out, float* lse_out, int rows, int S, int D, int out_dtype,
-                      float unit, int programmatic) {
+                      float unit, int programmatic, float out_scale) {
     // A programmatically launched successor (the next decode split grid) may start
     // its setup now; it waits for this grid's completion before touching memory.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -202,7 +203,7 @@ __global__ void __launch_bounds__(kMergeThreads)
         L = fmaf(ws, lr[s], L);
         x = fmaf(ws, ar[(size_t)s * D], x);
     }
-    x *= L > 0.f ? 1.f / L : 0.f;
+    x *= L > 0.f ? out_scale / L : 0.f;
     const size_t out = row * D + d;
     if (out_dtype == ATTN_BF16)
         reinterpret_cast<__nv_bfloat16*>(o)[out] = __float2bfloat16_rn(x);
@@ -270,7 +271,7 @@ cudaError_t launch_simt(const Problem& p, const void* q, const void* k, const vo
 
 cudaError_t launch_merge(const float* m, const float* l, const float* acc, void* o, float* m_out, float* l_out,
                          float* lse_out, int rows, int S, int D, int out_dtype, float unit, bool programmatic,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, float out_scale) {
     if (rows == 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(((size_t)rows * D + kMergeThreads - 1) / kMergeThreads));
@@ -283,7 +284,7 @@ cudaError_t launch_merge(const float* m, const float* l, const float* acc, void*
     cfg.attrs = attr;
     cfg.numAttrs = programmatic ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, attn_merge_kernel, m, l, acc, o, m_out, l_out, lse_out, rows, S, D, out_dtype,
-                              unit, programmatic ? 1 : 0);
+                              unit, programmatic ? 1 : 0, out_scale);
 }
 
 }  // namespace attn

@@ -185,8 +185,9 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int M, int N, bool b
 
 // Instruction descriptor, kind::f8f6f4 with E4M3 A and B (format code 0) and
 // an FP32 accumulator; the other fields as for kind::f16.
-__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool b_mn_major) {
-    return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool b_mn_major, bool a_mn_major = false) {
+    return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // Makes this thread's generic-proxy shared-memory writes visible to the async

@@ -195,10 +195,13 @@ def test_selftest_rejects_bad_limits(L):
     (dict(q=A8), -7),
     (dict(lse=ctypes.c_void_p(0x10002)), -7),
     (dict(M=0), 0),                      # empty output: nothing to do, no launch
+    (dict(path=1), -11),                 # no SIMT form for 8-bit inputs
+    (dict(path=7), -11),
+    (dict(path=3, Hq=32, Hkv=1, M=1), -11),   # decode needs (Hq/Hkv) * M <= 16
 ])
 def test_fp8_validation_status(L, kw, status):
-    a = dict(q=A16, k=A16, v=A16, o=A16, lse=None, B_=1, Hq=2, Hkv=2, M=8, N=8, D=128, dtype=0)
+    a = dict(q=A16, k=A16, v=A16, o=A16, lse=None, B_=1, Hq=2, Hkv=2, M=8, N=8, D=128, dtype=0, path=0)
     a.update(kw)
     st = L.attn_fwd_fp8(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B_"], a["Hq"], a["Hkv"], a["M"], a["N"],
-                        a["D"], 1, 0, 0.0, 1.0, 1.0, 1.0, a["dtype"], None)
+                        a["D"], 1, 0, 0.0, 1.0, 1.0, 1.0, a["dtype"], a["path"], None, 0, None)
     assert st == status

@@ -90,3 +90,68 @@ def test_fp8_full_size_sampled_rows():
     got = o.reshape(-1, w.D)[torch.tensor(rows)].cpu()
     H, sigma, wabs = row_bounds(qf, kf, vf, rows, True, 0, 1.0 / np.sqrt(w.D))
     check_fp8(got, want, H, sigma, wabs, torch.bfloat16, "full size")
+
+
+# --------------------------------------------------------------------------
+# Split-KV decode on E4M3 inputs (contiguous and paged caches)
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("shape,causal,window,descale", [
+    ((2, 8, 2, 1, 1500, 128), True, 700, (1.0, 1.0, 1.0)),
+    ((1, 32, 8, 1, 8192, 128), True, 0, (0.5, 0.25, 2.0)),
+    ((1, 4, 1, 3, 777, 128), True, 0, (1.0, 1.0, 1.0)),      # speculative rows: G * M = 12
+    ((3, 16, 1, 1, 2049, 128), False, 0, (1.0, 0.5, 1.0)),   # G = 16, ragged N
+])
+@pytest.mark.parametrize("path", [sa.PATH_AUTO, sa.PATH_DECODE, sa.PATH_PREFILL],
+                         ids=["auto", "decode", "prefill"])
+def test_fp8_decode_shapes(shape, causal, window, descale, path):
+    B, Hq, Hkv, M, N, D = shape
+    qd, kd, vd = descale
+    q, k, v = make_qkv_fp8(B, Hq, Hkv, M, N, D, 24, qd, kd, vd)
+    o, lse = sa.attention_fp8(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, window=window, q_descale=qd,
+                              k_descale=kd, v_descale=vd, with_lse=True, path=path)
+    torch.cuda.synchronize()
+    want, want_lse = oracle.attention_fp8(q, k, v, qd, kd, vd, causal=causal, window=window, with_lse=True)
+    H, sigma, wabs = bounds(deq(q, qd), deq(k, kd), deq(v, vd), causal, window, 1.0 / np.sqrt(D))
+    check_fp8(o, want, H, sigma, wabs, torch.bfloat16, f"{shape} path={path}")
+    assert np.abs(lse.cpu().double().numpy() - want_lse).max() <= 2e-3
+
+
+def test_fp8_decode_workload_full_size():
+    """The GQA decode shape (B=8, Hq=32, Hkv=8, M=1, N=8192, window 4096) in E4M3,
+    every row, with a caller workspace."""
+    from streaming_attention_gb300.inputs import DECODE_GQA as w
+    q, k, v = make_qkv_fp8(w.B, w.Hq, w.Hkv, w.M, w.N, w.D, 25)
+    nb = sa.attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.M, w.N, w.D, True, w.window, sa.PATH_DECODE)
+    ws = torch.empty(nb, dtype=torch.uint8, device=DEV)
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=DEV)
+    sa.attn_fwd_fp8(q.to(DEV), k.to(DEV), v.to(DEV), o, None, True, w.window, path=sa.PATH_DECODE, workspace=ws)
+    torch.cuda.synchronize()
+    want = oracle.attention_fp8(q, k, v, causal=True, window=w.window)
+    H, sigma, wabs = bounds(deq(q, 1.0), deq(k, 1.0), deq(v, 1.0), True, w.window, 1.0 / np.sqrt(w.D))
+    check_fp8(o, want, H, sigma, wabs, torch.bfloat16, "decode workload")
+
+
+@pytest.mark.parametrize("page_size", [16, 64, 128, 256])
+def test_fp8_paged_ragged_lengths(page_size):
+    from oracle_pins import to_pages
+    B, Hq, Hkv, M, Ncap, D = 4, 8, 2, 2, 1024, 128
+    qd, kd, vd = 0.5, 1.0, 2.0
+    q, k, v = make_qkv_fp8(B, Hq, Hkv, M, Ncap, D, 26, qd, kd, vd)
+    rng = np.random.default_rng(5)
+    kp, table = to_pages(k.float().numpy(), page_size, rng)
+    rng = np.random.default_rng(5)
+    vp, _ = to_pages(v.float().numpy(), page_size, rng)
+    f8 = torch.float8_e4m3fn
+    kp, vp = torch.from_numpy(kp).to(f8), torch.from_numpy(vp).to(f8)  # exact: the values came from E4M3
+    table = torch.from_numpy(table.astype(np.int32))
+    lens = [1000, 1, 1024, 517]
+    o = torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device=DEV)
+    sa.attn_decode_paged_fp8(q.to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV),
+                             torch.tensor(lens, dtype=torch.int32, device=DEV), o, Ncap, causal=True,
+                             q_descale=qd, k_descale=kd, v_descale=vd)
+    torch.cuda.synchronize()
+    want = oracle.attention_paged(deq(q, qd), deq(kp, kd), deq(vp, vd), table, lens, Ncap, True, 0)
+    qf, kf, vf = deq(q, qd), deq(k, kd), deq(v, vd)
+    for b, L in enumerate(lens):
+        H, sigma, wabs = bounds(qf[b:b + 1], kf[b:b + 1, :, :L], vf[b:b + 1, :, :L], True, 0, 1.0 / np.sqrt(D))
+        check_fp8(o[b:b + 1], want[b:b + 1], H, sigma, wabs, torch.bfloat16, f"page {page_size} seq {b}")
