@@ -543,10 +543,10 @@ def fp8_decode_measure(w, page_size, steps, dev, stream, flush):
         k, v = pool(k), pool(v)
         td = perm.reshape(w.B, npg).to(torch.int32).to(dev)
         lens = torch.full((w.B,), w.N, dtype=torch.int32, device=dev)
-        nb = sa.attn_decode_paged_workspace_bytes(w.B, w.Hq, w.Hkv, w.M, w.D, page_size, npg, w.N, w.causal,
-                                                  w.window)
+        nb = sa.attn_decode_paged_fp8_workspace_bytes(w.B, w.Hq, w.Hkv, w.M, w.D, page_size, npg, w.N, w.causal,
+                                                      w.window)
     else:
-        nb = sa.attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.M, w.N, w.D, w.causal, w.window, sa.PATH_DECODE)
+        nb = sa.attn_fwd_fp8_workspace_bytes(w.B, w.Hq, w.Hkv, w.M, w.N, w.D, w.causal, w.window, sa.PATH_DECODE)
     ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
     sets = [(q.to(dev), k.to(dev), v.to(dev), torch.empty(q.shape, dtype=torch.bfloat16, device=dev))
             for _ in range(r)]

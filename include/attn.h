@@ -153,10 +153,15 @@ ATTN_API int attn_fwd_lse(const void* q, const void* k, const void* v, void* o, 
  *   visible key range spans at least 512 keys, else prefill), ATTN_PATH_PREFILL,
  *   or ATTN_PATH_DECODE ((Hq/Hkv) * M <= 16, else ATTN_ERR_PATH); ATTN_PATH_SIMT
  *   is not offered (ATTN_ERR_PATH).
- *   workspace: for the decode path, attn_workspace_bytes(...) bytes of the same
- *   problem and path (the split plan is the 16-bit one), 16-byte aligned, or
- *   NULL to have it allocated stream-ordered; the prefill path needs none.
+ *   workspace: for the decode path, attn_fwd_fp8_workspace_bytes(...) bytes of
+ *   the same problem and path (the 8-bit kernel runs more splits than the
+ *   16-bit one), 16-byte aligned, or NULL to have it allocated stream-ordered;
+ *   the prefill path needs none.
  *   M == 0: nothing is written; N == 0: o is zero-filled (and lse set to -inf). */
+/* Bytes of caller workspace attn_fwd_fp8 needs for this problem on this path
+ * (0 for the prefill path, empty problems and invalid shapes). */
+ATTN_API size_t attn_fwd_fp8_workspace_bytes(int B, int Hq, int Hkv, int M, int N, int D,
+                                             int causal, int window, int path);
 ATTN_API int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
                           int B, int Hq, int Hkv, int M, int N, int D,
                           int causal, int window, float scale,
@@ -204,7 +209,12 @@ ATTN_API int attn_merge(const float* m, const float* l, const float* acc, void* 
 
 /* End-to-end call on HOST buffers: copies q, k, v from host memory into the
  * caller's device buffers, runs attn_fwd_ex with ATTN_PATH_AUTO, copies o back
- * to host memory, and synchronizes `stream` before returning.
+ * to host memory, and synchronizes `stream` before returning. On the prefill
+ * and SIMT paths the work is cut into up to 8 chunks of whole (batch, KV head)
+ * groups whose copies run on two internal copy streams, overlapping the
+ * kernels of other chunks on `stream` (the copies wait for the work already
+ * queued on `stream`); the decode path copies, computes and copies back in
+ * order on `stream`. Calls from several host threads are serialized.
  *   *_h: host pointers (pinned memory gives asynchronous copies);
  *   *_d: device buffers of the same sizes, owned by the caller;
  *   workspace/ws_bytes: as attn_fwd_ex (may be NULL/0 when none is needed).
@@ -290,8 +300,12 @@ ATTN_API int attn_decode_paged(const void* q, const void* k_pages, const void* v
  * encoding of attn_fwd_fp8) with per-tensor dequantization factors, and the
  * operation is attn_decode_paged of the dequantized tensors, written as
  * out_dtype (ATTN_BF16 / ATTN_FP16). The probabilities are rounded to E4M3
- * for the value product as in attn_fwd_fp8. Arguments, limits and workspace
- * (attn_decode_paged_workspace_bytes) as attn_decode_paged. */
+ * for the value product as in attn_fwd_fp8. Arguments and limits as
+ * attn_decode_paged; the workspace is attn_decode_paged_fp8_workspace_bytes(...)
+ * bytes (or NULL to have it allocated stream-ordered). */
+ATTN_API size_t attn_decode_paged_fp8_workspace_bytes(int B, int Hq, int Hkv, int M, int D,
+                                                      int page_size, int max_pages,
+                                                      int max_seq_len, int causal, int window);
 ATTN_API int attn_decode_paged_fp8(const void* q, const void* k_pages, const void* v_pages,
                                    const int* block_table, const int* seq_lens, void* o,
                                    int B, int Hq, int Hkv, int M, int D, int num_pages,

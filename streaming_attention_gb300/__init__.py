@@ -21,11 +21,13 @@ from .binding import (  # noqa: F401
     attn_bwd_workspace_bytes,
     attn_decode_paged,
     attn_decode_paged_fp8,
+    attn_decode_paged_fp8_workspace_bytes,
     attn_decode_paged_workspace_bytes,
     attn_fwd,
     attn_fwd_decode_noalloc,
     attn_fwd_ex,
     attn_fwd_fp8,
+    attn_fwd_fp8_workspace_bytes,
     attn_fwd_host,
     attn_fwd_lse,
     attn_merge,

@@ -72,6 +72,10 @@ def lib() -> ctypes.CDLL:
             L.attn_fwd_lse.restype = ci
             L.attn_fwd_fp8.argtypes = [vp] * 5 + [ci] * 8 + [cf, cf, cf, cf, ci, ci, vp, sz, vp]
             L.attn_fwd_fp8.restype = ci
+            L.attn_fwd_fp8_workspace_bytes.argtypes = [ci] * 9
+            L.attn_fwd_fp8_workspace_bytes.restype = sz
+            L.attn_decode_paged_fp8_workspace_bytes.argtypes = [ci] * 10
+            L.attn_decode_paged_fp8_workspace_bytes.restype = sz
             L.attn_bwd_workspace_bytes.argtypes = [ci, ci, ci]
             L.attn_bwd_workspace_bytes.restype = sz
             L.attn_bwd.argtypes = [vp] * 9 + [ci] * 8 + [cf, ci, vp, sz, vp]
@@ -174,6 +178,16 @@ def attention_lse(q, k, v, causal=False, window=0, scale=0.0, path=PATH_AUTO, st
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
     attn_fwd_lse(q, k, v, o, lse, causal, window, scale, path, None, stream)
     return o, lse
+
+
+def attn_fwd_fp8_workspace_bytes(B, Hq, Hkv, M, N, D, causal=False, window=0, path=PATH_AUTO) -> int:
+    return int(lib().attn_fwd_fp8_workspace_bytes(B, Hq, Hkv, M, N, D, int(bool(causal)), int(window), int(path)))
+
+
+def attn_decode_paged_fp8_workspace_bytes(B, Hq, Hkv, M, D, page_size, max_pages, max_seq_len, causal=True,
+                                          window=0) -> int:
+    return int(lib().attn_decode_paged_fp8_workspace_bytes(B, Hq, Hkv, M, D, page_size, max_pages, max_seq_len,
+                                                           int(bool(causal)), int(window)))
 
 
 def attn_fwd_fp8(q, k, v, o, lse=None, causal=False, window=0, scale=0.0, q_descale=1.0, k_descale=1.0,

@@ -4,6 +4,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "attn.h"
 #include "attn_internal.h"
 
@@ -124,6 +126,104 @@ int run(const Problem& p, const void* q, const void* k, const void* v, void* o, 
     }
 }
 
+// ---- host-buffer entry: copies and compute pipelined over chunks ----
+//
+// The problem is cut into chunks of whole (batch, KV head) groups, each a
+// smaller attention problem over contiguous slices of q, k, v and o. Chunk c's
+// host-to-device copies run on a copy stream, its kernel on the caller's
+// stream once they land, and its output copy on a second copy stream once the
+// kernel is done, so copies of one chunk overlap the compute and copies of
+// others. Streams and events are made once per device and reused; one host
+// call at a time uses them.
+constexpr int kHostChunks = 8;
+
+struct HostPipe {
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t start = nullptr, in[kHostChunks] = {}, done[kHostChunks] = {};
+    bool ready = false;
+};
+std::mutex g_host_mu;
+HostPipe g_host_pipe[kMaxDevices];
+
+HostPipe* host_pipe() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    HostPipe& hp = g_host_pipe[dev];
+    if (hp.ready) return &hp;
+    if (cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming) != cudaSuccess)
+        return nullptr;
+    for (int c = 0; c < kHostChunks; ++c)
+        if (cudaEventCreateWithFlags(&hp.in[c], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&hp.done[c], cudaEventDisableTiming) != cudaSuccess)
+            return nullptr;
+    hp.ready = true;
+    return &hp;
+}
+
+// One chunk: batches [b0, b0 + nb) and, within them, KV heads [g0, g0 + ng)
+// (either nb == 1 or all heads).
+struct HostChunk {
+    int b0, nb, g0, ng;
+};
+
+int host_chunks(const Problem& p, HostChunk* out) {
+    int n = 0;
+    if (p.B >= kHostChunks) {
+        const int per = (p.B + kHostChunks - 1) / kHostChunks;
+        for (int b = 0; b < p.B; b += per) out[n++] = HostChunk{b, per < p.B - b ? per : p.B - b, 0, p.Hkv};
+    } else {
+        int parts = kHostChunks / (p.B > 0 ? p.B : 1);
+        if (parts > p.Hkv) parts = p.Hkv;
+        const int per = (p.Hkv + parts - 1) / parts;
+        for (int b = 0; b < p.B; ++b)
+            for (int g = 0; g < p.Hkv; g += per) out[n++] = HostChunk{b, 1, g, per < p.Hkv - g ? per : p.Hkv - g};
+    }
+    return n;
+}
+
+int run_host_pipelined(const Problem& p, const char* q_h, const char* k_h, const char* v_h, char* o_h, char* q_d,
+                       char* k_d, char* v_d, char* o_d, int path, cudaStream_t s) {
+    std::lock_guard<std::mutex> lock(g_host_mu);
+    HostPipe* hp = host_pipe();
+    if (!hp) return ATTN_ERR_CUDA;
+    HostChunk ch[kHostChunks];
+    const int n = host_chunks(p, ch);
+    const size_t qrow = (size_t)p.M * p.D * 2, krow = (size_t)p.N * p.D * 2;  // bytes per head
+    // the copies into q_d, k_d, v_d wait for the work already queued on the stream
+    if (cudaEventRecord(hp->start, s) != cudaSuccess || cudaStreamWaitEvent(hp->h2d, hp->start, 0) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    int rc = ATTN_OK;
+    for (int c = 0; c < n && rc == ATTN_OK; ++c) {
+        const HostChunk& x = ch[c];
+        const size_t qoff = ((size_t)x.b0 * p.Hq + (size_t)x.g0 * p.G) * qrow;
+        const size_t koff = ((size_t)x.b0 * p.Hkv + x.g0) * krow;
+        const size_t qbytes = (size_t)x.nb * x.ng * p.G * qrow, kbytes = (size_t)x.nb * x.ng * krow;
+        if (cudaMemcpyAsync(q_d + qoff, q_h + qoff, qbytes, cudaMemcpyHostToDevice, hp->h2d) != cudaSuccess ||
+            cudaMemcpyAsync(k_d + koff, k_h + koff, kbytes, cudaMemcpyHostToDevice, hp->h2d) != cudaSuccess ||
+            cudaMemcpyAsync(v_d + koff, v_h + koff, kbytes, cudaMemcpyHostToDevice, hp->h2d) != cudaSuccess ||
+            cudaEventRecord(hp->in[c], hp->h2d) != cudaSuccess || cudaStreamWaitEvent(s, hp->in[c], 0) != cudaSuccess) {
+            rc = ATTN_ERR_CUDA;
+            break;
+        }
+        Problem sub;
+        rc = validate(q_d + qoff, k_d + koff, v_d + koff, o_d + qoff, x.nb, x.ng * p.G, x.ng, p.M, p.N, p.D, p.causal,
+                      p.window, p.scale, p.dtype, &sub);
+        if (rc == ATTN_OK) rc = run(sub, q_d + qoff, k_d + koff, v_d + koff, o_d + qoff, path, nullptr, 0, s);
+        if (rc != ATTN_OK) break;
+        if (cudaEventRecord(hp->done[c], s) != cudaSuccess || cudaStreamWaitEvent(hp->d2h, hp->done[c], 0) != cudaSuccess ||
+            cudaMemcpyAsync(o_h + qoff, o_d + qoff, qbytes, cudaMemcpyDeviceToHost, hp->d2h) != cudaSuccess)
+            rc = ATTN_ERR_CUDA;
+    }
+    // drain every stream the call used, whatever happened above
+    const cudaError_t e1 = cudaStreamSynchronize(hp->h2d);
+    const cudaError_t e2 = cudaStreamSynchronize(s);
+    const cudaError_t e3 = cudaStreamSynchronize(hp->d2h);
+    if (rc == ATTN_OK && (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess)) rc = ATTN_ERR_CUDA;
+    return rc;
+}
+
 }  // namespace
 
 int validate_problem(const void* q, const void* k, const void* v, const void* o, int B, int Hq, int Hkv, int M,
@@ -232,10 +332,16 @@ int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, 
     const size_t qb = (size_t)B * Hq * M * D * 2, kb = (size_t)B * Hkv * N * D * 2;
     if ((qb && (!q_h || !o_h)) || (kb && (!k_h || !v_h))) return ATTN_ERR_NULL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int path = choose_path(p, ATTN_PATH_AUTO);
+    // prefill and SIMT problems need no workspace, so their chunks run as
+    // independent problems with copies overlapping compute
+    if (path != ATTN_PATH_DECODE && qb > 0 && kb > 0 && p.B * p.Hkv > 1)
+        return run_host_pipelined(p, static_cast<const char*>(q_h), static_cast<const char*>(k_h),
+                                  static_cast<const char*>(v_h), static_cast<char*>(o_h), static_cast<char*>(q_d),
+                                  static_cast<char*>(k_d), static_cast<char*>(v_d), static_cast<char*>(o_d), path, s);
     if (qb && cudaMemcpyAsync(q_d, q_h, qb, cudaMemcpyHostToDevice, s) != cudaSuccess) return ATTN_ERR_CUDA;
     if (kb && cudaMemcpyAsync(k_d, k_h, kb, cudaMemcpyHostToDevice, s) != cudaSuccess) return ATTN_ERR_CUDA;
     if (kb && cudaMemcpyAsync(v_d, v_h, kb, cudaMemcpyHostToDevice, s) != cudaSuccess) return ATTN_ERR_CUDA;
-    const int path = choose_path(p, ATTN_PATH_AUTO);
     rc = run(p, q_d, k_d, v_d, o_d, path, workspace, ws_bytes, s);
     if (rc != ATTN_OK) return rc;
     if (qb && cudaMemcpyAsync(o_h, o_d, qb, cudaMemcpyDeviceToHost, s) != cudaSuccess) return ATTN_ERR_CUDA;

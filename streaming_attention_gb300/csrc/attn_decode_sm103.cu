@@ -39,7 +39,9 @@ constexpr int kChunkBytes = DBN * 128;  // one 128-byte column chunk of a 128-ro
 constexpr int kQChunk = DNR * 128;      // one 128-byte column chunk of the 16-row Q or P^T tile
 
 // Shared-memory plan for EB-byte inputs (2: BF16/FP16, 1: E4M3). The ring keeps
-// about 96 KB of K/V in flight per CTA either way (3 slots of 32 KB, 6 of 16 KB).
+// about 96 KB of K/V in flight per CTA either way (3 slots of 32 KB, 6 of 16 KB),
+// and two CTAs share an SM. (Three 8-bit CTAs per SM with 3 slots each, and
+// so more splits, measured slower: the extra merge work outweighed the gain.)
 template <int EB>
 struct DCfg {
     static constexpr int kSlots = EB == 1 ? 6 : 3;
@@ -625,9 +627,9 @@ cudaError_t launch_decode_any(const Problem& p, const void* q, const void* k, co
 }
 
 // Splits of `tiles` key tiles over `groups` KV groups: every CTA resident at
-// once when possible (two per SM), each streaming an equal run of tiles.
-void plan_splits(int tiles, int groups, int* chunk, int* S) {
-    const int slots = 2 * sm_count();
+// once when possible (per_sm per SM), each streaming an equal run of tiles.
+void plan_splits(int tiles, int groups, int* chunk, int* S, int per_sm) {
+    const int slots = per_sm * sm_count();
     int s = groups > 0 ? slots / groups : 1;
     if (s < 1) s = 1;
     if (s > tiles) s = tiles;
@@ -641,10 +643,18 @@ void plan_splits(int tiles, int groups, int* chunk, int* S) {
 
 bool decode_tc_supported(const Problem& p) { return p.D == DD && p.G * p.M <= DNR && p.B * p.Hkv <= 65535; }
 
-int decode_plan_tc(const Problem& p, int* chunk, int* S) {
+// CTAs resident per SM (two for both input widths; the plan keeps the 8-bit
+// switch so that its workspace query stays separate from the 16-bit one)
+int ctas_per_sm(const Problem& p, bool e4m3) {
+    (void)p;
+    (void)e4m3;
+    return 2;
+}
+
+int decode_plan_tc(const Problem& p, int* chunk, int* S, bool e4m3) {
     const int kbase = split_base(p);
     const int tiles = p.khi > kbase ? (p.khi - kbase + DBN - 1) / DBN : 1;
-    plan_splits(tiles, p.B * p.Hkv, chunk, S);
+    plan_splits(tiles, p.B * p.Hkv, chunk, S, ctas_per_sm(p, e4m3));
     return ATTN_OK;
 }
 
@@ -656,7 +666,7 @@ cudaError_t launch_decode_tc(const Problem& p, const void* q, const void* k, con
 // Paged: the plan must cover any sequence up to kv.max_len keys. Without a
 // window a sequence's range starts at key 0; with one it spans at most
 // window + M - 1 keys from an unaligned start.
-int decode_plan_paged(const Problem& p, const PagedKV& kv, int* chunk, int* S) {
+int decode_plan_paged(const Problem& p, const PagedKV& kv, int* chunk, int* S, bool e4m3) {
     const int len_tiles = (kv.max_len + DBN - 1) / DBN;
     int tiles = len_tiles;
     if (p.window > 0) {
@@ -665,7 +675,7 @@ int decode_plan_paged(const Problem& p, const PagedKV& kv, int* chunk, int* S) {
         if (wt < tiles) tiles = (int)wt;
     }
     if (tiles < 1) tiles = 1;
-    plan_splits(tiles, p.B * p.Hkv, chunk, S);
+    plan_splits(tiles, p.B * p.Hkv, chunk, S, ctas_per_sm(p, e4m3));
     return ATTN_OK;
 }
 

@@ -33,7 +33,7 @@ int choose_fp8_path(const Problem& p, int path) {
 int run_decode(const Problem& p, const void* q, const void* k, const void* v, void* o, float v_descale, void* ws,
                size_t ws_bytes, int* status, cudaStream_t s) {
     int chunk = 0, S = 0;
-    decode_plan_tc(p, &chunk, &S);
+    decode_plan_tc(p, &chunk, &S, true);
     const int rows = p.B * p.Hq * p.M;
     if (!ws || ws_bytes < split_workspace_bytes(rows, S, p.D)) return ATTN_ERR_WORKSPACE;
     if (!aligned16(ws)) return ATTN_ERR_ALIGN;
@@ -47,6 +47,22 @@ int run_decode(const Problem& p, const void* q, const void* k, const void* v, vo
 }  // namespace attn
 
 using namespace attn;
+
+extern "C" size_t attn_fwd_fp8_workspace_bytes(int B, int Hq, int Hkv, int M, int N, int D, int causal, int window,
+                                               int path) {
+    static const int16_t dummy[8] __attribute__((aligned(16))) = {};
+    Problem p;
+    if (path < ATTN_PATH_AUTO || path > ATTN_PATH_DECODE || path == ATTN_PATH_SIMT) return 0;
+    if (validate_problem(dummy, dummy, dummy, dummy, B, Hq, Hkv, M, N, D, causal, window, 0.f, ATTN_BF16, &p) !=
+            ATTN_OK ||
+        D != 128)
+        return 0;
+    if ((int64_t)B * Hq * M == 0 || N == 0) return 0;
+    if (choose_fp8_path(p, path) != ATTN_PATH_DECODE || !decode_tc_supported(p)) return 0;
+    int chunk = 0, S = 0;
+    decode_plan_tc(p, &chunk, &S, true);
+    return split_workspace_bytes(p.B * p.Hq * p.M, S, p.D);
+}
 
 extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                             int Hkv, int M, int N, int D, int causal, int window, float scale, float q_descale,
@@ -83,7 +99,7 @@ extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o
     if (path == ATTN_PATH_PREFILL) return launch_prefill_e4m3(p, q, k, v, o, status, v_descale, s);
     if (workspace) return run_decode(p, q, k, v, o, v_descale, workspace, ws_bytes, status, s);
     int chunk = 0, S = 0;
-    decode_plan_tc(p, &chunk, &S);
+    decode_plan_tc(p, &chunk, &S, true);
     const size_t bytes = split_workspace_bytes(p.B * p.Hq * p.M, S, p.D);
     void* ws = nullptr;
     if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) return ATTN_ERR_CUDA;

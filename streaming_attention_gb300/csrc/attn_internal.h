@@ -60,7 +60,8 @@ bool decode_supported(const Problem& p);
 int decode_plan(const Problem& p, int* chunk, int* S);
 // tcgen05 split kernel (D = 128, at most 16 grouped rows per KV head)
 bool decode_tc_supported(const Problem& p);
-int decode_plan_tc(const Problem& p, int* chunk, int* S);
+// e4m3: the plan of the 8-bit kernel (more CTAs per SM, so more splits)
+int decode_plan_tc(const Problem& p, int* chunk, int* S, bool e4m3 = false);
 cudaError_t launch_decode_tc(const Problem& p, const void* q, const void* k, const void* v, int chunk, int S,
                              const SplitWorkspace& ws, int* status, cudaStream_t stream);
 
@@ -74,7 +75,7 @@ struct PagedKV {
     const int* seq_lens;
     int num_pages, page_size, max_pages, max_len;
 };
-int decode_plan_paged(const Problem& p, const PagedKV& kv, int* chunk, int* S);
+int decode_plan_paged(const Problem& p, const PagedKV& kv, int* chunk, int* S, bool e4m3 = false);
 // e4m3: Q and the pools hold E4M3 bytes (p.scale_log2 then includes the Q and K
 // dequantization factors; the merge applies V's)
 cudaError_t launch_decode_paged(const Problem& p, const void* q, const PagedKV& kv, int chunk, int S,

@@ -73,9 +73,9 @@ int validate_paged(const void* q, const void* kp, const void* vp, const int* tab
 
 bool nothing_to_attend(const PagedCall& c) { return c.kv.max_len == 0 || c.kv.num_pages == 0 || c.p.Hkv == 0; }
 
-size_t paged_workspace(const PagedCall& c) {
+size_t paged_workspace(const PagedCall& c, bool e4m3 = false) {
     int chunk = 0, S = 0;
-    decode_plan_paged(c.p, c.kv, &chunk, &S);
+    decode_plan_paged(c.p, c.kv, &chunk, &S, e4m3);
     return split_workspace_bytes(c.p.B * c.p.Hq * c.p.M, S, c.p.D);
 }
 
@@ -85,7 +85,7 @@ int run_paged(const PagedCall& c, const void* q, void* o, void* ws, size_t ws_by
               bool e4m3 = false, float v_descale = 1.0f) {
     const Problem& p = c.p;
     int chunk = 0, S = 0;
-    decode_plan_paged(p, c.kv, &chunk, &S);
+    decode_plan_paged(p, c.kv, &chunk, &S, e4m3);
     const int rows = p.B * p.Hq * p.M;
     if (!ws || ws_bytes < split_workspace_bytes(rows, S, p.D)) return ATTN_ERR_WORKSPACE;
     if (!aligned(ws, 16)) return ATTN_ERR_ALIGN;
@@ -137,6 +137,18 @@ int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages, c
     return rc;
 }
 
+size_t attn_decode_paged_fp8_workspace_bytes(int B, int Hq, int Hkv, int M, int D, int page_size, int max_pages,
+                                             int max_seq_len, int causal, int window) {
+    static const int16_t dummy[8] __attribute__((aligned(16))) = {};
+    const int* idummy = reinterpret_cast<const int*>(dummy);
+    PagedCall c;
+    if (validate_paged(dummy, dummy, dummy, idummy, idummy, dummy, B, Hq, Hkv, M, D, 1, page_size, max_pages,
+                       max_seq_len, causal, window, 0.f, ATTN_BF16, &c) != ATTN_OK)
+        return 0;
+    if ((int64_t)B * Hq * M == 0 || nothing_to_attend(c)) return 0;
+    return paged_workspace(c, true);
+}
+
 int attn_decode_paged_fp8(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
                           const int* seq_lens, void* o, int B, int Hq, int Hkv, int M, int D, int num_pages,
                           int page_size, int max_pages, int max_seq_len, int causal, int window, float scale,
@@ -152,7 +164,7 @@ int attn_decode_paged_fp8(const void* q, const void* k_pages, const void* v_page
     // logits of the dequantized tensors: scale * q_descale * k_descale * <q, k>
     c.p.scale_log2 = (float)((double)c.p.scale * (double)q_descale * (double)k_descale * (double)kLog2e);
     if (workspace) return run_paged(c, q, o, workspace, ws_bytes, s, true, v_descale);
-    const size_t bytes = paged_workspace(c);
+    const size_t bytes = paged_workspace(c, true);
     void* ws = nullptr;
     if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) return ATTN_ERR_CUDA;
     rc = run_paged(c, q, o, ws, bytes, s, true, v_descale);

@@ -205,3 +205,16 @@ def test_fp8_validation_status(L, kw, status):
     st = L.attn_fwd_fp8(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B_"], a["Hq"], a["Hkv"], a["M"], a["N"],
                         a["D"], 1, 0, 0.0, 1.0, 1.0, 1.0, a["dtype"], a["path"], None, 0, None)
     assert st == status
+
+
+def test_fp8_workspace_bytes(L):
+    # the 8-bit decode plan has its own query (today the same split plan as the 16-bit one)
+    n8 = sa.attn_fwd_fp8_workspace_bytes(8, 32, 8, 1, 8192, 128, True, 4096, sa.PATH_DECODE)
+    n16 = sa.attn_workspace_bytes(8, 32, 8, 1, 8192, 128, True, 4096, sa.PATH_DECODE)
+    assert n8 == n16 > 0
+    assert sa.attn_fwd_fp8_workspace_bytes(8, 32, 8, 1, 8192, 128, True, 4096, sa.PATH_AUTO) == n8
+    assert sa.attn_fwd_fp8_workspace_bytes(8, 32, 8, 1, 8192, 128, True, 4096, sa.PATH_PREFILL) == 0
+    assert sa.attn_fwd_fp8_workspace_bytes(8, 32, 8, 1, 8192, 64, True, 4096, sa.PATH_DECODE) == 0
+    assert sa.attn_fwd_fp8_workspace_bytes(2, 32, 32, 4096, 4096, 128, True, 0, sa.PATH_AUTO) == 0
+    p8 = sa.attn_decode_paged_fp8_workspace_bytes(8, 32, 8, 1, 128, 16, 512, 8192, True, 4096)
+    assert p8 >= sa.attn_decode_paged_workspace_bytes(8, 32, 8, 1, 128, 16, 512, 8192, True, 4096) > 0

@@ -121,7 +121,9 @@ def test_fp8_decode_workload_full_size():
     every row, with a caller workspace."""
     from streaming_attention_gb300.inputs import DECODE_GQA as w
     q, k, v = make_qkv_fp8(w.B, w.Hq, w.Hkv, w.M, w.N, w.D, 25)
-    nb = sa.attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.M, w.N, w.D, True, w.window, sa.PATH_DECODE)
+    nb = sa.attn_fwd_fp8_workspace_bytes(w.B, w.Hq, w.Hkv, w.M, w.N, w.D, True, w.window, sa.PATH_DECODE)
+    assert nb > 0 and sa.attn_fwd_fp8_workspace_bytes(w.B, w.Hq, w.Hkv, w.M, w.N, w.D, True, w.window,
+                                                       sa.PATH_PREFILL) == 0
     ws = torch.empty(nb, dtype=torch.uint8, device=DEV)
     o = torch.empty(q.shape, dtype=torch.bfloat16, device=DEV)
     sa.attn_fwd_fp8(q.to(DEV), k.to(DEV), v.to(DEV), o, None, True, w.window, path=sa.PATH_DECODE, workspace=ws)
@@ -146,9 +148,12 @@ def test_fp8_paged_ragged_lengths(page_size):
     table = torch.from_numpy(table.astype(np.int32))
     lens = [1000, 1, 1024, 517]
     o = torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device=DEV)
+    use_ws = page_size in (16, 128)  # the others let the library allocate it
+    nb = sa.attn_decode_paged_fp8_workspace_bytes(B, Hq, Hkv, M, D, page_size, table.shape[1], Ncap, True, 0)
+    ws = torch.empty(nb, dtype=torch.uint8, device=DEV) if use_ws else None
     sa.attn_decode_paged_fp8(q.to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV),
                              torch.tensor(lens, dtype=torch.int32, device=DEV), o, Ncap, causal=True,
-                             q_descale=qd, k_descale=kd, v_descale=vd)
+                             q_descale=qd, k_descale=kd, v_descale=vd, workspace=ws)
     torch.cuda.synchronize()
     want = oracle.attention_paged(deq(q, qd), deq(kp, kd), deq(vp, vd), table, lens, Ncap, True, 0)
     qf, kf, vf = deq(q, qd), deq(k, kd), deq(v, vd)

@@ -212,3 +212,28 @@ def test_host_end_to_end_matches_device_call():
     sa.attn_fwd_host(qh, kh, vh, oh, qd, kd, vd, od, causal=True)
     ref = run(q, k, v, True)
     assert torch.equal(oh, ref.cpu())
+
+
+@pytest.mark.parametrize("shape,causal,window", [
+    ((1, 3, 3, 300, 300, 128), True, 0),        # three chunks of one KV head
+    ((3, 10, 5, 130, 257, 64), False, 0),       # two chunks per batch, uneven (3 + 2 heads)
+    ((10, 4, 1, 70, 90, 64), True, 33),         # chunks of whole batches (2 each)
+    ((2, 16, 4, 256, 512, 128), True, 0),       # GQA groups kept whole within a chunk
+    ((1, 2, 2, 40, 40, 32), False, 0),          # SIMT path (D = 32)
+])
+def test_host_pipelined_chunks_match_device_call(shape, causal, window):
+    """The host-buffer entry point cuts the problem into chunks of (batch, KV
+    head) groups; every row is computed by the same kernel as in one device
+    call, so the outputs are identical, and they match the oracle."""
+    B, Hq, Hkv, M, N, D = shape
+    q, k, v = make_qkv(B, Hq, Hkv, M, N, D, torch.bfloat16, 17)
+    qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+    oh = torch.full_like(qh, float("nan")).pin_memory()
+    qd, kd, vd = (torch.empty_like(t, device=DEV) for t in (q, k, v))
+    od = torch.empty_like(qd)
+    sa.attn_fwd_host(qh, kh, vh, oh, qd, kd, vd, od, causal=causal, window=window)
+    ref = sa.attention(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, window=window)
+    torch.cuda.synchronize()
+    assert torch.equal(oh, ref.cpu())
+    assert torch.equal(od, ref)
+    check(oh, oracle.attention(q, k, v, causal=causal, window=window), torch.bfloat16, f"host {shape}")
