@@ -216,8 +216,9 @@ def test_host_end_to_end_matches_device_call():
 
 @pytest.mark.parametrize("shape,causal,window", [
     ((1, 3, 3, 300, 300, 128), True, 0),        # three chunks of one KV head
-    ((3, 10, 5, 130, 257, 64), False, 0),       # two chunks per batch, uneven (3 + 2 heads)
-    ((10, 4, 1, 70, 90, 64), True, 33),         # chunks of whole batches (2 each)
+    ((1, 20, 20, 130, 257, 64), False, 0),      # seven chunks of three heads, the last of two
+    ((3, 10, 5, 130, 257, 64), False, 0),       # two chunks per batch (3 + 2 heads)
+    ((17, 2, 1, 70, 90, 64), True, 33),         # chunks of whole batches (3, 3, ..., 2)
     ((2, 16, 4, 256, 512, 128), True, 0),       # GQA groups kept whole within a chunk
     ((1, 2, 2, 40, 40, 32), False, 0),          # SIMT path (D = 32)
 ])
