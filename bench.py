@@ -286,8 +286,22 @@ def l2_flusher(dev):
     return flush
 
 
-def path_launches(path_name):
-    return {"decode": 2}.get(path_name, 1)
+def decode_splits(w, sms):
+    """The library's split plan for the decode path: as many splits per KV group
+    as fill two CTAs per SM, at most one per 128-key tile of the visible range."""
+    lo = max(0, (w.N - w.M) - w.window + 1) if w.window > 0 else 0
+    tiles = max(1, -(-(w.N - (lo // 128) * 128) // 128))
+    s = max(1, min(2 * sms // (w.B * w.Hkv), tiles, 4096))
+    per = -(-tiles // s)
+    return -(-tiles // per)
+
+
+def path_launches(path_name, w=None, sms=152):
+    """Kernel launches per call: prefill one; decode one when a group's splits
+    fit a thread-block cluster (they merge in the kernel), else split + merge."""
+    if path_name != "decode":
+        return 1
+    return 1 if w is not None and decode_splits(w, sms) <= 8 else 2
 
 
 def chosen_path(w):
@@ -400,7 +414,8 @@ def run_ours(args):
                                     "protocol": "graph replay of one call, L2 flushed (2x-L2 read) before each"}},
         "e2e": {"value": round(world * work / e2e_s / scale, 3), "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": path_launches(path_name) * args.steps,
+        "gpu_launches": path_launches(path_name, w, torch.cuda.get_device_properties(dev).multi_processor_count)
+        * args.steps,
         "roofline": {"bound": bound, "achieved": round(achieved, 3), "peak": peak, "unit": r_unit,
                      "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": pk_src},
         "clocks": clocks,

@@ -116,8 +116,10 @@ int run(const Problem& p, const void* q, const void* k, const void* v, void* o, 
             if (!ws || ws_bytes < split_workspace_bytes(rows, S, p.D)) return ATTN_ERR_WORKSPACE;
             if (!aligned16(ws)) return ATTN_ERR_ALIGN;
             SplitWorkspace w = split_workspace(ws, rows, S, p.D);
-            cudaError_t e = launch_decode(p, q, k, v, chunk, S, w, status, stream);
+            DecodeOut out{o, p.lse, 1.0f, false};
+            cudaError_t e = launch_decode(p, q, k, v, chunk, S, w, status, stream, &out);
             if (e != cudaSuccess) return ATTN_ERR_CUDA;
+            if (out.merged) return ATTN_OK;
             return cuda_status(launch_merge(w.m, w.l, w.acc, o, nullptr, nullptr, p.lse, rows, S, p.D, p.dtype,
                                             1.0f, true, stream));
         }

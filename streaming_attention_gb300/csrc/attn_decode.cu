@@ -28,8 +28,9 @@ int decode_plan(const Problem& p, int* chunk, int* S) {
 }
 
 cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const void* v, int chunk, int S,
-                          const SplitWorkspace& ws, int* status, cudaStream_t stream) {
-    if (decode_tc_supported(p)) return launch_decode_tc(p, q, k, v, chunk, S, ws, status, stream);
+                          const SplitWorkspace& ws, int* status, cudaStream_t stream, DecodeOut* out) {
+    if (decode_tc_supported(p)) return launch_decode_tc(p, q, k, v, chunk, S, ws, status, stream, out);
+    if (out) out->merged = false;
     return launch_simt(p, q, k, v, nullptr, chunk, S, &ws, stream);
 }
 

@@ -81,7 +81,35 @@ struct DecodeParams {
     const int* seq_lens;
     int page_size, max_pages, max_len;
     int oob_z;  // a pool coordinate past its last (page, head): TMA reads zeros there
+    // cluster merge (the S <= 8 splits of a group are one thread-block cluster):
+    // the CTAs combine the summaries through distributed shared memory, each
+    // writing some of the output rows and their log-sum-exp, so no merge kernel runs
+    int cluster;
+    void* o;
+    float* lse;
+    int out_dtype;
+    float out_scale;
 };
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// shared-memory address of the same variable in cluster CTA `rank`
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
 
 // Keys of one CTA's sequence: its length and the union [klo, khi) of the
 // ranges its M query rows may see; splits start at kbase (a tile boundary).
@@ -167,6 +195,8 @@ __global__ void __launch_bounds__(kDecThreads)
     const uint32_t bar_o = bar_free0 + 16;
     const uint32_t bar_red0 = bar_o + 8, bar_lred = bar_red0 + 16;  // shared-memory exchanges of the softmax
     float* red = reinterpret_cast<float*>(smem + C::kOffRed);
+    // cluster mode: this split's summary [R][D] acc, then [R] m, [R] l, in the ring once it is idle
+    float* part = reinterpret_cast<float*>(smem + C::kOffRing);
     float* lred = reinterpret_cast<float*>(smem + C::kOffLRed);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc);
     volatile uint32_t* abort_flag = tmem_slot + 1;
@@ -501,12 +531,30 @@ __global__ void __launch_bounds__(kDecThreads)
 #pragma unroll
             for (int r = 0; r < RP; ++r) {
                 if (r < p.R) {
+                    const float lsum = lred[r] + lred[DNR + r] + lred[2 * DNR + r] + lred[3 * DNR + r];
+                    if (p.cluster) {  // the summary stays in this CTA's (now idle) ring
+                        part[r * DD + kl] = __uint_as_float(o[r]);
+                        if (kl == 0) {
+                            part[DNR * DD + r] = m_ref[r];
+                            part[DNR * DD + DNR + r] = lsum;
+                        }
+                        continue;
+                    }
                     const size_t slot = (size_t)(row_base + r) * p.S + split;
                     p.ws_acc[slot * DD + kl] = __uint_as_float(o[r]);
                     if (kl == 0) {
                         p.ws_m[slot] = m_ref[r];
-                        p.ws_l[slot] = lred[r] + lred[DNR + r] + lred[2 * DNR + r] + lred[3 * DNR + r];
+                        p.ws_l[slot] = lsum;
                     }
+                }
+            }
+        } else if (p.cluster) {
+            // no key in this split (or it gave up): the empty summary
+            for (int r = 0; r < p.R; ++r) {
+                part[r * DD + kl] = 0.f;
+                if (kl == 0) {
+                    part[DNR * DD + r] = -INFINITY;
+                    part[DNR * DD + DNR + r] = 0.f;
                 }
             }
         } else if (T == 0) {
@@ -520,6 +568,54 @@ __global__ void __launch_bounds__(kDecThreads)
                 }
             }
         }
+    }
+
+    if (p.cluster) {
+        // every thread of every CTA of the cluster reaches this point (all waits
+        // above are bounded), so the cluster barriers complete
+        cluster_sync_all();
+        if (warp < 4) {
+            // rank s merges rows s, s + S, ...; thread kl = head dimension d: the
+            // common-maximum merge of the S summaries (maxima in base 2), one cast.
+            // All S summaries of a row are loaded before any is used, so the
+            // distributed-shared-memory round trips overlap.
+            const int kl = threadIdx.x;
+            const uint32_t local = smem_u32(part);
+            for (int r = (int)cluster_rank(); r < p.R; r += p.S) {
+                float ms[kMaxClusterSplits], ls[kMaxClusterSplits], as[kMaxClusterSplits];
+#pragma unroll
+                for (int sp = 0; sp < kMaxClusterSplits; ++sp) {
+                    ms[sp] = -INFINITY;
+                    ls[sp] = 0.f;
+                    as[sp] = 0.f;
+                    if (sp < p.S) {
+                        const uint32_t base = map_to_rank(local, sp);
+                        ms[sp] = ld_cluster_f32(base + 4u * (DNR * DD + r));
+                        ls[sp] = ld_cluster_f32(base + 4u * (DNR * DD + DNR + r));
+                        as[sp] = ld_cluster_f32(base + 4u * (r * DD + kl));
+                    }
+                }
+                float mx = -INFINITY;
+#pragma unroll
+                for (int sp = 0; sp < kMaxClusterSplits; ++sp) mx = fmaxf(mx, ms[sp]);
+                float L = 0.f, x = 0.f;
+#pragma unroll
+                for (int sp = 0; sp < kMaxClusterSplits; ++sp) {
+                    const float w = (ms[sp] == -INFINITY) ? 0.f : exp2f(ms[sp] - mx);  // an empty summary weighs 0
+                    L = fmaf(w, ls[sp], L);
+                    x = fmaf(w, as[sp], x);
+                }
+                x *= L > 0.f ? p.out_scale / L : 0.f;
+                const size_t out = (size_t)(row_base + r) * DD + kl;
+                if (p.out_dtype == ATTN_BF16)
+                    reinterpret_cast<uint16_t*>(p.o)[out] = (uint16_t)(pack_bf16(x, 0.f) & 0xFFFFu);
+                else
+                    reinterpret_cast<uint16_t*>(p.o)[out] = (uint16_t)(pack_f16(x, 0.f) & 0xFFFFu);
+                if (kl == 0 && p.lse) p.lse[row_base + r] = L > 0.f ? (mx + log2f(L)) * kLn2 : -INFINITY;
+            }
+        }
+        // every CTA keeps its shared memory until the others have read it
+        cluster_sync_all();
     }
 
     tc_fence_before();
@@ -544,7 +640,8 @@ int sm_count() {
 
 template <int EB, bool kBF16, int RP, bool kPaged>
 cudaError_t launch_decode_t(const Problem& pr, const void* q, const void* k, const void* v, const PagedKV* kv,
-                            int chunk, int S, const SplitWorkspace& ws, int* status, cudaStream_t stream) {
+                            int chunk, int S, const SplitWorkspace& ws, int* status, cudaStream_t stream,
+                            DecodeOut* out) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
@@ -590,6 +687,15 @@ cudaError_t launch_decode_t(const Problem& pr, const void* q, const void* k, con
         dp.max_len = kv->max_len;
         dp.oob_z = kv->num_pages * pr.Hkv;
     }
+    // Up to 8 splits of a group form one cluster and merge in the kernel
+    const bool cluster = out && out->o && S <= kMaxClusterSplits;
+    if (cluster) {
+        dp.cluster = 1;
+        dp.o = out->o;
+        dp.lse = out->lse;
+        dp.out_dtype = pr.dtype;
+        dp.out_scale = out->out_scale;
+    }
     // Programmatic launch: CTAs may start their setup (barriers, TMEM) while the
     // previous kernel in the stream drains; griddepcontrol.wait orders the rest.
     cudaLaunchConfig_t cfg = {};
@@ -597,12 +703,18 @@ cudaError_t launch_decode_t(const Problem& pr, const void* q, const void* k, con
     cfg.blockDim = dim3(kDecThreads);
     cfg.dynamicSmemBytes = DCfg<EB>::kSmem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)S;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_decode_kernel<EB, kBF16, RP, kPaged>, tq, tk, tv, dp);
+    cfg.numAttrs = cluster ? 2 : 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, attn_decode_kernel<EB, kBF16, RP, kPaged>, tq, tk, tv, dp);
+    if (out) out->merged = cluster && e == cudaSuccess;
+    return e;
 }
 
 // e4m3: 8-bit inputs (the problem's dtype is then the output type, which the
@@ -610,20 +722,20 @@ cudaError_t launch_decode_t(const Problem& pr, const void* q, const void* k, con
 template <bool kPaged>
 cudaError_t launch_decode_any(const Problem& p, const void* q, const void* k, const void* v, const PagedKV* kv,
                               int chunk, int S, const SplitWorkspace& ws, int* status, cudaStream_t stream,
-                              bool e4m3 = false) {
+                              DecodeOut* out, bool e4m3 = false) {
     const int R = p.G * p.M;
     if (e4m3) {
-        if (R <= 4) return launch_decode_t<1, true, 4, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream);
-        if (R <= 8) return launch_decode_t<1, true, 8, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream);
-        return launch_decode_t<1, true, 16, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream);
+        if (R <= 4) return launch_decode_t<1, true, 4, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream, out);
+        if (R <= 8) return launch_decode_t<1, true, 8, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream, out);
+        return launch_decode_t<1, true, 16, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream, out);
     }
     const bool bf = p.dtype == ATTN_BF16;
-    if (R <= 4) return bf ? launch_decode_t<2, true, 4, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream)
-                          : launch_decode_t<2, false, 4, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream);
-    if (R <= 8) return bf ? launch_decode_t<2, true, 8, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream)
-                          : launch_decode_t<2, false, 8, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream);
-    return bf ? launch_decode_t<2, true, 16, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream)
-              : launch_decode_t<2, false, 16, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream);
+    if (R <= 4) return bf ? launch_decode_t<2, true, 4, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream, out)
+                          : launch_decode_t<2, false, 4, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream, out);
+    if (R <= 8) return bf ? launch_decode_t<2, true, 8, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream, out)
+                          : launch_decode_t<2, false, 8, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream, out);
+    return bf ? launch_decode_t<2, true, 16, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream, out)
+              : launch_decode_t<2, false, 16, kPaged>(p, q, k, v, kv, chunk, S, ws, status, stream, out);
 }
 
 // Splits of `tiles` key tiles over `groups` KV groups: every CTA resident at
@@ -659,8 +771,8 @@ int decode_plan_tc(const Problem& p, int* chunk, int* S, bool e4m3) {
 }
 
 cudaError_t launch_decode_tc(const Problem& p, const void* q, const void* k, const void* v, int chunk, int S,
-                             const SplitWorkspace& ws, int* status, cudaStream_t stream) {
-    return launch_decode_any<false>(p, q, k, v, nullptr, chunk, S, ws, status, stream);
+                             const SplitWorkspace& ws, int* status, cudaStream_t stream, DecodeOut* out) {
+    return launch_decode_any<false>(p, q, k, v, nullptr, chunk, S, ws, status, stream, out);
 }
 
 // Paged: the plan must cover any sequence up to kv.max_len keys. Without a
@@ -680,13 +792,14 @@ int decode_plan_paged(const Problem& p, const PagedKV& kv, int* chunk, int* S, b
 }
 
 cudaError_t launch_decode_paged(const Problem& p, const void* q, const PagedKV& kv, int chunk, int S,
-                                const SplitWorkspace& ws, int* status, cudaStream_t stream, bool e4m3) {
-    return launch_decode_any<true>(p, q, nullptr, nullptr, &kv, chunk, S, ws, status, stream, e4m3);
+                                const SplitWorkspace& ws, int* status, cudaStream_t stream, DecodeOut* out,
+                                bool e4m3) {
+    return launch_decode_any<true>(p, q, nullptr, nullptr, &kv, chunk, S, ws, status, stream, out, e4m3);
 }
 
 cudaError_t launch_decode_e4m3(const Problem& p, const void* q, const void* k, const void* v, int chunk, int S,
-                               const SplitWorkspace& ws, int* status, cudaStream_t stream) {
-    return launch_decode_any<false>(p, q, k, v, nullptr, chunk, S, ws, status, stream, true);
+                               const SplitWorkspace& ws, int* status, cudaStream_t stream, DecodeOut* out) {
+    return launch_decode_any<false>(p, q, k, v, nullptr, chunk, S, ws, status, stream, out, true);
 }
 
 }  // namespace attn

@@ -38,7 +38,9 @@ int run_decode(const Problem& p, const void* q, const void* k, const void* v, vo
     if (!ws || ws_bytes < split_workspace_bytes(rows, S, p.D)) return ATTN_ERR_WORKSPACE;
     if (!aligned16(ws)) return ATTN_ERR_ALIGN;
     SplitWorkspace w = split_workspace(ws, rows, S, p.D);
-    if (launch_decode_e4m3(p, q, k, v, chunk, S, w, status, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    DecodeOut out{o, p.lse, v_descale, false};
+    if (launch_decode_e4m3(p, q, k, v, chunk, S, w, status, s, &out) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (out.merged) return ATTN_OK;
     return cuda_status(
         launch_merge(w.m, w.l, w.acc, o, nullptr, nullptr, p.lse, rows, S, p.D, p.dtype, 1.0f, true, s, v_descale));
 }

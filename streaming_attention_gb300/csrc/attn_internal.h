@@ -53,9 +53,19 @@ cudaError_t launch_simt(const Problem& p, const void* q, const void* k, const vo
 cudaError_t launch_merge(const float* m, const float* l, const float* acc, void* o, float* m_out,
                          float* l_out, float* lse_out, int rows, int S, int D, int out_dtype, float unit,
                          bool programmatic, cudaStream_t stream, float out_scale = 1.0f);
+// Where the split kernel may write the final output itself: when the splits of
+// a group fit one thread-block cluster (S <= kMaxClusterSplits) the kernel merges
+// them in the cluster and sets `merged`; otherwise the caller runs launch_merge.
+constexpr int kMaxClusterSplits = 8;
+struct DecodeOut {
+    void* o;           // [rows][D] of p.dtype (nullptr: never merge in the kernel)
+    float* lse;        // optional [rows] natural-log log-sum-exp
+    float out_scale;   // multiplies the merged output (V dequantization factor, else 1)
+    bool merged;       // set by the launch
+};
 cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const void* v,
                           int chunk, int S, const SplitWorkspace& ws, int* status,
-                          cudaStream_t stream);
+                          cudaStream_t stream, DecodeOut* out = nullptr);
 bool decode_supported(const Problem& p);
 int decode_plan(const Problem& p, int* chunk, int* S);
 // tcgen05 split kernel (D = 128, at most 16 grouped rows per KV head)
@@ -63,7 +73,7 @@ bool decode_tc_supported(const Problem& p);
 // e4m3: the plan of the 8-bit kernel (more CTAs per SM, so more splits)
 int decode_plan_tc(const Problem& p, int* chunk, int* S, bool e4m3 = false);
 cudaError_t launch_decode_tc(const Problem& p, const void* q, const void* k, const void* v, int chunk, int S,
-                             const SplitWorkspace& ws, int* status, cudaStream_t stream);
+                             const SplitWorkspace& ws, int* status, cudaStream_t stream, DecodeOut* out = nullptr);
 
 // Paged KV cache (decode): pools [num_pages][Hkv][page_size][D]; sequence b's
 // key j lives in row j % page_size of page block_table[b * max_pages + j / page_size];
@@ -79,10 +89,11 @@ int decode_plan_paged(const Problem& p, const PagedKV& kv, int* chunk, int* S, b
 // e4m3: Q and the pools hold E4M3 bytes (p.scale_log2 then includes the Q and K
 // dequantization factors; the merge applies V's)
 cudaError_t launch_decode_paged(const Problem& p, const void* q, const PagedKV& kv, int chunk, int S,
-                                const SplitWorkspace& ws, int* status, cudaStream_t stream, bool e4m3 = false);
+                                const SplitWorkspace& ws, int* status, cudaStream_t stream, DecodeOut* out = nullptr,
+                                bool e4m3 = false);
 // The tcgen05 split kernel on contiguous E4M3 inputs (same plan as launch_decode_tc)
 cudaError_t launch_decode_e4m3(const Problem& p, const void* q, const void* k, const void* v, int chunk, int S,
-                               const SplitWorkspace& ws, int* status, cudaStream_t stream);
+                               const SplitWorkspace& ws, int* status, cudaStream_t stream, DecodeOut* out = nullptr);
 
 // Backward pass (tcgen05, D in {64, 128}): the caller's tensors, device pointers.
 struct BwdArgs {

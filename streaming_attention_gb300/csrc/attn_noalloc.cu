@@ -71,7 +71,9 @@ extern "C" int attn_fwd_decode_noalloc(const void* q, const void* k, const void*
     // Every (row, split) summary the merge reads is written by the split
     // kernel of this same call, so nothing has to be cleared first.
     SplitWorkspace w = split_workspace(base, rows, S, p.D);
-    if (launch_decode(p, q, k, v, chunk, S, w, status, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    DecodeOut out{o, nullptr, 1.0f, false};
+    if (launch_decode(p, q, k, v, chunk, S, w, status, s, &out) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (out.merged) return ATTN_OK;
     if (launch_merge(w.m, w.l, w.acc, o, nullptr, nullptr, nullptr, rows, S, p.D, p.dtype, 1.0f, true, s) !=
         cudaSuccess)
         return ATTN_ERR_CUDA;

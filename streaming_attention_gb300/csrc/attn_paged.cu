@@ -92,7 +92,10 @@ int run_paged(const PagedCall& c, const void* q, void* o, void* ws, size_t ws_by
     int* status = device_status_ptr();
     if (!status) return ATTN_ERR_CUDA;
     SplitWorkspace w = split_workspace(ws, rows, S, p.D);
-    if (launch_decode_paged(p, q, c.kv, chunk, S, w, status, stream, e4m3) != cudaSuccess) return ATTN_ERR_CUDA;
+    DecodeOut out{o, nullptr, v_descale, false};
+    if (launch_decode_paged(p, q, c.kv, chunk, S, w, status, stream, &out, e4m3) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    if (out.merged) return ATTN_OK;
     return cuda_status(launch_merge(w.m, w.l, w.acc, o, nullptr, nullptr, nullptr, rows, S, p.D, p.dtype, 1.0f, true,
                                     stream, v_descale));
 }

@@ -53,7 +53,8 @@ def lse_check(got, want, what):
 @pytest.mark.parametrize("shape,causal,window", [
     ((2, 4, 2, 200, 333, 128), True, 0),
     ((1, 2, 2, 130, 130, 64), False, 0),
-    ((2, 8, 2, 1, 1500, 128), True, 700),
+    ((2, 8, 2, 1, 1500, 128), True, 700),     # decode: 6 splits per group, merged in a cluster
+    ((1, 4, 1, 1, 5000, 128), False, 0),      # decode: 40 splits, merged by the merge kernel
     ((1, 2, 1, 300, 100, 64), True, 0),   # rows past the keys see nothing: lse = -inf
 ])
 def test_forward_lse(path, shape, causal, window):
