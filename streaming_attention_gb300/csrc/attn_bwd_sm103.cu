@@ -677,42 +677,58 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_teardown(bs);
 }
 
-// delta = rowsum(dO * O) and lse2 = lse * log2(e) per row, padded to Mpad rows
-// per head (-inf and 0 past M), one warp per row.
+// dot product of eight 16-bit pairs held in two 16-byte vectors
 template <bool kBF16>
+__device__ __forceinline__ float dot8(const uint4& a, const uint4& b) {
+    const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float a0, a1, b0, b1;
+        if (kBF16) {
+            a0 = __uint_as_float(wa[i] << 16);
+            a1 = __uint_as_float(wa[i] & 0xFFFF0000u);
+            b0 = __uint_as_float(wb[i] << 16);
+            b1 = __uint_as_float(wb[i] & 0xFFFF0000u);
+        } else {
+            const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&wa[i]));
+            const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&wb[i]));
+            a0 = fa.x;
+            a1 = fa.y;
+            b0 = fb.x;
+            b1 = fb.y;
+        }
+        acc = fmaf(a0, b0, acc);
+        acc = fmaf(a1, b1, acc);
+    }
+    return acc;
+}
+
+// delta = rowsum(dO * O) and lse2 = lse * log2(e) per row, padded to Mpad rows
+// per head (-inf and 0 past M). D / 8 lanes per row, each with one 16-byte load
+// of O and of dO, so a warp covers 32 / (D / 8) rows; the row sums reduce
+// within each lane group.
+template <bool kBF16, int D>
 __global__ void __launch_bounds__(256)
     attn_bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ d_o, const float* __restrict__ lse,
-                        float* lse2, float* delta, int M, int Mpad, int D, int rows_pad) {
+                        float* lse2, float* delta, int M, int Mpad, int rows_pad) {
+    constexpr int kLanesPerRow = D / 8;
+    constexpr int kRowsPerWarp = 32 / kLanesPerRow;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int gr = blockIdx.x * 8 + warp;
-    if (gr >= rows_pad) return;
+    const int li = lane % kLanesPerRow;
+    const int gr = (blockIdx.x * 8 + warp) * kRowsPerWarp + lane / kLanesPerRow;
+    const bool valid = gr < rows_pad;
     const int bh = gr / Mpad, i = gr % Mpad;
-    if (i >= M) {
-        if (lane == 0) {
-            lse2[gr] = -INFINITY;
-            delta[gr] = 0.f;
-        }
-        return;
-    }
     const size_t row = (size_t)bh * M + i;
     float acc = 0.f;
-    for (int d = lane; d < D; d += 32) {
-        const uint16_t a = o[row * D + d], bb = d_o[row * D + d];
-        float fa, fb;
-        if (kBF16) {
-            fa = __uint_as_float((uint32_t)a << 16);
-            fb = __uint_as_float((uint32_t)bb << 16);
-        } else {
-            fa = __half2float(__ushort_as_half(a));
-            fb = __half2float(__ushort_as_half(bb));
-        }
-        acc = fmaf(fa, fb, acc);
-    }
+    if (valid && i < M)
+        acc = dot8<kBF16>(reinterpret_cast<const uint4*>(o + row * D)[li],
+                          reinterpret_cast<const uint4*>(d_o + row * D)[li]);
 #pragma unroll
-    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-    if (lane == 0) {
-        delta[gr] = acc;
-        lse2[gr] = lse[row] * kLog2e;
+    for (int s = kLanesPerRow / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (valid && li == 0) {
+        delta[gr] = i < M ? acc : 0.f;
+        lse2[gr] = i < M ? lse[row] * kLog2e : -INFINITY;
     }
 }
 
@@ -731,9 +747,10 @@ cudaError_t launch_bwd_t(const Problem& pr, const BwdArgs& a, const float* lse2,
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int rows_pad = pr.B * pr.Hq * Mpad;
-    attn_bwd_pre_kernel<kBF16><<<(rows_pad + 7) / 8, 256, 0, stream>>>(
+    constexpr int kPreRowsPerBlock = 8 * (32 / (D / 8));
+    attn_bwd_pre_kernel<kBF16, D><<<(rows_pad + kPreRowsPerBlock - 1) / kPreRowsPerBlock, 256, 0, stream>>>(
         static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.d_o), a.lse, const_cast<float*>(lse2),
-        const_cast<float*>(delta), pr.M, Mpad, D, rows_pad);
+        const_cast<float*>(delta), pr.M, Mpad, rows_pad);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     CUtensorMap tq, tk, tv, tdo;

@@ -160,3 +160,27 @@ def test_fp8_paged_ragged_lengths(page_size):
     for b, L in enumerate(lens):
         H, sigma, wabs = bounds(qf[b:b + 1], kf[b:b + 1, :, :L], vf[b:b + 1, :, :L], True, 0, 1.0 / np.sqrt(D))
         check_fp8(o[b:b + 1], want[b:b + 1], H, sigma, wabs, torch.bfloat16, f"page {page_size} seq {b}")
+
+
+def test_fp8_rising_maximum_stress():
+    """The long causal stress construction in E4M3 (Q[..., D-1] = 8, K[..., j, D-1]
+    rising from -42 to 42, each rounded to E4M3): the logit row maximum rises by
+    about 60 base-2 units along the keys, so the lazy rescale fires again and
+    again, while P stays within E4M3's range. Sampled rows, causal and noncausal."""
+    from streaming_attention_gb300.inputs import _ramp_bias
+    B, H, M, N, D = 1, 4, 4096, 4096, 128
+    g = torch.Generator().manual_seed(27)
+    q = torch.randn(B, H, M, D, generator=g)
+    k = torch.randn(B, H, N, D, generator=g)
+    v = torch.randn(B, H, N, D, generator=g)
+    _ramp_bias(q, k)
+    q, k, v = (t.to(torch.float8_e4m3fn) for t in (q, k, v))
+    qf, kf, vf = deq(q, 1.0), deq(k, 1.0), deq(v, 1.0)
+    rows = sample_rows(B, H, M, 64, seed=28)
+    for causal in (True, False):
+        o = sa.attention_fp8(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal)
+        torch.cuda.synchronize()
+        want = oracle.attention_rows(qf, kf, vf, rows, causal=causal)
+        got = o.reshape(-1, D)[torch.tensor(rows)].cpu()
+        H_, sigma, wabs = row_bounds(qf, kf, vf, rows, causal, 0, 1.0 / np.sqrt(D))
+        check_fp8(got, want, H_, sigma, wabs, torch.bfloat16, f"stress causal={causal}")
