@@ -489,6 +489,8 @@ def extra_measurements(args, dev, stream, flush):
         out["prefill_d128_bf16_noncausal_backward"] = backward_measure(PREFILL_D128, False, steps, dev, stream)
     if args.workload == PREFILL_D128.name:
         out["split_softmax_bf16_m1024_n131072"] = split_softmax_measure(1024, 131072, 4096, steps, dev, stream)
+        out["split_softmax_bf16_m1024_n131072_resident"] = split_softmax_measure(1024, 131072, 0, steps, dev,
+                                                                                  stream)
     if args.workload in (PREFILL_D128.name, DECODE_GQA.name):
         out["decode_gqa_e4m3"] = fp8_decode_measure(DECODE_GQA, None, steps, dev, stream, flush)
         out["decode_gqa_e4m3_paged128"] = fp8_decode_measure(DECODE_GQA, 128, steps, dev, stream, flush)
@@ -615,8 +617,9 @@ def backward_measure(w, causal, steps, dev, stream):
 
 def split_softmax_measure(M, N, chunk, steps, dev, stream):
     """Wide-row split softmax of a seeded N(0,1) [M, N] BF16 matrix; bytes are the
-    method's own traffic: x read twice (statistics, then normalization), y
-    written once."""
+    form's own traffic: x read twice (statistics, then normalization) and y
+    written once for the three-kernel form (chunk > 0); x read once and y
+    written once for the row-resident form (chunk 0)."""
     import streaming_attention_gb300 as sa
 
     x = (torch.randn(M, N, generator=torch.Generator().manual_seed(7)) * 4).to(torch.bfloat16)
@@ -627,10 +630,11 @@ def split_softmax_measure(M, N, chunk, steps, dev, stream):
         sa.split_softmax(t[0], chunk, y=t[1], workspace=ws, stream=st)
 
     ms = time_steady(fn_on, sets, steps, 3, stream)
-    nbytes = 3.0 * M * N * 2
+    nbytes = (3.0 if chunk else 2.0) * M * N * 2
     del sets
     return {"GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1), "us": round(ms * 1e3, 1),
-            "bytes": "x read twice + y written once", "path": f"split softmax, chunk {chunk}"}
+            "bytes": "x read twice + y written once" if chunk else "x read once + y written once",
+            "path": f"split softmax, chunk {chunk}" if chunk else "split softmax, row-resident clusters"}
 
 
 def paged_decode_measure(w, page_size, steps, dev, stream, flush):

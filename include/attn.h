@@ -322,10 +322,17 @@ ATTN_API int attn_decode_paged_fp8(const void* q, const void* k_pages, const voi
  * that normalizes, all on `stream`.
  *   x, y: device [M, N], dtype ATTN_FP32, ATTN_FP16 or ATTN_BF16 (both), 16-byte
  *         aligned; FP32 arithmetic, one cast of y. 1 <= N <= 131072; M >= 0
- *         (M == 0 launches nothing). chunk: 256, 1024 or 4096.
+ *         (M == 0 launches nothing); M <= 65535.
+ *   chunk: 256, 1024 or 4096 runs the three kernels with chunks of that many
+ *         columns; 0 runs the row-resident form: the row's chunks (at most 8,
+ *         of 4096 or 16384 columns) are the CTAs of one thread-block cluster,
+ *         keep their values on chip, exchange their (max, sum) pairs through
+ *         distributed shared memory, merge them the same way and normalize
+ *         without rereading x (x read once, y written once).
  *   workspace: 8 * M * (ceil(N / chunk) + 1) bytes (a float pair per chunk and
  *         one merged pair per row), 8-byte aligned, or NULL to have it
- *         allocated stream-ordered. Values are not validated; x must be finite. */
+ *         allocated stream-ordered; none for chunk 0 (workspace ignored).
+ *         Values are not validated; x must be finite. */
 ATTN_API size_t attn_split_softmax_workspace_bytes(int M, int N, int chunk);
 ATTN_API int attn_split_softmax(const void* x, void* y, int M, int N, int chunk, int dtype,
                                 void* workspace, size_t ws_bytes, void* stream);

@@ -431,20 +431,21 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
 extern "C" {
 
 size_t attn_split_softmax_workspace_bytes(int M, int N, int chunk) {
-    if (M < 0 || N < 1 || N > 131072 || !split_softmax_chunk_ok(chunk)) return 0;
+    if (M < 0 || M > 65535 || N < 1 || N > 131072 || !split_softmax_chunk_ok(chunk)) return 0;
     return split_softmax_ws_bytes(M, N, chunk);
 }
 
 int attn_split_softmax(const void* x, void* y, int M, int N, int chunk, int dtype, void* workspace, size_t ws_bytes,
                        void* stream) {
     if (dtype != ATTN_BF16 && dtype != ATTN_FP16 && dtype != ATTN_FP32) return ATTN_ERR_DTYPE;
-    if (M < 0 || N < 1 || N > 131072 || !split_softmax_chunk_ok(chunk)) return ATTN_ERR_SHAPE;
+    if (M < 0 || M > 65535 || N < 1 || N > 131072 || !split_softmax_chunk_ok(chunk)) return ATTN_ERR_SHAPE;
     if ((int64_t)M * N > kI32Max) return ATTN_ERR_OVERFLOW;
     if (M == 0) return ATTN_OK;
     if (!x || !y) return ATTN_ERR_NULL;
     if (!aligned16(x) || !aligned16(y)) return ATTN_ERR_ALIGN;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t need = split_softmax_ws_bytes(M, N, chunk);
+    if (need == 0) return cuda_status(launch_split_softmax(x, y, M, N, chunk, dtype, nullptr, s));
     if (workspace) {
         if (ws_bytes < need) return ATTN_ERR_WORKSPACE;
         if (reinterpret_cast<uintptr_t>(workspace) & 7u) return ATTN_ERR_ALIGN;

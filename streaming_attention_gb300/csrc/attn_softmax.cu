@@ -14,6 +14,13 @@
 // Scratch: [M][T + 1] (m, l) float pairs, the merged pair last (8 M (T + 1)
 // bytes, T = ceil(N / C)). Padded columns of the last chunk take -inf in the
 // maximum and 0 in the sum ("Kernel Notes & Checklist", gotchas ledger).
+//
+// Row-resident form (chunk 0): the same three steps with the reread served on
+// chip. The T <= 8 chunks of a row (256 * VPT columns each) are the CTAs of one
+// thread-block cluster; each keeps its chunk in registers, publishes its (m, l)
+// in shared memory, reads its peers' pairs through distributed shared memory,
+// merges them to the common maximum and normalizes its chunk from registers.
+// x is read once and y written once; no scratch.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -218,6 +225,149 @@ __global__ void __launch_bounds__(kSmThreads)
     }
 }
 
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// 16 raw bytes -> W floats (W = 16 / sizeof(T))
+template <typename T>
+__device__ __forceinline__ void unpack16(const uint4& a, float (&v)[16 / sizeof(T)]) {
+    if constexpr (sizeof(T) == 4) {
+        v[0] = __uint_as_float(a.x), v[1] = __uint_as_float(a.y), v[2] = __uint_as_float(a.z),
+        v[3] = __uint_as_float(a.w);
+    } else {
+        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+                v[2 * k] = __uint_as_float(w[k] << 16);
+                v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+            } else {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+                v[2 * k] = f.x, v[2 * k + 1] = f.y;
+            }
+        }
+    }
+}
+
+// Chunk blockIdx.x (= cluster rank) of row blockIdx.y; gridDim.x chunks per row.
+// kVec (N a multiple of 16 / sizeof(T)): each thread keeps its VPT values as the
+// raw 16-byte vectors it loaded (VPT * sizeof(T) / 4 registers) and widens them
+// in each pass; otherwise VPT floats.
+template <typename T, int VPT, bool kVec>
+__global__ void __launch_bounds__(kSmThreads, 3) attn_softmax_resident_kernel(const void* x, void* y, int N) {
+    constexpr int W = kVec ? 16 / (int)sizeof(T) : 1;
+    constexpr int NV = VPT / W;  // vectors (or scalars) per thread
+    __shared__ float red[8];
+    __shared__ float2 part;  // this chunk's (m, l), read by the whole cluster
+    const int chunk = blockIdx.x, row = blockIdx.y, T_ = gridDim.x;
+    const size_t base = (size_t)row * N;
+    const int c0 = chunk * VPT * kSmThreads;
+    using Raw = typename std::conditional<kVec, uint4, float>::type;
+    Raw raw[NV];
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        const int col = c0 + chunk_col<VPT, W>(v * W);
+        if constexpr (kVec) {
+            // with kVec the whole vector is in the row or wholly past it
+            raw[v] = col < N ? __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(x) + base + col))
+                             : make_uint4(0, 0, 0, 0);
+        } else {
+            raw[v] = col < N ? sm_load<T>(x, base + col) : 0.f;
+        }
+    }
+    // the values of vector v, times log2 e; padding columns -inf
+    auto values = [&](int v, float (&t)[W]) {
+        const int col = c0 + chunk_col<VPT, W>(v * W);
+        if constexpr (kVec) {
+            unpack16<T>(raw[v], t);
+        } else {
+            t[0] = raw[v];
+        }
+#pragma unroll
+        for (int k = 0; k < W; ++k) t[k] = col < N ? t[k] * kLog2e : -INFINITY;
+    };
+    float mx = -INFINITY;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        float t[W];
+        values(v, t);
+#pragma unroll
+        for (int k = 0; k < W; ++k) mx = fmaxf(mx, t[k]);
+    }
+    mx = block_reduce<true>(mx, red);  // finite: every chunk holds at least one column
+    float s = 0.f;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        float t[W];
+        values(v, t);
+#pragma unroll
+        for (int k = 0; k < W; ++k) s += exp2f(t[k] - mx);
+    }
+    s = block_reduce<false>(s, red);
+    if (threadIdx.x == 0) part = make_float2(mx, s);
+    cluster_sync_all();
+    // merge of the row's T pairs relative to their common maximum (the A1 rule)
+    const uint32_t local = (uint32_t)__cvta_generic_to_shared(&part);
+    float2 pr[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        pr[r] = make_float2(-INFINITY, 0.f);
+        if (r < T_) {
+            uint32_t a;
+            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(local), "r"(r));
+            asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(pr[r].x), "=f"(pr[r].y) : "r"(a) : "memory");
+        }
+    }
+    float gm = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) gm = fmaxf(gm, pr[r].x);
+    float L = 0.f;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) L += pr[r].x == -INFINITY ? 0.f : pr[r].y * exp2f(pr[r].x - gm);
+    const float inv = 1.f / L;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        const int col = c0 + chunk_col<VPT, W>(v * W);
+        if (col >= N) continue;
+        float t[W];
+        values(v, t);
+#pragma unroll
+        for (int k = 0; k < W; ++k) t[k] = exp2f(t[k] - gm) * inv;
+        if constexpr (kVec)
+            vstore<T, W>(y, base + col, t);
+        else
+            sm_store<T>(y, base + col, t[0]);
+    }
+    cluster_sync_all();  // every CTA keeps its pair until the whole cluster has read it
+}
+
+// Rows of at most 8 chunks: VPT = 16 up to 32768 columns, 64 up to 131072.
+template <typename T, int VPT>
+cudaError_t launch_resident_t(const void* x, void* y, int M, int N, cudaStream_t stream) {
+    const int C = VPT * kSmThreads, T_ = (N + C - 1) / C;
+    const bool vec = N % (16 / (int)sizeof(T)) == 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(T_, M);
+    cfg.blockDim = dim3(kSmThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)T_;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (vec) return cudaLaunchKernelEx(&cfg, attn_softmax_resident_kernel<T, VPT, true>, x, y, N);
+    return cudaLaunchKernelEx(&cfg, attn_softmax_resident_kernel<T, VPT, false>, x, y, N);
+}
+
+template <typename T>
+cudaError_t launch_resident(const void* x, void* y, int M, int N, cudaStream_t stream) {
+    if (N <= 8 * 16 * kSmThreads) return launch_resident_t<T, 16>(x, y, M, N, stream);
+    return launch_resident_t<T, 64>(x, y, M, N, stream);
+}
+
 template <typename T, int CPT>
 cudaError_t launch_sm_t(const void* x, void* y, int M, int N, float2* ws, cudaStream_t stream) {
     const int C = CPT * kSmThreads, T_ = (N + C - 1) / C;
@@ -248,15 +398,21 @@ cudaError_t launch_sm_c(const void* x, void* y, int M, int N, int chunk, float2*
 
 }  // namespace
 
-bool split_softmax_chunk_ok(int chunk) { return chunk == 256 || chunk == 1024 || chunk == 4096; }
+bool split_softmax_chunk_ok(int chunk) { return chunk == 0 || chunk == 256 || chunk == 1024 || chunk == 4096; }
 
 size_t split_softmax_ws_bytes(int M, int N, int chunk) {
+    if (chunk == 0) return 0;  // row-resident: no scratch
     const size_t T_ = ((size_t)N + chunk - 1) / chunk;
     return 8 * (size_t)M * (T_ + 1);
 }
 
 cudaError_t launch_split_softmax(const void* x, void* y, int M, int N, int chunk, int dtype, void* ws,
                                  cudaStream_t stream) {
+    if (chunk == 0) {
+        if (dtype == ATTN_FP32) return launch_resident<float>(x, y, M, N, stream);
+        if (dtype == ATTN_BF16) return launch_resident<__nv_bfloat16>(x, y, M, N, stream);
+        return launch_resident<__half>(x, y, M, N, stream);
+    }
     float2* w = static_cast<float2*>(ws);
     if (dtype == ATTN_FP32) return launch_sm_c<float>(x, y, M, N, chunk, w, stream);
     if (dtype == ATTN_BF16) return launch_sm_c<__nv_bfloat16>(x, y, M, N, chunk, w, stream);

@@ -157,6 +157,11 @@ def test_paged_workspace_bytes(L):
     assert paged(L, table=A4, lens=A4, B_=0) == 0
 
 
+def test_split_softmax_resident_needs_no_scratch(L):
+    assert sa.attn_split_softmax_workspace_bytes(1024, 131072, 0) == 0
+    assert sa.attn_split_softmax_workspace_bytes(1024, 131072, 4096) == 8 * 1024 * 33
+
+
 def test_split_softmax_scratch_matches_the_a2_worked_answer(L):
     import json
     fx = json.load(open(os.path.join(ROOT, "tests", "golden", "a2_split_softmax_example.json")))
@@ -171,6 +176,7 @@ def test_split_softmax_scratch_matches_the_a2_worked_answer(L):
     (dict(N=131073), -2),
     (dict(chunk=512), -2),
     (dict(M=20000, N=131072), -6),
+    (dict(M=70000, N=16), -2),       # more rows than one grid dimension holds
     (dict(x=None), -1),
     (dict(y=A8), -7),
 ])
