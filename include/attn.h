@@ -352,7 +352,9 @@ ATTN_API int attn_last_device_status(void* stream);
  * trap or hang: the context stays usable. The pages have no counterpart. */
 ATTN_API int attn_selftest_bounded_wait(unsigned timeout_us, void* stream);
 
-/* Library ABI version (major*100 + minor). */
+/* Library ABI version (major*100 + minor). 101 adds the E4M3 entry points
+ * (attn_fwd_fp8, attn_decode_paged_fp8 and their workspace queries), chunk 0
+ * of attn_split_softmax and attn_selftest_bounded_wait; nothing of 100 changed. */
 ATTN_API int attn_version(void);
 
 #ifdef __cplusplus

@@ -377,7 +377,7 @@ int attn_last_device_status(void* stream) {
     return word ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }
 
-int attn_version(void) { return 100; }
+int attn_version(void) { return 101; }
 
 }  // extern "C"
 
