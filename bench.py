@@ -409,6 +409,10 @@ def run_ours(args):
                           f"{per_set / 1e6:.0f} MB each (L2 {l2 / 1e6:.0f} MB)"),
                    "timing": "CUDA events around one CUDA-graph replay of K back-to-back C-ABI calls",
                    "eager_ms_per_step": round(eager_ms, 4),
+                   # causal prefill also counted the other common way (half the noncausal FLOPs)
+                   **({"tflops_as_noncausal_half": round(
+                       0.5 * 4.0 * w.D * w.B * w.Hq * w.M * w.N / (ms_max * 1e-3) / 1e12, 2)}
+                      if not decode and w.causal and w.window <= 0 else {}),
                    "cold_call_us": {"median": round(statistics.median(cold) * 1e3, 2),
                                     "samples": [round(x * 1e3, 2) for x in cold],
                                     "protocol": "graph replay of one call, L2 flushed (2x-L2 read) before each"}},
