@@ -11,11 +11,14 @@
 // the end.
 //
 // Each CTA streams one split (a run of 128-key tiles) of one KV head through a
-// 3-slot TMA ring, K and V tiles in the order the MMAs consume them, and
-// writes the split's unnormalized summary (m, l, acc) for its rows; the merge
-// kernel combines splits with the common-maximum rule ("Compare reasoning
-// after your own attempt", central-idea table, A1 and A2 rows). Masks, ghost
-// rows, lazy rescale and bounded waits follow the prefill kernel.
+// TMA ring (3 slots of 16-bit tiles, 6 of 8-bit tiles), K and V tiles in the
+// order the MMAs consume them, and forms the split's unnormalized summary
+// (m, l, acc) for its rows. The summaries are combined with the common-maximum
+// rule ("Compare reasoning after your own attempt", central-idea table, A1 and
+// A2 rows): when a KV head has at most 8 splits they form one thread-block
+// cluster and merge through distributed shared memory, each CTA writing some
+// of the output rows; otherwise they go to the workspace for the merge kernel.
+// Masks, ghost rows, lazy rescale and bounded waits follow the prefill kernel.
 #include <mutex>
 
 #include "attn_internal.h"

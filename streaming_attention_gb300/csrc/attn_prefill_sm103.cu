@@ -37,6 +37,10 @@
 // Every wait is bounded (1 s); on expiry the CTA raises an abort flag, sets
 // the device status word, drains its in-flight copies and MMAs, frees TMEM
 // and exits.
+//
+// The same kernel takes 8-bit E4M3 inputs (kIn = kInE4M3): both products run
+// as kind::f8f6f4 with 32-element K steps, a D = 128 row is one 128-byte
+// swizzle chunk, and P is rounded to E4M3, four per TMEM column.
 #include <mutex>
 
 #include "attn_internal.h"
