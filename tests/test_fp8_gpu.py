@@ -184,3 +184,23 @@ def test_fp8_rising_maximum_stress():
         got = o.reshape(-1, D)[torch.tensor(rows)].cpu()
         H_, sigma, wabs = row_bounds(qf, kf, vf, rows, causal, 0, 1.0 / np.sqrt(D))
         check_fp8(got, want, H_, sigma, wabs, torch.bfloat16, f"stress causal={causal}")
+
+
+@pytest.mark.parametrize("shape,causal,window,out_dtype", [
+    ((40, 16, 1, 1, 1000, 128), True, 0, torch.float16),     # 16 grouped rows (the widest softmax form), cluster merge
+    ((2, 8, 2, 4, 2500, 128), True, 600, torch.float16),     # speculative rows with a window
+    ((1, 8, 1, 2, 20000, 128), False, 0, torch.bfloat16),    # more than 8 splits: the merge kernel path
+])
+def test_fp8_decode_output_types_and_split_forms(shape, causal, window, out_dtype):
+    B, Hq, Hkv, M, N, D = shape
+    q, k, v = make_qkv_fp8(B, Hq, Hkv, M, N, D, 29, 1.0, 0.5, 1.5)
+    o, lse = sa.attention_fp8(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, window=window, k_descale=0.5,
+                              v_descale=1.5, out_dtype=out_dtype, with_lse=True, path=sa.PATH_DECODE)
+    torch.cuda.synchronize()
+    want, want_lse = oracle.attention_fp8(q, k, v, 1.0, 0.5, 1.5, causal=causal, window=window, with_lse=True)
+    H, sigma, wabs = bounds(deq(q, 1.0), deq(k, 0.5), deq(v, 1.5), causal, window, 1.0 / np.sqrt(D))
+    check_fp8(o, want, H, sigma, wabs, out_dtype, f"{shape} {out_dtype}")
+    g = lse.cpu().double().numpy()
+    assert np.array_equal(np.isneginf(g), np.isneginf(want_lse))
+    fin = np.isfinite(want_lse)
+    assert np.abs(g[fin] - want_lse[fin]).max() <= 2e-3
