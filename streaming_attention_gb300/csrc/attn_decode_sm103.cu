@@ -97,6 +97,12 @@ struct DecodeParams {
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
+// The closing barrier orders nothing in memory (the remote reads it protects have
+// returned their values): a relaxed arrival does not wait for this CTA's global
+// stores to complete, as a release would.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed;\n\tbarrier.cluster.wait;" ::: "memory");
+}
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -618,7 +624,7 @@ __global__ void __launch_bounds__(kDecThreads)
             }
         }
         // every CTA keeps its shared memory until the others have read it
-        cluster_sync_all();
+        cluster_sync_relaxed();
     }
 
     tc_fence_before();

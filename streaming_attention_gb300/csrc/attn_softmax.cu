@@ -228,6 +228,12 @@ __global__ void __launch_bounds__(kSmThreads)
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
+// The closing barrier orders nothing in memory (the remote reads it protects have
+// returned their values): a relaxed arrival does not wait for this CTA's global
+// stores to complete, as a release would.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed;\n\tbarrier.cluster.wait;" ::: "memory");
+}
 
 // 16 raw bytes -> W floats (W = 16 / sizeof(T))
 template <typename T>
@@ -339,7 +345,7 @@ __global__ void __launch_bounds__(kSmThreads, 3) attn_softmax_resident_kernel(co
         else
             sm_store<T>(y, base + col, t[0]);
     }
-    cluster_sync_all();  // every CTA keeps its pair until the whole cluster has read it
+    cluster_sync_relaxed();  // every CTA keeps its pair until the whole cluster has read it
 }
 
 // Rows of at most 8 chunks: VPT = 16 up to 32768 columns, 64 up to 131072.
