@@ -84,7 +84,8 @@ typedef enum {
     ATTN_PATH_AUTO = 0,
     ATTN_PATH_SIMT = 1,    /* CUDA-core streaming kernel, any supported D */
     ATTN_PATH_PREFILL = 2, /* warp-specialized TMA + tcgen05 + TMEM kernel, D in {64,128} */
-    ATTN_PATH_DECODE = 3   /* split-KV over grouped query heads, then the merge kernel */
+    ATTN_PATH_DECODE = 3   /* split-KV over grouped query heads; the splits merged in a thread-block
+                              cluster (at most 8 splits per KV head) or by the merge kernel */
 } attn_path_t;
 
 /* Forward attention, the spec entry point.
