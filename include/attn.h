@@ -88,7 +88,7 @@ typedef enum {
                               cluster (at most 8 splits per KV head) or by the merge kernel */
 } attn_path_t;
 
-/* Forward attention, the spec entry point.
+/* Forward attention, the library's main entry point.
  *   q [B,Hq,M,D], k/v [B,Hkv,N,D], o [B,Hq,M,D]: device pointers (see above).
  *   dtype: ATTN_BF16 or ATTN_FP16 for all four tensors.
  * Picks the path as ATTN_PATH_AUTO does. When that path needs workspace
