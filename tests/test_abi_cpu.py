@@ -224,3 +224,31 @@ def test_fp8_workspace_bytes(L):
     assert sa.attn_fwd_fp8_workspace_bytes(2, 32, 32, 4096, 4096, 128, True, 0, sa.PATH_AUTO) == 0
     p8 = sa.attn_decode_paged_fp8_workspace_bytes(8, 32, 8, 1, 128, 16, 512, 8192, True, 4096)
     assert p8 >= sa.attn_decode_paged_workspace_bytes(8, 32, 8, 1, 128, 16, 512, 8192, True, 4096) > 0
+
+
+def paged_fp8(L, q=A16, kp=A16, vp=A16, table=A16, lens=A16, o=A16, B_=2, Hq=8, Hkv=2, M=1, D=128, num_pages=4,
+              page_size=16, max_pages=2, max_seq_len=32, dtype=0):
+    return L.attn_decode_paged_fp8(q, kp, vp, table, lens, o, B_, Hq, Hkv, M, D, num_pages, page_size, max_pages,
+                                   max_seq_len, 1, 0, 0.0, 1.0, 1.0, 1.0, dtype, None, 0, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dtype=2), -3),               # the output is BF16 or FP16
+    (dict(page_size=48), -2),
+    (dict(Hq=6, Hkv=4), -5),
+    (dict(D=64), -4),
+    (dict(Hq=16, Hkv=2, M=3), -11),
+    (dict(kp=None), -1),
+    (dict(o=A8), -7),
+    (dict(B_=0), 0),                   # no rows: nothing to do, no launch
+])
+def test_paged_fp8_validation_status(L, kw, status):
+    assert paged_fp8(L, **kw) == status
+
+
+def test_fp8_workspace_queries_reject_bad_shapes(L):
+    assert sa.attn_fwd_fp8_workspace_bytes(-1, 32, 8, 1, 8192, 128, True, 0, sa.PATH_DECODE) == 0
+    assert sa.attn_fwd_fp8_workspace_bytes(8, 32, 8, 1, 8192, 128, True, 0, sa.PATH_SIMT) == 0
+    assert sa.attn_fwd_fp8_workspace_bytes(1, 64, 1, 1, 8192, 128, True, 0, sa.PATH_DECODE) == 0  # 64 rows > 16
+    assert sa.attn_decode_paged_fp8_workspace_bytes(8, 32, 8, 1, 64, 16, 512, 8192, True, 0) == 0  # D = 64
+    assert sa.attn_decode_paged_fp8_workspace_bytes(8, 32, 8, 1, 128, 48, 512, 8192, True, 0) == 0  # page 48
