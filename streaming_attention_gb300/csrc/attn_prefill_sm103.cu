@@ -242,8 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int t = 0; t < NQ; ++t) {
             mbar_init(bar.s_full(t), 1);
-            mbar_init(bar.p_full(t), 4 * 32);
-            mbar_init(bar.o_free(t), 4 * 32);
+            mbar_init(bar.p_full(t), 4);  // one arrival per softmax warp
+            mbar_init(bar.o_free(t), 4);
         }
         mbar_init(bar.o_final, 1);
         mbar_init(bar.drain, 1);
@@ -489,7 +489,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar.p_full(t));
+                __syncwarp();  // the warp's TMEM stores are ordered before lane 0's arrival
+                if (lane == 0) mbar_arrive(bar.p_full(t));
             }
             if (!ok) break;
 
@@ -513,7 +514,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // O_t may now take the next tile's first value product
             tc_fence_before();
-            mbar_arrive(bar.o_free(t));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar.o_free(t));
             if (row < p.M) {
                 uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
