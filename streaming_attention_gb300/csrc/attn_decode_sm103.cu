@@ -224,14 +224,14 @@ __global__ void __launch_bounds__(kDecThreads)
         }
         mbar_init(bar_s0, 1);
         mbar_init(bar_s0 + 8, 1);
-        mbar_init(bar_p0, 128);
-        mbar_init(bar_p0 + 8, 128);
+        mbar_init(bar_p0, 4);  // one arrival per softmax warp
+        mbar_init(bar_p0 + 8, 4);
         mbar_init(bar_free0, 1);
         mbar_init(bar_free0 + 8, 1);
         mbar_init(bar_o, 1);
-        mbar_init(bar_red0, 128);
-        mbar_init(bar_red0 + 8, 128);
-        mbar_init(bar_lred, 128);
+        mbar_init(bar_red0, 4);
+        mbar_init(bar_red0 + 8, 4);
+        mbar_init(bar_lred, 4);
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -454,7 +454,7 @@ __global__ void __launch_bounds__(kDecThreads)
                 for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
                 if (lane == 0) redj[warp * DNR + r] = x;
             }
-            mbar_arrive(bar_red0 + 8 * (j & 1));
+            if (lane == 0) mbar_arrive(bar_red0 + 8 * (j & 1));  // lane 0 wrote the warp's maxima
             if (!(ok = dwait_warp(bar_red0 + 8 * (j & 1), (j >> 1) & 1, abort_flag, p.status))) break;
             bool need_any = false;
             float alpha[RP];
@@ -508,7 +508,8 @@ __global__ void __launch_bounds__(kDecThreads)
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(bar_p0 + 8 * (j & 1));
+            __syncwarp();  // every lane's P^T bytes and TMEM stores before lane 0's arrival
+            if (lane == 0) mbar_arrive(bar_p0 + 8 * (j & 1));
         }
 
         // summary of this split: m (base 2), l, acc for the group's rows
@@ -527,7 +528,7 @@ __global__ void __launch_bounds__(kDecThreads)
                     if (lane == 0) lred[warp * DNR + r] = x;
                 }
             }
-            mbar_arrive(bar_lred);
+            if (lane == 0) mbar_arrive(bar_lred);  // lane 0 wrote the warp's row sums
             have = dwait_warp(bar_lred, 0, abort_flag, p.status);
         }
         if (have) {
