@@ -221,7 +221,7 @@ __device__ __forceinline__ BSetup bwd_setup(uint8_t* smem) {
         }
         for (int h = 0; h < 2; ++h) {
             mbar_init(b.st(h), 1);
-            mbar_init(b.pp(h), 8 * 32);
+            mbar_init(b.pp(h), 8);  // one arrival per elementwise warp
         }
         mbar_init(b.bar_done, 1);
         mbar_init(b.bar_drain, 1);
@@ -426,7 +426,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bs.pp(0));
+            __syncwarp();  // the warp's TMEM stores before lane 0's arrival
+            if ((threadIdx.x & 31) == 0) mbar_arrive(bs.pp(0));
             // ---- phase B: dS^T = P^T (dP^T - delta), packed over dP^T ----
             // (masked entries have P = 0 already)
             if (!(ok = bwait_warp(bs.st(1), it & 1, bs.abort_flag, p.status))) break;
@@ -456,7 +457,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bs.pp(1));
+            __syncwarp();  // the warp's TMEM stores before lane 0's arrival
+            if ((threadIdx.x & 31) == 0) mbar_arrive(bs.pp(1));
         }
         uint16_t* dk_row = reinterpret_cast<uint16_t*>(p.out0) + ((size_t)grp * p.N + key) * D;
         uint16_t* dv_row = reinterpret_cast<uint16_t*>(p.out1) + ((size_t)grp * p.N + key) * D;
@@ -636,7 +638,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bs.pp(0));
+            __syncwarp();  // the warp's TMEM stores before lane 0's arrival
+            if ((threadIdx.x & 31) == 0) mbar_arrive(bs.pp(0));
             // ---- phase B: dS = P (dP - delta), packed over dP ----
             if (!(ok = bwait_warp(bs.st(1), it & 1, bs.abort_flag, p.status))) break;
             tc_fence_after();
@@ -660,7 +663,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bs.pp(1));
+            __syncwarp();  // the warp's TMEM stores before lane 0's arrival
+            if ((threadIdx.x & 31) == 0) mbar_arrive(bs.pp(1));
         }
         uint16_t* dq_row = reinterpret_cast<uint16_t*>(p.out0) + ((size_t)bh * p.M + row) * D;
         const bool write = row < p.M;
