@@ -353,6 +353,20 @@ ATTN_API int attn_last_device_status(void* stream);
  * trap or hang: the context stays usable. The pages have no counterpart. */
 ATTN_API int attn_selftest_bounded_wait(unsigned timeout_us, void* stream);
 
+/* Failure-path self-test of the prefill kernel itself: runs the noncausal
+ * tcgen05 prefill (D = 128, dtype ATTN_BF16 / ATTN_FP16) on the caller's
+ * device buffers (as attn_fwd) with the softmax warps of query tile 0
+ * withholding their P-ready arrival at score tile `withhold_at` of each CTA's
+ * walk. The issuing thread's bounded wait (1 s) runs out, and every CTA that
+ * reaches that tile raises the abort flag, drains its copies and MMAs, frees
+ * TMEM and exits; attn_last_device_status then returns ATTN_ERR_TIMEOUT and the
+ * context stays usable. o is left unspecified. No fault, trap or hang.
+ * Returns a validation status (withhold_at < 0 or an empty problem:
+ * ATTN_ERR_SHAPE), ATTN_ERR_CUDA, or ATTN_OK once launched. */
+ATTN_API int attn_selftest_prefill_abort(const void* q, const void* k, const void* v, void* o,
+                                         int B, int Hq, int Hkv, int M, int N, int D, int dtype,
+                                         long long withhold_at, void* stream);
+
 /* Library ABI version (major*100 + minor). 101 adds the E4M3 entry points
  * (attn_fwd_fp8, attn_decode_paged_fp8 and their workspace queries), chunk 0
  * of attn_split_softmax and attn_selftest_bounded_wait; nothing of 100 changed. */

@@ -36,6 +36,7 @@ from .binding import (  # noqa: F401
     last_device_status,
     lib,
     selftest_bounded_wait,
+    selftest_prefill_abort,
     split_softmax,
     library_path,
     strerror,

@@ -86,6 +86,8 @@ def lib() -> ctypes.CDLL:
             L.attn_split_softmax.restype = ci
             L.attn_selftest_bounded_wait.argtypes = [ctypes.c_uint, vp]
             L.attn_selftest_bounded_wait.restype = ci
+            L.attn_selftest_prefill_abort.argtypes = [vp] * 4 + [ci] * 7 + [ctypes.c_longlong, vp]
+            L.attn_selftest_prefill_abort.restype = ci
             L.attn_version.argtypes = []
             L.attn_version.restype = ci
             _lib = L
@@ -375,6 +377,15 @@ def split_softmax(x, chunk=1024, y=None, workspace=None, stream=None) -> torch.T
 def selftest_bounded_wait(timeout_us=20000, stream=None) -> None:
     """C-ABI ``attn_selftest_bounded_wait``: a wait that runs out on purpose (no fault)."""
     _check(lib().attn_selftest_bounded_wait(int(timeout_us), _stream(stream)), "attn_selftest_bounded_wait")
+
+
+def selftest_prefill_abort(q, k, v, o, withhold_at=2, stream=None) -> None:
+    """C-ABI ``attn_selftest_prefill_abort``: the prefill kernel with one P-ready
+    arrival withheld, so every CTA takes its abort path (no fault)."""
+    B, Hq, Hkv, M, N, D = _dims(q, k, v, o)
+    _check(lib().attn_selftest_prefill_abort(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, Hq, Hkv, M, N, D,
+                                             _DTYPES[q.dtype], int(withhold_at), _stream(stream)),
+           "attn_selftest_prefill_abort")
 
 
 def last_device_status(stream=None) -> int:

@@ -120,6 +120,10 @@ int* device_status_ptr();
 int launch_prefill(const Problem& p, const void* q, const void* k, const void* v, void* o,
                    int* status, cudaStream_t stream);
 bool prefill_supported(const Problem& p);
+// The prefill kernel with one P-ready arrival withheld (failure-path self-test;
+// D = 128): its bounded waits run out and every CTA takes the abort path.
+int launch_prefill_withheld(const Problem& p, const void* q, const void* k, const void* v, void* o, int* status,
+                            long withhold_p_at, cudaStream_t stream);
 // The same kernel on E4M3 inputs (D = 128); p.dtype is the output type and
 // p.scale_log2 already includes the Q and K dequantization factors.
 int launch_prefill_e4m3(const Problem& p, const void* q, const void* k, const void* v, void* o, int* status,

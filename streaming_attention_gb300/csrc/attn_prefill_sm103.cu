@@ -96,6 +96,10 @@ struct PrefillParams {
     int BH;     // B * Hq
     int nqb;    // work tiles per head (ceil(M / 256))
     int tiles;  // BH * nqb
+    // failure-path self-test only (-1 otherwise): the softmax warps of query tile 0
+    // withhold their P-ready arrival for this score tile (counted over the CTA's walk),
+    // so the issuing thread's bounded wait runs out and the whole CTA takes its abort path
+    long withhold_p_at;
 };
 
 struct Bars {
@@ -490,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();  // the warp's TMEM stores are ordered before lane 0's arrival
-                if (lane == 0) mbar_arrive(bar.p_full(t));
+                if (lane == 0 && !(t == 0 && g == p.withhold_p_at)) mbar_arrive(bar.p_full(t));
             }
             if (!ok) break;
 
@@ -547,7 +551,7 @@ int sm_count_prefill() {
 
 template <int D, int kIn, bool kBF16>
 int launch_t(const Problem& pr, const void* q, const void* k, const void* v, void* o, int* status, float v_scale,
-             cudaStream_t stream) {
+             cudaStream_t stream, long withhold_p_at = -1) {
     constexpr int EB = kIn == kInE4M3 ? 1 : 2;
     using C = Cfg<D, EB>;
     static std::once_flag once;
@@ -578,6 +582,7 @@ int launch_t(const Problem& pr, const void* q, const void* k, const void* v, voi
     pp.BH = pr.B * pr.Hq;
     pp.nqb = (pr.M + NQ * BM - 1) / (NQ * BM);
     pp.tiles = pp.BH * pp.nqb;
+    pp.withhold_p_at = withhold_p_at;
     const int grid = pp.tiles < sm_count_prefill() ? pp.tiles : sm_count_prefill();
     attn_prefill_kernel<D, kIn, kBF16><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, pp);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
@@ -597,6 +602,14 @@ int launch_prefill(const Problem& p, const void* q, const void* k, const void* v
     if (p.D == 64) return bf16 ? launch_t<64, kInBF16, true>(p, q, k, v, o, status, 1.f, stream)
                                : launch_t<64, kInF16, false>(p, q, k, v, o, status, 1.f, stream);
     return ATTN_ERR_HEADDIM;
+}
+
+int launch_prefill_withheld(const Problem& p, const void* q, const void* k, const void* v, void* o, int* status,
+                            long withhold_p_at, cudaStream_t stream) {
+    if (p.D != 128) return ATTN_ERR_HEADDIM;
+    return p.dtype == ATTN_BF16
+               ? launch_t<128, kInBF16, true>(p, q, k, v, o, status, 1.f, stream, withhold_p_at)
+               : launch_t<128, kInF16, false>(p, q, k, v, o, status, 1.f, stream, withhold_p_at);
 }
 
 int launch_prefill_e4m3(const Problem& p, const void* q, const void* k, const void* v, void* o, int* status,

@@ -252,3 +252,13 @@ def test_fp8_workspace_queries_reject_bad_shapes(L):
     assert sa.attn_fwd_fp8_workspace_bytes(1, 64, 1, 1, 8192, 128, True, 0, sa.PATH_DECODE) == 0  # 64 rows > 16
     assert sa.attn_decode_paged_fp8_workspace_bytes(8, 32, 8, 1, 64, 16, 512, 8192, True, 0) == 0  # D = 64
     assert sa.attn_decode_paged_fp8_workspace_bytes(8, 32, 8, 1, 128, 48, 512, 8192, True, 0) == 0  # page 48
+
+
+def test_prefill_abort_selftest_validation(L):
+    # validation answers before any launch
+    st = L.attn_selftest_prefill_abort(A16, A16, A16, A16, 1, 2, 2, 64, 64, 64, 0, 1, None)
+    assert st == -4  # D must be 128
+    st = L.attn_selftest_prefill_abort(A16, A16, A16, A16, 1, 2, 2, 64, 64, 128, 0, -1, None)
+    assert st == -2
+    st = L.attn_selftest_prefill_abort(A16, A16, A16, A16, 1, 2, 2, 0, 64, 128, 0, 1, None)
+    assert st == -2
