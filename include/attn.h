@@ -246,7 +246,10 @@ ATTN_API int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, vo
  *   Every call, on any stream, shares the one array and leaves its contents
  *   behind: calls whose work may overlap on the GPU race and must be
  *   serialized by the caller (one stream, or events). Nothing in the array
- *   needs clearing: each call writes every summary it reads. */
+ *   needs clearing: each call writes every summary it reads. (When a KV head
+ *   has at most 8 splits -- D = 128 and enough KV heads, as in typical GQA
+ *   decode -- the splits merge inside their thread-block cluster and the
+ *   array is not touched at all.) */
 #define ATTN_NOALLOC_SCRATCH_BYTES (8u << 20)
 ATTN_API int attn_fwd_decode_noalloc(const void* q, const void* k, const void* v, void* o,
                                      int B, int Hq, int Hkv, int M, int N, int D,
