@@ -60,3 +60,35 @@ def test_single_rank_needs_no_process_group():
 
     ms_max, value = bench.whole_job(5e12, 10.0, 1, torch.device("cpu"), 1e12)
     assert ms_max == 10.0 and value == pytest.approx(500.0)
+
+
+def test_bench_launch_count_follows_the_library_split_plan():
+    """bench.py counts one launch per decode call when a KV head's splits fit a
+    cluster (<= 8) and two otherwise; its copy of the split plan must agree with
+    the library's, read back here from the workspace size the library asks for
+    (no GPU: the library plans for 148 SMs when it cannot query the device)."""
+    import bench
+    import streaming_attention_gb300 as sa
+    from streaming_attention_gb300 import build as B
+    from streaming_attention_gb300.inputs import DECODE_GQA
+
+    B.build()
+
+    def splits_from_workspace(w):
+        nb = sa.attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.M, w.N, w.D, w.causal, w.window, sa.PATH_DECODE)
+        rows, D = w.B * w.Hq * w.M, w.D
+        up = lambda x: (x + 255) // 256 * 256  # noqa: E731
+        for S in range(1, 4097):
+            if 2 * up(rows * S * 4) + up(rows * S * D * 4) == nb:
+                return S
+        raise AssertionError(f"no split count gives {nb} bytes")
+
+    # the SM count the library plans for: the device's, or 148 without one
+    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 148
+    cases = [DECODE_GQA, DECODE_GQA.with_(B=1, Hkv=1, Hq=8, N=9000, window=0),
+             DECODE_GQA.with_(B=2, Hkv=2, Hq=8, N=1000, window=0)]
+    for w in cases:
+        assert bench.decode_splits(w, sms) == splits_from_workspace(w), w
+    assert bench.path_launches("decode", DECODE_GQA, sms) == 1
+    assert bench.path_launches("decode", cases[1], sms) == 2
+    assert bench.path_launches("prefill_or_simt", DECODE_GQA, sms) == 1
