@@ -29,7 +29,8 @@
  *   Precision   FP16 or BF16 in and out, FP32 accumulation, one cast at the
  *               end (scope table: FP32 epilogue, then one output cast). P is
  *               rounded to the input type before the P.V product (contract
- *               notes under the scope table).
+ *               notes under the scope table). attn_fwd_fp8 and
+ *               attn_decode_paged_fp8 take E4M3 inputs instead (see there).
  *   Pointers    q, k, v, o are DEVICE pointers owned by the caller, 16-byte
  *               aligned; o must not overlap q, k or v. They may be NULL only
  *               when the tensor has zero elements.
