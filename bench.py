@@ -382,7 +382,7 @@ def run_ours(args):
         peak, bound, r_unit = pk["bf16_tflops"], "tensor", "TFLOP/s"
         if w.dtype == torch.float16:
             peak = pk["bf16_tflops"]  # fp16 and bf16 share the dense tensor rate
-    achieved = work / (ms * 1e-3) / scale  # per-rank step time: one launch (prefill) or split + merge (decode)
+    achieved = work / (ms * 1e-3) / scale  # per-rank step time: one launch (prefill; decode with <= 8 splits per KV head)
     traffic = stored_traffic(w.name)
 
     also = {}
