@@ -37,6 +37,9 @@
  *   Streams     `stream` is a cudaStream_t (NULL = legacy default stream).
  *               Every call is asynchronous on it and never synchronizes,
  *               except attn_fwd_host and attn_last_device_status.
+ *   Devices     calls run on the current CUDA device. Each kernel's shared-
+ *               memory limit is raised once per process, on the device of its
+ *               first launch: use one process per GPU (as torchrun does).
  *   Values      only metadata is validated, never values (scope notes: wrappers
  *               validate metadata but do not scan values); inputs must be
  *               finite. Every tensor's element count must fit a signed 32-bit
