@@ -262,3 +262,17 @@ def test_prefill_abort_selftest_validation(L):
     assert st == -2
     st = L.attn_selftest_prefill_abort(A16, A16, A16, A16, 1, 2, 2, 0, 64, 128, 0, 1, None)
     assert st == -2
+
+
+def test_host_entry_validation(L):
+    # device buffers validated as attn_fwd does, then the host pointers; no copy is started
+    args = [A16, A16, A16, A16, A16, A16, A16, A16, 1, 2, 2, 8, 8, 64, 0, 0, 0.0, 0, None, 0, None]
+    bad_host = list(args)
+    bad_host[0] = None  # q_h
+    assert L.attn_fwd_host(*bad_host) == -1
+    bad_dev = list(args)
+    bad_dev[4] = ctypes.c_void_p(0x10008)  # q_d misaligned
+    assert L.attn_fwd_host(*bad_dev) == -7
+    bad_shape = list(args)
+    bad_shape[9], bad_shape[10] = 6, 4  # Hq % Hkv != 0
+    assert L.attn_fwd_host(*bad_shape) == -5
