@@ -5,7 +5,6 @@ Gradient tolerance: every gradient element is a sum over up to M (or N) products
 of 16-bit-rounded operands (P, dS, dO, Q, K), so its error grows with its size:
 |got - want| <= atol + rtol * |want| elementwise with atol = rtol = 2e-2 (BF16)
 or 1e-2 (FP16), and the mean error at most 2e-3 * max(1, mean |want|)."""
-import math
 
 import numpy as np
 import pytest
