@@ -33,6 +33,11 @@ _SRC = os.path.join(_HERE, "attn_oracle.c")
 _LOCK = threading.Lock()
 _LIBS: dict = {}
 
+# Planted-mistake switch of the Python functions below, the counterpart of the
+# C source's ORACLE_MUTANT: 0 is the real oracle; the pin tests set another
+# value for the length of one test to show that each planted mistake fails a pin.
+PY_MUTANT = 0
+
 # -ffp-contract=off keeps the FP64 results identical on x86_64 and aarch64.
 CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off", "-fno-fast-math"]
 
@@ -190,12 +195,15 @@ class Oracle:
         lens = np.asarray(seq_lens, dtype=np.int64).reshape(-1)
         B, Hq, M, D = q.shape
         num_pages, Hkv, page_size, _ = kp.shape
-        cap = min(int(max_seq_len), table.shape[1] * page_size)
+        # 19 plants lengths that ignore max_seq_len
+        cap = table.shape[1] * page_size if PY_MUTANT == 19 else min(int(max_seq_len), table.shape[1] * page_size)
         o = np.zeros((B, Hq, M, D), dtype=np.float64)
         for b in range(B):
             L = int(min(max(lens[b], 0), cap))
             j = np.arange(L)
             pages, rows = table[b, j // page_size], j % page_size
+            if PY_MUTANT == 20:  # planted: pages taken in pool order, not through the table
+                pages = b * table.shape[1] + j // page_size
             kb = np.ascontiguousarray(kp[pages, :, rows, :].transpose(1, 0, 2))[None]  # [1, Hkv, L, D]
             vb = np.ascontiguousarray(vp[pages, :, rows, :].transpose(1, 0, 2))[None]
             o[b] = self.attention(q[b:b + 1], kb, vb, causal, window, scale, nthreads)[0]
@@ -254,7 +262,7 @@ def cpu_threads() -> int:
 # --------------------------------------------------------------------------
 def visible_mask(M, N, causal, window):
     """[M, N] boolean: key j visible to query row i (position i + N - M)."""
-    pos = np.arange(M)[:, None] + (N - M)
+    pos = np.arange(M)[:, None] + (0 if PY_MUTANT == 14 else N - M)  # 14 plants top-left alignment
     j = np.arange(N)[None, :]
     keep = np.ones((M, N), dtype=bool)
     if causal:
@@ -293,10 +301,16 @@ def attention_backward(q, k, v, do, causal=False, window=0, scale=None, heads=No
         e = np.where(keep, np.exp(s - np.where(any_key, mu, 0.0)), 0.0)
         z = e.sum(axis=1, keepdims=True)
         p = np.divide(e, z, out=np.zeros_like(e), where=z > 0)
-        dv[b, g] += p.T @ do[b, h]
+        if PY_MUTANT == 12:  # planted: a KV head keeps only its last query head's share
+            dv[b, g] = p.T @ do[b, h]
+        else:
+            dv[b, g] += p.T @ do[b, h]
         dp = do[b, h] @ v[b, g].T
-        ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
-        dq[b, h] = scale * (ds @ k[b, g])
+        if PY_MUTANT == 11:  # planted: the row-sum term of the softmax VJP dropped
+            ds = p * dp
+        else:
+            ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+        dq[b, h] = (1.0 if PY_MUTANT == 13 else scale) * (ds @ k[b, g])  # 13 plants a dropped scale
         dk[b, g] += scale * (ds.T @ q[b, h])
     return dq, dk, dv
 
@@ -312,6 +326,8 @@ def softmax_rows(x):
     if x.shape[0] == 0:
         return x.copy()
     e = np.exp(x - x.max(axis=1, keepdims=True))
+    if PY_MUTANT == 15:  # planted: normalized over columns instead of rows
+        return e / e.sum(axis=0, keepdims=True)
     return e / e.sum(axis=1, keepdims=True)
 
 
@@ -336,7 +352,9 @@ def decode_e4m3(codes) -> np.ndarray:
     sign = np.where(b & 0x80, -1.0, 1.0)
     e = (b >> 3) & 0xF
     m = (b & 0x7).astype(np.float64)
-    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2((e - 7).astype(np.float64)))
+    bias = 8 if PY_MUTANT == 16 else 7  # 16 plants a wrong exponent bias
+    lead = 1.0 if PY_MUTANT == 17 else 0.0  # 17 plants an implicit one on subnormals
+    mag = np.where(e == 0, (lead + m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2((e - bias).astype(np.float64)))
     mag = np.where((e == 15) & (b & 0x7 == 7), np.nan, mag)
     return sign * mag
 
@@ -348,7 +366,7 @@ def attention_fp8(q, k, v, q_descale=1.0, k_descale=1.0, v_descale=1.0, causal=F
     attention (and log-sum-exp) of those tensors."""
     qd = float(q_descale) * decode_e4m3(q)
     kd = float(k_descale) * decode_e4m3(k)
-    vd = float(v_descale) * decode_e4m3(v)
+    vd = (1.0 if PY_MUTANT == 18 else float(v_descale)) * decode_e4m3(v)  # 18 plants a dropped V factor
     if with_lse:
         return attention_lse(qd, kd, vd, causal, window, scale, nthreads)
     return attention(qd, kd, vd, causal, window, scale, nthreads)

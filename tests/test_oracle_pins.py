@@ -71,3 +71,32 @@ def test_planted_mistake_is_caught(mutant, mutant_dir):
         except (AssertionError, ValueError, IndexError):
             failed.append(pin.__name__)
     assert failed, f"mutant {mutant} ({MUTANTS[mutant]}) passed every pin"
+
+
+# Planted mistakes in the Python functions (oracle.PY_MUTANT = n), each of
+# which must also fail at least one pin.
+PY_MUTANTS = {
+    11: "backward: softmax VJP without its row-sum term",
+    12: "backward: GQA dk/dv keep one query head's share",
+    13: "backward: dq without the scale",
+    14: "backward: top-left causal alignment",
+    15: "row softmax normalized over columns",
+    16: "E4M3 exponent bias 8",
+    17: "E4M3 subnormals with an implicit one",
+    18: "E4M3 attention drops the V factor",
+    19: "paged: lengths not cut at max_seq_len",
+    20: "paged: pages taken in pool order, not through the block table",
+}
+
+
+@pytest.mark.parametrize("mutant", sorted(PY_MUTANTS), ids=lambda n: f"m{n}")
+def test_planted_python_mistake_is_caught(mutant, oracle_lib, monkeypatch):
+    monkeypatch.setattr(oracle, "PY_MUTANT", mutant)
+    failed = []
+    for pin in P.ALL_PINS:
+        try:
+            with np.errstate(all="ignore"):
+                pin(oracle_lib)
+        except (AssertionError, ValueError, IndexError):
+            failed.append(pin.__name__)
+    assert failed, f"mutant {mutant} ({PY_MUTANTS[mutant]}) passed every pin"
