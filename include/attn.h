@@ -83,10 +83,14 @@ typedef enum {
 
 /* Kernel paths. AUTO picks: split-KV decode when (Hq/Hkv)*M <= 16 and the
  * visible key range is long; the tcgen05 prefill kernel for D in {64, 128};
- * the SIMT kernel otherwise (D in {16, 32, 64, 128}). */
+ * the SIMT kernel otherwise (D in {16, 32, 64, 128}).
+ * The SIMT kernel, which also runs split decode for D = 64, for more than 16
+ * grouped rows and for B*Hkv > 65535, and the log-sum-exp of an N == 0 call,
+ * takes at most 65535 (batch, query head) pairs: B*Hq > 65535 there returns
+ * ATTN_ERR_PATH (AUTO then prefers the prefill kernel for D in {64, 128}). */
 typedef enum {
     ATTN_PATH_AUTO = 0,
-    ATTN_PATH_SIMT = 1,    /* CUDA-core streaming kernel, any supported D */
+    ATTN_PATH_SIMT = 1,    /* CUDA-core streaming kernel, any supported D, B*Hq <= 65535 */
     ATTN_PATH_PREFILL = 2, /* warp-specialized TMA + tcgen05 + TMEM kernel, D in {64,128} */
     ATTN_PATH_DECODE = 3   /* split-KV over grouped query heads; the splits merged in a thread-block
                               cluster (at most 8 splits per KV head) or by the merge kernel */

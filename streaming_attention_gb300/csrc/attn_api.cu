@@ -76,7 +76,9 @@ bool empty_output(const Problem& p) { return (int64_t)p.B * p.Hq * p.M == 0; }
 
 int choose_path(const Problem& p, int path) {
     if (path != ATTN_PATH_AUTO) return path;
-    if (decode_supported(p) && (int64_t)p.G * p.M <= 16 && (p.khi - p.klo) >= 512) return ATTN_PATH_DECODE;
+    if (decode_supported(p) && (int64_t)p.G * p.M <= 16 && (p.khi - p.klo) >= 512 &&
+        (decode_tc_supported(p) || simt_grid_ok(p)))
+        return ATTN_PATH_DECODE;
     if (prefill_supported(p)) return ATTN_PATH_PREFILL;
     return ATTN_PATH_SIMT;
 }
@@ -95,6 +97,9 @@ int run(const Problem& p, const void* q, const void* k, const void* v, void* o, 
     if (path == ATTN_PATH_PREFILL && p.D != 64 && p.D != 128) return ATTN_ERR_HEADDIM;
     if (path == ATTN_PATH_DECODE && !decode_supported(p)) return ATTN_ERR_HEADDIM;
     if (empty_output(p)) return ATTN_OK;
+    const bool simt = p.N == 0 ? p.lse != nullptr
+                               : path == ATTN_PATH_SIMT || (path == ATTN_PATH_DECODE && !decode_tc_supported(p));
+    if (simt && !simt_grid_ok(p)) return ATTN_ERR_PATH;
     if (p.N == 0) {  // every row sees no key: output 0 (and a log-sum-exp of -inf)
         if (p.lse) return cuda_status(launch_simt(p, q, k, v, o, 0, 1, nullptr, stream));
         const size_t bytes = (size_t)p.B * p.Hq * p.M * p.D * 2;

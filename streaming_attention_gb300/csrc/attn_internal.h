@@ -33,6 +33,11 @@ __host__ __device__ inline void key_range(int p, int N, int causal, int window, 
     *hi = h;
 }
 
+// The CUDA-core kernel (the SIMT path, and split decode of shapes the tcgen05
+// split kernel does not take) runs one (batch, query head) per grid y index,
+// whose limit is 65535.
+inline bool simt_grid_ok(const Problem& p) { return (long long)p.B * p.Hq <= 65535; }
+
 // Split-KV workspace: the union key range [klo, khi) is cut into S chunks of
 // `chunk` keys (a multiple of 128) starting at split_base(p); partial summaries are [rows][S] floats m and l (m in base-2
 // logit units) and [rows][S][D] floats acc. Each part is 256-byte aligned.

@@ -60,6 +60,7 @@ extern "C" int attn_fwd_decode_noalloc(const void* q, const void* k, const void*
         const size_t bytes = (size_t)p.B * p.Hq * p.M * p.D * 2;
         return cudaMemsetAsync(o, 0, bytes, s) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
     }
+    if (!decode_tc_supported(p) && !simt_grid_ok(p)) return ATTN_ERR_PATH;
     int chunk = 0, S = 0;
     rc = decode_plan(p, &chunk, &S);
     if (rc != ATTN_OK) return rc;

@@ -81,6 +81,20 @@ def test_forced_path_checks(L):
         assert st == -4, path
 
 
+def test_simt_grid_limit(L):
+    # the CUDA-core kernel takes at most 65535 (batch, query head) pairs; the
+    # check comes before any launch
+    for D in (16, 32):  # AUTO has no other kernel for these head dimensions
+        assert fwd(L, B_=1, Hq=65536, Hkv=65536, M=1, N=8, D=D) == -11, D
+    args = (A16, A16, A16, A16, 1, 65536, 65536, 1, 256, 64, 0, 0, 0.0, 0)
+    assert L.attn_fwd_ex(*args, sa.PATH_SIMT, None, 0, None) == -11
+    assert L.attn_fwd_ex(*args, sa.PATH_DECODE, None, 0, None) == -11  # D = 64 splits run on it too
+    assert L.attn_fwd_decode_noalloc(*args, None) == -11
+    # AUTO leaves decode to the prefill kernel when the split kernel would not fit
+    assert sa.attn_workspace_bytes(1, 4096, 4096, 1, 512, 64, 0, 0, sa.PATH_AUTO) > 0
+    assert sa.attn_workspace_bytes(1, 65536, 4096, 1, 512, 64, 0, 0, sa.PATH_AUTO) == 0
+
+
 def test_workspace_bytes(L):
     # prefill and SIMT need none; decode needs room for its split summaries
     assert sa.attn_workspace_bytes(2, 32, 32, 4096, 4096, 128, True, 0, sa.PATH_SIMT) == 0
