@@ -223,7 +223,8 @@ ATTN_API int attn_merge(const float* m, const float* l, const float* acc, void* 
  * groups whose copies run on two internal copy streams, overlapping the
  * kernels of other chunks on `stream` (the copies wait for the work already
  * queued on `stream`); the decode path copies, computes and copies back in
- * order on `stream`. Calls from several host threads are serialized.
+ * order on `stream`. Chunked calls from several host threads are serialized
+ * (they share the internal copy streams and events).
  *   *_h: host pointers (pinned memory gives asynchronous copies);
  *   *_d: device buffers of the same sizes, owned by the caller;
  *   workspace/ws_bytes: as attn_fwd_ex (may be NULL/0 when none is needed).
