@@ -390,6 +390,17 @@ def pin_backward_i2_example(orc):
     assert np.allclose(dk.reshape(-1), fx["dx"], rtol=0, atol=fx["tol"])
     assert np.allclose(dv.reshape(-1), y, rtol=0, atol=1e-15)            # dv = P^T do
     assert abs(dq.reshape(-1)[0] - float(np.dot(fx["dx"], np.log(y)))) < 1e-12  # dq = dS k
+    # the same worked answer's second point: a gradient that is constant along
+    # a row (here dP = do . v_j, constant when every value row is the same)
+    # gives a zero logit gradient, since the weights sum to one; so dq = dk = 0,
+    # with every mask and GQA, while dv = P^T do stays nonzero
+    for causal, window, Hq, Hkv in ((False, 0, 2, 1), (True, 0, 2, 2), (True, 3, 4, 2)):
+        q, k = _rand((1, Hq, 5, 3), 61), _rand((1, Hkv, 6, 3), 62)
+        v = np.broadcast_to(_rand((1, Hkv, 1, 3), 63), (1, Hkv, 6, 3)).copy()
+        do = _rand((1, Hq, 5, 3), 64)
+        dq, dk, dv = orc_backward(q, k, v, do, causal, window, 1.0 / math.sqrt(3))
+        assert np.abs(dq).max() < 1e-13 and np.abs(dk).max() < 1e-13, (causal, window)
+        assert np.abs(dv).max() > 0.1
 
 
 def orc_backward(q, k, v, do, causal, window, scale):
