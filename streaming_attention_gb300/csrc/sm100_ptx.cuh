@@ -50,20 +50,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Non-blocking test: true once the phase with the given parity has completed
-// (never suspends the thread, unlike try_wait).
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // ---------------------------------------------------------------------------
 // TMA (bulk tensor copies global -> shared, completion on an mbarrier)
 // ---------------------------------------------------------------------------
@@ -194,11 +180,6 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool b_mn_major,
 // proxy (TMA, tensor core) before it signals them.
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Barrier among `count` threads of the CTA (ids 1..15; 0 is __syncthreads).
-__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 __device__ __forceinline__ float ex2(float x) {
