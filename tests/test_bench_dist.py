@@ -92,3 +92,40 @@ def test_bench_launch_count_follows_the_library_split_plan():
     assert bench.path_launches("decode", DECODE_GQA, sms) == 1
     assert bench.path_launches("decode", cases[1], sms) == 2
     assert bench.path_launches("prefill_or_simt", DECODE_GQA, sms) == 1
+
+
+def _run_bench(args, env_extra=None):
+    import json
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, **(env_extra or {}))
+    r = subprocess.run([sys.executable, "bench.py", *args], cwd=root, env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    return [json.loads(ln) for ln in lines]
+
+
+@pytest.mark.parametrize("workload,unit", [("tiny_b1_h2_64x64_d64_bf16", "TFLOP/s"),
+                                           ("decode_gqa_b8_hq32_hkv8_m1_n8192_w4096_d128_bf16", "GB/s")])
+def test_reference_arm_prints_one_contract_line(workload, unit):
+    """The reference arm (the FP64 oracle on the host cores) needs no GPU: one
+    JSON line with the contract's keys, in the unit of the workload's metric."""
+    (line,) = _run_bench(["--impl", "reference", "--steps", "1", "--warmup", "3", "--cpu-seconds", "1",
+                          "--workload", workload])
+    assert line["impl"] == "reference" and line["unit"] == unit and line["value"] > 0
+    for key in ("metric", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling", "dtype",
+                "data", "config"):
+        assert key in line, key
+    assert line["steps"] == 1 and line["warmup"] == 3 and line["vs_baseline"] is None
+    assert line["config"]["workload"] == workload
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_print_nothing():
+    assert _run_bench(["--impl", "reference", "--steps", "1", "--warmup", "3", "--cpu-seconds", "1",
+                       "--workload", "tiny_b1_h2_64x64_d64_bf16"], {"RANK": "1", "WORLD_SIZE": "2"}) == []
