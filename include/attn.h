@@ -249,7 +249,9 @@ ATTN_API int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, vo
  *   Arguments, layout and errors are those of attn_fwd; the caller still
  *   provides q, k, v and o. D must be 64 or 128.
  *   Returns ATTN_ERR_WORKSPACE when the problem's split summaries
- *   (attn_workspace_bytes(..., ATTN_PATH_DECODE)) exceed the array.
+ *   (attn_workspace_bytes(..., ATTN_PATH_DECODE)) exceed the array, and
+ *   ATTN_ERR_PATH when the splits would run on the SIMT kernel (D = 64, or
+ *   more than 16 grouped rows) with B*Hq > 65535.
  *   The first call on a device looks up the array's device address (with
  *   that device current); make that first call before any stream capture.
  *   Every call, on any stream, shares the one array and leaves its contents
