@@ -31,15 +31,20 @@
  *               rounded to the input type before the P.V product (contract
  *               notes under the scope table). attn_fwd_fp8 and
  *               attn_decode_paged_fp8 take E4M3 inputs instead (see there).
+ *   dtype       every dtype / out_dtype argument is an attn_dtype_t (an
+ *               int-sized enum): ATTN_BF16 or ATTN_FP16, and ATTN_FP32 where an
+ *               entry point says so.
  *   Pointers    q, k, v, o are DEVICE pointers owned by the caller, 16-byte
  *               aligned; o must not overlap q, k or v. They may be NULL only
  *               when the tensor has zero elements.
- *   Streams     `stream` is a cudaStream_t (NULL = legacy default stream).
+ *   Streams     `stream` is a cudaStream_t passed as void* so that this header
+ *               needs no CUDA header (NULL = legacy default stream).
  *               Every call is asynchronous on it and never synchronizes,
  *               except attn_fwd_host and attn_last_device_status.
- *   Devices     calls run on the current CUDA device. Each kernel's shared-
- *               memory limit is raised once per process, on the device of its
- *               first launch: use one process per GPU (as torchrun does).
+ *   Devices     calls run on the current CUDA device. Per-device setup (kernel
+ *               shared-memory limits, the SM count, the status word's address)
+ *               happens on the first call with that device current, so one
+ *               process may drive several GPUs.
  *   Values      only metadata is validated, never values (scope notes: wrappers
  *               validate metadata but do not scan values); inputs must be
  *               finite. Every tensor's element count must fit a signed 32-bit
@@ -75,7 +80,7 @@ typedef enum {
     ATTN_ERR_GQA = -5,       /* Hq is not a multiple of Hkv */
     ATTN_ERR_OVERFLOW = -6,  /* an element count does not fit a signed 32-bit index */
     ATTN_ERR_ALIGN = -7,     /* a pointer is not 16-byte aligned */
-    ATTN_ERR_WORKSPACE = -8, /* workspace NULL or smaller than attn_workspace_bytes() */
+    ATTN_ERR_WORKSPACE = -8, /* workspace NULL or smaller than the size query returns */
     ATTN_ERR_CUDA = -9,      /* a CUDA runtime/driver call failed (launch, copy, ...) */
     ATTN_ERR_TIMEOUT = -10,  /* a kernel gave up on a bounded wait (see attn_last_device_status) */
     ATTN_ERR_PATH = -11      /* the requested path cannot run this problem */
@@ -106,22 +111,52 @@ typedef enum {
  * Returns ATTN_OK or a negative status. */
 ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o,
                       int B, int Hq, int Hkv, int M, int N, int D,
-                      int causal, int window, float scale, int dtype, void* stream);
+                      int causal, int window, float scale, attn_dtype_t dtype, void* stream);
+
+/* Per-call scratch. The split-KV decode path keeps one partial summary
+ * (m, l, acc[D]) per (query row, split) in device scratch that lives for one
+ * call, the same arrangement as the course's wide-row split softmax
+ * ("Intermediate and advanced kernel workshops", level table, A2: three
+ * ordered kernels with per-call scratch; answer key, worked answer A2, where
+ * 4 rows x 33 chunks need 1088 scratch bytes). The caller may own that scratch
+ * (attn_fwd_ws, attn_fwd_ex) instead of having attn_fwd allocate it.
+ * Layout: three 256-byte-aligned parts, m[rows][S] and l[rows][S] (float,
+ * m in base-2 logit units) and acc[rows][S][D] (float), rows = B*Hq*M, S the
+ * number of splits the library plans for the problem. */
+
+/* Bytes of workspace attn_fwd_ws needs for a problem of these sizes (the path
+ * attn_fwd would take), enough for either value of `causal`; 0 when that path
+ * needs none, for empty problems and for invalid shapes. */
+ATTN_API size_t attn_workspace_bytes(int B, int Hq, int Hkv, int M, int N, int D, int window);
+
+/* attn_fwd with caller-owned device workspace instead of a stream-ordered
+ * allocation: the same path choice (ATTN_PATH_AUTO) and the same result.
+ *   workspace: device memory of at least attn_workspace_bytes(B, Hq, Hkv, M,
+ *         N, D, window) bytes, 16-byte aligned; NULL (with ws_bytes 0) is
+ *         allowed when that size is 0. A smaller or missing workspace on a
+ *         path that needs one returns ATTN_ERR_WORKSPACE with nothing
+ *         launched. The memory must stay untouched until the work queued on
+ *         `stream` has finished; its contents need no clearing. */
+ATTN_API int attn_fwd_ws(const void* q, const void* k, const void* v, void* o,
+                         int B, int Hq, int Hkv, int M, int N, int D,
+                         int causal, int window, float scale, attn_dtype_t dtype,
+                         void* workspace, size_t ws_bytes, void* stream);
 
 /* Bytes of caller workspace that attn_fwd_ex needs for this problem on this
  * path (0 when the path needs none). Returns 0 for invalid shapes too. */
-ATTN_API size_t attn_workspace_bytes(int B, int Hq, int Hkv, int M, int N, int D,
-                                     int causal, int window, int path);
+ATTN_API size_t attn_workspace_bytes_ex(int B, int Hq, int Hkv, int M, int N, int D,
+                                        int causal, int window, int path);
 
 /* attn_fwd with an explicit path and caller-owned device workspace.
  *   path: an attn_path_t; a forced path that cannot run the problem returns
  *         ATTN_ERR_PATH (or ATTN_ERR_HEADDIM for an unsupported D).
- *   workspace: device memory of at least attn_workspace_bytes(...) bytes,
- *         16-byte aligned, or NULL when that is 0. It must stay untouched
- *         until the work queued on `stream` has finished. */
+ *   workspace: device memory of at least attn_workspace_bytes_ex(...) bytes
+ *         for the same problem and path, 16-byte aligned, or NULL when that
+ *         is 0. It must stay untouched until the work queued on `stream` has
+ *         finished. */
 ATTN_API int attn_fwd_ex(const void* q, const void* k, const void* v, void* o,
                          int B, int Hq, int Hkv, int M, int N, int D,
-                         int causal, int window, float scale, int dtype, int path,
+                         int causal, int window, float scale, attn_dtype_t dtype, int path,
                          void* workspace, size_t ws_bytes, void* stream);
 
 /* attn_fwd_ex that also writes each row's log-sum-exp of its logits,
@@ -136,7 +171,7 @@ ATTN_API int attn_fwd_ex(const void* q, const void* k, const void* v, void* o,
  *        (cudaMallocAsync / cudaFreeAsync) as attn_fwd does. */
 ATTN_API int attn_fwd_lse(const void* q, const void* k, const void* v, void* o, float* lse,
                           int B, int Hq, int Hkv, int M, int N, int D,
-                          int causal, int window, float scale, int dtype, int path,
+                          int causal, int window, float scale, attn_dtype_t dtype, int path,
                           void* workspace, size_t ws_bytes, void* stream);
 
 /* Forward pass on 8-bit E4M3 inputs (the OCP 8-bit floating-point E4M3
@@ -175,7 +210,7 @@ ATTN_API int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, 
                           int B, int Hq, int Hkv, int M, int N, int D,
                           int causal, int window, float scale,
                           float q_descale, float k_descale, float v_descale,
-                          int out_dtype, int path, void* workspace, size_t ws_bytes, void* stream);
+                          attn_dtype_t out_dtype, int path, void* workspace, size_t ws_bytes, void* stream);
 
 /* Backward pass: gradients of L = sum(dO * O) for O = attention(Q, K, V).
  * Each row of the weight gradient is the softmax vector-Jacobian product of
@@ -197,7 +232,7 @@ ATTN_API size_t attn_bwd_workspace_bytes(int B, int Hq, int M);
 ATTN_API int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* d_o,
                       const float* lse, void* dq, void* dk, void* dv,
                       int B, int Hq, int Hkv, int M, int N, int D,
-                      int causal, int window, float scale, int dtype,
+                      int causal, int window, float scale, attn_dtype_t dtype,
                       void* workspace, size_t ws_bytes, void* stream);
 
 /* Merge of split summaries, the pages' common-maximum rule (answer key,
@@ -213,7 +248,7 @@ ATTN_API int attn_bwd(const void* q, const void* k, const void* v, const void* o
  *   merged summary.
  * rows >= 0, 1 <= S <= 4096, 1 <= D <= 256. */
 ATTN_API int attn_merge(const float* m, const float* l, const float* acc, void* o,
-                        float* m_out, float* l_out, int rows, int S, int D, int out_dtype,
+                        float* m_out, float* l_out, int rows, int S, int D, attn_dtype_t out_dtype,
                         void* stream);
 
 /* End-to-end call on HOST buffers: copies q, k, v from host memory into the
@@ -232,7 +267,7 @@ ATTN_API int attn_merge(const float* m, const float* l, const float* acc, void* 
 ATTN_API int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h,
                            void* q_d, void* k_d, void* v_d, void* o_d,
                            int B, int Hq, int Hkv, int M, int N, int D,
-                           int causal, int window, float scale, int dtype,
+                           int causal, int window, float scale, attn_dtype_t dtype,
                            void* workspace, size_t ws_bytes, void* stream);
 
 /* Split-KV decode forward that allocates no memory.
@@ -249,7 +284,8 @@ ATTN_API int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, vo
  *   Arguments, layout and errors are those of attn_fwd; the caller still
  *   provides q, k, v and o. D must be 64 or 128.
  *   Returns ATTN_ERR_WORKSPACE when the problem's split summaries
- *   (attn_workspace_bytes(..., ATTN_PATH_DECODE)) exceed the array, and
+ *   (attn_workspace_bytes_ex(..., ATTN_PATH_DECODE)) exceed the array and the
+ *   splits do not merge inside their cluster (see below), and
  *   ATTN_ERR_PATH when the splits would run on the SIMT kernel (D = 64, or
  *   more than 16 grouped rows) with B*Hq > 65535.
  *   The first call on a device looks up the array's device address (with
@@ -257,14 +293,16 @@ ATTN_API int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, vo
  *   Every call, on any stream, shares the one array and leaves its contents
  *   behind: calls whose work may overlap on the GPU race and must be
  *   serialized by the caller (one stream, or events). Nothing in the array
- *   needs clearing: each call writes every summary it reads. (When a KV head
- *   has at most 8 splits -- D = 128 and enough KV heads, as in typical GQA
- *   decode -- the splits merge inside their thread-block cluster and the
- *   array is not touched at all.) */
+ *   needs clearing: each call writes every summary it reads, including an
+ *   empty one for a split that sees no key or gives up on a bounded wait (the
+ *   output is then unspecified and attn_last_device_status reports it). When
+ *   a KV head has at most 8 splits -- D = 128 and enough KV heads, as in
+ *   typical GQA decode -- the splits merge inside their thread-block cluster,
+ *   the array is not touched at all, and its size does not limit the problem. */
 #define ATTN_NOALLOC_SCRATCH_BYTES (8u << 20)
 ATTN_API int attn_fwd_decode_noalloc(const void* q, const void* k, const void* v, void* o,
                                      int B, int Hq, int Hkv, int M, int N, int D,
-                                     int causal, int window, float scale, int dtype, void* stream);
+                                     int causal, int window, float scale, attn_dtype_t dtype, void* stream);
 
 /* Split-KV decode over a PAGED KV cache: the KV-cache slice of the course's
  * plan ("Kernel Notes & Checklist", section 3, the plan, week +3: sliding
@@ -308,7 +346,7 @@ ATTN_API int attn_decode_paged(const void* q, const void* k_pages, const void* v
                                const int* block_table, const int* seq_lens, void* o,
                                int B, int Hq, int Hkv, int M, int D,
                                int num_pages, int page_size, int max_pages, int max_seq_len,
-                               int causal, int window, float scale, int dtype,
+                               int causal, int window, float scale, attn_dtype_t dtype,
                                void* workspace, size_t ws_bytes, void* stream);
 
 /* attn_decode_paged on an E4M3 cache: q and both pools hold E4M3 bytes (the
@@ -326,7 +364,7 @@ ATTN_API int attn_decode_paged_fp8(const void* q, const void* k_pages, const voi
                                    int B, int Hq, int Hkv, int M, int D, int num_pages,
                                    int page_size, int max_pages, int max_seq_len,
                                    int causal, int window, float scale,
-                                   float q_descale, float k_descale, float v_descale, int out_dtype,
+                                   float q_descale, float k_descale, float v_descale, attn_dtype_t out_dtype,
                                    void* workspace, size_t ws_bytes, void* stream);
 
 /* Wide-row split softmax, the course's workshop A2 ("Intermediate and advanced
@@ -349,7 +387,7 @@ ATTN_API int attn_decode_paged_fp8(const void* q, const void* k_pages, const voi
  *         allocated stream-ordered; none for chunk 0 (workspace ignored).
  *         Values are not validated; x must be finite. */
 ATTN_API size_t attn_split_softmax_workspace_bytes(int M, int N, int chunk);
-ATTN_API int attn_split_softmax(const void* x, void* y, int M, int N, int chunk, int dtype,
+ATTN_API int attn_split_softmax(const void* x, void* y, int M, int N, int chunk, attn_dtype_t dtype,
                                 void* workspace, size_t ws_bytes, void* stream);
 
 /* Human-readable text for a status code (static storage). */
@@ -378,12 +416,14 @@ ATTN_API int attn_selftest_bounded_wait(unsigned timeout_us, void* stream);
  * Returns a validation status (withhold_at < 0 or an empty problem:
  * ATTN_ERR_SHAPE), ATTN_ERR_CUDA, or ATTN_OK once launched. */
 ATTN_API int attn_selftest_prefill_abort(const void* q, const void* k, const void* v, void* o,
-                                         int B, int Hq, int Hkv, int M, int N, int D, int dtype,
+                                         int B, int Hq, int Hkv, int M, int N, int D, attn_dtype_t dtype,
                                          long long withhold_at, void* stream);
 
-/* Library ABI version (major*100 + minor). 101 adds the E4M3 entry points
- * (attn_fwd_fp8, attn_decode_paged_fp8 and their workspace queries), chunk 0
- * of attn_split_softmax and attn_selftest_bounded_wait; nothing of 100 changed. */
+/* Library ABI version (major*100 + minor). 200: attn_workspace_bytes takes the
+ * seven size arguments of attn_fwd_ws (the former nine-argument query is now
+ * attn_workspace_bytes_ex), attn_fwd_ws is added, and dtype arguments are
+ * typed attn_dtype_t (same size and values as before). 101 added the E4M3
+ * entry points, chunk 0 of attn_split_softmax and attn_selftest_bounded_wait. */
 ATTN_API int attn_version(void);
 
 #ifdef __cplusplus

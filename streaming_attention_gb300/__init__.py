@@ -26,6 +26,7 @@ from .binding import (  # noqa: F401
     attn_fwd,
     attn_fwd_decode_noalloc,
     attn_fwd_ex,
+    attn_fwd_ws,
     attn_fwd_fp8,
     attn_fwd_fp8_workspace_bytes,
     attn_fwd_host,
@@ -33,6 +34,7 @@ from .binding import (  # noqa: F401
     attn_merge,
     attn_split_softmax_workspace_bytes,
     attn_workspace_bytes,
+    attn_workspace_bytes_ex,
     last_device_status,
     lib,
     selftest_bounded_wait,

@@ -50,8 +50,12 @@ def lib() -> ctypes.CDLL:
             L.attn_fwd.restype = ci
             L.attn_fwd_ex.argtypes = [vp, vp, vp, vp] + [ci] * 8 + [cf, ci, ci, vp, sz, vp]
             L.attn_fwd_ex.restype = ci
-            L.attn_workspace_bytes.argtypes = [ci] * 9
+            L.attn_workspace_bytes.argtypes = [ci] * 7
             L.attn_workspace_bytes.restype = sz
+            L.attn_workspace_bytes_ex.argtypes = [ci] * 9
+            L.attn_workspace_bytes_ex.restype = sz
+            L.attn_fwd_ws.argtypes = [vp, vp, vp, vp] + [ci] * 8 + [cf, ci, vp, sz, vp]
+            L.attn_fwd_ws.restype = ci
             L.attn_merge.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, vp]
             L.attn_merge.restype = ci
             L.attn_fwd_host.argtypes = [vp] * 8 + [ci] * 8 + [cf, ci, vp, sz, vp]
@@ -137,8 +141,14 @@ def _dims(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: Optional[torch.T
     return B, Hq, Hkv, M, N, D
 
 
-def attn_workspace_bytes(B, Hq, Hkv, M, N, D, causal=False, window=0, path=PATH_AUTO) -> int:
-    return int(lib().attn_workspace_bytes(B, Hq, Hkv, M, N, D, int(bool(causal)), int(window), int(path)))
+def attn_workspace_bytes(B, Hq, Hkv, M, N, D, window=0) -> int:
+    """C-ABI ``attn_workspace_bytes``: workspace bytes ``attn_fwd_ws`` needs (either causal value)."""
+    return int(lib().attn_workspace_bytes(B, Hq, Hkv, M, N, D, int(window)))
+
+
+def attn_workspace_bytes_ex(B, Hq, Hkv, M, N, D, causal=False, window=0, path=PATH_AUTO) -> int:
+    """C-ABI ``attn_workspace_bytes_ex``: workspace bytes ``attn_fwd_ex`` needs on ``path``."""
+    return int(lib().attn_workspace_bytes_ex(B, Hq, Hkv, M, N, D, int(bool(causal)), int(window), int(path)))
 
 
 def attn_fwd(q, k, v, o, causal=False, window=0, scale=0.0, stream=None) -> None:
@@ -147,6 +157,16 @@ def attn_fwd(q, k, v, o, causal=False, window=0, scale=0.0, stream=None) -> None
     st = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, Hq, Hkv, M, N, D, int(bool(causal)), int(window),
                         float(scale or 0.0), _DTYPES[q.dtype], _stream(stream))
     _check(st, "attn_fwd")
+
+
+def attn_fwd_ws(q, k, v, o, causal=False, window=0, scale=0.0, workspace=None, stream=None) -> None:
+    """C-ABI ``attn_fwd_ws``: the path ``attn_fwd`` takes, with caller workspace (a uint8 device tensor)."""
+    B, Hq, Hkv, M, N, D = _dims(q, k, v, o)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().attn_fwd_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, Hq, Hkv, M, N, D, int(bool(causal)),
+                           int(window), float(scale or 0.0), _DTYPES[q.dtype], _ptr(workspace), ws_bytes,
+                           _stream(stream))
+    _check(st, "attn_fwd_ws")
 
 
 def attn_fwd_ex(q, k, v, o, causal=False, window=0, scale=0.0, path=PATH_AUTO, workspace=None,
@@ -255,7 +275,7 @@ def attention(q, k, v, causal=False, window=0, scale=0.0, path=PATH_AUTO, stream
         attn_fwd(q, k, v, o, causal, window, scale, stream)
     else:
         B, Hq, Hkv, M, N, D = _dims(q, k, v, o)
-        nbytes = attn_workspace_bytes(B, Hq, Hkv, M, N, D, causal, window, path)
+        nbytes = attn_workspace_bytes_ex(B, Hq, Hkv, M, N, D, causal, window, path)
         ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device) if nbytes else None
         attn_fwd_ex(q, k, v, o, causal, window, scale, path, ws, stream)
     return o

@@ -46,8 +46,9 @@ def sources():
 
 
 def _deps():
+    # every file a translation unit may include: headers and the .inc fragments
     return sources() + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + \
-        glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
+        glob.glob(os.path.join(CSRC, "*.inc")) + glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
 
 
 def up_to_date() -> bool:

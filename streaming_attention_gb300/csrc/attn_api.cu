@@ -12,22 +12,28 @@
 namespace attn {
 namespace {
 
-// Device status word: kernels set it when a bounded wait gives up.
+// Device status word, one per device: kernels set it when a bounded wait gives
+// up. Every stream on the device shares it (attn_last_device_status reads and
+// clears it).
 __device__ int g_status_word;
 
-constexpr int kMaxDevices = 64;
+PerDeviceOnce g_status_once;
 int* g_status_ptr[kMaxDevices] = {};
 
 int* status_ptr() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    if (!g_status_ptr[dev]) {
+    const cudaError_t e = once_per_device(g_status_once, [dev] {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
-        g_status_ptr[dev] = static_cast<int*>(p);
-    }
-    return g_status_ptr[dev];
+        const cudaError_t r = cudaGetSymbolAddress(&p, g_status_word);
+        if (r == cudaSuccess) g_status_ptr[dev] = static_cast<int*>(p);
+        return r;
+    });
+    return e == cudaSuccess ? g_status_ptr[dev] : nullptr;
 }
+
+PerDeviceOnce g_sm_once;
+int g_sm_count[kMaxDevices] = {};
 
 constexpr int64_t kI32Max = 2147483647LL;
 
@@ -240,6 +246,15 @@ int validate_problem(const void* q, const void* k, const void* v, const void* o,
 
 int* device_status_ptr() { return status_ptr(); }
 
+int device_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    const cudaError_t e = once_per_device(g_sm_once, [dev] {
+        return cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+    });
+    return e == cudaSuccess ? g_sm_count[dev] : 0;
+}
+
 size_t split_workspace_bytes(int rows, int S, int D) {
     auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
     const size_t ml = up((size_t)rows * S * sizeof(float));
@@ -262,7 +277,7 @@ using namespace attn;
 extern "C" {
 
 int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int M, int N, int D,
-                int causal, int window, float scale, int dtype, int path, void* workspace, size_t ws_bytes,
+                int causal, int window, float scale, attn_dtype_t dtype, int path, void* workspace, size_t ws_bytes,
                 void* stream) {
     if (path < ATTN_PATH_AUTO || path > ATTN_PATH_DECODE) return ATTN_ERR_PATH;
     Problem p;
@@ -272,7 +287,7 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, int B, int
 }
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int M, int N, int D,
-             int causal, int window, float scale, int dtype, void* stream) {
+             int causal, int window, float scale, attn_dtype_t dtype, void* stream) {
     Problem p;
     int rc = validate(q, k, v, o, B, Hq, Hkv, M, N, D, causal, window, scale, dtype, &p);
     if (rc != ATTN_OK) return rc;
@@ -288,7 +303,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq
 }
 
 int attn_fwd_lse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int M,
-                 int N, int D, int causal, int window, float scale, int dtype, int path, void* workspace,
+                 int N, int D, int causal, int window, float scale, attn_dtype_t dtype, int path, void* workspace,
                  size_t ws_bytes, void* stream) {
     if (path < ATTN_PATH_AUTO || path > ATTN_PATH_DECODE) return ATTN_ERR_PATH;
     Problem p;
@@ -308,7 +323,7 @@ int attn_fwd_lse(const void* q, const void* k, const void* v, void* o, float* ls
     return rc;
 }
 
-size_t attn_workspace_bytes(int B, int Hq, int Hkv, int M, int N, int D, int causal, int window, int path) {
+size_t attn_workspace_bytes_ex(int B, int Hq, int Hkv, int M, int N, int D, int causal, int window, int path) {
     Problem p;
     // placeholder non-null pointers: only the shape is checked here
     static const int16_t dummy[8] __attribute__((aligned(16))) = {};
@@ -319,8 +334,28 @@ size_t attn_workspace_bytes(int B, int Hq, int Hkv, int M, int N, int D, int cau
     return workspace_for(p, choose_path(p, path));
 }
 
+size_t attn_workspace_bytes(int B, int Hq, int Hkv, int M, int N, int D, int window) {
+    const size_t a = attn_workspace_bytes_ex(B, Hq, Hkv, M, N, D, 0, window, ATTN_PATH_AUTO);
+    const size_t b = attn_workspace_bytes_ex(B, Hq, Hkv, M, N, D, 1, window, ATTN_PATH_AUTO);
+    return a > b ? a : b;
+}
+
+int attn_fwd_ws(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int M, int N, int D,
+                int causal, int window, float scale, attn_dtype_t dtype, void* workspace, size_t ws_bytes,
+                void* stream) {
+    Problem p;
+    int rc = validate(q, k, v, o, B, Hq, Hkv, M, N, D, causal, window, scale, dtype, &p);
+    if (rc != ATTN_OK) return rc;
+    const int path = choose_path(p, ATTN_PATH_AUTO);
+    // the caller's workspace is checked before anything is launched
+    const size_t need = empty_output(p) || p.N == 0 ? 0 : workspace_for(p, path);
+    if (need > 0 && (!workspace || ws_bytes < need)) return ATTN_ERR_WORKSPACE;
+    if (need > 0 && !aligned16(workspace)) return ATTN_ERR_ALIGN;
+    return run(p, q, k, v, o, path, workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
 int attn_merge(const float* m, const float* l, const float* acc, void* o, float* m_out, float* l_out, int rows,
-               int S, int D, int out_dtype, void* stream) {
+               int S, int D, attn_dtype_t out_dtype, void* stream) {
     if (rows < 0 || S < 1 || S > 4096 || D < 1 || D > 256) return ATTN_ERR_SHAPE;
     if (out_dtype != ATTN_BF16 && out_dtype != ATTN_FP16 && out_dtype != ATTN_FP32) return ATTN_ERR_DTYPE;
     if ((int64_t)rows * S * D > kI32Max) return ATTN_ERR_OVERFLOW;
@@ -332,7 +367,7 @@ int attn_merge(const float* m, const float* l, const float* acc, void* o, float*
 
 int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, void* q_d, void* k_d, void* v_d,
                   void* o_d, int B, int Hq, int Hkv, int M, int N, int D, int causal, int window, float scale,
-                  int dtype, void* workspace, size_t ws_bytes, void* stream) {
+                  attn_dtype_t dtype, void* workspace, size_t ws_bytes, void* stream) {
     Problem p;
     int rc = validate(q_d, k_d, v_d, o_d, B, Hq, Hkv, M, N, D, causal, window, scale, dtype, &p);
     if (rc != ATTN_OK) return rc;
@@ -382,7 +417,7 @@ int attn_last_device_status(void* stream) {
     return word ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }
 
-int attn_version(void) { return 101; }
+int attn_version(void) { return 200; }
 
 }  // extern "C"
 
@@ -396,7 +431,7 @@ size_t attn_bwd_workspace_bytes(int B, int Hq, int M) {
 
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* d_o, const float* lse, void* dq,
              void* dk, void* dv, int B, int Hq, int Hkv, int M, int N, int D, int causal, int window, float scale,
-             int dtype, void* workspace, size_t ws_bytes, void* stream) {
+             attn_dtype_t dtype, void* workspace, size_t ws_bytes, void* stream) {
     Problem p;
     int rc = validate(q, k, v, o, B, Hq, Hkv, M, N, D, causal, window, scale, dtype, &p);
     if (rc != ATTN_OK) return rc;
@@ -440,7 +475,7 @@ size_t attn_split_softmax_workspace_bytes(int M, int N, int chunk) {
     return split_softmax_ws_bytes(M, N, chunk);
 }
 
-int attn_split_softmax(const void* x, void* y, int M, int N, int chunk, int dtype, void* workspace, size_t ws_bytes,
+int attn_split_softmax(const void* x, void* y, int M, int N, int chunk, attn_dtype_t dtype, void* workspace, size_t ws_bytes,
                        void* stream) {
     if (dtype != ATTN_BF16 && dtype != ATTN_FP16 && dtype != ATTN_FP32) return ATTN_ERR_DTYPE;
     if (M < 0 || M > 65535 || N < 1 || N > 131072 || !split_softmax_chunk_ok(chunk)) return ATTN_ERR_SHAPE;

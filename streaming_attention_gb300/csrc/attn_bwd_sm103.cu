@@ -740,14 +740,14 @@ template <int D, bool kBF16>
 cudaError_t launch_bwd_t(const Problem& pr, const BwdArgs& a, const float* lse2, const float* delta, int Mpad,
                          int* status, cudaStream_t stream) {
     using C = BCfg<D>;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        C::kSmem);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(attn_bwd_dq_kernel<D, kBF16>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    static PerDeviceOnce attr_once;
+    const cudaError_t attr_err = once_per_device(attr_once, [] {
+        cudaError_t e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, kBF16>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D, kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     C::kSmem);
+        return e;
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int rows_pad = pr.B * pr.Hq * Mpad;

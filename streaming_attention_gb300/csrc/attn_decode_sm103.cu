@@ -567,8 +567,9 @@ __global__ void __launch_bounds__(kDecThreads)
                     part[DNR * DD + DNR + r] = 0.f;
                 }
             }
-        } else if (T == 0) {
-            // no key of this split: the empty summary
+        } else {
+            // no key of this split, or it gave up on a bounded wait: the empty
+            // summary, so the merge never reads a slot this call did not write
             for (int r = 0; r < p.R; ++r) {
                 const size_t slot = (size_t)(row_base + r) * p.S + split;
                 p.ws_acc[slot * DD + kl] = 0.f;
@@ -637,26 +638,18 @@ __global__ void __launch_bounds__(kDecThreads)
 }
 
 int sm_count() {
-    static int n = 0;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
-                                                      cudaSuccess)
-            n = 148;
-    });
-    return n;
+    const int n = device_sm_count();
+    return n > 0 ? n : 148;
 }
 
 template <int EB, bool kBF16, int RP, bool kPaged>
 cudaError_t launch_decode_t(const Problem& pr, const void* q, const void* k, const void* v, const PagedKV* kv,
                             int chunk, int S, const SplitWorkspace& ws, int* status, cudaStream_t stream,
                             DecodeOut* out) {
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(attn_decode_kernel<EB, kBF16, RP, kPaged>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, DCfg<EB>::kSmem);
+    static PerDeviceOnce attr_once;
+    const cudaError_t attr_err = once_per_device(attr_once, [] {
+        return cudaFuncSetAttribute(attn_decode_kernel<EB, kBF16, RP, kPaged>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, DCfg<EB>::kSmem);
     });
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap tq, tk, tv;

@@ -68,7 +68,7 @@ extern "C" size_t attn_fwd_fp8_workspace_bytes(int B, int Hq, int Hkv, int M, in
 
 extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                             int Hkv, int M, int N, int D, int causal, int window, float scale, float q_descale,
-                            float k_descale, float v_descale, int out_dtype, int path, void* workspace,
+                            float k_descale, float v_descale, attn_dtype_t out_dtype, int path, void* workspace,
                             size_t ws_bytes, void* stream) {
     if (path < ATTN_PATH_AUTO || path > ATTN_PATH_DECODE || path == ATTN_PATH_SIMT) return ATTN_ERR_PATH;
     Problem p;

@@ -4,9 +4,41 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "attn.h"
 
 namespace attn {
+
+// ---- per-device host state -------------------------------------------------
+// Kernel attributes (the dynamic shared-memory limit) and cached device
+// properties belong to one device; each is set up once per device, on the
+// first launch with that device current, so one process may drive several GPUs.
+constexpr int kMaxDevices = 64;
+
+struct PerDeviceOnce {
+    std::atomic<uint64_t> done{0};  // bit d: set up on device d
+    std::mutex mu;
+};
+
+// Runs fn() (returning cudaError_t) once per device: on the first call with that
+// device current. A failure is returned and not cached, so a later call retries.
+template <class F>
+cudaError_t once_per_device(PerDeviceOnce& o, F&& fn) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    const uint64_t bit = 1ull << dev;
+    if (o.done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(o.mu);
+    if (o.done.load(std::memory_order_relaxed) & bit) return cudaSuccess;
+    const cudaError_t e = fn();
+    if (e == cudaSuccess) o.done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
+
+// Number of SMs of the current device (cached per device); 0 when it cannot be read.
+int device_sm_count();
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;

@@ -24,7 +24,6 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = ATTN_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
 
@@ -49,7 +48,7 @@ using namespace attn;
 
 extern "C" int attn_fwd_decode_noalloc(const void* q, const void* k, const void* v, void* o, int B, int Hq,
                                        int Hkv, int M, int N, int D, int causal, int window, float scale,
-                                       int dtype, void* stream) {
+                                       attn_dtype_t dtype, void* stream) {
     Problem p;
     int rc = validate_problem(q, k, v, o, B, Hq, Hkv, M, N, D, causal, window, scale, dtype, &p);
     if (rc != ATTN_OK) return rc;
@@ -65,13 +64,22 @@ extern "C" int attn_fwd_decode_noalloc(const void* q, const void* k, const void*
     rc = decode_plan(p, &chunk, &S);
     if (rc != ATTN_OK) return rc;
     const int rows = p.B * p.Hq * p.M;
-    if (split_workspace_bytes(rows, S, p.D) > kNoAllocScratchBytes) return ATTN_ERR_WORKSPACE;
-    void* base = scratch_ptr();
+    // With at most kMaxClusterSplits splits per KV head the tcgen05 split kernel
+    // merges them inside its thread-block cluster and never touches the array,
+    // so only the other plans are limited by the array's size.
+    const bool in_cluster = decode_tc_supported(p) && S <= kMaxClusterSplits;
+    if (!in_cluster && split_workspace_bytes(rows, S, p.D) > kNoAllocScratchBytes) return ATTN_ERR_WORKSPACE;
     int* status = device_status_ptr();
-    if (!base || !status) return ATTN_ERR_CUDA;
+    if (!status) return ATTN_ERR_CUDA;
     // Every (row, split) summary the merge reads is written by the split
-    // kernel of this same call, so nothing has to be cleared first.
-    SplitWorkspace w = split_workspace(base, rows, S, p.D);
+    // kernel of this same call (an empty one where a split sees no key or
+    // gives up), so nothing has to be cleared first.
+    SplitWorkspace w{nullptr, nullptr, nullptr};
+    if (!in_cluster) {
+        void* base = scratch_ptr();
+        if (!base) return ATTN_ERR_CUDA;
+        w = split_workspace(base, rows, S, p.D);
+    }
     DecodeOut out{o, nullptr, 1.0f, false};
     if (launch_decode(p, q, k, v, chunk, S, w, status, s, &out) != cudaSuccess) return ATTN_ERR_CUDA;
     if (out.merged) return ATTN_OK;

@@ -121,7 +121,7 @@ size_t attn_decode_paged_workspace_bytes(int B, int Hq, int Hkv, int M, int D, i
 
 int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
                       const int* seq_lens, void* o, int B, int Hq, int Hkv, int M, int D, int num_pages,
-                      int page_size, int max_pages, int max_seq_len, int causal, int window, float scale, int dtype,
+                      int page_size, int max_pages, int max_seq_len, int causal, int window, float scale, attn_dtype_t dtype,
                       void* workspace, size_t ws_bytes, void* stream) {
     PagedCall c;
     int rc = validate_paged(q, k_pages, v_pages, block_table, seq_lens, o, B, Hq, Hkv, M, D, num_pages, page_size,
@@ -155,7 +155,7 @@ size_t attn_decode_paged_fp8_workspace_bytes(int B, int Hq, int Hkv, int M, int 
 int attn_decode_paged_fp8(const void* q, const void* k_pages, const void* v_pages, const int* block_table,
                           const int* seq_lens, void* o, int B, int Hq, int Hkv, int M, int D, int num_pages,
                           int page_size, int max_pages, int max_seq_len, int causal, int window, float scale,
-                          float q_descale, float k_descale, float v_descale, int out_dtype, void* workspace,
+                          float q_descale, float k_descale, float v_descale, attn_dtype_t out_dtype, void* workspace,
                           size_t ws_bytes, void* stream) {
     PagedCall c;
     int rc = validate_paged(q, k_pages, v_pages, block_table, seq_lens, o, B, Hq, Hkv, M, D, num_pages, page_size,

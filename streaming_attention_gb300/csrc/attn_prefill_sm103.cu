@@ -41,8 +41,6 @@
 // The same kernel takes 8-bit E4M3 inputs (kIn = kInE4M3): both products run
 // as kind::f8f6f4 with 32-element K steps, a D = 128 row is one 128-byte
 // swizzle chunk, and P is rounded to E4M3, four per TMEM column.
-#include <mutex>
-
 #include "attn_internal.h"
 #include "sm100_ptx.cuh"
 #include "tma_map.h"
@@ -172,6 +170,44 @@ __device__ bool wait_warp(uint32_t bar, uint32_t parity, volatile uint32_t* abor
         }
         if (__shfl_sync(0xffffffffu, stop, 0)) return false;
     }
+}
+
+// Packed FP32 pairs (lo in the low word): one fma/add/mul.f32x2 instruction
+// does the work of two, which matters because the softmax warps share each SM
+// sub-partition's issue slots with the MMA-issuing and TMA threads.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+// three-input maximum / minimum (one instruction for two new values)
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
 }
 
 template <bool kBF16>
@@ -425,19 +461,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (key < lo || key >= hi) s[q4][e] = __float_as_uint(masked_s);
                         }
                 }
+                // row maximum (minimum for a negative scale) in four independent
+                // chains of three-input operations
                 float mx;
-                if (c >= 0.f) {
-                    mx = -INFINITY;
+                {
+#define SV(i) __uint_as_float(s[(i) >> 5][(i) & 31])
+                    float a0 = SV(0), a1 = SV(1), a2 = SV(2), a3 = SV(3);
+                    if (c >= 0.f) {
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4)
+                        for (int i = 4; i < 128; i += 8) {
+                            a0 = max3f(a0, SV(i), SV(i + 1));
+                            a1 = max3f(a1, SV(i + 2), SV(i + 3));
+                            if (i + 4 < 128) {
+                                a2 = max3f(a2, SV(i + 4), SV(i + 5));
+                                a3 = max3f(a3, SV(i + 6), SV(i + 7));
+                            }
+                        }
+                        mx = max3f(a0, a1, fmaxf(a2, a3));
+                    } else {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(s[q4][e]));
-                } else {
-                    mx = INFINITY;
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) mx = fminf(mx, __uint_as_float(s[q4][e]));
+                        for (int i = 4; i < 128; i += 8) {
+                            a0 = min3f(a0, SV(i), SV(i + 1));
+                            a1 = min3f(a1, SV(i + 2), SV(i + 3));
+                            if (i + 4 < 128) {
+                                a2 = min3f(a2, SV(i + 4), SV(i + 5));
+                                a3 = min3f(a3, SV(i + 6), SV(i + 7));
+                            }
+                        }
+                        mx = min3f(a0, a1, fminf(a2, a3));
+                    }
+#undef SV
                 }
                 const float m_tile = mx * c;  // -inf when the whole tile is masked for this row
                 const float m_new = fmaxf(m_ref, m_tile);
@@ -450,16 +503,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // ghost-row pin: while every key so far is masked, exponentiate against 0
                 const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-                const float neg_m = -m_use;
+                // p = 2^(s c - m_use) for pairs of keys (packed FMA), summed into l
+                // in two packed chains, rounded to the P type and written over S
+                const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-m_use, -m_use);
+                uint64_t lsum[2] = {0ull, 0ull};
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     if constexpr (EB == 2) {
                         uint32_t packed[16];
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
-                            const float p0 = ex2(fmaf(__uint_as_float(s[q4][2 * e]), c, neg_m));
-                            const float p1 = ex2(fmaf(__uint_as_float(s[q4][2 * e + 1]), c, neg_m));
-                            l += p0 + p1;
+                            float x0, x1;
+                            f2_unpack(f2_fma(f2_pack(__uint_as_float(s[q4][2 * e]), __uint_as_float(s[q4][2 * e + 1])),
+                                             c2, nm2),
+                                      x0, x1);
+                            const float p0 = ex2(x0), p1 = ex2(x1);
+                            lsum[e & 1] = f2_add(lsum[e & 1], f2_pack(p0, p1));
                             packed[e] = pack2<kBF16>(p0, p1);
                         }
                         tmem_st_x16(tS + q4 * 16, packed);  // P overwrites the first 64 columns of S
@@ -471,12 +530,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int e = 0; e < 8; ++e) {
                             float pv[4];
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) pv[i] = ex2(fmaf(__uint_as_float(s[q4][4 * e + i]), c, neg_m));
-                            l += (pv[0] + pv[1]) + (pv[2] + pv[3]);
+                            for (int h = 0; h < 2; ++h) {
+                                const int e2 = 2 * e + h;
+                                float x0, x1;
+                                f2_unpack(f2_fma(f2_pack(__uint_as_float(s[q4][2 * e2]),
+                                                         __uint_as_float(s[q4][2 * e2 + 1])),
+                                                 c2, nm2),
+                                          x0, x1);
+                                pv[2 * h] = ex2(x0);
+                                pv[2 * h + 1] = ex2(x1);
+                                lsum[h] = f2_add(lsum[h], f2_pack(pv[2 * h], pv[2 * h + 1]));
+                            }
                             packed[e] = pack_e4m3x4(pv[0], pv[1], pv[2], pv[3]);
                         }
                         tmem_st_x8(tS + q4 * 8, packed);  // P overwrites the first 32 columns of S
                     }
+                }
+                {
+                    float l0, l1, l2, l3;
+                    f2_unpack(lsum[0], l0, l1);
+                    f2_unpack(lsum[1], l2, l3);
+                    l += (l0 + l1) + (l2 + l3);
                 }
                 // rescale the accumulator (the value product of the previous key tile
                 // has completed: its commit preceded this tile's score commit)
@@ -486,8 +560,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint32_t o[32];
                         tmem_ld_x32(tO + ch * 32, o);
                         tmem_wait_ld_x32(o);
+                        const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        for (int e = 0; e < 16; ++e) {
+                            float y0, y1;
+                            f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), a2), y0,
+                                      y1);
+                            o[2 * e] = __float_as_uint(y0);
+                            o[2 * e + 1] = __float_as_uint(y1);
+                        }
                         tmem_st_x32(tO + ch * 32, o);
                     }
                 }
@@ -537,30 +618,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-int sm_count_prefill() {
-    static int n = 0;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
-                                                      cudaSuccess)
-            n = 148;
-    });
-    return n;
-}
-
 template <int D, int kIn, bool kBF16>
 int launch_t(const Problem& pr, const void* q, const void* k, const void* v, void* o, int* status, float v_scale,
              cudaStream_t stream, long withhold_p_at = -1) {
     constexpr int EB = kIn == kInE4M3 ? 1 : 2;
     using C = Cfg<D, EB>;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(attn_prefill_kernel<D, kIn, kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        C::kSmemBytes);
-    });
-    if (attr_err != cudaSuccess) return ATTN_ERR_CUDA;
+    static PerDeviceOnce attr_once;
+    if (once_per_device(attr_once, [] {
+            return cudaFuncSetAttribute(attn_prefill_kernel<D, kIn, kBF16>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        }) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    const int sms = device_sm_count();
+    if (sms <= 0) return ATTN_ERR_CUDA;
     CUtensorMap tq, tk, tv;
     if (!make_tensor_map(&tq, q, D, pr.M, pr.B * pr.Hq, BM, kBF16, EB) ||
         !make_tensor_map(&tk, k, D, pr.N, pr.B * pr.Hkv, BN, kBF16, EB) ||
@@ -583,7 +653,7 @@ int launch_t(const Problem& pr, const void* q, const void* k, const void* v, voi
     pp.nqb = (pr.M + NQ * BM - 1) / (NQ * BM);
     pp.tiles = pp.BH * pp.nqb;
     pp.withhold_p_at = withhold_p_at;
-    const int grid = pp.tiles < sm_count_prefill() ? pp.tiles : sm_count_prefill();
+    const int grid = pp.tiles < sms ? pp.tiles : sms;
     attn_prefill_kernel<D, kIn, kBF16><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, pp);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

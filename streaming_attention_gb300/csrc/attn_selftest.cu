@@ -47,7 +47,7 @@ extern "C" int attn_selftest_bounded_wait(unsigned timeout_us, void* stream) {
 }
 
 extern "C" int attn_selftest_prefill_abort(const void* q, const void* k, const void* v, void* o, int B, int Hq,
-                                           int Hkv, int M, int N, int D, int dtype, long long withhold_at,
+                                           int Hkv, int M, int N, int D, attn_dtype_t dtype, long long withhold_at,
                                            void* stream) {
     Problem p;
     int rc = validate_problem(q, k, v, o, B, Hq, Hkv, M, N, D, 0, 0, 0.f, dtype, &p);

@@ -91,18 +91,39 @@ def test_simt_grid_limit(L):
     assert L.attn_fwd_ex(*args, sa.PATH_DECODE, None, 0, None) == -11  # D = 64 splits run on it too
     assert L.attn_fwd_decode_noalloc(*args, None) == -11
     # AUTO leaves decode to the prefill kernel when the split kernel would not fit
-    assert sa.attn_workspace_bytes(1, 4096, 4096, 1, 512, 64, 0, 0, sa.PATH_AUTO) > 0
-    assert sa.attn_workspace_bytes(1, 65536, 4096, 1, 512, 64, 0, 0, sa.PATH_AUTO) == 0
+    assert sa.attn_workspace_bytes_ex(1, 4096, 4096, 1, 512, 64, 0, 0, sa.PATH_AUTO) > 0
+    assert sa.attn_workspace_bytes_ex(1, 65536, 4096, 1, 512, 64, 0, 0, sa.PATH_AUTO) == 0
 
 
 def test_workspace_bytes(L):
     # prefill and SIMT need none; decode needs room for its split summaries
-    assert sa.attn_workspace_bytes(2, 32, 32, 4096, 4096, 128, True, 0, sa.PATH_SIMT) == 0
-    n = sa.attn_workspace_bytes(8, 32, 8, 1, 8192, 128, True, 4096, sa.PATH_DECODE)
+    assert sa.attn_workspace_bytes_ex(2, 32, 32, 4096, 4096, 128, True, 0, sa.PATH_SIMT) == 0
+    n = sa.attn_workspace_bytes_ex(8, 32, 8, 1, 8192, 128, True, 4096, sa.PATH_DECODE)
     rows = 8 * 32
     assert n >= rows * 4 * (128 + 2)
-    assert sa.attn_workspace_bytes(8, 32, 8, 1, 8192, 128, True, 4096, sa.PATH_AUTO) == n
-    assert sa.attn_workspace_bytes(-1, 32, 8, 1, 8192, 128, True, 4096, 0) == 0
+    assert sa.attn_workspace_bytes_ex(8, 32, 8, 1, 8192, 128, True, 4096, sa.PATH_AUTO) == n
+    assert sa.attn_workspace_bytes_ex(-1, 32, 8, 1, 8192, 128, True, 4096, 0) == 0
+
+
+def test_boundary_workspace_query_and_fwd_ws(L):
+    """The survey's boundary: attn_workspace_bytes(B, Hq, Hkv, M, N, D, window)
+    sizes the workspace of attn_fwd_ws (the path attn_fwd takes) for either
+    causal value, and attn_fwd_ws refuses a missing or short workspace before
+    launching anything."""
+    dec = (8, 32, 8, 1, 8192, 128)
+    n = sa.attn_workspace_bytes(*dec, 4096)
+    assert n > 0
+    assert n == max(sa.attn_workspace_bytes_ex(*dec, c, 4096, sa.PATH_AUTO) for c in (0, 1))
+    assert sa.attn_workspace_bytes(2, 32, 32, 4096, 4096, 128, 0) == 0  # prefill needs none
+    assert sa.attn_workspace_bytes(-1, 32, 8, 1, 8192, 128, 0) == 0
+    assert sa.attn_workspace_bytes(8, 32, 8, 0, 8192, 128, 0) == 0  # empty output
+    args = (A16, A16, A16, A16, *dec, 1, 4096, 0.0, 0)
+    assert L.attn_fwd_ws(*args, None, 0, None) == -8
+    assert L.attn_fwd_ws(*args, A16, n - 1, None) == -8
+    assert L.attn_fwd_ws(*args, A8, n, None) == -7
+    # metadata validation comes first, as for attn_fwd
+    assert L.attn_fwd_ws(A16, A16, A16, A16, 1, 6, 4, 8, 8, 64, 0, 0, 0.0, 0, None, 0, None) == -5
+    assert L.attn_fwd_ws(A16, A16, A16, A16, 1, 2, 2, 8, 8, 64, 0, 0, 0.0, 9, None, 0, None) == -3
 
 
 def test_merge_validation(L):
@@ -230,7 +251,7 @@ def test_fp8_validation_status(L, kw, status):
 def test_fp8_workspace_bytes(L):
     # the 8-bit decode plan has its own query (today the same split plan as the 16-bit one)
     n8 = sa.attn_fwd_fp8_workspace_bytes(8, 32, 8, 1, 8192, 128, True, 4096, sa.PATH_DECODE)
-    n16 = sa.attn_workspace_bytes(8, 32, 8, 1, 8192, 128, True, 4096, sa.PATH_DECODE)
+    n16 = sa.attn_workspace_bytes_ex(8, 32, 8, 1, 8192, 128, True, 4096, sa.PATH_DECODE)
     assert n8 == n16 > 0
     assert sa.attn_fwd_fp8_workspace_bytes(8, 32, 8, 1, 8192, 128, True, 4096, sa.PATH_AUTO) == n8
     assert sa.attn_fwd_fp8_workspace_bytes(8, 32, 8, 1, 8192, 128, True, 4096, sa.PATH_PREFILL) == 0

@@ -75,7 +75,7 @@ def test_bench_launch_count_follows_the_library_split_plan():
     B.build()
 
     def splits_from_workspace(w):
-        nb = sa.attn_workspace_bytes(w.B, w.Hq, w.Hkv, w.M, w.N, w.D, w.causal, w.window, sa.PATH_DECODE)
+        nb = sa.attn_workspace_bytes_ex(w.B, w.Hq, w.Hkv, w.M, w.N, w.D, w.causal, w.window, sa.PATH_DECODE)
         rows, D = w.B * w.Hq * w.M, w.D
         up = lambda x: (x + 255) // 256 * 256  # noqa: E731
         for S in range(1, 4097):

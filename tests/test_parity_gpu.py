@@ -137,11 +137,22 @@ def test_decode_split_paths(shape, mask):
         check(run(q, k, v, mask[0], mask[1], path), want, torch.bfloat16, f"{shape} {mask} path={path}")
 
 
-def sampled(w, causal, window, path, dtype=None, count=192):
+def whole_heads(B, H, M):
+    """Every row of the first, the middle and the last (batch, head): the
+    persistent prefill kernel deals each CTA work tiles from many heads, so
+    whole heads cover every work tile of those heads, the last ones scheduled
+    included."""
+    heads = sorted({0, (B * H) // 2, B * H - 1})
+    return [bh * M + i for bh in heads for i in range(M)]
+
+
+def sampled(w, causal, window, path, dtype=None, count=192, heads=False):
     dtype = dtype or w.dtype
     q, k, v = workload_inputs(w, dtype)
     o = run(q, k, v, causal, window, path)
     rows = sample_rows(w.B, w.Hq, w.M, count, seed=w.seed)
+    if heads:
+        rows = sorted(set(rows) | set(whole_heads(w.B, w.Hq, w.M)))
     want = oracle.attention_rows(q, k, v, rows, causal=causal, window=window)
     got = o.reshape(-1, w.D)[torch.tensor(rows, device=o.device)]
     assert torch.isfinite(o).all()
@@ -157,7 +168,7 @@ def test_prefill_d64_full_size(causal, path):
 @pytest.mark.parametrize("variant", ["bf16_causal", "bf16_noncausal", "fp16_causal"])
 def test_prefill_d128_full_size(variant):
     dtype = torch.float16 if variant.startswith("fp16") else torch.bfloat16
-    sampled(PREFILL_D128, "noncausal" not in variant, 0, sa.PATH_AUTO, dtype)
+    sampled(PREFILL_D128, "noncausal" not in variant, 0, sa.PATH_AUTO, dtype, heads=True)
 
 
 @pytest.mark.parametrize("path", [sa.PATH_AUTO, sa.PATH_DECODE, sa.PATH_SIMT], ids=PATH_NAMES.get)
@@ -170,7 +181,7 @@ def test_decode_gqa_full_size(path):
 
 
 def test_long_causal_stress_full_size():
-    sampled(LONG_CAUSAL, True, 0, sa.PATH_AUTO, count=160)
+    sampled(LONG_CAUSAL, True, 0, sa.PATH_AUTO, count=160, heads=True)
 
 
 def test_merge_kernel_worked_example():
@@ -238,3 +249,34 @@ def test_host_pipelined_chunks_match_device_call(shape, causal, window):
     assert torch.equal(oh, ref.cpu())
     assert torch.equal(od, ref)
     check(oh, oracle.attention(q, k, v, causal=causal, window=window), torch.bfloat16, f"host {shape}")
+
+
+@pytest.mark.parametrize("case", ["decode", "prefill"])
+def test_fwd_ws_boundary_against_oracle(case):
+    """The survey's boundary through ctypes: attn_workspace_bytes sizes the
+    caller's workspace for attn_fwd_ws (per-call scratch, as the course's
+    wide-row split softmax keeps it), which takes the path attn_fwd takes."""
+    import ctypes
+
+    if case == "decode":
+        w = DECODE_GQA
+        q, k, v = workload_inputs(w)
+        causal, window = True, w.window
+    else:
+        q, k, v = make_qkv(1, 4, 2, 300, 700, 128, torch.bfloat16, seed=21)
+        causal, window = True, 0
+    B, Hq, M, D = q.shape
+    Hkv, N = k.shape[1], k.shape[2]
+    L = sa.lib()
+    n = L.attn_workspace_bytes(B, Hq, Hkv, M, N, D, window)
+    assert (n > 0) == (case == "decode")
+    ws = torch.empty(max(n, 1), dtype=torch.uint8, device=DEV)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    o = torch.full_like(qd, float("nan"))
+    st = L.attn_fwd_ws(ctypes.c_void_p(qd.data_ptr()), ctypes.c_void_p(kd.data_ptr()), ctypes.c_void_p(vd.data_ptr()),
+                       ctypes.c_void_p(o.data_ptr()), B, Hq, Hkv, M, N, D, int(causal), window, 0.0, sa.ATTN_BF16,
+                       ctypes.c_void_p(ws.data_ptr()) if n else None, n,
+                       ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0, sa.strerror(st)
+    torch.cuda.synchronize()
+    check(o, oracle.attention(q, k, v, causal=causal, window=window), torch.bfloat16, f"attn_fwd_ws {case}")
