@@ -28,6 +28,16 @@
 // loaded as soon as the last score product of the current one has read Q, and
 // the next tile's first value product into O_t waits only until the epilogue
 // of the current tile has pulled O_t out of TMEM, so epilogues overlap MMAs.
+// The epilogue writes each normalized 64-column half of a query tile into a
+// 16 KB staging box in shared memory (in the TMA's 128-byte swizzle) and one
+// thread stores it with a TMA copy: a row-per-thread global store would touch
+// 32 rows per instruction and hold up the next tile's TMEM reads behind it.
+//
+// The single MMA-issuing thread keeps the tensor pipe fed only if it spends
+// little time between MMA groups (the pipe queues about one MMA), so it makes
+// one commit per key tile for the ring (after S_1(j), freeing K_j and V_(j-1)
+// together) and tests the readiness of V_j and P_0(j) between the two halves
+// of the S_1(j) group, while queued MMAs run, instead of waiting after it.
 //
 // Rescaling is lazy: a row's reference maximum moves only when the new
 // maximum exceeds it by more than 8 (base-2 units), so p = 2^(t - m_ref) <= 256
@@ -72,9 +82,13 @@ struct Cfg {
     static constexpr int kStages = (kRowBytes == 256) ? 4 : 8;
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = NQ * kTileBytes;
-    static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
-    // q_full, q_free, full[S], empty[S], s_full[2], p_full[2], o_final, o_free[2], drain
-    static constexpr int kNumBars = 2 + 2 * kStages + 2 + 2 + 1 + 2 + 1;
+    // output staging: one 128-row x 128-byte box per query tile (64 output columns,
+    // 16-bit), written by the softmax warps and stored to global memory by TMA
+    static constexpr int kStageBytes = BM * 128;
+    static constexpr int kStageOff = kKVOff + kStages * kTileBytes;
+    static constexpr int kBarOff = kStageOff + NQ * kStageBytes;
+    // q_full, q_free, full[S], empty[S], s_full[2], p_full[2], o_final, o_free[2], drain, stg_full[2], stg_free[2]
+    static constexpr int kNumBars = 2 + 2 * kStages + 2 + 2 + 1 + 2 + 1 + 2 + 2;
     static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
 };
@@ -101,7 +115,9 @@ struct PrefillParams {
 };
 
 struct Bars {
-    uint32_t q_full, q_free, full0, empty0, s0, p0, o_final, o_free0, drain;
+    uint32_t q_full, q_free, full0, empty0, s0, p0, o_final, o_free0, drain, stg_full0, stg_free0;
+    __device__ uint32_t stg_full(int t) const { return stg_full0 + 8u * t; }
+    __device__ uint32_t stg_free(int t) const { return stg_free0 + 8u * t; }
     __device__ uint32_t full(int s) const { return full0 + 8u * s; }
     __device__ uint32_t empty(int s) const { return empty0 + 8u * s; }
     __device__ uint32_t s_full(int t) const { return s0 + 8u * t; }
@@ -220,10 +236,11 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 // 16-bit inputs, 32 for 8-bit), so each K step only adds a compile-time offset
 // to a 64-bit descriptor. Every K step covers 32 bytes of a row: 16 elements
 // of 16 bits or 32 of 8 bits.
-template <int D, int EB>
-__device__ __forceinline__ void mma_group_s(uint32_t d_tmem, uint64_t a0, uint64_t b0, uint32_t idesc) {
+template <int D, int EB, class F>
+__device__ __forceinline__ void mma_group_s(uint32_t d_tmem, uint64_t a0, uint64_t b0, uint32_t idesc, F&& between) {
 #pragma unroll
     for (int kk = 0; kk < D * EB / 32; ++kk) {
+        if (kk == D * EB / 64) between();
         const uint64_t off = (uint64_t)((((kk >> 2) * Cfg<D, EB>::kChunkBytes) + (kk & 3) * 32) >> 4);
         if constexpr (EB == 1)
             mma_ss_f8(d_tmem, a0 + off, b0 + off, idesc, kk > 0 ? 1u : 0u);
@@ -250,14 +267,17 @@ __device__ __forceinline__ void mma_group_pv(uint32_t d_tmem, uint32_t a_tmem, u
 template <int D, int kIn, bool kBF16>  // kBF16: output type (and input type for 16-bit inputs)
 __global__ void __launch_bounds__(kThreads, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                        const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
+                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                        const PrefillParams p) {
     constexpr int EB = kIn == kInE4M3 ? 1 : 2;
     using C = Cfg<D, EB>;
+    constexpr int kHalf = C::kStages / 2;  // empty barriers: one per pair of slots freed together
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sQ = sbase + C::kQOff;
     const uint32_t sKV = sbase + C::kKVOff;
+    const uint32_t sStage = sbase + C::kStageOff;
     Bars bar;
     bar.q_full = sbase + C::kBarOff;
     bar.q_free = bar.q_full + 8;
@@ -268,6 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bar.o_final = bar.p0 + 16;
     bar.o_free0 = bar.o_final + 8;
     bar.drain = bar.o_free0 + 16;
+    bar.stg_full0 = bar.drain + 8;
+    bar.stg_free0 = bar.stg_full0 + 16;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff);
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
@@ -287,6 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(bar.o_final, 1);
         mbar_init(bar.drain, 1);
+        for (int t = 0; t < NQ; ++t) {
+            mbar_init(bar.stg_full(t), 4);  // one arrival per softmax warp of the tile
+            mbar_init(bar.stg_free(t), 1);  // the tile's storing thread
+        }
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -305,6 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tmQ);
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
+            prefetch_tmap(&tmO);
             int u = 0, tc = 0;  // ring position and work tiles with keys, across the whole walk
             int q_issued = 0;   // Q loads issued
             bool ok = true;
@@ -319,11 +346,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_3d(sQ + t * C::kTileBytes + c * C::kChunkBytes, &tmQ, c * C::kChunkElems, wk.row0 + t * BM,
                                     wk.bh, bar.q_full);
                 ++q_issued;
-                // K_j and V_j alternate through the ring in the order the MMA uses them
+                // K_j and V_j alternate through the ring in the order the MMA uses them.
+                // One commit after S_1(J) frees K_J and V_(J-1) (empty barrier J % kHalf, phase
+                // J / kHalf); K_J reuses K_(J-kHalf)'s slot and V_J reuses V_(J-kHalf)'s.
                 for (int x = 0; x < 2 * wk.n; ++x, ++u) {
                     const int s = u % C::kStages;
+                    const int J = u >> 1;
+                    const int Jf = (u & 1) ? J - kHalf + 1 : J - kHalf;  // the step whose commit frees this slot
                     if (u >= C::kStages &&
-                        !(ok = wait_one(bar.empty(s), ((u / C::kStages) - 1) & 1, abort_flag, p.status)))
+                        !(ok = wait_one(bar.empty(Jf % kHalf), (Jf / kHalf) & 1, abort_flag, p.status)))
                         break;
                     mbar_arrive_expect_tx(bar.full(s), C::kTileBytes);
                     const CUtensorMap* tm = (x & 1) ? &tmV : &tmK;
@@ -355,12 +386,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dv = sw128_desc(sKV, C::kChunkBytes, 1024);
             constexpr uint64_t kSlotStep = (uint64_t)(C::kTileBytes >> 4);
             auto issue_s = [&](int t, int slot) {
-                mma_group_s<D, EB>(tmem + col_s(t), t ? dq1 : dq0, dk + (uint64_t)slot * kSlotStep, idS);
+                mma_group_s<D, EB>(tmem + col_s(t), t ? dq1 : dq0, dk + (uint64_t)slot * kSlotStep, idS, [] {});
             };
             // O_t += P_t V; the first product of a tile overwrites O_t, after the
             // previous tile's epilogue has read it out
+            bool p_ready = false;  // P_0's phase was seen complete in the middle of the S_1 group
             auto issue_pv = [&](int t, int slot, bool first) {
-                if (!wait_one(bar.p_full(t), ps[t] & 1, abort_flag, p.status)) return false;
+                if (!(t == 0 && p_ready) && !wait_one(bar.p_full(t), ps[t] & 1, abort_flag, p.status)) return false;
                 ++ps[t];
                 if (first && tc > 0 && !wait_one(bar.o_free(t), (tc - 1) & 1, abort_flag, p.status)) return false;
                 tc_fence_after();
@@ -383,19 +415,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit(bar.s_full(0));
                     if (jj > 0) {
                         if (!(ok = issue_pv(1, slot_v_prev, jj - 1 == 0))) break;
-                        mma_commit(bar.empty(slot_v_prev));
                     }
-                    issue_s(1, sk);
+                    // S_1, with the readiness of V_j and P_0 tested between its halves (a test
+                    // there overlaps the MMAs already queued; a wait after the group does not)
+                    bool v_ready = false;
+                    p_ready = false;
+                    mma_group_s<D, EB>(tmem + col_s(1), dq1, dk + (uint64_t)sk * kSlotStep, idS, [&] {
+                        v_ready = mbar_test(bar.full(sv), (uv / C::kStages) & 1);
+                        p_ready = mbar_test(bar.p_full(0), ps[0] & 1);
+                    });
                     mma_commit(bar.s_full(1));
                     if (jj == n - 1) mma_commit(bar.q_free);  // Q is read for the last time
-                    mma_commit(bar.empty(sk));
-                    if (!(ok = wait_one(bar.full(sv), (uv / C::kStages) & 1, abort_flag, p.status))) break;
+                    mma_commit(bar.empty((uk >> 1) % kHalf));  // K_j and V_(j-1) are read
+                    if (!v_ready && !(ok = wait_one(bar.full(sv), (uv / C::kStages) & 1, abort_flag, p.status))) break;
                     if (!(ok = issue_pv(0, sv, jj == 0))) break;
                     slot_v_prev = sv;
                 }
                 if (!ok) break;
                 if (!(ok = issue_pv(1, slot_v_prev, n - 1 == 0))) break;
-                mma_commit(bar.empty(slot_v_prev));
                 mma_commit(bar.o_final);  // this tile's O_0 and O_1 are final
                 ++tc;
             }
@@ -416,6 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float masked_s = c >= 0.f ? -INFINITY : INFINITY;  // scores that give t = -inf
         const int off = p.N - p.M;
         int g = 0, tc = 0;  // score tiles and work tiles with keys, across the walk
+        int nst = 0;        // output boxes stored from this tile's staging buffer
         bool ok = true;
         Work wk;
         for (int w = 0; ok && work_tile(p, w, &wk); ++w) {
@@ -579,7 +617,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
 
-            // ---------------- epilogue: O / l, one cast, store rows < M ----------------
+            // ---------------- epilogue: O / l, one cast, rows < M ----------------
+            // Per 64-column half: the four warps of the tile write their rows, normalized
+            // and cast, into the tile's staging box (128-byte swizzle, as the tensor map
+            // expects), and the tile's first thread stores the box with one TMA copy,
+            // which writes rows < M only.
             if (!(ok = wait_warp(bar.o_final, tc & 1, abort_flag, p.status))) break;
             ++tc;
             tc_fence_after();
@@ -587,27 +629,58 @@ __global__ void __launch_bounds__(kThreads, 1)
             // log sum_j e^(scale s_j) = ln 2 * (m_ref + log2 l) (p was taken against m_ref)
             if (p.lse && row < p.M)
                 p.lse[(size_t)wk.bh * p.M + row] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
-            uint32_t w16[D / 2];  // the row as packed 16-bit pairs
+            const uint32_t stg = sStage + t * C::kStageBytes;
+            const uint32_t my_row = stg + r_in_tile * 128;
+            const uint64_t inv2 = f2_pack(inv, inv);
 #pragma unroll
-            for (int ch = 0; ch < D / 32; ++ch) {
-                uint32_t o[32];
-                tmem_ld_x32(tO + ch * 32, o);
-                tmem_wait_ld_x32(o);
+            for (int h = 0; h < D / 64; ++h) {
+                uint32_t o[2][32];
+                tmem_ld_x32(tO + h * 64, o[0]);
+                tmem_ld_x32(tO + h * 64 + 32, o[1]);
+                tmem_wait_ld_x32(o[0]);
+                reg_after_x32(o[1]);
+                if (h == D / 64 - 1) {
+                    // O_t is read out: it may take the next tile's first value product
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar.o_free(t));
+                }
+                // the box's previous store must have read it
+                if (nst > 0 && !(ok = wait_warp(bar.stg_free(t), (nst - 1) & 1, abort_flag, p.status))) break;
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    w16[ch * 16 + e] = pack2<kBF16>(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+                for (int c8 = 0; c8 < 8; ++c8) {  // 16-byte chunk c8: columns 8 c8 .. 8 c8 + 7 of the half
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int col = c8 * 8 + 2 * e;
+                        float y0, y1;
+                        f2_unpack(f2_mul(f2_pack(__uint_as_float(o[col >> 5][col & 31]),
+                                                 __uint_as_float(o[col >> 5][(col & 31) + 1])),
+                                         inv2),
+                                  y0, y1);
+                        w4[e] = pack2<kBF16>(y0, y1);
+                    }
+                    st_shared_v4(my_row + ((c8 ^ (r_in_tile & 7)) << 4), w4[0], w4[1], w4[2], w4[3]);
+                }
+                fence_proxy_async_smem();  // the box is read by the TMA (async proxy)
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar.stg_full(t));
+                if (wq == 0 && lane == 0) {
+                    if ((ok = wait_one(bar.stg_full(t), nst & 1, abort_flag, p.status))) {
+                        tma_store_3d(&tmO, stg, h * 64, wk.row0 + t * BM, wk.bh);
+                        bulk_commit();
+                        bulk_wait_read0();  // the box may be written again
+                        mbar_arrive(bar.stg_free(t));
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                ++nst;
+                if (!ok) break;
             }
-            // O_t may now take the next tile's first value product
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar.o_free(t));
-            if (row < p.M) {
-                uint4* dst = reinterpret_cast<uint4*>(orow);
-#pragma unroll
-                for (int v4 = 0; v4 < D / 8; ++v4)
-                    dst[v4] = make_uint4(w16[4 * v4], w16[4 * v4 + 1], w16[4 * v4 + 2], w16[4 * v4 + 3]);
-            }
+            if (!ok) break;
         }
+        // every output copy this thread issued must complete before the CTA exits
+        if (wq == 0 && lane == 0) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -631,10 +704,11 @@ int launch_t(const Problem& pr, const void* q, const void* k, const void* v, voi
         return ATTN_ERR_CUDA;
     const int sms = device_sm_count();
     if (sms <= 0) return ATTN_ERR_CUDA;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if (!make_tensor_map(&tq, q, D, pr.M, pr.B * pr.Hq, BM, kBF16, EB) ||
         !make_tensor_map(&tk, k, D, pr.N, pr.B * pr.Hkv, BN, kBF16, EB) ||
-        !make_tensor_map(&tv, v, D, pr.N, pr.B * pr.Hkv, BN, kBF16, EB))
+        !make_tensor_map(&tv, v, D, pr.N, pr.B * pr.Hkv, BN, kBF16, EB) ||
+        !make_tensor_map(&to, o, D, pr.M, pr.B * pr.Hq, BM, kBF16, 2))
         return ATTN_ERR_CUDA;
     PrefillParams pp;
     pp.o = o;
@@ -654,7 +728,7 @@ int launch_t(const Problem& pr, const void* q, const void* k, const void* v, voi
     pp.tiles = pp.BH * pp.nqb;
     pp.withhold_p_at = withhold_p_at;
     const int grid = pp.tiles < sms ? pp.tiles : sms;
-    attn_prefill_kernel<D, kIn, kBF16><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, pp);
+    attn_prefill_kernel<D, kIn, kBF16><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, pp);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
