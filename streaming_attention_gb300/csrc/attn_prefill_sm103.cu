@@ -491,13 +491,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (need_mask) {
                     int lo = 0, hi = 0;
                     key_range(pos, p.N, p.causal, p.window, &lo, &hi);
+                    const int vlo = lo - key0, vhi = hi - key0;  // this row's visible columns of the tile
+                    if (p.window > 0) {
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4)
+                        for (int q4 = 0; q4 < 4; ++q4)
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const int key = key0 + q4 * 32 + e;
-                            if (key < lo || key >= hi) s[q4][e] = __float_as_uint(masked_s);
-                        }
+                            for (int e = 0; e < 32; ++e)
+                                if (q4 * 32 + e < vlo || q4 * 32 + e >= vhi) s[q4][e] = __float_as_uint(masked_s);
+                    } else {  // no window: vlo <= 0, only the end of the range cuts
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                if (q4 * 32 + e >= vhi) s[q4][e] = __float_as_uint(masked_s);
+                    }
                 }
                 // row maximum (minimum for a negative scale) in four independent
                 // chains of three-input operations
