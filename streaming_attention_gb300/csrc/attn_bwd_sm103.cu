@@ -24,6 +24,9 @@
 //     dS over dP, dQ += dS K.
 // S and dP are thus computed twice (7 products instead of 5); in exchange
 // neither kernel needs atomics or a transpose through shared memory.
+// The elementwise passes run on packed FP32 pairs (fma/add/mul.f32x2; the row
+// statistics are stored negated for that), and each kernel's outputs leave
+// through the idle stage ring as swizzled boxes stored by TMA.
 // Tiles outside the causal / window range are skipped; only edge tiles mask.
 // Every wait is bounded (1 s); on expiry a CTA sets the device status word,
 // drains its copies and MMAs, frees TMEM and exits.
@@ -57,10 +60,10 @@ struct BCfg {
     static constexpr int kStages = 2;
     static constexpr int kOffStat = 0;                                  // 2 stationary tiles
     static constexpr int kOffStage = 2 * kTile;                         // stage s: 2 tiles at + s * 2 * kTile
-    static constexpr int kOffVec = kOffStage + kStages * 2 * kTile;     // stage s: lse2[128], delta[128]
+    static constexpr int kOffVec = kOffStage + kStages * 2 * kTile;     // stage s: nlse2[128], ndelta[128]
     static constexpr int kOffBar = kOffVec + kStages * 2 * BT * 4;
-    // stat_full, full[2], empty[2], st_full[2], p_full[2], done, drain
-    static constexpr int kNumBars = 1 + 2 * kStages + 6;
+    // stat_full, full[2], empty[2], st_full[2], p_full[2], done, drain, ep
+    static constexpr int kNumBars = 1 + 2 * kStages + 7;
     static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
     static constexpr int kSmem = kOffMisc + 16 + 1024;
     // TMEM columns
@@ -71,8 +74,10 @@ struct BCfg {
 struct BwdParams {
     void* out0;          // dK (dK/dV kernel) or dQ (dQ kernel)
     void* out1;          // dV (dK/dV kernel)
-    const float* lse2;   // [B*Hq][Mpad]: lse * log2(e); -inf past M
-    const float* delta;  // [B*Hq][Mpad]: rowsum(dO * O); 0 past M
+    // per-row statistics, negated so that the elementwise passes add them with packed
+    // FMA/add instructions (which have no negated operand)
+    const float* nlse2;   // [B*Hq][Mpad]: -lse * log2(e); +inf past M (those rows are masked)
+    const float* ndelta;  // [B*Hq][Mpad]: -rowsum(dO * O); 0 past M
     int* status;
     int Hq, Hkv, M, N, G, Mpad;
     int causal, window;
@@ -167,31 +172,42 @@ __device__ __forceinline__ uint32_t bpack2(float lo, float hi) {
     return kBF16 ? pack_bf16(lo, hi) : pack_f16(lo, hi);
 }
 
-// Writes half `half` of one [D] row of FP32 TMEM columns (this thread's lane) as
-// 16-bit values.
+// Output epilogue through shared memory: once the last product has completed,
+// the stage ring is idle, so it holds the outputs as 128-row x 64-column boxes
+// (16 KB each, in the TMA's 128-byte swizzle) that one thread stores with TMA
+// copies (a row-per-thread global store touches 32 rows per instruction).
+// Warp column half `half` owns columns [half D / 2, (half + 1) D / 2) of every
+// output; this thread writes its lane's row r of them, times `mul`, as 16 bits.
 template <int D, bool kBF16>
-__device__ __forceinline__ void store_row(uint32_t taddr, float mul, uint16_t* dst, bool write, int half) {
+__device__ __forceinline__ void stage_row(uint32_t taddr, float mul, uint32_t boxes, int r, int half) {
+    const uint64_t m2 = f2_pack(mul, mul);
 #pragma unroll
     for (int c = 0; c < D / 64; ++c) {
-        const int ch = half * (D / 64) + c;
+        const int col0 = half * (D / 2) + c * 32;  // 32 columns per TMEM load
         uint32_t v[32];
-        tmem_ld_x32(taddr + ch * 32, v);
+        tmem_ld_x32(taddr + col0, v);
         tmem_wait_ld_x32(v);
-        uint32_t w[16];
+        const uint32_t row = boxes + (col0 / 64) * (BT * 128) + r * 128;
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-            w[e] = bpack2<kBF16>(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
-        if (write) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + ch * 32);
+        for (int c8 = 0; c8 < 4; ++c8) {  // 16-byte chunk (col0 % 64) / 8 + c8 of the box row
+            uint32_t w4[4];
 #pragma unroll
-            for (int x = 0; x < 4; ++x) d4[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+            for (int e = 0; e < 4; ++e) {
+                float y0, y1;
+                f2_unpack(f2_mul(f2_pack(__uint_as_float(v[c8 * 8 + 2 * e]), __uint_as_float(v[c8 * 8 + 2 * e + 1])),
+                                 m2),
+                          y0, y1);
+                w4[e] = kBF16 ? pack_bf16(y0, y1) : pack_f16(y0, y1);
+            }
+            const int chunk = (col0 % 64) / 8 + c8;
+            st_shared_v4(row + ((chunk ^ (r & 7)) << 4), w4[0], w4[1], w4[2], w4[3]);
         }
     }
 }
 
 // Shared setup of both kernels: barriers, TMEM (512 columns), abort flag.
 struct BSetup {
-    uint32_t sbase, bar_stat, bar_full0, bar_empty0, bar_st0, bar_p0, bar_done, bar_drain, tmem;
+    uint32_t sbase, bar_stat, bar_full0, bar_empty0, bar_st0, bar_p0, bar_done, bar_drain, bar_ep, tmem;
     volatile uint32_t* abort_flag;
     __device__ uint32_t full(int s) const { return bar_full0 + 8u * s; }
     __device__ uint32_t empty(int s) const { return bar_empty0 + 8u * s; }
@@ -211,6 +227,7 @@ __device__ __forceinline__ BSetup bwd_setup(uint8_t* smem) {
     b.bar_p0 = b.bar_st0 + 16;
     b.bar_done = b.bar_p0 + 16;
     b.bar_drain = b.bar_done + 8;
+    b.bar_ep = b.bar_drain + 8;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc);
     b.abort_flag = tmem_slot + 1;
     if (threadIdx.x == 0) {
@@ -225,6 +242,7 @@ __device__ __forceinline__ BSetup bwd_setup(uint8_t* smem) {
         }
         mbar_init(b.bar_done, 1);
         mbar_init(b.bar_drain, 1);
+        mbar_init(b.bar_ep, 8);  // one arrival per elementwise warp: its output rows are staged
         *b.abort_flag = 0u;
         fence_mbar_init();
     }
@@ -248,6 +266,22 @@ __device__ __forceinline__ void bwd_teardown(const BSetup& b) {
     }
 }
 
+// Thread 0 stores the staged boxes (per output, D / 64 boxes of 64 columns) once
+// all eight elementwise warps have arrived, then waits for the copies to complete.
+template <int D>
+__device__ __forceinline__ void store_boxes(const BSetup& b, uint32_t boxes, const CUtensorMap* out0,
+                                            const CUtensorMap* out1, int nout, int row0, int z, int* status) {
+    if (threadIdx.x != 0) return;
+    const bool ready = bwait_one(b.bar_ep, 0, b.abort_flag, status);
+    if (!ready || *b.abort_flag) return;
+    constexpr int per = D / 64;
+    for (int o = 0; o < nout; ++o)
+        for (int h = 0; h < per; ++h)
+            tma_store_3d(o ? out1 : out0, boxes + (o * per + h) * (BT * 128), h * 64, row0, z);
+    bulk_commit();
+    bulk_wait_all();
+}
+
 // ---------------------------------------------------------------------------
 // dK / dV: one CTA per (128-key tile, KV head)
 // ---------------------------------------------------------------------------
@@ -255,6 +289,7 @@ template <int D, bool kBF16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                         const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
                          const BwdParams p) {
     using C = BCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -305,8 +340,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     tma_load_3d(dq + C::kTile + c * C::kChunk, &tmdO, c * 64, i0, bh, bs.full(s));
                 }
                 const uint32_t vec = bs.sbase + C::kOffVec + s * 2 * BT * 4;
-                bulk_g2s(vec, p.lse2 + (size_t)bh * p.Mpad + i0, BT * 4, bs.full(s));
-                bulk_g2s(vec + BT * 4, p.delta + (size_t)bh * p.Mpad + i0, BT * 4, bs.full(s));
+                bulk_g2s(vec, p.nlse2 + (size_t)bh * p.Mpad + i0, BT * 4, bs.full(s));
+                bulk_g2s(vec + BT * 4, p.ndelta + (size_t)bh * p.Mpad + i0, BT * 4, bs.full(s));
                 issued = it + 1;
             }
             // every issued copy lands before the CTA may exit
@@ -377,8 +412,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const bool need_mask = (i0 + BT > p.M) || (k0 + BT > p.N) ||
                                    (p.causal && k0 + BT - 1 > i0 + off) ||
                                    (p.window > 0 && k0 <= i0 + BT - 1 + off - p.window);
-            const float* lse2 = reinterpret_cast<const float*>(smem + C::kOffVec + s * 2 * BT * 4);
-            const float* del = lse2 + BT;
+            const float* nlse2 = reinterpret_cast<const float*>(smem + C::kOffVec + s * 2 * BT * 4);
+            const float* ndel = nlse2 + BT;
+            const uint64_t c2 = f2_pack(c, c);
             // ---- phase A: P^T = exp2(S^T c - lse2), packed over S^T ----
             if (!(ok = bwait_warp(bs.st(0), it & 1, bs.abort_flag, p.status))) break;
             // the stage's row vectors came by bulk copy: observe their barrier too (its
@@ -404,14 +440,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 auto chunk = [&](auto masked) {
 #pragma unroll
                     for (int g4 = 0; g4 < 8; ++g4) {
-                        const float4 l4 = reinterpret_cast<const float4*>(lse2 + c0)[g4];
-                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-                        float pr[4];
+                        const float4 l4 = reinterpret_cast<const float4*>(nlse2 + c0)[g4];
+                        const int e = g4 * 4;
+                        float x[4], pr[4];
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2,
+                                         f2_pack(l4.x, l4.y)),
+                                  x[0], x[1]);
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])), c2,
+                                         f2_pack(l4.z, l4.w)),
+                                  x[2], x[3]);
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
-                            const int e = g4 * 4 + u;
-                            float pv = ex2(fmaf(__uint_as_float(sv[e]), c, -lv[u]));
-                            if (decltype(masked)::value) pv = (e >= elo && e < ehi) ? pv : 0.f;
+                            float pv = ex2(x[u]);
+                            if (decltype(masked)::value) pv = (e + u >= elo && e + u < ehi) ? pv : 0.f;
                             pr[u] = pv;
                         }
                         pk[2 * g4] = bpack2<kBF16>(pr[0], pr[1]);
@@ -443,15 +484,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 uint32_t dk[16];
 #pragma unroll
                 for (int g4 = 0; g4 < 8; ++g4) {
-                    const float4 d4 = reinterpret_cast<const float4*>(del + c0)[g4];
-                    float p0, p1, p2, p3;
+                    const float4 d4 = reinterpret_cast<const float4*>(ndel + c0)[g4];
+                    float p0, p1, p2, p3, y0, y1, y2, y3;
                     unpack2<kBF16>(pv16[2 * g4], p0, p1);
                     unpack2<kBF16>(pv16[2 * g4 + 1], p2, p3);
                     const int e = g4 * 4;
-                    dk[2 * g4] = bpack2<kBF16>(p0 * (__uint_as_float(dpv[e]) - d4.x),
-                                               p1 * (__uint_as_float(dpv[e + 1]) - d4.y));
-                    dk[2 * g4 + 1] = bpack2<kBF16>(p2 * (__uint_as_float(dpv[e + 2]) - d4.z),
-                                                   p3 * (__uint_as_float(dpv[e + 3]) - d4.w));
+                    f2_unpack(f2_mul(f2_pack(p0, p1), f2_add(f2_pack(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])),
+                                                             f2_pack(d4.x, d4.y))),
+                              y0, y1);
+                    f2_unpack(f2_mul(f2_pack(p2, p3),
+                                     f2_add(f2_pack(__uint_as_float(dpv[e + 2]), __uint_as_float(dpv[e + 3])),
+                                            f2_pack(d4.z, d4.w))),
+                              y2, y3);
+                    dk[2 * g4] = bpack2<kBF16>(y0, y1);
+                    dk[2 * g4 + 1] = bpack2<kBF16>(y2, y3);
                 }
                 tmem_st_x16(bs.tmem + lane_base + C::kColDP + packed_col(q4), dk);
             }
@@ -471,10 +517,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     reinterpret_cast<uint4*>(dv_row)[x] = make_uint4(0, 0, 0, 0);
                 }
             }
-        } else if (ok && bwait_warp(bs.bar_done, 0, bs.abort_flag, p.status)) {
-            tc_fence_after();
-            store_row<D, kBF16>(bs.tmem + lane_base + C::kColAcc0, p.scale, dk_row, write, half);
-            store_row<D, kBF16>(bs.tmem + lane_base + C::kColAcc1, 1.f, dv_row, write, half);
+        } else {
+            const uint32_t boxes = bs.sbase + C::kOffStage;  // dK boxes, then dV boxes
+            if (ok && bwait_warp(bs.bar_done, 0, bs.abort_flag, p.status)) {
+                tc_fence_after();
+                stage_row<D, kBF16>(bs.tmem + lane_base + C::kColAcc0, p.scale, boxes, kl, half);
+                stage_row<D, kBF16>(bs.tmem + lane_base + C::kColAcc1, 1.f, boxes + (D / 64) * BT * 128, kl, half);
+                fence_proxy_async_smem();  // the boxes are read by the TMA (async proxy)
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bs.bar_ep);  // every warp arrives, also after giving up
+            store_boxes<D>(bs, boxes, &tmdK, &tmdV, 2, k0, grp, p.status);
         }
     }
     bwd_teardown(bs);
@@ -487,7 +540,7 @@ template <int D, bool kBF16>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                       const BwdParams p) {
+                       const __grid_constant__ CUtensorMap tmdQ, const BwdParams p) {
     using C = BCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -588,8 +641,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int row = i0 + r;
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const float c = p.scale_log2;
-        const float lse2 = p.lse2[(size_t)bh * p.Mpad + row];  // -inf past M
-        const float del = p.delta[(size_t)bh * p.Mpad + row];
+        const float nlse2 = p.nlse2[(size_t)bh * p.Mpad + row];  // +inf past M (masked)
+        const float ndel = p.ndelta[(size_t)bh * p.Mpad + row];
+        const uint64_t c2 = f2_pack(c, c), nl2 = f2_pack(nlse2, nlse2), nd2 = f2_pack(ndel, ndel);
         const int pos = row + off;
         bool ok = true;
         for (int it = 0; ok && it < T; ++it) {
@@ -619,11 +673,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 auto chunk = [&](auto masked) {
 #pragma unroll
                     for (int e2 = 0; e2 < 16; ++e2) {
-                        float pr[2];
+                        float x[2], pr[2];
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * e2]), __uint_as_float(sv[2 * e2 + 1])), c2, nl2),
+                                  x[0], x[1]);
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
                             const int e = 2 * e2 + u;
-                            float pv = ex2(fmaf(__uint_as_float(sv[e]), c, -lse2));
+                            float pv = ex2(x[u]);
                             if (decltype(masked)::value) pv = (e >= elo && e < ehi) ? pv : 0.f;
                             pr[u] = pv;
                         }
@@ -654,10 +710,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 uint32_t dk[16];
 #pragma unroll
                 for (int e2 = 0; e2 < 16; ++e2) {
-                    float p0, p1;
+                    float p0, p1, y0, y1;
                     unpack2<kBF16>(pv16[e2], p0, p1);
-                    dk[e2] = bpack2<kBF16>(p0 * (__uint_as_float(dpv[2 * e2]) - del),
-                                           p1 * (__uint_as_float(dpv[2 * e2 + 1]) - del));
+                    f2_unpack(f2_mul(f2_pack(p0, p1),
+                                     f2_add(f2_pack(__uint_as_float(dpv[2 * e2]), __uint_as_float(dpv[2 * e2 + 1])), nd2)),
+                              y0, y1);
+                    dk[e2] = bpack2<kBF16>(y0, y1);
                 }
                 tmem_st_x16(bs.tmem + lane_base + C::kColDP + packed_col(q4), dk);
             }
@@ -673,9 +731,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                 for (int x = half * (D / 16); x < (half + 1) * (D / 16); ++x)
                     reinterpret_cast<uint4*>(dq_row)[x] = make_uint4(0, 0, 0, 0);
-        } else if (ok && bwait_warp(bs.bar_done, 0, bs.abort_flag, p.status)) {
-            tc_fence_after();
-            store_row<D, kBF16>(bs.tmem + lane_base + C::kColAcc0, p.scale, dq_row, write, half);
+        } else {
+            const uint32_t boxes = bs.sbase + C::kOffStage;
+            if (ok && bwait_warp(bs.bar_done, 0, bs.abort_flag, p.status)) {
+                tc_fence_after();
+                stage_row<D, kBF16>(bs.tmem + lane_base + C::kColAcc0, p.scale, boxes, r, half);
+                fence_proxy_async_smem();  // the boxes are read by the TMA (async proxy)
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bs.bar_ep);  // every warp arrives, also after giving up
+            store_boxes<D>(bs, boxes, &tmdQ, &tmdQ, 1, i0, bh, p.status);
         }
     }
     bwd_teardown(bs);
@@ -708,14 +773,14 @@ __device__ __forceinline__ float dot8(const uint4& a, const uint4& b) {
     return acc;
 }
 
-// delta = rowsum(dO * O) and lse2 = lse * log2(e) per row, padded to Mpad rows
-// per head (-inf and 0 past M). D / 8 lanes per row, each with one 16-byte load
+// ndelta = -rowsum(dO * O) and nlse2 = -lse * log2(e) per row, padded to Mpad rows
+// per head (+inf and 0 past M). D / 8 lanes per row, each with one 16-byte load
 // of O and of dO, so a warp covers 32 / (D / 8) rows; the row sums reduce
 // within each lane group.
 template <bool kBF16, int D>
 __global__ void __launch_bounds__(256)
     attn_bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ d_o, const float* __restrict__ lse,
-                        float* lse2, float* delta, int M, int Mpad, int rows_pad) {
+                        float* nlse2, float* ndelta, int M, int Mpad, int rows_pad) {
     constexpr int kLanesPerRow = D / 8;
     constexpr int kRowsPerWarp = 32 / kLanesPerRow;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -731,8 +796,8 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int s = kLanesPerRow / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
     if (valid && li == 0) {
-        delta[gr] = i < M ? acc : 0.f;
-        lse2[gr] = i < M ? lse[row] * kLog2e : -INFINITY;
+        ndelta[gr] = i < M ? -acc : 0.f;
+        nlse2[gr] = i < M ? -(lse[row] * kLog2e) : INFINITY;
     }
 }
 
@@ -757,15 +822,18 @@ cudaError_t launch_bwd_t(const Problem& pr, const BwdArgs& a, const float* lse2,
         const_cast<float*>(delta), pr.M, Mpad, rows_pad);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
     if (!make_tensor_map(&tq, a.q, D, pr.M, pr.B * pr.Hq, BT, kBF16) ||
         !make_tensor_map(&tdo, a.d_o, D, pr.M, pr.B * pr.Hq, BT, kBF16) ||
         !make_tensor_map(&tk, a.k, D, pr.N, pr.B * pr.Hkv, BT, kBF16) ||
-        !make_tensor_map(&tv, a.v, D, pr.N, pr.B * pr.Hkv, BT, kBF16))
+        !make_tensor_map(&tv, a.v, D, pr.N, pr.B * pr.Hkv, BT, kBF16) ||
+        !make_tensor_map(&tdq, a.dq, D, pr.M, pr.B * pr.Hq, BT, kBF16) ||
+        !make_tensor_map(&tdk, a.dk, D, pr.N, pr.B * pr.Hkv, BT, kBF16) ||
+        !make_tensor_map(&tdv, a.dv, D, pr.N, pr.B * pr.Hkv, BT, kBF16))
         return cudaErrorInvalidValue;
     BwdParams bp = {};
-    bp.lse2 = lse2;
-    bp.delta = delta;
+    bp.nlse2 = lse2;
+    bp.ndelta = delta;
     bp.status = status;
     bp.Hq = pr.Hq;
     bp.Hkv = pr.Hkv;
@@ -782,14 +850,15 @@ cudaError_t launch_bwd_t(const Problem& pr, const BwdArgs& a, const float* lse2,
     bp.out1 = a.dv;
     bp.groups = pr.B * pr.Hkv;
     bp.ntile = (pr.N + BT - 1) / BT;
-    attn_bwd_dkdv_kernel<D, kBF16><<<bp.groups * bp.ntile, kBwdThreads, C::kSmem, stream>>>(tq, tk, tv, tdo, bp);
+    attn_bwd_dkdv_kernel<D, kBF16><<<bp.groups * bp.ntile, kBwdThreads, C::kSmem, stream>>>(tq, tk, tv, tdo, tdk,
+                                                                                           tdv, bp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // dQ
     bp.out0 = a.dq;
     bp.out1 = nullptr;
     bp.groups = pr.B * pr.Hq;
     bp.ntile = (pr.M + BT - 1) / BT;
-    attn_bwd_dq_kernel<D, kBF16><<<bp.groups * bp.ntile, kBwdThreads, C::kSmem, stream>>>(tq, tk, tv, tdo, bp);
+    attn_bwd_dq_kernel<D, kBF16><<<bp.groups * bp.ntile, kBwdThreads, C::kSmem, stream>>>(tq, tk, tv, tdo, tdq, bp);
     return cudaGetLastError();
 }
 

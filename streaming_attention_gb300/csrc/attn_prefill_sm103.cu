@@ -28,10 +28,13 @@
 // loaded as soon as the last score product of the current one has read Q, and
 // the next tile's first value product into O_t waits only until the epilogue
 // of the current tile has pulled O_t out of TMEM, so epilogues overlap MMAs.
-// The epilogue writes each normalized 64-column half of a query tile into a
-// 16 KB staging box in shared memory (in the TMA's 128-byte swizzle) and one
-// thread stores it with a TMA copy: a row-per-thread global store would touch
-// 32 rows per instruction and hold up the next tile's TMEM reads behind it.
+// The epilogue goes through shared memory: each softmax warp writes its 32
+// normalized rows of a 64-column half into its own 4 KB area (16-byte chunks in
+// a 128-byte swizzle) and copies them out with stores of four whole 128-byte
+// row segments per instruction. A row-per-thread global store would touch 32
+// rows per instruction and hold up the next tile's TMEM reads; a TMA store of
+// the area would queue behind the next tile's Q and K/V loads in the SM's TMA
+// unit (measured: about 4,000 cycles at every work-tile transition).
 //
 // The single MMA-issuing thread keeps the tensor pipe fed only if it spends
 // little time between MMA groups (the pipe queues about one MMA), so it makes
@@ -82,13 +85,11 @@ struct Cfg {
     static constexpr int kStages = (kRowBytes == 256) ? 4 : 8;
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = NQ * kTileBytes;
-    // output staging: one 128-row x 128-byte box per query tile (64 output columns,
-    // 16-bit), written by the softmax warps and stored to global memory by TMA
-    static constexpr int kStageBytes = BM * 128;
+    // output staging: 4 KB per softmax warp (its 32 rows x 64 columns of 16-bit output)
     static constexpr int kStageOff = kKVOff + kStages * kTileBytes;
-    static constexpr int kBarOff = kStageOff + NQ * kStageBytes;
-    // q_full, q_free, full[S], empty[S], s_full[2], p_full[2], o_final, o_free[2], drain, stg_full[2], stg_free[2]
-    static constexpr int kNumBars = 2 + 2 * kStages + 2 + 2 + 1 + 2 + 1 + 2 + 2;
+    static constexpr int kBarOff = kStageOff + 8 * 4096;
+    // q_full, q_free, full[S], empty[S], s_full[2], p_full[2], o_final, o_free[2], drain
+    static constexpr int kNumBars = 2 + 2 * kStages + 2 + 2 + 1 + 2 + 1;
     static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
 };
@@ -115,9 +116,7 @@ struct PrefillParams {
 };
 
 struct Bars {
-    uint32_t q_full, q_free, full0, empty0, s0, p0, o_final, o_free0, drain, stg_full0, stg_free0;
-    __device__ uint32_t stg_full(int t) const { return stg_full0 + 8u * t; }
-    __device__ uint32_t stg_free(int t) const { return stg_free0 + 8u * t; }
+    uint32_t q_full, q_free, full0, empty0, s0, p0, o_final, o_free0, drain;
     __device__ uint32_t full(int s) const { return full0 + 8u * s; }
     __device__ uint32_t empty(int s) const { return empty0 + 8u * s; }
     __device__ uint32_t s_full(int t) const { return s0 + 8u * t; }
@@ -188,44 +187,6 @@ __device__ bool wait_warp(uint32_t bar, uint32_t parity, volatile uint32_t* abor
     }
 }
 
-// Packed FP32 pairs (lo in the low word): one fma/add/mul.f32x2 instruction
-// does the work of two, which matters because the softmax warps share each SM
-// sub-partition's issue slots with the MMA-issuing and TMA threads.
-__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-// three-input maximum / minimum (one instruction for two new values)
-__device__ __forceinline__ float max3f(float a, float b, float c) {
-    float r;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-    return r;
-}
-__device__ __forceinline__ float min3f(float a, float b, float c) {
-    float r;
-    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-    return r;
-}
-
 template <bool kBF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     return kBF16 ? pack_bf16(lo, hi) : pack_f16(lo, hi);
@@ -267,8 +228,7 @@ __device__ __forceinline__ void mma_group_pv(uint32_t d_tmem, uint32_t a_tmem, u
 template <int D, int kIn, bool kBF16>  // kBF16: output type (and input type for 16-bit inputs)
 __global__ void __launch_bounds__(kThreads, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                        const PrefillParams p) {
+                        const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
     constexpr int EB = kIn == kInE4M3 ? 1 : 2;
     using C = Cfg<D, EB>;
     constexpr int kHalf = C::kStages / 2;  // empty barriers: one per pair of slots freed together
@@ -288,8 +248,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     bar.o_final = bar.p0 + 16;
     bar.o_free0 = bar.o_final + 8;
     bar.drain = bar.o_free0 + 16;
-    bar.stg_full0 = bar.drain + 8;
-    bar.stg_free0 = bar.stg_full0 + 16;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff);
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
@@ -309,10 +267,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(bar.o_final, 1);
         mbar_init(bar.drain, 1);
-        for (int t = 0; t < NQ; ++t) {
-            mbar_init(bar.stg_full(t), 4);  // one arrival per softmax warp of the tile
-            mbar_init(bar.stg_free(t), 1);  // the tile's storing thread
-        }
         *abort_flag = 0u;
         fence_mbar_init();
     }
@@ -331,7 +285,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tmQ);
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
-            prefetch_tmap(&tmO);
             int u = 0, tc = 0;  // ring position and work tiles with keys, across the whole walk
             int q_issued = 0;   // Q loads issued
             bool ok = true;
@@ -453,7 +406,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float masked_s = c >= 0.f ? -INFINITY : INFINITY;  // scores that give t = -inf
         const int off = p.N - p.M;
         int g = 0, tc = 0;  // score tiles and work tiles with keys, across the walk
-        int nst = 0;        // output boxes stored from this tile's staging buffer
         bool ok = true;
         Work wk;
         for (int w = 0; ok && work_tile(p, w, &wk); ++w) {
@@ -625,10 +577,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
 
             // ---------------- epilogue: O / l, one cast, rows < M ----------------
-            // Per 64-column half: the four warps of the tile write their rows, normalized
-            // and cast, into the tile's staging box (128-byte swizzle, as the tensor map
-            // expects), and the tile's first thread stores the box with one TMA copy,
-            // which writes rows < M only.
+            // Per 64-column half: each warp writes its 32 rows, normalized and cast,
+            // into its own 4 KB staging area (16-byte chunks in a 128-byte swizzle, so
+            // neither the writes nor the reads conflict), then copies them out with
+            // 16-byte stores of four whole 128-byte row segments per instruction
+            // (a row-per-thread store would touch 32 rows per instruction).
             if (!(ok = wait_warp(bar.o_final, tc & 1, abort_flag, p.status))) break;
             ++tc;
             tc_fence_after();
@@ -636,9 +589,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // log sum_j e^(scale s_j) = ln 2 * (m_ref + log2 l) (p was taken against m_ref)
             if (p.lse && row < p.M)
                 p.lse[(size_t)wk.bh * p.M + row] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
-            const uint32_t stg = sStage + t * C::kStageBytes;
-            const uint32_t my_row = stg + r_in_tile * 128;
+            const uint32_t wst = sStage + (t * 4 + wq) * 4096;  // this warp's staging area
             const uint64_t inv2 = f2_pack(inv, inv);
+            char* obase = reinterpret_cast<char*>(p.o) + ((size_t)wk.bh * p.M + wk.row0 + t * BM + wq * 32) * (D * 2);
+            const int rows_left = p.M - (wk.row0 + t * BM + wq * 32);  // rows of this warp below M
 #pragma unroll
             for (int h = 0; h < D / 64; ++h) {
                 uint32_t o[2][32];
@@ -652,8 +606,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar.o_free(t));
                 }
-                // the box's previous store must have read it
-                if (nst > 0 && !(ok = wait_warp(bar.stg_free(t), (nst - 1) & 1, abort_flag, p.status))) break;
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8) {  // 16-byte chunk c8: columns 8 c8 .. 8 c8 + 7 of the half
                     uint32_t w4[4];
@@ -667,27 +619,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   y0, y1);
                         w4[e] = pack2<kBF16>(y0, y1);
                     }
-                    st_shared_v4(my_row + ((c8 ^ (r_in_tile & 7)) << 4), w4[0], w4[1], w4[2], w4[3]);
+                    st_shared_v4(wst + lane * 128 + ((c8 ^ (lane & 7)) << 4), w4[0], w4[1], w4[2], w4[3]);
                 }
-                fence_proxy_async_smem();  // the box is read by the TMA (async proxy)
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar.stg_full(t));
-                if (wq == 0 && lane == 0) {
-                    if ((ok = wait_one(bar.stg_full(t), nst & 1, abort_flag, p.status))) {
-                        tma_store_3d(&tmO, stg, h * 64, wk.row0 + t * BM, wk.bh);
-                        bulk_commit();
-                        bulk_wait_read0();  // the box may be written again
-                        mbar_arrive(bar.stg_free(t));
-                    }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {  // rows 4 i .. 4 i + 3 of the warp, one 16-byte chunk per lane
+                    const int rr = 4 * i + (lane >> 3), ch = lane & 7;
+                    const uint4 v4 = ld_shared_v4(wst + rr * 128 + ((ch ^ (rr & 7)) << 4));
+                    if (rr < rows_left)
+                        *reinterpret_cast<uint4*>(obase + (size_t)rr * (D * 2) + h * 128 + ch * 16) = v4;
                 }
-                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                ++nst;
-                if (!ok) break;
+                __syncwarp();  // the area is read before the next half overwrites it
             }
-            if (!ok) break;
         }
-        // every output copy this thread issued must complete before the CTA exits
-        if (wq == 0 && lane == 0) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -711,11 +655,10 @@ int launch_t(const Problem& pr, const void* q, const void* k, const void* v, voi
         return ATTN_ERR_CUDA;
     const int sms = device_sm_count();
     if (sms <= 0) return ATTN_ERR_CUDA;
-    CUtensorMap tq, tk, tv, to;
+    CUtensorMap tq, tk, tv;
     if (!make_tensor_map(&tq, q, D, pr.M, pr.B * pr.Hq, BM, kBF16, EB) ||
         !make_tensor_map(&tk, k, D, pr.N, pr.B * pr.Hkv, BN, kBF16, EB) ||
-        !make_tensor_map(&tv, v, D, pr.N, pr.B * pr.Hkv, BN, kBF16, EB) ||
-        !make_tensor_map(&to, o, D, pr.M, pr.B * pr.Hq, BM, kBF16, 2))
+        !make_tensor_map(&tv, v, D, pr.N, pr.B * pr.Hkv, BN, kBF16, EB))
         return ATTN_ERR_CUDA;
     PrefillParams pp;
     pp.o = o;
@@ -735,7 +678,7 @@ int launch_t(const Problem& pr, const void* q, const void* k, const void* v, voi
     pp.tiles = pp.BH * pp.nqb;
     pp.withhold_p_at = withhold_p_at;
     const int grid = pp.tiles < sms ? pp.tiles : sms;
-    attn_prefill_kernel<D, kIn, kBF16><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, pp);
+    attn_prefill_kernel<D, kIn, kBF16><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, pp);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
