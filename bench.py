@@ -476,12 +476,17 @@ def extra_measurements(args, dev, stream, flush):
                             ("prefill_d64_bf16_noncausal", PREFILL_D64, False),
                             ("prefill_d64_bf16_causal", PREFILL_D64, True),
                             ("long_causal_16k_fp16", LONG_CAUSAL, True),
+                            # the pair-MMA prefill (explicit path; AUTO runs the one-CTA kernel)
+                            ("prefill_d128_bf16_causal_pair", PREFILL_D128, True),
+                            ("prefill_d128_bf16_noncausal_pair", PREFILL_D128, False),
                             ("decode_gqa", DECODE_GQA, DECODE_GQA.causal)):
         if name.startswith(("prefill", "long")) and args.workload != PREFILL_D128.name:
             continue
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size
         _, sets, _ = rotation(w, dev, l2)
         path, pname = chosen_path(w)
+        if name.endswith("_pair"):
+            path, pname = sa.PATH_PREFILL_PAIR, "prefill pair MMA (cta_group::2)"
         nb = sa.attn_workspace_bytes_ex(w.B, w.Hq, w.Hkv, w.M, w.N, w.D, causal, w.window, path)
         ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
 

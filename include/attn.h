@@ -97,8 +97,11 @@ typedef enum {
     ATTN_PATH_AUTO = 0,
     ATTN_PATH_SIMT = 1,    /* CUDA-core streaming kernel, any supported D, B*Hq <= 65535 */
     ATTN_PATH_PREFILL = 2, /* warp-specialized TMA + tcgen05 + TMEM kernel, D in {64,128} */
-    ATTN_PATH_DECODE = 3   /* split-KV over grouped query heads; the splits merged in a thread-block
+    ATTN_PATH_DECODE = 3,  /* split-KV over grouped query heads; the splits merged in a thread-block
                               cluster (at most 8 splits per KV head) or by the merge kernel */
+    ATTN_PATH_PREFILL_PAIR = 4 /* the prefill on the pair MMA (tcgen05 cta_group::2): clusters of two
+                              CTAs share 512-row work tiles, each loading half of every K/V tile;
+                              D = 128, BF16/FP16; never chosen by AUTO */
 } attn_path_t;
 
 /* Forward attention, the library's main entry point.

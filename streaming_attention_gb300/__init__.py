@@ -12,6 +12,7 @@ from .binding import (  # noqa: F401
     PATH_AUTO,
     PATH_DECODE,
     PATH_PREFILL,
+    PATH_PREFILL_PAIR,
     PATH_SIMT,
     AttnError,
     attention,

@@ -17,7 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_FILE = os.path.join(_HERE, "libattn_gb300.so")
 
 ATTN_BF16, ATTN_FP16, ATTN_FP32 = 0, 1, 2
-PATH_AUTO, PATH_SIMT, PATH_PREFILL, PATH_DECODE = 0, 1, 2, 3
+PATH_AUTO, PATH_SIMT, PATH_PREFILL, PATH_DECODE, PATH_PREFILL_PAIR = 0, 1, 2, 3, 4
 ATTN_OK = 0
 
 _DTYPES = {torch.bfloat16: ATTN_BF16, torch.float16: ATTN_FP16, torch.float32: ATTN_FP32}

@@ -101,6 +101,7 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CU
 int run(const Problem& p, const void* q, const void* k, const void* v, void* o, int path, void* ws,
         size_t ws_bytes, cudaStream_t stream) {
     if (path == ATTN_PATH_PREFILL && p.D != 64 && p.D != 128) return ATTN_ERR_HEADDIM;
+    if (path == ATTN_PATH_PREFILL_PAIR && p.D != 128) return ATTN_ERR_HEADDIM;
     if (path == ATTN_PATH_DECODE && !decode_supported(p)) return ATTN_ERR_HEADDIM;
     if (empty_output(p)) return ATTN_OK;
     const bool simt = p.N == 0 ? p.lse != nullptr
@@ -119,6 +120,9 @@ int run(const Problem& p, const void* q, const void* k, const void* v, void* o, 
         case ATTN_PATH_PREFILL:
             if (!prefill_supported(p)) return ATTN_ERR_PATH;
             return launch_prefill(p, q, k, v, o, status, stream);
+        case ATTN_PATH_PREFILL_PAIR:
+            if (!prefill_pair_supported(p)) return ATTN_ERR_PATH;
+            return launch_prefill_pair(p, q, k, v, o, status, stream);
         case ATTN_PATH_DECODE: {
             int chunk = 0, S = 0;
             int rc = decode_plan(p, &chunk, &S);
@@ -279,7 +283,7 @@ extern "C" {
 int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, int B, int Hq, int Hkv, int M, int N, int D,
                 int causal, int window, float scale, attn_dtype_t dtype, int path, void* workspace, size_t ws_bytes,
                 void* stream) {
-    if (path < ATTN_PATH_AUTO || path > ATTN_PATH_DECODE) return ATTN_ERR_PATH;
+    if (path < ATTN_PATH_AUTO || path > ATTN_PATH_PREFILL_PAIR) return ATTN_ERR_PATH;
     Problem p;
     int rc = validate(q, k, v, o, B, Hq, Hkv, M, N, D, causal, window, scale, dtype, &p);
     if (rc != ATTN_OK) return rc;
@@ -305,7 +309,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, int B, int Hq
 int attn_fwd_lse(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int M,
                  int N, int D, int causal, int window, float scale, attn_dtype_t dtype, int path, void* workspace,
                  size_t ws_bytes, void* stream) {
-    if (path < ATTN_PATH_AUTO || path > ATTN_PATH_DECODE) return ATTN_ERR_PATH;
+    if (path < ATTN_PATH_AUTO || path > ATTN_PATH_PREFILL_PAIR) return ATTN_ERR_PATH;
     Problem p;
     int rc = validate(q, k, v, o, B, Hq, Hkv, M, N, D, causal, window, scale, dtype, &p);
     if (rc != ATTN_OK) return rc;
@@ -329,7 +333,7 @@ size_t attn_workspace_bytes_ex(int B, int Hq, int Hkv, int M, int N, int D, int 
     static const int16_t dummy[8] __attribute__((aligned(16))) = {};
     if (validate(dummy, dummy, dummy, dummy, B, Hq, Hkv, M, N, D, causal, window, 0.f, ATTN_BF16, &p) != ATTN_OK)
         return 0;
-    if (path < ATTN_PATH_AUTO || path > ATTN_PATH_DECODE) return 0;
+    if (path < ATTN_PATH_AUTO || path > ATTN_PATH_PREFILL_PAIR) return 0;
     if (empty_output(p) || p.N == 0) return 0;
     return workspace_for(p, choose_path(p, path));
 }

@@ -157,6 +157,11 @@ int* device_status_ptr();
 int launch_prefill(const Problem& p, const void* q, const void* k, const void* v, void* o,
                    int* status, cudaStream_t stream);
 bool prefill_supported(const Problem& p);
+// The pair-MMA prefill (tcgen05 cta_group::2, clusters of two CTAs), D = 128,
+// 16-bit inputs: returns ATTN_OK, ATTN_ERR_HEADDIM or ATTN_ERR_CUDA.
+int launch_prefill_pair(const Problem& p, const void* q, const void* k, const void* v, void* o, int* status,
+                        cudaStream_t stream);
+bool prefill_pair_supported(const Problem& p);
 // The prefill kernel with one P-ready arrival withheld (failure-path self-test;
 // D = 128): its bounded waits run out and every CTA takes the abort path.
 int launch_prefill_withheld(const Problem& p, const void* q, const void* k, const void* v, void* o, int* status,

@@ -75,10 +75,16 @@ def test_forced_path_checks(L):
     # an out-of-range path value is rejected before any launch
     st = L.attn_fwd_ex(A16, A16, A16, A16, 1, 2, 2, 8, 8, 64, 0, 0, 0.0, 0, 9, None, 0, None)
     assert st == -11
-    # decode and prefill need D in {64, 128}
-    for path in (sa.PATH_DECODE, sa.PATH_PREFILL):
+    # decode and prefill need D in {64, 128}; the pair-MMA prefill D = 128
+    for path in (sa.PATH_DECODE, sa.PATH_PREFILL, sa.PATH_PREFILL_PAIR):
         st = L.attn_fwd_ex(A16, A16, A16, A16, 1, 2, 2, 8, 8, 32, 0, 0, 0.0, 0, path, None, 0, None)
         assert st == -4, path
+    assert L.attn_fwd_ex(A16, A16, A16, A16, 1, 2, 2, 8, 8, 64, 0, 0, 0.0, 0, sa.PATH_PREFILL_PAIR, None, 0,
+                         None) == -4
+    assert L.attn_fwd_ex(A16, A16, A16, A16, 1, 2, 2, 8, 8, 128, 0, 0, 0.0, 0, 5, None, 0, None) == -11
+    # the E4M3 entry point offers neither the CUDA-core nor the pair path
+    assert L.attn_fwd_fp8(A16, A16, A16, A16, None, 1, 2, 2, 8, 8, 128, 0, 0, 0.0, 1.0, 1.0, 1.0, 0,
+                          sa.PATH_PREFILL_PAIR, None, 0, None) == -11
 
 
 def test_simt_grid_limit(L):
