@@ -121,13 +121,30 @@ __device__ bool bwait_warp(uint32_t bar, uint32_t parity, volatile uint32_t* abo
     }
 }
 
+// Warp-uniform bounded wait that ignores the abort flag (for the final drain).
+__device__ bool bwait_warp_final(uint32_t bar, uint32_t parity, int* status) {
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+        int stop = 0;
+        if ((threadIdx.x & 31) == 0 && globaltimer_ns() - t0 > kBwdTimeoutNs) {
+            atomicExch(status, 1);
+            stop = 1;
+        }
+        if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+    }
+}
+
+// The MMA issuer is a whole warp: every lane runs the issuing loop, so operands
+// stay warp-uniform, and one elected lane issues each MMA and commit (the _el
+// forms). The two helpers below are called by that warp only.
 // C = A B^T over D (both operands K-major [128][D] tiles, 128 x 128 result)
 template <int D>
 __device__ __forceinline__ void mma_rows_by_rows(uint32_t d_tmem, uint64_t a0, uint64_t b0, uint32_t idesc) {
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
         const uint64_t off = (uint64_t)((((kk >> 2) * BCfg<D>::kChunk) + (kk & 3) * 32) >> 4);
-        mma_ss(d_tmem, a0 + off, b0 + off, idesc, kk > 0 ? 1u : 0u);
+        mma_ss_el(d_tmem, a0 + off, b0 + off, idesc, kk > 0 ? 1u : 0u);
     }
 }
 // A 16-bit operand of 128 along K lives in TMEM as two packed blocks: K 0..63 in
@@ -142,7 +159,7 @@ __device__ __forceinline__ void mma_tmem_by_tile(uint32_t d_tmem, uint32_t a_tme
                                                  bool first) {
 #pragma unroll
     for (int kk = 0; kk < BT / 16; ++kk)
-        mma_ts(d_tmem, a_tmem + (kk >> 2) * 64 + (kk & 3) * 8, b0 + (uint64_t)((kk * 16 * 128) >> 4), idesc,
+        mma_ts_el(d_tmem, a_tmem + (kk >> 2) * 64 + (kk & 3) * 8, b0 + (uint64_t)((kk * 16 * 128) >> 4), idesc,
                (first && kk == 0) ? 0u : 1u);
 }
 
@@ -350,7 +367,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 bwait_one(bs.full(x & 1), (x >> 1) & 1, bs.abort_flag, p.status, false);
         }
     } else if (warp == kBMmaWarp) {
-        if (lane == 0 && T > 0) {
+        if (T > 0) {  // the whole warp (see mma_rows_by_rows)
             constexpr uint32_t idS = idesc_f16(kBF16, BT, BT, false);
             constexpr uint32_t idAcc = idesc_f16(kBF16, BT, D, true);
             const uint64_t dK = sw128_desc(bs.sbase + C::kOffStat, 16, 1024);
@@ -362,14 +379,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             auto stage_q = [&](int it) { return bs.sbase + C::kOffStage + (it & 1) * 2 * C::kTile; };
             auto issue_s = [&](int it) {  // S^T = K Q^T
                 mma_rows_by_rows<D>(bs.tmem + C::kColS, dK, sw128_desc(stage_q(it), 16, 1024), idS);
-                mma_commit(bs.st(0));
+                mma_commit_el(bs.st(0));
             };
             auto issue_dp = [&](int it) {  // dP^T = V dO^T
                 mma_rows_by_rows<D>(bs.tmem + C::kColDP, dV, sw128_desc(stage_q(it) + C::kTile, 16, 1024), idS);
-                mma_commit(bs.st(1));
+                mma_commit_el(bs.st(1));
             };
-            bool ok = bwait_one(bs.bar_stat, 0, bs.abort_flag, p.status) &&
-                      bwait_one(bs.full(0), 0, bs.abort_flag, p.status);
+            bool ok = bwait_warp(bs.bar_stat, 0, bs.abort_flag, p.status) &&
+                      bwait_warp(bs.full(0), 0, bs.abort_flag, p.status);
             if (ok) {
                 tc_fence_after();
                 issue_s(0);
@@ -377,26 +394,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             for (int it = 0; ok && it < T; ++it) {
                 const uint32_t sq = stage_q(it);
-                if (!(ok = bwait_one(bs.pp(0), it & 1, bs.abort_flag, p.status))) break;
+                if (!(ok = bwait_warp(bs.pp(0), it & 1, bs.abort_flag, p.status))) break;
                 tc_fence_after();
                 mma_tmem_by_tile(bs.tmem + C::kColAcc1, bs.tmem + C::kColS, sw128_desc(sq + C::kTile, C::kChunk, 1024),
                                  idAcc, it == 0);  // dV += P^T dO
-                if (!(ok = bwait_one(bs.pp(1), it & 1, bs.abort_flag, p.status))) break;
+                if (!(ok = bwait_warp(bs.pp(1), it & 1, bs.abort_flag, p.status))) break;
                 tc_fence_after();
                 const bool more = it + 1 < T;
                 if (more) {
-                    if (!(ok = bwait_one(bs.full((it + 1) & 1), ((it + 1) >> 1) & 1, bs.abort_flag, p.status))) break;
+                    if (!(ok = bwait_warp(bs.full((it + 1) & 1), ((it + 1) >> 1) & 1, bs.abort_flag, p.status))) break;
                     tc_fence_after();
                     issue_s(it + 1);
                 }
                 mma_tmem_by_tile(bs.tmem + C::kColAcc0, bs.tmem + C::kColDP, sw128_desc(sq, C::kChunk, 1024), idAcc,
                                  it == 0);  // dK += dS^T Q
-                mma_commit(bs.empty(it & 1));  // Q, dO of this tile fully read
+                mma_commit_el(bs.empty(it & 1));  // Q, dO of this tile fully read
                 if (more) issue_dp(it + 1);
             }
-            if (ok) mma_commit(bs.bar_done);
-            mma_commit(bs.bar_drain);
-            bwait_one(bs.bar_drain, 0, bs.abort_flag, p.status, false);
+            if (ok) mma_commit_el(bs.bar_done);
+            mma_commit_el(bs.bar_drain);
+            bwait_warp_final(bs.bar_drain, 0, p.status);
         }
         __syncwarp();
     } else {
@@ -591,7 +608,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 bwait_one(bs.full(x & 1), (x >> 1) & 1, bs.abort_flag, p.status, false);
         }
     } else if (warp == kBMmaWarp) {
-        if (lane == 0 && T > 0) {
+        if (T > 0) {  // the whole warp (see mma_rows_by_rows)
             constexpr uint32_t idS = idesc_f16(kBF16, BT, BT, false);
             constexpr uint32_t idAcc = idesc_f16(kBF16, BT, D, true);
             const uint64_t dQ = sw128_desc(bs.sbase + C::kOffStat, 16, 1024);
@@ -601,14 +618,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             auto stage_k = [&](int it) { return bs.sbase + C::kOffStage + (it & 1) * 2 * C::kTile; };
             auto issue_s = [&](int it) {  // S = Q K^T
                 mma_rows_by_rows<D>(bs.tmem + C::kColS, dQ, sw128_desc(stage_k(it), 16, 1024), idS);
-                mma_commit(bs.st(0));
+                mma_commit_el(bs.st(0));
             };
             auto issue_dp = [&](int it) {  // dP = dO V^T
                 mma_rows_by_rows<D>(bs.tmem + C::kColDP, ddO, sw128_desc(stage_k(it) + C::kTile, 16, 1024), idS);
-                mma_commit(bs.st(1));
+                mma_commit_el(bs.st(1));
             };
-            bool ok = bwait_one(bs.bar_stat, 0, bs.abort_flag, p.status) &&
-                      bwait_one(bs.full(0), 0, bs.abort_flag, p.status);
+            bool ok = bwait_warp(bs.bar_stat, 0, bs.abort_flag, p.status) &&
+                      bwait_warp(bs.full(0), 0, bs.abort_flag, p.status);
             if (ok) {
                 tc_fence_after();
                 issue_s(0);
@@ -617,22 +634,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int it = 0; ok && it < T; ++it) {
                 const uint32_t sk = stage_k(it);
                 const bool more = it + 1 < T;
-                if (!(ok = bwait_one(bs.pp(0), it & 1, bs.abort_flag, p.status))) break;
+                if (!(ok = bwait_warp(bs.pp(0), it & 1, bs.abort_flag, p.status))) break;
                 if (more) {
-                    if (!(ok = bwait_one(bs.full((it + 1) & 1), ((it + 1) >> 1) & 1, bs.abort_flag, p.status))) break;
+                    if (!(ok = bwait_warp(bs.full((it + 1) & 1), ((it + 1) >> 1) & 1, bs.abort_flag, p.status))) break;
                     tc_fence_after();
                     issue_s(it + 1);
                 }
-                if (!(ok = bwait_one(bs.pp(1), it & 1, bs.abort_flag, p.status))) break;
+                if (!(ok = bwait_warp(bs.pp(1), it & 1, bs.abort_flag, p.status))) break;
                 tc_fence_after();
                 mma_tmem_by_tile(bs.tmem + C::kColAcc0, bs.tmem + C::kColDP, sw128_desc(sk, C::kChunk, 1024), idAcc,
                                  it == 0);  // dQ += dS K
-                mma_commit(bs.empty(it & 1));  // K, V of this tile fully read
+                mma_commit_el(bs.empty(it & 1));  // K, V of this tile fully read
                 if (more) issue_dp(it + 1);
             }
-            if (ok) mma_commit(bs.bar_done);
-            mma_commit(bs.bar_drain);
-            bwait_one(bs.bar_drain, 0, bs.abort_flag, p.status, false);
+            if (ok) mma_commit_el(bs.bar_done);
+            mma_commit_el(bs.bar_drain);
+            bwait_warp_final(bs.bar_drain, 0, p.status);
         }
         __syncwarp();
     } else {

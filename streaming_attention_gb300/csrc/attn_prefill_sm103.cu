@@ -6,7 +6,7 @@
 //   warps 0-3  softmax + epilogue for query tile 0 (one TMEM lane = one row = one thread)
 //   warps 4-7  softmax + epilogue for query tile 1
 //   warp 8     TMA producer: Q of each work tile, then K_j, V_j through a shared-memory ring
-//   warp 9     MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j
+//   warp 9     MMA issuer (whole warp, one elected lane issues): S_t = Q_t K_j^T and O_t += P_t V_j
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 [384,384+D).
 // P_t (16-bit, two per column) overwrites the first 64 columns of S_t.
 //
@@ -36,9 +36,13 @@
 // the area would queue behind the next tile's Q and K/V loads in the SM's TMA
 // unit (measured: about 4,000 cycles at every work-tile transition).
 //
-// The single MMA-issuing thread keeps the tensor pipe fed only if it spends
-// little time between MMA groups (the pipe queues about one MMA), so it makes
-// one commit per key tile for the ring (after S_1(j), freeing K_j and V_(j-1)
+// The issuer keeps the tensor pipe fed only if it spends little time per MMA
+// and between MMA groups (the pipe queues about one MMA). The whole warp runs
+// the issuing loop, so descriptors and TMEM addresses are warp-uniform values,
+// and one elected lane issues each instruction; run by one divergent thread,
+// the same loop took about 83 cycles per MMA, against 64 of tensor work for a
+// 128 x 128 x 16 product, and the kernel 10 % longer. The issuer also makes one
+// commit per key tile for the ring (after S_1(j), freeing K_j and V_(j-1)
 // together) and tests the readiness of V_j and P_0(j) between the two halves
 // of the S_1(j) group, while queued MMAs run, instead of waiting after it.
 //
@@ -187,6 +191,25 @@ __device__ bool wait_warp(uint32_t bar, uint32_t parity, volatile uint32_t* abor
     }
 }
 
+// Warp-uniform readiness test (true only if every lane saw the phase complete).
+__device__ __forceinline__ bool test_warp(uint32_t bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, mbar_test(bar, parity));
+}
+
+// Warp-uniform bounded wait that ignores the abort flag (for the final drain).
+__device__ bool wait_warp_final(uint32_t bar, uint32_t parity, int* status) {
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+        int stop = 0;
+        if ((threadIdx.x & 31) == 0 && globaltimer_ns() - t0 > kTimeoutNs) {
+            atomicExch(status, 1);
+            stop = 1;
+        }
+        if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+    }
+}
+
 template <bool kBF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     return kBF16 ? pack_bf16(lo, hi) : pack_f16(lo, hi);
@@ -204,9 +227,9 @@ __device__ __forceinline__ void mma_group_s(uint32_t d_tmem, uint64_t a0, uint64
         if (kk == D * EB / 64) between();
         const uint64_t off = (uint64_t)((((kk >> 2) * Cfg<D, EB>::kChunkBytes) + (kk & 3) * 32) >> 4);
         if constexpr (EB == 1)
-            mma_ss_f8(d_tmem, a0 + off, b0 + off, idesc, kk > 0 ? 1u : 0u);
+            mma_ss_f8_el(d_tmem, a0 + off, b0 + off, idesc, kk > 0 ? 1u : 0u);
         else
-            mma_ss(d_tmem, a0 + off, b0 + off, idesc, kk > 0 ? 1u : 0u);
+            mma_ss_el(d_tmem, a0 + off, b0 + off, idesc, kk > 0 ? 1u : 0u);
     }
 }
 // P from TMEM (8 columns per K step: two 16-bit or four 8-bit values per
@@ -219,9 +242,9 @@ __device__ __forceinline__ void mma_group_pv(uint32_t d_tmem, uint32_t a_tmem, u
     for (int kk = 0; kk < BN / kStep; ++kk) {
         const uint64_t b = b0 + (uint64_t)((kk * kStep * 128) >> 4);
         if constexpr (EB == 1)
-            mma_ts_f8(d_tmem, a_tmem + kk * 8, b, idesc, (first && kk == 0) ? 0u : 1u);
+            mma_ts_f8_el(d_tmem, a_tmem + kk * 8, b, idesc, (first && kk == 0) ? 0u : 1u);
         else
-            mma_ts(d_tmem, a_tmem + kk * 8, b, idesc, (first && kk == 0) ? 0u : 1u);
+            mma_ts_el(d_tmem, a_tmem + kk * 8, b, idesc, (first && kk == 0) ? 0u : 1u);
     }
 }
 
@@ -325,7 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issuer ----------------
-        if (lane == 0) {
+        // The whole warp runs the loop (operands stay warp-uniform); one elected lane
+        // issues each MMA and commit.
+        {
             constexpr uint32_t idS = EB == 1 ? idesc_e4m3(BM, BN, false) : idesc_f16(kBF16, BM, BN, false);
             constexpr uint32_t idPV = EB == 1 ? idesc_e4m3(BM, D, true) : idesc_f16(kBF16, BM, D, true);
             int u = 0, tc = 0;
@@ -345,9 +370,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // previous tile's epilogue has read it out
             bool p_ready = false;  // P_0's phase was seen complete in the middle of the S_1 group
             auto issue_pv = [&](int t, int slot, bool first) {
-                if (!(t == 0 && p_ready) && !wait_one(bar.p_full(t), ps[t] & 1, abort_flag, p.status)) return false;
+                if (!(t == 0 && p_ready) && !wait_warp(bar.p_full(t), ps[t] & 1, abort_flag, p.status)) return false;
                 ++ps[t];
-                if (first && tc > 0 && !wait_one(bar.o_free(t), (tc - 1) & 1, abort_flag, p.status)) return false;
+                if (first && tc > 0 && !wait_warp(bar.o_free(t), (tc - 1) & 1, abort_flag, p.status)) return false;
                 tc_fence_after();
                 mma_group_pv<EB>(tmem + col_o(t), tmem + col_s(t), dv + (uint64_t)slot * kSlotStep, idPV, first);
                 return true;
@@ -356,16 +381,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int w = 0; ok && work_tile(p, w, &wk); ++w) {
                 const int n = wk.n;
                 if (n == 0) continue;
-                if (!(ok = wait_one(bar.q_full, tc & 1, abort_flag, p.status))) break;
+                if (!(ok = wait_warp(bar.q_full, tc & 1, abort_flag, p.status))) break;
                 tc_fence_after();
                 int slot_v_prev = 0;
                 for (int jj = 0; jj < n; ++jj) {
                     const int uk = u++, sk = uk % C::kStages;
                     const int uv = u++, sv = uv % C::kStages;
-                    if (!(ok = wait_one(bar.full(sk), (uk / C::kStages) & 1, abort_flag, p.status))) break;
+                    if (!(ok = wait_warp(bar.full(sk), (uk / C::kStages) & 1, abort_flag, p.status))) break;
                     tc_fence_after();
                     issue_s(0, sk);
-                    mma_commit(bar.s_full(0));
+                    mma_commit_el(bar.s_full(0));
                     if (jj > 0) {
                         if (!(ok = issue_pv(1, slot_v_prev, jj - 1 == 0))) break;
                     }
@@ -374,24 +399,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bool v_ready = false;
                     p_ready = false;
                     mma_group_s<D, EB>(tmem + col_s(1), dq1, dk + (uint64_t)sk * kSlotStep, idS, [&] {
-                        v_ready = mbar_test(bar.full(sv), (uv / C::kStages) & 1);
-                        p_ready = mbar_test(bar.p_full(0), ps[0] & 1);
+                        v_ready = test_warp(bar.full(sv), (uv / C::kStages) & 1);
+                        p_ready = test_warp(bar.p_full(0), ps[0] & 1);
                     });
-                    mma_commit(bar.s_full(1));
-                    if (jj == n - 1) mma_commit(bar.q_free);  // Q is read for the last time
-                    mma_commit(bar.empty((uk >> 1) % kHalf));  // K_j and V_(j-1) are read
-                    if (!v_ready && !(ok = wait_one(bar.full(sv), (uv / C::kStages) & 1, abort_flag, p.status))) break;
+                    mma_commit_el(bar.s_full(1));
+                    if (jj == n - 1) mma_commit_el(bar.q_free);  // Q is read for the last time
+                    mma_commit_el(bar.empty((uk >> 1) % kHalf));  // K_j and V_(j-1) are read
+                    if (!v_ready && !(ok = wait_warp(bar.full(sv), (uv / C::kStages) & 1, abort_flag, p.status))) break;
                     if (!(ok = issue_pv(0, sv, jj == 0))) break;
                     slot_v_prev = sv;
                 }
                 if (!ok) break;
                 if (!(ok = issue_pv(1, slot_v_prev, n - 1 == 0))) break;
-                mma_commit(bar.o_final);  // this tile's O_0 and O_1 are final
+                mma_commit_el(bar.o_final);  // this tile's O_0 and O_1 are final
                 ++tc;
             }
             // all MMAs done before TMEM and shared memory are released
-            mma_commit(bar.drain);
-            wait_one(bar.drain, 0, abort_flag, p.status, false);
+            mma_commit_el(bar.drain);
+            wait_warp_final(bar.drain, 0, p.status);
         }
         __syncwarp();
     } else {
