@@ -28,6 +28,9 @@
 // loaded as soon as the last score product of the current one has read Q, and
 // the next tile's first value product into O_t waits only until the epilogue
 // of the current tile has pulled O_t out of TMEM, so epilogues overlap MMAs.
+// Each query tile's epilogue starts as soon as its own last value product has
+// completed (one O-final barrier per tile), about one softmax step before the
+// other tile's.
 // The epilogue goes through shared memory: each softmax warp writes its 32
 // normalized rows of a 64-column half into its own 4 KB area (16-byte chunks in
 // a 128-byte swizzle) and copies them out with stores of four whole 128-byte
@@ -92,8 +95,8 @@ struct Cfg {
     // output staging: 4 KB per softmax warp (its 32 rows x 64 columns of 16-bit output)
     static constexpr int kStageOff = kKVOff + kStages * kTileBytes;
     static constexpr int kBarOff = kStageOff + 8 * 4096;
-    // q_full, q_free, full[S], empty[S], s_full[2], p_full[2], o_final, o_free[2], drain
-    static constexpr int kNumBars = 2 + 2 * kStages + 2 + 2 + 1 + 2 + 1;
+    // q_full, q_free, full[S], empty[S], s_full[2], p_full[2], o_final[2], o_free[2], drain
+    static constexpr int kNumBars = 2 + 2 * kStages + 2 + 2 + 2 + 2 + 1;
     static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
 };
@@ -120,11 +123,12 @@ struct PrefillParams {
 };
 
 struct Bars {
-    uint32_t q_full, q_free, full0, empty0, s0, p0, o_final, o_free0, drain;
+    uint32_t q_full, q_free, full0, empty0, s0, p0, o_final0, o_free0, drain;
     __device__ uint32_t full(int s) const { return full0 + 8u * s; }
     __device__ uint32_t empty(int s) const { return empty0 + 8u * s; }
     __device__ uint32_t s_full(int t) const { return s0 + 8u * t; }
     __device__ uint32_t p_full(int t) const { return p0 + 8u * t; }
+    __device__ uint32_t o_final(int t) const { return o_final0 + 8u * t; }
     __device__ uint32_t o_free(int t) const { return o_free0 + 8u * t; }
 };
 
@@ -268,8 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bar.empty0 = bar.full0 + 8 * C::kStages;
     bar.s0 = bar.empty0 + 8 * C::kStages;
     bar.p0 = bar.s0 + 16;
-    bar.o_final = bar.p0 + 16;
-    bar.o_free0 = bar.o_final + 8;
+    bar.o_final0 = bar.p0 + 16;
+    bar.o_free0 = bar.o_final0 + 16;
     bar.drain = bar.o_free0 + 16;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff);
     volatile uint32_t* abort_flag = tmem_slot + 1;
@@ -288,7 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar.p_full(t), 4);  // one arrival per softmax warp
             mbar_init(bar.o_free(t), 4);
         }
-        mbar_init(bar.o_final, 1);
+        mbar_init(bar.o_final(0), 1);
+        mbar_init(bar.o_final(1), 1);
         mbar_init(bar.drain, 1);
         *abort_flag = 0u;
         fence_mbar_init();
@@ -407,11 +412,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit_el(bar.empty((uk >> 1) % kHalf));  // K_j and V_(j-1) are read
                     if (!v_ready && !(ok = wait_warp(bar.full(sv), (uv / C::kStages) & 1, abort_flag, p.status))) break;
                     if (!(ok = issue_pv(0, sv, jj == 0))) break;
+                    if (jj == n - 1) mma_commit_el(bar.o_final(0));  // O_0 of this tile is final
                     slot_v_prev = sv;
                 }
                 if (!ok) break;
                 if (!(ok = issue_pv(1, slot_v_prev, n - 1 == 0))) break;
-                mma_commit_el(bar.o_final);  // this tile's O_0 and O_1 are final
+                mma_commit_el(bar.o_final(1));  // O_1 of this tile is final
                 ++tc;
             }
             // all MMAs done before TMEM and shared memory are released
@@ -607,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // neither the writes nor the reads conflict), then copies them out with
             // 16-byte stores of four whole 128-byte row segments per instruction
             // (a row-per-thread store would touch 32 rows per instruction).
-            if (!(ok = wait_warp(bar.o_final, tc & 1, abort_flag, p.status))) break;
+            if (!(ok = wait_warp(bar.o_final(t), tc & 1, abort_flag, p.status))) break;
             ++tc;
             tc_fence_after();
             const float inv = l > 0.f ? p.v_scale / l : 0.f;  // no visible key: output 0
