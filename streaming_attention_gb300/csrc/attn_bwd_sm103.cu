@@ -15,13 +15,16 @@
 //   dK/dV kernel: one CTA per (128-key tile, KV head); K and V stay in shared
 //     memory while the query tiles of all G query heads of the group stream
 //     through a 2-stage TMA ring (Q, dO, and their rows' lse and delta).
-//     S^T = K Q^T and dP^T = V dO^T land in TMEM (TMEM lane = key); the four
+//     S^T = K Q^T and dP^T = V dO^T land in TMEM (TMEM lane = key); the
 //     elementwise warps turn them into P^T and dS^T (16-bit, written over the
 //     first half of each), and the MMA warp accumulates dV += P^T dO and
-//     dK += dS^T Q in TMEM.
+//     dK += dS^T Q in TMEM. The elementwise warps keep their P^T in registers
+//     for the dS^T pass, so the next tile's S^T may overwrite P^T as soon as
+//     the dV product has read it.
 //   dQ kernel: one CTA per (128-row query tile, query head); Q and dO stay,
-//     K and V tiles stream; S = Q K^T and dP = dO V^T in TMEM (lane = row),
-//     dS over dP, dQ += dS K.
+//     K and V tiles stream; S = Q K^T and dP = dO V^T in TMEM (lane = row);
+//     the elementwise warps take S into registers (which frees it for the next
+//     tile's product at once) and keep P there; dS over dP, dQ += dS K.
 // S and dP are thus computed twice (7 products instead of 5); in exchange
 // neither kernel needs atomics or a transpose through shared memory.
 // The elementwise passes run on packed FP32 pairs (fma/add/mul.f32x2; the row
@@ -68,7 +71,6 @@ struct BCfg {
     static constexpr int kSmem = kOffMisc + 16 + 1024;
     // TMEM columns
     static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + D;
-    static constexpr uint32_t kColP = 384;  // dQ kernel: P (16-bit pairs), moved out of S
 };
 
 struct BwdParams {
@@ -229,7 +231,8 @@ struct BSetup {
     __device__ uint32_t full(int s) const { return bar_full0 + 8u * s; }
     __device__ uint32_t empty(int s) const { return bar_empty0 + 8u * s; }
     __device__ uint32_t st(int x) const { return bar_st0 + 8u * x; }  // x = 0: S computed; 1: dP computed
-    __device__ uint32_t pp(int x) const { return bar_p0 + 8u * x; }   // x = 0: P written; 1: dS written
+    // x = 0: P written (dK/dV kernel) or S taken into registers (dQ kernel); 1: dS written
+    __device__ uint32_t pp(int x) const { return bar_p0 + 8u * x; }
 };
 
 template <int D>
@@ -374,8 +377,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint64_t dV = sw128_desc(bs.sbase + C::kOffStat + C::kTile, 16, 1024);
             // Two-phase pipeline: S^T and dP^T of a tile are full 128-wide products; the
             // elementwise warps write P^T over S^T (phase A) while dP^T is computed, then
-            // dS^T over dP^T (phase B). dV needs only phase A; the next tile's S^T goes in
-            // as soon as phase B has read P^T, ahead of this tile's dK product.
+            // dS^T over dP^T (phase B), taking P^T from their registers. dV needs only
+            // phase A, and the next tile's S^T follows dV at once, ahead of phase B and
+            // of this tile's dK product.
             auto stage_q = [&](int it) { return bs.sbase + C::kOffStage + (it & 1) * 2 * C::kTile; };
             auto issue_s = [&](int it) {  // S^T = K Q^T
                 mma_rows_by_rows<D>(bs.tmem + C::kColS, dK, sw128_desc(stage_q(it), 16, 1024), idS);
@@ -398,14 +402,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tc_fence_after();
                 mma_tmem_by_tile(bs.tmem + C::kColAcc1, bs.tmem + C::kColS, sw128_desc(sq + C::kTile, C::kChunk, 1024),
                                  idAcc, it == 0);  // dV += P^T dO
-                if (!(ok = bwait_warp(bs.pp(1), it & 1, bs.abort_flag, p.status))) break;
-                tc_fence_after();
+                // the next S^T may overwrite P^T now: dV reads it first (same pipe), and
+                // phase B takes P from the elementwise warps' registers
                 const bool more = it + 1 < T;
                 if (more) {
                     if (!(ok = bwait_warp(bs.full((it + 1) & 1), ((it + 1) >> 1) & 1, bs.abort_flag, p.status))) break;
                     tc_fence_after();
                     issue_s(it + 1);
                 }
+                if (!(ok = bwait_warp(bs.pp(1), it & 1, bs.abort_flag, p.status))) break;
+                tc_fence_after();
                 mma_tmem_by_tile(bs.tmem + C::kColAcc0, bs.tmem + C::kColDP, sw128_desc(sq, C::kChunk, 1024), idAcc,
                                  it == 0);  // dK += dS^T Q
                 mma_commit_el(bs.empty(it & 1));  // Q, dO of this tile fully read
@@ -426,6 +432,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int it = 0; ok && it < T; ++it) {
             const int s = it & 1;
             const int i0 = (qt0 + (it + rot) % T % nq) * BT;
+            uint32_t pkeep[2][16];  // this thread's packed P of phase A, used again by phase B
             const bool need_mask = (i0 + BT > p.M) || (k0 + BT > p.N) ||
                                    (p.causal && k0 + BT - 1 > i0 + off) ||
                                    (p.window > 0 && k0 <= i0 + BT - 1 + off - p.window);
@@ -481,6 +488,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 else
                     chunk(std::false_type{});
                 tmem_st_x16(bs.tmem + lane_base + C::kColS + packed_col(q4), pk);
+#pragma unroll
+                for (int x = 0; x < 16; ++x) pkeep[qq][x] = pk[x];
             }
             tmem_wait_st();
             tc_fence_before();
@@ -493,11 +502,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
             for (int qq = 0; qq < 2; ++qq) {
                 const int q4 = 2 * half + qq, c0 = q4 * 32;
-                uint32_t dpv[32], pv16[16];
+                uint32_t dpv[32];
                 tmem_ld_x32(bs.tmem + lane_base + C::kColDP + c0, dpv);
-                tmem_ld_x16(bs.tmem + lane_base + C::kColS + packed_col(q4), pv16);
                 tmem_wait_ld_x32(dpv);
-                reg_after_x16(pv16);
+                const uint32_t* pv16 = pkeep[qq];
                 uint32_t dk[16];
 #pragma unroll
                 for (int g4 = 0; g4 < 8; ++g4) {
@@ -613,8 +621,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             constexpr uint32_t idAcc = idesc_f16(kBF16, BT, D, true);
             const uint64_t dQ = sw128_desc(bs.sbase + C::kOffStat, 16, 1024);
             const uint64_t ddO = sw128_desc(bs.sbase + C::kOffStat + C::kTile, 16, 1024);
-            // Two-phase pipeline: full 128-wide S and dP; phase A moves P (16-bit) out of S,
-            // which frees S for the next tile's product at once; phase B writes dS over dP.
+            // Two-phase pipeline: full 128-wide S and dP; phase A takes S into registers,
+            // which frees S for the next tile's product at once, and keeps P there; phase B
+            // writes dS over dP.
             auto stage_k = [&](int it) { return bs.sbase + C::kOffStage + (it & 1) * 2 * C::kTile; };
             auto issue_s = [&](int it) {  // S = Q K^T
                 mma_rows_by_rows<D>(bs.tmem + C::kColS, dQ, sw128_desc(stage_k(it), 16, 1024), idS);
@@ -668,15 +677,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const bool need_mask = (i0 + BT > p.M) || (k0 + BT > p.N) ||
                                    (p.causal && k0 + BT - 1 > i0 + off) ||
                                    (p.window > 0 && k0 <= i0 + BT - 1 + off - p.window);
-            // ---- phase A: P = exp2(S c - lse2), moved to its own columns ----
+            // ---- phase A: P = exp2(S c - lse2), kept in registers ----
             if (!(ok = bwait_warp(bs.st(0), it & 1, bs.abort_flag, p.status))) break;
             tc_fence_after();
+            uint32_t sva[2][32];
+            tmem_ld_x32(bs.tmem + lane_base + C::kColS + 64 * half, sva[0]);
+            tmem_ld_x32(bs.tmem + lane_base + C::kColS + 64 * half + 32, sva[1]);
+            tmem_wait_ld_x32(sva[0]);
+            reg_after_x32(sva[1]);
+            // S is in registers: the next tile's score product may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) mbar_arrive(bs.pp(0));
+            uint32_t pkeep[2][16];
 #pragma unroll
             for (int qq = 0; qq < 2; ++qq) {
                 const int q4 = 2 * half + qq, c0 = q4 * 32;  // TMEM column = key of the tile
-                uint32_t sv[32];
-                tmem_ld_x32(bs.tmem + lane_base + C::kColS + c0, sv);
-                tmem_wait_ld_x32(sv);
+                const uint32_t* sv = sva[qq];
                 // visible keys of this chunk for this thread's row: e in [elo, ehi)
                 int elo = 0, ehi = 32;
                 if (need_mask) {
@@ -707,23 +724,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     chunk(std::true_type{});
                 else
                     chunk(std::false_type{});
-                tmem_st_x16(bs.tmem + lane_base + C::kColP + q4 * 16, pk);
+#pragma unroll
+                for (int x = 0; x < 16; ++x) pkeep[qq][x] = pk[x];
             }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();  // the warp's TMEM stores before lane 0's arrival
-            if ((threadIdx.x & 31) == 0) mbar_arrive(bs.pp(0));
             // ---- phase B: dS = P (dP - delta), packed over dP ----
             if (!(ok = bwait_warp(bs.st(1), it & 1, bs.abort_flag, p.status))) break;
             tc_fence_after();
 #pragma unroll
             for (int qq = 0; qq < 2; ++qq) {
                 const int q4 = 2 * half + qq, c0 = q4 * 32;
-                uint32_t dpv[32], pv16[16];
+                uint32_t dpv[32];
                 tmem_ld_x32(bs.tmem + lane_base + C::kColDP + c0, dpv);
-                tmem_ld_x16(bs.tmem + lane_base + C::kColP + q4 * 16, pv16);
                 tmem_wait_ld_x32(dpv);
-                reg_after_x16(pv16);
+                const uint32_t* pv16 = pkeep[qq];
                 uint32_t dk[16];
 #pragma unroll
                 for (int e2 = 0; e2 < 16; ++e2) {
