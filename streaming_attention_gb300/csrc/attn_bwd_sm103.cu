@@ -26,7 +26,10 @@
 //     the elementwise warps take S into registers (which frees it for the next
 //     tile's product at once) and keep P there; dS over dP, dQ += dS K.
 // S and dP are thus computed twice (7 products instead of 5); in exchange
-// neither kernel needs atomics or a transpose through shared memory.
+// neither kernel needs atomics or a transpose through shared memory. The dQ
+// kernel reads nothing the dK/dV kernel writes, so it is launched
+// programmatically: its CTAs start on the SMs the dK/dV grid's last wave
+// leaves idle, and each waits for that grid only before it exits.
 // The elementwise passes run on packed FP32 pairs (fma/add/mul.f32x2; the row
 // statistics are stored negated for that), and each kernel's outputs leave
 // through the idle stage ring as swizzled boxes stored by TMA.
@@ -314,6 +317,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     using C = BCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // The dQ kernel (launched after this one, programmatically) reads nothing this
+    // kernel writes: its CTAs may start on SMs this grid's last wave leaves idle.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const BSetup bs = bwd_setup<D>(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -774,6 +780,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
     }
     bwd_teardown(bs);
+    // This grid completes only after the dK/dV grid it may overlap has completed and its
+    // writes are visible (its CTAs start while that grid's last wave runs).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // dot product of eight 16-bit pairs held in two 16-byte vectors
@@ -888,8 +897,17 @@ cudaError_t launch_bwd_t(const Problem& pr, const BwdArgs& a, const float* lse2,
     bp.out1 = nullptr;
     bp.groups = pr.B * pr.Hq;
     bp.ntile = (pr.M + BT - 1) / BT;
-    attn_bwd_dq_kernel<D, kBF16><<<bp.groups * bp.ntile, kBwdThreads, C::kSmem, stream>>>(tq, tk, tv, tdo, tdq, bp);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(bp.groups * bp.ntile);
+    cfg.blockDim = dim3(kBwdThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_bwd_dq_kernel<D, kBF16>, tq, tk, tv, tdo, tdq, bp);
 }
 
 }  // namespace
