@@ -489,34 +489,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 if (q4 * 32 + e >= vhi) s[q4][e] = __float_as_uint(masked_s);
                     }
                 }
-                // row maximum (minimum for a negative scale) in four independent
-                // chains of three-input operations
+                // row maximum (minimum for a negative scale) with three-input operations
                 float mx;
                 {
 #define SV(i) __uint_as_float(s[(i) >> 5][(i) & 31])
-                    float a0 = SV(0), a1 = SV(1), a2 = SV(2), a3 = SV(3);
+                    // eight chains over 16 columns each (depth 8), then a two-level tree
+                    float a[8];
                     if (c >= 0.f) {
 #pragma unroll
-                        for (int i = 4; i < 128; i += 8) {
-                            a0 = max3f(a0, SV(i), SV(i + 1));
-                            a1 = max3f(a1, SV(i + 2), SV(i + 3));
-                            if (i + 4 < 128) {
-                                a2 = max3f(a2, SV(i + 4), SV(i + 5));
-                                a3 = max3f(a3, SV(i + 6), SV(i + 7));
-                            }
+                        for (int k = 0; k < 8; ++k) {
+                            a[k] = max3f(SV(16 * k), SV(16 * k + 1), SV(16 * k + 2));
+#pragma unroll
+                            for (int e = 3; e < 15; e += 2) a[k] = max3f(a[k], SV(16 * k + e), SV(16 * k + e + 1));
+                            a[k] = fmaxf(a[k], SV(16 * k + 15));
                         }
-                        mx = max3f(a0, a1, fmaxf(a2, a3));
+                        mx = max3f(max3f(a[0], a[1], a[2]), max3f(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
                     } else {
 #pragma unroll
-                        for (int i = 4; i < 128; i += 8) {
-                            a0 = min3f(a0, SV(i), SV(i + 1));
-                            a1 = min3f(a1, SV(i + 2), SV(i + 3));
-                            if (i + 4 < 128) {
-                                a2 = min3f(a2, SV(i + 4), SV(i + 5));
-                                a3 = min3f(a3, SV(i + 6), SV(i + 7));
-                            }
+                        for (int k = 0; k < 8; ++k) {
+                            a[k] = min3f(SV(16 * k), SV(16 * k + 1), SV(16 * k + 2));
+#pragma unroll
+                            for (int e = 3; e < 15; e += 2) a[k] = min3f(a[k], SV(16 * k + e), SV(16 * k + e + 1));
+                            a[k] = fminf(a[k], SV(16 * k + 15));
                         }
-                        mx = min3f(a0, a1, fminf(a2, a3));
+                        mx = min3f(min3f(a[0], a[1], a[2]), min3f(a[3], a[4], a[5]), fminf(a[6], a[7]));
                     }
 #undef SV
                 }
