@@ -161,6 +161,20 @@ __device__ bool dwait_warp(uint32_t bar, uint32_t parity, volatile uint32_t* abo
     }
 }
 
+// Warp-uniform bounded wait that ignores the abort flag (for the final drain).
+__device__ bool dwait_warp_final(uint32_t bar, uint32_t parity, int* status) {
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+        int stop = 0;
+        if ((threadIdx.x & 31) == 0 && globaltimer_ns() - t0 > kDecTimeoutNs) {
+            atomicExch(status, 1);
+            stop = 1;
+        }
+        if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+    }
+}
+
 // Sequence position u of the ring -> (is V, tile index): K_0, K_1, V_0, K_2, V_1, ..., K_{T-1}, V_{T-2}, V_{T-1}
 __device__ __forceinline__ void ring_item(int u, int T, bool* is_v, int* tile) {
     if (u == 2 * T - 1) {
@@ -359,14 +373,15 @@ __global__ void __launch_bounds__(kDecThreads)
             }
         }
     } else if (warp == kDecMmaWarp) {
-        if (lane == 0 && T > 0) {
+        // the whole warp runs the issuing loop; one elected lane issues each MMA and commit
+        if (T > 0) {
             constexpr uint32_t idS =
                 EB == 1 ? idesc_e4m3(DBN, DNR, false, false) : idesc_f16(kBF16, DBN, DNR, false, false);
             constexpr uint32_t idPV =
                 EB == 1 ? idesc_e4m3(DD, DNR, false, true) : idesc_f16(kBF16, DD, DNR, false, true);
             auto issue_s = [&](int j) {
                 const int u = ring_pos_k(j), s = u % kSlots;
-                if (!dwait_one(bar_full0 + 8 * s, (u / kSlots) & 1, abort_flag, p.status)) return false;
+                if (!dwait_warp(bar_full0 + 8 * s, (u / kSlots) & 1, abort_flag, p.status)) return false;
                 tc_fence_after();
                 // one K step covers 32 bytes of D: 16 elements of 16 bits, 32 of 8
                 for (int kk = 0; kk < DD * EB / 32; ++kk) {
@@ -374,18 +389,18 @@ __global__ void __launch_bounds__(kDecThreads)
                     const uint64_t a = sw128_desc(sRing + s * kTileBytes + off, 16, 1024);
                     const uint64_t bq = sw128_desc(sQ + (kk >> 2) * kQChunk + (kk & 3) * 32, 16, 1024);
                     if constexpr (EB == 1)
-                        mma_ss_f8(tmem + dcol_s(j & 1), a, bq, idS, kk > 0 ? 1u : 0u);
+                        mma_ss_f8_el(tmem + dcol_s(j & 1), a, bq, idS, kk > 0 ? 1u : 0u);
                     else
-                        mma_ss(tmem + dcol_s(j & 1), a, bq, idS, kk > 0 ? 1u : 0u);
+                        mma_ss_el(tmem + dcol_s(j & 1), a, bq, idS, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(bar_s0 + 8 * (j & 1));
-                mma_commit(bar_empty0 + 8 * s);
+                mma_commit_el(bar_s0 + 8 * (j & 1));
+                mma_commit_el(bar_empty0 + 8 * s);
                 return true;
             };
             auto issue_pv = [&](int j) {
                 const int u = ring_pos_v(j, T), s = u % kSlots;
-                if (!dwait_one(bar_full0 + 8 * s, (u / kSlots) & 1, abort_flag, p.status)) return false;
-                if (!dwait_one(bar_p0 + 8 * (j & 1), (j >> 1) & 1, abort_flag, p.status)) return false;
+                if (!dwait_warp(bar_full0 + 8 * s, (u / kSlots) & 1, abort_flag, p.status)) return false;
+                if (!dwait_warp(bar_p0 + 8 * (j & 1), (j >> 1) & 1, abort_flag, p.status)) return false;
                 tc_fence_after();
                 // one K step covers 32 / EB keys: that many 128-byte rows of V
                 for (int kk = 0; kk < DBN * EB / 32; ++kk) {
@@ -394,22 +409,22 @@ __global__ void __launch_bounds__(kDecThreads)
                     const uint64_t bp = sw128_desc(sP + (j & 1) * C::kPBytes + (kk >> 2) * kQChunk + (kk & 3) * 32,
                                                    16, 1024);
                     if constexpr (EB == 1)
-                        mma_ss_f8(tmem + kColOT, a, bp, idPV, (j > 0 || kk > 0) ? 1u : 0u);
+                        mma_ss_f8_el(tmem + kColOT, a, bp, idPV, (j > 0 || kk > 0) ? 1u : 0u);
                     else
-                        mma_ss(tmem + kColOT, a, bp, idPV, (j > 0 || kk > 0) ? 1u : 0u);
+                        mma_ss_el(tmem + kColOT, a, bp, idPV, (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(bar_free0 + 8 * (j & 1));
-                mma_commit(bar_empty0 + 8 * s);
+                mma_commit_el(bar_free0 + 8 * (j & 1));
+                mma_commit_el(bar_empty0 + 8 * s);
                 return true;
             };
-            bool ok = dwait_one(bar_q, 0, abort_flag, p.status);
+            bool ok = dwait_warp(bar_q, 0, abort_flag, p.status);
             for (int j = 0; ok && j < T; ++j) {
                 ok = issue_s(j);
                 if (ok && j > 0) ok = issue_pv(j - 1);
             }
             if (ok) issue_pv(T - 1);
-            mma_commit(bar_o);
-            dwait_one(bar_o, 0, abort_flag, p.status, false);
+            mma_commit_el(bar_o);
+            dwait_warp_final(bar_o, 0, p.status);
         }
         __syncwarp();
     } else {
