@@ -12,7 +12,9 @@
 //
 // Each CTA streams one split (a run of 128-key tiles) of one KV head through a
 // TMA ring (3 slots of 16-bit tiles, 6 of 8-bit tiles), K and V tiles in the
-// order the MMAs consume them, and forms the split's unnormalized summary
+// order the MMAs consume them (for the 8-bit contiguous cache in rounds of two
+// tiles, so the softmax's cross-warp maximum exchange and P handshake come once
+// per 256 keys), and forms the split's unnormalized summary
 // (m, l, acc) for its rows. The summaries are combined with the common-maximum
 // rule ("Compare reasoning after your own attempt", central-idea table, A1 and
 // A2 rows): when a KV head has at most 8 splits they form one thread-block
@@ -191,6 +193,39 @@ __device__ __forceinline__ void ring_item(int u, int T, bool* is_v, int* tile) {
         *tile = (u - 2) / 2;
     }
 }
+// The same for two-tile rounds (8-bit contiguous decode): K_0, K_1, then per round
+// i >= 1 K_2i, K_2i+1, V_2i-2, V_2i-1, then the last round's V tiles; the last
+// round holds one tile when T is odd.
+__device__ __forceinline__ void ring_item2(int u, int T, bool* is_v, int* tile) {
+    const int R = (T + 1) / 2;
+    if (u < min(2, T)) {
+        *is_v = false;
+        *tile = u;
+        return;
+    }
+    if (R >= 2) {
+        const int full_end = 2 + 4 * (R - 2);  // end of the full rounds 1 .. R-2
+        const int nk_last = min(2, T - 2 * (R - 1));
+        const int body_end = full_end + nk_last + 2;
+        if (u < full_end) {
+            const int i = 1 + (u - 2) / 4, o = (u - 2) % 4;
+            *is_v = o >= 2;
+            *tile = o < 2 ? 2 * i + o : 2 * (i - 1) + (o - 2);
+            return;
+        }
+        if (u < body_end) {
+            const int o = u - full_end;
+            *is_v = o >= nk_last;
+            *tile = o < nk_last ? 2 * (R - 1) + o : 2 * (R - 2) + (o - nk_last);
+            return;
+        }
+        *is_v = true;
+        *tile = 2 * (R - 1) + (u - body_end);
+        return;
+    }
+    *is_v = true;
+    *tile = u - min(2, T);
+}
 __device__ __forceinline__ int ring_pos_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
 __device__ __forceinline__ int ring_pos_v(int j, int T) { return j == T - 1 ? 2 * T - 1 : 2 * j + 2; }
 
@@ -205,6 +240,13 @@ __global__ void __launch_bounds__(kDecThreads)
     using C = DCfg<EB>;
     constexpr int kSlots = C::kSlots;
     constexpr int kTileBytes = C::kTileBytes;
+    // 8-bit contiguous decode: two key tiles per softmax round, so the cross-warp
+    // maximum exchange and the P handshake happen once per 256 keys
+    constexpr bool kR2 = EB == 1 && !kPaged;
+    constexpr int kNP = kR2 ? 4 : 2;                  // S^T and P^T buffers
+    constexpr uint32_t kCols = kR2 ? 128u : kTmemCols;
+    constexpr uint32_t kColO = kR2 ? 64u : kColOT;
+    static_assert(C::kOffP + kNP * C::kPBytes <= C::kOffRing, "P^T buffers overlap the ring");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -250,11 +292,11 @@ __global__ void __launch_bounds__(kDecThreads)
         fence_mbar_init();
     }
     // P^T buffers start at zero (rows >= R are never written afterwards)
-    for (int x = threadIdx.x; x < 2 * C::kPBytes / 16; x += blockDim.x)
+    for (int x = threadIdx.x; x < kNP * C::kPBytes / 16; x += blockDim.x)
         reinterpret_cast<uint4*>(smem + C::kOffP)[x] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (warp == kDecMmaWarp) {
-        tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
+        tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), kCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -299,7 +341,10 @@ __global__ void __launch_bounds__(kDecThreads)
                     break;
                 bool is_v;
                 int tile;
-                ring_item(u, T, &is_v, &tile);
+                if constexpr (kR2)
+                    ring_item2(u, T, &is_v, &tile);
+                else
+                    ring_item(u, T, &is_v, &tile);
                 mbar_arrive_expect_tx(bar_full0 + 8 * s, kTileBytes);
                 const CUtensorMap* tm = is_v ? &tmV : &tmK;
                 for (int c = 0; c < C::kChunks; ++c)
@@ -409,20 +454,74 @@ __global__ void __launch_bounds__(kDecThreads)
                     const uint64_t bp = sw128_desc(sP + (j & 1) * C::kPBytes + (kk >> 2) * kQChunk + (kk & 3) * 32,
                                                    16, 1024);
                     if constexpr (EB == 1)
-                        mma_ss_f8_el(tmem + kColOT, a, bp, idPV, (j > 0 || kk > 0) ? 1u : 0u);
+                        mma_ss_f8_el(tmem + kColO, a, bp, idPV, (j > 0 || kk > 0) ? 1u : 0u);
                     else
-                        mma_ss_el(tmem + kColOT, a, bp, idPV, (j > 0 || kk > 0) ? 1u : 0u);
+                        mma_ss_el(tmem + kColO, a, bp, idPV, (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit_el(bar_free0 + 8 * (j & 1));
                 mma_commit_el(bar_empty0 + 8 * s);
                 return true;
             };
-            bool ok = dwait_warp(bar_q, 0, abort_flag, p.status);
-            for (int j = 0; ok && j < T; ++j) {
-                ok = issue_s(j);
-                if (ok && j > 0) ok = issue_pv(j - 1);
+            if constexpr (kR2) {
+                // rounds of two tiles: S^T of round i into buffers 2i, 2i+1 (mod 4), one
+                // score commit per round, then the value products of round i-1
+                int u = 0;  // ring position, in the producer's order
+                auto take = [&](int* sl) {
+                    *sl = u % kSlots;
+                    const bool r = dwait_warp(bar_full0 + 8 * *sl, (u / kSlots) & 1, abort_flag, p.status);
+                    ++u;
+                    return r;
+                };
+                auto round_pv = [&](int ir) {
+                    if (!dwait_warp(bar_p0 + 8 * (ir & 1), (ir >> 1) & 1, abort_flag, p.status)) return false;
+                    const int n = min(2, T - 2 * ir);
+                    for (int a = 0; a < n; ++a) {
+                        const int t = 2 * ir + a;
+                        int sl;
+                        if (!take(&sl)) return false;
+                        tc_fence_after();
+                        for (int kk = 0; kk < DBN * EB / 32; ++kk) {
+                            const uint64_t av =
+                                sw128_desc(sRing + sl * kTileBytes + kk * (32 / EB) * 128, kChunkBytes, 1024);
+                            const uint64_t bp = sw128_desc(sP + (t & 3) * C::kPBytes + (kk >> 2) * kQChunk + (kk & 3) * 32,
+                                                           16, 1024);
+                            mma_ss_f8_el(tmem + kColO, av, bp, idPV, (t > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        mma_commit_el(bar_empty0 + 8 * sl);
+                    }
+                    mma_commit_el(bar_free0 + 8 * (ir & 1));
+                    return true;
+                };
+                const int R = (T + 1) / 2;
+                bool ok = dwait_warp(bar_q, 0, abort_flag, p.status);
+                for (int i = 0; ok && i < R; ++i) {
+                    const int n = min(2, T - 2 * i);
+                    for (int a = 0; ok && a < n; ++a) {
+                        const int t = 2 * i + a;
+                        int sl;
+                        if (!(ok = take(&sl))) break;
+                        tc_fence_after();
+                        for (int kk = 0; kk < DD * EB / 32; ++kk) {
+                            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                            const uint64_t ak = sw128_desc(sRing + sl * kTileBytes + off, 16, 1024);
+                            const uint64_t bq = sw128_desc(sQ + (kk >> 2) * kQChunk + (kk & 3) * 32, 16, 1024);
+                            mma_ss_f8_el(tmem + 16u * (uint32_t)(t & 3), ak, bq, idS, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit_el(bar_empty0 + 8 * sl);
+                    }
+                    if (!ok) break;
+                    mma_commit_el(bar_s0 + 8 * (i & 1));  // both score tiles of round i
+                    if (i > 0) ok = round_pv(i - 1);
+                }
+                if (ok) round_pv(R - 1);
+            } else {
+                bool ok = dwait_warp(bar_q, 0, abort_flag, p.status);
+                for (int j = 0; ok && j < T; ++j) {
+                    ok = issue_s(j);
+                    if (ok && j > 0) ok = issue_pv(j - 1);
+                }
+                if (ok) issue_pv(T - 1);
             }
-            if (ok) issue_pv(T - 1);
             mma_commit_el(bar_o);
             dwait_warp_final(bar_o, 0, p.status);
         }
@@ -446,85 +545,180 @@ __global__ void __launch_bounds__(kDecThreads)
             l_part[r] = 0.f;
         }
         bool ok = true;
-        for (int j = 0; j < T; ++j) {
-            const int key = k0 + j * DBN + kl;
-            if (!(ok = dwait_warp(bar_s0 + 8 * (j & 1), (j >> 1) & 1, abort_flag, p.status))) break;
-            tc_fence_after();
-            uint32_t sr[16];
-            tmem_ld_x16(tmem + lane_base + dcol_s(j & 1), sr);
-            asm volatile("tcgen05.wait::ld.sync.aligned;"
-                         : "+r"(sr[0]), "+r"(sr[1]), "+r"(sr[2]), "+r"(sr[3]), "+r"(sr[4]), "+r"(sr[5]), "+r"(sr[6]),
-                           "+r"(sr[7]), "+r"(sr[8]), "+r"(sr[9]), "+r"(sr[10]), "+r"(sr[11]), "+r"(sr[12]),
-                           "+r"(sr[13]), "+r"(sr[14]), "+r"(sr[15])::"memory");
-            float t[RP];
-#pragma unroll
-            for (int r = 0; r < RP; ++r)
-                t[r] = (key >= lo[r] && key < hi[r]) ? __uint_as_float(sr[r]) * c : -INFINITY;
-            // tile row maxima across the 128 keys
-            float* redj = red + (j & 1) * 4 * DNR;
-#pragma unroll
-            for (int r = 0; r < RP; ++r) {
-                float x = t[r];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-                if (lane == 0) redj[warp * DNR + r] = x;
-            }
-            if (lane == 0) mbar_arrive(bar_red0 + 8 * (j & 1));  // lane 0 wrote the warp's maxima
-            if (!(ok = dwait_warp(bar_red0 + 8 * (j & 1), (j >> 1) & 1, abort_flag, p.status))) break;
-            bool need_any = false;
-            float alpha[RP];
-#pragma unroll
-            for (int r = 0; r < RP; ++r) {
-                alpha[r] = 1.f;
-                const float mt = fmaxf(fmaxf(redj[r], redj[DNR + r]), fmaxf(redj[2 * DNR + r], redj[3 * DNR + r]));
-                const float m_new = fmaxf(m_ref[r], mt);
-                if (m_new > m_ref[r] + kDecRescale) {
-                    alpha[r] = ex2(m_ref[r] - m_new);
-                    l_part[r] *= alpha[r];
-                    m_ref[r] = m_new;
-                    need_any = true;
-                }
-            }
-            // P^T buffer j&1 was last read by the value product of tile j-2
-            if (j >= 2 && !(ok = dwait_warp(bar_free0 + 8 * (j & 1), ((j - 2) >> 1) & 1, abort_flag, p.status)))
-                break;
-            uint8_t* pbuf = smem + C::kOffP + (j & 1) * C::kPBytes;
-#pragma unroll
-            for (int r = 0; r < RP; ++r) {
-                const float m_use = (m_ref[r] == -INFINITY) ? 0.f : m_ref[r];
-                const float pr = ex2(t[r] - m_use);
-                l_part[r] += pr;
-                // P^T row r, key kl, in the 128-byte swizzle: 16-byte granule g of row r sits at g ^ (r & 7)
-                if constexpr (EB == 1) {
-                    const int off = r * 128 + ((((kl >> 4) ^ (r & 7))) << 4) + (kl & 15);
-                    pbuf[off] = (uint8_t)(pack_e4m3x4(pr, 0.f, 0.f, 0.f) & 0xFFu);
-                } else {
-                    const int kc = kl >> 6, k64 = kl & 63;
-                    const uint32_t pk = kBF16 ? pack_bf16(pr, 0.f) : pack_f16(pr, 0.f);
-                    const int off = kc * kQChunk + r * 128 + ((((k64 >> 3) ^ (r & 7))) << 4) + (k64 & 7) * 2;
-                    *reinterpret_cast<uint16_t*>(pbuf + off) = (uint16_t)(pk & 0xFFFFu);
-                }
-            }
-            // lazy rescale of O^T (needs the value product of tile j-1 complete)
-            if (need_any && j > 0) {
-                if (!(ok = dwait_warp(bar_free0 + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag, p.status)))
-                    break;
+        if constexpr (kR2) {
+            const int R = (T + 1) / 2;
+            for (int i = 0; i < R; ++i) {
+                const int n = min(2, T - 2 * i);  // tiles of this round
+                if (!(ok = dwait_warp(bar_s0 + 8 * (i & 1), (i >> 1) & 1, abort_flag, p.status))) break;
                 tc_fence_after();
-                uint32_t o[16];
-                tmem_ld_x16(tmem + lane_base + kColOT, o);
-                asm volatile("tcgen05.wait::ld.sync.aligned;"
-                             : "+r"(o[0]), "+r"(o[1]), "+r"(o[2]), "+r"(o[3]), "+r"(o[4]), "+r"(o[5]), "+r"(o[6]),
-                               "+r"(o[7]), "+r"(o[8]), "+r"(o[9]), "+r"(o[10]), "+r"(o[11]), "+r"(o[12]),
-                               "+r"(o[13]), "+r"(o[14]), "+r"(o[15])::"memory");
+                uint32_t sr[2][16];
 #pragma unroll
-                for (int r = 0; r < RP; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[r]);
-                tmem_st_x16(tmem + lane_base + kColOT, o);
-                tmem_wait_st();
+                for (int e = 0; e < 16; ++e) sr[1][e] = 0u;
+                tmem_ld_x16(tmem + lane_base + 16u * (uint32_t)((2 * i) & 3), sr[0]);
+                if (n == 2) tmem_ld_x16(tmem + lane_base + 16u * (uint32_t)((2 * i + 1) & 3), sr[1]);
+                asm volatile("tcgen05.wait::ld.sync.aligned;"
+                             : "+r"(sr[0][0]), "+r"(sr[0][1]), "+r"(sr[0][2]), "+r"(sr[0][3]), "+r"(sr[0][4]),
+                               "+r"(sr[0][5]), "+r"(sr[0][6]), "+r"(sr[0][7]), "+r"(sr[0][8]), "+r"(sr[0][9]),
+                               "+r"(sr[0][10]), "+r"(sr[0][11]), "+r"(sr[0][12]), "+r"(sr[0][13]), "+r"(sr[0][14]),
+                               "+r"(sr[0][15])::"memory");
+                asm volatile(""
+                             : "+r"(sr[1][0]), "+r"(sr[1][1]), "+r"(sr[1][2]), "+r"(sr[1][3]), "+r"(sr[1][4]),
+                               "+r"(sr[1][5]), "+r"(sr[1][6]), "+r"(sr[1][7]), "+r"(sr[1][8]), "+r"(sr[1][9]),
+                               "+r"(sr[1][10]), "+r"(sr[1][11]), "+r"(sr[1][12]), "+r"(sr[1][13]), "+r"(sr[1][14]),
+                               "+r"(sr[1][15])::"memory");
+                float t[2][RP];
+#pragma unroll
+                for (int a = 0; a < 2; ++a) {
+                    const int key = k0 + (2 * i + a) * DBN + kl;
+#pragma unroll
+                    for (int r = 0; r < RP; ++r)
+                        t[a][r] = (a < n && key >= lo[r] && key < hi[r]) ? __uint_as_float(sr[a][r]) * c : -INFINITY;
+                }
+                // round row maxima across the 256 keys
+                float* redj = red + (i & 1) * 4 * DNR;
+#pragma unroll
+                for (int r = 0; r < RP; ++r) {
+                    float x = fmaxf(t[0][r], t[1][r]);
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+                    if (lane == 0) redj[warp * DNR + r] = x;
+                }
+                if (lane == 0) mbar_arrive(bar_red0 + 8 * (i & 1));  // lane 0 wrote the warp's maxima
+                if (!(ok = dwait_warp(bar_red0 + 8 * (i & 1), (i >> 1) & 1, abort_flag, p.status))) break;
+                bool need_any = false;
+                float alpha[RP];
+#pragma unroll
+                for (int r = 0; r < RP; ++r) {
+                    alpha[r] = 1.f;
+                    const float mt = fmaxf(fmaxf(redj[r], redj[DNR + r]), fmaxf(redj[2 * DNR + r], redj[3 * DNR + r]));
+                    const float m_new = fmaxf(m_ref[r], mt);
+                    if (m_new > m_ref[r] + kDecRescale) {
+                        alpha[r] = ex2(m_ref[r] - m_new);
+                        l_part[r] *= alpha[r];
+                        m_ref[r] = m_new;
+                        need_any = true;
+                    }
+                }
+                // this round's P^T buffers were last read by the value products of round i-2
+                if (i >= 2 && !(ok = dwait_warp(bar_free0 + 8 * (i & 1), ((i - 2) >> 1) & 1, abort_flag, p.status)))
+                    break;
+#pragma unroll
+                for (int a = 0; a < 2; ++a) {
+                    if (a >= n) break;
+                    uint8_t* pbuf = smem + C::kOffP + ((2 * i + a) & 3) * C::kPBytes;
+#pragma unroll
+                    for (int r = 0; r < RP; ++r) {
+                        const float m_use = (m_ref[r] == -INFINITY) ? 0.f : m_ref[r];
+                        const float pr = ex2(t[a][r] - m_use);
+                        l_part[r] += pr;
+                        // P^T row r, key kl, in the 128-byte swizzle: 16-byte granule g of row r sits at g ^ (r & 7)
+                        const int off = r * 128 + ((((kl >> 4) ^ (r & 7))) << 4) + (kl & 15);
+                        pbuf[off] = (uint8_t)(pack_e4m3x4(pr, 0.f, 0.f, 0.f) & 0xFFu);
+                    }
+                }
+                // lazy rescale of O^T (needs the value products of round i-1 complete)
+                if (need_any && i > 0) {
+                    if (!(ok = dwait_warp(bar_free0 + 8 * ((i - 1) & 1), ((i - 1) >> 1) & 1, abort_flag, p.status)))
+                        break;
+                    tc_fence_after();
+                    uint32_t o[16];
+                    tmem_ld_x16(tmem + lane_base + kColO, o);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                                 : "+r"(o[0]), "+r"(o[1]), "+r"(o[2]), "+r"(o[3]), "+r"(o[4]), "+r"(o[5]), "+r"(o[6]),
+                                   "+r"(o[7]), "+r"(o[8]), "+r"(o[9]), "+r"(o[10]), "+r"(o[11]), "+r"(o[12]),
+                                   "+r"(o[13]), "+r"(o[14]), "+r"(o[15])::"memory");
+#pragma unroll
+                    for (int r = 0; r < RP; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[r]);
+                    tmem_st_x16(tmem + lane_base + kColO, o);
+                    tmem_wait_st();
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();  // every lane's P^T bytes and TMEM stores before lane 0's arrival
+                if (lane == 0) mbar_arrive(bar_p0 + 8 * (i & 1));
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();  // every lane's P^T bytes and TMEM stores before lane 0's arrival
-            if (lane == 0) mbar_arrive(bar_p0 + 8 * (j & 1));
+        } else {
+            for (int j = 0; j < T; ++j) {
+                const int key = k0 + j * DBN + kl;
+                if (!(ok = dwait_warp(bar_s0 + 8 * (j & 1), (j >> 1) & 1, abort_flag, p.status))) break;
+                tc_fence_after();
+                uint32_t sr[16];
+                tmem_ld_x16(tmem + lane_base + dcol_s(j & 1), sr);
+                asm volatile("tcgen05.wait::ld.sync.aligned;"
+                             : "+r"(sr[0]), "+r"(sr[1]), "+r"(sr[2]), "+r"(sr[3]), "+r"(sr[4]), "+r"(sr[5]), "+r"(sr[6]),
+                               "+r"(sr[7]), "+r"(sr[8]), "+r"(sr[9]), "+r"(sr[10]), "+r"(sr[11]), "+r"(sr[12]),
+                               "+r"(sr[13]), "+r"(sr[14]), "+r"(sr[15])::"memory");
+                float t[RP];
+#pragma unroll
+                for (int r = 0; r < RP; ++r)
+                    t[r] = (key >= lo[r] && key < hi[r]) ? __uint_as_float(sr[r]) * c : -INFINITY;
+                // tile row maxima across the 128 keys
+                float* redj = red + (j & 1) * 4 * DNR;
+#pragma unroll
+                for (int r = 0; r < RP; ++r) {
+                    float x = t[r];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+                    if (lane == 0) redj[warp * DNR + r] = x;
+                }
+                if (lane == 0) mbar_arrive(bar_red0 + 8 * (j & 1));  // lane 0 wrote the warp's maxima
+                if (!(ok = dwait_warp(bar_red0 + 8 * (j & 1), (j >> 1) & 1, abort_flag, p.status))) break;
+                bool need_any = false;
+                float alpha[RP];
+#pragma unroll
+                for (int r = 0; r < RP; ++r) {
+                    alpha[r] = 1.f;
+                    const float mt = fmaxf(fmaxf(redj[r], redj[DNR + r]), fmaxf(redj[2 * DNR + r], redj[3 * DNR + r]));
+                    const float m_new = fmaxf(m_ref[r], mt);
+                    if (m_new > m_ref[r] + kDecRescale) {
+                        alpha[r] = ex2(m_ref[r] - m_new);
+                        l_part[r] *= alpha[r];
+                        m_ref[r] = m_new;
+                        need_any = true;
+                    }
+                }
+                // P^T buffer j&1 was last read by the value product of tile j-2
+                if (j >= 2 && !(ok = dwait_warp(bar_free0 + 8 * (j & 1), ((j - 2) >> 1) & 1, abort_flag, p.status)))
+                    break;
+                uint8_t* pbuf = smem + C::kOffP + (j & 1) * C::kPBytes;
+#pragma unroll
+                for (int r = 0; r < RP; ++r) {
+                    const float m_use = (m_ref[r] == -INFINITY) ? 0.f : m_ref[r];
+                    const float pr = ex2(t[r] - m_use);
+                    l_part[r] += pr;
+                    // P^T row r, key kl, in the 128-byte swizzle: 16-byte granule g of row r sits at g ^ (r & 7)
+                    if constexpr (EB == 1) {
+                        const int off = r * 128 + ((((kl >> 4) ^ (r & 7))) << 4) + (kl & 15);
+                        pbuf[off] = (uint8_t)(pack_e4m3x4(pr, 0.f, 0.f, 0.f) & 0xFFu);
+                    } else {
+                        const int kc = kl >> 6, k64 = kl & 63;
+                        const uint32_t pk = kBF16 ? pack_bf16(pr, 0.f) : pack_f16(pr, 0.f);
+                        const int off = kc * kQChunk + r * 128 + ((((k64 >> 3) ^ (r & 7))) << 4) + (k64 & 7) * 2;
+                        *reinterpret_cast<uint16_t*>(pbuf + off) = (uint16_t)(pk & 0xFFFFu);
+                    }
+                }
+                // lazy rescale of O^T (needs the value product of tile j-1 complete)
+                if (need_any && j > 0) {
+                    if (!(ok = dwait_warp(bar_free0 + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag, p.status)))
+                        break;
+                    tc_fence_after();
+                    uint32_t o[16];
+                    tmem_ld_x16(tmem + lane_base + kColO, o);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                                 : "+r"(o[0]), "+r"(o[1]), "+r"(o[2]), "+r"(o[3]), "+r"(o[4]), "+r"(o[5]), "+r"(o[6]),
+                                   "+r"(o[7]), "+r"(o[8]), "+r"(o[9]), "+r"(o[10]), "+r"(o[11]), "+r"(o[12]),
+                                   "+r"(o[13]), "+r"(o[14]), "+r"(o[15])::"memory");
+#pragma unroll
+                    for (int r = 0; r < RP; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[r]);
+                    tmem_st_x16(tmem + lane_base + kColO, o);
+                    tmem_wait_st();
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();  // every lane's P^T bytes and TMEM stores before lane 0's arrival
+                if (lane == 0) mbar_arrive(bar_p0 + 8 * (j & 1));
+            }
+
         }
 
         // summary of this split: m (base 2), l, acc for the group's rows
@@ -548,7 +742,7 @@ __global__ void __launch_bounds__(kDecThreads)
         }
         if (have) {
             uint32_t o[16];
-            tmem_ld_x16(tmem + lane_base + kColOT, o);
+            tmem_ld_x16(tmem + lane_base + kColO, o);
             asm volatile("tcgen05.wait::ld.sync.aligned;"
                          : "+r"(o[0]), "+r"(o[1]), "+r"(o[2]), "+r"(o[3]), "+r"(o[4]), "+r"(o[5]), "+r"(o[6]),
                            "+r"(o[7]), "+r"(o[8]), "+r"(o[9]), "+r"(o[10]), "+r"(o[11]), "+r"(o[12]), "+r"(o[13]),
@@ -648,7 +842,7 @@ __global__ void __launch_bounds__(kDecThreads)
     __syncthreads();
     if (warp == kDecMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, kCols);
     }
 }
 
