@@ -116,6 +116,21 @@ def test_fp8_decode_shapes(shape, causal, window, descale, path):
     assert np.abs(lse.cpu().double().numpy() - want_lse).max() <= 2e-3
 
 
+@pytest.mark.parametrize("N,causal,window", [(256, True, 0), (384, True, 0), (512, False, 0), (640, True, 0),
+                                             (1100, True, 300), (1100, False, 0)])
+def test_fp8_decode_round_counts(N, causal, window):
+    """304 KV groups (B = 76, Hkv = 4) take one split each, so a CTA streams all
+    ceil(N / 128) key tiles: the 8-bit decode's rounds of two tiles with an even
+    and an odd tile count, several rounds, and a window that starts inside a round."""
+    B, Hq, Hkv, M, D = 76, 8, 4, 1, 128
+    q, k, v = make_qkv_fp8(B, Hq, Hkv, M, N, D, 31, 1.0, 1.0, 1.0)
+    o = sa.attention_fp8(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, window=window, path=sa.PATH_DECODE)
+    torch.cuda.synchronize()
+    want = oracle.attention_fp8(q, k, v, causal=causal, window=window)
+    H, sigma, wabs = bounds(deq(q, 1.0), deq(k, 1.0), deq(v, 1.0), causal, window, 1.0 / np.sqrt(D))
+    check_fp8(o, want, H, sigma, wabs, torch.bfloat16, f"rounds N={N} causal={causal} window={window}")
+
+
 def test_fp8_decode_workload_full_size():
     """The GQA decode shape (B=8, Hq=32, Hkv=8, M=1, N=8192, window 4096) in E4M3,
     every row, with a caller workspace."""
