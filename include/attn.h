@@ -398,7 +398,11 @@ ATTN_API const char* attn_strerror(int status);
 
 /* Synchronizes `stream`, then returns and clears the device status word that
  * kernels set when a bounded wait gives up: ATTN_OK when none did, else
- * ATTN_ERR_TIMEOUT. ATTN_ERR_CUDA if the synchronization itself failed. */
+ * ATTN_ERR_TIMEOUT. ATTN_ERR_CUDA if the synchronization itself failed.
+ * There is one status word per device, shared by every stream and host thread
+ * that calls into the library on that device: a give-up on one stream is
+ * reported to, and cleared by, whichever caller reads the word first (a caller
+ * that needs per-stream attribution must serialize its status reads). */
 ATTN_API int attn_last_device_status(void* stream);
 
 /* Self-test of failure reporting: launches one CTA that waits on an mbarrier
