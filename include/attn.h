@@ -416,7 +416,7 @@ ATTN_API int attn_selftest_bounded_wait(unsigned timeout_us, void* stream);
  * tcgen05 prefill (D = 128, dtype ATTN_BF16 / ATTN_FP16) on the caller's
  * device buffers (as attn_fwd) with the softmax warps of query tile 0
  * withholding their P-ready arrival at score tile `withhold_at` of each CTA's
- * walk. The issuing thread's bounded wait (1 s) runs out, and every CTA that
+ * walk. The issuing warp's bounded wait (1 s) runs out, and every CTA that
  * reaches that tile raises the abort flag, drains its copies and MMAs, frees
  * TMEM and exits; attn_last_device_status then returns ATTN_ERR_TIMEOUT and the
  * context stays usable. o is left unspecified. No fault, trap or hang.

@@ -118,7 +118,7 @@ struct PrefillParams {
     int tiles;  // BH * nqb
     // failure-path self-test only (-1 otherwise): the softmax warps of query tile 0
     // withhold their P-ready arrival for this score tile (counted over the CTA's walk),
-    // so the issuing thread's bounded wait runs out and the whole CTA takes its abort path
+    // so the issuing warp's bounded wait runs out and the whole CTA takes its abort path
     long withhold_p_at;
 };
 
@@ -219,7 +219,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     return kBF16 ? pack_bf16(lo, hi) : pack_f16(lo, hi);
 }
 
-// MMA groups issued from precomputed descriptors: the issuing thread must
+// MMA groups issued from precomputed descriptors: the issuing warp must
 // keep up with the tensor core (a 128x128 MMA step retires in 64 cycles for
 // 16-bit inputs, 32 for 8-bit), so each K step only adds a compile-time offset
 // to a 64-bit descriptor. Every K step covers 32 bytes of a row: 16 elements

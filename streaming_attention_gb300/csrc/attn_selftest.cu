@@ -2,7 +2,7 @@
 // waits on an mbarrier phase that nothing completes, with the same bounded-wait
 // pattern the kernels use (poll, then give up after a time limit), and reports
 // through the device status word. attn_selftest_prefill_abort: the real prefill
-// kernel with one P-ready arrival withheld, so its issuing thread's wait runs out
+// kernel with one P-ready arrival withheld, so its issuing warp's wait runs out
 // and every CTA takes its abort path (drain copies and MMAs, free TMEM, exit).
 // Nothing faults, traps or hangs: the kernels return normally.
 #include "attn_internal.h"
