@@ -519,6 +519,13 @@ def extra_measurements(args, dev, stream, flush):
     if args.workload in (PREFILL_D128.name, DECODE_GQA.name):
         for ps in (16, 128):
             out[f"decode_gqa_paged{ps}"] = paged_decode_measure(DECODE_GQA, ps, steps, dev, stream, flush)
+        # shapes of the grouped CUDA-core paged kernel: D = 64, and 8 speculative
+        # rows per sequence (32 grouped rows per KV head) at D = 128
+        import dataclasses
+        d64 = dataclasses.replace(DECODE_GQA, name="decode_gqa_b8_hq32_hkv8_m1_n8192_w4096_d64_bf16", D=64)
+        out["decode_gqa_d64_paged16"] = paged_decode_measure(d64, 16, steps, dev, stream, flush)
+        m8 = dataclasses.replace(DECODE_GQA, name="decode_gqa_b8_hq32_hkv8_m8_n8192_w4096_d128_bf16", M=8)
+        out["decode_gqa_m8_paged16"] = paged_decode_measure(m8, 16, steps, dev, stream, flush)
     return out
 
 
@@ -694,8 +701,13 @@ def paged_decode_measure(w, page_size, steps, dev, stream, flush):
 
     ms = time_steady(fn_on, sets, steps, 3, stream)
     cold = statistics.median(time_graph(lambda st: fn_on(sets[0], st), steps, 3, flush))
-    return {"GB/s": round(decode_bytes(w) / (ms * 1e-3) / 1e9, 1), "us": round(ms * 1e3, 2),
-            "cold_call_us": round(cold * 1e3, 2), "path": f"paged decode, {page_size}-key pages, shuffled pool"}
+    gbs = decode_bytes(w) / (ms * 1e-3) / 1e9
+    pk, pk_src = peaks()
+    kernel = "tcgen05 split" if w.D == 128 and (w.Hq // w.Hkv) * w.M <= 16 else "grouped CUDA-core"
+    return {"GB/s": round(gbs, 1), "us": round(ms * 1e3, 2), "cold_call_us": round(cold * 1e3, 2),
+            "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4), "peak_source": pk_src,
+            "path": f"paged decode ({kernel} kernel), {page_size}-key pages, shuffled pool",
+            "shape": {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "M": w.M, "N": w.N, "window": w.window, "D": w.D}}
 
 
 # ----------------------------------------------------------------------------

@@ -89,15 +89,16 @@ typedef enum {
 /* Kernel paths. AUTO picks: split-KV decode when (Hq/Hkv)*M <= 16 and the
  * visible key range is long; the tcgen05 prefill kernel for D in {64, 128};
  * the SIMT kernel otherwise (D in {16, 32, 64, 128}).
- * The SIMT kernel, which also runs split decode for D = 64, for more than 16
- * grouped rows and for B*Hkv > 65535, and the log-sum-exp of an N == 0 call,
+ * The SIMT kernel, which also runs split decode for D = 64 and for
+ * B*Hkv > 65535, and the log-sum-exp of an N == 0 call,
  * takes at most 65535 (batch, query head) pairs: B*Hq > 65535 there returns
  * ATTN_ERR_PATH (AUTO then prefers the prefill kernel for D in {64, 128}). */
 typedef enum {
     ATTN_PATH_AUTO = 0,
     ATTN_PATH_SIMT = 1,    /* CUDA-core streaming kernel, any supported D, B*Hq <= 65535 */
     ATTN_PATH_PREFILL = 2, /* warp-specialized TMA + tcgen05 + TMEM kernel, D in {64,128} */
-    ATTN_PATH_DECODE = 3,  /* split-KV over grouped query heads; the splits merged in a thread-block
+    ATTN_PATH_DECODE = 3,  /* split-KV over grouped query heads (D = 128 on tcgen05: the grouped
+                              rows of a KV head in CTAs of 16); the splits merged in a thread-block
                               cluster (at most 8 splits per KV head) or by the merge kernel */
     ATTN_PATH_PREFILL_PAIR = 4 /* the prefill on the pair MMA (tcgen05 cta_group::2): clusters of two
                               CTAs share 512-row work tiles, each loading half of every K/V tile;
@@ -198,7 +199,7 @@ ATTN_API int attn_fwd_lse(const void* q, const void* k, const void* v, void* o, 
  *   checked).
  *   path: ATTN_PATH_AUTO (split-KV decode when (Hq/Hkv) * M <= 16 and the
  *   visible key range spans at least 512 keys, else prefill), ATTN_PATH_PREFILL,
- *   or ATTN_PATH_DECODE ((Hq/Hkv) * M <= 16, else ATTN_ERR_PATH); ATTN_PATH_SIMT
+ *   or ATTN_PATH_DECODE (any number of grouped rows, in CTAs of 16); ATTN_PATH_SIMT
  *   is not offered (ATTN_ERR_PATH).
  *   workspace: for the decode path, attn_fwd_fp8_workspace_bytes(...) bytes of
  *   the same problem and path (the 8-bit kernel runs more splits than the
@@ -289,8 +290,8 @@ ATTN_API int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, vo
  *   Returns ATTN_ERR_WORKSPACE when the problem's split summaries
  *   (attn_workspace_bytes_ex(..., ATTN_PATH_DECODE)) exceed the array and the
  *   splits do not merge inside their cluster (see below), and
- *   ATTN_ERR_PATH when the splits would run on the SIMT kernel (D = 64, or
- *   more than 16 grouped rows) with B*Hq > 65535.
+ *   ATTN_ERR_PATH when the splits would run on the SIMT kernel (D = 64) with
+ *   B*Hq > 65535.
  *   The first call on a device looks up the array's device address (with
  *   that device current); make that first call before any stream capture.
  *   Every call, on any stream, shares the one array and leaves its contents
@@ -332,14 +333,22 @@ ATTN_API int attn_fwd_decode_noalloc(const void* q, const void* k, const void* v
  *   page_size   16, 32, 64 or a multiple of 128.
  *   max_seq_len a host-side bound of the seq_lens values: it sizes the split
  *               plan; keys past it are ignored.
- *   D must be 128 (ATTN_ERR_HEADDIM) and (Hq/Hkv) * M at most 16
- *   (ATTN_ERR_PATH); B * Hkv <= 65535.
+ *   D is 16, 32, 64 or 128 (else ATTN_ERR_HEADDIM); B * Hkv <= 65535 and at
+ *   most 16 * 65535 (D = 128) or 8 * 65535 (else) grouped rows (Hq/Hkv) * M
+ *   per KV head (else ATTN_ERR_OVERFLOW).
+ *   Kernels: D = 128 runs the tcgen05 split kernel (pages gathered by TMA, the
+ *   grouped rows of a KV head in CTAs of 16); D in {16, 32, 64} runs a grouped
+ *   CUDA-core kernel (one block per split, sequence, KV head and eight grouped
+ *   rows, each 32-key tile gathered from its pages once for all of them). Both
+ *   end in the same common-maximum merge.
  *   Every element of a page that a sequence uses must be finite, also in the
  *   rows of its last page past L_b: masked keys get probability 0, and their
  *   value rows are still multiplied by it.
  *   workspace: device memory of attn_decode_paged_workspace_bytes(...) bytes,
  *   16-byte aligned; NULL makes the call allocate it stream-ordered
- *   (cudaMallocAsync / cudaFreeAsync on `stream`), as attn_fwd does.
+ *   (cudaMallocAsync / cudaFreeAsync on `stream`), as attn_fwd does. The
+ *   size is 0 when the grouped kernel plans one split per sequence (it then
+ *   writes o itself) and the workspace is not read.
  *   When num_pages == 0 or min(max_seq_len, max_pages * page_size) == 0, o is
  *   zero-filled. */
 ATTN_API size_t attn_decode_paged_workspace_bytes(int B, int Hq, int Hkv, int M, int D,

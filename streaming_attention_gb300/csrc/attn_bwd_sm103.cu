@@ -168,14 +168,6 @@ __device__ __forceinline__ void mma_tmem_by_tile(uint32_t d_tmem, uint32_t a_tme
                (first && kk == 0) ? 0u : 1u);
 }
 
-// Orders later uses of r after the preceding asm statements (no instruction).
-__device__ __forceinline__ void reg_after_x16(uint32_t (&r)[16]) {
-    asm volatile(""
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
-                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
-                   "+r"(r[15])::"memory");
-}
-
 // 16-bit pair (low half first) -> two floats
 template <bool kBF16>
 __device__ __forceinline__ void unpack2(uint32_t w, float& lo, float& hi) {

@@ -1,7 +1,10 @@
 // Split-KV decode on the tcgen05 tensor cores (sm_103a), D = 128.
 //
 // Decode has few query rows per KV head: the R = (Hq/Hkv) * M rows that share
-// one KV head (GQA grouping) are processed together, padded to 16. The score
+// one KV head (GQA grouping) are processed together, padded to 16; more than 16
+// are cut into blocks of 16 rows, one CTA each along the grid's z (each streams
+// the split's K/V tiles; the blocks of one split run side by side, so their
+// re-reads of the same tiles mostly hit L2). The score
 // tile is computed transposed, S^T[128 keys x 16 rows] = K_tile Q^T, so the
 // 128 keys fill the MMA's M dimension instead of 112 padded query rows; then
 // O^T[128 dims x 16 rows] += V_tile^T P^T. One thread owns one key for the
@@ -76,7 +79,8 @@ struct DecodeParams {
     float* ws_l;
     float* ws_acc;
     int* status;
-    int Hq, Hkv, M, N, G, R;
+    int Hq, Hkv, M, N, G;
+    int R;  // grouped query rows per KV head (G * M); CTA z takes rows [16 z, 16 z + 16) of them
     int causal, window;
     float scale_log2;
     int klo, khi, kbase, chunk, S;
@@ -270,7 +274,9 @@ __global__ void __launch_bounds__(kDecThreads)
     const int split = blockIdx.x;
     const int grp = blockIdx.y;  // b * Hkv + g
     const int b = grp / p.Hkv, g = grp % p.Hkv;
-    const int row_base = (b * p.Hq + g * p.G) * p.M;  // first global row of the group
+    const int rblk = blockIdx.z;  // block of 16 of the group's grouped rows
+    const int R = min(DNR, p.R - rblk * DNR);  // rows of this CTA
+    const int row_base = (b * p.Hq + g * p.G) * p.M + rblk * DNR;  // first global row of this CTA
 
     if (threadIdx.x == 0) {
         mbar_init(bar_q, 1);
@@ -534,9 +540,9 @@ __global__ void __launch_bounds__(kDecThreads)
         int lo[RP], hi[RP];
 #pragma unroll
         for (int r = 0; r < RP; ++r) {
-            const int i = r % p.M;
+            const int i = (rblk * DNR + r) % p.M;
             key_range(i + sq.N - p.M, sq.N, p.causal, p.window, &lo[r], &hi[r]);
-            if (r >= p.R) hi[r] = lo[r];  // padding rows see nothing: their scores are -inf, p = 0
+            if (r >= R) hi[r] = lo[r];  // padding rows see nothing: their scores are -inf, p = 0
         }
         float m_ref[RP], l_part[RP];
 #pragma unroll
@@ -730,7 +736,7 @@ __global__ void __launch_bounds__(kDecThreads)
             tc_fence_after();
 #pragma unroll
             for (int r = 0; r < RP; ++r) {
-                if (r < p.R) {
+                if (r < R) {
                     float x = l_part[r];
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
@@ -749,7 +755,7 @@ __global__ void __launch_bounds__(kDecThreads)
                            "+r"(o[14]), "+r"(o[15])::"memory");
 #pragma unroll
             for (int r = 0; r < RP; ++r) {
-                if (r < p.R) {
+                if (r < R) {
                     const float lsum = lred[r] + lred[DNR + r] + lred[2 * DNR + r] + lred[3 * DNR + r];
                     if (p.cluster) {  // the summary stays in this CTA's (now idle) ring
                         part[r * DD + kl] = __uint_as_float(o[r]);
@@ -769,7 +775,7 @@ __global__ void __launch_bounds__(kDecThreads)
             }
         } else if (p.cluster) {
             // no key in this split (or it gave up): the empty summary
-            for (int r = 0; r < p.R; ++r) {
+            for (int r = 0; r < R; ++r) {
                 part[r * DD + kl] = 0.f;
                 if (kl == 0) {
                     part[DNR * DD + r] = -INFINITY;
@@ -779,7 +785,7 @@ __global__ void __launch_bounds__(kDecThreads)
         } else {
             // no key of this split, or it gave up on a bounded wait: the empty
             // summary, so the merge never reads a slot this call did not write
-            for (int r = 0; r < p.R; ++r) {
+            for (int r = 0; r < R; ++r) {
                 const size_t slot = (size_t)(row_base + r) * p.S + split;
                 p.ws_acc[slot * DD + kl] = 0.f;
                 if (kl == 0) {
@@ -801,7 +807,7 @@ __global__ void __launch_bounds__(kDecThreads)
             // distributed-shared-memory round trips overlap.
             const int kl = threadIdx.x;
             const uint32_t local = smem_u32(part);
-            for (int r = (int)cluster_rank(); r < p.R; r += p.S) {
+            for (int r = (int)cluster_rank(); r < R; r += p.S) {
                 float ms[kMaxClusterSplits], ls[kMaxClusterSplits], as[kMaxClusterSplits];
 #pragma unroll
                 for (int sp = 0; sp < kMaxClusterSplits; ++sp) {
@@ -911,7 +917,7 @@ cudaError_t launch_decode_t(const Problem& pr, const void* q, const void* k, con
     // Programmatic launch: CTAs may start their setup (barriers, TMEM) while the
     // previous kernel in the stream drains; griddepcontrol.wait orders the rest.
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(S, pr.B * pr.Hkv);
+    cfg.gridDim = dim3(S, pr.B * pr.Hkv, (pr.G * pr.M + DNR - 1) / DNR);
     cfg.blockDim = dim3(kDecThreads);
     cfg.dynamicSmemBytes = DCfg<EB>::kSmem;
     cfg.stream = stream;
@@ -965,7 +971,13 @@ void plan_splits(int tiles, int groups, int* chunk, int* S, int per_sm) {
 
 }  // namespace
 
-bool decode_tc_supported(const Problem& p) { return p.D == DD && p.G * p.M <= DNR && p.B * p.Hkv <= 65535; }
+// Any number of grouped rows: CTAs of 16 rows each along the grid's z (at most 65535).
+bool decode_tc_supported(const Problem& p) {
+    return p.D == DD && p.B * p.Hkv <= 65535 && ((long long)p.G * p.M + DNR - 1) / DNR <= 65535;
+}
+
+// (KV group, block of 16 grouped rows) pairs: the CTAs of one split
+static int row_groups(const Problem& p) { return p.B * p.Hkv * ((p.G * p.M + DNR - 1) / DNR); }
 
 // CTAs resident per SM (two for both input widths; the plan keeps the 8-bit
 // switch so that its workspace query stays separate from the 16-bit one)
@@ -978,7 +990,7 @@ int ctas_per_sm(const Problem& p, bool e4m3) {
 int decode_plan_tc(const Problem& p, int* chunk, int* S, bool e4m3) {
     const int kbase = split_base(p);
     const int tiles = p.khi > kbase ? (p.khi - kbase + DBN - 1) / DBN : 1;
-    plan_splits(tiles, p.B * p.Hkv, chunk, S, ctas_per_sm(p, e4m3));
+    plan_splits(tiles, row_groups(p), chunk, S, ctas_per_sm(p, e4m3));
     return ATTN_OK;
 }
 
@@ -999,7 +1011,7 @@ int decode_plan_paged(const Problem& p, const PagedKV& kv, int* chunk, int* S, b
         if (wt < tiles) tiles = (int)wt;
     }
     if (tiles < 1) tiles = 1;
-    plan_splits(tiles, p.B * p.Hkv, chunk, S, ctas_per_sm(p, e4m3));
+    plan_splits(tiles, row_groups(p), chunk, S, ctas_per_sm(p, e4m3));
     return ATTN_OK;
 }
 

@@ -26,7 +26,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // rule of the 16-bit forward), else the prefill kernel
 int choose_fp8_path(const Problem& p, int path) {
     if (path != ATTN_PATH_AUTO) return path;
-    if (decode_tc_supported(p) && (p.khi - p.klo) >= 512) return ATTN_PATH_DECODE;
+    if (decode_tc_supported(p) && (int64_t)p.G * p.M <= 16 && (p.khi - p.klo) >= 512) return ATTN_PATH_DECODE;
     return ATTN_PATH_PREFILL;
 }
 

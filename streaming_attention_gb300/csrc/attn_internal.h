@@ -105,7 +105,7 @@ cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const 
                           cudaStream_t stream, DecodeOut* out = nullptr);
 bool decode_supported(const Problem& p);
 int decode_plan(const Problem& p, int* chunk, int* S);
-// tcgen05 split kernel (D = 128, at most 16 grouped rows per KV head)
+// tcgen05 split kernel (D = 128; grouped rows per KV head in CTAs of 16)
 bool decode_tc_supported(const Problem& p);
 // e4m3: the plan of the 8-bit kernel (more CTAs per SM, so more splits)
 int decode_plan_tc(const Problem& p, int* chunk, int* S, bool e4m3 = false);
@@ -128,6 +128,17 @@ int decode_plan_paged(const Problem& p, const PagedKV& kv, int* chunk, int* S, b
 cudaError_t launch_decode_paged(const Problem& p, const void* q, const PagedKV& kv, int chunk, int S,
                                 const SplitWorkspace& ws, int* status, cudaStream_t stream, DecodeOut* out = nullptr,
                                 bool e4m3 = false);
+// Which kernel takes a paged call: the tcgen05 split kernel (D = 128), else the
+// grouped CUDA-core kernel (D in {16, 32, 64}; grouped rows up to 8 * 65535).
+bool paged_tc_supported(const Problem& p);
+bool paged_group_supported(const Problem& p);
+int paged_group_plan(const Problem& p, const PagedKV& kv, int* chunk, int* S);
+// ws may be null when S == 1 (the kernel then writes o, times out_scale);
+// otherwise the caller merges the summaries. e4m3: Q and the pools hold E4M3
+// bytes and p.dtype is the output type.
+cudaError_t launch_paged_group(const Problem& p, const void* q, const PagedKV& kv, int chunk, int S,
+                               const SplitWorkspace* ws, void* o, float out_scale, bool e4m3,
+                               cudaStream_t stream);
 // The tcgen05 split kernel on contiguous E4M3 inputs (same plan as launch_decode_tc)
 cudaError_t launch_decode_e4m3(const Problem& p, const void* q, const void* k, const void* v, int chunk, int S,
                                const SplitWorkspace& ws, int* status, cudaStream_t stream, DecodeOut* out = nullptr);

@@ -1,6 +1,7 @@
 // C ABI of split-KV decode over a paged KV cache (16-bit or E4M3): metadata
-// validation, the split plan, the tcgen05 split kernel in paged mode and the
-// merge kernel.
+// validation, the split plan, and the kernels: the tcgen05 split kernel in
+// paged mode (D = 128, at most 16 grouped query rows per KV head) or the
+// grouped CUDA-core kernel (every other shape), then the merge kernel.
 // Attention over a KV-cache slice is the decode step the course's plan names
 // next ("Kernel Notes & Checklist", section 3, the plan, week +3: sliding
 // window + GQA + KV-cache slice); pages of the cache are gathered by the TMA
@@ -37,9 +38,8 @@ int validate_paged(const void* q, const void* kp, const void* vp, const int* tab
     if (Hq > 0 && Hkv == 0) return ATTN_ERR_SHAPE;
     if (!page_size_ok(page_size)) return ATTN_ERR_SHAPE;
     if (Hq > 0 && Hq % Hkv != 0) return ATTN_ERR_GQA;
-    if (D != 128) return ATTN_ERR_HEADDIM;
+    if (D != 16 && D != 32 && D != 64 && D != 128) return ATTN_ERR_HEADDIM;
     const int G = Hkv > 0 ? Hq / Hkv : 1;
-    if ((int64_t)G * M > 16) return ATTN_ERR_PATH;
     const int64_t nq = (int64_t)B * Hq * M * D;
     const int64_t npool = (int64_t)num_pages * Hkv * page_size * D;
     const int64_t ntab = (int64_t)B * max_pages;
@@ -68,14 +68,26 @@ int validate_paged(const void* q, const void* kp, const void* vp, const int* tab
     p.khi = max_len;
     p.lse = nullptr;
     c->kv = PagedKV{kp, vp, table, lens, num_pages, page_size, max_pages, max_len};
+    if (!paged_tc_supported(p) && !paged_group_supported(p)) return ATTN_ERR_OVERFLOW;
     return ATTN_OK;
 }
 
 bool nothing_to_attend(const PagedCall& c) { return c.kv.max_len == 0 || c.kv.num_pages == 0 || c.p.Hkv == 0; }
 
+// The split plan of the kernel that runs this call.
+void paged_plan(const PagedCall& c, bool e4m3, int* chunk, int* S) {
+    if (paged_tc_supported(c.p))
+        decode_plan_paged(c.p, c.kv, chunk, S, e4m3);
+    else
+        paged_group_plan(c.p, c.kv, chunk, S);
+}
+
+// Scratch for the splits' summaries; the grouped kernel with one split writes
+// the output itself and needs none.
 size_t paged_workspace(const PagedCall& c, bool e4m3 = false) {
     int chunk = 0, S = 0;
-    decode_plan_paged(c.p, c.kv, &chunk, &S, e4m3);
+    paged_plan(c, e4m3, &chunk, &S);
+    if (!paged_tc_supported(c.p) && S == 1) return 0;
     return split_workspace_bytes(c.p.B * c.p.Hq * c.p.M, S, c.p.D);
 }
 
@@ -85,8 +97,18 @@ int run_paged(const PagedCall& c, const void* q, void* o, void* ws, size_t ws_by
               bool e4m3 = false, float v_descale = 1.0f) {
     const Problem& p = c.p;
     int chunk = 0, S = 0;
-    decode_plan_paged(p, c.kv, &chunk, &S, e4m3);
+    paged_plan(c, e4m3, &chunk, &S);
     const int rows = p.B * p.Hq * p.M;
+    if (!paged_tc_supported(p)) {
+        if (S == 1) return cuda_status(launch_paged_group(p, q, c.kv, chunk, S, nullptr, o, v_descale, e4m3, stream));
+        if (!ws || ws_bytes < split_workspace_bytes(rows, S, p.D)) return ATTN_ERR_WORKSPACE;
+        if (!aligned(ws, 16)) return ATTN_ERR_ALIGN;
+        SplitWorkspace w = split_workspace(ws, rows, S, p.D);
+        if (launch_paged_group(p, q, c.kv, chunk, S, &w, o, v_descale, e4m3, stream) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        return cuda_status(launch_merge(w.m, w.l, w.acc, o, nullptr, nullptr, nullptr, rows, S, p.D, p.dtype, 1.0f,
+                                        false, stream, v_descale));
+    }
     if (!ws || ws_bytes < split_workspace_bytes(rows, S, p.D)) return ATTN_ERR_WORKSPACE;
     if (!aligned(ws, 16)) return ATTN_ERR_ALIGN;
     int* status = device_status_ptr();
@@ -133,6 +155,7 @@ int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages, c
         return cuda_status(cudaMemsetAsync(o, 0, (size_t)B * Hq * M * D * 2, s));
     if (workspace) return run_paged(c, q, o, workspace, ws_bytes, s);
     const size_t bytes = paged_workspace(c);
+    if (bytes == 0) return run_paged(c, q, o, nullptr, 0, s);
     void* ws = nullptr;
     if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) return ATTN_ERR_CUDA;
     rc = run_paged(c, q, o, ws, bytes, s);
@@ -168,6 +191,7 @@ int attn_decode_paged_fp8(const void* q, const void* k_pages, const void* v_page
     c.p.scale_log2 = (float)((double)c.p.scale * (double)q_descale * (double)k_descale * (double)kLog2e);
     if (workspace) return run_paged(c, q, o, workspace, ws_bytes, s, true, v_descale);
     const size_t bytes = paged_workspace(c, true);
+    if (bytes == 0) return run_paged(c, q, o, nullptr, 0, s, true, v_descale);
     void* ws = nullptr;
     if (cudaMallocAsync(&ws, bytes, s) != cudaSuccess) return ATTN_ERR_CUDA;
     rc = run_paged(c, q, o, ws, bytes, s, true, v_descale);

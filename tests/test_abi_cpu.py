@@ -168,8 +168,10 @@ def paged(L, q=A16, kp=A16, vp=A16, table=A16, lens=A16, o=A16, B_=2, Hq=8, Hkv=
     (dict(page_size=0), -2),
     (dict(Hkv=0), -2),
     (dict(Hq=6, Hkv=4), -5),
-    (dict(D=64), -4),
-    (dict(Hq=16, Hkv=2, M=3), -11),   # 8 grouped heads x 3 rows > 16
+    (dict(D=48), -4),
+    (dict(D=256), -4),
+    (dict(Hq=2, Hkv=2, M=1100000), -6),        # D = 128: more than 16 x 65535 grouped rows
+    (dict(Hq=2, Hkv=2, M=600000, D=64), -6),   # D = 64: more than 8 x 65535 grouped rows
     (dict(num_pages=1 << 20, page_size=128), -6),
     (dict(B_=70000, Hkv=1, Hq=1), -6),
     (dict(q=None), -1),
@@ -191,7 +193,10 @@ def test_paged_workspace_bytes(L):
     assert nb > 0 and nb % 256 == 0
     S = nb // (rows * 4 * 130)
     assert 1 <= S <= 64
-    assert sa.attn_decode_paged_workspace_bytes(8, 32, 8, 1, 64, 16, 512, 8192, True, 0) == 0   # D = 64
+    assert sa.attn_decode_paged_workspace_bytes(8, 32, 8, 1, 48, 16, 512, 8192, True, 0) == 0   # D = 48
+    # D = 64 (the grouped CUDA-core kernel) and 32 grouped rows per KV head at D = 128 (two CTAs of 16)
+    assert sa.attn_decode_paged_workspace_bytes(8, 32, 8, 1, 64, 16, 512, 8192, True, 0) % 256 == 0
+    assert sa.attn_decode_paged_workspace_bytes(2, 32, 1, 1, 128, 16, 512, 8192, True, 0) > 0
     assert sa.attn_decode_paged_workspace_bytes(8, 32, 8, 1, 128, 16, 512, 0, True, 0) == 0     # no keys
     assert sa.attn_decode_paged_workspace_bytes(0, 32, 8, 1, 128, 16, 512, 8192, True, 0) == 0  # no rows
     # a 4-byte aligned table and length array are accepted (validation passes, nothing launched: B = 0)
@@ -244,7 +249,7 @@ def test_selftest_rejects_bad_limits(L):
     (dict(M=0), 0),                      # empty output: nothing to do, no launch
     (dict(path=1), -11),                 # no SIMT form for 8-bit inputs
     (dict(path=7), -11),
-    (dict(path=3, Hq=32, Hkv=1, M=1), -11),   # decode needs (Hq/Hkv) * M <= 16
+    (dict(path=3, Hq=1, Hkv=1, M=1100000), -11),  # more than 16 x 65535 grouped rows for the decode grid
 ])
 def test_fp8_validation_status(L, kw, status):
     a = dict(q=A16, k=A16, v=A16, o=A16, lse=None, B_=1, Hq=2, Hkv=2, M=8, N=8, D=128, dtype=0, path=0)
@@ -277,8 +282,7 @@ def paged_fp8(L, q=A16, kp=A16, vp=A16, table=A16, lens=A16, o=A16, B_=2, Hq=8, 
     (dict(dtype=2), -3),               # the output is BF16 or FP16
     (dict(page_size=48), -2),
     (dict(Hq=6, Hkv=4), -5),
-    (dict(D=64), -4),
-    (dict(Hq=16, Hkv=2, M=3), -11),
+    (dict(D=48), -4),
     (dict(kp=None), -1),
     (dict(o=A8), -7),
     (dict(B_=0), 0),                   # no rows: nothing to do, no launch
@@ -290,8 +294,10 @@ def test_paged_fp8_validation_status(L, kw, status):
 def test_fp8_workspace_queries_reject_bad_shapes(L):
     assert sa.attn_fwd_fp8_workspace_bytes(-1, 32, 8, 1, 8192, 128, True, 0, sa.PATH_DECODE) == 0
     assert sa.attn_fwd_fp8_workspace_bytes(8, 32, 8, 1, 8192, 128, True, 0, sa.PATH_SIMT) == 0
-    assert sa.attn_fwd_fp8_workspace_bytes(1, 64, 1, 1, 8192, 128, True, 0, sa.PATH_DECODE) == 0  # 64 rows > 16
-    assert sa.attn_decode_paged_fp8_workspace_bytes(8, 32, 8, 1, 64, 16, 512, 8192, True, 0) == 0  # D = 64
+    # 64 grouped rows: four CTAs of 16 rows per KV head on the decode path; AUTO takes the prefill
+    assert sa.attn_fwd_fp8_workspace_bytes(1, 64, 1, 1, 8192, 128, True, 0, sa.PATH_DECODE) > 0
+    assert sa.attn_fwd_fp8_workspace_bytes(1, 64, 1, 1, 8192, 128, True, 0, sa.PATH_AUTO) == 0
+    assert sa.attn_decode_paged_fp8_workspace_bytes(8, 32, 8, 1, 48, 16, 512, 8192, True, 0) == 0  # D = 48
     assert sa.attn_decode_paged_fp8_workspace_bytes(8, 32, 8, 1, 128, 48, 512, 8192, True, 0) == 0  # page 48
 
 

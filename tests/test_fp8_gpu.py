@@ -100,6 +100,8 @@ def test_fp8_full_size_sampled_rows():
     ((1, 32, 8, 1, 8192, 128), True, 0, (0.5, 0.25, 2.0)),
     ((1, 4, 1, 3, 777, 128), True, 0, (1.0, 1.0, 1.0)),      # speculative rows: G * M = 12
     ((3, 16, 1, 1, 2049, 128), False, 0, (1.0, 0.5, 1.0)),   # G = 16, ragged N
+    ((2, 32, 1, 1, 1500, 128), True, 300, (1.0, 1.0, 1.0)),  # 32 grouped rows: two CTAs of 16 on the decode path
+    ((1, 8, 2, 5, 900, 128), True, 0, (0.5, 1.0, 1.0)),      # 20 grouped rows, the second CTA partly empty
 ])
 @pytest.mark.parametrize("path", [sa.PATH_AUTO, sa.PATH_DECODE, sa.PATH_PREFILL],
                          ids=["auto", "decode", "prefill"])
@@ -175,6 +177,39 @@ def test_fp8_paged_ragged_lengths(page_size):
     for b, L in enumerate(lens):
         H, sigma, wabs = bounds(qf[b:b + 1], kf[b:b + 1, :, :L], vf[b:b + 1, :, :L], True, 0, 1.0 / np.sqrt(D))
         check_fp8(o[b:b + 1], want[b:b + 1], H, sigma, wabs, torch.bfloat16, f"page {page_size} seq {b}")
+
+
+@pytest.mark.parametrize("D,G,M,page_size", [(64, 4, 1, 16), (32, 2, 2, 64), (128, 8, 4, 32), (128, 32, 1, 128)])
+def test_fp8_paged_group_shapes(D, G, M, page_size):
+    """E4M3 paged decode on the grouped CUDA-core kernel: D < 128, or more than
+    16 grouped rows per KV head at D = 128; FP16 output for one case."""
+    from oracle_pins import to_pages
+    B, Hkv, Ncap = 3, 2, 1024
+    Hq = G * Hkv
+    qd, kd, vd = 0.5, 1.0, 2.0
+    q, k, v = make_qkv_fp8(B, Hq, Hkv, M, Ncap, D, 28, qd, kd, vd)
+    rng = np.random.default_rng(6)
+    kp, table = to_pages(k.float().numpy(), page_size, rng)
+    rng = np.random.default_rng(6)
+    vp, _ = to_pages(v.float().numpy(), page_size, rng)
+    f8 = torch.float8_e4m3fn
+    kp, vp = torch.from_numpy(kp).to(f8), torch.from_numpy(vp).to(f8)  # exact: the values came from E4M3
+    table = torch.from_numpy(table.astype(np.int32))
+    lens = [1000, 2, 517]
+    out_dtype = torch.float16 if D == 32 else torch.bfloat16
+    for window in (0, 300):
+        o = torch.full(q.shape, float("nan"), dtype=out_dtype, device=DEV)
+        sa.attn_decode_paged_fp8(q.to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV),
+                                 torch.tensor(lens, dtype=torch.int32, device=DEV), o, Ncap, causal=True,
+                                 window=window, q_descale=qd, k_descale=kd, v_descale=vd)
+        torch.cuda.synchronize()
+        want = oracle.attention_paged(deq(q, qd), deq(kp, kd), deq(vp, vd), table, lens, Ncap, True, window)
+        qf, kf, vf = deq(q, qd), deq(k, kd), deq(v, vd)
+        for b, L in enumerate(lens):
+            H, sigma, wabs = bounds(qf[b:b + 1], kf[b:b + 1, :, :L], vf[b:b + 1, :, :L], True, window,
+                                    1.0 / np.sqrt(D))
+            check_fp8(o[b:b + 1], want[b:b + 1], H, sigma, wabs, out_dtype,
+                      f"D={D} G={G} M={M} window={window} seq {b}")
 
 
 def test_fp8_rising_maximum_stress():

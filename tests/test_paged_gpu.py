@@ -20,9 +20,9 @@ def no_device_timeouts():
     assert sa.last_device_status() == 0, "a kernel gave up on a bounded wait"
 
 
-def paged_case(B, Hq, Hkv, M, Ncap, page_size, dtype, seed, shuffle=True):
+def paged_case(B, Hq, Hkv, M, Ncap, page_size, dtype, seed, shuffle=True, D=128):
     """Seeded q and a contiguous cache cut into pages (shuffled in the pool)."""
-    q, k, v = make_qkv(B, Hq, Hkv, M, Ncap, 128, dtype, seed)
+    q, k, v = make_qkv(B, Hq, Hkv, M, Ncap, D, dtype, seed)
     r = np.random.default_rng(seed) if shuffle else None
     kp, table = to_pages(k.float().numpy(), page_size, r)
     r = np.random.default_rng(seed) if shuffle else None
@@ -119,5 +119,73 @@ def test_paged_decode_workload_full_size():
     want = oracle.attention_paged(q, kp, vp, table, [w.N] * w.B, w.N, w.causal, w.window)
     check(o, want, w.dtype, "paged decode workload")
     ref = sa.attention(q.to(DEV), k.to(DEV), v.to(DEV), causal=w.causal, window=w.window, path=sa.PATH_DECODE)
+    torch.cuda.synchronize()
+    assert torch.allclose(o.float(), ref.float(), atol=2e-2, rtol=0)
+
+
+# ---------------------------------------------------------------------------
+# The grouped CUDA-core kernel: head dimensions 16, 32, 64, and more than 16
+# grouped query rows per KV head at D = 128
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("D", [16, 32, 64])
+@pytest.mark.parametrize("page_size", [16, 64, 128])
+@pytest.mark.parametrize("causal,window", [(True, 0), (True, 300), (False, 0), (False, 200)])
+def test_paged_group_head_dims(D, page_size, causal, window):
+    B, Hq, Hkv, M, Ncap = 5, 8, 2, 1, 1024
+    dtype = torch.bfloat16 if page_size != 64 else torch.float16
+    q, kp, vp, table = paged_case(B, Hq, Hkv, M, Ncap, page_size, dtype, 31, D=D)
+    lens = [1000, 1, 0, 1024, 517]
+    o = run_paged(q, kp, vp, table, lens, Ncap, causal, window)
+    want = oracle.attention_paged(q, kp, vp, table, lens, Ncap, causal, window)
+    check(o, want, dtype, f"D={D} page {page_size} causal={causal} window={window}")
+    assert torch.all(o[2] == 0)  # the empty sequence
+
+
+@pytest.mark.parametrize("D,G,M", [(128, 8, 4), (128, 32, 1), (128, 4, 5), (128, 16, 9), (64, 4, 5), (64, 16, 1),
+                                   (32, 2, 11)])
+def test_paged_group_many_grouped_rows(D, G, M):
+    """More than 16 grouped rows per KV head at D = 128 (the tcgen05 kernel in
+    CTAs of 16 rows, the last one partly empty) and D < 128 (the grouped
+    CUDA-core kernel in blocks of eight rows), with sequences shorter than M
+    (rows with no visible key under causal)."""
+    B, Hkv, Ncap, ps = 3, 2, 768, 32
+    q, kp, vp, table = paged_case(B, G * Hkv, Hkv, M, Ncap, ps, torch.float16, 37, D=D)
+    lens = [768, 301, 3]
+    for causal, window in ((True, 0), (True, 129), (False, 0)):
+        o = run_paged(q, kp, vp, table, lens, Ncap, causal, window)
+        want = oracle.attention_paged(q, kp, vp, table, lens, Ncap, causal, window)
+        check(o, want, torch.float16, f"D={D} G={G} M={M} causal={causal} window={window}")
+
+
+def test_paged_group_one_split_writes_output():
+    """Enough (sequence, KV head) pairs that the grouped kernel plans one split:
+    no workspace (its size is 0), the kernel writes o itself."""
+    B, Hq, Hkv, M, Ncap, ps, D = 96, 8, 8, 1, 256, 16, 64
+    nb = sa.attn_decode_paged_workspace_bytes(B, Hq, Hkv, M, D, ps, Ncap // ps, Ncap, True, 0)
+    assert nb == 0
+    q, kp, vp, table = paged_case(B, Hq, Hkv, M, Ncap, ps, torch.bfloat16, 41, D=D)
+    lens = [int(x) for x in np.random.default_rng(41).integers(0, Ncap + 1, size=B)]
+    for workspace in (True, False):
+        o = run_paged(q, kp, vp, table, lens, Ncap, True, 0, workspace=workspace)
+        want = oracle.attention_paged(q, kp, vp, table, lens, Ncap, True, 0)
+        check(o, want, torch.bfloat16, f"one split, workspace={workspace}")
+
+
+def test_paged_group_decode_workload_d64():
+    """The GQA decode workload's shape at D = 64 (B=8, Hq=32, Hkv=8, N=8192,
+    window 4096), its cache cut into 16-key pages in shuffled order, against the
+    oracle on every row and against the contiguous decode path."""
+    B, Hq, Hkv, M, N, W, D = 8, 32, 8, 1, 8192, 4096, 64
+    q, k, v = make_qkv(B, Hq, Hkv, M, N, D, torch.bfloat16, 43)
+    r = np.random.default_rng(43)
+    kp, table = to_pages(k.float().numpy(), 16, r)
+    r = np.random.default_rng(43)
+    vp, _ = to_pages(v.float().numpy(), 16, r)
+    kp, vp = torch.from_numpy(kp).to(torch.bfloat16), torch.from_numpy(vp).to(torch.bfloat16)
+    table = torch.from_numpy(table.astype(np.int32))
+    o = run_paged(q, kp, vp, table, [N] * B, N, True, W)
+    want = oracle.attention_paged(q, kp, vp, table, [N] * B, N, True, W)
+    check(o, want, torch.bfloat16, "paged decode D=64")
+    ref = sa.attention(q.to(DEV), k.to(DEV), v.to(DEV), causal=True, window=W, path=sa.PATH_DECODE)
     torch.cuda.synchronize()
     assert torch.allclose(o.float(), ref.float(), atol=2e-2, rtol=0)

@@ -123,13 +123,16 @@ def test_fully_masked_rows_are_zero(path):
 
 
 @pytest.mark.parametrize("shape", [(2, 8, 2, 1, 1000), (1, 16, 4, 3, 2500), (3, 4, 4, 2, 700), (1, 32, 2, 1, 600),
-                                   (32, 8, 8, 1, 1000), (16, 16, 4, 2, 1500), (40, 4, 4, 1, 2100)],
+                                   (32, 8, 8, 1, 1000), (16, 16, 4, 2, 1500), (40, 4, 4, 1, 2100),
+                                   (1, 32, 1, 1, 1000), (2, 8, 2, 5, 900), (4, 64, 2, 3, 1300)],
                          ids=str)
 @pytest.mark.parametrize("mask", [(True, 0), (True, 333), (False, 0)], ids=str)
 def test_decode_split_paths(shape, mask):
-    """Few groups give many splits of one tile; many groups (the last three
-    shapes) give few splits of several tiles each, which runs the K/V ring
-    around several times."""
+    """Few groups give many splits of one tile; many groups (shapes 5-7) give
+    few splits of several tiles each, which runs the K/V ring around several
+    times; the last three have 32, 20 and 96 grouped rows per KV head, which the
+    decode path takes in CTAs of 16 rows (the last one partly empty, rows of one
+    query head split across two CTAs)."""
     B, Hq, Hkv, M, N = shape
     q, k, v = make_qkv(B, Hq, Hkv, M, N, 128, torch.bfloat16, seed=N)
     want = oracle.attention(q, k, v, causal=mask[0], window=mask[1])
