@@ -38,6 +38,8 @@ from streaming_attention_gb300.inputs import (  # noqa: E402
 
 # the D=128 prefill shape in FP16 (same seed and sizes)
 FP16_D128 = PREFILL_D128.with_(dtype=torch.float16, name="prefill_b2_h32_4096x4096_d128_fp16_causal")
+# the GQA decode shape at head dimension 64 (same seed)
+DECODE_D64 = DECODE_GQA.with_(D=64, name="decode_gqa_b8_hq32_hkv8_m1_n8192_w4096_d64_bf16")
 
 METRIC = "attention fwd TFLOP/s (decode: GB/s) and % of GB300 roofline, 1 GPU"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -296,11 +298,13 @@ def l2_flusher(dev):
 
 
 def decode_splits(w, sms):
-    """The library's split plan for the decode path: as many splits per KV group
-    as fill two CTAs per SM, at most one per 128-key tile of the visible range."""
+    """The library's split plan for the decode path: as many splits per (KV group,
+    block of 16 grouped rows) as fill two CTAs per SM, at most one per 128-key
+    tile of the visible range."""
     lo = max(0, (w.N - w.M) - w.window + 1) if w.window > 0 else 0
     tiles = max(1, -(-(w.N - (lo // 128) * 128) // 128))
-    s = max(1, min(2 * sms // (w.B * w.Hkv), tiles, 4096))
+    groups = w.B * w.Hkv * -(-(w.Hq // w.Hkv) * w.M // 16)
+    s = max(1, min(2 * sms // groups, tiles, 4096))
     per = -(-tiles // s)
     return -(-tiles // per)
 
@@ -479,7 +483,8 @@ def extra_measurements(args, dev, stream, flush):
                             # the pair-MMA prefill (explicit path; AUTO runs the one-CTA kernel)
                             ("prefill_d128_bf16_causal_pair", PREFILL_D128, True),
                             ("prefill_d128_bf16_noncausal_pair", PREFILL_D128, False),
-                            ("decode_gqa", DECODE_GQA, DECODE_GQA.causal)):
+                            ("decode_gqa", DECODE_GQA, DECODE_GQA.causal),
+                            ("decode_gqa_d64", DECODE_D64, DECODE_GQA.causal)):
         if name.startswith(("prefill", "long")) and args.workload != PREFILL_D128.name:
             continue
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -496,8 +501,11 @@ def extra_measurements(args, dev, stream, flush):
         ms = time_steady(fn_on, sets, steps, 3, stream)
         cold = statistics.median(time_graph(lambda st: fn_on(sets[0], st), steps, 3, flush))
         if pname == "decode":
-            out[name] = {"GB/s": round(decode_bytes(w) / (ms * 1e-3) / 1e9, 1), "us": round(ms * 1e3, 2),
-                         "cold_call_us": round(cold * 1e3, 2), "path": pname}
+            gbs = decode_bytes(w) / (ms * 1e-3) / 1e9
+            out[name] = {"GB/s": round(gbs, 1), "us": round(ms * 1e3, 2), "cold_call_us": round(cold * 1e3, 2),
+                         "frac_of_hbm": round(gbs / peaks()[0]["hbm_gbs"], 4), "path": pname,
+                         "shape": {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "M": w.M, "N": w.N, "window": w.window,
+                                   "D": w.D}}
         else:
             out[name] = {"TFLOP/s": round(flops(w, causal) / (ms * 1e-3) / 1e12, 2), "us": round(ms * 1e3, 1),
                          "cold_call_us": round(cold * 1e3, 1), "path": pname}
@@ -519,11 +527,10 @@ def extra_measurements(args, dev, stream, flush):
     if args.workload in (PREFILL_D128.name, DECODE_GQA.name):
         for ps in (16, 128):
             out[f"decode_gqa_paged{ps}"] = paged_decode_measure(DECODE_GQA, ps, steps, dev, stream, flush)
-        # shapes of the grouped CUDA-core paged kernel: D = 64, and 8 speculative
-        # rows per sequence (32 grouped rows per KV head) at D = 128
+        # D = 64 (upper half of each tile read as zeros), and 8 speculative rows
+        # per sequence (32 grouped rows per KV head: two CTAs of 16) at D = 128
         import dataclasses
-        d64 = dataclasses.replace(DECODE_GQA, name="decode_gqa_b8_hq32_hkv8_m1_n8192_w4096_d64_bf16", D=64)
-        out["decode_gqa_d64_paged16"] = paged_decode_measure(d64, 16, steps, dev, stream, flush)
+        out["decode_gqa_d64_paged16"] = paged_decode_measure(DECODE_D64, 16, steps, dev, stream, flush)
         m8 = dataclasses.replace(DECODE_GQA, name="decode_gqa_b8_hq32_hkv8_m8_n8192_w4096_d128_bf16", M=8)
         out["decode_gqa_m8_paged16"] = paged_decode_measure(m8, 16, steps, dev, stream, flush)
     return out

@@ -89,15 +89,15 @@ typedef enum {
 /* Kernel paths. AUTO picks: split-KV decode when (Hq/Hkv)*M <= 16 and the
  * visible key range is long; the tcgen05 prefill kernel for D in {64, 128};
  * the SIMT kernel otherwise (D in {16, 32, 64, 128}).
- * The SIMT kernel, which also runs split decode for D = 64 and for
- * B*Hkv > 65535, and the log-sum-exp of an N == 0 call,
+ * The SIMT kernel, which also runs split decode for B*Hkv > 65535 and the
+ * log-sum-exp of an N == 0 call,
  * takes at most 65535 (batch, query head) pairs: B*Hq > 65535 there returns
  * ATTN_ERR_PATH (AUTO then prefers the prefill kernel for D in {64, 128}). */
 typedef enum {
     ATTN_PATH_AUTO = 0,
     ATTN_PATH_SIMT = 1,    /* CUDA-core streaming kernel, any supported D, B*Hq <= 65535 */
     ATTN_PATH_PREFILL = 2, /* warp-specialized TMA + tcgen05 + TMEM kernel, D in {64,128} */
-    ATTN_PATH_DECODE = 3,  /* split-KV over grouped query heads (D = 128 on tcgen05: the grouped
+    ATTN_PATH_DECODE = 3,  /* split-KV over grouped query heads (tcgen05, D = 64 or 128: the grouped
                               rows of a KV head in CTAs of 16); the splits merged in a thread-block
                               cluster (at most 8 splits per KV head) or by the merge kernel */
     ATTN_PATH_PREFILL_PAIR = 4 /* the prefill on the pair MMA (tcgen05 cta_group::2): clusters of two
@@ -290,8 +290,8 @@ ATTN_API int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, vo
  *   Returns ATTN_ERR_WORKSPACE when the problem's split summaries
  *   (attn_workspace_bytes_ex(..., ATTN_PATH_DECODE)) exceed the array and the
  *   splits do not merge inside their cluster (see below), and
- *   ATTN_ERR_PATH when the splits would run on the SIMT kernel (D = 64) with
- *   B*Hq > 65535.
+ *   ATTN_ERR_PATH when B*Hkv > 65535 and B*Hq > 65535 (the splits would run
+ *   on the SIMT kernel, whose grid takes at most 65535 (batch, query head) pairs).
  *   The first call on a device looks up the array's device address (with
  *   that device current); make that first call before any stream capture.
  *   Every call, on any stream, shares the one array and leaves its contents
@@ -300,7 +300,7 @@ ATTN_API int attn_fwd_host(const void* q_h, const void* k_h, const void* v_h, vo
  *   needs clearing: each call writes every summary it reads, including an
  *   empty one for a split that sees no key or gives up on a bounded wait (the
  *   output is then unspecified and attn_last_device_status reports it). When
- *   a KV head has at most 8 splits -- D = 128 and enough KV heads, as in
+ *   a KV head has at most 8 splits -- enough KV heads, as in
  *   typical GQA decode -- the splits merge inside their thread-block cluster,
  *   the array is not touched at all, and its size does not limit the problem. */
 #define ATTN_NOALLOC_SCRATCH_BYTES (8u << 20)
@@ -334,13 +334,13 @@ ATTN_API int attn_fwd_decode_noalloc(const void* q, const void* k, const void* v
  *   max_seq_len a host-side bound of the seq_lens values: it sizes the split
  *               plan; keys past it are ignored.
  *   D is 16, 32, 64 or 128 (else ATTN_ERR_HEADDIM); B * Hkv <= 65535 and at
- *   most 16 * 65535 (D = 128) or 8 * 65535 (else) grouped rows (Hq/Hkv) * M
- *   per KV head (else ATTN_ERR_OVERFLOW).
- *   Kernels: D = 128 runs the tcgen05 split kernel (pages gathered by TMA, the
- *   grouped rows of a KV head in CTAs of 16); D in {16, 32, 64} runs a grouped
- *   CUDA-core kernel (one block per split, sequence, KV head and eight grouped
- *   rows, each 32-key tile gathered from its pages once for all of them). Both
- *   end in the same common-maximum merge.
+ *   most 16 * 65535 (D = 64 and 128) or 8 * 65535 (D = 16 and 32) grouped
+ *   rows (Hq/Hkv) * M per KV head (else ATTN_ERR_OVERFLOW).
+ *   Kernels: D = 64 and 128 run the tcgen05 split kernel (pages gathered by
+ *   TMA, the grouped rows of a KV head in CTAs of 16); D = 16 and 32 run a
+ *   grouped CUDA-core kernel (one block per split, sequence, KV head and eight
+ *   grouped rows, each 32-key tile gathered from its pages once for all of
+ *   them). Both end in the same common-maximum merge.
  *   Every element of a page that a sequence uses must be finite, also in the
  *   rows of its last page past L_b: masked keys get probability 0, and their
  *   value rows are still multiplied by it.
@@ -366,7 +366,8 @@ ATTN_API int attn_decode_paged(const void* q, const void* k_pages, const void* v
  * operation is attn_decode_paged of the dequantized tensors, written as
  * out_dtype (ATTN_BF16 / ATTN_FP16). The probabilities are rounded to E4M3
  * for the value product as in attn_fwd_fp8. Arguments and limits as
- * attn_decode_paged; the workspace is attn_decode_paged_fp8_workspace_bytes(...)
+ * attn_decode_paged, except that D = 64 runs the grouped CUDA-core kernel (so
+ * at most 8 * 65535 grouped rows); the workspace is attn_decode_paged_fp8_workspace_bytes(...)
  * bytes (or NULL to have it allocated stream-ordered). */
 ATTN_API size_t attn_decode_paged_fp8_workspace_bytes(int B, int Hq, int Hkv, int M, int D,
                                                       int page_size, int max_pages,

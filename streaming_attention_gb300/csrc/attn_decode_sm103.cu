@@ -1,4 +1,5 @@
-// Split-KV decode on the tcgen05 tensor cores (sm_103a), D = 128.
+// Split-KV decode on the tcgen05 tensor cores (sm_103a), D = 128 (and D = 64 for
+// 16-bit inputs, read as D = 128 with the upper 64 columns zero).
 //
 // Decode has few query rows per KV head: the R = (Hq/Hkv) * M rows that share
 // one KV head (GQA grouping) are processed together, padded to 16; more than 16
@@ -81,6 +82,7 @@ struct DecodeParams {
     int* status;
     int Hq, Hkv, M, N, G;
     int R;  // grouped query rows per KV head (G * M); CTA z takes rows [16 z, 16 z + 16) of them
+    int D;  // head dimension of the tensors: 128, or 64 (16-bit), whose upper 64 columns read as zeros
     int causal, window;
     float scale_log2;
     int klo, khi, kbase, chunk, S;
@@ -274,6 +276,7 @@ __global__ void __launch_bounds__(kDecThreads)
     const int split = blockIdx.x;
     const int grp = blockIdx.y;  // b * Hkv + g
     const int b = grp / p.Hkv, g = grp % p.Hkv;
+    const int Dh = EB == 1 ? DD : p.D;  // head dimension of the tensors (8-bit inputs: 128)
     const int rblk = blockIdx.z;  // block of 16 of the group's grouped rows
     const int R = min(DNR, p.R - rblk * DNR);  // rows of this CTA
     const int row_base = (b * p.Hq + g * p.G) * p.M + rblk * DNR;  // first global row of this CTA
@@ -766,7 +769,7 @@ __global__ void __launch_bounds__(kDecThreads)
                         continue;
                     }
                     const size_t slot = (size_t)(row_base + r) * p.S + split;
-                    p.ws_acc[slot * DD + kl] = __uint_as_float(o[r]);
+                    if (kl < Dh) p.ws_acc[slot * Dh + kl] = __uint_as_float(o[r]);
                     if (kl == 0) {
                         p.ws_m[slot] = m_ref[r];
                         p.ws_l[slot] = lsum;
@@ -787,7 +790,7 @@ __global__ void __launch_bounds__(kDecThreads)
             // summary, so the merge never reads a slot this call did not write
             for (int r = 0; r < R; ++r) {
                 const size_t slot = (size_t)(row_base + r) * p.S + split;
-                p.ws_acc[slot * DD + kl] = 0.f;
+                if (kl < Dh) p.ws_acc[slot * Dh + kl] = 0.f;
                 if (kl == 0) {
                     p.ws_m[slot] = -INFINITY;
                     p.ws_l[slot] = 0.f;
@@ -832,11 +835,13 @@ __global__ void __launch_bounds__(kDecThreads)
                     x = fmaf(w, as[sp], x);
                 }
                 x *= L > 0.f ? p.out_scale / L : 0.f;
-                const size_t out = (size_t)(row_base + r) * DD + kl;
-                if (p.out_dtype == ATTN_BF16)
+                const size_t out = (size_t)(row_base + r) * Dh + kl;
+                if (kl >= Dh) {
+                } else if (p.out_dtype == ATTN_BF16) {
                     reinterpret_cast<uint16_t*>(p.o)[out] = (uint16_t)(pack_bf16(x, 0.f) & 0xFFFFu);
-                else
+                } else {
                     reinterpret_cast<uint16_t*>(p.o)[out] = (uint16_t)(pack_f16(x, 0.f) & 0xFFFFu);
+                }
                 if (kl == 0 && p.lse) p.lse[row_base + r] = L > 0.f ? (mx + log2f(L)) * kLn2 : -INFINITY;
             }
         }
@@ -868,14 +873,19 @@ cudaError_t launch_decode_t(const Problem& pr, const void* q, const void* k, con
     });
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap tq, tk, tv;
-    if (!make_tensor_map(&tq, q, DD, pr.B * pr.Hq * pr.M, 1, DNR, kBF16, EB)) return cudaErrorInvalidValue;
+    // D = 64 (16-bit): the maps' rows are 64 elements, so the second 64-column box of
+    // every Q, K and V tile lies past the row and reads as zeros; the products then
+    // run as for D = 128 (the zero half adds nothing to the scores, and the upper
+    // 64 rows of O^T stay zero and are never written out).
+    if (EB == 1 && pr.D != DD) return cudaErrorInvalidValue;
+    if (!make_tensor_map(&tq, q, pr.D, pr.B * pr.Hq * pr.M, 1, DNR, kBF16, EB)) return cudaErrorInvalidValue;
     if (kPaged) {
         const int box = kv->page_size < DBN ? kv->page_size : DBN;
-        if (!make_tensor_map(&tk, kv->k_pages, DD, kv->page_size, kv->num_pages * pr.Hkv, box, kBF16, EB) ||
-            !make_tensor_map(&tv, kv->v_pages, DD, kv->page_size, kv->num_pages * pr.Hkv, box, kBF16, EB))
+        if (!make_tensor_map(&tk, kv->k_pages, pr.D, kv->page_size, kv->num_pages * pr.Hkv, box, kBF16, EB) ||
+            !make_tensor_map(&tv, kv->v_pages, pr.D, kv->page_size, kv->num_pages * pr.Hkv, box, kBF16, EB))
             return cudaErrorInvalidValue;
-    } else if (!make_tensor_map(&tk, k, DD, pr.N, pr.B * pr.Hkv, DBN, kBF16, EB) ||
-               !make_tensor_map(&tv, v, DD, pr.N, pr.B * pr.Hkv, DBN, kBF16, EB)) {
+    } else if (!make_tensor_map(&tk, k, pr.D, pr.N, pr.B * pr.Hkv, DBN, kBF16, EB) ||
+               !make_tensor_map(&tv, v, pr.D, pr.N, pr.B * pr.Hkv, DBN, kBF16, EB)) {
         return cudaErrorInvalidValue;
     }
     DecodeParams dp = {};
@@ -889,6 +899,7 @@ cudaError_t launch_decode_t(const Problem& pr, const void* q, const void* k, con
     dp.N = pr.N;
     dp.G = pr.G;
     dp.R = pr.G * pr.M;
+    dp.D = pr.D;
     dp.causal = pr.causal;
     dp.window = pr.window;
     dp.scale_log2 = pr.scale_log2;
@@ -971,9 +982,10 @@ void plan_splits(int tiles, int groups, int* chunk, int* S, int per_sm) {
 
 }  // namespace
 
-// Any number of grouped rows: CTAs of 16 rows each along the grid's z (at most 65535).
+// D = 128, or 64 with 16-bit inputs (the 8-bit entry points take D = 128 only);
+// any number of grouped rows: CTAs of 16 rows each along the grid's z (at most 65535).
 bool decode_tc_supported(const Problem& p) {
-    return p.D == DD && p.B * p.Hkv <= 65535 && ((long long)p.G * p.M + DNR - 1) / DNR <= 65535;
+    return (p.D == DD || p.D == 64) && p.B * p.Hkv <= 65535 && ((long long)p.G * p.M + DNR - 1) / DNR <= 65535;
 }
 
 // (KV group, block of 16 grouped rows) pairs: the CTAs of one split

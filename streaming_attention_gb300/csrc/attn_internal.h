@@ -105,7 +105,7 @@ cudaError_t launch_decode(const Problem& p, const void* q, const void* k, const 
                           cudaStream_t stream, DecodeOut* out = nullptr);
 bool decode_supported(const Problem& p);
 int decode_plan(const Problem& p, int* chunk, int* S);
-// tcgen05 split kernel (D = 128; grouped rows per KV head in CTAs of 16)
+// tcgen05 split kernel (D = 128, or 64 for 16-bit inputs; grouped rows per KV head in CTAs of 16)
 bool decode_tc_supported(const Problem& p);
 // e4m3: the plan of the 8-bit kernel (more CTAs per SM, so more splits)
 int decode_plan_tc(const Problem& p, int* chunk, int* S, bool e4m3 = false);
@@ -128,9 +128,10 @@ int decode_plan_paged(const Problem& p, const PagedKV& kv, int* chunk, int* S, b
 cudaError_t launch_decode_paged(const Problem& p, const void* q, const PagedKV& kv, int chunk, int S,
                                 const SplitWorkspace& ws, int* status, cudaStream_t stream, DecodeOut* out = nullptr,
                                 bool e4m3 = false);
-// Which kernel takes a paged call: the tcgen05 split kernel (D = 128), else the
-// grouped CUDA-core kernel (D in {16, 32, 64}; grouped rows up to 8 * 65535).
-bool paged_tc_supported(const Problem& p);
+// Which kernel takes a paged call: the tcgen05 split kernel (D = 128; D = 64 for
+// 16-bit caches), else the grouped CUDA-core kernel (D in {16, 32, 64}; grouped
+// rows up to 8 * 65535).
+bool paged_tc_supported(const Problem& p, bool e4m3);
 bool paged_group_supported(const Problem& p);
 int paged_group_plan(const Problem& p, const PagedKV& kv, int* chunk, int* S);
 // ws may be null when S == 1 (the kernel then writes o, times out_scale);

@@ -1,7 +1,7 @@
 // C ABI of split-KV decode over a paged KV cache (16-bit or E4M3): metadata
 // validation, the split plan, and the kernels: the tcgen05 split kernel in
-// paged mode (D = 128, at most 16 grouped query rows per KV head) or the
-// grouped CUDA-core kernel (every other shape), then the merge kernel.
+// paged mode (D = 128; D = 64 for 16-bit caches) or the grouped CUDA-core
+// kernel (every other head dimension), then the merge kernel.
 // Attention over a KV-cache slice is the decode step the course's plan names
 // next ("Kernel Notes & Checklist", section 3, the plan, week +3: sliding
 // window + GQA + KV-cache slice); pages of the cache are gathered by the TMA
@@ -31,7 +31,8 @@ struct PagedCall {
 // element counts, null pointers of non-empty tensors, alignment.
 int validate_paged(const void* q, const void* kp, const void* vp, const int* table, const int* lens, const void* o,
                    int B, int Hq, int Hkv, int M, int D, int num_pages, int page_size, int max_pages,
-                   int max_seq_len, int causal, int window, float scale, int dtype, PagedCall* c) {
+                   int max_seq_len, int causal, int window, float scale, int dtype, PagedCall* c,
+                   bool e4m3 = false) {
     if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_DTYPE;
     if (B < 0 || Hq < 0 || Hkv < 0 || M < 0 || D <= 0 || num_pages < 0 || max_pages < 0 || max_seq_len < 0)
         return ATTN_ERR_SHAPE;
@@ -68,7 +69,7 @@ int validate_paged(const void* q, const void* kp, const void* vp, const int* tab
     p.khi = max_len;
     p.lse = nullptr;
     c->kv = PagedKV{kp, vp, table, lens, num_pages, page_size, max_pages, max_len};
-    if (!paged_tc_supported(p) && !paged_group_supported(p)) return ATTN_ERR_OVERFLOW;
+    if (!paged_tc_supported(p, e4m3) && !paged_group_supported(p)) return ATTN_ERR_OVERFLOW;
     return ATTN_OK;
 }
 
@@ -76,7 +77,7 @@ bool nothing_to_attend(const PagedCall& c) { return c.kv.max_len == 0 || c.kv.nu
 
 // The split plan of the kernel that runs this call.
 void paged_plan(const PagedCall& c, bool e4m3, int* chunk, int* S) {
-    if (paged_tc_supported(c.p))
+    if (paged_tc_supported(c.p, e4m3))
         decode_plan_paged(c.p, c.kv, chunk, S, e4m3);
     else
         paged_group_plan(c.p, c.kv, chunk, S);
@@ -87,7 +88,7 @@ void paged_plan(const PagedCall& c, bool e4m3, int* chunk, int* S) {
 size_t paged_workspace(const PagedCall& c, bool e4m3 = false) {
     int chunk = 0, S = 0;
     paged_plan(c, e4m3, &chunk, &S);
-    if (!paged_tc_supported(c.p) && S == 1) return 0;
+    if (!paged_tc_supported(c.p, e4m3) && S == 1) return 0;
     return split_workspace_bytes(c.p.B * c.p.Hq * c.p.M, S, c.p.D);
 }
 
@@ -99,7 +100,7 @@ int run_paged(const PagedCall& c, const void* q, void* o, void* ws, size_t ws_by
     int chunk = 0, S = 0;
     paged_plan(c, e4m3, &chunk, &S);
     const int rows = p.B * p.Hq * p.M;
-    if (!paged_tc_supported(p)) {
+    if (!paged_tc_supported(p, e4m3)) {
         if (S == 1) return cuda_status(launch_paged_group(p, q, c.kv, chunk, S, nullptr, o, v_descale, e4m3, stream));
         if (!ws || ws_bytes < split_workspace_bytes(rows, S, p.D)) return ATTN_ERR_WORKSPACE;
         if (!aligned(ws, 16)) return ATTN_ERR_ALIGN;
@@ -169,7 +170,7 @@ size_t attn_decode_paged_fp8_workspace_bytes(int B, int Hq, int Hkv, int M, int 
     const int* idummy = reinterpret_cast<const int*>(dummy);
     PagedCall c;
     if (validate_paged(dummy, dummy, dummy, idummy, idummy, dummy, B, Hq, Hkv, M, D, 1, page_size, max_pages,
-                       max_seq_len, causal, window, 0.f, ATTN_BF16, &c) != ATTN_OK)
+                       max_seq_len, causal, window, 0.f, ATTN_BF16, &c, true) != ATTN_OK)
         return 0;
     if ((int64_t)B * Hq * M == 0 || nothing_to_attend(c)) return 0;
     return paged_workspace(c, true);
@@ -182,7 +183,7 @@ int attn_decode_paged_fp8(const void* q, const void* k_pages, const void* v_page
                           size_t ws_bytes, void* stream) {
     PagedCall c;
     int rc = validate_paged(q, k_pages, v_pages, block_table, seq_lens, o, B, Hq, Hkv, M, D, num_pages, page_size,
-                            max_pages, max_seq_len, causal, window, scale, out_dtype, &c);
+                            max_pages, max_seq_len, causal, window, scale, out_dtype, &c, true);
     if (rc != ATTN_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if ((int64_t)B * Hq * M == 0) return ATTN_OK;

@@ -1,5 +1,6 @@
 // Grouped CUDA-core decode over a paged KV cache: the head dimensions the
-// tcgen05 split kernel does not take (16, 32 and 64), for 16-bit and E4M3 caches.
+// tcgen05 split kernel does not take (16 and 32; 64 for E4M3 caches), for
+// 16-bit and E4M3 caches.
 //
 // One block owns one split of one sequence's key range for one KV head and up
 // to eight of that head's grouped query rows (one warp per row: query head
@@ -272,7 +273,7 @@ cudaError_t launch_group_d(const GroupArgs& a, int D, dim3 grid, cudaStream_t st
 
 }  // namespace
 
-bool paged_tc_supported(const Problem& p) { return decode_tc_supported(p); }
+bool paged_tc_supported(const Problem& p, bool e4m3) { return decode_tc_supported(p) && (!e4m3 || p.D == 128); }
 
 bool paged_group_supported(const Problem& p) {
     return (p.D == 16 || p.D == 32 || p.D == 64 || p.D == 128) &&

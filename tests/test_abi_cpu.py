@@ -94,11 +94,14 @@ def test_simt_grid_limit(L):
         assert fwd(L, B_=1, Hq=65536, Hkv=65536, M=1, N=8, D=D) == -11, D
     args = (A16, A16, A16, A16, 1, 65536, 65536, 1, 256, 64, 0, 0, 0.0, 0)
     assert L.attn_fwd_ex(*args, sa.PATH_SIMT, None, 0, None) == -11
-    assert L.attn_fwd_ex(*args, sa.PATH_DECODE, None, 0, None) == -11  # D = 64 splits run on it too
+    # B*Hkv > 65535 is past the tcgen05 decode's grid too, so its D = 64 splits run on the CUDA-core kernel
+    assert L.attn_fwd_ex(*args, sa.PATH_DECODE, None, 0, None) == -11
     assert L.attn_fwd_decode_noalloc(*args, None) == -11
-    # AUTO leaves decode to the prefill kernel when the split kernel would not fit
+    # the tcgen05 decode (D = 64 and 128) only needs B*Hkv <= 65535: B*Hq may exceed it
     assert sa.attn_workspace_bytes_ex(1, 4096, 4096, 1, 512, 64, 0, 0, sa.PATH_AUTO) > 0
-    assert sa.attn_workspace_bytes_ex(1, 65536, 4096, 1, 512, 64, 0, 0, sa.PATH_AUTO) == 0
+    assert sa.attn_workspace_bytes_ex(1, 65536, 4096, 1, 512, 64, 0, 0, sa.PATH_AUTO) > 0
+    # AUTO leaves decode to the prefill kernel when no split kernel fits (D = 64, B*Hkv > 65535)
+    assert sa.attn_workspace_bytes_ex(1, 65536, 65536, 1, 512, 64, 0, 0, sa.PATH_AUTO) == 0
 
 
 def test_workspace_bytes(L):
@@ -170,8 +173,8 @@ def paged(L, q=A16, kp=A16, vp=A16, table=A16, lens=A16, o=A16, B_=2, Hq=8, Hkv=
     (dict(Hq=6, Hkv=4), -5),
     (dict(D=48), -4),
     (dict(D=256), -4),
-    (dict(Hq=2, Hkv=2, M=1100000), -6),        # D = 128: more than 16 x 65535 grouped rows
-    (dict(Hq=2, Hkv=2, M=600000, D=64), -6),   # D = 64: more than 8 x 65535 grouped rows
+    (dict(Hq=2, Hkv=2, M=1100000), -6),        # D = 128 (and 64): more than 16 x 65535 grouped rows
+    (dict(Hq=2, Hkv=2, M=600000, D=32), -6),   # D = 32: more than 8 x 65535 grouped rows
     (dict(num_pages=1 << 20, page_size=128), -6),
     (dict(B_=70000, Hkv=1, Hq=1), -6),
     (dict(q=None), -1),

@@ -124,8 +124,9 @@ def test_paged_decode_workload_full_size():
 
 
 # ---------------------------------------------------------------------------
-# The grouped CUDA-core kernel: head dimensions 16, 32, 64, and more than 16
-# grouped query rows per KV head at D = 128
+# Head dimensions 16 and 32 (the grouped CUDA-core kernel) and 64 (the tcgen05
+# kernel, the upper 64 columns of each tile read as zeros); more than 16
+# grouped query rows per KV head
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("D", [16, 32, 64])
 @pytest.mark.parametrize("page_size", [16, 64, 128])
@@ -144,10 +145,10 @@ def test_paged_group_head_dims(D, page_size, causal, window):
 @pytest.mark.parametrize("D,G,M", [(128, 8, 4), (128, 32, 1), (128, 4, 5), (128, 16, 9), (64, 4, 5), (64, 16, 1),
                                    (32, 2, 11)])
 def test_paged_group_many_grouped_rows(D, G, M):
-    """More than 16 grouped rows per KV head at D = 128 (the tcgen05 kernel in
-    CTAs of 16 rows, the last one partly empty) and D < 128 (the grouped
-    CUDA-core kernel in blocks of eight rows), with sequences shorter than M
-    (rows with no visible key under causal)."""
+    """More than 16 grouped rows per KV head at D = 128 and 64 (the tcgen05
+    kernel in CTAs of 16 rows, the last one partly empty) and D = 32 (the
+    grouped CUDA-core kernel in blocks of eight rows), with sequences shorter
+    than M (rows with no visible key under causal)."""
     B, Hkv, Ncap, ps = 3, 2, 768, 32
     q, kp, vp, table = paged_case(B, G * Hkv, Hkv, M, Ncap, ps, torch.float16, 37, D=D)
     lens = [768, 301, 3]
@@ -158,9 +159,9 @@ def test_paged_group_many_grouped_rows(D, G, M):
 
 
 def test_paged_group_one_split_writes_output():
-    """Enough (sequence, KV head) pairs that the grouped kernel plans one split:
-    no workspace (its size is 0), the kernel writes o itself."""
-    B, Hq, Hkv, M, Ncap, ps, D = 96, 8, 8, 1, 256, 16, 64
+    """Enough (sequence, KV head) pairs that the grouped CUDA-core kernel (D = 32)
+    plans one split: no workspace (its size is 0), the kernel writes o itself."""
+    B, Hq, Hkv, M, Ncap, ps, D = 96, 8, 8, 1, 256, 16, 32
     nb = sa.attn_decode_paged_workspace_bytes(B, Hq, Hkv, M, D, ps, Ncap // ps, Ncap, True, 0)
     assert nb == 0
     q, kp, vp, table = paged_case(B, Hq, Hkv, M, Ncap, ps, torch.bfloat16, 41, D=D)
@@ -171,7 +172,7 @@ def test_paged_group_one_split_writes_output():
         check(o, want, torch.bfloat16, f"one split, workspace={workspace}")
 
 
-def test_paged_group_decode_workload_d64():
+def test_paged_decode_workload_d64():
     """The GQA decode workload's shape at D = 64 (B=8, Hq=32, Hkv=8, N=8192,
     window 4096), its cache cut into 16-key pages in shuffled order, against the
     oracle on every row and against the contiguous decode path."""

@@ -127,17 +127,19 @@ def test_fully_masked_rows_are_zero(path):
                                    (1, 32, 1, 1, 1000), (2, 8, 2, 5, 900), (4, 64, 2, 3, 1300)],
                          ids=str)
 @pytest.mark.parametrize("mask", [(True, 0), (True, 333), (False, 0)], ids=str)
-def test_decode_split_paths(shape, mask):
-    """Few groups give many splits of one tile; many groups (shapes 5-7) give
+@pytest.mark.parametrize("D", [64, 128])
+def test_decode_split_paths(shape, mask, D):
+    """D = 64 runs the same tcgen05 kernel with the upper 64 columns of every
+    tile read as zeros. Few groups give many splits of one tile; many groups (shapes 5-7) give
     few splits of several tiles each, which runs the K/V ring around several
     times; the last three have 32, 20 and 96 grouped rows per KV head, which the
     decode path takes in CTAs of 16 rows (the last one partly empty, rows of one
     query head split across two CTAs)."""
     B, Hq, Hkv, M, N = shape
-    q, k, v = make_qkv(B, Hq, Hkv, M, N, 128, torch.bfloat16, seed=N)
+    q, k, v = make_qkv(B, Hq, Hkv, M, N, D, torch.bfloat16, seed=N)
     want = oracle.attention(q, k, v, causal=mask[0], window=mask[1])
     for path in (sa.PATH_DECODE, sa.PATH_AUTO, sa.PATH_SIMT):
-        check(run(q, k, v, mask[0], mask[1], path), want, torch.bfloat16, f"{shape} {mask} path={path}")
+        check(run(q, k, v, mask[0], mask[1], path), want, torch.bfloat16, f"{shape} {mask} D={D} path={path}")
 
 
 def whole_heads(B, H, M):
