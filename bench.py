@@ -514,6 +514,10 @@ def extra_measurements(args, dev, stream, flush):
         for causal in (True, False):
             name = "prefill_d128_e4m3_" + ("causal" if causal else "noncausal")
             out[name] = fp8_measure(PREFILL_D128, causal, steps, dev, stream, flush)
+        # D = 64 in E4M3: the 128-column kernel with the upper half of every tile zero
+        for causal in (False, True):
+            name = "prefill_d64_e4m3_" + ("causal" if causal else "noncausal")
+            out[name] = fp8_measure(PREFILL_D64, causal, steps, dev, stream, flush)
     if args.workload == PREFILL_D128.name:
         out["prefill_d128_bf16_causal_backward"] = backward_measure(PREFILL_D128, True, steps, dev, stream)
         out["prefill_d128_bf16_noncausal_backward"] = backward_measure(PREFILL_D128, False, steps, dev, stream)
@@ -566,7 +570,8 @@ def fp8_measure(w, causal, steps, dev, stream, flush):
             "fp8_peak_tflops": round(fp8_peak, 1) if fp8_peak else None,
             "peak_source": f"derived: 2 x {pk_src} bf16 (nominal 8-bit / 16-bit dense ratio)",
             "frac_of_bf16_peak": round(tf / pk["bf16_tflops"], 4) if pk.get("bf16_tflops") else None,
-            "path": "prefill tcgen05 kind::f8f6f4 (E4M3 Q, K, V and P)"}
+            "path": "prefill tcgen05 kind::f8f6f4 (E4M3 Q, K, V and P)"
+            + (", D = 64 read as 128 with the upper half zero" if w.D == 64 else "")}
 
 
 def fp8_decode_measure(w, page_size, steps, dev, stream, flush):

@@ -195,12 +195,13 @@ ATTN_API int attn_fwd_lse(const void* q, const void* k, const void* v, void* o, 
  *   q: device bytes [B, Hq, M, D]; k, v: device bytes [B, Hkv, N, D]; o: device
  *   [B, Hq, M, D] of out_dtype (ATTN_BF16 / ATTN_FP16, else ATTN_ERR_DTYPE); all
  *   16-byte aligned. lse: as attn_fwd_lse (of the dequantized logits), or NULL.
- *   D must be 128 (ATTN_ERR_HEADDIM). Descale factors must be finite (not
- *   checked).
- *   path: ATTN_PATH_AUTO (split-KV decode when (Hq/Hkv) * M <= 16 and the
- *   visible key range spans at least 512 keys, else prefill), ATTN_PATH_PREFILL,
- *   or ATTN_PATH_DECODE (any number of grouped rows, in CTAs of 16); ATTN_PATH_SIMT
- *   is not offered (ATTN_ERR_PATH).
+ *   D is 128 or 64 (else ATTN_ERR_HEADDIM); D = 64 runs the prefill kernel's
+ *   128-column form with the upper 64 columns of every tile read as zeros.
+ *   Descale factors must be finite (not checked).
+ *   path: ATTN_PATH_AUTO (split-KV decode when D = 128, (Hq/Hkv) * M <= 16 and
+ *   the visible key range spans at least 512 keys, else prefill),
+ *   ATTN_PATH_PREFILL, or ATTN_PATH_DECODE (D = 128 only, any number of grouped
+ *   rows, in CTAs of 16); ATTN_PATH_SIMT is not offered (ATTN_ERR_PATH).
  *   workspace: for the decode path, attn_fwd_fp8_workspace_bytes(...) bytes of
  *   the same problem and path (the 8-bit kernel runs more splits than the
  *   16-bit one), 16-byte aligned, or NULL to have it allocated stream-ordered;

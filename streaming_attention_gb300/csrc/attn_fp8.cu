@@ -26,7 +26,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // rule of the 16-bit forward), else the prefill kernel
 int choose_fp8_path(const Problem& p, int path) {
     if (path != ATTN_PATH_AUTO) return path;
-    if (decode_tc_supported(p) && (int64_t)p.G * p.M <= 16 && (p.khi - p.klo) >= 512) return ATTN_PATH_DECODE;
+    if (p.D == 128 && decode_tc_supported(p) && (int64_t)p.G * p.M <= 16 && (p.khi - p.klo) >= 512)
+        return ATTN_PATH_DECODE;
     return ATTN_PATH_PREFILL;
 }
 
@@ -58,7 +59,7 @@ extern "C" size_t attn_fwd_fp8_workspace_bytes(int B, int Hq, int Hkv, int M, in
     if (validate_problem(dummy, dummy, dummy, dummy, B, Hq, Hkv, M, N, D, causal, window, 0.f, ATTN_BF16, &p) !=
             ATTN_OK ||
         D != 128)
-        return 0;
+        return 0;  // D = 64 runs the prefill kernel, which needs no workspace
     if ((int64_t)B * Hq * M == 0 || N == 0) return 0;
     if (choose_fp8_path(p, path) != ATTN_PATH_DECODE || !decode_tc_supported(p)) return 0;
     int chunk = 0, S = 0;
@@ -76,11 +77,11 @@ extern "C" int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o
     // alignment; the element count of an 8-bit tensor is the same bound
     int rc = validate_problem(q, k, v, o, B, Hq, Hkv, M, N, D, causal, window, scale, out_dtype, &p);
     if (rc != ATTN_OK) return rc;
-    if (D != 128) return ATTN_ERR_HEADDIM;
+    if (D != 128 && D != 64) return ATTN_ERR_HEADDIM;
     const int64_t rows = (int64_t)B * Hq * M;
     if (rows > 0 && lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_ALIGN;
     path = choose_fp8_path(p, path);
-    if (path == ATTN_PATH_DECODE && !decode_tc_supported(p)) return ATTN_ERR_PATH;
+    if (path == ATTN_PATH_DECODE && (D != 128 || !decode_tc_supported(p))) return ATTN_ERR_PATH;
     if (path == ATTN_PATH_PREFILL && !prefill_supported(p)) return ATTN_ERR_PATH;
     if (rows == 0) return ATTN_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -252,7 +252,10 @@ __device__ __forceinline__ void mma_group_pv(uint32_t d_tmem, uint32_t a_tmem, u
     }
 }
 
-template <int D, int kIn, bool kBF16>  // kBF16: output type (and input type for 16-bit inputs)
+// kBF16: output type (and input type for 16-bit inputs). DO: columns of the
+// tensors and the output (D, or 64 for 8-bit inputs run as D = 128: the upper
+// 64 columns of every Q, K and V tile read as zeros and are never written out).
+template <int D, int kIn, bool kBF16, int DO = D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
@@ -441,13 +444,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         Work wk;
         for (int w = 0; ok && work_tile(p, w, &wk); ++w) {
             const int row = wk.row0 + t * BM + r_in_tile;
-            uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + ((size_t)wk.bh * p.M + row) * D;
+            uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + ((size_t)wk.bh * p.M + row) * DO;
             if (wk.n == 0) {  // no row of this tile sees any key: output 0
                 if (row < p.M) {
                     if (p.lse) p.lse[(size_t)wk.bh * p.M + row] = -INFINITY;
                     uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
-                    for (int v4 = 0; v4 < D / 8; ++v4) dst[v4] = make_uint4(0, 0, 0, 0);
+                    for (int v4 = 0; v4 < DO / 8; ++v4) dst[v4] = make_uint4(0, 0, 0, 0);
                 }
                 continue;
             }
@@ -618,16 +621,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 p.lse[(size_t)wk.bh * p.M + row] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
             const uint32_t wst = sStage + (t * 4 + wq) * 4096;  // this warp's staging area
             const uint64_t inv2 = f2_pack(inv, inv);
-            char* obase = reinterpret_cast<char*>(p.o) + ((size_t)wk.bh * p.M + wk.row0 + t * BM + wq * 32) * (D * 2);
+            char* obase = reinterpret_cast<char*>(p.o) + ((size_t)wk.bh * p.M + wk.row0 + t * BM + wq * 32) * (DO * 2);
             const int rows_left = p.M - (wk.row0 + t * BM + wq * 32);  // rows of this warp below M
 #pragma unroll
-            for (int h = 0; h < D / 64; ++h) {
+            for (int h = 0; h < DO / 64; ++h) {
                 uint32_t o[2][32];
                 tmem_ld_x32(tO + h * 64, o[0]);
                 tmem_ld_x32(tO + h * 64 + 32, o[1]);
                 tmem_wait_ld_x32(o[0]);
                 reg_after_x32(o[1]);
-                if (h == D / 64 - 1) {
+                if (h == DO / 64 - 1) {
                     // O_t is read out: it may take the next tile's first value product
                     tc_fence_before();
                     __syncwarp();
@@ -654,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int rr = 4 * i + (lane >> 3), ch = lane & 7;
                     const uint4 v4 = ld_shared_v4(wst + rr * 128 + ((ch ^ (rr & 7)) << 4));
                     if (rr < rows_left)
-                        *reinterpret_cast<uint4*>(obase + (size_t)rr * (D * 2) + h * 128 + ch * 16) = v4;
+                        *reinterpret_cast<uint4*>(obase + (size_t)rr * (DO * 2) + h * 128 + ch * 16) = v4;
                 }
                 __syncwarp();  // the area is read before the next half overwrites it
             }
@@ -669,23 +672,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, int kIn, bool kBF16>
+template <int D, int kIn, bool kBF16, int DO = D>
 int launch_t(const Problem& pr, const void* q, const void* k, const void* v, void* o, int* status, float v_scale,
              cudaStream_t stream, long withhold_p_at = -1) {
     constexpr int EB = kIn == kInE4M3 ? 1 : 2;
     using C = Cfg<D, EB>;
     static PerDeviceOnce attr_once;
     if (once_per_device(attr_once, [] {
-            return cudaFuncSetAttribute(attn_prefill_kernel<D, kIn, kBF16>,
+            return cudaFuncSetAttribute(attn_prefill_kernel<D, kIn, kBF16, DO>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         }) != cudaSuccess)
         return ATTN_ERR_CUDA;
     const int sms = device_sm_count();
     if (sms <= 0) return ATTN_ERR_CUDA;
     CUtensorMap tq, tk, tv;
-    if (!make_tensor_map(&tq, q, D, pr.M, pr.B * pr.Hq, BM, kBF16, EB) ||
-        !make_tensor_map(&tk, k, D, pr.N, pr.B * pr.Hkv, BN, kBF16, EB) ||
-        !make_tensor_map(&tv, v, D, pr.N, pr.B * pr.Hkv, BN, kBF16, EB))
+    if (!make_tensor_map(&tq, q, DO, pr.M, pr.B * pr.Hq, BM, kBF16, EB) ||
+        !make_tensor_map(&tk, k, DO, pr.N, pr.B * pr.Hkv, BN, kBF16, EB) ||
+        !make_tensor_map(&tv, v, DO, pr.N, pr.B * pr.Hkv, BN, kBF16, EB))
         return ATTN_ERR_CUDA;
     PrefillParams pp;
     pp.o = o;
@@ -705,7 +708,7 @@ int launch_t(const Problem& pr, const void* q, const void* k, const void* v, voi
     pp.tiles = pp.BH * pp.nqb;
     pp.withhold_p_at = withhold_p_at;
     const int grid = pp.tiles < sms ? pp.tiles : sms;
-    attn_prefill_kernel<D, kIn, kBF16><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, pp);
+    attn_prefill_kernel<D, kIn, kBF16, DO><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, pp);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -735,9 +738,15 @@ int launch_prefill_withheld(const Problem& p, const void* q, const void* k, cons
 
 int launch_prefill_e4m3(const Problem& p, const void* q, const void* k, const void* v, void* o, int* status,
                         float v_scale, cudaStream_t stream) {
-    if (p.D != 128) return ATTN_ERR_HEADDIM;
-    return p.dtype == ATTN_BF16 ? launch_t<128, kInE4M3, true>(p, q, k, v, o, status, v_scale, stream)
-                                : launch_t<128, kInE4M3, false>(p, q, k, v, o, status, v_scale, stream);
+    if (p.D == 128)
+        return p.dtype == ATTN_BF16 ? launch_t<128, kInE4M3, true>(p, q, k, v, o, status, v_scale, stream)
+                                    : launch_t<128, kInE4M3, false>(p, q, k, v, o, status, v_scale, stream);
+    // D = 64: the 128-column kernel on 64-byte rows read through 128-byte boxes
+    // (columns 64..127 read as zeros), writing 64 output columns
+    if (p.D == 64)
+        return p.dtype == ATTN_BF16 ? launch_t<128, kInE4M3, true, 64>(p, q, k, v, o, status, v_scale, stream)
+                                    : launch_t<128, kInE4M3, false, 64>(p, q, k, v, o, status, v_scale, stream);
+    return ATTN_ERR_HEADDIM;
 }
 
 }  // namespace attn

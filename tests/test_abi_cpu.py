@@ -243,8 +243,9 @@ def test_selftest_rejects_bad_limits(L):
 @pytest.mark.parametrize("kw,status", [
     (dict(dtype=7), -3),
     (dict(dtype=2), -3),                 # FP32 output is not offered
-    (dict(D=64), -4),
+    (dict(D=32), -4),
     (dict(D=48), -4),
+    (dict(path=3, D=64), -11),           # the 8-bit split decode is D = 128 only; D = 64 runs the prefill
     (dict(Hq=6, Hkv=4), -5),
     (dict(k=None), -1),
     (dict(q=A8), -7),

@@ -35,8 +35,11 @@ def deq(t, d):
     ((1, 2, 2, 300, 100, 128), True, 0, (1.0, 1.0, 1.0)),      # rows with no visible key
     ((1, 3, 1, 1, 777, 128), True, 64, (1.0, 1.0, 1.0)),       # one query row
 ])
-def test_fp8_forward_against_oracle(out_dtype, shape, causal, window, descale):
-    B, Hq, Hkv, M, N, D = shape
+@pytest.mark.parametrize("D", [64, 128])
+def test_fp8_forward_against_oracle(out_dtype, shape, causal, window, descale, D):
+    """D = 64 runs the 128-column prefill with the upper half of every tile
+    read as zeros (AUTO never takes the 8-bit split decode at D = 64)."""
+    B, Hq, Hkv, M, N, _ = shape
     qd, kd, vd = descale
     q, k, v = make_qkv_fp8(B, Hq, Hkv, M, N, D, 21, qd, kd, vd)
     scale = 1.0 / np.sqrt(D)
@@ -75,6 +78,22 @@ def test_fp8_empty_dims():
     o, lse = sa.attention_fp8(q.to(DEV), k.to(DEV), v.to(DEV), with_lse=True)
     torch.cuda.synchronize()
     assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+
+
+def test_fp8_d64_many_work_tiles_and_no_decode_path():
+    """E4M3 at D = 64 over more work tiles than SMs (each persistent CTA walks
+    several), every row; the explicit split-decode path refuses D = 64."""
+    B, Hq, Hkv, M, N, D = 2, 16, 4, 1100, 1300, 64
+    q, k, v = make_qkv_fp8(B, Hq, Hkv, M, N, D, 29, 1.0, 0.5, 1.0)
+    o = sa.attention_fp8(q.to(DEV), k.to(DEV), v.to(DEV), causal=True, k_descale=0.5)
+    torch.cuda.synchronize()
+    want = oracle.attention_fp8(q, k, v, 1.0, 0.5, 1.0, causal=True)
+    H, sigma, wabs = bounds(deq(q, 1.0), deq(k, 0.5), deq(v, 1.0), True, 0, 1.0 / np.sqrt(D))
+    check_fp8(o, want, H, sigma, wabs, torch.bfloat16, "E4M3 D=64 many work tiles")
+    o2 = torch.empty(q.shape, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(sa.AttnError) as e:
+        sa.attn_fwd_fp8(q.to(DEV), k.to(DEV), v.to(DEV), o2, None, True, 0, path=sa.PATH_DECODE)
+    assert e.value.status == -11
 
 
 def test_fp8_full_size_sampled_rows():
