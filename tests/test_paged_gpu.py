@@ -190,3 +190,26 @@ def test_paged_decode_workload_d64():
     ref = sa.attention(q.to(DEV), k.to(DEV), v.to(DEV), causal=True, window=W, path=sa.PATH_DECODE)
     torch.cuda.synchronize()
     assert torch.allclose(o.float(), ref.float(), atol=2e-2, rtol=0)
+
+
+@pytest.mark.parametrize("D", [32, 128])
+def test_paged_table_entries_outside_the_pool_read_zeros(D):
+    """Block-table entries outside [0, num_pages) (negative or past the pool)
+    read a page of zeros on both kernels (the tcgen05 kernel through a TMA
+    coordinate past the pool, the grouped kernel through a bounds check): the
+    result equals the oracle on the pool extended by one zero page that those
+    entries point to."""
+    B, Hq, Hkv, M, Ncap, ps = 3, 8, 2, 1, 512, 32
+    q, kp, vp, table = paged_case(B, Hq, Hkv, M, Ncap, ps, torch.bfloat16, 47, D=D)
+    num_pages = kp.shape[0]
+    bad = table.clone()
+    bad[0, 3] = -1
+    bad[1, 0] = num_pages
+    bad[2, 7] = num_pages + 1000
+    lens = [500, 512, 300]
+    o = run_paged(q, kp, vp, bad, lens, Ncap, True, 0)
+    zero = torch.zeros((1,) + tuple(kp.shape[1:]), dtype=kp.dtype)
+    kz, vz = torch.cat([kp, zero]), torch.cat([vp, zero])
+    fixed = torch.where((bad < 0) | (bad >= num_pages), torch.full_like(bad, num_pages), bad)
+    want = oracle.attention_paged(q, kz, vz, fixed, lens, Ncap, True, 0)
+    check(o, want, torch.bfloat16, f"out-of-pool table entries D={D}")
