@@ -116,6 +116,9 @@ struct PrefillParams {
     int BH;     // B * Hq
     int nqb;    // work tiles per head (ceil(M / 256))
     int tiles;  // BH * nqb
+    // > 0: walk the heads in groups of this many (every work tile has the same
+    // length); 0: all heads' last query blocks first, longest first
+    int head_group;
     // failure-path self-test only (-1 otherwise): the softmax warps of query tile 0
     // withhold their P-ready arrival for this score tile (counted over the CTA's walk),
     // so the issuing warp's bounded wait runs out and the whole CTA takes its abort path
@@ -142,8 +145,21 @@ __device__ __forceinline__ bool work_tile(const PrefillParams& p, int w, Work* t
     const int grid = gridDim.x, c = blockIdx.x;
     const int idx = w * grid + ((w & 1) ? grid - 1 - c : c);
     if (idx >= p.tiles) return false;
-    const int qb = p.nqb - 1 - idx / p.BH;
-    t->bh = idx % p.BH;
+    int qb;
+    if (p.head_group > 0) {
+        // equal work tiles: a group of heads at a time, so that the K/V the CTAs
+        // running at once read (a few heads' worth) stays in L2
+        const int per = p.head_group * p.nqb;
+        const int h0 = (idx / per) * p.head_group, j = idx % per;
+        const int hn = min(p.head_group, p.BH - h0);
+        qb = p.nqb - 1 - j / hn;
+        t->bh = h0 + j % hn;
+    } else {
+        // longest work tiles first over all heads (causal and window tiles differ
+        // in length): the last wave holds the shortest ones
+        qb = p.nqb - 1 - idx / p.BH;
+        t->bh = idx % p.BH;
+    }
     const int b = t->bh / p.Hq, h = t->bh % p.Hq;
     t->kvh = b * p.Hkv + h / p.G;
     t->row0 = qb * (NQ * BM);
@@ -708,6 +724,11 @@ int launch_t(const Problem& pr, const void* q, const void* k, const void* v, voi
     pp.tiles = pp.BH * pp.nqb;
     pp.withhold_p_at = withhold_p_at;
     const int grid = pp.tiles < sms ? pp.tiles : sms;
+    // Work tiles of equal length (no causal mask, no window) over at least four
+    // waves: heads in groups of about one wave's worth of tiles (measured: the
+    // D = 128 noncausal 4096 workload 3.5 % faster; with 1.7 waves, or tiles of
+    // different lengths, the all-heads longest-first order is faster).
+    pp.head_group = (!pr.causal && pr.window <= 0 && pp.tiles >= 4 * grid) ? (grid + pp.nqb - 1) / pp.nqb : 0;
     attn_prefill_kernel<D, kIn, kBF16, DO><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, pp);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

@@ -105,6 +105,21 @@ def test_prefill_many_work_tiles(case, D):
     check(o.reshape(-1, D)[torch.tensor(rows, device=o.device)], want, torch.bfloat16, f"{case} D={D}")
 
 
+def test_prefill_noncausal_head_groups():
+    """Noncausal work tiles of equal length over at least four waves: the
+    persistent CTAs walk the heads in groups of about one wave's worth (here
+    160 query heads x 4 query blocks = 640 work tiles, groups of 38 heads, the
+    last one of 8), GQA groups of 5. Whole first, middle and last heads and
+    sampled rows against the oracle."""
+    B, Hq, Hkv, M, N, D = 2, 80, 16, 1024, 1024, 64
+    q, k, v = make_qkv(B, Hq, Hkv, M, N, D, torch.bfloat16, seed=31)
+    o = run(q, k, v, False, 0, sa.PATH_PREFILL)
+    rows = sorted(set(sample_rows(B, Hq, M, 300, seed=31)) | set(whole_heads(B, Hq, M)))
+    want = oracle.attention_rows(q, k, v, rows, causal=False)
+    assert torch.isfinite(o).all()
+    check(o.reshape(-1, D)[torch.tensor(rows, device=o.device)], want, torch.bfloat16, "head groups")
+
+
 @pytest.mark.parametrize("D", [16, 32])
 @pytest.mark.parametrize("mask", [(False, 0), (True, 0), (True, 9)], ids=str)
 def test_small_head_dims_simt(D, mask):
