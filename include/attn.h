@@ -229,8 +229,10 @@ ATTN_API int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, 
  *   all of dtype, 16-byte aligned; lse: device float [B, Hq, M] from the forward
  *   of the same q, k, v, causal, window and scale. dq, dk, dv are written (not
  *   accumulated) and must not overlap the inputs.
- *   D must be 64 or 128 (ATTN_ERR_HEADDIM). M == 0 or N == 0: the gradients
- *   that exist are zero-filled.
+ *   D is 64 or 128 (tcgen05 kernels; P and dS rounded to dtype for their
+ *   products) or 16 or 32 (CUDA-core kernels, P and dS kept in FP32, at most
+ *   65535 (batch, query head) pairs, else ATTN_ERR_PATH); else ATTN_ERR_HEADDIM.
+ *   M == 0 or N == 0: the gradients that exist are zero-filled.
  *   workspace: device memory of attn_bwd_workspace_bytes(B, Hq, M) bytes,
  *   16-byte aligned, or NULL to have it allocated stream-ordered. */
 ATTN_API size_t attn_bwd_workspace_bytes(int B, int Hq, int M);

@@ -439,7 +439,9 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
     Problem p;
     int rc = validate(q, k, v, o, B, Hq, Hkv, M, N, D, causal, window, scale, dtype, &p);
     if (rc != ATTN_OK) return rc;
-    if (D != 64 && D != 128) return ATTN_ERR_HEADDIM;
+    if (D != 16 && D != 32 && D != 64 && D != 128) return ATTN_ERR_HEADDIM;
+    // the CUDA-core kernels of D = 16, 32 take one (batch, head) per grid y index
+    if (D < 64 && (int64_t)B * Hq > 65535) return ATTN_ERR_PATH;
     const int64_t nq = (int64_t)B * Hq * M * D, nk = (int64_t)B * Hkv * N * D;
     if ((nq > 0 && (!d_o || !lse || !dq)) || (nk > 0 && (!dk || !dv))) return ATTN_ERR_NULL;
     if ((d_o && !aligned16(d_o)) || (dq && !aligned16(dq)) || (dk && !aligned16(dk)) || (dv && !aligned16(dv)) ||

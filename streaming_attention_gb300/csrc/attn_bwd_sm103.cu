@@ -36,6 +36,7 @@
 // Tiles outside the causal / window range are skipped; only edge tiles mask.
 // Every wait is bounded (1 s); on expiry a CTA sets the device status word,
 // drains its copies and MMAs, frees TMEM and exits.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include <mutex>
@@ -832,6 +833,235 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// ---------------------------------------------------------------------------
+// CUDA-core backward for the small head dimensions (D = 16, 32): the same
+// formulas and the same split (one kernel owns dK and dV of key rows, the other
+// dQ of query rows; nothing is accumulated across blocks), one warp per output
+// row, one lane per query row (dK/dV) or per key (dQ) of a 32-wide tile staged
+// in shared memory as FP32. P and dS stay FP32 (no 16-bit rounding between the
+// products): a correct covering path for the pages' own head dimensions.
+// ---------------------------------------------------------------------------
+struct SimtBwdArgs {
+    const uint16_t *q, *k, *v, *d_o;
+    const float* nlse2;   // [B*Hq][Mpad], from the pre kernel
+    const float* ndelta;  // [B*Hq][Mpad]
+    uint16_t *dq, *dk, *dv;
+    int Hq, Hkv, M, N, G, Mpad;
+    int causal, window;
+    float scale, scale_log2;
+};
+
+constexpr int kSBRows = 4;   // output rows (warps) per block
+constexpr int kSBTile = 32;  // staged rows per tile, one per lane
+
+template <bool kBF16>
+__device__ __forceinline__ float ld16(const uint16_t* p, size_t i) {
+    const uint32_t x = p[i];
+    return kBF16 ? __uint_as_float(x << 16) : __half2float(__ushort_as_half((unsigned short)x));
+}
+template <bool kBF16>
+__device__ __forceinline__ uint16_t st16(float x) {
+    return kBF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(x)) : __half_as_ushort(__float2half_rn(x));
+}
+
+// dK, dV: block = kSBRows key rows of one KV head (grid: key-row blocks x B*Hkv).
+// For every query head of the group and every 32-row query tile that may see
+// the block's keys: lane = query row, p = exp2(s c - lse2), dp = dO . v,
+// ds = p (dp - delta); dV += p dO, dK += ds Q (a shuffle sum over the lanes).
+template <bool kBF16, int D>
+__global__ void __launch_bounds__(kSBRows * 32) attn_bwd_simt_dkdv_kernel(const SimtBwdArgs a) {
+    constexpr int EPL = (D + 31) / 32;
+    __shared__ float qs[kSBTile][D + 1], dos[kSBTile][D + 1];
+    __shared__ float kr[kSBRows][D], vr[kSBRows][D];
+    __shared__ float l2s[kSBTile], dls[kSBTile];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int grp = blockIdx.y, b = grp / a.Hkv, g = grp % a.Hkv;
+    const int j0 = blockIdx.x * kSBRows, j = j0 + warp;
+    const int jl = min(j0 + kSBRows, a.N) - 1;  // the block's last key
+    const int off = a.N - a.M;                  // row i sits at key position i + off
+    const size_t kvrow = (size_t)grp * a.N;
+    for (int x = threadIdx.x; x < kSBRows * D; x += blockDim.x) {
+        const int r = x / D, d = x % D;
+        const bool in = j0 + r < a.N;
+        kr[r][d] = in ? ld16<kBF16>(a.k, (kvrow + j0 + r) * D + d) : 0.f;
+        vr[r][d] = in ? ld16<kBF16>(a.v, (kvrow + j0 + r) * D + d) : 0.f;
+    }
+    // query rows that may see any of the block's keys
+    int i_lo = 0, i_hi = a.M;
+    if (a.causal) i_lo = max(0, j0 - off);
+    if (a.window > 0) i_hi = min(a.M, jl + a.window - off);
+    float ak[EPL], av[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) ak[e] = av[e] = 0.f;
+    for (int hh = 0; hh < a.G; ++hh) {
+        const int bh = b * a.Hq + g * a.G + hh;
+        for (int i0 = i_lo; i0 < i_hi; i0 += kSBTile) {
+            __syncthreads();  // the previous tile consumed (and kr, vr written)
+            for (int x = threadIdx.x; x < kSBTile * D; x += blockDim.x) {
+                const int r = x / D, d = x % D, i = i0 + r;
+                const bool in = i < i_hi;
+                qs[r][d] = in ? ld16<kBF16>(a.q, ((size_t)bh * a.M + i) * D + d) : 0.f;
+                dos[r][d] = in ? ld16<kBF16>(a.d_o, ((size_t)bh * a.M + i) * D + d) : 0.f;
+            }
+            if (threadIdx.x < kSBTile) {
+                const int i = i0 + threadIdx.x;
+                l2s[threadIdx.x] = i < i_hi ? a.nlse2[(size_t)bh * a.Mpad + i] : 0.f;
+                dls[threadIdx.x] = i < i_hi ? a.ndelta[(size_t)bh * a.Mpad + i] : 0.f;
+            }
+            __syncthreads();
+            if (j < a.N) {
+                const int i = i0 + lane;
+                int lo = 0, hi = 0;
+                if (i < i_hi) key_range(i + off, a.N, a.causal, a.window, &lo, &hi);
+                float p = 0.f, ds = 0.f;
+                if (j >= lo && j < hi) {
+                    float s = 0.f, dp = 0.f;
+#pragma unroll
+                    for (int d = 0; d < D; ++d) {
+                        s = fmaf(qs[lane][d], kr[warp][d], s);
+                        dp = fmaf(dos[lane][d], vr[warp][d], dp);
+                    }
+                    p = exp2f(fmaf(s, a.scale_log2, l2s[lane]));
+                    ds = p * (dp + dls[lane]);
+                }
+#pragma unroll 4
+                for (int ii = 0; ii < kSBTile; ++ii) {
+                    const float pi = __shfl_sync(0xffffffffu, p, ii), dsi = __shfl_sync(0xffffffffu, ds, ii);
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) {
+                        const int d = lane + 32 * e;
+                        if (d < D) {
+                            av[e] = fmaf(pi, dos[ii][d], av[e]);
+                            ak[e] = fmaf(dsi, qs[ii][d], ak[e]);
+                        }
+                    }
+                }
+            }
+        }
+    }
+    if (j >= a.N) return;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+        const int d = lane + 32 * e;
+        if (d < D) {
+            a.dk[(kvrow + j) * D + d] = st16<kBF16>(ak[e] * a.scale);
+            a.dv[(kvrow + j) * D + d] = st16<kBF16>(av[e]);
+        }
+    }
+}
+
+// dQ: block = kSBRows query rows of one query head (grid: row blocks x B*Hq);
+// lane = key of a 32-key tile over the keys the block's rows may see.
+template <bool kBF16, int D>
+__global__ void __launch_bounds__(kSBRows * 32) attn_bwd_simt_dq_kernel(const SimtBwdArgs a) {
+    constexpr int EPL = (D + 31) / 32;
+    __shared__ float ks[kSBTile][D + 1], vs[kSBTile][D + 1];
+    __shared__ float qr[kSBRows][D], dor[kSBRows][D];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.y, b = bh / a.Hq, h = bh % a.Hq;
+    const size_t kvrow = ((size_t)b * a.Hkv + h / a.G) * a.N;
+    const int r0 = blockIdx.x * kSBRows, i = r0 + warp;
+    const int rl = min(r0 + kSBRows, a.M) - 1;
+    const int off = a.N - a.M;
+    for (int x = threadIdx.x; x < kSBRows * D; x += blockDim.x) {
+        const int r = x / D, d = x % D;
+        const bool in = r0 + r < a.M;
+        qr[r][d] = in ? ld16<kBF16>(a.q, ((size_t)bh * a.M + r0 + r) * D + d) : 0.f;
+        dor[r][d] = in ? ld16<kBF16>(a.d_o, ((size_t)bh * a.M + r0 + r) * D + d) : 0.f;
+    }
+    // keys any row of the block may see (both bounds grow with the position)
+    int lo_f, hi_f, lo_l, hi_l;
+    key_range(r0 + off, a.N, a.causal, a.window, &lo_f, &hi_f);
+    key_range(rl + off, a.N, a.causal, a.window, &lo_l, &hi_l);
+    int r_lo = 0, r_hi = 0;
+    float nl2 = 0.f, nd = 0.f;
+    if (i < a.M) {
+        key_range(i + off, a.N, a.causal, a.window, &r_lo, &r_hi);
+        nl2 = a.nlse2[(size_t)bh * a.Mpad + i];
+        nd = a.ndelta[(size_t)bh * a.Mpad + i];
+    }
+    float aq[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) aq[e] = 0.f;
+    for (int t0 = lo_f; t0 < hi_l; t0 += kSBTile) {
+        __syncthreads();
+        for (int x = threadIdx.x; x < kSBTile * D; x += blockDim.x) {
+            const int r = x / D, d = x % D, jj = t0 + r;
+            const bool in = jj < hi_l;
+            ks[r][d] = in ? ld16<kBF16>(a.k, (kvrow + jj) * D + d) : 0.f;
+            vs[r][d] = in ? ld16<kBF16>(a.v, (kvrow + jj) * D + d) : 0.f;
+        }
+        __syncthreads();
+        if (i < a.M) {
+            const int jj = t0 + lane;
+            float ds = 0.f;
+            if (jj >= r_lo && jj < r_hi) {
+                float s = 0.f, dp = 0.f;
+#pragma unroll
+                for (int d = 0; d < D; ++d) {
+                    s = fmaf(qr[warp][d], ks[lane][d], s);
+                    dp = fmaf(dor[warp][d], vs[lane][d], dp);
+                }
+                const float p = exp2f(fmaf(s, a.scale_log2, nl2));
+                ds = p * (dp + nd);
+            }
+#pragma unroll 4
+            for (int u = 0; u < kSBTile; ++u) {
+                const float dsu = __shfl_sync(0xffffffffu, ds, u);
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) {
+                    const int d = lane + 32 * e;
+                    if (d < D) aq[e] = fmaf(dsu, ks[u][d], aq[e]);
+                }
+            }
+        }
+    }
+    if (i >= a.M) return;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+        const int d = lane + 32 * e;
+        if (d < D) a.dq[((size_t)bh * a.M + i) * D + d] = st16<kBF16>(aq[e] * a.scale);
+    }
+}
+
+template <int D, bool kBF16>
+cudaError_t launch_bwd_simt_t(const Problem& pr, const BwdArgs& a, const float* lse2, const float* delta, int Mpad,
+                              cudaStream_t stream) {
+    const int rows_pad = pr.B * pr.Hq * Mpad;
+    constexpr int kPreRowsPerBlock = 8 * (32 / (D / 8));
+    attn_bwd_pre_kernel<kBF16, D><<<(rows_pad + kPreRowsPerBlock - 1) / kPreRowsPerBlock, 256, 0, stream>>>(
+        static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.d_o), a.lse, const_cast<float*>(lse2),
+        const_cast<float*>(delta), pr.M, Mpad, rows_pad);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    SimtBwdArgs sa;
+    sa.q = static_cast<const uint16_t*>(a.q);
+    sa.k = static_cast<const uint16_t*>(a.k);
+    sa.v = static_cast<const uint16_t*>(a.v);
+    sa.d_o = static_cast<const uint16_t*>(a.d_o);
+    sa.nlse2 = lse2;
+    sa.ndelta = delta;
+    sa.dq = static_cast<uint16_t*>(a.dq);
+    sa.dk = static_cast<uint16_t*>(a.dk);
+    sa.dv = static_cast<uint16_t*>(a.dv);
+    sa.Hq = pr.Hq;
+    sa.Hkv = pr.Hkv;
+    sa.M = pr.M;
+    sa.N = pr.N;
+    sa.G = pr.G;
+    sa.Mpad = Mpad;
+    sa.causal = pr.causal;
+    sa.window = pr.window;
+    sa.scale = pr.scale;
+    sa.scale_log2 = pr.scale_log2;
+    attn_bwd_simt_dkdv_kernel<kBF16, D>
+        <<<dim3((pr.N + kSBRows - 1) / kSBRows, pr.B * pr.Hkv), kSBRows * 32, 0, stream>>>(sa);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    attn_bwd_simt_dq_kernel<kBF16, D>
+        <<<dim3((pr.M + kSBRows - 1) / kSBRows, pr.B * pr.Hq), kSBRows * 32, 0, stream>>>(sa);
+    return cudaGetLastError();
+}
+
 template <int D, bool kBF16>
 cudaError_t launch_bwd_t(const Problem& pr, const BwdArgs& a, const float* lse2, const float* delta, int Mpad,
                          int* status, cudaStream_t stream) {
@@ -922,6 +1152,12 @@ cudaError_t launch_bwd(const Problem& p, const BwdArgs& a, void* ws, int* status
     if (p.D == 64)
         return bf ? launch_bwd_t<64, true>(p, a, lse2, delta, Mpad, status, stream)
                   : launch_bwd_t<64, false>(p, a, lse2, delta, Mpad, status, stream);
+    if (p.D == 32)
+        return bf ? launch_bwd_simt_t<32, true>(p, a, lse2, delta, Mpad, stream)
+                  : launch_bwd_simt_t<32, false>(p, a, lse2, delta, Mpad, stream);
+    if (p.D == 16)
+        return bf ? launch_bwd_simt_t<16, true>(p, a, lse2, delta, Mpad, stream)
+                  : launch_bwd_simt_t<16, false>(p, a, lse2, delta, Mpad, stream);
     return cudaErrorInvalidValue;
 }
 

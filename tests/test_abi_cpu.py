@@ -327,3 +327,23 @@ def test_host_entry_validation(L):
     bad_shape = list(args)
     bad_shape[9], bad_shape[10] = 6, 4  # Hq % Hkv != 0
     assert L.attn_fwd_host(*bad_shape) == -5
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=48), -4),
+    (dict(D=256), -4),
+    (dict(Hq=6, Hkv=4), -5),
+    (dict(dq=None), -1),
+    (dict(lse=ctypes.c_void_p(0x10002)), -7),
+    (dict(B_=0, D=16), 0),   # no rows and no keys: nothing to write, no launch
+    (dict(B_=0, D=32), 0),
+    (dict(B_=1, Hq=65536, Hkv=65536, D=16), -11),   # past the CUDA-core kernels' grid
+])
+def test_bwd_validation_status(L, kw, status):
+    """attn_bwd takes D in {16, 32, 64, 128}; validation answers before any launch."""
+    a = dict(q=A16, k=A16, v=A16, o=A16, d_o=A16, lse=A16, dq=A16, dk=A16, dv=A16, B_=1, Hq=2, Hkv=2, M=8,
+             N=8, D=128)
+    a.update(kw)
+    st = L.attn_bwd(a["q"], a["k"], a["v"], a["o"], a["d_o"], a["lse"], a["dq"], a["dk"], a["dv"], a["B_"],
+                    a["Hq"], a["Hkv"], a["M"], a["N"], a["D"], 1, 0, 0.0, 0, None, 0, None)
+    assert st == status

@@ -98,6 +98,26 @@ def test_backward_against_oracle(dtype, shape, causal, window):
     grad_check(dv, wv, dtype, "dv")
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "fp16"])
+@pytest.mark.parametrize("shape,causal,window", [
+    ((1, 2, 2, 77, 77, 16), True, 0),
+    ((2, 4, 2, 100, 150, 32), False, 0),      # GQA, M < N
+    ((1, 4, 1, 130, 130, 32), True, 40),      # window, four heads share one KV head
+    ((1, 2, 2, 90, 40, 16), True, 0),         # rows with no visible key
+    ((1, 3, 3, 1, 200, 32), True, 17),        # one query row
+])
+def test_backward_small_head_dims(dtype, shape, causal, window):
+    """D = 16 and 32 (the pages' own head dimensions) on the CUDA-core backward."""
+    B, Hq, Hkv, M, N, D = shape
+    q, k, v = make_qkv(B, Hq, Hkv, M, N, D, dtype, 13)
+    d_o = torch.randn(B, Hq, M, D, generator=torch.Generator().manual_seed(14)).to(dtype)
+    dq, dk, dv = run_bwd(q, k, v, d_o, causal, window)
+    wq, wk, wv = oracle.attention_backward(q, k, v, d_o, causal=causal, window=window)
+    grad_check(dq, wq, dtype, "dq")
+    grad_check(dk, wk, dtype, "dk")
+    grad_check(dv, wv, dtype, "dv")
+
+
 def test_backward_empty_dims():
     q, k, v = make_qkv(1, 2, 2, 0, 64, 128, torch.bfloat16, 0)
     d_o = torch.zeros_like(q)
