@@ -4,8 +4,8 @@
 // ("Compare reasoning after your own attempt", central-idea table, A2 row:
 // each split's statistics are combined after rescaling; the stream orders the kernels).
 //
-// D = 128 with at most 16 grouped query rows per KV head runs the tcgen05
-// split kernel; other shapes run the SIMT kernel in split mode.
+// D = 64 and 128 run the tcgen05 split kernel (grouped query rows in CTAs of
+// 16); other shapes (B * Hkv > 65535) run the SIMT kernel in split mode.
 #include "attn_internal.h"
 
 namespace attn {

@@ -178,7 +178,8 @@ bool prefill_pair_supported(const Problem& p);
 // D = 128): its bounded waits run out and every CTA takes the abort path.
 int launch_prefill_withheld(const Problem& p, const void* q, const void* k, const void* v, void* o, int* status,
                             long withhold_p_at, cudaStream_t stream);
-// The same kernel on E4M3 inputs (D = 128); p.dtype is the output type and
+// The same kernel on E4M3 inputs (D = 128, or 64 read as 128 with the upper
+// half zero); p.dtype is the output type and
 // p.scale_log2 already includes the Q and K dequantization factors.
 int launch_prefill_e4m3(const Problem& p, const void* q, const void* k, const void* v, void* o, int* status,
                         float v_scale, cudaStream_t stream);
