@@ -273,7 +273,7 @@ def test_host_pipelined_chunks_match_device_call(shape, causal, window):
 
 @pytest.mark.parametrize("case", ["decode", "prefill"])
 def test_fwd_ws_boundary_against_oracle(case):
-    """The survey's boundary through ctypes: attn_workspace_bytes sizes the
+    """The workspace boundary calls through ctypes: attn_workspace_bytes sizes the
     caller's workspace for attn_fwd_ws (per-call scratch, as the course's
     wide-row split softmax keeps it), which takes the path attn_fwd takes."""
     import ctypes
