@@ -115,7 +115,7 @@ def test_workspace_bytes(L):
 
 
 def test_boundary_workspace_query_and_fwd_ws(L):
-    """The survey's boundary: attn_workspace_bytes(B, Hq, Hkv, M, N, D, window)
+    """The workspace boundary calls: attn_workspace_bytes(B, Hq, Hkv, M, N, D, window)
     sizes the workspace of attn_fwd_ws (the path attn_fwd takes) for either
     causal value, and attn_fwd_ws refuses a missing or short workspace before
     launching anything."""
