@@ -50,6 +50,7 @@ THROUGH_ARRAY = [
     (1, 32, 4, 1, 32768, 128, torch.bfloat16, True, 0, 71),    # 64 splits per KV head, 1.1 MB of summaries
     (2, 16, 4, 2, 3000, 128, torch.float16, True, 1000, 77),  # 9 splits, 64 rows
     (2, 8, 2, 1, 5000, 64, torch.bfloat16, False, 0, 78),      # D = 64: 40 splits per KV head
+    (1, 20, 1, 1, 3000, 128, torch.bfloat16, True, 0, 80),     # 20 grouped rows: two CTAs of 16 rows, 24 splits
 ]
 
 
