@@ -56,6 +56,29 @@ def test_fp8_forward_against_oracle(out_dtype, shape, causal, window, descale, D
         assert np.abs(g[fin] - want_lse[fin]).max() <= 2e-3
 
 
+@pytest.mark.parametrize("path", [sa.PATH_AUTO, sa.PATH_PREFILL, sa.PATH_DECODE], ids=["auto", "prefill", "decode"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("shape,causal,window", [
+    ((1, 2, 2, 1, 1), False, 0),      # one query, one key
+    ((1, 2, 2, 5, 1), True, 0),       # one key: rows before it output 0
+    ((2, 4, 2, 1, 3), True, 1),       # window 1: each row sees only its own position
+    ((1, 2, 2, 200, 200), True, 1),   # window 1 over several tiles
+])
+def test_fp8_extreme_small_shapes(shape, causal, window, D, path):
+    B, Hq, Hkv, M, N = shape
+    q, k, v = make_qkv_fp8(B, Hq, Hkv, M, N, D, 30, 1.0, 1.0, 1.0)
+    try:
+        o = sa.attention_fp8(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, window=window, path=path)
+    except sa.AttnError as e:
+        assert e.status == -11, e  # the 8-bit split decode takes D = 128 only
+        assert path == sa.PATH_DECODE and D == 64
+        pytest.skip(str(e))
+    torch.cuda.synchronize()
+    want = oracle.attention_fp8(q, k, v, causal=causal, window=window)
+    H, sigma, wabs = bounds(deq(q, 1.0), deq(k, 1.0), deq(v, 1.0), causal, window, 1.0 / np.sqrt(D))
+    check_fp8(o, want, H, sigma, wabs, torch.bfloat16, f"{shape} causal={causal} window={window} D={D}")
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_fp8_zero_queries_give_exact_means(causal):
     """All-zero queries: every visible key scores 0, every probability is exactly

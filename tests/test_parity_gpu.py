@@ -120,6 +120,31 @@ def test_prefill_noncausal_head_groups():
     check(o.reshape(-1, D)[torch.tensor(rows, device=o.device)], want, torch.bfloat16, "head groups")
 
 
+@pytest.mark.parametrize("path", ALL_PATHS, ids=PATH_NAMES.get)
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("shape,causal,window", [
+    ((1, 2, 2, 1, 1), False, 0),        # one query, one key
+    ((1, 2, 2, 1, 1), True, 0),
+    ((1, 2, 2, 5, 1), True, 0),         # one key: only the last row sees it (causal), the rest output 0
+    ((1, 2, 2, 129, 1), False, 0),      # one key for a tile and a ragged row
+    ((2, 4, 2, 1, 3), True, 1),         # window 1: each row sees only its own position
+    ((1, 2, 2, 200, 200), True, 1),     # window 1 over several tiles: the diagonal alone
+    ((1, 2, 1, 1, 129), False, 0),      # one row over a tile and one key
+], ids=str)
+def test_extreme_small_shapes(shape, causal, window, D, path):
+    """Single keys, single rows and a one-key window on every forward path
+    (paths that cannot run a shape are skipped by their own status)."""
+    B, Hq, Hkv, M, N = shape
+    q, k, v = make_qkv(B, Hq, Hkv, M, N, D, torch.bfloat16, seed=M + N + D)
+    want = oracle.attention(q, k, v, causal=causal, window=window)
+    try:
+        o = run(q, k, v, causal, window, path)
+    except sa.AttnError as e:
+        assert e.status in (-4, -11), e  # head dimension or path not offered for this shape
+        pytest.skip(f"path {path}: {e}")
+    check(o, want, torch.bfloat16, f"{shape} causal={causal} window={window} D={D} path={path}")
+
+
 @pytest.mark.parametrize("D", [16, 32])
 @pytest.mark.parametrize("mask", [(False, 0), (True, 0), (True, 9)], ids=str)
 def test_small_head_dims_simt(D, mask):
