@@ -118,6 +118,25 @@ def test_backward_small_head_dims(dtype, shape, causal, window):
     grad_check(dv, wv, dtype, "dv")
 
 
+@pytest.mark.parametrize("D", [32, 64, 128])
+@pytest.mark.parametrize("scale", [0.2, -0.1])
+def test_backward_explicit_scales(D, scale):
+    """A caller-given logit scale (including a negative one) through the forward
+    log-sum-exp and the backward."""
+    B, Hq, Hkv, M, N = 1, 4, 2, 150, 200
+    q, k, v = make_qkv(B, Hq, Hkv, M, N, D, torch.bfloat16, 15)
+    d_o = torch.randn(B, Hq, M, D, generator=torch.Generator().manual_seed(16)).to(torch.bfloat16)
+    qd, kd, vd, dod = q.to(DEV), k.to(DEV), v.to(DEV), d_o.to(DEV)
+    o, lse = sa.attention_lse(qd, kd, vd, causal=True, scale=scale)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    sa.attn_bwd(qd, kd, vd, o, dod, lse, dq, dk, dv, causal=True, scale=scale)
+    torch.cuda.synchronize()
+    wq, wk, wv = oracle.attention_backward(q, k, v, d_o, causal=True, scale=scale)
+    grad_check(dq, wq, torch.bfloat16, "dq")
+    grad_check(dk, wk, torch.bfloat16, "dk")
+    grad_check(dv, wv, torch.bfloat16, "dv")
+
+
 def test_backward_empty_dims():
     q, k, v = make_qkv(1, 2, 2, 0, 64, 128, torch.bfloat16, 0)
     d_o = torch.zeros_like(q)

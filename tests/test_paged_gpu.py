@@ -213,3 +213,19 @@ def test_paged_table_entries_outside_the_pool_read_zeros(D):
     fixed = torch.where((bad < 0) | (bad >= num_pages), torch.full_like(bad, num_pages), bad)
     want = oracle.attention_paged(q, kz, vz, fixed, lens, Ncap, True, 0)
     check(o, want, torch.bfloat16, f"out-of-pool table entries D={D}")
+
+
+@pytest.mark.parametrize("D", [32, 128])
+@pytest.mark.parametrize("scale", [0.3, -0.1])
+def test_paged_explicit_scales(D, scale):
+    """A caller-given logit scale, including a negative one, on both paged kernels."""
+    B, Hq, Hkv, M, Ncap, ps = 3, 8, 2, 2, 512, 32
+    q, kp, vp, table = paged_case(B, Hq, Hkv, M, Ncap, ps, torch.bfloat16, 53, D=D)
+    lens = [500, 7, 512]
+    qd, kd, vd = q.to(DEV), kp.to(DEV), vp.to(DEV)
+    td, ld = table.to(DEV), torch.tensor(lens, dtype=torch.int32, device=DEV)
+    o = torch.full_like(qd, float("nan"))
+    sa.attn_decode_paged(qd, kd, vd, td, ld, o, Ncap, True, 100, scale)
+    torch.cuda.synchronize()
+    want = oracle.attention_paged(q, kp, vp, table, lens, Ncap, True, 100, scale)
+    check(o, want, torch.bfloat16, f"paged D={D} scale={scale}")

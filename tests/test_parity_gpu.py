@@ -145,6 +145,23 @@ def test_extreme_small_shapes(shape, causal, window, D, path):
     check(o, want, torch.bfloat16, f"{shape} causal={causal} window={window} D={D} path={path}")
 
 
+@pytest.mark.parametrize("path", ALL_PATHS, ids=PATH_NAMES.get)
+@pytest.mark.parametrize("scale", [0.05, 0.3, -0.08])
+@pytest.mark.parametrize("shape,causal,window", [
+    ((1, 4, 2, 300, 300, 128), True, 0),
+    ((2, 4, 1, 1, 1500, 64), True, 600),    # decode shape
+    ((1, 2, 2, 200, 333, 64), False, 0),
+], ids=str)
+def test_explicit_scales(shape, causal, window, scale, path):
+    """A caller-given logit scale, including a negative one (masked keys must
+    still get probability 0 whatever the sign of the scaled scores)."""
+    B, Hq, Hkv, M, N, D = shape
+    q, k, v = make_qkv(B, Hq, Hkv, M, N, D, torch.bfloat16, seed=M + N)
+    want = oracle.attention(q, k, v, causal=causal, window=window, scale=scale)
+    check(run(q, k, v, causal, window, path, scale=scale), want, torch.bfloat16,
+          f"{shape} scale={scale} path={path}")
+
+
 @pytest.mark.parametrize("D", [16, 32])
 @pytest.mark.parametrize("mask", [(False, 0), (True, 0), (True, 9)], ids=str)
 def test_small_head_dims_simt(D, mask):
