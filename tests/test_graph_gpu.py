@@ -68,12 +68,13 @@ def test_attn_fwd_fp8_in_a_graph(path):
     assert torch.equal(o, want_o) and torch.equal(lse, want_lse)
 
 
-def test_paged_decode_in_a_graph():
+@pytest.mark.parametrize("D", [32, 64, 128])  # 32: the grouped CUDA-core kernel; 64, 128: tcgen05
+def test_paged_decode_in_a_graph(D):
     B, Hq, Hkv, M, page, npg = 3, 8, 2, 1, 64, 12
     g0 = torch.Generator().manual_seed(46)
-    q = torch.randn(B, Hq, M, 128, generator=g0).to(torch.bfloat16).to(DEV)
-    kp = torch.randn(B * npg, Hkv, page, 128, generator=g0).to(torch.bfloat16).to(DEV)
-    vp = torch.randn(B * npg, Hkv, page, 128, generator=g0).to(torch.bfloat16).to(DEV)
+    q = torch.randn(B, Hq, M, D, generator=g0).to(torch.bfloat16).to(DEV)
+    kp = torch.randn(B * npg, Hkv, page, D, generator=g0).to(torch.bfloat16).to(DEV)
+    vp = torch.randn(B * npg, Hkv, page, D, generator=g0).to(torch.bfloat16).to(DEV)
     table = torch.randperm(B * npg, generator=g0).reshape(B, npg).to(torch.int32).to(DEV)
     lens = torch.tensor([700, 5, 768], dtype=torch.int32, device=DEV)
     o = torch.empty_like(q)
@@ -87,8 +88,9 @@ def test_paged_decode_in_a_graph():
     assert torch.equal(o, want)
 
 
-def test_backward_in_a_graph():
-    B, Hq, Hkv, M, N, D = 1, 4, 2, 256, 384, 128
+@pytest.mark.parametrize("D", [32, 128])  # 32: the CUDA-core backward; 128: tcgen05
+def test_backward_in_a_graph(D):
+    B, Hq, Hkv, M, N = 1, 4, 2, 256, 384
     q, k, v = (t.to(DEV) for t in make_qkv(B, Hq, Hkv, M, N, D, torch.bfloat16, 47))
     d_o = torch.randn(q.shape, generator=torch.Generator().manual_seed(48)).to(torch.bfloat16).to(DEV)
     o, lse = sa.attention_lse(q, k, v, causal=True)
