@@ -521,6 +521,9 @@ def extra_measurements(args, dev, stream, flush):
     if args.workload == PREFILL_D128.name:
         out["prefill_d128_bf16_causal_backward"] = backward_measure(PREFILL_D128, True, steps, dev, stream)
         out["prefill_d128_bf16_noncausal_backward"] = backward_measure(PREFILL_D128, False, steps, dev, stream)
+        # the CUDA-core backward of the small head dimensions (a covering path), on a 1024-row shape
+        small = PREFILL_D64.with_(D=32, name="prefill_b4_h16_1024x1024_d32_bf16")
+        out["prefill_d32_bf16_causal_backward"] = backward_measure(small, True, steps, dev, stream)
     if args.workload == PREFILL_D128.name:
         out["split_softmax_bf16_m1024_n131072"] = split_softmax_measure(1024, 131072, 4096, steps, dev, stream)
         out["split_softmax_bf16_m1024_n131072_resident"] = split_softmax_measure(1024, 131072, 0, steps, dev,
@@ -537,6 +540,9 @@ def extra_measurements(args, dev, stream, flush):
         out["decode_gqa_d64_paged16"] = paged_decode_measure(DECODE_D64, 16, steps, dev, stream, flush)
         m8 = dataclasses.replace(DECODE_GQA, name="decode_gqa_b8_hq32_hkv8_m8_n8192_w4096_d128_bf16", M=8)
         out["decode_gqa_m8_paged16"] = paged_decode_measure(m8, 16, steps, dev, stream, flush)
+        # the grouped CUDA-core paged kernel (D = 32, a covering path)
+        d32 = DECODE_GQA.with_(D=32, name="decode_gqa_b8_hq32_hkv8_m1_n8192_w4096_d32_bf16")
+        out["decode_gqa_d32_paged16"] = paged_decode_measure(d32, 16, steps, dev, stream, flush)
     return out
 
 
@@ -653,8 +659,10 @@ def backward_measure(w, causal, steps, dev, stream):
     ms = time_steady(fn_on, bsets, steps, 3, stream)
     work = 2.5 * flops(w, causal)
     del bsets
+    kern = "tcgen05 dK/dV kernel + dQ kernel" if w.D in (64, 128) else "CUDA-core dK/dV kernel + dQ kernel"
     return {"TFLOP/s": round(work / (ms * 1e-3) / 1e12, 2), "us": round(ms * 1e3, 1),
-            "flops": "2.5x forward (five products over allowed pairs)", "path": "backward (dK/dV kernel + dQ kernel)"}
+            "flops": "2.5x forward (five products over allowed pairs)", "path": f"backward ({kern})",
+            "shape": {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "M": w.M, "N": w.N, "D": w.D}}
 
 
 def split_softmax_measure(M, N, chunk, steps, dev, stream):
@@ -715,7 +723,7 @@ def paged_decode_measure(w, page_size, steps, dev, stream, flush):
     cold = statistics.median(time_graph(lambda st: fn_on(sets[0], st), steps, 3, flush))
     gbs = decode_bytes(w) / (ms * 1e-3) / 1e9
     pk, pk_src = peaks()
-    kernel = "tcgen05 split" if w.D == 128 and (w.Hq // w.Hkv) * w.M <= 16 else "grouped CUDA-core"
+    kernel = "tcgen05 split" if w.D in (64, 128) else "grouped CUDA-core"
     return {"GB/s": round(gbs, 1), "us": round(ms * 1e3, 2), "cold_call_us": round(cold * 1e3, 2),
             "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4), "peak_source": pk_src,
             "path": f"paged decode ({kernel} kernel), {page_size}-key pages, shuffled pool",

@@ -851,7 +851,7 @@ struct SimtBwdArgs {
     float scale, scale_log2;
 };
 
-constexpr int kSBRows = 4;   // output rows (warps) per block
+constexpr int kSBRows = 16;  // output rows (warps) per block
 constexpr int kSBTile = 32;  // staged rows per tile, one per lane
 
 template <bool kBF16>
